@@ -1,0 +1,304 @@
+/*
+ * libquads -- NVFP4 W4A4 linear and MoE-expert layers with residual activation
+ * compensation, and TRACE rollout-guided rounding, for sm_103a (GB300).
+ *
+ * Sources for what each call computes (page title, then section):
+ *   [QUADS]  "Technical Summary: QUADS - Stabilizing NVFP4 Reinforcement Learning
+ *            for MoE via Quantization-error Alignment" (gist.science): section 1
+ *            (NVFP4 is a native W4A4 format, E2M1 grid with 8 levels per sign),
+ *            2.1 (activation error Delta X_q), 2.2 B "Residual Activation
+ *            Compensation" -- "Mechanism" (second-pass quantization of the
+ *            high-residual channels, correction added back to the output) and
+ *            "Implementation" (top channels by residual magnitude, fused kernels
+ *            that keep the native W4A4 GEMM).
+ *   [TRACE]  "TRACE: Rollout-Guided Quantization-Aware Training for FP4
+ *            Reinforcement Learning of MoE Language Models" (paper.rainbus.top
+ *            digest): "NVFP4 与 E2M1 码本" (global scale + per-block scale, round
+ *            to nearest), "核心方法" (q_TRACE, Eq. (3)), "MoE 专家路由敏感性"
+ *            (router assigns each token a few experts).
+ *
+ * Conventions for every call:
+ *   - Every data pointer is a DEVICE pointer owned by the caller; the library
+ *     never allocates device memory.  Calls that need scratch take a caller
+ *     buffer `workspace` of at least quads_workspace_size(...) bytes.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     only enqueues work on it and returns; no call synchronises the stream.
+ *   - Host-side argument checks return QUADS_ERR_INVALID_ARG,
+ *     QUADS_ERR_UNSUPPORTED_SHAPE or QUADS_ERR_MISALIGNED before anything is
+ *     enqueued; a launch failure returns QUADS_ERR_CUDA.  quads_last_error_detail()
+ *     gives a one-line reason (per host thread).  Device-side failures (a GEMM
+ *     pipeline wait that exceeded its time limit, a device-side shape check)
+ *     are latched in a device word read by quads_device_status().
+ *   - bf16 tensors are row-major with a leading dimension in elements that is
+ *     a multiple of 8; pointers are 16-byte aligned.
+ *
+ * NVFP4 storage:
+ *   codes   uint8 [rows, ld_codes]: two E2M1 codes per byte, element 2i of a row
+ *           in the low nibble, 2i+1 in the high nibble; code bit 3 is the sign.
+ *   scales  one unsigned E4M3 byte per 16 consecutive elements of a row.
+ *           QUADS_SCALES_LINEAR: uint8 [rows, cols/16], row-major.
+ *           QUADS_SCALES_TCGEN05: the layout the tensor-core block-scaled MMA
+ *           reads: rows in blocks of 128, scale columns in blocks of 4; each
+ *           (128-row, 4-column) block is 512 contiguous bytes, the blocks are
+ *           ordered row-block major, and inside a block the byte of (row r,
+ *           scale column c) is at (r % 32) * 16 + ((r / 32) % 4) * 4 + c % 4.
+ *           Requires cols % 64 == 0; the buffer holds ceil(rows/128)*128 rows,
+ *           padding rows read as scale 0.
+ *   tensor scale: one float per row group, s_t = amax / (6 * 448) (1.0 when 0).
+ *
+ * Rounding (fixed so that GPU and reference agree bit for bit): per 16-block
+ * m = max|x|, u = m / (6 s_t), s = E4M3(u) (nearest, ties to even, saturating
+ * at 448), d = E4M3value(s) * s_t, code = E2M1(x * (1/d)) (nearest, ties to
+ * even, saturating at 6, sign kept), every step one IEEE float32 operation; a
+ * block whose d is 0 or whose 1/d overflows gets codes 0.
+ */
+#ifndef QUADS_H
+#define QUADS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QUADS_OK = 0,
+  QUADS_ERR_INVALID_ARG = 1,
+  QUADS_ERR_UNSUPPORTED_SHAPE = 2,
+  QUADS_ERR_MISALIGNED = 3,
+  QUADS_ERR_CUDA = 4,
+  QUADS_ERR_DEVICE_TIMEOUT = 5,
+  QUADS_ERR_DEVICE_CHECK = 6,
+  QUADS_ERR_WORKSPACE = 7
+} quads_status_t;
+
+enum { QUADS_SCALES_LINEAR = 0, QUADS_SCALES_TCGEN05 = 1 };
+enum { QUADS_OUT_F32 = 0, QUADS_OUT_BF16 = 1 };
+enum { QUADS_EPILOGUE_NONE = 0, QUADS_EPILOGUE_SWIGLU = 1 };
+enum {
+  QUADS_OP_QUANTIZE = 0,
+  QUADS_OP_SELECT = 1,
+  QUADS_OP_GEMM = 2,
+  QUADS_OP_MOE_GEMM = 3
+};
+
+/* Rows of the score-partial array are chunks of this many consecutive rows. */
+#define QUADS_SCORE_CHUNK_ROWS 32
+/* The grouped GEMM's row groups (experts) are padded to multiples of this. */
+#define QUADS_MOE_ROW_ALIGN 128
+
+/* Library version as major*10000 + minor*100 + patch. */
+int quads_version(void);
+const char* quads_status_string(quads_status_t s);
+/* One-line reason for the last non-OK status returned on this host thread. */
+const char* quads_last_error_detail(void);
+
+/*
+ * Reads and clears the device-side error word after synchronising `stream`
+ * (this call does synchronise).  *device_code = 0 when no kernel reported a
+ * problem; QUADS_ERR_DEVICE_TIMEOUT when a GEMM pipeline wait gave up (the
+ * kernel then stopped and released its tensor memory); QUADS_ERR_DEVICE_CHECK
+ * when a kernel found a device-resident argument out of range (e.g. a group
+ * offset that is not a multiple of 32 in score mode).
+ */
+quads_status_t quads_device_status(void* stream, int32_t* device_code);
+
+/* Bytes of scratch the call `op` needs for the given shape (0 if none).
+ *   QUADS_OP_QUANTIZE: num_groups floats of tensor amax.
+ *   QUADS_OP_SELECT:   rows*k floats (the residual slice) + num_groups floats.
+ *   QUADS_OP_GEMM:     the requantized selected weight columns Q(W_sel):
+ *                      n*kpad/2 code bytes + n*kpad/16 scale bytes (+ alignment).
+ *   QUADS_OP_MOE_GEMM: the same for num_groups experts.
+ * `cols` is the channel count (K) and `n` the output width (N, unused for the
+ * activation-side ops).  kpad = k rounded up to 64 (k <= 256) or to 256. */
+size_t quads_workspace_size(int32_t op, int64_t rows, int64_t cols, int64_t n, int32_t k,
+                            int32_t num_groups);
+
+/* kpad for a selection of k channels: the width in elements of the stored
+ * residual-slice and selected-weight operands (zero codes in the padding). */
+int32_t quads_kpad(int32_t k);
+
+/*
+ * quads_quantize_nvfp4 -- online RTN quantization of a bf16 activation (or
+ * weight) matrix to NVFP4, one tensor scale per row group, optionally with the
+ * per-channel residual energy partials used to pick the high-residual channels.
+ * [TRACE] "NVFP4 与 E2M1 码本"; [QUADS] 2.1 (Delta X_q) and 2.2 B "Mechanism".
+ *
+ *   x [rows, cols] bf16, leading dimension ldx (elements).
+ *   row_index      nullable; output row r reads input row row_index[r].
+ *   group_offsets  nullable ([0, rows] = one group); else device int32
+ *                  [num_groups + 1], ascending, first 0, every offset but the
+ *                  last a multiple of 32; the last (<= rows) is the number of
+ *                  rows processed -- rows past it are neither read nor written,
+ *                  so `rows` may be a capacity (e.g. padded expert rows).
+ *   tensor_scale_in nullable device float [num_groups]: use these tensor
+ *                  scales instead of computing amax / 2688.
+ *   codes [rows, ld_codes] (ld_codes >= cols/2, multiple of 16); scales in
+ *                  scale_layout (LINEAR: [rows, cols/16]); tensor_scale_out
+ *                  device float [num_groups] (written even when scales are given).
+ *   score_partials nullable device float [ceil(rows/32), cols]: entry
+ *                  [c, j] = sum over rows 32c..32c+31 (row order) of R^2 with
+ *                  R = x - dequant(code), float32 adds, no fused multiply-add.
+ *   workspace      >= quads_workspace_size(QUADS_OP_QUANTIZE, ...).
+ * cols % 16 == 0 (cols % 64 == 0 for the TCGEN05 scale layout).
+ */
+quads_status_t quads_quantize_nvfp4(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                                    const int32_t* row_index, const int32_t* group_offsets,
+                                    int32_t num_groups, const float* tensor_scale_in,
+                                    uint8_t* codes, int64_t ld_codes, uint8_t* scales,
+                                    int32_t scale_layout, float* tensor_scale_out,
+                                    float* score_partials, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
+/*
+ * quads_select_residual_channels -- per row group: channel score = sum of the
+ * group's score-partial rows in ascending order (float32); the k channels with
+ * the largest score (ties -> lower channel index) returned ascending in
+ * sel[g*k .. g*k+k); the residual slice R[:, sel] recomputed from x and the
+ * block scales (R = x - dequant(RTN code)), quantized again to NVFP4 with its
+ * own tensor scale per group (16-blocks along the selected channels).
+ * [QUADS] 2.2 B "Mechanism" and "Implementation" (binary channel mask over the
+ * top channels by residual magnitude; here the mask is stored as the sorted
+ * index list).
+ *
+ *   x, rows, cols, ldx, group_offsets, num_groups: as for the quantizer call
+ *                  that produced `scales`, `tensor_scale` and `score_partials`.
+ *   k              1..cols, multiple of 16.
+ *   sel            device int32 [num_groups, k].
+ *   scores_out     nullable device float [num_groups, cols].
+ *   r_codes        [rows, kpad/2] bytes (kpad = quads_kpad(k)); columns k..kpad
+ *                  are written as code 0.
+ *   r_scales       r_scale_layout; LINEAR: [rows, kpad/16]; TCGEN05: kpad
+ *                  columns, padding blocks 0.
+ *   r_tensor_scale device float [num_groups].
+ *   workspace      >= quads_workspace_size(QUADS_OP_SELECT, rows, cols, 0, k, num_groups).
+ * Requires cols <= 8192.
+ */
+quads_status_t quads_select_residual_channels(
+    const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* group_offsets,
+    int32_t num_groups, const uint8_t* scales, int32_t scale_layout, const float* tensor_scale,
+    const float* score_partials, int32_t k, int32_t* sel, float* scores_out, uint8_t* r_codes,
+    uint8_t* r_scales, int32_t r_scale_layout, float* r_tensor_scale, void* workspace,
+    size_t workspace_bytes, void* stream);
+
+/*
+ * quads_w4a4_gemm_comp -- Y = s_a s_w Q(A) Q(W)^T + s_r s_w Q(R_sel) Q(W_sel)^T
+ * in one kernel on the tcgen05 block-scaled tensor cores (two TMEM
+ * accumulators summed in the epilogue).  [QUADS] 2.2 B "Mechanism" (correction
+ * added back to the quantized output) and section 1 (native W4A4 GEMM).
+ * Q(W_sel) is built inside the call (into `workspace`) from the packed weight:
+ * the selected columns of DQ(Q(W)) in units of s_w, requantized in 16-blocks
+ * along the selection with s_w kept.
+ *
+ *   A: a_codes [M, K/2], a_scales TCGEN05 (ceil(M/128)*128 rows), a_tensor_scale device [1].
+ *   W: w_codes [N, K/2], w_scales TCGEN05, w_tensor_scale device [1].
+ *   r_codes NULL -> plain W4A4 (sel, r_* ignored); else r_codes [M, kpad/2],
+ *   r_scales TCGEN05 over kpad columns, r_tensor_scale [1], sel [k] ascending.
+ *   y [M, ldy] float32 or bf16 (y_dtype).
+ * K % 64 == 0, N % 128 == 0, M >= 1.
+ */
+quads_status_t quads_w4a4_gemm_comp(int64_t M, int64_t N, int64_t K, const uint8_t* a_codes,
+                                    const uint8_t* a_scales, const float* a_tensor_scale,
+                                    const uint8_t* w_codes, const uint8_t* w_scales,
+                                    const float* w_tensor_scale, const uint8_t* r_codes,
+                                    const uint8_t* r_scales, const float* r_tensor_scale,
+                                    const int32_t* sel, int32_t k, void* y, int32_t y_dtype,
+                                    int64_t ldy, void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
+/*
+ * quads_moe_grouped_gemm -- the compensated W4A4 product for every expert of an
+ * MoE layer in one persistent kernel.  Rows of the A operands are grouped by
+ * expert; group e occupies rows [expert_offsets[e], expert_offsets[e+1]) of the
+ * padded row space (offsets multiples of 128), of which the first
+ * expert_counts[e] are real tokens.
+ *
+ *   a_codes [rows_capacity, K/2], a_scales TCGEN05; a_tensor_scale [1] or
+ *     [num_experts] (a_scale_per_expert).
+ *   w_codes [num_experts * N, K/2] (expert e's rows e*N..), w_scales TCGEN05 over
+ *     the same num_experts*N rows, w_tensor_scale [num_experts].
+ *   r_codes NULL -> plain; else [rows_capacity, kpad/2] + TCGEN05 scales,
+ *     r_tensor_scale [1] or [num_experts] (r_scale_per_expert); sel [k] shared
+ *     (sel_per_expert = 0) or [num_experts, k].
+ *   epilogue NONE: y [rows_capacity, ldy] (F32 or BF16), rows past a group's
+ *     count are not written.  SWIGLU: W's 128-row tiles hold 64 gate rows then
+ *     the matching 64 up rows; y bf16 [rows_capacity, N/2] gets
+ *     silu(g) * u, and padding rows of each group are written as 0.
+ * N % 128 == 0, K % 64 == 0.
+ */
+quads_status_t quads_moe_grouped_gemm(
+    int32_t num_experts, int64_t rows_capacity, int64_t N, int64_t K,
+    const int32_t* expert_offsets, const int32_t* expert_counts, const uint8_t* a_codes,
+    const uint8_t* a_scales, const float* a_tensor_scale, int32_t a_scale_per_expert,
+    const uint8_t* w_codes, const uint8_t* w_scales, const float* w_tensor_scale,
+    const uint8_t* r_codes, const uint8_t* r_scales, const float* r_tensor_scale,
+    int32_t r_scale_per_expert, const int32_t* sel, int32_t sel_per_expert, int32_t k,
+    int32_t epilogue, void* y, int32_t y_dtype, int64_t ldy, void* workspace,
+    size_t workspace_bytes, void* stream);
+
+/*
+ * quads_trace_round -- TRACE rollout-guided rounding ([TRACE] "核心方法", Eq. (3)):
+ * v = x_train * (1/d) under the rollout block's d; q-/q+ = the signed E2M1
+ * levels just below/above v (clamped to +-6); emit whichever is nearer the
+ * rollout code's value (a zero result takes the sign of v; a block with
+ * rollout d == 0 gives 0x0).
+ *
+ *   x_train [rows, cols] bf16 (ldx); rollout_codes [rows, ld_codes]; rollout
+ *   scales LINEAR [rows, cols/16]; rollout_tensor_scale device [1];
+ *   codes_out [rows, ld_codes].
+ *   counters nullable device uint64 [3], ADDED to: #(RTN code != rollout code),
+ *   #(TRACE code != rollout code), #(RTN mismatches one signed level away),
+ *   codes compared by value (+0 == -0).
+ */
+quads_status_t quads_trace_round(const void* x_train, int64_t rows, int64_t cols, int64_t ldx,
+                                 const uint8_t* rollout_codes, int64_t ld_codes,
+                                 const uint8_t* rollout_scales,
+                                 const float* rollout_tensor_scale, uint8_t* codes_out,
+                                 unsigned long long* counters, void* stream);
+
+/*
+ * quads_moe_route -- router top-k and the token -> expert dispatch plan
+ * ([TRACE] "MoE 专家路由敏感性").  Per token: the topk largest logits (ties ->
+ * lower expert id), kept in ascending expert order; gate = exp(l - lmax) /
+ * sum over the chosen (float32); then per expert the rows of its tokens in
+ * ascending token order, each group padded to a multiple of 128 rows.
+ *
+ *   logits [tokens, num_experts] float32 (num_experts <= 256, topk <= 16).
+ *   topk_idx int32 [tokens, topk], gates float32 [tokens, topk].
+ *   expert_counts int32 [num_experts], expert_offsets int32 [num_experts + 1].
+ *   row_token int32 [rows_capacity] (-1 on padding rows), token_row int32
+ *   [tokens, topk] (row of each slot).
+ *   rows_capacity >= tokens*topk + num_experts*127 (checked on the host).
+ */
+quads_status_t quads_moe_route(const float* logits, int32_t tokens, int32_t num_experts,
+                               int32_t topk, int32_t* topk_idx, float* gates,
+                               int32_t* expert_counts, int32_t* expert_offsets,
+                               int32_t* row_token, int32_t* token_row, int64_t rows_capacity,
+                               void* stream);
+
+/*
+ * quads_moe_gather -- copy NVFP4 rows into expert order: row r of the output is
+ * row row_token[r] of the input (zeros where row_token[r] < 0), for rows
+ * r < expert_offsets[num_experts] (as written by quads_moe_route).  Input
+ * scales LINEAR, output scales TCGEN05 (the grouped GEMM's operand layout).
+ *   in_codes [tokens, cols/2] -> out_codes [rows_capacity, cols/2];
+ *   in_scales [tokens, cols/16] -> out_scales TCGEN05 (cols % 64 == 0).
+ */
+quads_status_t quads_moe_gather(const int32_t* row_token, const int32_t* expert_offsets,
+                                int32_t num_experts, int64_t rows_capacity, int64_t cols,
+                                const uint8_t* in_codes, const uint8_t* in_scales,
+                                uint8_t* out_codes, uint8_t* out_scales, void* stream);
+
+/*
+ * quads_moe_combine -- out[t] = bf16( sum_j gates[t, j] * y[token_row[t, j]] )
+ * in float32, j ascending (ascending expert id).  y bf16 [rows, ldy].
+ */
+quads_status_t quads_moe_combine(const void* y, int64_t ldy, const int32_t* token_row,
+                                 const float* gates, int32_t tokens, int32_t topk,
+                                 int64_t hidden, void* out, int64_t ldo, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QUADS_H */

@@ -1,0 +1,106 @@
+// Host-side glue of the libquads C ABI: status strings, per-thread error
+// detail, workspace sizing and the device error word.
+#include <cstdarg>
+#include <cstdio>
+
+#include "common.cuh"
+
+namespace quads {
+
+static thread_local char g_detail[512] = "";
+
+void set_detail(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof(g_detail), fmt, ap);
+  va_end(ap);
+}
+
+quads_status_t fail(quads_status_t s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof(g_detail), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+quads_status_t check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(QUADS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return QUADS_OK;
+}
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
+}
+
+int read_quant_device_error(cudaStream_t);
+int read_gemm_device_error();
+
+}  // namespace quads
+
+using namespace quads;
+
+extern "C" int quads_version(void) { return 100; }
+
+extern "C" const char* quads_status_string(quads_status_t s) {
+  switch (s) {
+    case QUADS_OK: return "ok";
+    case QUADS_ERR_INVALID_ARG: return "invalid argument";
+    case QUADS_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case QUADS_ERR_MISALIGNED: return "misaligned pointer or leading dimension";
+    case QUADS_ERR_CUDA: return "CUDA error";
+    case QUADS_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+    case QUADS_ERR_DEVICE_CHECK: return "device-side argument check failed";
+    case QUADS_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+extern "C" const char* quads_last_error_detail(void) { return g_detail; }
+
+extern "C" int32_t quads_kpad(int32_t k) {
+  if (k <= 64) return 64;
+  if (k <= 128) return 128;
+  if (k <= 256) return 256;
+  return (k + 255) / 256 * 256;
+}
+
+extern "C" size_t quads_workspace_size(int32_t op, int64_t rows, int64_t cols, int64_t n,
+                                       int32_t k, int32_t num_groups) {
+  const size_t G = num_groups > 0 ? (size_t)num_groups : 1;
+  switch (op) {
+    case QUADS_OP_QUANTIZE:
+      return G * 4;
+    case QUADS_OP_SELECT:
+      return (((size_t)rows * (size_t)k * 4 + 255) & ~(size_t)255) + G * 4;
+    case QUADS_OP_GEMM:
+    case QUADS_OP_MOE_GEMM: {
+      const size_t e = op == QUADS_OP_MOE_GEMM ? G : 1;
+      const size_t kp = (size_t)quads_kpad(k);
+      const size_t brows = e * (size_t)n;
+      return ((brows * kp / 2 + 1023) & ~(size_t)1023) + brows * kp / 16;
+    }
+  }
+  (void)cols;
+  return 0;
+}
+
+extern "C" quads_status_t quads_device_status(void* stream, int32_t* device_code) {
+  if (!device_code) return fail(QUADS_ERR_INVALID_ARG, "device_status: null output");
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(QUADS_ERR_CUDA, "device_status: %s", cudaGetErrorString(e));
+  int g = read_gemm_device_error();
+  int q = read_quant_device_error((cudaStream_t)stream);
+  *device_code = g ? g : q;
+  return QUADS_OK;
+}

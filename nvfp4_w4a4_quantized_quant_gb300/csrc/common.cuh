@@ -1,0 +1,171 @@
+// Shared device helpers for libquads (sm_103a).
+//
+// NVFP4 element/scale arithmetic follows the NVFP4 description of the TRACE
+// digest ("NVFP4 与 E2M1 码本": global scale + per-16-block scale, round to
+// nearest E2M1 level) with every step an IEEE float32 operation, so that codes
+// and scale bytes are reproducible bit for bit.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/quads.h"
+
+namespace quads {
+
+constexpr int kBlock = 16;            // elements per block scale
+constexpr int kScoreChunk = QUADS_SCORE_CHUNK_ROWS;
+constexpr float kE2M1Max = 6.0f;
+constexpr float kE4M3Max = 448.0f;
+
+// ----------------------------------------------------------------- host status
+void set_detail(const char* fmt, ...);
+quads_status_t fail(quads_status_t s, const char* fmt, ...);
+quads_status_t check_launch(const char* what);
+int num_sms();
+
+// ------------------------------------------------------------ scale layouts
+// Byte offset of scale column c (a 16-element block) of row r in the
+// tensor-core layout: 128-row x 4-column blocks of 512 bytes, row-block major.
+__host__ __device__ __forceinline__ int64_t sf_tc_offset(int64_t r, int64_t c, int64_t ncols16) {
+  return ((r >> 7) * (ncols16 >> 2) + (c >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (c & 3);
+}
+__host__ __device__ __forceinline__ int64_t sf_offset(int layout, int64_t r, int64_t c,
+                                                      int64_t ncols16) {
+  return layout == QUADS_SCALES_TCGEN05 ? sf_tc_offset(r, c, ncols16) : r * ncols16 + c;
+}
+// Bytes of a TCGEN05-layout scale array for rows x cols elements.
+__host__ __device__ __forceinline__ int64_t sf_tc_bytes(int64_t rows, int64_t cols) {
+  return ((rows + 127) / 128) * 128 * (cols / 16);
+}
+
+// ------------------------------------------------------------ conversions
+// E4M3 byte -> float, from the format: bias 7, 3 mantissa bits, subnormals.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+  uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  if (e == 0) return (float)m * 0.001953125f;  // m * 2^-9, exact
+  return __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// Non-negative float -> E4M3 byte, nearest/even, saturating at 448.
+__device__ __forceinline__ uint32_t f32_to_e4m3_sat(float u) {
+  u = fminf(u, kE4M3Max);
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(u));
+  return r & 0xFFu;
+}
+
+// Eight floats -> eight E2M1 codes packed in 32 bits (element i in nibble i).
+__device__ __forceinline__ uint32_t f32x8_to_e2m1(const float* v) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(out)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]),
+        "f"(v[7]));
+  return out;
+}
+
+// E2M1 code (4 bits) -> float value, from the format: 2 exponent bits (bias 1),
+// 1 mantissa bit, subnormal 0.5 step.
+__device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
+  uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  float mag = e == 0 ? 0.5f * (float)m : __uint_as_float(((e + 126u) << 23) | (m << 22));
+  return (c & 8u) ? -mag : mag;
+}
+
+// Eight packed codes -> eight floats via the hardware E2M1 -> f16 converter.
+__device__ __forceinline__ void e2m1x8_to_f32(uint32_t packed, float* out) {
+  uint32_t h[4];
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(packed));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 hh = *reinterpret_cast<__half2*>(&h[i]);
+    float2 f = __half22float2(hh);
+    out[2 * i] = f.x;
+    out[2 * i + 1] = f.y;
+  }
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// Tensor scale from the tensor's absolute maximum: fl(amax / 2688), 1 if 0.
+__device__ __forceinline__ float tensor_scale_from_amax(float amax) {
+  float s = __fdiv_rn(amax, kE2M1Max * kE4M3Max);
+  return s == 0.0f ? 1.0f : s;
+}
+
+struct BlockScale {
+  uint32_t byte;  // E4M3 scale byte
+  float d;        // E4M3value * s_t
+  float r;        // 1 / d (correctly rounded)
+  bool zero;      // d == 0 or 1/d overflowed: all codes 0
+};
+
+// Block scale of a 16-block with absolute maximum m under tensor scale s_t.
+__device__ __forceinline__ BlockScale block_scale(float m, float s_t) {
+  BlockScale b;
+  float u = __fdiv_rn(m, __fmul_rn(kE2M1Max, s_t));
+  b.byte = f32_to_e4m3_sat(u);
+  b.d = __fmul_rn(e4m3_to_f32(b.byte), s_t);
+  b.r = __frcp_rn(b.d);
+  b.zero = (b.d == 0.0f) || isinf(b.r);
+  return b;
+}
+
+// Block scale for a byte that is already known (decode side).
+__device__ __forceinline__ BlockScale block_scale_from_byte(uint32_t byte, float s_t) {
+  BlockScale b;
+  b.byte = byte;
+  b.d = __fmul_rn(e4m3_to_f32(byte), s_t);
+  b.r = __frcp_rn(b.d);
+  b.zero = (b.d == 0.0f) || isinf(b.r);
+  return b;
+}
+
+// Quantize 8 values of one block: returns packed codes; writes levels*d residuals
+// when want_residual.
+__device__ __forceinline__ uint32_t quantize8(const float* x, const BlockScale& bs) {
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(x[i], bs.r);
+  uint32_t c = f32x8_to_e2m1(v);
+  return bs.zero ? 0u : c;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Group index of `row` for ascending offsets goff[0..G] (binary search).
+__device__ __forceinline__ int group_of(const int32_t* goff, int G, int64_t row) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (goff[mid] <= row) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+}  // namespace quads

@@ -1,0 +1,706 @@
+// Compensated NVFP4 W4A4 GEMM on the sm_103a tensor cores.
+//
+//   Y = s_a s_w * Q(A) Q(W)^T  +  s_r s_w * Q(R_sel) Q(W_sel)^T
+//
+// [QUADS technical summary] 2.2 B "Mechanism": the correction of the selected
+// high-residual channels is added back to the quantized output; section 1: the
+// bulk stays a native W4A4 GEMM.  Here both products run in one persistent
+// kernel: the main K loop accumulates into one TMEM accumulator, the k-channel
+// correction loop into a second one, and the epilogue forms a1*acc1 + a2*acc2.
+//
+// Design (one CTA per SM, 128x128 output tiles, K tiles of 256 FP4 = 128 B):
+//   warp 0     TMA producer: A/B code tiles by tensor-map TMA (128B swizzle),
+//              scale-factor atoms by bulk copy, into a 6-stage smem ring.
+//   warp 1     TMEM allocator + MMA issuer (one thread): tcgen05.cp moves the
+//              stage's scale atoms into TMEM, then tcgen05.mma
+//              .kind::mxf4nvf4.block_scale.scale_vec::4X (M=128, N=128, K=64).
+//   warps 2-5  epilogue: tcgen05.ld of both accumulators, scale, store.
+// TMEM columns: acc1 double-buffered (0-127, 128-255), acc2 (256-383),
+// scale-factor ring (384-511, 4 buffers x 32 columns).
+// Every mbarrier wait is bounded; on timeout the kernel latches an error word,
+// stops all roles, and still releases its TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdio>
+
+#include "common.cuh"
+
+namespace quads {
+namespace gemm {
+
+constexpr int BM = 128, BN = 128;
+constexpr int BK_BYTES = 128;                 // 256 FP4 elements per K tile
+constexpr int STAGES = 6;
+constexpr int A_TILE = BM * BK_BYTES;         // 16 KB
+constexpr int B_TILE = BN * BK_BYTES;         // 16 KB
+constexpr int SF_TILE = 4 * 512;              // 4 atoms (128 rows x 16 blocks)
+constexpr int STAGE_BYTES = A_TILE + B_TILE + 2 * SF_TILE;
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 512;
+constexpr int ACC2_COL = 256;
+constexpr int SF_COL = 384;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*barriers*/ + 1024 /*align*/;
+constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per wait
+
+enum { OUT_F32 = 0, OUT_BF16 = 1, OUT_SWIGLU = 2 };
+
+struct Params {
+  int E, N, K, kpad, Nt;
+  int64_t M;                    // dense rows (row_off == nullptr)
+  const int32_t* row_off;       // [E+1] padded row offsets (multiples of 128) or null
+  const int32_t* row_cnt;       // [E] real rows (null: all rows of the tile range are real)
+  const uint8_t* a_sf;
+  const uint8_t* b_sf;
+  const uint8_t* r_sf;
+  const uint8_t* ws_sf;
+  const float* a_ts;
+  const float* b_ts;
+  const float* r_ts;
+  int a_ts_pe, r_ts_pe;
+  int comp;
+  void* y;
+  int64_t ldy;
+  int out_mode;
+  int* err;
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: false when the wait gave up (error latched) or another role aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t* b, uint32_t parity, volatile int* abort_flag,
+                                         int* err) {
+  if (mbar_try_wait(b, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (mbar_try_wait(b, parity)) return true;
+    if ((++spins & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        atomicExch(err, QUADS_ERR_DEVICE_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t* b) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(b))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand tile, rows of 128 bytes,
+// 128-byte swizzle, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;             // leading-dimension offset (unused for this layout)
+  d |= (uint64_t)(1024 >> 4) << 32;   // stride between 8-row groups
+  d |= (uint64_t)1 << 46;             // descriptor version
+  d |= (uint64_t)2 << 61;             // 128-byte swizzle
+  return d;
+}
+// Descriptor of one 512-byte scale atom: 32 rows of 16 bytes, no swizzle,
+// 8-row core matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Instruction descriptor: kind::mxf4nvf4, A and B E2M1, K-major, UE4M3 scales,
+// scale-factor ids 0, dense.
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc));
+}
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb));
+}
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tc_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- tile schedule
+struct Tile {
+  int e;
+  int64_t m0;   // first row of the tile in the A row space
+  int n0;       // first output column
+  int64_t row_end;  // rows >= row_end are not real (not stored for OUT_F32/BF16)
+};
+
+__device__ __forceinline__ int64_t total_tiles(const Params& p) {
+  if (!p.row_off) return ((p.M + BM - 1) / BM) * p.Nt;
+  return (int64_t)(p.row_off[p.E] / BM) * p.Nt;
+}
+
+__device__ __forceinline__ Tile decode_tile(const Params& p, int64_t t) {
+  Tile r;
+  if (!p.row_off) {
+    const int64_t Mt = (p.M + BM - 1) / BM;
+    r.e = 0;
+    r.m0 = (t % Mt) * BM;
+    r.n0 = (int)(t / Mt) * BN;
+    r.row_end = p.M;
+    return r;
+  }
+  // expert e holds tiles [row_off[e]/128 * Nt, row_off[e+1]/128 * Nt), m fastest
+  int lo = 0, hi = p.E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)(p.row_off[mid] / BM) * p.Nt <= t) lo = mid; else hi = mid - 1;
+  }
+  const int e = lo;
+  const int64_t base = (int64_t)(p.row_off[e] / BM) * p.Nt;
+  const int64_t mt_e = (p.row_off[e + 1] - p.row_off[e]) / BM;
+  const int64_t local = t - base;
+  r.e = e;
+  r.m0 = p.row_off[e] + (local % mt_e) * BM;
+  r.n0 = (int)(local / mt_e) * BN;
+  r.row_end = p.row_off[e] + (p.row_cnt ? p.row_cnt[e] : (p.row_off[e + 1] - p.row_off[e]));
+  return r;
+}
+
+// ---------------------------------------------------------------- the kernel
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmW,
+                const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = bars;                 // [STAGES]
+  uint64_t* empty = bars + STAGES;       // [STAGES]
+  uint64_t* sf_free = bars + 2 * STAGES; // [4]
+  uint64_t* acc_full = sf_free + 4;      // [2]
+  uint64_t* acc_empty = acc_full + 2;    // [2]
+  uint32_t* tmem_holder = (uint32_t*)(acc_empty + 2);
+  volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
+    for (int i = 0; i < 4; ++i) mbar_init(&sf_free[i], 1);
+    for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 128); }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_holder)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  const int64_t ntiles = total_tiles(p);
+  const int KT = (p.K + 255) / 256;
+  const int KTc = p.comp ? (p.kpad + 255) / 256 : 0;
+  const int64_t a_sf_rb = (int64_t)(p.K / 64) * 512;    // bytes per 128-row block
+  const int64_t r_sf_rb = (int64_t)(p.kpad / 64) * 512;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t it = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      const Tile tl = decode_tile(p, t);
+      const int64_t brow = (int64_t)tl.e * p.N + tl.n0;
+      for (int kt = 0; kt < KT + KTc && ok; ++kt, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!wait_bar(&empty[s], ph ^ 1, abort_flag, p.err)) { ok = false; break; }
+        const bool corr = kt >= KT;
+        const int kk = corr ? kt - KT : kt;
+        const int klen = corr ? p.kpad : p.K;
+        const int nsteps = min(4, (klen - kk * 256) / 64);
+        uint8_t* st = smem + s * STAGE_BYTES;
+        mbar_expect_tx(&full[s], A_TILE + B_TILE + 2 * nsteps * 512);
+        if (!corr) {
+          tma_load_2d(st, &tmA, kk * BK_BYTES, (int)tl.m0, &full[s]);
+          tma_load_2d(st + A_TILE, &tmB, kk * BK_BYTES, (int)brow, &full[s]);
+          bulk_load(st + A_TILE + B_TILE, p.a_sf + (tl.m0 / BM) * a_sf_rb + kk * SF_TILE,
+                    nsteps * 512, &full[s]);
+          bulk_load(st + A_TILE + B_TILE + SF_TILE, p.b_sf + (brow / BN) * a_sf_rb + kk * SF_TILE,
+                    nsteps * 512, &full[s]);
+        } else {
+          tma_load_2d(st, &tmR, kk * BK_BYTES, (int)tl.m0, &full[s]);
+          tma_load_2d(st + A_TILE, &tmW, kk * BK_BYTES, (int)brow, &full[s]);
+          bulk_load(st + A_TILE + B_TILE, p.r_sf + (tl.m0 / BM) * r_sf_rb + kk * SF_TILE,
+                    nsteps * 512, &full[s]);
+          bulk_load(st + A_TILE + B_TILE + SF_TILE, p.ws_sf + (brow / BN) * r_sf_rb + kk * SF_TILE,
+                    nsteps * 512, &full[s]);
+        }
+      }
+    }
+    if (!ok && it > 0) {
+      // let copies already issued land before the CTA can exit
+      const uint32_t last = it - 1;
+      wait_bar(&full[last % STAGES], (last / STAGES) & 1, abort_flag, p.err);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_nvf4(BM, BN);
+    uint32_t it = 0;
+    uint32_t j = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++j) {
+      const uint32_t b = j & 1;
+      if (!wait_bar(&acc_empty[b], ((j >> 1) & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
+      tc_fence_after();
+      for (int kt = 0; kt < KT + KTc && ok; ++kt, ++it) {
+        const bool corr = kt >= KT;
+        const int kk = corr ? kt - KT : kt;
+        if (corr && kk == 0 && j > 0) {
+          // acc2 is free once the previous tile's epilogue is done
+          if (!wait_bar(&acc_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!wait_bar(&full[s], ph, abort_flag, p.err)) { ok = false; break; }
+        const uint32_t sb = it & 3;
+        if (!wait_bar(&sf_free[sb], ((it >> 2) & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const int klen = corr ? p.kpad : p.K;
+        const int nsteps = min(4, (klen - kk * 256) / 64);
+        uint8_t* st = smem + s * STAGE_BYTES;
+        const uint32_t sa = smem_u32(st), sbb = smem_u32(st + A_TILE);
+        const uint32_t ssfa = smem_u32(st + A_TILE + B_TILE);
+        const uint32_t ssfb = ssfa + SF_TILE;
+        const uint32_t tsf = tmem + SF_COL + sb * 32;
+        for (int q = 0; q < nsteps; ++q) {
+          tc_cp_sf(tsf + q * 4, desc_sf(ssfa + q * 512));
+          tc_cp_sf(tsf + 16 + q * 4, desc_sf(ssfb + q * 512));
+        }
+        const uint32_t dcol = corr ? (tmem + ACC2_COL) : (tmem + b * BN);
+        for (int q = 0; q < nsteps; ++q) {
+          tc_mma(dcol, desc_sw128(sa + q * 32), desc_sw128(sbb + q * 32), idesc, tsf + q * 4,
+                 tsf + 16 + q * 4, (kk > 0 || q > 0) ? 1u : 0u);
+        }
+        tc_commit(&empty[s]);
+        tc_commit(&sf_free[sb]);
+      }
+      if (!ok) break;
+      tc_commit(&acc_full[b]);
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    const int row_in_tile = quad * 32 + lane;
+    uint32_t j = 0;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++j) {
+      const Tile tl = decode_tile(p, t);
+      const uint32_t b = j & 1;
+      // lane 0 waits, the warp follows it (tcgen05.ld needs the whole warp)
+      int okw = 0;
+      if (lane == 0) okw = wait_bar(&acc_full[b], (j >> 1) & 1, abort_flag, p.err) ? 1 : 0;
+      okw = __shfl_sync(0xffffffffu, okw, 0);
+      if (!okw) break;
+      tc_fence_after();
+      const float bts = p.b_ts[tl.e];
+      const float a1 = __fmul_rn(p.a_ts[p.a_ts_pe ? tl.e : 0], bts);
+      const float a2 = p.comp ? __fmul_rn(p.r_ts[p.r_ts_pe ? tl.e : 0], bts) : 0.0f;
+      const int64_t row = tl.m0 + row_in_tile;
+      const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+      const uint32_t t1 = tmem + lane_base + b * BN;
+      const uint32_t t2 = tmem + lane_base + ACC2_COL;
+      if (p.out_mode == OUT_SWIGLU) {
+        // tile columns [0,64) are gate rows of W, [64,128) the matching up rows
+        const bool store = row < (p.row_off ? (int64_t)p.row_off[tl.e + 1] : p.M);
+        __nv_bfloat16* y = (__nv_bfloat16*)p.y + row * p.ldy + tl.n0 / 2;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+          float g1[16], u1[16], g2[16], u2[16];
+          tc_ld16(t1 + c0, g1);
+          tc_ld16(t1 + 64 + c0, u1);
+          if (p.comp) { tc_ld16(t2 + c0, g2); tc_ld16(t2 + 64 + c0, u2); }
+          tc_wait_ld();
+          uint32_t packed[8];
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            float h[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              float g = a1 * g1[i + q], u = a1 * u1[i + q];
+              if (p.comp) { g = fmaf(a2, g2[i + q], g); u = fmaf(a2, u2[i + q], u); }
+              h[q] = g / (1.0f + expf(-g)) * u;
+            }
+            __nv_bfloat162 hb = __floats2bfloat162_rn(h[0], h[1]);
+            packed[i / 2] = *reinterpret_cast<uint32_t*>(&hb);
+          }
+          if (store) {
+            uint4* dst = reinterpret_cast<uint4*>(y + c0);
+            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          }
+        }
+      } else {
+        const bool store = row < tl.row_end;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          float v1[16], v2[16];
+          tc_ld16(t1 + c0, v1);
+          if (p.comp) tc_ld16(t2 + c0, v2);
+          tc_wait_ld();
+          float o[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] = p.comp ? fmaf(a2, v2[i], a1 * v1[i]) : a1 * v1[i];
+          if (store) {
+            if (p.out_mode == OUT_F32) {
+              float4* dst = reinterpret_cast<float4*>((float*)p.y + row * p.ldy + tl.n0 + c0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            } else {
+              uint32_t packed[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                __nv_bfloat162 hb = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+                packed[i] = *reinterpret_cast<uint32_t*>(&hb);
+              }
+              uint4* dst = reinterpret_cast<uint4*>((__nv_bfloat16*)p.y + row * p.ldy + tl.n0 + c0);
+              dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+              dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[b]);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TMEM_COLS));
+  }
+}
+
+// ---------------------------------------------------------------- Q(W_sel)
+// For every weight row n (of every expert) and every 16-block of the selected
+// channels: gather the selected columns of DQ(Q(W)) in units of s_w
+// (level * E4M3 scale, exact), requantize with tensor scale 1 (s_w kept).
+// Output codes [E*N, kpad/2] and TCGEN05 scales over kpad columns.
+__global__ void __launch_bounds__(256) wsel_kernel(
+    const uint8_t* __restrict__ wc, const uint8_t* __restrict__ wsf, int64_t rows /*E*N*/, int N,
+    int K, const int32_t* __restrict__ sel, int sel_pe, int k, int kpad,
+    uint8_t* __restrict__ oc, uint8_t* __restrict__ osf) {
+  const int nb = kpad >> 4;
+  const int64_t total = rows * nb;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / nb;
+    const int blk = (int)(i % nb);
+    uint32_t lo = 0, hi = 0, sbyte = 0;
+    if (blk * 16 < k) {
+      const int e = (int)(r / N);
+      const int32_t* s = sel + (sel_pe ? (int64_t)e * k : 0) + blk * 16;
+      float w[16];
+      float m = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int c = s[j];
+        const uint32_t byte = wc[r * (K >> 1) + (c >> 1)];
+        const uint32_t code = (c & 1) ? (byte >> 4) : (byte & 15u);
+        const float sc = e4m3_to_f32(wsf[sf_tc_offset(r, c >> 4, K >> 4)]);
+        w[j] = __fmul_rn(e2m1_to_f32(code), sc);
+        m = fmaxf(m, fabsf(w[j]));
+      }
+      const BlockScale bs = block_scale(m, 1.0f);
+      lo = quantize8(w, bs);
+      hi = quantize8(w + 8, bs);
+      sbyte = bs.byte;
+    }
+    uint2* dst = reinterpret_cast<uint2*>(oc + r * (kpad >> 1) + blk * 8);
+    *dst = make_uint2(lo, hi);
+    osf[sf_tc_offset(r, blk, nb)] = (uint8_t)sbyte;
+  }
+}
+
+// ---------------------------------------------------------------- host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+  }
+  return fn;
+}
+
+// 2-D byte tensor [rows, width_bytes] (row pitch ld_bytes), box 128 B x 128 rows,
+// 128-byte swizzle, out-of-range elements read as zero.
+static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t width_bytes,
+                     int64_t ld_bytes) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)width_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld_bytes};
+  cuuint32_t box[2] = {BK_BYTES, BM};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static __device__ int g_gemm_error;
+
+struct Launch {
+  int64_t M, rows_cap;
+  int E, N, K, k, kpad;
+  const int32_t* row_off;
+  const int32_t* row_cnt;
+  const uint8_t *a, *a_sf, *b, *b_sf, *r, *r_sf;
+  const float *a_ts, *b_ts, *r_ts;
+  int a_pe, r_pe;
+  const int32_t* sel;
+  int sel_pe;
+  void* y;
+  int64_t ldy;
+  int out_mode;
+  void* ws;
+  size_t ws_bytes;
+  cudaStream_t stream;
+};
+
+static quads_status_t launch(const Launch& L) {
+  const bool comp = L.r != nullptr;
+  const int64_t brows = (int64_t)L.E * L.N;
+  uint8_t* ws_codes = nullptr;
+  uint8_t* ws_sf = nullptr;
+  if (comp) {
+    const size_t need = quads_workspace_size(L.row_off ? QUADS_OP_MOE_GEMM : QUADS_OP_GEMM, 0,
+                                             L.K, L.N, L.k, L.E);
+    if (!L.ws || L.ws_bytes < need)
+      return fail(QUADS_ERR_WORKSPACE, "gemm: workspace needs %zu bytes", need);
+    ws_codes = (uint8_t*)L.ws;
+    ws_sf = ws_codes + (((size_t)brows * (L.kpad / 2) + 1023) & ~(size_t)1023);
+    const int64_t total = brows * (L.kpad / 16);
+    int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)num_sms() * 16);
+    wsel_kernel<<<blocks, 256, 0, L.stream>>>(L.b, L.b_sf, brows, L.N, L.K, L.sel, L.sel_pe, L.k,
+                                               L.kpad, ws_codes, ws_sf);
+  }
+  CUtensorMap tA, tB, tR, tW;
+  const int64_t arows = L.row_off ? L.rows_cap : L.M;
+  if (!make_map(&tA, L.a, arows, L.K / 2, L.K / 2) || !make_map(&tB, L.b, brows, L.K / 2, L.K / 2))
+    return fail(QUADS_ERR_CUDA, "gemm: cuTensorMapEncodeTiled failed for A/W");
+  if (comp) {
+    if (!make_map(&tR, L.r, arows, L.kpad / 2, L.kpad / 2) ||
+        !make_map(&tW, ws_codes, brows, L.kpad / 2, L.kpad / 2))
+      return fail(QUADS_ERR_CUDA, "gemm: cuTensorMapEncodeTiled failed for R/W_sel");
+  } else {
+    tR = tA;
+    tW = tB;
+  }
+  Params p;
+  p.E = L.E; p.N = L.N; p.K = L.K; p.kpad = comp ? L.kpad : 0; p.Nt = L.N / BN;
+  p.M = L.M; p.row_off = L.row_off; p.row_cnt = L.row_cnt;
+  p.a_sf = L.a_sf; p.b_sf = L.b_sf; p.r_sf = L.r_sf; p.ws_sf = ws_sf;
+  p.a_ts = L.a_ts; p.b_ts = L.b_ts; p.r_ts = L.r_ts; p.a_ts_pe = L.a_pe; p.r_ts_pe = L.r_pe;
+  p.comp = comp ? 1 : 0;
+  p.y = L.y; p.ldy = L.ldy; p.out_mode = L.out_mode;
+  static int* errp = nullptr;
+  if (!errp && cudaGetSymbolAddress((void**)&errp, g_gemm_error) != cudaSuccess)
+    return fail(QUADS_ERR_CUDA, "gemm: cannot resolve the device error word");
+  p.err = errp;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    attr_set = true;
+  }
+  int64_t grid = num_sms();
+  if (!L.row_off) grid = std::min<int64_t>(grid, ((L.M + BM - 1) / BM) * (L.N / BN));
+  gemm_kernel<<<(int)grid, NUM_THREADS, SMEM_BYTES, L.stream>>>(tA, tB, tR, tW, p);
+  return check_launch("gemm");
+}
+
+}  // namespace gemm
+
+int read_gemm_device_error() {
+  int v = 0;
+  cudaMemcpyFromSymbol(&v, gemm::g_gemm_error, sizeof(int));
+  int zero = 0;
+  cudaMemcpyToSymbol(gemm::g_gemm_error, &zero, sizeof(int));
+  return v;
+}
+
+}  // namespace quads
+
+using namespace quads;
+
+static bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+extern "C" quads_status_t quads_w4a4_gemm_comp(int64_t M, int64_t N, int64_t K,
+                                               const uint8_t* a_codes, const uint8_t* a_scales,
+                                               const float* a_tensor_scale, const uint8_t* w_codes,
+                                               const uint8_t* w_scales, const float* w_tensor_scale,
+                                               const uint8_t* r_codes, const uint8_t* r_scales,
+                                               const float* r_tensor_scale, const int32_t* sel,
+                                               int32_t k, void* y, int32_t y_dtype, int64_t ldy,
+                                               void* workspace, size_t workspace_bytes,
+                                               void* stream) {
+  if (!a_codes || !a_scales || !a_tensor_scale || !w_codes || !w_scales || !w_tensor_scale || !y)
+    return fail(QUADS_ERR_INVALID_ARG, "gemm: null operand pointer");
+  if (M < 1 || N % 128 || N <= 0 || K % 64 || K <= 0)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "gemm: need M>=1, N%%128==0, K%%64==0 (M=%lld N=%lld K=%lld)", (long long)M, (long long)N, (long long)K);
+  if (M > (1ll << 31) - 256 || (int64_t)N * K / 2 > (1ll << 40))
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "gemm: shape too large");
+  if (y_dtype != QUADS_OUT_F32 && y_dtype != QUADS_OUT_BF16)
+    return fail(QUADS_ERR_INVALID_ARG, "gemm: y_dtype");
+  if (ldy < N || (y_dtype == QUADS_OUT_F32 ? ldy % 4 : ldy % 8))
+    return fail(QUADS_ERR_MISALIGNED, "gemm: ldy must be >= N and keep 16-byte rows");
+  if (!al16(a_codes) || !al16(w_codes) || !al16(a_scales) || !al16(w_scales) || !al16(y) ||
+      (r_codes && (!al16(r_codes) || !al16(r_scales))))
+    return fail(QUADS_ERR_MISALIGNED, "gemm: operands must be 16-byte aligned");
+  if (r_codes && (!r_scales || !r_tensor_scale || !sel || k <= 0 || k % 16 || k > K))
+    return fail(QUADS_ERR_INVALID_ARG, "gemm: compensation needs r_scales, r_tensor_scale, sel and 16<=k<=K, k%%16==0");
+  gemm::Launch L{};
+  L.M = M; L.rows_cap = M; L.E = 1; L.N = (int)N; L.K = (int)K; L.k = k;
+  L.kpad = r_codes ? quads_kpad(k) : 0;
+  L.row_off = nullptr; L.row_cnt = nullptr;
+  L.a = a_codes; L.a_sf = a_scales; L.b = w_codes; L.b_sf = w_scales;
+  L.r = r_codes; L.r_sf = r_scales;
+  L.a_ts = a_tensor_scale; L.b_ts = w_tensor_scale; L.r_ts = r_tensor_scale;
+  L.a_pe = 0; L.r_pe = 0; L.sel = sel; L.sel_pe = 0;
+  L.y = y; L.ldy = ldy; L.out_mode = y_dtype == QUADS_OUT_F32 ? gemm::OUT_F32 : gemm::OUT_BF16;
+  L.ws = workspace; L.ws_bytes = workspace_bytes; L.stream = (cudaStream_t)stream;
+  return gemm::launch(L);
+}
+
+extern "C" quads_status_t quads_moe_grouped_gemm(
+    int32_t num_experts, int64_t rows_capacity, int64_t N, int64_t K,
+    const int32_t* expert_offsets, const int32_t* expert_counts, const uint8_t* a_codes,
+    const uint8_t* a_scales, const float* a_tensor_scale, int32_t a_scale_per_expert,
+    const uint8_t* w_codes, const uint8_t* w_scales, const float* w_tensor_scale,
+    const uint8_t* r_codes, const uint8_t* r_scales, const float* r_tensor_scale,
+    int32_t r_scale_per_expert, const int32_t* sel, int32_t sel_per_expert, int32_t k,
+    int32_t epilogue, void* y, int32_t y_dtype, int64_t ldy, void* workspace,
+    size_t workspace_bytes, void* stream) {
+  if (!expert_offsets || !a_codes || !a_scales || !a_tensor_scale || !w_codes || !w_scales ||
+      !w_tensor_scale || !y)
+    return fail(QUADS_ERR_INVALID_ARG, "moe_gemm: null operand pointer");
+  if (num_experts < 1 || rows_capacity < 1 || rows_capacity % 128 || N % 128 || N <= 0 ||
+      K % 64 || K <= 0)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "moe_gemm: need experts>=1, rows_capacity%%128==0, N%%128==0, K%%64==0");
+  if (epilogue != QUADS_EPILOGUE_NONE && epilogue != QUADS_EPILOGUE_SWIGLU)
+    return fail(QUADS_ERR_INVALID_ARG, "moe_gemm: epilogue");
+  if (epilogue == QUADS_EPILOGUE_SWIGLU && y_dtype != QUADS_OUT_BF16)
+    return fail(QUADS_ERR_INVALID_ARG, "moe_gemm: SWIGLU writes bf16");
+  const int64_t ycols = epilogue == QUADS_EPILOGUE_SWIGLU ? N / 2 : N;
+  if (ldy < ycols || (y_dtype == QUADS_OUT_F32 ? ldy % 4 : ldy % 8))
+    return fail(QUADS_ERR_MISALIGNED, "moe_gemm: ldy");
+  if (!al16(a_codes) || !al16(w_codes) || !al16(a_scales) || !al16(w_scales) || !al16(y) ||
+      (r_codes && (!al16(r_codes) || !al16(r_scales))))
+    return fail(QUADS_ERR_MISALIGNED, "moe_gemm: operands must be 16-byte aligned");
+  if (r_codes && (!r_scales || !r_tensor_scale || !sel || k <= 0 || k % 16 || k > K))
+    return fail(QUADS_ERR_INVALID_ARG, "moe_gemm: compensation needs r_scales, r_tensor_scale, sel and valid k");
+  gemm::Launch L{};
+  L.M = rows_capacity; L.rows_cap = rows_capacity; L.E = num_experts; L.N = (int)N; L.K = (int)K;
+  L.k = k; L.kpad = r_codes ? quads_kpad(k) : 0;
+  L.row_off = expert_offsets; L.row_cnt = expert_counts;
+  L.a = a_codes; L.a_sf = a_scales; L.b = w_codes; L.b_sf = w_scales;
+  L.r = r_codes; L.r_sf = r_scales;
+  L.a_ts = a_tensor_scale; L.b_ts = w_tensor_scale; L.r_ts = r_tensor_scale;
+  L.a_pe = a_scale_per_expert; L.r_pe = r_scale_per_expert; L.sel = sel; L.sel_pe = sel_per_expert;
+  L.y = y; L.ldy = ldy;
+  L.out_mode = epilogue == QUADS_EPILOGUE_SWIGLU ? gemm::OUT_SWIGLU
+               : (y_dtype == QUADS_OUT_F32 ? gemm::OUT_F32 : gemm::OUT_BF16);
+  L.ws = workspace; L.ws_bytes = workspace_bytes; L.stream = (cudaStream_t)stream;
+  return gemm::launch(L);
+}

@@ -1,0 +1,252 @@
+// MoE dispatch around the grouped compensated GEMM: router top-k with gate
+// weights, the deterministic token -> expert row plan (groups padded to 128
+// rows), the gather of NVFP4 rows into expert order, and the gate-weighted
+// combine.  [TRACE digest] "MoE 专家路由敏感性": the router sends every token to a
+// few experts by gate score.
+//
+// Determinism: counts use integer atomics (order-free); every row position is
+// a prefix count over tokens, so the plan is identical from run to run.
+#include <algorithm>
+#include <cstdio>
+
+#include "common.cuh"
+
+namespace quads {
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopk = 16;
+
+// One warp per token.  Lane l holds logits l, l+32, ...; each of topk rounds
+// takes the warp arg-max (ties -> lower expert id) and removes it.
+__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T,
+                                                    int E, int topk, int32_t* __restrict__ idx,
+                                                    float* __restrict__ gates,
+                                                    int32_t* __restrict__ counts) {
+  const int lane = threadIdx.x & 31;
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t >= T) return;
+  float v[kMaxExperts / 32];
+  const int per = (E + 31) / 32;
+#pragma unroll
+  for (int i = 0; i < kMaxExperts / 32; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (i < per && e < E) ? logits[(int64_t)t * E + e] : -INFINITY;
+  }
+  uint32_t taken = 0;
+  int chosen[kMaxTopk];
+  float chosen_l[kMaxTopk];
+  for (int r = 0; r < topk; ++r) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int e = lane + 32 * i;
+      if (i < per && e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
+        bv = v[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+    }
+    chosen[r] = be;
+    chosen_l[r] = bv;
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+  }
+  if (lane == 0) {
+    // gates: exp(l - lmax) / sum over the chosen, lmax = the first pick
+    float p[kMaxTopk];
+    float s = 0.0f;
+    for (int r = 0; r < topk; ++r) { p[r] = expf(chosen_l[r] - chosen_l[0]); s += p[r]; }
+    // emit in ascending expert order (insertion sort of <= 16 entries)
+    for (int a = 1; a < topk; ++a)
+      for (int b = a; b > 0 && chosen[b - 1] > chosen[b]; --b) {
+        int te = chosen[b]; chosen[b] = chosen[b - 1]; chosen[b - 1] = te;
+        float tp = p[b]; p[b] = p[b - 1]; p[b - 1] = tp;
+      }
+    for (int r = 0; r < topk; ++r) {
+      idx[(int64_t)t * topk + r] = chosen[r];
+      gates[(int64_t)t * topk + r] = p[r] / s;
+      atomicAdd(&counts[chosen[r]], 1);
+    }
+  }
+}
+
+// Padded offsets: off[e+1] = off[e] + roundup(count[e], 128).  One block.
+__global__ void plan_kernel(const int32_t* __restrict__ counts, int E, int32_t* __restrict__ off) {
+  __shared__ int s[kMaxExperts];
+  const int e = threadIdx.x;
+  if (e < E) s[e] = (counts[e] + QUADS_MOE_ROW_ALIGN - 1) / QUADS_MOE_ROW_ALIGN * QUADS_MOE_ROW_ALIGN;
+  __syncthreads();
+  if (e == 0) {
+    int acc = 0;
+    off[0] = 0;
+    for (int i = 0; i < E; ++i) { acc += s[i]; off[i + 1] = acc; }
+  }
+}
+
+// One block per expert: scan the tokens in order; a token routed to the expert
+// gets the next row of its group.  Padding rows get row_token = -1.
+__global__ void __launch_bounds__(1024) assign_kernel(const int32_t* __restrict__ idx, int T,
+                                                      int topk, const int32_t* __restrict__ off,
+                                                      const int32_t* __restrict__ counts,
+                                                      int32_t* __restrict__ row_token,
+                                                      int32_t* __restrict__ token_row) {
+  __shared__ int warp_tot[32];
+  __shared__ int base_s;
+  const int e = blockIdx.x;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (threadIdx.x == 0) base_s = 0;
+  __syncthreads();
+  for (int t0 = 0; t0 < T; t0 += blockDim.x) {
+    const int t = t0 + threadIdx.x;
+    int slot = -1;
+    if (t < T)
+      for (int j = 0; j < topk; ++j)
+        if (idx[(int64_t)t * topk + j] == e) slot = j;
+    const int f = slot >= 0 ? 1 : 0;
+    const unsigned bal = __ballot_sync(0xffffffffu, f);
+    const int pre = __popc(bal & ((1u << lane) - 1u));
+    if (lane == 0) warp_tot[w] = __popc(bal);
+    __syncthreads();
+    int wbase = 0;
+    for (int i = 0; i < w; ++i) wbase += warp_tot[i];
+    if (f) {
+      const int row = off[e] + base_s + wbase + pre;
+      row_token[row] = t;
+      token_row[(int64_t)t * topk + slot] = row;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int tot = 0;
+      for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += warp_tot[i];
+      base_s += tot;
+    }
+    __syncthreads();
+  }
+  for (int r = off[e] + counts[e] + threadIdx.x; r < off[e + 1]; r += blockDim.x) row_token[r] = -1;
+}
+
+// One warp per output row: codes (16 B per lane-iteration), then the row's
+// scale bytes in groups of 4 (one 64-element atom column each).
+__global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__ row_token,
+                                                     const int32_t* __restrict__ off, int E,
+                                                     int64_t cap, int cols,
+                                                     const uint8_t* __restrict__ ic,
+                                                     const uint8_t* __restrict__ isf,
+                                                     uint8_t* __restrict__ oc,
+                                                     uint8_t* __restrict__ osf) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nrows = off[E];
+  const int cbytes = cols >> 1;
+  const int ncols16 = cols >> 4;
+  for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < nrows;
+       r += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+    const int t = row_token[r];
+    for (int b = lane * 16; b < cbytes; b += 512) {
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (t >= 0) v = *reinterpret_cast<const uint4*>(ic + (int64_t)t * cbytes + b);
+      *reinterpret_cast<uint4*>(oc + r * cbytes + b) = v;
+    }
+    for (int a = lane; a < (ncols16 >> 2); a += 32) {
+      uint32_t v = 0;
+      if (t >= 0) v = *reinterpret_cast<const uint32_t*>(isf + (int64_t)t * ncols16 + 4 * a);
+      *reinterpret_cast<uint32_t*>(osf + sf_tc_offset(r, 4 * a, ncols16)) = v;
+    }
+  }
+}
+
+// out[t, :] = bf16(sum_j gate[t, j] * y[row(t, j), :]), float32, j ascending.
+__global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __restrict__ y,
+                                                      int64_t ldy,
+                                                      const int32_t* __restrict__ token_row,
+                                                      const float* __restrict__ gates, int T,
+                                                      int topk, int H, __nv_bfloat16* __restrict__ out,
+                                                      int64_t ldo) {
+  const int vec = H >> 3;
+  const int64_t total = (int64_t)T * vec;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / vec);
+    const int c = (int)(i % vec) * 8;
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int j = 0; j < topk; ++j) {
+      const int r = token_row[(int64_t)t * topk + j];
+      const float g = gates[(int64_t)t * topk + j];
+      float f[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(y + (int64_t)r * ldy + c), f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = fmaf(g, f[q], acc[q]);
+    }
+    uint32_t pk[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+      pk[q] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(out + (int64_t)t * ldo + c) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
+}
+
+}  // namespace quads
+
+using namespace quads;
+
+extern "C" quads_status_t quads_moe_route(const float* logits, int32_t tokens, int32_t num_experts,
+                                          int32_t topk, int32_t* topk_idx, float* gates,
+                                          int32_t* expert_counts, int32_t* expert_offsets,
+                                          int32_t* row_token, int32_t* token_row,
+                                          int64_t rows_capacity, void* stream) {
+  if (!logits || !topk_idx || !gates || !expert_counts || !expert_offsets || !row_token || !token_row)
+    return fail(QUADS_ERR_INVALID_ARG, "moe_route: null pointer argument");
+  if (tokens < 0 || num_experts < 1 || num_experts > kMaxExperts || topk < 1 ||
+      topk > kMaxTopk || topk > num_experts)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "moe_route: need 1<=experts<=256, 1<=topk<=min(16, experts)");
+  if (rows_capacity < (int64_t)tokens * topk + (int64_t)num_experts * (QUADS_MOE_ROW_ALIGN - 1))
+    return fail(QUADS_ERR_INVALID_ARG, "moe_route: rows_capacity too small");
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaMemsetAsync(expert_counts, 0, (size_t)num_experts * 4, st);
+  if (tokens > 0)
+    route_kernel<<<(tokens * 32 + 255) / 256, 256, 0, st>>>(logits, tokens, num_experts, topk,
+                                                             topk_idx, gates, expert_counts);
+  plan_kernel<<<1, kMaxExperts, 0, st>>>(expert_counts, num_experts, expert_offsets);
+  assign_kernel<<<num_experts, 1024, 0, st>>>(topk_idx, tokens, topk, expert_offsets,
+                                              expert_counts, row_token, token_row);
+  return check_launch("moe_route");
+}
+
+extern "C" quads_status_t quads_moe_gather(const int32_t* row_token, const int32_t* expert_offsets,
+                                           int32_t num_experts, int64_t rows_capacity,
+                                           int64_t cols, const uint8_t* in_codes,
+                                           const uint8_t* in_scales, uint8_t* out_codes,
+                                           uint8_t* out_scales, void* stream) {
+  if (!row_token || !expert_offsets || !in_codes || !in_scales || !out_codes || !out_scales)
+    return fail(QUADS_ERR_INVALID_ARG, "moe_gather: null pointer argument");
+  if (cols <= 0 || cols % 64 || rows_capacity % 128)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "moe_gather: cols %% 64 and rows_capacity %% 128");
+  if (((uintptr_t)in_codes | (uintptr_t)out_codes) & 15u || ((uintptr_t)in_scales | (uintptr_t)out_scales) & 3u)
+    return fail(QUADS_ERR_MISALIGNED, "moe_gather: alignment");
+  cudaStream_t st = (cudaStream_t)stream;
+  const int blocks = (int)std::min<int64_t>((rows_capacity * 32 + 255) / 256, (int64_t)num_sms() * 16);
+  gather_kernel<<<blocks, 256, 0, st>>>(row_token, expert_offsets, num_experts, rows_capacity,
+                                        (int)cols, in_codes, in_scales, out_codes, out_scales);
+  return check_launch("moe_gather");
+}
+
+extern "C" quads_status_t quads_moe_combine(const void* y, int64_t ldy, const int32_t* token_row,
+                                            const float* gates, int32_t tokens, int32_t topk,
+                                            int64_t hidden, void* out, int64_t ldo, void* stream) {
+  if (!y || !token_row || !gates || !out) return fail(QUADS_ERR_INVALID_ARG, "moe_combine: null pointer");
+  if (hidden <= 0 || hidden % 8 || ldy % 8 || ldo % 8 || ldy < hidden || ldo < hidden)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "moe_combine: hidden/ld must be multiples of 8");
+  if (tokens == 0) return QUADS_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t work = (int64_t)tokens * (hidden / 8);
+  const int blocks = (int)std::min<int64_t>((work + 255) / 256, (int64_t)num_sms() * 8);
+  combine_kernel<<<blocks, 256, 0, st>>>((const __nv_bfloat16*)y, ldy, token_row, gates, tokens,
+                                         topk, (int)hidden, (__nv_bfloat16*)out, ldo);
+  return check_launch("moe_combine");
+}

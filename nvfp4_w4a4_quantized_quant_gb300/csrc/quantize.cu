@@ -1,0 +1,546 @@
+// Activation-side kernels: tensor amax, NVFP4 RTN quantization with fused
+// residual-energy partials, top-k residual channel selection, the second
+// quantization of the residual slice, and TRACE rollout-guided rounding.
+//
+// [TRACE digest] "NVFP4 与 E2M1 码本": per-tensor scale + per-block scale, RTN.
+// [QUADS technical summary] 2.1: Delta X_q = X - DQ(Q(X)); 2.2 B "Mechanism":
+// second-pass quantization of the channels with the largest FP4 error;
+// "Implementation": a channel mask picks the top channels by residual magnitude.
+// [TRACE digest] "核心方法", Eq. (3): q_TRACE = argmin_{q in {q-, q+}} |q - q_rollout|.
+//
+// All of these are HBM-bound: 16-byte vector loads (8 bf16 per lane), warp
+// shuffles for the 16-element block maximum, no shared-memory staging needed
+// because every byte is read once and used in registers.
+#include <cstdio>
+
+#include "common.cuh"
+
+namespace quads {
+
+static __device__ int g_quant_error;  // device-side argument check failures
+
+// ---------------------------------------------------------------- amax
+// One block per 32-row chunk (inside one group), threads over (row, 8-col vector).
+__global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restrict__ x,
+                                                   int64_t rows, int cols, int64_t ldx,
+                                                   const int32_t* __restrict__ row_index,
+                                                   const int32_t* __restrict__ goff, int G,
+                                                   uint32_t* __restrict__ amax_bits) {
+  const int64_t end = goff ? (int64_t)goff[G] : rows;
+  const int vec_per_row = cols >> 3;
+  const int64_t nchunks = (end + kScoreChunk - 1) / kScoreChunk;
+  __shared__ float red[8];
+  for (int64_t chunk = blockIdx.x; chunk < nchunks; chunk += gridDim.x) {
+    const int64_t r0 = chunk * kScoreChunk;
+    const int64_t r1 = min(r0 + kScoreChunk, end);
+    const int g = goff ? group_of(goff, G, r0) : 0;
+    if (goff && r1 > goff[g + 1]) atomicExch(&g_quant_error, QUADS_ERR_DEVICE_CHECK);
+    float m = 0.0f;
+    const int total = (int)(r1 - r0) * vec_per_row;
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+      const int64_t r = r0 + i / vec_per_row;
+      const int v = i % vec_per_row;
+      const int64_t src = row_index ? (int64_t)row_index[r] : r;
+      uint4 u = __ldg(reinterpret_cast<const uint4*>(x + src * ldx) + v);
+      float f[8];
+      bf16x8_to_f32(u, f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
+    }
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+      v = warp_max(v);
+      if (threadIdx.x == 0 && v > 0.0f) atomicMax(&amax_bits[g], __float_as_uint(v));
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void tensor_scale_kernel(const uint32_t* __restrict__ amax_bits, int G,
+                                    float* __restrict__ st_out) {
+  for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < G; g += gridDim.x * blockDim.x)
+    st_out[g] = tensor_scale_from_amax(__uint_as_float(amax_bits[g]));
+}
+
+// ---------------------------------------------------------------- quantize
+// A warp owns one (32-row chunk, 256-column slab) task: lane l holds columns
+// slab*256 + 8l .. +7 and walks the chunk's rows in order, so the residual
+// energy of its 8 columns is summed row by row in float32 (the fixed order the
+// score definition uses).  Lanes 2i and 2i+1 form one 16-element block.
+template <bool kScores>
+__global__ void __launch_bounds__(256) quantize_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
+    const int32_t* __restrict__ row_index, const int32_t* __restrict__ goff, int G,
+    const float* __restrict__ st, uint8_t* __restrict__ codes, int64_t ldc,
+    uint8_t* __restrict__ scales, int layout, float* __restrict__ partials) {
+  const int lane = threadIdx.x & 31;
+  const int64_t end = goff ? (int64_t)goff[G] : rows;
+  const int nslab = (cols + 255) >> 8;
+  const int64_t nchunks = (end + kScoreChunk - 1) / kScoreChunk;
+  const int64_t ntasks = nchunks * nslab;
+  const int ncols16 = cols >> 4;
+  const int64_t warp_global = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t task = warp_global; task < ntasks; task += nwarps) {
+    const int64_t chunk = task / nslab;
+    const int slab = (int)(task % nslab);
+    const int col = slab * 256 + lane * 8;
+    const bool active = col < cols;
+    const int64_t r0 = chunk * kScoreChunk;
+    const int64_t r1 = min(r0 + kScoreChunk, end);
+    int g = goff ? group_of(goff, G, r0) : 0;
+    int64_t gend = goff ? (int64_t)goff[g + 1] : end;
+    float s_t = st[g];
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int64_t r = r0; r < r1; r += 4) {
+      uint4 u[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        u[q] = make_uint4(0, 0, 0, 0);
+        if (active && r + q < r1) {
+          const int64_t src = row_index ? (int64_t)row_index[r + q] : r + q;
+          u[q] = __ldg(reinterpret_cast<const uint4*>(x + src * ldx + col));
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int64_t row = r + q;
+        if (row >= r1) break;
+        while (row >= gend) {  // (score mode: never; chunks do not straddle groups)
+          ++g;
+          gend = goff[g + 1];
+          s_t = st[g];
+        }
+        float f[8];
+        bf16x8_to_f32(u[q], f);
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        const BlockScale bs = block_scale(m, s_t);
+        const uint32_t c = quantize8(f, bs);
+        if (active) {
+          *reinterpret_cast<uint32_t*>(codes + row * ldc + (col >> 1)) = c;
+          if ((lane & 1) == 0) scales[sf_offset(layout, row, col >> 4, ncols16)] = (uint8_t)bs.byte;
+        }
+        if (kScores) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float dq = __fmul_rn(e2m1_to_f32((c >> (4 * j)) & 15u), bs.d);
+            const float R = __fsub_rn(f[j], dq);
+            acc[j] = __fadd_rn(acc[j], __fmul_rn(R, R));
+          }
+        }
+      }
+    }
+    if (kScores && active) {
+      float4* p = reinterpret_cast<float4*>(partials + chunk * cols + col);
+      p[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      p[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- select
+// One block per group: scores = ordered sum of the group's chunk partials;
+// bitonic sort of (score, ~index) keys descending; mark the top k; compact
+// the marked channels in ascending order.
+__global__ void __launch_bounds__(1024) select_kernel(const float* __restrict__ partials,
+                                                      int cols, const int32_t* __restrict__ goff,
+                                                      int G, int64_t rows, int k,
+                                                      int32_t* __restrict__ sel,
+                                                      float* __restrict__ scores_out) {
+  extern __shared__ unsigned long long keys[];  // [npow2]
+  __shared__ int warp_sums[32];
+  const int g = blockIdx.x;
+  const int64_t a = goff ? (int64_t)goff[g] : 0;
+  const int64_t b = goff ? (int64_t)goff[g + 1] : rows;
+  int npow2 = 1;
+  while (npow2 < cols) npow2 <<= 1;
+  const int64_t c0 = a / kScoreChunk;
+  const int64_t c1 = (b + kScoreChunk - 1) / kScoreChunk;
+  for (int c = threadIdx.x; c < npow2; c += blockDim.x) {
+    unsigned long long key = 0ull;
+    if (c < cols) {
+      float s = 0.0f;
+      for (int64_t ch = c0; ch < c1; ++ch) s = __fadd_rn(s, partials[ch * cols + c]);
+      if (scores_out) scores_out[(int64_t)g * cols + c] = s;
+      key = ((unsigned long long)__float_as_uint(s) << 32) | (0xFFFFFFFFu - (uint32_t)c);
+    }
+    keys[c] = key;
+  }
+  __syncthreads();
+  for (int size = 2; size <= npow2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < npow2; i += blockDim.x) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool desc = (i & size) == 0;
+          const unsigned long long ki = keys[i], kj = keys[j];
+          if (desc ? (ki < kj) : (ki > kj)) { keys[i] = kj; keys[j] = ki; }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // keys[0..k) are the top k; turn them into a mask over channels, reusing keys[] storage
+  // after reading: first collect the indices into registers via a second pass.
+  __shared__ int mask_words[256];  // cols <= 8192 -> 256 x 32 bits
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) mask_words[i] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < k; i += blockDim.x) {
+    const uint32_t c = 0xFFFFFFFFu - (uint32_t)(keys[i] & 0xFFFFFFFFull);
+    atomicOr(&mask_words[c >> 5], 1 << (c & 31));
+  }
+  __syncthreads();
+  // ordered compaction: exclusive prefix of popcounts over the 256 words
+  const int nwords = (cols + 31) >> 5;
+  int cnt = 0;
+  if (threadIdx.x < nwords) cnt = __popc(mask_words[threadIdx.x]);
+  // block exclusive scan over threads 0..nwords-1 (nwords <= 256)
+  int v = cnt;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  if (lane == 31) warp_sums[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    int s = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int t = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += t;
+    }
+    warp_sums[lane] = s;
+  }
+  __syncthreads();
+  int base = v - cnt + (w > 0 ? warp_sums[w - 1] : 0);
+  if (threadIdx.x < nwords) {
+    uint32_t word = (uint32_t)mask_words[threadIdx.x];
+    while (word) {
+      const int bit = __ffs(word) - 1;
+      word &= word - 1;
+      sel[(int64_t)g * k + base++] = threadIdx.x * 32 + bit;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- residual slice
+// R[:, sel] recomputed from x and the stored block scales; one block per 32-row
+// chunk (one group), per-group amax of |R| by atomicMax on the float bits.
+__global__ void __launch_bounds__(256) rsel_residual_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
+    const int32_t* __restrict__ goff, int G, const uint8_t* __restrict__ scales, int layout,
+    const float* __restrict__ st, const int32_t* __restrict__ sel, int k,
+    float* __restrict__ rs, uint32_t* __restrict__ amax_bits) {
+  __shared__ float red[8];
+  const int64_t end = goff ? (int64_t)goff[G] : rows;
+  const int64_t nchunks = (end + kScoreChunk - 1) / kScoreChunk;
+  const int ncols16 = cols >> 4;
+  for (int64_t chunk = blockIdx.x; chunk < nchunks; chunk += gridDim.x) {
+    const int64_t r0 = chunk * kScoreChunk, r1 = min(r0 + kScoreChunk, end);
+    const int g = goff ? group_of(goff, G, r0) : 0;
+    const float s_t = st[g];
+    const int32_t* sg = sel + (int64_t)g * k;
+    float m = 0.0f;
+    const int total = (int)(r1 - r0) * k;
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+      const int64_t r = r0 + i / k;
+      const int j = i % k;
+      const int c = sg[j];
+      const float xv = __bfloat162float(x[r * ldx + c]);
+      const BlockScale bs = block_scale_from_byte(scales[sf_offset(layout, r, c >> 4, ncols16)], s_t);
+      float v[8] = {__fmul_rn(xv, bs.r), 0, 0, 0, 0, 0, 0, 0};
+      const uint32_t code = bs.zero ? 0u : (f32x8_to_e2m1(v) & 15u);
+      const float R = __fsub_rn(xv, __fmul_rn(e2m1_to_f32(code), bs.d));
+      rs[r * k + j] = R;
+      m = fmaxf(m, fabsf(R));
+    }
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+      v = warp_max(v);
+      if (threadIdx.x == 0 && v > 0.0f) atomicMax(&amax_bits[g], __float_as_uint(v));
+    }
+    __syncthreads();
+  }
+}
+
+// Quantize the float32 residual slice [rows, k] (16-blocks along the selection)
+// into codes [rows, kpad/2] and scales (kpad columns, padding blocks 0).
+// One thread per 8 elements; lanes 2i/2i+1 share a block.
+__global__ void __launch_bounds__(256) rsel_quantize_kernel(
+    const float* __restrict__ rs, int64_t rows, int k, int kpad, const int32_t* __restrict__ goff,
+    int G, const uint32_t* __restrict__ amax_bits, uint8_t* __restrict__ rcodes,
+    uint8_t* __restrict__ rscales, int layout, float* __restrict__ rst) {
+  const int64_t end = goff ? (int64_t)goff[G] : rows;
+  const int vec_per_row = kpad >> 3;  // even
+  const int64_t total = rows * vec_per_row;  // padding rows (>= end) get zeros
+  const int ncols16 = kpad >> 4;
+  if (blockIdx.x == 0)
+    for (int g = threadIdx.x; g < G; g += blockDim.x)
+      rst[g] = tensor_scale_from_amax(__uint_as_float(amax_bits[g]));
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+       i < ((total + 31) / 32) * 32; i += (int64_t)gridDim.x * blockDim.x) {
+    const bool in = i < total;
+    const int64_t r = in ? i / vec_per_row : 0;
+    const int col = in ? (int)(i % vec_per_row) * 8 : 0;
+    float f[8];
+    const bool live = in && r < end && col < k;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[j] = 0.0f;
+    float s_t = 1.0f;
+    if (live) {
+      const float4* p = reinterpret_cast<const float4*>(rs + r * k + col);
+      const float4 a = p[0], b = p[1];
+      f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+      f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+      const int g = goff ? group_of(goff, G, r) : 0;
+      s_t = tensor_scale_from_amax(__uint_as_float(amax_bits[g]));
+    }
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    const BlockScale bs = block_scale(m, s_t);
+    uint32_t c = quantize8(f, bs);
+    uint32_t sb = bs.byte;
+    if (!live) { c = 0u; sb = 0u; }
+    if (in) {
+      *reinterpret_cast<uint32_t*>(rcodes + r * (kpad >> 1) + (col >> 1)) = c;
+      if (((col >> 3) & 1) == 0) rscales[sf_offset(layout, r, col >> 4, ncols16)] = (uint8_t)sb;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- TRACE
+// Signed E2M1 levels ascending, +0 and -0 merged: index 0..14 = -6 .. 6.
+__device__ __forceinline__ int signed_level_index(float q) {
+  const float a = fabsf(q);
+  // magnitude index 0..7 of an exact level
+  int mi = a == 0.f ? 0 : a == 0.5f ? 1 : a == 1.f ? 2 : a == 1.5f ? 3 : a == 2.f ? 4
+         : a == 3.f ? 5 : a == 4.f ? 6 : 7;
+  return q < 0.f ? 7 - mi : 7 + mi;
+}
+
+__device__ __forceinline__ float level_of_index(int i) {
+  const int mi = i >= 7 ? i - 7 : 7 - i;
+  const float mag = e2m1_to_f32((uint32_t)mi);
+  return i < 7 ? -mag : mag;
+}
+
+__global__ void __launch_bounds__(256) trace_kernel(
+    const __nv_bfloat16* __restrict__ xt, int64_t rows, int cols, int64_t ldx,
+    const uint8_t* __restrict__ rcodes, int64_t ldc, const uint8_t* __restrict__ rscales,
+    const float* __restrict__ rst, uint8_t* __restrict__ out,
+    unsigned long long* __restrict__ counters) {
+  const int vec_per_row = cols >> 3;
+  const int64_t total = rows * vec_per_row;
+  const float s_t = rst[0];
+  unsigned int n_rtn = 0, n_tr = 0, n_adj = 0;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / vec_per_row;
+    const int col = (int)(i % vec_per_row) * 8;
+    float f[8];
+    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(xt + r * ldx + col)), f);
+    const uint32_t rc = *reinterpret_cast<const uint32_t*>(rcodes + r * ldc + (col >> 1));
+    const BlockScale bs = block_scale_from_byte(rscales[r * (cols >> 4) + (col >> 4)], s_t);
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = bs.zero ? 0.0f : __fmul_rn(f[j], bs.r);
+    const uint32_t rtn = bs.zero ? 0u : f32x8_to_e2m1(v);
+    uint32_t outw = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float qr = e2m1_to_f32((rc >> (4 * j)) & 15u);
+      const float qn = e2m1_to_f32((rtn >> (4 * j)) & 15u);
+      uint32_t code;
+      float qt;
+      if (bs.zero) {
+        code = 0u;
+        qt = 0.0f;
+      } else {
+        // neighbours of v: the RTN level is one of them; the other is the next
+        // level on the far side of v (or the same when v is a level / clamped)
+        const float vc = fminf(fmaxf(v[j], -6.0f), 6.0f);
+        const int in_ = signed_level_index(qn);
+        int ilo = in_, ihi = in_;
+        if (qn > vc) ilo = in_ - 1;
+        else if (qn < vc) ihi = in_ + 1;
+        const float qlo = level_of_index(ilo), qhi = level_of_index(ihi);
+        qt = fabsf(qlo - qr) <= fabsf(qhi - qr) ? qlo : qhi;
+        const uint32_t mag = (uint32_t)(signed_level_index(fabsf(qt)) - 7);
+        const bool neg = qt < 0.0f || (qt == 0.0f && signbit(v[j]));
+        code = mag | (neg ? 8u : 0u);
+      }
+      outw |= code << (4 * j);
+      if (qn != qr) {
+        ++n_rtn;
+        if (abs(signed_level_index(qn) - signed_level_index(qr)) == 1) ++n_adj;
+      }
+      if (qt != qr) ++n_tr;
+    }
+    *reinterpret_cast<uint32_t*>(out + r * ldc + (col >> 1)) = outw;
+  }
+  if (counters) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      n_rtn += __shfl_xor_sync(0xffffffffu, n_rtn, o);
+      n_tr += __shfl_xor_sync(0xffffffffu, n_tr, o);
+      n_adj += __shfl_xor_sync(0xffffffffu, n_adj, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+      if (n_rtn) atomicAdd(&counters[0], (unsigned long long)n_rtn);
+      if (n_tr) atomicAdd(&counters[1], (unsigned long long)n_tr);
+      if (n_adj) atomicAdd(&counters[2], (unsigned long long)n_adj);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- host side
+static int grid_for(int64_t work_items, int per_block, int max_blocks_per_sm = 8) {
+  int64_t b = (work_items + per_block - 1) / per_block;
+  int64_t cap = (int64_t)num_sms() * max_blocks_per_sm;
+  if (b > cap) b = cap;
+  if (b < 1) b = 1;
+  return (int)b;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int read_quant_device_error(cudaStream_t) {
+  int v = 0;
+  cudaMemcpyFromSymbol(&v, g_quant_error, sizeof(int));
+  int zero = 0;
+  cudaMemcpyToSymbol(g_quant_error, &zero, sizeof(int));
+  return v;
+}
+
+}  // namespace quads
+
+using namespace quads;
+
+extern "C" quads_status_t quads_quantize_nvfp4(
+    const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* row_index,
+    const int32_t* group_offsets, int32_t num_groups, const float* tensor_scale_in,
+    uint8_t* codes, int64_t ld_codes, uint8_t* scales, int32_t scale_layout,
+    float* tensor_scale_out, float* score_partials, void* workspace, size_t workspace_bytes,
+    void* stream) {
+  if (!x || !codes || !scales || !tensor_scale_out)
+    return fail(QUADS_ERR_INVALID_ARG, "quantize: null x/codes/scales/tensor_scale_out");
+  if (rows < 0 || cols <= 0 || cols % 16)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "quantize: cols=%lld must be a positive multiple of 16", (long long)cols);
+  if (scale_layout == QUADS_SCALES_TCGEN05 && cols % 64)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "quantize: TCGEN05 scale layout needs cols %% 64 == 0");
+  if (scale_layout != QUADS_SCALES_LINEAR && scale_layout != QUADS_SCALES_TCGEN05)
+    return fail(QUADS_ERR_INVALID_ARG, "quantize: bad scale_layout %d", scale_layout);
+  if (ldx < cols || ldx % 8 || ld_codes < cols / 2 || ld_codes % 16)
+    return fail(QUADS_ERR_MISALIGNED, "quantize: ldx=%lld (>=cols, %%8) ld_codes=%lld (>=cols/2, %%16)", (long long)ldx, (long long)ld_codes);
+  if (!aligned16(x) || !aligned16(codes) || (score_partials && !aligned16(score_partials)))
+    return fail(QUADS_ERR_MISALIGNED, "quantize: x/codes/score_partials must be 16-byte aligned");
+  const int G = group_offsets ? num_groups : 1;
+  if (group_offsets && num_groups < 1) return fail(QUADS_ERR_INVALID_ARG, "quantize: num_groups < 1");
+  if (!tensor_scale_in && (workspace_bytes < (size_t)G * 4 || !workspace))
+    return fail(QUADS_ERR_WORKSPACE, "quantize: workspace needs %d bytes", G * 4);
+  if (rows == 0) return QUADS_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const float* stp = tensor_scale_in;
+  if (!tensor_scale_in) {
+    uint32_t* amax = (uint32_t*)workspace;
+    cudaMemsetAsync(amax, 0, (size_t)G * 4, st);
+    amax_kernel<<<grid_for((rows + 31) / 32, 1, 16), 256, 0, st>>>(
+        (const __nv_bfloat16*)x, rows, (int)cols, ldx, row_index, group_offsets, G, amax);
+    tensor_scale_kernel<<<(G + 255) / 256, 256, 0, st>>>(amax, G, tensor_scale_out);
+    stp = tensor_scale_out;
+  } else if (tensor_scale_in != tensor_scale_out) {
+    cudaMemcpyAsync(tensor_scale_out, tensor_scale_in, (size_t)G * 4, cudaMemcpyDeviceToDevice, st);
+  }
+  if (scale_layout == QUADS_SCALES_TCGEN05 && rows % 128) {
+    // padding rows of the last 128-row block must read as scale 0
+    const int64_t ncols16 = cols / 16;
+    const int64_t start = (rows / 128) * (ncols16 / 4) * 512;
+    cudaMemsetAsync(scales + start, 0, (size_t)(sf_tc_bytes(rows, cols) - start), st);
+  }
+  const int64_t ntasks = ((rows + 31) / 32) * ((cols + 255) / 256);
+  const int blocks = grid_for(ntasks, 8, 8);
+  if (score_partials)
+    quantize_kernel<true><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)x, rows, (int)cols, ldx,
+                                                  row_index, group_offsets, G, stp, codes,
+                                                  ld_codes, scales, scale_layout, score_partials);
+  else
+    quantize_kernel<false><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)x, rows, (int)cols, ldx,
+                                                   row_index, group_offsets, G, stp, codes,
+                                                   ld_codes, scales, scale_layout, nullptr);
+  return check_launch("quantize");
+}
+
+extern "C" quads_status_t quads_select_residual_channels(
+    const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* group_offsets,
+    int32_t num_groups, const uint8_t* scales, int32_t scale_layout, const float* tensor_scale,
+    const float* score_partials, int32_t k, int32_t* sel, float* scores_out, uint8_t* r_codes,
+    uint8_t* r_scales, int32_t r_scale_layout, float* r_tensor_scale, void* workspace,
+    size_t workspace_bytes, void* stream) {
+  if (!x || !scales || !tensor_scale || !score_partials || !sel || !r_codes || !r_scales || !r_tensor_scale)
+    return fail(QUADS_ERR_INVALID_ARG, "select: null pointer argument");
+  if (cols <= 0 || cols % 16 || cols > 8192)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "select: cols=%lld must be a multiple of 16 and <= 8192", (long long)cols);
+  if (k <= 0 || k % 16 || k > cols)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "select: k=%d must be a multiple of 16 in [16, cols]", k);
+  if (ldx < cols) return fail(QUADS_ERR_MISALIGNED, "select: ldx < cols");
+  const int G = group_offsets ? num_groups : 1;
+  const int kpad = quads_kpad(k);
+  const size_t need = quads_workspace_size(QUADS_OP_SELECT, rows, cols, 0, k, G);
+  if (!workspace || workspace_bytes < need)
+    return fail(QUADS_ERR_WORKSPACE, "select: workspace needs %zu bytes", need);
+  if (rows == 0) return QUADS_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  int npow2 = 1;
+  while (npow2 < cols) npow2 <<= 1;
+  const size_t smem = (size_t)npow2 * 8;
+  if (smem > 48 * 1024)
+    cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  select_kernel<<<G, 1024, smem, st>>>(score_partials, (int)cols, group_offsets, G, rows, k, sel,
+                                       scores_out);
+  float* rs = (float*)workspace;
+  uint32_t* amax = (uint32_t*)((char*)workspace + (((size_t)rows * k * 4 + 255) & ~(size_t)255));
+  cudaMemsetAsync(amax, 0, (size_t)G * 4, st);
+  rsel_residual_kernel<<<grid_for((rows + 31) / 32, 1, 16), 256, 0, st>>>(
+      (const __nv_bfloat16*)x, rows, (int)cols, ldx, group_offsets, G, scales, scale_layout,
+      tensor_scale, sel, k, rs, amax);
+  if (r_scale_layout == QUADS_SCALES_TCGEN05 && rows % 128) {
+    const int64_t start = (rows / 128) * (kpad / 64) * 512;
+    cudaMemsetAsync(r_scales + start, 0, (size_t)(sf_tc_bytes(rows, kpad) - start), st);
+  }
+  rsel_quantize_kernel<<<grid_for(rows * (kpad / 8), 256), 256, 0, st>>>(
+      rs, rows, k, kpad, group_offsets, G, amax, r_codes, r_scales, r_scale_layout, r_tensor_scale);
+  return check_launch("select");
+}
+
+extern "C" quads_status_t quads_trace_round(const void* x_train, int64_t rows, int64_t cols,
+                                            int64_t ldx, const uint8_t* rollout_codes,
+                                            int64_t ld_codes, const uint8_t* rollout_scales,
+                                            const float* rollout_tensor_scale, uint8_t* codes_out,
+                                            unsigned long long* counters, void* stream) {
+  if (!x_train || !rollout_codes || !rollout_scales || !rollout_tensor_scale || !codes_out)
+    return fail(QUADS_ERR_INVALID_ARG, "trace_round: null pointer argument");
+  if (cols <= 0 || cols % 16) return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "trace_round: cols %% 16");
+  if (ldx < cols || ldx % 8 || ld_codes < cols / 2 || ld_codes % 4 || !aligned16(x_train))
+    return fail(QUADS_ERR_MISALIGNED, "trace_round: leading dimensions / alignment");
+  if (rows == 0) return QUADS_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  trace_kernel<<<grid_for(rows * (cols / 8), 256), 256, 0, st>>>(
+      (const __nv_bfloat16*)x_train, rows, (int)cols, ldx, rollout_codes, ld_codes,
+      rollout_scales, rollout_tensor_scale, codes_out, counters);
+  return check_launch("trace_round");
+}

@@ -1,0 +1,144 @@
+"""The two rollout-side layers built from libquads calls, with every buffer
+allocated once so a forward pass only enqueues kernels (and can be captured
+in a CUDA graph).
+
+CompensatedLinear   Y = Q(X) Q(W)^T + Q(R_sel) Q(W_sel)^T
+MoEExpertLayer      route -> quantize X (+select) -> gather -> grouped GEMM1
+                    (+SwiGLU) -> quantize h per expert (+select) -> grouped
+                    GEMM2 -> combine
+
+[QUADS technical summary] 2.2 B "Residual Activation Compensation (Rollout
+Side)"; [TRACE digest] "MoE 专家路由敏感性".
+"""
+from __future__ import annotations
+
+import torch
+
+from . import quads as Q
+
+
+class CompensatedLinear:
+    """One compensated W4A4 projection with pre-quantized weights (weights are
+    quantized once, as after a weight sync; activations every call)."""
+
+    def __init__(self, w: torch.Tensor, k: int, max_rows: int, out_dtype=torch.bfloat16,
+                 compensate: bool = True):
+        self.N, self.K = w.shape
+        self.k, self.compensate = k, compensate
+        dev = w.device
+        self.wq, _ = Q.quantize_nvfp4(w, scale_layout=Q.TCGEN05)
+        self.max_rows = max_rows
+        kp = Q.kpad(k)
+        self.bufs = dict(
+            codes=torch.empty((max_rows, self.K // 2), dtype=torch.uint8, device=dev),
+            scales=torch.empty(Q.sf_tc_bytes(max_rows, self.K), dtype=torch.uint8, device=dev),
+            ts=torch.empty(1, dtype=torch.float32, device=dev),
+            part=torch.empty(((max_rows + 31) // 32, self.K), dtype=torch.float32, device=dev),
+            sel=torch.empty((1, k), dtype=torch.int32, device=dev),
+            rc=torch.empty((max_rows, kp // 2), dtype=torch.uint8, device=dev),
+            rs=torch.empty(Q.sf_tc_bytes(max_rows, kp), dtype=torch.uint8, device=dev),
+            rts=torch.empty(1, dtype=torch.float32, device=dev),
+            y=torch.empty((max_rows, self.N), dtype=out_dtype, device=dev),
+        )
+        self.ws_q = torch.empty(Q.workspace_size(Q.OP_QUANTIZE, max_rows, self.K), dtype=torch.uint8,
+                                device=dev)
+        self.ws_s = torch.empty(Q.workspace_size(Q.OP_SELECT, max_rows, self.K, 0, k),
+                                dtype=torch.uint8, device=dev)
+        self.ws_g = torch.empty(Q.workspace_size(Q.OP_GEMM, 0, self.K, self.N, k), dtype=torch.uint8,
+                                device=dev)
+
+    def forward(self, x: torch.Tensor, stream=None) -> torch.Tensor:
+        b = self.bufs
+        M = x.shape[0]
+        assert M <= self.max_rows
+        xq, part = Q.quantize_nvfp4(x, scale_layout=Q.TCGEN05, scores=self.compensate,
+                                    workspace=self.ws_q, stream=stream,
+                                    out=(b["codes"][:M], b["scales"], b["ts"],
+                                         b["part"][: (M + 31) // 32] if self.compensate else None))
+        y = b["y"][:M]
+        if not self.compensate:
+            return Q.w4a4_gemm_comp(xq, self.wq, out=y, stream=stream)
+        sel, _, r = Q.select_residual_channels(x, xq, part, self.k, r_scale_layout=Q.TCGEN05,
+                                               workspace=self.ws_s, stream=stream,
+                                               out=(b["sel"], b["rc"][:M], b["rs"], b["rts"]))
+        return Q.w4a4_gemm_comp(xq, self.wq, r, sel, self.k, out=y, workspace=self.ws_g,
+                                stream=stream)
+
+
+class MoEExpertLayer:
+    """Routed expert FFN (gate+up, SwiGLU, down) with NVFP4 W4A4 GEMMs and
+    residual compensation on both GEMMs."""
+
+    def __init__(self, w1: torch.Tensor, w2: torch.Tensor, topk: int, k1: int, k2: int,
+                 max_tokens: int, compensate: bool = True):
+        self.E, twoF, self.H = w1.shape
+        self.F = twoF // 2
+        assert w2.shape == (self.E, self.H, self.F)
+        self.topk, self.k1, self.k2, self.compensate = topk, k1, k2, compensate
+        dev = w1.device
+        self.w1q = Q.quantize_expert_weights(w1, swiglu_interleave=True)
+        self.w2q = Q.quantize_expert_weights(w2)
+        T, E, H, F = max_tokens, self.E, self.H, self.F
+        cap = Q.moe_rows_capacity(T, topk, E)
+        self.cap, self.max_tokens = cap, T
+        kp1, kp2 = Q.kpad(k1), Q.kpad(k2)
+        u8, f32, i32 = torch.uint8, torch.float32, torch.int32
+        e = lambda *s, dt=u8: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
+        self.b = dict(
+            route=dict(idx=e((T, topk), dt=i32), gates=e((T, topk), dt=f32), counts=e(E, dt=i32),
+                       offsets=e(E + 1, dt=i32), row_token=e(cap, dt=i32),
+                       token_row=e((T, topk), dt=i32)),
+            xc=e((T, H // 2)), xs=e(T * (H // 16)), xts=e(1, dt=f32), xpart=e(((T + 31) // 32, H), dt=f32),
+            sel1=e((1, k1), dt=i32), r1c=e((T, kp1 // 2)), r1s=e(T * (kp1 // 16)), r1ts=e(1, dt=f32),
+            a1c=e((cap, H // 2)), a1s=e(Q.sf_tc_bytes(cap, H)),
+            g1c=e((cap, kp1 // 2)), g1s=e(Q.sf_tc_bytes(cap, kp1)),
+            h=e((cap, F), dt=torch.bfloat16),
+            hc=e((cap, F // 2)), hs=e(Q.sf_tc_bytes(cap, F)), hts=e(E, dt=f32),
+            hpart=e((cap // 32, F), dt=f32),
+            sel2=e((E, k2), dt=i32), r2c=e((cap, kp2 // 2)), r2s=e(Q.sf_tc_bytes(cap, kp2)),
+            r2ts=e(E, dt=f32),
+            y=e((cap, H), dt=torch.bfloat16), out=e((T, H), dt=torch.bfloat16),
+        )
+        self.ws = dict(
+            q1=e(Q.workspace_size(Q.OP_QUANTIZE, T, H)),
+            s1=e(Q.workspace_size(Q.OP_SELECT, T, H, 0, k1)),
+            g1=e(Q.workspace_size(Q.OP_MOE_GEMM, 0, H, 2 * F, k1, E)),
+            q2=e(Q.workspace_size(Q.OP_QUANTIZE, cap, F, 0, 0, E)),
+            s2=e(Q.workspace_size(Q.OP_SELECT, cap, F, 0, k2, E)),
+            g2=e(Q.workspace_size(Q.OP_MOE_GEMM, 0, F, H, k2, E)),
+        )
+
+    def forward(self, x: torch.Tensor, logits: torch.Tensor, stream=None) -> dict:
+        b, ws, T = self.b, self.ws, x.shape[0]
+        assert T == self.max_tokens, "buffers are sized for a fixed token count"
+        E, H, F = self.E, self.H, self.F
+        comp = self.compensate
+        plan = Q.moe_route(logits, self.topk, rows_capacity=self.cap, out=b["route"], stream=stream)
+        xq, xpart = Q.quantize_nvfp4(x, scores=comp, workspace=ws["q1"], stream=stream,
+                                     out=(b["xc"], b["xs"], b["xts"], b["xpart"] if comp else None))
+        a1 = Q.moe_gather(plan, xq, out=(b["a1c"], b["a1s"]), stream=stream)
+        r1 = sel1 = None
+        if comp:
+            sel1, _, xr = Q.select_residual_channels(x, xq, xpart, self.k1, workspace=ws["s1"],
+                                                     stream=stream,
+                                                     out=(b["sel1"], b["r1c"], b["r1s"], b["r1ts"]))
+            r1 = Q.moe_gather(plan, xr, out=(b["g1c"], b["g1s"]), stream=stream)
+        h = Q.moe_grouped_gemm(plan, a1, self.w1q, E, 2 * F, r1, sel1, self.k1,
+                               epilogue=Q.EPI_SWIGLU, workspace=ws["g1"], out=b["h"], stream=stream)
+        hq, hpart = Q.quantize_nvfp4(h, group_offsets=plan["offsets"], num_groups=E,
+                                     scale_layout=Q.TCGEN05, scores=comp, rows=self.cap,
+                                     workspace=ws["q2"], stream=stream,
+                                     out=(b["hc"], b["hs"], b["hts"], b["hpart"] if comp else None))
+        r2 = sel2 = None
+        if comp:
+            sel2, _, r2 = Q.select_residual_channels(h, hq, hpart, self.k2,
+                                                     group_offsets=plan["offsets"], num_groups=E,
+                                                     r_scale_layout=Q.TCGEN05, workspace=ws["s2"],
+                                                     stream=stream,
+                                                     out=(b["sel2"], b["r2c"], b["r2s"], b["r2ts"]))
+        y = Q.moe_grouped_gemm(plan, hq, self.w2q, E, H, r2, sel2, self.k2,
+                               a_scale_per_expert=True, r_scale_per_expert=True,
+                               sel_per_expert=True, workspace=ws["g2"], out=b["y"], stream=stream)
+        out = Q.moe_combine(y, plan, out=b["out"], stream=stream)
+        return dict(out=out, plan=plan, xq=xq, sel1=sel1, a1=a1, r1=r1, h=h, hq=hq, sel2=sel2,
+                    r2=r2, y=y)

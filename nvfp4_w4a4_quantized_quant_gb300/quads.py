@@ -1,0 +1,327 @@
+"""Thin Python binding of the libquads C ABI (ctypes).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels; PyTorch supplies device memory (output and workspace tensors) and the
+current CUDA stream.  There is no CPU or PyTorch fallback -- if the library is
+not built, or no CUDA device is present, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from .build import LIB, ROOT
+
+LINEAR, TCGEN05 = 0, 1
+OUT_F32, OUT_BF16 = 0, 1
+EPI_NONE, EPI_SWIGLU = 0, 1
+OP_QUANTIZE, OP_SELECT, OP_GEMM, OP_MOE_GEMM = 0, 1, 2, 3
+SCORE_CHUNK_ROWS = 32
+MOE_ROW_ALIGN = 128
+
+_P, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+
+_SIGS = {
+    "quads_version": (ctypes.c_int, []),
+    "quads_status_string": (ctypes.c_char_p, [_I32]),
+    "quads_last_error_detail": (ctypes.c_char_p, []),
+    "quads_device_status": (_I32, [_P, ctypes.POINTER(_I32)]),
+    "quads_workspace_size": (_SZ, [_I32, _I64, _I64, _I64, _I32, _I32]),
+    "quads_kpad": (_I32, [_I32]),
+    "quads_quantize_nvfp4": (_I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _I64, _P, _I32,
+                                    _P, _P, _P, _SZ, _P]),
+    "quads_select_residual_channels": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _I32, _P, _P,
+                                              _I32, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P]),
+    "quads_w4a4_gemm_comp": (_I32, [_I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                    _I32, _P, _I32, _I64, _P, _SZ, _P]),
+    "quads_moe_grouped_gemm": (_I32, [_I32, _I64, _I64, _I64, _P, _P, _P, _P, _P, _I32, _P, _P,
+                                      _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _P, _I32, _I64,
+                                      _P, _SZ, _P]),
+    "quads_trace_round": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _P, _P]),
+    "quads_moe_route": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _I64, _P]),
+    "quads_moe_gather": (_I32, [_P, _P, _I32, _I64, _I64, _P, _P, _P, _P, _P]),
+    "quads_moe_combine": (_I32, [_P, _I64, _P, _P, _I32, _I32, _I64, _P, _I64, _P]),
+}
+
+_lib = None
+
+
+def header_symbols() -> list[str]:
+    """Every function the public header declares."""
+    text = open(os.path.join(ROOT, "include", "quads.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(quads_[a-z0-9_]+)\s*\(", text)))
+
+
+def load(path: str = LIB):
+    """Load libquads.so (no CUDA device needed for loading)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"libquads is not built ({path}); run "
+                               "nvfp4_w4a4_quantized_quant_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = lib
+    return _lib
+
+
+class QuadsError(RuntimeError):
+    pass
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        lib = load()
+        raise QuadsError(f"{what}: {lib.quads_status_string(status).decode()} -- "
+                         f"{lib.quads_last_error_detail().decode()}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise QuadsError("libquads takes device tensors only")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def kpad(k: int) -> int:
+    return int(load().quads_kpad(k))
+
+
+def workspace_size(op, rows=0, cols=0, n=0, k=0, groups=1) -> int:
+    return int(load().quads_workspace_size(op, rows, cols, n, k, groups))
+
+
+def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]):
+    if ws is not None:
+        if ws.numel() < nbytes:
+            raise QuadsError(f"workspace of {ws.numel()} bytes < {nbytes}")
+        return ws
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+
+def sf_tc_bytes(rows: int, cols: int) -> int:
+    return ((rows + 127) // 128) * 128 * (cols // 16)
+
+
+def device_status(stream=None) -> int:
+    code = _I32(0)
+    _check(load().quads_device_status(_stream(stream), ctypes.byref(code)), "device_status")
+    return int(code.value)
+
+
+@dataclass
+class QTensor:
+    """NVFP4 tensor: packed codes [rows, cols/2], scale bytes in `layout`, tensor scales [G]."""
+    codes: torch.Tensor
+    scales: torch.Tensor
+    tensor_scale: torch.Tensor
+    rows: int
+    cols: int
+    layout: int
+
+
+def quantize_nvfp4(x: torch.Tensor, *, group_offsets=None, num_groups: int = 1,
+                   tensor_scale_in=None, scale_layout: int = LINEAR, scores: bool = False,
+                   row_index=None, rows: Optional[int] = None, workspace=None, out=None,
+                   stream=None):
+    """x bf16 [rows, cols] -> (QTensor, score partials [ceil(rows/32), cols] or None)."""
+    lib = load()
+    assert x.dtype == torch.bfloat16 and x.dim() == 2
+    rows = x.shape[0] if rows is None else rows
+    cols = x.shape[1]
+    G = num_groups if group_offsets is not None else 1
+    dev = x.device
+    if out is None:
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+        nsf = sf_tc_bytes(rows, cols) if scale_layout == TCGEN05 else rows * (cols // 16)
+        scales = torch.empty(nsf, dtype=torch.uint8, device=dev)
+        ts = torch.empty(G, dtype=torch.float32, device=dev)
+        part = (torch.empty(((rows + 31) // 32, cols), dtype=torch.float32, device=dev)
+                if scores else None)
+    else:
+        codes, scales, ts, part = out
+    ws = _workspace(workspace_size(OP_QUANTIZE, rows, cols, 0, 0, G), dev, workspace)
+    _check(lib.quads_quantize_nvfp4(_ptr(x), rows, cols, x.stride(0), _ptr(row_index),
+                                    _ptr(group_offsets), G, _ptr(tensor_scale_in), _ptr(codes),
+                                    codes.stride(0), _ptr(scales), scale_layout, _ptr(ts),
+                                    _ptr(part), _ptr(ws), ws.numel(), _stream(stream)),
+           "quantize_nvfp4")
+    return QTensor(codes, scales, ts, rows, cols, scale_layout), part
+
+
+def select_residual_channels(x: torch.Tensor, q: QTensor, partials: torch.Tensor, k: int, *,
+                             group_offsets=None, num_groups: int = 1,
+                             r_scale_layout: int = LINEAR, want_scores: bool = False,
+                             workspace=None, out=None, stream=None):
+    """-> (sel int32 [G, k], scores [G, cols] or None, QTensor of Q(R_sel) [rows, kpad])."""
+    lib = load()
+    G = num_groups if group_offsets is not None else 1
+    rows, cols = q.rows, q.cols
+    kp = kpad(k)
+    dev = x.device
+    if out is None:
+        sel = torch.empty((G, k), dtype=torch.int32, device=dev)
+        rc = torch.empty((rows, kp // 2), dtype=torch.uint8, device=dev)
+        nsf = sf_tc_bytes(rows, kp) if r_scale_layout == TCGEN05 else rows * (kp // 16)
+        rs = torch.empty(nsf, dtype=torch.uint8, device=dev)
+        rts = torch.empty(G, dtype=torch.float32, device=dev)
+    else:
+        sel, rc, rs, rts = out
+    sc = torch.empty((G, cols), dtype=torch.float32, device=dev) if want_scores else None
+    ws = _workspace(workspace_size(OP_SELECT, rows, cols, 0, k, G), dev, workspace)
+    _check(lib.quads_select_residual_channels(
+        _ptr(x), rows, cols, x.stride(0), _ptr(group_offsets), G, _ptr(q.scales), q.layout,
+        _ptr(q.tensor_scale), _ptr(partials), k, _ptr(sel), _ptr(sc), _ptr(rc), _ptr(rs),
+        r_scale_layout, _ptr(rts), _ptr(ws), ws.numel(), _stream(stream)),
+        "select_residual_channels")
+    return sel, sc, QTensor(rc, rs, rts, rows, kp, r_scale_layout)
+
+
+def w4a4_gemm_comp(a: QTensor, w: QTensor, r: Optional[QTensor] = None, sel=None, k: int = 0, *,
+                   out_dtype=torch.bfloat16, workspace=None, out=None, stream=None):
+    """Y [M, N] = Q(A) Q(W)^T (+ Q(R_sel) Q(W_sel)^T when r is given)."""
+    lib = load()
+    M, K, N = a.rows, a.cols, w.rows
+    y = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=a.codes.device)
+    yd = OUT_F32 if y.dtype == torch.float32 else OUT_BF16
+    ws = None
+    if r is not None:
+        ws = _workspace(workspace_size(OP_GEMM, 0, K, N, k, 1), y.device, workspace)
+    _check(lib.quads_w4a4_gemm_comp(
+        M, N, K, _ptr(a.codes), _ptr(a.scales), _ptr(a.tensor_scale), _ptr(w.codes),
+        _ptr(w.scales), _ptr(w.tensor_scale), _ptr(r.codes if r else None),
+        _ptr(r.scales if r else None), _ptr(r.tensor_scale if r else None), _ptr(sel), k,
+        _ptr(y), yd, y.stride(0), _ptr(ws), ws.numel() if ws is not None else 0,
+        _stream(stream)), "w4a4_gemm_comp")
+    return y
+
+
+def moe_grouped_gemm(plan: dict, a: QTensor, w: QTensor, num_experts: int, n: int,
+                     r: Optional[QTensor] = None, sel=None, k: int = 0, *,
+                     a_scale_per_expert: bool = False, r_scale_per_expert: bool = False,
+                     sel_per_expert: bool = False, epilogue: int = EPI_NONE,
+                     out_dtype=torch.bfloat16, workspace=None, out=None, stream=None):
+    """Grouped compensated GEMM over the experts of `plan` (from moe_route)."""
+    lib = load()
+    cap = plan["rows_capacity"]
+    K = a.cols
+    ycols = n // 2 if epilogue == EPI_SWIGLU else n
+    y = out if out is not None else torch.empty((cap, ycols), dtype=out_dtype, device=a.codes.device)
+    yd = OUT_F32 if y.dtype == torch.float32 else OUT_BF16
+    ws = None
+    if r is not None:
+        ws = _workspace(workspace_size(OP_MOE_GEMM, 0, K, n, k, num_experts), y.device, workspace)
+    _check(lib.quads_moe_grouped_gemm(
+        num_experts, cap, n, K, _ptr(plan["offsets"]), _ptr(plan["counts"]), _ptr(a.codes),
+        _ptr(a.scales), _ptr(a.tensor_scale), int(a_scale_per_expert), _ptr(w.codes),
+        _ptr(w.scales), _ptr(w.tensor_scale), _ptr(r.codes if r else None),
+        _ptr(r.scales if r else None), _ptr(r.tensor_scale if r else None),
+        int(r_scale_per_expert), _ptr(sel), int(sel_per_expert), k, epilogue, _ptr(y), yd,
+        y.stride(0), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)),
+        "moe_grouped_gemm")
+    return y
+
+
+def trace_round(x_train: torch.Tensor, rollout: QTensor, *, counters=None, out=None, stream=None):
+    """-> (codes [rows, cols/2], counters int64 [3]: rtn mismatches, trace mismatches, rtn off-by-one)."""
+    lib = load()
+    rows, cols = x_train.shape
+    if rollout.layout != LINEAR:
+        raise QuadsError("trace_round takes LINEAR rollout scales")
+    codes = out if out is not None else torch.empty((rows, cols // 2), dtype=torch.uint8,
+                                                    device=x_train.device)
+    if counters is None:
+        counters = torch.zeros(3, dtype=torch.int64, device=x_train.device)
+    _check(lib.quads_trace_round(_ptr(x_train), rows, cols, x_train.stride(0),
+                                 _ptr(rollout.codes), rollout.codes.stride(0),
+                                 _ptr(rollout.scales), _ptr(rollout.tensor_scale), _ptr(codes),
+                                 _ptr(counters), _stream(stream)), "trace_round")
+    return codes, counters
+
+
+def moe_rows_capacity(tokens: int, topk: int, experts: int) -> int:
+    cap = tokens * topk + experts * (MOE_ROW_ALIGN - 1)
+    return (cap + MOE_ROW_ALIGN - 1) // MOE_ROW_ALIGN * MOE_ROW_ALIGN
+
+
+def moe_route(logits: torch.Tensor, topk: int, *, rows_capacity: Optional[int] = None,
+              out=None, stream=None) -> dict:
+    lib = load()
+    T, E = logits.shape
+    cap = rows_capacity or moe_rows_capacity(T, topk, E)
+    dev = logits.device
+    if out is None:
+        out = dict(idx=torch.empty((T, topk), dtype=torch.int32, device=dev),
+                   gates=torch.empty((T, topk), dtype=torch.float32, device=dev),
+                   counts=torch.empty(E, dtype=torch.int32, device=dev),
+                   offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                   row_token=torch.empty(cap, dtype=torch.int32, device=dev),
+                   token_row=torch.empty((T, topk), dtype=torch.int32, device=dev))
+    _check(lib.quads_moe_route(_ptr(logits), T, E, topk, _ptr(out["idx"]), _ptr(out["gates"]),
+                               _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["row_token"]),
+                               _ptr(out["token_row"]), cap, _stream(stream)), "moe_route")
+    out.update(rows_capacity=cap, tokens=T, experts=E, topk=topk)
+    return out
+
+
+def moe_gather(plan: dict, q: QTensor, *, out=None, stream=None) -> QTensor:
+    lib = load()
+    cap, cols = plan["rows_capacity"], q.cols
+    dev = q.codes.device
+    if out is None:
+        oc = torch.empty((cap, cols // 2), dtype=torch.uint8, device=dev)
+        osf = torch.empty(sf_tc_bytes(cap, cols), dtype=torch.uint8, device=dev)
+    else:
+        oc, osf = out
+    _check(lib.quads_moe_gather(_ptr(plan["row_token"]), _ptr(plan["offsets"]), plan["experts"],
+                                cap, cols, _ptr(q.codes), _ptr(q.scales), _ptr(oc), _ptr(osf),
+                                _stream(stream)), "moe_gather")
+    return QTensor(oc, osf, q.tensor_scale, cap, cols, TCGEN05)
+
+
+def moe_combine(y: torch.Tensor, plan: dict, *, out=None, stream=None) -> torch.Tensor:
+    lib = load()
+    T, topk, H = plan["tokens"], plan["topk"], y.shape[1]
+    o = out if out is not None else torch.empty((T, H), dtype=torch.bfloat16, device=y.device)
+    _check(lib.quads_moe_combine(_ptr(y), y.stride(0), _ptr(plan["token_row"]),
+                                 _ptr(plan["gates"]), T, topk, H, _ptr(o), o.stride(0),
+                                 _stream(stream)), "moe_combine")
+    return o
+
+
+def swiglu_row_index(experts: int, ffn: int, hidden: int, device) -> torch.Tensor:
+    """Row order of the stacked W1 [E*2F, H] that puts 64 gate rows and the
+    matching 64 up rows in every 128-row tile (what the SwiGLU epilogue reads)."""
+    assert ffn % 64 == 0
+    l = torch.arange(2 * ffn, dtype=torch.int64)
+    tile, within = l // 128, l % 128
+    src = torch.where(within < 64, tile * 64 + within, ffn + tile * 64 + (within - 64))
+    full = (torch.arange(experts, dtype=torch.int64)[:, None] * (2 * ffn) + src[None, :]).reshape(-1)
+    return full.to(torch.int32).to(device)
+
+
+def quantize_expert_weights(w: torch.Tensor, *, swiglu_interleave: bool = False,
+                            stream=None) -> QTensor:
+    """Stacked expert weights bf16 [E, N, K] -> NVFP4 with one tensor scale per
+    expert and tensor-core scale layout (N % 128 == 0)."""
+    E, N, K = w.shape
+    flat = w.reshape(E * N, K)
+    offs = torch.arange(0, E * N + 1, N, dtype=torch.int32, device=w.device)
+    ri = swiglu_row_index(E, N // 2, K, w.device) if swiglu_interleave else None
+    q, _ = quantize_nvfp4(flat, group_offsets=offs, num_groups=E, scale_layout=TCGEN05,
+                          row_index=ri, stream=stream)
+    return q

@@ -137,6 +137,22 @@ def channel_scores(R: np.ndarray, group_offsets=None, chunk: int = SCORE_CHUNK_R
     return out
 
 
+def chunk_partials(R: np.ndarray, end: int | None = None, chunk: int = SCORE_CHUNK_ROWS) -> np.ndarray:
+    """The per-chunk sums that ``channel_scores`` adds up: row c of the result is
+    the row-by-row float32 sum of R^2 over rows [32c, 32c+32) (rows < end).  Only
+    meaningful when every group starts at a multiple of the chunk size."""
+    R = np.asarray(R, dtype=np.float32)
+    end = R.shape[0] if end is None else end
+    n = (end + chunk - 1) // chunk
+    out = np.zeros((n, R.shape[1]), np.float32)
+    for c in range(n):
+        acc = np.zeros(R.shape[1], np.float32)
+        for r in range(c * chunk, min(c * chunk + chunk, end)):
+            acc = (acc + (R[r] * R[r]).astype(np.float32)).astype(np.float32)
+        out[c] = acc
+    return out
+
+
 def select_channels(scores: np.ndarray, k: int) -> np.ndarray:
     """Top-k channels by score (ties -> lower index), returned in ascending order."""
     scores = np.asarray(scores, dtype=np.float32)

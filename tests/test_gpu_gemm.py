@@ -1,0 +1,121 @@
+"""GPU parity of the compensated W4A4 GEMM (tcgen05 block-scaled MMA) against
+the oracle's float64 product: max |dY| <= 1e-3 * sum|a||b| per element and a
+relative Frobenius error <= 1e-5 (float32 output); bf16 output additionally
+allows its own rounding (2^-8 relative).  Q(W_sel), built inside the call, is
+read back from the workspace and must match bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import bf16_tensor, codes_np, f32, unswizzle
+from nvfp4_w4a4_quantized_quant_gb300 import inputs
+from oracle import gemm as G
+from oracle import nvfp4 as Q
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(lib, xb, wb, k, out_dtype, comp=True):
+    x, w = bf16_tensor(xb), bf16_tensor(wb)
+    xq, part = lib.quantize_nvfp4(x, scores=True, scale_layout=1)
+    wq, _ = lib.quantize_nvfp4(w, scale_layout=1)
+    if not comp:
+        return lib.w4a4_gemm_comp(xq, wq, out_dtype=out_dtype), None, None
+    sel, _, r = lib.select_residual_channels(x, xq, part, k, r_scale_layout=1)
+    N, K = wb.shape
+    ws = torch.zeros(lib.workspace_size(lib.OP_GEMM, 0, K, N, k, 1), dtype=torch.uint8, device="cuda")
+    y = lib.w4a4_gemm_comp(xq, wq, r, sel, k, out_dtype=out_dtype, workspace=ws)
+    return y, sel, ws
+
+
+def _oracle(xb, wb, k, rows=None, comp=True):
+    xf, wf = f32(xb), f32(wb)
+    ref = Q.quantize_full(xf, k)
+    wc, ws, wst = Q.quantize_groups(wf)
+    rows = slice(None) if rows is None else rows
+    if not comp:
+        return G.gemm_comp(ref["codes"][rows], ref["scales"][rows], ref["s_t"][0], wc, ws, wst[0]) + (ref, None)
+    wsc, wss = Q.requantize_weight_columns(wc, ws, ref["sel"][0])
+    Y, B = G.gemm_comp(ref["codes"][rows], ref["scales"][rows], ref["s_t"][0], wc, ws, wst[0],
+                       ref["r_codes"][rows], ref["r_scales"][rows], ref["r_s_t"][0], wsc, wss)
+    return Y, B, ref, (wsc, wss)
+
+
+def _check(y, Y, B, bf16_out):
+    yv = y.float().cpu().numpy().astype(np.float64)
+    err = np.abs(yv - Y)
+    tol = 1e-3 * B + (2.0 ** -8 * np.abs(Y) if bf16_out else 0.0) + 1e-30
+    assert np.all(err <= tol), f"max err {err.max()} at {np.unravel_index(np.argmax(err - tol), err.shape)}"
+    if not bf16_out:
+        rel = np.linalg.norm(yv - Y) / max(np.linalg.norm(Y), 1e-30)
+        assert rel <= 1e-5, rel
+    return float(err.max())
+
+
+def _check_wsel(lib, ws, N, k, oracle_wsel):
+    kp = lib.kpad(k)
+    raw = ws.cpu().numpy()
+    codes = raw[: N * kp // 2].reshape(N, kp // 2)
+    off = (N * kp // 2 + 1023) // 1024 * 1024
+    sf = torch.from_numpy(raw[off: off + N * kp // 16].copy())
+    from oracle.formats import unpack_nibbles
+    c = unpack_nibbles(codes)
+    s = unswizzle(sf, N, kp)
+    wsc, wss = oracle_wsel
+    assert np.array_equal(c[:, :k], wsc) and not c[:, k:].any()
+    assert np.array_equal(s[:, : k // 16], wss) and not s[:, k // 16:].any()
+
+
+def test_single_linear_f32(lib):
+    d = inputs.single_linear(0)
+    y, sel, ws = _run(lib, d["x"], d["w"], d["k"], torch.float32)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    Y, B, ref, wsel = _oracle(d["x"], d["w"], d["k"])
+    assert np.array_equal(sel.cpu().numpy(), ref["sel"])
+    _check(y, Y, B, False)
+    _check_wsel(lib, ws, 256, d["k"], wsel)
+
+
+def test_single_linear_plain_w4a4(lib):
+    d = inputs.single_linear(0)
+    y, _, _ = _run(lib, d["x"], d["w"], d["k"], torch.float32, comp=False)
+    Y, B, _, _ = _oracle(d["x"], d["w"], d["k"], comp=False)
+    _check(y, Y, B, False)
+
+
+@pytest.mark.parametrize("M,N,K,k", [(200, 256, 320, 48), (1, 128, 64, 16), (129, 384, 1024, 256),
+                                     (300, 128, 512, 272)])
+def test_ragged_shapes_f32(lib, M, N, K, k):
+    rng = inputs.make_rng(M + N + K)
+    xb = inputs.f32_to_bf16_bits(inputs.student_t4(rng, (M, K)))
+    wb = inputs.f32_to_bf16_bits(rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02))
+    y, sel, ws = _run(lib, xb, wb, k, torch.float32)
+    torch.cuda.synchronize()
+    Y, B, ref, wsel = _oracle(xb, wb, k)
+    assert np.array_equal(sel.cpu().numpy(), ref["sel"])
+    _check(y, Y, B, False)
+    _check_wsel(lib, ws, N, k, wsel)
+
+
+def test_dense_projection_full_size_sampled_rows(lib):
+    """4096x2048 activations, 6144x2048 weights, k=128, bf16 output -- the
+    benchmark's dense configuration; 96 sampled rows checked against float64."""
+    d = inputs.dense_projection(0)
+    y, sel, ws = _run(lib, d["x"], d["w"], d["k"], torch.bfloat16)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(4096, 96, replace=False))
+    rows[-1] = 4095
+    Y, B, ref, wsel = _oracle(d["x"], d["w"], d["k"], rows)
+    assert np.array_equal(sel.cpu().numpy(), ref["sel"])
+    _check(y[torch.from_numpy(rows).cuda()], Y, B, True)
+    _check_wsel(lib, ws, 6144, d["k"], wsel)
+
+
+def test_repeat_calls_are_deterministic(lib):
+    d = inputs.single_linear(0)
+    y1, _, _ = _run(lib, d["x"], d["w"], d["k"], torch.float32)
+    y2, _, _ = _run(lib, d["x"], d["w"], d["k"], torch.float32)
+    assert torch.equal(y1, y2)

@@ -1,0 +1,194 @@
+"""GPU parity of the activation-side kernels against the oracle: quantizer
+(codes, scale bytes in both layouts, tensor scales, residual-energy partials),
+channel selection and the second quantization, and TRACE rounding.  Integer
+outputs must match bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import bf16_tensor, codes_np, f32, linear_scales
+from nvfp4_w4a4_quantized_quant_gb300 import inputs
+from oracle import formats as F
+from oracle import nvfp4 as Q
+from oracle import trace as T
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(name):
+    rng = inputs.make_rng(11)
+    if name == "single_linear":
+        return inputs.single_linear(0)["x"]
+    if name == "dense_projection":
+        return inputs.dense_projection(0)["x"]
+    if name == "ragged":          # 3 tiles of rows + a ragged tail, 2 slabs + partial
+        return inputs.f32_to_bf16_bits(inputs.student_t4(rng, (389, 320)) * np.float32(4))
+    if name == "edge":            # zeros, ties, -0, saturation, huge/tiny blocks
+        x = np.zeros((70, 128), np.float32)
+        x[0, :4] = [60.0, 84.0, 36.0, 144.0]            # exact ties with d = 24
+        x[1, :16] = -0.0
+        x[2, :3] = [-0.01, 1e-3, 6.0]
+        x[3] = 3.0e4 * inputs.student_t4(rng, (128,))
+        x[4] = 1e-6 * inputs.student_t4(rng, (128,))
+        x[5, ::16] = 448.0 * 6
+        x[6:] = inputs.student_t4(rng, (64, 128))
+        return inputs.f32_to_bf16_bits(x)
+    if name == "zeros":
+        return np.zeros((33, 64), np.uint16)
+    raise KeyError(name)
+
+
+CASES = ["single_linear", "ragged", "edge", "zeros", "dense_projection"]
+
+
+@pytest.mark.parametrize("name", CASES)
+@pytest.mark.parametrize("layout", [0, 1])
+def test_quantize_bit_exact(lib, name, layout):
+    bits = _case(name)
+    rows, cols = bits.shape
+    if layout == 1 and cols % 64:
+        pytest.skip("tensor-core layout needs cols % 64 == 0")
+    x = bf16_tensor(bits)
+    q, part = lib.quantize_nvfp4(x, scale_layout=layout, scores=True)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    xf = f32(bits)
+    oc, osc, ost = Q.quantize_groups(xf)
+    assert q.tensor_scale.cpu().numpy()[0] == ost[0]
+    assert np.array_equal(codes_np(q.codes, cols), oc)
+    assert np.array_equal(linear_scales(q), osc)
+    R = Q.residual(xf, oc, osc, ost[0])
+    assert np.array_equal(part.cpu().numpy(), Q.chunk_partials(R))
+
+
+def test_quantize_groups_and_row_index(lib):
+    rng = inputs.make_rng(3)
+    x = inputs.student_t4(rng, (256, 192))
+    x[64:160] *= np.float32(50.0)
+    bits = inputs.f32_to_bf16_bits(x)
+    perm = rng.permutation(256).astype(np.int32)
+    offs = np.array([0, 64, 160, 224, 256], np.int32)
+    xt = bf16_tensor(bits)
+    q, part = lib.quantize_nvfp4(xt, group_offsets=torch.from_numpy(offs).cuda(), num_groups=4,
+                                 row_index=torch.from_numpy(perm).cuda(), scores=True)
+    torch.cuda.synchronize()
+    xp = f32(bits)[perm]
+    oc, osc, ost = Q.quantize_groups(xp, offs)
+    assert np.array_equal(q.tensor_scale.cpu().numpy(), ost)
+    assert np.array_equal(codes_np(q.codes, 192), oc)
+    assert np.array_equal(linear_scales(q), osc)
+    R = np.concatenate([Q.residual(xp[a:b], oc[a:b], osc[a:b], ost[g])
+                        for g, (a, b) in enumerate(zip(offs[:-1], offs[1:]))])
+    assert np.array_equal(part.cpu().numpy(), Q.chunk_partials(R))
+
+
+def test_quantize_given_tensor_scale(lib):
+    bits = _case("ragged")
+    x = bf16_tensor(bits)
+    ts = torch.tensor([0.0123], dtype=torch.float32, device="cuda")
+    q, _ = lib.quantize_nvfp4(x, tensor_scale_in=ts)
+    oc, osc = Q.quantize(f32(bits), np.float32(0.0123))
+    assert np.array_equal(codes_np(q.codes, bits.shape[1]), oc)
+    assert np.array_equal(linear_scales(q), osc)
+
+
+@pytest.mark.parametrize("name,k,layout", [("single_linear", 16, 0), ("ragged", 48, 1),
+                                           ("dense_projection", 128, 1), ("edge", 32, 0),
+                                           ("zeros", 16, 0)])
+def test_select_and_second_quantization_bit_exact(lib, name, k, layout):
+    bits = _case(name)
+    rows, cols = bits.shape
+    if layout == 1 and cols % 64:
+        layout = 0
+    x = bf16_tensor(bits)
+    q, part = lib.quantize_nvfp4(x, scores=True, scale_layout=layout)
+    sel, scores, r = lib.select_residual_channels(x, q, part, k, r_scale_layout=layout,
+                                                  want_scores=True)
+    torch.cuda.synchronize()
+    ref = Q.quantize_full(f32(bits), k)
+    assert np.array_equal(scores.cpu().numpy(), ref["scores"])
+    assert np.array_equal(sel.cpu().numpy(), ref["sel"])
+    assert r.tensor_scale.cpu().numpy()[0] == ref["r_s_t"][0]
+    kp = lib.kpad(k)
+    rc = codes_np(r.codes, kp)
+    assert np.array_equal(rc[:, :k], ref["r_codes"]) and not rc[:, k:].any()
+    rs = linear_scales(r, rows, kp)
+    assert np.array_equal(rs[:, : k // 16], ref["r_scales"]) and not rs[:, k // 16:].any()
+
+
+def test_select_per_group(lib):
+    rng = inputs.make_rng(5)
+    x = inputs.student_t4(rng, (320, 256))
+    x[:, 7] *= 30
+    x[128:, 200] *= 30
+    bits = inputs.f32_to_bf16_bits(x)
+    offs = np.array([0, 128, 256, 320], np.int32)
+    ot = torch.from_numpy(offs).cuda()
+    xt = bf16_tensor(bits)
+    q, part = lib.quantize_nvfp4(xt, group_offsets=ot, num_groups=3, scores=True, scale_layout=1)
+    sel, _, r = lib.select_residual_channels(xt, q, part, 32, group_offsets=ot, num_groups=3,
+                                             r_scale_layout=1)
+    torch.cuda.synchronize()
+    ref = Q.quantize_full(f32(bits), 32, offs)
+    assert np.array_equal(sel.cpu().numpy(), ref["sel"])
+    assert np.array_equal(r.tensor_scale.cpu().numpy(), ref["r_s_t"])
+    assert np.array_equal(codes_np(r.codes, 64)[:, :32], ref["r_codes"])
+    assert np.array_equal(linear_scales(r, 320, 64)[:, :2], ref["r_scales"])
+
+
+@pytest.mark.parametrize("rows,cols", [(64, 256), (1000, 512), (16384, 2048)])
+def test_trace_round_bit_exact(lib, rows, cols):
+    d = inputs.trace_rounding(0, rows, cols)
+    xr, xt = bf16_tensor(d["x_rollout"]), bf16_tensor(d["x_train"])
+    rq, _ = lib.quantize_nvfp4(xr)
+    codes, cnt = lib.trace_round(xt, rq)
+    torch.cuda.synchronize()
+    xrf, xtf = f32(d["x_rollout"]), f32(d["x_train"])
+    rc, rs, st = Q.quantize_groups(xrf)
+    oc, ocnt = T.trace_round(xtf, rc, rs, st[0])
+    assert np.array_equal(codes_np(codes, cols), oc)
+    c = cnt.cpu().numpy().tolist()
+    assert c == [ocnt["rtn_mismatch"], ocnt["trace_mismatch"], ocnt["rtn_off_by_one"]]
+    assert c[1] <= c[0]
+
+
+def test_trace_worked_example_on_gpu(lib):
+    xr = np.zeros((1, 16), np.float32)
+    xr[0, 0], xr[0, 1] = 59.75, 144.0
+    xt = xr.copy()
+    xt[0, 0] = 60.25
+    rq, _ = lib.quantize_nvfp4(bf16_tensor(inputs.f32_to_bf16_bits(xr)))
+    codes, cnt = lib.trace_round(bf16_tensor(inputs.f32_to_bf16_bits(xt)), rq)
+    assert F.e2m1_decode(codes_np(codes, 16)[0, 0]) == 2.0
+    assert cnt.cpu().tolist() == [1, 0, 1]
+
+
+def test_conversions_exhaustive_against_oracle(lib):
+    """Every bf16 bit pattern through the quantizer with unit scales: each block
+    holds 6*448 so s_t = 1, and the block scale is 448 -> d = 448."""
+    allb = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    v = f32(allb)
+    keep = np.isfinite(v) & (np.abs(v) <= 2688)
+    vals = allb[keep]
+    n = (len(vals) + 14) // 15 * 15
+    vals = np.concatenate([vals, np.zeros(n - len(vals), np.uint16)]).reshape(-1, 15)
+    big = inputs.f32_to_bf16_bits(np.full((vals.shape[0], 1), 2688.0, np.float32))
+    bits = np.concatenate([big, vals], axis=1)
+    q, _ = lib.quantize_nvfp4(bf16_tensor(bits))
+    oc, osc, _ = Q.quantize_groups(f32(bits))
+    assert np.array_equal(codes_np(q.codes, 16), oc)
+    assert np.array_equal(linear_scales(q), osc)
+
+
+def test_block_scale_encoding_exhaustive(lib):
+    """Every bf16 magnitude as a block maximum under tensor scale 1: scale byte = E4M3(m / 6)."""
+    allb = np.arange(1 << 15, dtype=np.uint32).astype(np.uint16)      # sign bit clear
+    v = f32(allb)
+    vals = allb[np.isfinite(v)]
+    bits = np.zeros((len(vals), 16), np.uint16)
+    bits[:, 0] = vals
+    one = torch.ones(1, dtype=torch.float32, device="cuda")
+    q, _ = lib.quantize_nvfp4(bf16_tensor(bits), tensor_scale_in=one)
+    oc, osc = Q.quantize(f32(bits), np.float32(1.0))
+    assert np.array_equal(linear_scales(q), osc)
+    assert np.array_equal(codes_np(q.codes, 16), oc)
