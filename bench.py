@@ -1,0 +1,398 @@
+"""Benchmark of the NVFP4 W4A4 residual-compensation MoE expert layer on GB300.
+
+One step = one pass of the rollout-side hot path over one batch: router top-8
+and dispatch plan, NVFP4 quantization of the tokens with residual-energy
+partials, top-k residual channel selection and second quantization, gather
+into expert order, grouped compensated GEMM1 with the SwiGLU epilogue,
+per-expert quantization and selection of h, grouped compensated GEMM2, and
+the gate-weighted combine (weights are pre-quantized once, as after a weight
+sync).  Workload: 8192 tokens, hidden 2048, 128 experts, top-8, expert FFN 768,
+k = 64 selected channels per GEMM, seeded synthetic inputs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  `value` is the whole-job MoE GEMM throughput in TFLOP/s
+(algorithmic FLOPs of both grouped GEMMs, main + correction, over real rows)
+divided by the device-timed step; `e2e` is the same metric through the C ABI
+from pinned host buffers with the copies inside the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = dict(tokens=8192, hidden=2048, experts=128, topk=8, ffn=768, k1=64, k2=64)
+METRIC = "W4A4+residual-comp MoE GEMM TFLOPS (% FP4 peak); quantizer GB/s (% HBM)"
+FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense ratio used to scale the measured bf16 peak
+
+
+def moe_flops(w=WORKLOAD) -> float:
+    rows = w["tokens"] * w["topk"]
+    H, F = w["hidden"], w["ffn"]
+    g1 = 2.0 * rows * (2 * F) * (H + w["k1"])
+    g2 = 2.0 * rows * H * (F + w["k2"])
+    return g1 + g2
+
+
+def gemm1_bytes(w=WORKLOAD) -> float:
+    """Algorithmic HBM bytes of one grouped GEMM1 launch: NVFP4 weights of all
+    experts (0.5625 B/element), NVFP4 A rows, the correction operands, bf16 h."""
+    rows, H, F, E = w["tokens"] * w["topk"], w["hidden"], w["ffn"], w["experts"]
+    kp = 64 if w["k1"] <= 64 else 128
+    return (E * 2 * F * H * 0.5625 + rows * H * 0.5625 + rows * kp * 0.5625
+            + E * 2 * F * kp * 0.5625 + rows * F * 2)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index, self.proc, self.path = index, None, None
+
+    def start(self):
+        try:
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names[1:], parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------- oracle leg
+ORACLE_SAMPLE_EXPERTS = 2
+REFERENCE_TOKENS = 2048        # per reference-arm step: a quarter of the batch
+
+
+def oracle_sample(seed=0, tokens=None):
+    """The oracle on a bounded sample of the workload: routing and activation
+    quantization/selection of `tokens` tokens (default all), then the full
+    expert FFN (both compensated GEMMs) of the first experts, with the router
+    restricted to them.  Returns (flops, seconds)."""
+    import numpy as np
+    from nvfp4_w4a4_quantized_quant_gb300 import inputs
+    from oracle import moe as M
+    w = WORKLOAD
+    d = inputs.moe_layer(seed, tokens=tokens or w["tokens"], hidden=w["hidden"],
+                         experts=w["experts"], topk=w["topk"], ffn=w["ffn"], k=w["k1"],
+                         with_weights=False)
+    rng = inputs.make_rng(seed + 1)
+    E, H, F = ORACLE_SAMPLE_EXPERTS, w["hidden"], w["ffn"]
+    w1 = (rng.standard_normal((E, 2 * F, H), dtype=np.float32) * np.float32(0.02))
+    w2 = (rng.standard_normal((E, H, F), dtype=np.float32) * np.float32(0.02))
+    x = inputs.bf16_bits_to_f32(d["x"])
+    w1q, w2q = M.quantize_weights(w1), M.quantize_weights(w2)
+    logits = d["logits"][:, :E]             # routing restricted to the sampled experts
+    t0 = time.perf_counter()
+    res = M.moe_layer(x, logits, w1q, w2q, w["k1"], w["k2"], topk=min(w["topk"], E),
+                      experts_subset=list(range(E)))
+    dt = time.perf_counter() - t0
+    rows = sum(len(res["tokens"][e]) for e in range(E))
+    fl = 2.0 * rows * (2 * F) * (H + w["k1"]) + 2.0 * rows * H * (F + w["k2"])
+    return fl, dt
+
+
+def cpu_baseline(threads=None):
+    threads = threads or len(os.sched_getaffinity(0))
+    env = dict(os.environ, OMP_NUM_THREADS=str(threads), OPENBLAS_NUM_THREADS=str(threads),
+               MKL_NUM_THREADS=str(threads), CUDA_VISIBLE_DEVICES="")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; f,t=bench.oracle_sample(); "
+            "print(json.dumps(dict(flops=f, seconds=t)))" % ROOT)
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                         timeout=900)
+    if out.returncode != 0:
+        return {"value": None, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                "error": out.stderr.strip().splitlines()[-1:] }
+    r = json.loads(out.stdout.strip().splitlines()[-1])
+    return {"value": r["flops"] / r["seconds"] / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "seconds": round(r["seconds"], 2),
+            "sample": f"all {WORKLOAD['tokens']} tokens routed/quantized/selected; expert FFN of "
+                      f"{ORACLE_SAMPLE_EXPERTS} experts (router restricted to them), numpy float32/float64"}
+
+
+# ----------------------------------------------------------------- GPU leg
+def build_layer(torch, seed=0):
+    import numpy as np
+    from nvfp4_w4a4_quantized_quant_gb300 import inputs
+    from nvfp4_w4a4_quantized_quant_gb300.layer import MoEExpertLayer
+    w = WORKLOAD
+    d = inputs.moe_layer(seed, tokens=w["tokens"], hidden=w["hidden"], experts=w["experts"],
+                         topk=w["topk"], ffn=w["ffn"], k=w["k1"], with_weights=False)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    E, H, F = w["experts"], w["hidden"], w["ffn"]
+    w1 = (torch.randn((E, 2 * F, H), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    w2 = (torch.randn((E, H, F), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    layer = MoEExpertLayer(w1, w2, w["topk"], w["k1"], w["k2"], w["tokens"])
+    del w1, w2
+    x_host = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    l_host = torch.from_numpy(d["logits"]).pin_memory()
+    return layer, x_host, l_host
+
+
+def timed(torch, fn, steps, flush, stream):
+    """Sum of per-step device times (ms) with an L2 flush before each step."""
+    tot = 0.0
+    for _ in range(steps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        tot += a.elapsed_time(b)
+    return tot
+
+
+def run_gpu(args):
+    import torch
+    from nvfp4_w4a4_quantized_quant_gb300 import quads as Q
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    Q.load()
+    pk = peaks()
+    layer, x_host, l_host = build_layer(torch, seed=rank)
+    x = x_host.cuda()
+    logits = l_host.cuda()
+    stream = torch.cuda.Stream()
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush = lambda: flush_buf.random_(0, 255)  # noqa: E731  (writes 256 MB > L2)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            layer.forward(x, logits)
+        torch.cuda.synchronize()
+        n0 = Q.kernel_launch_count()
+        layer.forward(x, logits)
+        torch.cuda.synchronize()
+        launches_per_step = Q.kernel_launch_count() - n0
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            layer.forward(x, logits)
+        torch.cuda.synchronize()
+        assert Q.device_status(stream) == 0
+
+    def step():
+        graph.replay()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        clocks = ClockSampler(local)
+        clocks.start()
+        time.sleep(0.3)
+        torch.cuda.synchronize()
+        t_ms = timed(torch, step, args.steps, flush, stream)
+        clk = clocks.stop()
+
+        # per-kernel timing of the dominant kernel (grouped GEMM1) inside the same stream
+        plan = layer.b["route"]
+        def g1():
+            Q.moe_grouped_gemm(dict(plan, rows_capacity=layer.cap, experts=layer.E), layer._a1,
+                               layer.w1q, layer.E, 2 * layer.F, layer._r1, layer.b["sel1"],
+                               layer.k1, epilogue=Q.EPI_SWIGLU, workspace=layer.ws["g1"],
+                               out=layer.b["h"], stream=stream)
+        g1_ms = timed(torch, g1, args.steps, flush, stream) / args.steps
+
+        # quantizer alone on the layer input (scores on): algorithmic bytes
+        xq_out = (layer.b["xc"], layer.b["xs"], layer.b["xts"], layer.b["xpart"])
+        def qx():
+            Q.quantize_nvfp4(x, scores=True, workspace=layer.ws["q1"], out=xq_out, stream=stream)
+        q_ms = timed(torch, qx, args.steps, flush, stream) / args.steps
+
+        # end to end: pinned host input -> device, step, output -> pinned host
+        out_host = torch.empty(layer.b["out"].shape, dtype=torch.bfloat16).pin_memory()
+        def e2e():
+            x.copy_(x_host, non_blocking=True)
+            logits.copy_(l_host, non_blocking=True)
+            graph.replay()
+            out_host.copy_(layer.b["out"], non_blocking=True)
+        e2e_ms = timed(torch, e2e, args.steps, flush, stream)
+    torch.cuda.synchronize()
+
+    ms = t_ms / args.steps
+    e_ms = e2e_ms / args.steps
+    if dist:
+        t = torch.tensor([ms, e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e_ms = t.tolist()
+    if rank != 0:
+        return
+    fl = moe_flops()
+    value = world * fl / (ms * 1e-3) / 1e12
+    e2e_val = world * fl / (e_ms * 1e-3) / 1e12
+    T, H, E = WORKLOAD["tokens"], WORKLOAD["hidden"], WORKLOAD["experts"]
+    q_bytes = T * H * 2 + T * H * 0.5 + T * H / 16 + (T // 32) * H * 4
+    fp4_peak = pk["bf16_sus"] * FP4_OVER_BF16
+    g1_bytes = gemm1_bytes()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "nvfp4 (e2m1 codes, e4m3 block scales, fp32 tensor scale; fp32 accumulate)",
+        "data": "synthetic (seeded: Student-t(4) tokens, N(0,1) router logits, N(0,0.02) weights)",
+        "config": {"workload": "moe_expert_layer", **WORKLOAD, "l2": "flushed (256 MB write) before every step",
+                   "graph": "CUDA graph replay of the whole step", "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "frac_of_fp4_peak": round(value / fp4_peak, 4),
+        "fp4_peak_tflops": round(fp4_peak, 1),
+        "fp4_peak_source": f"{pk['src']} bf16 sustained {pk['bf16_sus']} x nominal fp4/bf16 ratio {FP4_OVER_BF16}",
+        "roofline": {
+            "kernel": "grouped compensated GEMM1 (gate+up, SwiGLU epilogue)",
+            "bound": "hbm",
+            "achieved": round(g1_bytes / (g1_ms * 1e-3) / 1e9, 1),
+            "peak": pk["hbm"],
+            "unit": "GB/s",
+            "frac": round(g1_bytes / (g1_ms * 1e-3) / 1e9 / pk["hbm"], 4),
+            "traffic": None,
+            "ms": round(g1_ms, 4),
+            "tflops": round(2.0 * T * WORKLOAD["topk"] * 2 * WORKLOAD["ffn"] * (H + WORKLOAD["k1"]) / (g1_ms * 1e-3) / 1e12, 1),
+            "algorithmic_bytes": int(g1_bytes),
+            "peak_source": pk["src"],
+        },
+        "quantizer": {"gbs": round(q_bytes / (q_ms * 1e-3) / 1e9, 1), "frac_hbm": round(q_bytes / (q_ms * 1e-3) / 1e9 / pk["hbm"], 4),
+                      "ms": round(q_ms, 4), "shape": [T, H], "algorithmic_bytes": int(q_bytes)},
+        "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(x_host.numel() * 2 + l_host.numel() * 4),
+                "d2h_bytes_per_step": int(out_host.numel() * 2), "ms_per_step": round(e_ms, 4)},
+        "gpu_launches": int(launches_per_step * args.steps),
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_profile(args):
+    """A plain sequence of eager forward passes (no graph, no flush, no clock
+    sampling) for an ncu launch list or a single-kernel capture."""
+    import torch
+    from nvfp4_w4a4_quantized_quant_gb300 import quads as Q
+    torch.cuda.set_device(0)
+    Q.load()
+    layer, x_host, l_host = build_layer(torch)
+    x, logits = x_host.cuda(), l_host.cuda()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup + args.steps):
+        layer.forward(x, logits)
+    torch.cuda.synchronize()
+    assert Q.device_status() == 0
+    print(json.dumps({"profile_steps": args.warmup + args.steps,
+                      "launches": Q.kernel_launch_count()}))
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    fl_tot, t_tot = 0.0, 0.0
+    for _ in range(args.warmup):
+        pass                      # the oracle has no warm-up state; warm-up steps are not repeated
+    for s in range(args.steps):
+        fl, dt = oracle_sample(seed=s, tokens=REFERENCE_TOKENS)
+        fl_tot += fl
+        t_tot += dt
+    v = fl_tot / t_tot / 1e12
+    threads = len(os.sched_getaffinity(0))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t_tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4 values in float32/float64 (numpy)", "data": "synthetic",
+        "config": {"workload": "moe_expert_layer", **WORKLOAD},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"per step: {REFERENCE_TOKENS} tokens routed/quantized/selected, expert FFN of {ORACLE_SAMPLE_EXPERTS} experts (router restricted to them)"},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="libquads", choices=["libquads", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="eager steps only, for ncu launch lists / captures")
+    args = ap.parse_args()
+    if args.warmup < 3 and not args.profile:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    elif args.profile:
+        run_profile(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

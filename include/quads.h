@@ -90,6 +90,9 @@ enum {
 
 /* Library version as major*10000 + minor*100 + patch. */
 int quads_version(void);
+/* Number of CUDA kernels this library has launched (or recorded into a graph
+ * under stream capture) from the calling process since it was loaded. */
+uint64_t quads_kernel_launch_count(void);
 const char* quads_status_string(quads_status_t s);
 /* One-line reason for the last non-OK status returned on this host thread. */
 const char* quads_last_error_detail(void);
@@ -134,7 +137,7 @@ int32_t quads_kpad(int32_t k);
  *                  so `rows` may be a capacity (e.g. padded expert rows).
  *   tensor_scale_in nullable device float [num_groups]: use these tensor
  *                  scales instead of computing amax / 2688.
- *   codes [rows, ld_codes] (ld_codes >= cols/2, multiple of 16); scales in
+ *   codes [rows, ld_codes] (ld_codes >= cols/2, multiple of 4); scales in
  *                  scale_layout (LINEAR: [rows, cols/16]); tensor_scale_out
  *                  device float [num_groups] (written even when scales are given).
  *   score_partials nullable device float [ceil(rows/32), cols]: entry

@@ -1,5 +1,6 @@
 // Host-side glue of the libquads C ABI: status strings, per-thread error
 // detail, workspace sizing and the device error word.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 
@@ -24,7 +25,10 @@ quads_status_t fail(quads_status_t s, const char* fmt, ...) {
   return s;
 }
 
-quads_status_t check_launch(const char* what) {
+static std::atomic<unsigned long long> g_launches{0};
+
+quads_status_t check_launch(const char* what, int kernels_launched) {
+  g_launches += (unsigned long long)kernels_launched;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(QUADS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
   return QUADS_OK;
@@ -51,6 +55,8 @@ int read_gemm_device_error();
 using namespace quads;
 
 extern "C" int quads_version(void) { return 100; }
+
+extern "C" uint64_t quads_kernel_launch_count(void) { return (uint64_t)g_launches.load(); }
 
 extern "C" const char* quads_status_string(quads_status_t s) {
   switch (s) {

@@ -22,7 +22,7 @@ constexpr float kE4M3Max = 448.0f;
 // ----------------------------------------------------------------- host status
 void set_detail(const char* fmt, ...);
 quads_status_t fail(quads_status_t s, const char* fmt, ...);
-quads_status_t check_launch(const char* what);
+quads_status_t check_launch(const char* what, int kernels_launched);
 int num_sms();
 
 // ------------------------------------------------------------ scale layouts

@@ -607,7 +607,7 @@ static quads_status_t launch(const Launch& L) {
   int64_t grid = num_sms();
   if (!L.row_off) grid = std::min<int64_t>(grid, ((L.M + BM - 1) / BM) * (L.N / BN));
   gemm_kernel<<<(int)grid, NUM_THREADS, SMEM_BYTES, L.stream>>>(tA, tB, tR, tW, p);
-  return check_launch("gemm");
+  return check_launch("gemm", comp ? 2 : 1);
 }
 
 }  // namespace gemm

@@ -215,7 +215,7 @@ extern "C" quads_status_t quads_moe_route(const float* logits, int32_t tokens, i
   plan_kernel<<<1, kMaxExperts, 0, st>>>(expert_counts, num_experts, expert_offsets);
   assign_kernel<<<num_experts, 1024, 0, st>>>(topk_idx, tokens, topk, expert_offsets,
                                               expert_counts, row_token, token_row);
-  return check_launch("moe_route");
+  return check_launch("moe_route", tokens > 0 ? 3 : 2);
 }
 
 extern "C" quads_status_t quads_moe_gather(const int32_t* row_token, const int32_t* expert_offsets,
@@ -233,7 +233,7 @@ extern "C" quads_status_t quads_moe_gather(const int32_t* row_token, const int32
   const int blocks = (int)std::min<int64_t>((rows_capacity * 32 + 255) / 256, (int64_t)num_sms() * 16);
   gather_kernel<<<blocks, 256, 0, st>>>(row_token, expert_offsets, num_experts, rows_capacity,
                                         (int)cols, in_codes, in_scales, out_codes, out_scales);
-  return check_launch("moe_gather");
+  return check_launch("moe_gather", 1);
 }
 
 extern "C" quads_status_t quads_moe_combine(const void* y, int64_t ldy, const int32_t* token_row,
@@ -248,5 +248,5 @@ extern "C" quads_status_t quads_moe_combine(const void* y, int64_t ldy, const in
   const int blocks = (int)std::min<int64_t>((work + 255) / 256, (int64_t)num_sms() * 8);
   combine_kernel<<<blocks, 256, 0, st>>>((const __nv_bfloat16*)y, ldy, token_row, gates, tokens,
                                          topk, (int)hidden, (__nv_bfloat16*)out, ldo);
-  return check_launch("moe_combine");
+  return check_launch("moe_combine", 1);
 }

@@ -445,8 +445,8 @@ extern "C" quads_status_t quads_quantize_nvfp4(
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "quantize: TCGEN05 scale layout needs cols %% 64 == 0");
   if (scale_layout != QUADS_SCALES_LINEAR && scale_layout != QUADS_SCALES_TCGEN05)
     return fail(QUADS_ERR_INVALID_ARG, "quantize: bad scale_layout %d", scale_layout);
-  if (ldx < cols || ldx % 8 || ld_codes < cols / 2 || ld_codes % 16)
-    return fail(QUADS_ERR_MISALIGNED, "quantize: ldx=%lld (>=cols, %%8) ld_codes=%lld (>=cols/2, %%16)", (long long)ldx, (long long)ld_codes);
+  if (ldx < cols || ldx % 8 || ld_codes < cols / 2 || ld_codes % 4)
+    return fail(QUADS_ERR_MISALIGNED, "quantize: ldx=%lld (>=cols, %%8) ld_codes=%lld (>=cols/2, %%4)", (long long)ldx, (long long)ld_codes);
   if (!aligned16(x) || !aligned16(codes) || (score_partials && !aligned16(score_partials)))
     return fail(QUADS_ERR_MISALIGNED, "quantize: x/codes/score_partials must be 16-byte aligned");
   const int G = group_offsets ? num_groups : 1;
@@ -482,7 +482,7 @@ extern "C" quads_status_t quads_quantize_nvfp4(
     quantize_kernel<false><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)x, rows, (int)cols, ldx,
                                                    row_index, group_offsets, G, stp, codes,
                                                    ld_codes, scales, scale_layout, nullptr);
-  return check_launch("quantize");
+  return check_launch("quantize", tensor_scale_in ? 1 : 3);
 }
 
 extern "C" quads_status_t quads_select_residual_channels(
@@ -524,7 +524,7 @@ extern "C" quads_status_t quads_select_residual_channels(
   }
   rsel_quantize_kernel<<<grid_for(rows * (kpad / 8), 256), 256, 0, st>>>(
       rs, rows, k, kpad, group_offsets, G, amax, r_codes, r_scales, r_scale_layout, r_tensor_scale);
-  return check_launch("select");
+  return check_launch("select", 3);
 }
 
 extern "C" quads_status_t quads_trace_round(const void* x_train, int64_t rows, int64_t cols,
@@ -542,5 +542,5 @@ extern "C" quads_status_t quads_trace_round(const void* x_train, int64_t rows, i
   trace_kernel<<<grid_for(rows * (cols / 8), 256), 256, 0, st>>>(
       (const __nv_bfloat16*)x_train, rows, (int)cols, ldx, rollout_codes, ld_codes,
       rollout_scales, rollout_tensor_scale, codes_out, counters);
-  return check_launch("trace_round");
+  return check_launch("trace_round", 1);
 }

@@ -140,5 +140,6 @@ class MoEExpertLayer:
                                a_scale_per_expert=True, r_scale_per_expert=True,
                                sel_per_expert=True, workspace=ws["g2"], out=b["y"], stream=stream)
         out = Q.moe_combine(y, plan, out=b["out"], stream=stream)
+        self._a1, self._r1 = a1, r1
         return dict(out=out, plan=plan, xq=xq, sel1=sel1, a1=a1, r1=r1, h=h, hq=hq, sel2=sel2,
                     r2=r2, y=y)

@@ -28,6 +28,7 @@ _P, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_
 
 _SIGS = {
     "quads_version": (ctypes.c_int, []),
+    "quads_kernel_launch_count": (ctypes.c_uint64, []),
     "quads_status_string": (ctypes.c_char_p, [_I32]),
     "quads_last_error_detail": (ctypes.c_char_p, []),
     "quads_device_status": (_I32, [_P, ctypes.POINTER(_I32)]),
@@ -115,6 +116,11 @@ def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]):
 
 def sf_tc_bytes(rows: int, cols: int) -> int:
     return ((rows + 127) // 128) * 128 * (cols // 16)
+
+
+def kernel_launch_count() -> int:
+    """Kernels launched (or captured) by libquads in this process so far."""
+    return int(load().quads_kernel_launch_count())
 
 
 def device_status(stream=None) -> int:

@@ -1,0 +1,73 @@
+"""CPU checks of the C ABI: the library builds and loads without a GPU, exports
+every function the header declares, and rejects bad arguments on the host
+before touching the device."""
+import ctypes
+
+import pytest
+
+from nvfp4_w4a4_quantized_quant_gb300 import build, quads
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return quads.load()
+
+
+def test_exports_every_header_symbol(lib):
+    syms = quads.header_symbols()
+    assert len(syms) >= 14
+    assert [s for s in syms if not hasattr(lib, s)] == []
+    assert lib.quads_version() == 100
+
+
+def test_status_strings_and_sizes(lib):
+    assert lib.quads_status_string(0) == b"ok"
+    assert lib.quads_status_string(5) == b"device pipeline wait timed out"
+    assert [lib.quads_kpad(k) for k in (16, 64, 80, 128, 192, 256, 272)] == [64, 64, 128, 128, 256, 256, 512]
+    assert lib.quads_workspace_size(quads.OP_QUANTIZE, 10, 64, 0, 0, 3) == 12
+    sel = lib.quads_workspace_size(quads.OP_SELECT, 100, 256, 0, 16, 2)
+    assert sel == ((100 * 16 * 4 + 255) // 256) * 256 + 8
+    g = lib.quads_workspace_size(quads.OP_GEMM, 0, 2048, 6144, 128, 1)
+    assert g == ((6144 * 64 + 1023) // 1024) * 1024 + 6144 * 8
+
+
+def _err(lib):
+    return lib.quads_last_error_detail().decode()
+
+
+def test_host_side_argument_checks_need_no_gpu(lib):
+    p = ctypes.c_void_p(16)     # never dereferenced: every call below fails validation first
+    st = lib.quads_quantize_nvfp4(p, 8, 15, 16, None, None, 1, None, p, 8, p, 0, p, None, p, 64, None)
+    assert st == 2 and "multiple of 16" in _err(lib)
+    st = lib.quads_quantize_nvfp4(None, 8, 16, 16, None, None, 1, None, p, 8, p, 0, p, None, p, 64, None)
+    assert st == 1
+    st = lib.quads_quantize_nvfp4(p, 8, 32, 16, None, None, 1, None, p, 16, p, 0, p, None, p, 64, None)
+    assert st == 3                                   # ldx < cols
+    st = lib.quads_quantize_nvfp4(p, 8, 32, 32, None, None, 1, None, p, 16, p, 1, p, None, p, 64, None)
+    assert st == 2                                   # tcgen05 layout needs cols % 64
+    st = lib.quads_w4a4_gemm_comp(64, 100, 256, p, p, p, p, p, p, None, None, None, None, 0, p, 0, 100,
+                                  None, 0, None)
+    assert st == 2 and "N%128" in _err(lib)
+    st = lib.quads_w4a4_gemm_comp(64, 128, 256, p, p, p, p, p, p, p, p, p, p, 8, p, 0, 128, None, 0, None)
+    assert st == 1                                   # k not a multiple of 16
+    st = lib.quads_select_residual_channels(p, 64, 256, 256, None, 1, p, 0, p, p, 17, p, None, p, p, 0, p,
+                                            p, 1 << 20, None)
+    assert st == 2
+    st = lib.quads_moe_route(p, 100, 300, 8, p, p, p, p, p, p, 1 << 20, None)
+    assert st == 2                                   # > 256 experts
+    st = lib.quads_moe_route(p, 100, 16, 8, p, p, p, p, p, p, 10, None)
+    assert st == 1 and "rows_capacity" in _err(lib)
+    st = lib.quads_moe_grouped_gemm(4, 1000, 256, 256, p, None, p, p, p, 0, p, p, p, None, None, None,
+                                    0, None, 0, 0, 0, p, 1, 256, None, 0, None)
+    assert st == 2                                   # rows_capacity % 128
+    st = lib.quads_trace_round(p, 4, 24, 24, p, 12, p, p, p, None, None)
+    assert st == 2
+
+
+def test_product_path_never_imports_the_oracle():
+    import pathlib
+    pkg = pathlib.Path(quads.__file__).parent
+    for f in list(pkg.glob("*.py")) + list(pkg.glob("csrc/*")):
+        text = f.read_text()
+        assert "import oracle" not in text and "from oracle" not in text, f
