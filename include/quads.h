@@ -80,7 +80,8 @@ enum {
   QUADS_OP_QUANTIZE = 0,
   QUADS_OP_SELECT = 1,
   QUADS_OP_GEMM = 2,
-  QUADS_OP_MOE_GEMM = 3
+  QUADS_OP_MOE_GEMM = 3,
+  QUADS_OP_MOE_ROUTE = 4
 };
 
 /* Rows of the score-partial array are chunks of this many consecutive rows. */
@@ -109,10 +110,12 @@ quads_status_t quads_device_status(void* stream, int32_t* device_code);
 
 /* Bytes of scratch the call `op` needs for the given shape (0 if none).
  *   QUADS_OP_QUANTIZE: num_groups floats of tensor amax.
- *   QUADS_OP_SELECT:   rows*k floats (the residual slice) + num_groups floats.
+ *   QUADS_OP_SELECT:   rows*k floats (the residual slice) + num_groups floats
+ *                      (its amax) + num_groups*cols floats (channel scores).
  *   QUADS_OP_GEMM:     the requantized selected weight columns Q(W_sel):
  *                      n*kpad/2 code bytes + n*kpad/16 scale bytes (+ alignment).
  *   QUADS_OP_MOE_GEMM: the same for num_groups experts.
+ *   QUADS_OP_MOE_ROUTE: one bit per (token, expert): rows = tokens, cols = experts.
  * `cols` is the channel count (K) and `n` the output width (N, unused for the
  * activation-side ops).  kpad = k rounded up to 64 (k <= 256) or to 256. */
 size_t quads_workspace_size(int32_t op, int64_t rows, int64_t cols, int64_t n, int32_t k,
@@ -137,6 +140,9 @@ int32_t quads_kpad(int32_t k);
  *                  so `rows` may be a capacity (e.g. padded expert rows).
  *   tensor_scale_in nullable device float [num_groups]: use these tensor
  *                  scales instead of computing amax / 2688.
+ *   tensor_amax_in nullable device float [num_groups]: the groups' absolute
+ *                  maxima, already known (e.g. from the producing GEMM's
+ *                  epilogue); s_t = amax / 2688 without another pass over x.
  *   codes [rows, ld_codes] (ld_codes >= cols/2, multiple of 4); scales in
  *                  scale_layout (LINEAR: [rows, cols/16]); tensor_scale_out
  *                  device float [num_groups] (written even when scales are given).
@@ -149,7 +155,8 @@ int32_t quads_kpad(int32_t k);
 quads_status_t quads_quantize_nvfp4(const void* x, int64_t rows, int64_t cols, int64_t ldx,
                                     const int32_t* row_index, const int32_t* group_offsets,
                                     int32_t num_groups, const float* tensor_scale_in,
-                                    uint8_t* codes, int64_t ld_codes, uint8_t* scales,
+                                    const float* tensor_amax_in, uint8_t* codes,
+                                    int64_t ld_codes, uint8_t* scales,
                                     int32_t scale_layout, float* tensor_scale_out,
                                     float* score_partials, void* workspace,
                                     size_t workspace_bytes, void* stream);
@@ -190,12 +197,14 @@ quads_status_t quads_select_residual_channels(
  * in one kernel on the tcgen05 block-scaled tensor cores (two TMEM
  * accumulators summed in the epilogue).  [QUADS] 2.2 B "Mechanism" (correction
  * added back to the quantized output) and section 1 (native W4A4 GEMM).
- * Q(W_sel) is built inside the call (into `workspace`) from the packed weight:
- * the selected columns of DQ(Q(W)) in units of s_w, requantized in 16-blocks
- * along the selection with s_w kept.
+ * Q(W_sel) is built inside the call (into `workspace`) from the column-major
+ * copy of the packed weight (quads_weight_columns): the selected columns of
+ * DQ(Q(W)) in units of s_w, requantized in 16-blocks along the selection with
+ * s_w kept.
  *
  *   A: a_codes [M, K/2], a_scales TCGEN05 (ceil(M/128)*128 rows), a_tensor_scale device [1].
- *   W: w_codes [N, K/2], w_scales TCGEN05, w_tensor_scale device [1].
+ *   W: w_codes [N, K/2], w_scales TCGEN05, w_tensor_scale device [1];
+ *   w_codes_t / w_scales_t: its column-major copy (required with compensation).
  *   r_codes NULL -> plain W4A4 (sel, r_* ignored); else r_codes [M, kpad/2],
  *   r_scales TCGEN05 over kpad columns, r_tensor_scale [1], sel [k] ascending.
  *   y [M, ldy] float32 or bf16 (y_dtype).
@@ -204,7 +213,8 @@ quads_status_t quads_select_residual_channels(
 quads_status_t quads_w4a4_gemm_comp(int64_t M, int64_t N, int64_t K, const uint8_t* a_codes,
                                     const uint8_t* a_scales, const float* a_tensor_scale,
                                     const uint8_t* w_codes, const uint8_t* w_scales,
-                                    const float* w_tensor_scale, const uint8_t* r_codes,
+                                    const float* w_tensor_scale, const uint8_t* w_codes_t,
+                                    const uint8_t* w_scales_t, const uint8_t* r_codes,
                                     const uint8_t* r_scales, const float* r_tensor_scale,
                                     const int32_t* sel, int32_t k, void* y, int32_t y_dtype,
                                     int64_t ldy, void* workspace, size_t workspace_bytes,
@@ -220,7 +230,8 @@ quads_status_t quads_w4a4_gemm_comp(int64_t M, int64_t N, int64_t K, const uint8
  *   a_codes [rows_capacity, K/2], a_scales TCGEN05; a_tensor_scale [1] or
  *     [num_experts] (a_scale_per_expert).
  *   w_codes [num_experts * N, K/2] (expert e's rows e*N..), w_scales TCGEN05 over
- *     the same num_experts*N rows, w_tensor_scale [num_experts].
+ *     the same num_experts*N rows, w_tensor_scale [num_experts]; w_codes_t /
+ *     w_scales_t its column-major copy per expert (required with compensation).
  *   r_codes NULL -> plain; else [rows_capacity, kpad/2] + TCGEN05 scales,
  *     r_tensor_scale [1] or [num_experts] (r_scale_per_expert); sel [k] shared
  *     (sel_per_expert = 0) or [num_experts, k].
@@ -228,6 +239,9 @@ quads_status_t quads_w4a4_gemm_comp(int64_t M, int64_t N, int64_t K, const uint8
  *     count are not written.  SWIGLU: W's 128-row tiles hold 64 gate rows then
  *     the matching 64 up rows; y bf16 [rows_capacity, N/2] gets
  *     silu(g) * u, and padding rows of each group are written as 0.
+ *   y_amax nullable device float [num_experts]: set to the largest |stored
+ *     output| of each expert (zeroed by this call first) -- the tensor amax
+ *     the next quantization needs, computed in the epilogue.
  * N % 128 == 0, K % 64 == 0.
  */
 quads_status_t quads_moe_grouped_gemm(
@@ -235,10 +249,26 @@ quads_status_t quads_moe_grouped_gemm(
     const int32_t* expert_offsets, const int32_t* expert_counts, const uint8_t* a_codes,
     const uint8_t* a_scales, const float* a_tensor_scale, int32_t a_scale_per_expert,
     const uint8_t* w_codes, const uint8_t* w_scales, const float* w_tensor_scale,
-    const uint8_t* r_codes, const uint8_t* r_scales, const float* r_tensor_scale,
-    int32_t r_scale_per_expert, const int32_t* sel, int32_t sel_per_expert, int32_t k,
-    int32_t epilogue, void* y, int32_t y_dtype, int64_t ldy, void* workspace,
-    size_t workspace_bytes, void* stream);
+    const uint8_t* w_codes_t, const uint8_t* w_scales_t, const uint8_t* r_codes,
+    const uint8_t* r_scales, const float* r_tensor_scale, int32_t r_scale_per_expert,
+    const int32_t* sel, int32_t sel_per_expert, int32_t k, int32_t epilogue, void* y,
+    int32_t y_dtype, int64_t ldy, float* y_amax, void* workspace, size_t workspace_bytes,
+    void* stream);
+
+/*
+ * quads_weight_columns -- column-major copy of NVFP4 weights, made once per
+ * weight update, from which the selected input channels are gathered with
+ * contiguous reads (the selection changes every batch, the weights do not).
+ * For each of num_groups stacked matrices of rows_per_group rows:
+ *   codes_t [num_groups][cols][rows_per_group/2]: byte (c, n/2) holds the codes
+ *     of rows n (low nibble) and n+1 (high nibble) at column c;
+ *   scales_t [num_groups][cols/16][rows_per_group]: the block-scale byte.
+ * Input: w_codes [num_groups*rows_per_group, cols/2], w_scales TCGEN05.
+ * rows_per_group % 128 == 0, cols % 64 == 0.
+ */
+quads_status_t quads_weight_columns(const uint8_t* w_codes, const uint8_t* w_scales,
+                                    int32_t num_groups, int64_t rows_per_group, int64_t cols,
+                                    uint8_t* codes_t, uint8_t* scales_t, void* stream);
 
 /*
  * quads_trace_round -- TRACE rollout-guided rounding ([TRACE] "核心方法", Eq. (3)):
@@ -273,12 +303,13 @@ quads_status_t quads_trace_round(const void* x_train, int64_t rows, int64_t cols
  *   row_token int32 [rows_capacity] (-1 on padding rows), token_row int32
  *   [tokens, topk] (row of each slot).
  *   rows_capacity >= tokens*topk + num_experts*127 (checked on the host).
+ *   workspace >= quads_workspace_size(QUADS_OP_MOE_ROUTE, tokens, num_experts, 0, 0, 1).
  */
 quads_status_t quads_moe_route(const float* logits, int32_t tokens, int32_t num_experts,
                                int32_t topk, int32_t* topk_idx, float* gates,
                                int32_t* expert_counts, int32_t* expert_offsets,
                                int32_t* row_token, int32_t* token_row, int64_t rows_capacity,
-                               void* stream);
+                               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * quads_moe_gather -- copy NVFP4 rows into expert order: row r of the output is

@@ -14,7 +14,8 @@
 //   warp 1     TMEM allocator + MMA issuer (one thread): tcgen05.cp moves the
 //              stage's scale atoms into TMEM, then tcgen05.mma
 //              .kind::mxf4nvf4.block_scale.scale_vec::4X (M=128, N=128, K=64).
-//   warps 2-5  epilogue: tcgen05.ld of both accumulators, scale, store.
+//   warps 2-9  epilogue: tcgen05.ld of both accumulators, scale, store; two
+//              warps per TMEM lane quadrant, each owning half of the columns.
 // TMEM columns: acc1 double-buffered (0-127, 128-255), acc2 (256-383),
 // scale-factor ring (384-511, 4 buffers x 32 columns).
 // Every mbarrier wait is bounded; on timeout the kernel latches an error word,
@@ -37,7 +38,8 @@ constexpr int A_TILE = BM * BK_BYTES;         // 16 KB
 constexpr int B_TILE = BN * BK_BYTES;         // 16 KB
 constexpr int SF_TILE = 4 * 512;              // 4 atoms (128 rows x 16 blocks)
 constexpr int STAGE_BYTES = A_TILE + B_TILE + 2 * SF_TILE;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 320;               // 10 warps: producer, MMA, 8 epilogue
+constexpr int EPI_THREADS = 256;
 constexpr int TMEM_COLS = 512;
 constexpr int ACC2_COL = 256;
 constexpr int SF_COL = 384;
@@ -63,6 +65,7 @@ struct Params {
   void* y;
   int64_t ldy;
   int out_mode;
+  uint32_t* y_amax;             // nullable [E]: max |stored y| per group (float bits)
   int* err;
 };
 
@@ -264,7 +267,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
     for (int i = 0; i < 4; ++i) mbar_init(&sf_free[i], 1);
-    for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 128); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], EPI_THREADS); }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -376,7 +379,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
-    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    const int quad = warp & 3;         // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;  // which half of the tile's columns
     const int row_in_tile = quad * 32 + lane;
     uint32_t j = 0;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++j) {
@@ -395,12 +399,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
       const uint32_t t1 = tmem + lane_base + b * BN;
       const uint32_t t2 = tmem + lane_base + ACC2_COL;
+      float amax = 0.0f;
       if (p.out_mode == OUT_SWIGLU) {
-        // tile columns [0,64) are gate rows of W, [64,128) the matching up rows
+        // tile columns [0,64) are gate rows of W, [64,128) the matching up rows;
+        // this warp produces h columns [32*half, 32*half + 32) of the tile
         const bool store = row < (p.row_off ? (int64_t)p.row_off[tl.e + 1] : p.M);
         __nv_bfloat16* y = (__nv_bfloat16*)p.y + row * p.ldy + tl.n0 / 2;
 #pragma unroll 1
-        for (int c0 = 0; c0 < 64; c0 += 16) {
+        for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
           float g1[16], u1[16], g2[16], u2[16];
           tc_ld16(t1 + c0, g1);
           tc_ld16(t1 + 64 + c0, u1);
@@ -414,10 +420,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int q = 0; q < 2; ++q) {
               float g = a1 * g1[i + q], u = a1 * u1[i + q];
               if (p.comp) { g = fmaf(a2, g2[i + q], g); u = fmaf(a2, u2[i + q], u); }
-              h[q] = g / (1.0f + expf(-g)) * u;
+              h[q] = __fdividef(g * u, 1.0f + __expf(-g));   // silu(g) * u
             }
             __nv_bfloat162 hb = __floats2bfloat162_rn(h[0], h[1]);
             packed[i / 2] = *reinterpret_cast<uint32_t*>(&hb);
+            const float2 hr = __bfloat1622float2(hb);
+            amax = fmaxf(amax, fmaxf(fabsf(hr.x), fabsf(hr.y)));
           }
           if (store) {
             uint4* dst = reinterpret_cast<uint4*>(y + c0);
@@ -425,10 +433,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
           }
         }
+        if (!store) amax = 0.0f;
       } else {
         const bool store = row < tl.row_end;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 16) {
+        for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
           float v1[16], v2[16];
           tc_ld16(t1 + c0, v1);
           if (p.comp) tc_ld16(t2 + c0, v2);
@@ -442,12 +451,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
               for (int i = 0; i < 4; ++i)
                 dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(o[i]));
             } else {
               uint32_t packed[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 __nv_bfloat162 hb = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
                 packed[i] = *reinterpret_cast<uint32_t*>(&hb);
+                const float2 hr = __bfloat1622float2(hb);
+                amax = fmaxf(amax, fmaxf(fabsf(hr.x), fabsf(hr.y)));
               }
               uint4* dst = reinterpret_cast<uint4*>((__nv_bfloat16*)p.y + row * p.ldy + tl.n0 + c0);
               dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
@@ -458,6 +471,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_before();
       mbar_arrive(&acc_empty[b]);
+      if (p.y_amax) {
+        amax = warp_max(amax);
+        if (lane == 0 && amax > 0.0f) atomicMax(&p.y_amax[tl.e], __float_as_uint(amax));
+      }
     }
   }
   __syncthreads();
@@ -469,32 +486,65 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ---------------------------------------------------------------- Q(W_sel)
-// For every weight row n (of every expert) and every 16-block of the selected
+// Column-major copy of an NVFP4 weight, made once per weight update: for group
+// g (rows g*N .. g*N+N-1), codes_t[g][c][n/2] holds the codes of rows n, n+1 at
+// column c (n even -> low nibble) and scales_t[g][c/16][n] the block scale, so
+// the k selected columns are read as k contiguous runs.
+__global__ void __launch_bounds__(256) wtrans_kernel(const uint8_t* __restrict__ wc,
+                                                     const uint8_t* __restrict__ wsf, int G, int N,
+                                                     int K, uint8_t* __restrict__ ct,
+                                                     uint8_t* __restrict__ st) {
+  const int64_t nbytes = (int64_t)G * K * (N / 2);
+  const int64_t nsc = (int64_t)G * (K / 16) * N;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nbytes + nsc;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    if (i < nbytes) {
+      const int64_t np = i % (N / 2);
+      const int64_t c = (i / (N / 2)) % K;
+      const int64_t g = i / ((int64_t)(N / 2) * K);
+      const int64_t r0 = g * N + 2 * np;
+      const uint32_t b0 = wc[r0 * (K / 2) + c / 2], b1 = wc[(r0 + 1) * (K / 2) + c / 2];
+      const uint32_t sh = (c & 1) * 4;
+      ct[i] = (uint8_t)(((b0 >> sh) & 15u) | (((b1 >> sh) & 15u) << 4));
+    } else {
+      const int64_t j = i - nbytes;
+      const int64_t n = j % N;
+      const int64_t cb = (j / N) % (K / 16);
+      const int64_t g = j / ((int64_t)N * (K / 16));
+      st[j] = wsf[sf_tc_offset(g * N + n, cb, K / 16)];
+    }
+  }
+}
+
+// For every weight row r (of every expert) and every 16-block of the selected
 // channels: gather the selected columns of DQ(Q(W)) in units of s_w
 // (level * E4M3 scale, exact), requantize with tensor scale 1 (s_w kept).
+// Reads the column-major copy (consecutive threads = consecutive rows).
 // Output codes [E*N, kpad/2] and TCGEN05 scales over kpad columns.
 __global__ void __launch_bounds__(256) wsel_kernel(
-    const uint8_t* __restrict__ wc, const uint8_t* __restrict__ wsf, int64_t rows /*E*N*/, int N,
+    const uint8_t* __restrict__ ct, const uint8_t* __restrict__ st, int64_t rows /*E*N*/, int N,
     int K, const int32_t* __restrict__ sel, int sel_pe, int k, int kpad,
     uint8_t* __restrict__ oc, uint8_t* __restrict__ osf) {
   const int nb = kpad >> 4;
   const int64_t total = rows * nb;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / nb;
-    const int blk = (int)(i % nb);
+    const int64_t r = i % rows;
+    const int blk = (int)(i / rows);
     uint32_t lo = 0, hi = 0, sbyte = 0;
     if (blk * 16 < k) {
-      const int e = (int)(r / N);
-      const int32_t* s = sel + (sel_pe ? (int64_t)e * k : 0) + blk * 16;
+      const int64_t e = r / N, n = r % N;
+      const int32_t* s = sel + (sel_pe ? e * k : 0) + blk * 16;
+      const uint8_t* cte = ct + e * (int64_t)K * (N / 2) + n / 2;
+      const uint8_t* ste = st + e * (int64_t)(K / 16) * N + n;
+      const uint32_t sh = (n & 1) * 4;
       float w[16];
       float m = 0.0f;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int c = s[j];
-        const uint32_t byte = wc[r * (K >> 1) + (c >> 1)];
-        const uint32_t code = (c & 1) ? (byte >> 4) : (byte & 15u);
-        const float sc = e4m3_to_f32(wsf[sf_tc_offset(r, c >> 4, K >> 4)]);
+        const uint32_t code = (cte[(int64_t)c * (N / 2)] >> sh) & 15u;
+        const float sc = e4m3_to_f32(ste[(int64_t)(c >> 4) * N]);
         w[j] = __fmul_rn(e2m1_to_f32(code), sc);
         m = fmaxf(m, fabsf(w[j]));
       }
@@ -503,8 +553,7 @@ __global__ void __launch_bounds__(256) wsel_kernel(
       hi = quantize8(w + 8, bs);
       sbyte = bs.byte;
     }
-    uint2* dst = reinterpret_cast<uint2*>(oc + r * (kpad >> 1) + blk * 8);
-    *dst = make_uint2(lo, hi);
+    *reinterpret_cast<uint2*>(oc + r * (kpad >> 1) + blk * 8) = make_uint2(lo, hi);
     osf[sf_tc_offset(r, blk, nb)] = (uint8_t)sbyte;
   }
 }
@@ -546,7 +595,7 @@ struct Launch {
   int E, N, K, k, kpad;
   const int32_t* row_off;
   const int32_t* row_cnt;
-  const uint8_t *a, *a_sf, *b, *b_sf, *r, *r_sf;
+  const uint8_t *a, *a_sf, *b, *b_sf, *b_t, *b_sf_t, *r, *r_sf;
   const float *a_ts, *b_ts, *r_ts;
   int a_pe, r_pe;
   const int32_t* sel;
@@ -554,6 +603,7 @@ struct Launch {
   void* y;
   int64_t ldy;
   int out_mode;
+  float* y_amax;
   void* ws;
   size_t ws_bytes;
   cudaStream_t stream;
@@ -573,8 +623,8 @@ static quads_status_t launch(const Launch& L) {
     ws_sf = ws_codes + (((size_t)brows * (L.kpad / 2) + 1023) & ~(size_t)1023);
     const int64_t total = brows * (L.kpad / 16);
     int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)num_sms() * 16);
-    wsel_kernel<<<blocks, 256, 0, L.stream>>>(L.b, L.b_sf, brows, L.N, L.K, L.sel, L.sel_pe, L.k,
-                                               L.kpad, ws_codes, ws_sf);
+    wsel_kernel<<<blocks, 256, 0, L.stream>>>(L.b_t, L.b_sf_t, brows, L.N, L.K, L.sel, L.sel_pe,
+                                               L.k, L.kpad, ws_codes, ws_sf);
   }
   CUtensorMap tA, tB, tR, tW;
   const int64_t arows = L.row_off ? L.rows_cap : L.M;
@@ -595,6 +645,8 @@ static quads_status_t launch(const Launch& L) {
   p.a_ts = L.a_ts; p.b_ts = L.b_ts; p.r_ts = L.r_ts; p.a_ts_pe = L.a_pe; p.r_ts_pe = L.r_pe;
   p.comp = comp ? 1 : 0;
   p.y = L.y; p.ldy = L.ldy; p.out_mode = L.out_mode;
+  p.y_amax = (uint32_t*)L.y_amax;
+  if (L.y_amax) cudaMemsetAsync(L.y_amax, 0, (size_t)L.E * 4, L.stream);
   static int* errp = nullptr;
   if (!errp && cudaGetSymbolAddress((void**)&errp, g_gemm_error) != cudaSuccess)
     return fail(QUADS_ERR_CUDA, "gemm: cannot resolve the device error word");
@@ -630,6 +682,7 @@ extern "C" quads_status_t quads_w4a4_gemm_comp(int64_t M, int64_t N, int64_t K,
                                                const uint8_t* a_codes, const uint8_t* a_scales,
                                                const float* a_tensor_scale, const uint8_t* w_codes,
                                                const uint8_t* w_scales, const float* w_tensor_scale,
+                                               const uint8_t* w_codes_t, const uint8_t* w_scales_t,
                                                const uint8_t* r_codes, const uint8_t* r_scales,
                                                const float* r_tensor_scale, const int32_t* sel,
                                                int32_t k, void* y, int32_t y_dtype, int64_t ldy,
@@ -648,17 +701,20 @@ extern "C" quads_status_t quads_w4a4_gemm_comp(int64_t M, int64_t N, int64_t K,
   if (!al16(a_codes) || !al16(w_codes) || !al16(a_scales) || !al16(w_scales) || !al16(y) ||
       (r_codes && (!al16(r_codes) || !al16(r_scales))))
     return fail(QUADS_ERR_MISALIGNED, "gemm: operands must be 16-byte aligned");
-  if (r_codes && (!r_scales || !r_tensor_scale || !sel || k <= 0 || k % 16 || k > K))
-    return fail(QUADS_ERR_INVALID_ARG, "gemm: compensation needs r_scales, r_tensor_scale, sel and 16<=k<=K, k%%16==0");
+  if (r_codes && (!r_scales || !r_tensor_scale || !sel || !w_codes_t || !w_scales_t || k <= 0 ||
+                  k % 16 || k > K))
+    return fail(QUADS_ERR_INVALID_ARG, "gemm: compensation needs r_scales, r_tensor_scale, sel, the column-major weight copy and 16<=k<=K, k%%16==0");
   gemm::Launch L{};
   L.M = M; L.rows_cap = M; L.E = 1; L.N = (int)N; L.K = (int)K; L.k = k;
   L.kpad = r_codes ? quads_kpad(k) : 0;
   L.row_off = nullptr; L.row_cnt = nullptr;
   L.a = a_codes; L.a_sf = a_scales; L.b = w_codes; L.b_sf = w_scales;
+  L.b_t = w_codes_t; L.b_sf_t = w_scales_t;
   L.r = r_codes; L.r_sf = r_scales;
   L.a_ts = a_tensor_scale; L.b_ts = w_tensor_scale; L.r_ts = r_tensor_scale;
   L.a_pe = 0; L.r_pe = 0; L.sel = sel; L.sel_pe = 0;
   L.y = y; L.ldy = ldy; L.out_mode = y_dtype == QUADS_OUT_F32 ? gemm::OUT_F32 : gemm::OUT_BF16;
+  L.y_amax = nullptr;
   L.ws = workspace; L.ws_bytes = workspace_bytes; L.stream = (cudaStream_t)stream;
   return gemm::launch(L);
 }
@@ -668,9 +724,10 @@ extern "C" quads_status_t quads_moe_grouped_gemm(
     const int32_t* expert_offsets, const int32_t* expert_counts, const uint8_t* a_codes,
     const uint8_t* a_scales, const float* a_tensor_scale, int32_t a_scale_per_expert,
     const uint8_t* w_codes, const uint8_t* w_scales, const float* w_tensor_scale,
+    const uint8_t* w_codes_t, const uint8_t* w_scales_t,
     const uint8_t* r_codes, const uint8_t* r_scales, const float* r_tensor_scale,
     int32_t r_scale_per_expert, const int32_t* sel, int32_t sel_per_expert, int32_t k,
-    int32_t epilogue, void* y, int32_t y_dtype, int64_t ldy, void* workspace,
+    int32_t epilogue, void* y, int32_t y_dtype, int64_t ldy, float* y_amax, void* workspace,
     size_t workspace_bytes, void* stream) {
   if (!expert_offsets || !a_codes || !a_scales || !a_tensor_scale || !w_codes || !w_scales ||
       !w_tensor_scale || !y)
@@ -688,19 +745,36 @@ extern "C" quads_status_t quads_moe_grouped_gemm(
   if (!al16(a_codes) || !al16(w_codes) || !al16(a_scales) || !al16(w_scales) || !al16(y) ||
       (r_codes && (!al16(r_codes) || !al16(r_scales))))
     return fail(QUADS_ERR_MISALIGNED, "moe_gemm: operands must be 16-byte aligned");
-  if (r_codes && (!r_scales || !r_tensor_scale || !sel || k <= 0 || k % 16 || k > K))
-    return fail(QUADS_ERR_INVALID_ARG, "moe_gemm: compensation needs r_scales, r_tensor_scale, sel and valid k");
+  if (r_codes && (!r_scales || !r_tensor_scale || !sel || !w_codes_t || !w_scales_t || k <= 0 ||
+                  k % 16 || k > K))
+    return fail(QUADS_ERR_INVALID_ARG, "moe_gemm: compensation needs r_scales, r_tensor_scale, sel, the column-major weight copy and valid k");
   gemm::Launch L{};
   L.M = rows_capacity; L.rows_cap = rows_capacity; L.E = num_experts; L.N = (int)N; L.K = (int)K;
   L.k = k; L.kpad = r_codes ? quads_kpad(k) : 0;
   L.row_off = expert_offsets; L.row_cnt = expert_counts;
   L.a = a_codes; L.a_sf = a_scales; L.b = w_codes; L.b_sf = w_scales;
+  L.b_t = w_codes_t; L.b_sf_t = w_scales_t;
   L.r = r_codes; L.r_sf = r_scales;
   L.a_ts = a_tensor_scale; L.b_ts = w_tensor_scale; L.r_ts = r_tensor_scale;
   L.a_pe = a_scale_per_expert; L.r_pe = r_scale_per_expert; L.sel = sel; L.sel_pe = sel_per_expert;
-  L.y = y; L.ldy = ldy;
+  L.y = y; L.ldy = ldy; L.y_amax = y_amax;
   L.out_mode = epilogue == QUADS_EPILOGUE_SWIGLU ? gemm::OUT_SWIGLU
                : (y_dtype == QUADS_OUT_F32 ? gemm::OUT_F32 : gemm::OUT_BF16);
   L.ws = workspace; L.ws_bytes = workspace_bytes; L.stream = (cudaStream_t)stream;
   return gemm::launch(L);
+}
+
+extern "C" quads_status_t quads_weight_columns(const uint8_t* w_codes, const uint8_t* w_scales,
+                                               int32_t num_groups, int64_t rows_per_group,
+                                               int64_t cols, uint8_t* codes_t, uint8_t* scales_t,
+                                               void* stream) {
+  if (!w_codes || !w_scales || !codes_t || !scales_t)
+    return fail(QUADS_ERR_INVALID_ARG, "weight_columns: null pointer argument");
+  if (num_groups < 1 || rows_per_group <= 0 || rows_per_group % 128 || cols <= 0 || cols % 64)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "weight_columns: rows_per_group %% 128 and cols %% 64");
+  const int64_t total = (int64_t)num_groups * cols * (rows_per_group / 2 + rows_per_group / 16);
+  const int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)num_sms() * 32);
+  gemm::wtrans_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(
+      w_codes, w_scales, num_groups, (int)rows_per_group, (int)cols, codes_t, scales_t);
+  return check_launch("weight_columns", 1);
 }

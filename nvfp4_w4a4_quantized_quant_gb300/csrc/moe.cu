@@ -16,63 +16,78 @@ namespace quads {
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopk = 16;
 
-// One warp per token.  Lane l holds logits l, l+32, ...; each of topk rounds
-// takes the warp arg-max (ties -> lower expert id) and removes it.
+// One warp per token.  Lane l holds logits l, l+32, ...; round r takes the
+// warp arg-max (ties -> lower expert id), removes it, and lane r keeps it.
+// The chosen experts are then ranked by id (ascending slot order), gates are
+// exp(l - lmax) / sum over the chosen, the token's expert set is written as a
+// bit mask, and per-expert counts go through a shared-memory histogram.
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T,
                                                     int E, int topk, int32_t* __restrict__ idx,
                                                     float* __restrict__ gates,
-                                                    int32_t* __restrict__ counts) {
+                                                    int32_t* __restrict__ counts,
+                                                    uint32_t* __restrict__ emask) {
+  __shared__ int hist[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
   const int lane = threadIdx.x & 31;
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (t >= T) return;
-  float v[kMaxExperts / 32];
-  const int per = (E + 31) / 32;
-#pragma unroll
-  for (int i = 0; i < kMaxExperts / 32; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = (i < per && e < E) ? logits[(int64_t)t * E + e] : -INFINITY;
-  }
-  uint32_t taken = 0;
-  int chosen[kMaxTopk];
-  float chosen_l[kMaxTopk];
-  for (int r = 0; r < topk; ++r) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
+  const int words = (E + 31) >> 5;
+  if (t < T) {
+    float v[kMaxExperts / 32];
+    const int per = words;
 #pragma unroll
     for (int i = 0; i < kMaxExperts / 32; ++i) {
       const int e = lane + 32 * i;
-      if (i < per && e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
-        bv = v[i];
-        be = e;
-      }
+      v[i] = (i < per && e < E) ? logits[(int64_t)t * E + e] : -INFINITY;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-    }
-    chosen[r] = be;
-    chosen_l[r] = bv;
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-  }
-  if (lane == 0) {
-    // gates: exp(l - lmax) / sum over the chosen, lmax = the first pick
-    float p[kMaxTopk];
-    float s = 0.0f;
-    for (int r = 0; r < topk; ++r) { p[r] = expf(chosen_l[r] - chosen_l[0]); s += p[r]; }
-    // emit in ascending expert order (insertion sort of <= 16 entries)
-    for (int a = 1; a < topk; ++a)
-      for (int b = a; b > 0 && chosen[b - 1] > chosen[b]; --b) {
-        int te = chosen[b]; chosen[b] = chosen[b - 1]; chosen[b - 1] = te;
-        float tp = p[b]; p[b] = p[b - 1]; p[b - 1] = tp;
-      }
+    uint32_t taken = 0;
+    int my_e = 0x7fffffff;
+    float my_l = -INFINITY, lmax = -INFINITY;
     for (int r = 0; r < topk; ++r) {
-      idx[(int64_t)t * topk + r] = chosen[r];
-      gates[(int64_t)t * topk + r] = p[r] / s;
-      atomicAdd(&counts[chosen[r]], 1);
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < kMaxExperts / 32; ++i) {
+        const int e = lane + 32 * i;
+        if (i < per && e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
+          bv = v[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+      }
+      if (r == 0) lmax = bv;
+      if (lane == r) { my_e = be; my_l = bv; }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    }
+    const bool mine = lane < topk;
+    float p = mine ? expf(my_l - lmax) : 0.0f;
+    float s = p;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    int rank = 0;
+    for (int j = 0; j < topk; ++j) {
+      const int ej = __shfl_sync(0xffffffffu, my_e, j);
+      rank += (ej < my_e) ? 1 : 0;
+    }
+    if (mine) {
+      idx[(int64_t)t * topk + rank] = my_e;
+      gates[(int64_t)t * topk + rank] = p / s;
+      atomicAdd(&hist[my_e], 1);
+    }
+    for (int w = 0; w < words; ++w) {
+      const uint32_t bit = (mine && (my_e >> 5) == w) ? (1u << (my_e & 31)) : 0u;
+      const uint32_t m = __reduce_or_sync(0xffffffffu, bit);
+      if (lane == 0) emask[(int64_t)t * words + w] = m;
     }
   }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (hist[e]) atomicAdd(&counts[e], hist[e]);
 }
 
 // Padded offsets: off[e+1] = off[e] + roundup(count[e], 128).  One block.
@@ -88,26 +103,30 @@ __global__ void plan_kernel(const int32_t* __restrict__ counts, int E, int32_t* 
   }
 }
 
-// One block per expert: scan the tokens in order; a token routed to the expert
-// gets the next row of its group.  Padding rows get row_token = -1.
-__global__ void __launch_bounds__(1024) assign_kernel(const int32_t* __restrict__ idx, int T,
-                                                      int topk, const int32_t* __restrict__ off,
+// One block per expert: scan the tokens in order (one bit of the token's expert
+// mask each); a token routed to the expert gets the next row of its group and
+// its slot is the number of its experts with a lower id.  Padding rows get
+// row_token = -1.
+__global__ void __launch_bounds__(1024) assign_kernel(const uint32_t* __restrict__ emask, int T,
+                                                      int E, int topk,
+                                                      const int32_t* __restrict__ off,
                                                       const int32_t* __restrict__ counts,
                                                       int32_t* __restrict__ row_token,
                                                       int32_t* __restrict__ token_row) {
   __shared__ int warp_tot[32];
   __shared__ int base_s;
   const int e = blockIdx.x;
+  const int words = (E + 31) >> 5;
+  const int ew = e >> 5;
+  const uint32_t ebit = 1u << (e & 31);
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   if (threadIdx.x == 0) base_s = 0;
   __syncthreads();
+  const int e0 = off[e];
   for (int t0 = 0; t0 < T; t0 += blockDim.x) {
     const int t = t0 + threadIdx.x;
-    int slot = -1;
-    if (t < T)
-      for (int j = 0; j < topk; ++j)
-        if (idx[(int64_t)t * topk + j] == e) slot = j;
-    const int f = slot >= 0 ? 1 : 0;
+    const uint32_t word = t < T ? emask[(int64_t)t * words + ew] : 0u;
+    const int f = (word & ebit) ? 1 : 0;
     const unsigned bal = __ballot_sync(0xffffffffu, f);
     const int pre = __popc(bal & ((1u << lane) - 1u));
     if (lane == 0) warp_tot[w] = __popc(bal);
@@ -115,7 +134,9 @@ __global__ void __launch_bounds__(1024) assign_kernel(const int32_t* __restrict_
     int wbase = 0;
     for (int i = 0; i < w; ++i) wbase += warp_tot[i];
     if (f) {
-      const int row = off[e] + base_s + wbase + pre;
+      int slot = __popc(word & (ebit - 1u));
+      for (int i = 0; i < ew; ++i) slot += __popc(emask[(int64_t)t * words + i]);
+      const int row = e0 + base_s + wbase + pre;
       row_token[row] = t;
       token_row[(int64_t)t * topk + slot] = row;
     }
@@ -127,7 +148,7 @@ __global__ void __launch_bounds__(1024) assign_kernel(const int32_t* __restrict_
     }
     __syncthreads();
   }
-  for (int r = off[e] + counts[e] + threadIdx.x; r < off[e + 1]; r += blockDim.x) row_token[r] = -1;
+  for (int r = e0 + counts[e] + threadIdx.x; r < off[e + 1]; r += blockDim.x) row_token[r] = -1;
 }
 
 // One warp per output row: codes (16 B per lane-iteration), then the row's
@@ -199,7 +220,8 @@ extern "C" quads_status_t quads_moe_route(const float* logits, int32_t tokens, i
                                           int32_t topk, int32_t* topk_idx, float* gates,
                                           int32_t* expert_counts, int32_t* expert_offsets,
                                           int32_t* row_token, int32_t* token_row,
-                                          int64_t rows_capacity, void* stream) {
+                                          int64_t rows_capacity, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
   if (!logits || !topk_idx || !gates || !expert_counts || !expert_offsets || !row_token || !token_row)
     return fail(QUADS_ERR_INVALID_ARG, "moe_route: null pointer argument");
   if (tokens < 0 || num_experts < 1 || num_experts > kMaxExperts || topk < 1 ||
@@ -207,13 +229,17 @@ extern "C" quads_status_t quads_moe_route(const float* logits, int32_t tokens, i
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "moe_route: need 1<=experts<=256, 1<=topk<=min(16, experts)");
   if (rows_capacity < (int64_t)tokens * topk + (int64_t)num_experts * (QUADS_MOE_ROW_ALIGN - 1))
     return fail(QUADS_ERR_INVALID_ARG, "moe_route: rows_capacity too small");
+  const size_t need = quads_workspace_size(QUADS_OP_MOE_ROUTE, tokens, num_experts, 0, topk, 1);
+  if (!workspace || workspace_bytes < need)
+    return fail(QUADS_ERR_WORKSPACE, "moe_route: workspace needs %zu bytes", need);
+  uint32_t* emask = (uint32_t*)workspace;
   cudaStream_t st = (cudaStream_t)stream;
   cudaMemsetAsync(expert_counts, 0, (size_t)num_experts * 4, st);
   if (tokens > 0)
     route_kernel<<<(tokens * 32 + 255) / 256, 256, 0, st>>>(logits, tokens, num_experts, topk,
-                                                             topk_idx, gates, expert_counts);
+                                                             topk_idx, gates, expert_counts, emask);
   plan_kernel<<<1, kMaxExperts, 0, st>>>(expert_counts, num_experts, expert_offsets);
-  assign_kernel<<<num_experts, 1024, 0, st>>>(topk_idx, tokens, topk, expert_offsets,
+  assign_kernel<<<num_experts, 1024, 0, st>>>(emask, tokens, num_experts, topk, expert_offsets,
                                               expert_counts, row_token, token_row);
   return check_launch("moe_route", tokens > 0 ? 3 : 2);
 }

@@ -20,7 +20,8 @@ namespace quads {
 static __device__ int g_quant_error;  // device-side argument check failures
 
 // ---------------------------------------------------------------- amax
-// One block per 32-row chunk (inside one group), threads over (row, 8-col vector).
+// One block per 32-row chunk (inside one group), threads over (row, 8-col
+// vector), eight 16-byte loads in flight per thread.
 __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restrict__ x,
                                                    int64_t rows, int cols, int64_t ldx,
                                                    const int32_t* __restrict__ row_index,
@@ -37,15 +38,25 @@ __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restri
     if (goff && r1 > goff[g + 1]) atomicExch(&g_quant_error, QUADS_ERR_DEVICE_CHECK);
     float m = 0.0f;
     const int total = (int)(r1 - r0) * vec_per_row;
-    for (int i = threadIdx.x; i < total; i += blockDim.x) {
-      const int64_t r = r0 + i / vec_per_row;
-      const int v = i % vec_per_row;
-      const int64_t src = row_index ? (int64_t)row_index[r] : r;
-      uint4 u = __ldg(reinterpret_cast<const uint4*>(x + src * ldx) + v);
-      float f[8];
-      bf16x8_to_f32(u, f);
+    for (int i0 = threadIdx.x; i0 < total; i0 += 8 * blockDim.x) {
+      uint4 u[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
+      for (int q = 0; q < 8; ++q) {
+        const int i = i0 + q * blockDim.x;
+        u[q] = make_uint4(0, 0, 0, 0);
+        if (i < total) {
+          const int64_t r = r0 + i / vec_per_row;
+          const int64_t src = row_index ? (int64_t)row_index[r] : r;
+          u[q] = __ldg(reinterpret_cast<const uint4*>(x + src * ldx) + (i % vec_per_row));
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float f[8];
+        bf16x8_to_f32(u[q], f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
+      }
     }
     m = warp_max(m);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
@@ -69,7 +80,38 @@ __global__ void tensor_scale_kernel(const uint32_t* __restrict__ amax_bits, int 
 // A warp owns one (32-row chunk, 256-column slab) task: lane l holds columns
 // slab*256 + 8l .. +7 and walks the chunk's rows in order, so the residual
 // energy of its 8 columns is summed row by row in float32 (the fixed order the
-// score definition uses).  Lanes 2i and 2i+1 form one 16-element block.
+// score definition uses).  Lanes 2i and 2i+1 form one 16-element block.  Loads
+// of the next 4 rows are issued before the current 4 are processed.
+template <bool kScores>
+__device__ __forceinline__ void quantize_row(const uint4& raw, float s_t, int lane, bool active,
+                                             int64_t row, int col, int ncols16, uint8_t* codes,
+                                             int64_t ldc, uint8_t* scales, int layout,
+                                             float2* acc) {
+  float f[8];
+  bf16x8_to_f32(raw, f);
+  float m = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  const BlockScale bs = block_scale(m, s_t);
+  const uint32_t c = quantize8(f, bs);
+  if (active) {
+    *reinterpret_cast<uint32_t*>(codes + row * ldc + (col >> 1)) = c;
+    if ((lane & 1) == 0) scales[sf_offset(layout, row, col >> 4, ncols16)] = (uint8_t)bs.byte;
+  }
+  if (kScores) {
+    float lv[8];
+    e2m1x8_to_f32(c, lv);
+    const float2 d2 = make_float2(bs.d, bs.d);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 dq = __fmul2_rn(make_float2(lv[2 * j], lv[2 * j + 1]), d2);
+      const float2 R = __fadd2_rn(make_float2(f[2 * j], f[2 * j + 1]), make_float2(-dq.x, -dq.y));
+      acc[j] = __fadd2_rn(acc[j], __fmul2_rn(R, R));
+    }
+  }
+}
+
 template <bool kScores>
 __global__ void __launch_bounds__(256) quantize_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
@@ -94,11 +136,10 @@ __global__ void __launch_bounds__(256) quantize_kernel(
     int g = goff ? group_of(goff, G, r0) : 0;
     int64_t gend = goff ? (int64_t)goff[g + 1] : end;
     float s_t = st[g];
-    float acc[8];
+    float2 acc[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-    for (int64_t r = r0; r < r1; r += 4) {
-      uint4 u[4];
+    for (int j = 0; j < 4; ++j) acc[j] = make_float2(0.0f, 0.0f);
+    auto load4 = [&](int64_t r, uint4* u) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         u[q] = make_uint4(0, 0, 0, 0);
@@ -107,6 +148,11 @@ __global__ void __launch_bounds__(256) quantize_kernel(
           u[q] = __ldg(reinterpret_cast<const uint4*>(x + src * ldx + col));
         }
       }
+    };
+    uint4 cur[4], nxt[4];
+    load4(r0, cur);
+    for (int64_t r = r0; r < r1; r += 4) {
+      if (r + 4 < r1) load4(r + 4, nxt);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int64_t row = r + q;
@@ -116,64 +162,73 @@ __global__ void __launch_bounds__(256) quantize_kernel(
           gend = goff[g + 1];
           s_t = st[g];
         }
-        float f[8];
-        bf16x8_to_f32(u[q], f);
-        float m = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        const BlockScale bs = block_scale(m, s_t);
-        const uint32_t c = quantize8(f, bs);
-        if (active) {
-          *reinterpret_cast<uint32_t*>(codes + row * ldc + (col >> 1)) = c;
-          if ((lane & 1) == 0) scales[sf_offset(layout, row, col >> 4, ncols16)] = (uint8_t)bs.byte;
-        }
-        if (kScores) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float dq = __fmul_rn(e2m1_to_f32((c >> (4 * j)) & 15u), bs.d);
-            const float R = __fsub_rn(f[j], dq);
-            acc[j] = __fadd_rn(acc[j], __fmul_rn(R, R));
-          }
-        }
+        quantize_row<kScores>(cur[q], s_t, lane, active, row, col, ncols16, codes, ldc, scales,
+                              layout, acc);
       }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
     }
     if (kScores && active) {
       float4* p = reinterpret_cast<float4*>(partials + chunk * cols + col);
-      p[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      p[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      p[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+      p[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
     }
   }
 }
 
 // ---------------------------------------------------------------- select
-// One block per group: scores = ordered sum of the group's chunk partials;
-// bitonic sort of (score, ~index) keys descending; mark the top k; compact
-// the marked channels in ascending order.
-__global__ void __launch_bounds__(1024) select_kernel(const float* __restrict__ partials,
-                                                      int cols, const int32_t* __restrict__ goff,
-                                                      int G, int64_t rows, int k,
-                                                      int32_t* __restrict__ sel,
-                                                      float* __restrict__ scores_out) {
-  extern __shared__ unsigned long long keys[];  // [npow2]
-  __shared__ int warp_sums[32];
-  const int g = blockIdx.x;
+// Channel scores: one warp per (group, channel).  The group's chunk partials
+// are added in ascending chunk order starting from 0: lane l holds 8
+// consecutive chunks, adds them to the running total it receives from lane
+// l-1, and hands the total on -- the same sequence of float32 adds as a single
+// loop over the chunks.
+__global__ void __launch_bounds__(256) score_kernel(const float* __restrict__ partials, int cols,
+                                                    const int32_t* __restrict__ goff, int G,
+                                                    int64_t rows, float* __restrict__ scores) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (w >= (int64_t)G * cols) return;
+  const int g = (int)(w / cols);
+  const int c = (int)(w % cols);
   const int64_t a = goff ? (int64_t)goff[g] : 0;
   const int64_t b = goff ? (int64_t)goff[g + 1] : rows;
-  int npow2 = 1;
-  while (npow2 < cols) npow2 <<= 1;
   const int64_t c0 = a / kScoreChunk;
   const int64_t c1 = (b + kScoreChunk - 1) / kScoreChunk;
+  float t = 0.0f;
+  for (int64_t base = c0; base < c1; base += 256) {
+    float v[8];
+    const int64_t my = base + 8 * lane;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = (my + i < c1) ? partials[(my + i) * cols + c] : 0.0f;
+    const int cnt = (int)max((int64_t)0, min((int64_t)8, c1 - my));
+#pragma unroll 1
+    for (int l = 0; l < 32; ++l) {
+      if (lane == l)
+        for (int i = 0; i < cnt; ++i) t = __fadd_rn(t, v[i]);
+      t = __shfl_sync(0xffffffffu, t, l);
+    }
+  }
+  if (lane == 0) scores[(int64_t)g * cols + c] = t;
+}
+
+// One block per group: bitonic sort of (score, ~index) keys descending, mark
+// the top k, compact the marked channels in ascending order.
+__global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ scores, int cols,
+                                                    int k, int32_t* __restrict__ sel) {
+  extern __shared__ unsigned long long keys[];  // [npow2]
+  __shared__ int warp_sums[32];
+  __shared__ int mask_words[256];               // cols <= 8192
+  const int g = blockIdx.x;
+  int npow2 = 1;
+  while (npow2 < cols) npow2 <<= 1;
   for (int c = threadIdx.x; c < npow2; c += blockDim.x) {
     unsigned long long key = 0ull;
-    if (c < cols) {
-      float s = 0.0f;
-      for (int64_t ch = c0; ch < c1; ++ch) s = __fadd_rn(s, partials[ch * cols + c]);
-      if (scores_out) scores_out[(int64_t)g * cols + c] = s;
-      key = ((unsigned long long)__float_as_uint(s) << 32) | (0xFFFFFFFFu - (uint32_t)c);
-    }
+    if (c < cols)
+      key = ((unsigned long long)__float_as_uint(scores[(int64_t)g * cols + c]) << 32) |
+            (0xFFFFFFFFu - (uint32_t)c);
     keys[c] = key;
   }
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) mask_words[i] = 0;
   __syncthreads();
   for (int size = 2; size <= npow2; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
@@ -188,21 +243,14 @@ __global__ void __launch_bounds__(1024) select_kernel(const float* __restrict__ 
       __syncthreads();
     }
   }
-  // keys[0..k) are the top k; turn them into a mask over channels, reusing keys[] storage
-  // after reading: first collect the indices into registers via a second pass.
-  __shared__ int mask_words[256];  // cols <= 8192 -> 256 x 32 bits
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) mask_words[i] = 0;
-  __syncthreads();
   for (int i = threadIdx.x; i < k; i += blockDim.x) {
     const uint32_t c = 0xFFFFFFFFu - (uint32_t)(keys[i] & 0xFFFFFFFFull);
     atomicOr(&mask_words[c >> 5], 1 << (c & 31));
   }
   __syncthreads();
-  // ordered compaction: exclusive prefix of popcounts over the 256 words
   const int nwords = (cols + 31) >> 5;
   int cnt = 0;
   if (threadIdx.x < nwords) cnt = __popc(mask_words[threadIdx.x]);
-  // block exclusive scan over threads 0..nwords-1 (nwords <= 256)
   int v = cnt;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
@@ -213,13 +261,13 @@ __global__ void __launch_bounds__(1024) select_kernel(const float* __restrict__ 
   if (lane == 31) warp_sums[w] = v;
   __syncthreads();
   if (w == 0) {
-    int s = warp_sums[lane];
+    int s2 = warp_sums[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int t = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += t;
+      int t = __shfl_up_sync(0xffffffffu, s2, o);
+      if (lane >= o) s2 += t;
     }
-    warp_sums[lane] = s;
+    warp_sums[lane] = s2;
   }
   __syncthreads();
   int base = v - cnt + (w > 0 ? warp_sums[w - 1] : 0);
@@ -434,7 +482,8 @@ using namespace quads;
 extern "C" quads_status_t quads_quantize_nvfp4(
     const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* row_index,
     const int32_t* group_offsets, int32_t num_groups, const float* tensor_scale_in,
-    uint8_t* codes, int64_t ld_codes, uint8_t* scales, int32_t scale_layout,
+    const float* tensor_amax_in, uint8_t* codes, int64_t ld_codes, uint8_t* scales,
+    int32_t scale_layout,
     float* tensor_scale_out, float* score_partials, void* workspace, size_t workspace_bytes,
     void* stream) {
   if (!x || !codes || !scales || !tensor_scale_out)
@@ -451,12 +500,21 @@ extern "C" quads_status_t quads_quantize_nvfp4(
     return fail(QUADS_ERR_MISALIGNED, "quantize: x/codes/score_partials must be 16-byte aligned");
   const int G = group_offsets ? num_groups : 1;
   if (group_offsets && num_groups < 1) return fail(QUADS_ERR_INVALID_ARG, "quantize: num_groups < 1");
-  if (!tensor_scale_in && (workspace_bytes < (size_t)G * 4 || !workspace))
+  if (tensor_scale_in && tensor_amax_in)
+    return fail(QUADS_ERR_INVALID_ARG, "quantize: give tensor_scale_in or tensor_amax_in, not both");
+  if (!tensor_scale_in && !tensor_amax_in && (workspace_bytes < (size_t)G * 4 || !workspace))
     return fail(QUADS_ERR_WORKSPACE, "quantize: workspace needs %d bytes", G * 4);
   if (rows == 0) return QUADS_OK;
   cudaStream_t st = (cudaStream_t)stream;
   const float* stp = tensor_scale_in;
-  if (!tensor_scale_in) {
+  int launched = 1;
+  if (tensor_amax_in) {
+    tensor_scale_kernel<<<(G + 255) / 256, 256, 0, st>>>((const uint32_t*)tensor_amax_in, G,
+                                                          tensor_scale_out);
+    stp = tensor_scale_out;
+    launched = 2;
+  } else if (!tensor_scale_in) {
+    launched = 3;
     uint32_t* amax = (uint32_t*)workspace;
     cudaMemsetAsync(amax, 0, (size_t)G * 4, st);
     amax_kernel<<<grid_for((rows + 31) / 32, 1, 16), 256, 0, st>>>(
@@ -482,7 +540,7 @@ extern "C" quads_status_t quads_quantize_nvfp4(
     quantize_kernel<false><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)x, rows, (int)cols, ldx,
                                                    row_index, group_offsets, G, stp, codes,
                                                    ld_codes, scales, scale_layout, nullptr);
-  return check_launch("quantize", tensor_scale_in ? 1 : 3);
+  return check_launch("quantize", launched);
 }
 
 extern "C" quads_status_t quads_select_residual_channels(
@@ -509,11 +567,16 @@ extern "C" quads_status_t quads_select_residual_channels(
   while (npow2 < cols) npow2 <<= 1;
   const size_t smem = (size_t)npow2 * 8;
   if (smem > 48 * 1024)
-    cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  select_kernel<<<G, 1024, smem, st>>>(score_partials, (int)cols, group_offsets, G, rows, k, sel,
-                                       scores_out);
+    cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   float* rs = (float*)workspace;
-  uint32_t* amax = (uint32_t*)((char*)workspace + (((size_t)rows * k * 4 + 255) & ~(size_t)255));
+  const size_t rs_bytes = ((size_t)rows * k * 4 + 255) & ~(size_t)255;
+  uint32_t* amax = (uint32_t*)((char*)workspace + rs_bytes);
+  float* scores = scores_out ? scores_out
+                             : (float*)((char*)workspace + rs_bytes + (((size_t)G * 4 + 255) & ~(size_t)255));
+  const int64_t nw = (int64_t)G * cols;
+  score_kernel<<<(int)((nw * 32 + 255) / 256), 256, 0, st>>>(score_partials, (int)cols,
+                                                             group_offsets, G, rows, scores);
+  topk_kernel<<<G, 1024, smem, st>>>(scores, (int)cols, k, sel);
   cudaMemsetAsync(amax, 0, (size_t)G * 4, st);
   rsel_residual_kernel<<<grid_for((rows + 31) / 32, 1, 16), 256, 0, st>>>(
       (const __nv_bfloat16*)x, rows, (int)cols, ldx, group_offsets, G, scales, scale_layout,
@@ -524,7 +587,7 @@ extern "C" quads_status_t quads_select_residual_channels(
   }
   rsel_quantize_kernel<<<grid_for(rows * (kpad / 8), 256), 256, 0, st>>>(
       rs, rows, k, kpad, group_offsets, G, amax, r_codes, r_scales, r_scale_layout, r_tensor_scale);
-  return check_launch("select", 3);
+  return check_launch("select", 4);
 }
 
 extern "C" quads_status_t quads_trace_round(const void* x_train, int64_t rows, int64_t cols,

@@ -27,6 +27,7 @@ class CompensatedLinear:
         self.k, self.compensate = k, compensate
         dev = w.device
         self.wq, _ = Q.quantize_nvfp4(w, scale_layout=Q.TCGEN05)
+        Q.weight_columns(self.wq)
         self.max_rows = max_rows
         kp = Q.kpad(k)
         self.bufs = dict(
@@ -96,10 +97,11 @@ class MoEExpertLayer:
             hc=e((cap, F // 2)), hs=e(Q.sf_tc_bytes(cap, F)), hts=e(E, dt=f32),
             hpart=e((cap // 32, F), dt=f32),
             sel2=e((E, k2), dt=i32), r2c=e((cap, kp2 // 2)), r2s=e(Q.sf_tc_bytes(cap, kp2)),
-            r2ts=e(E, dt=f32),
+            r2ts=e(E, dt=f32), hamax=e(E, dt=f32),
             y=e((cap, H), dt=torch.bfloat16), out=e((T, H), dt=torch.bfloat16),
         )
         self.ws = dict(
+            rt=e(Q.workspace_size(Q.OP_MOE_ROUTE, T, E, 0, topk)),
             q1=e(Q.workspace_size(Q.OP_QUANTIZE, T, H)),
             s1=e(Q.workspace_size(Q.OP_SELECT, T, H, 0, k1)),
             g1=e(Q.workspace_size(Q.OP_MOE_GEMM, 0, H, 2 * F, k1, E)),
@@ -113,7 +115,8 @@ class MoEExpertLayer:
         assert T == self.max_tokens, "buffers are sized for a fixed token count"
         E, H, F = self.E, self.H, self.F
         comp = self.compensate
-        plan = Q.moe_route(logits, self.topk, rows_capacity=self.cap, out=b["route"], stream=stream)
+        plan = Q.moe_route(logits, self.topk, rows_capacity=self.cap, out=b["route"],
+                           workspace=ws["rt"], stream=stream)
         xq, xpart = Q.quantize_nvfp4(x, scores=comp, workspace=ws["q1"], stream=stream,
                                      out=(b["xc"], b["xs"], b["xts"], b["xpart"] if comp else None))
         a1 = Q.moe_gather(plan, xq, out=(b["a1c"], b["a1s"]), stream=stream)
@@ -123,10 +126,13 @@ class MoEExpertLayer:
                                                      stream=stream,
                                                      out=(b["sel1"], b["r1c"], b["r1s"], b["r1ts"]))
             r1 = Q.moe_gather(plan, xr, out=(b["g1c"], b["g1s"]), stream=stream)
+        # GEMM1's epilogue also leaves each expert's max |h| for h's tensor scale
         h = Q.moe_grouped_gemm(plan, a1, self.w1q, E, 2 * F, r1, sel1, self.k1,
-                               epilogue=Q.EPI_SWIGLU, workspace=ws["g1"], out=b["h"], stream=stream)
+                               epilogue=Q.EPI_SWIGLU, y_amax=b["hamax"], workspace=ws["g1"],
+                               out=b["h"], stream=stream)
         hq, hpart = Q.quantize_nvfp4(h, group_offsets=plan["offsets"], num_groups=E,
-                                     scale_layout=Q.TCGEN05, scores=comp, rows=self.cap,
+                                     tensor_amax_in=b["hamax"], scale_layout=Q.TCGEN05,
+                                     scores=comp, rows=self.cap,
                                      workspace=ws["q2"], stream=stream,
                                      out=(b["hc"], b["hs"], b["hts"], b["hpart"] if comp else None))
         r2 = sel2 = None

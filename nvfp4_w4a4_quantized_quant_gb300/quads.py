@@ -20,7 +20,7 @@ from .build import LIB, ROOT
 LINEAR, TCGEN05 = 0, 1
 OUT_F32, OUT_BF16 = 0, 1
 EPI_NONE, EPI_SWIGLU = 0, 1
-OP_QUANTIZE, OP_SELECT, OP_GEMM, OP_MOE_GEMM = 0, 1, 2, 3
+OP_QUANTIZE, OP_SELECT, OP_GEMM, OP_MOE_GEMM, OP_MOE_ROUTE = 0, 1, 2, 3, 4
 SCORE_CHUNK_ROWS = 32
 MOE_ROW_ALIGN = 128
 
@@ -34,17 +34,18 @@ _SIGS = {
     "quads_device_status": (_I32, [_P, ctypes.POINTER(_I32)]),
     "quads_workspace_size": (_SZ, [_I32, _I64, _I64, _I64, _I32, _I32]),
     "quads_kpad": (_I32, [_I32]),
-    "quads_quantize_nvfp4": (_I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _I64, _P, _I32,
-                                    _P, _P, _P, _SZ, _P]),
+    "quads_quantize_nvfp4": (_I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P, _I64, _P,
+                                    _I32, _P, _P, _P, _SZ, _P]),
     "quads_select_residual_channels": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _I32, _P, _P,
                                               _I32, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P]),
     "quads_w4a4_gemm_comp": (_I32, [_I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                                    _I32, _P, _I32, _I64, _P, _SZ, _P]),
+                                    _P, _P, _I32, _P, _I32, _I64, _P, _SZ, _P]),
     "quads_moe_grouped_gemm": (_I32, [_I32, _I64, _I64, _I64, _P, _P, _P, _P, _P, _I32, _P, _P,
-                                      _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _P, _I32, _I64,
-                                      _P, _SZ, _P]),
+                                      _P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _P,
+                                      _I32, _I64, _P, _P, _SZ, _P]),
+    "quads_weight_columns": (_I32, [_P, _P, _I32, _I64, _I64, _P, _P, _P]),
     "quads_trace_round": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _P, _P]),
-    "quads_moe_route": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _I64, _P]),
+    "quads_moe_route": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _I64, _P, _SZ, _P]),
     "quads_moe_gather": (_I32, [_P, _P, _I32, _I64, _I64, _P, _P, _P, _P, _P]),
     "quads_moe_combine": (_I32, [_P, _I64, _P, _P, _I32, _I32, _I64, _P, _I64, _P]),
 }
@@ -131,17 +132,21 @@ def device_status(stream=None) -> int:
 
 @dataclass
 class QTensor:
-    """NVFP4 tensor: packed codes [rows, cols/2], scale bytes in `layout`, tensor scales [G]."""
+    """NVFP4 tensor: packed codes [rows, cols/2], scale bytes in `layout`, tensor scales [G].
+    Weights also carry their column-major copy (codes_t, scales_t) for the W_sel gather."""
     codes: torch.Tensor
     scales: torch.Tensor
     tensor_scale: torch.Tensor
     rows: int
     cols: int
     layout: int
+    codes_t: Optional[torch.Tensor] = None
+    scales_t: Optional[torch.Tensor] = None
 
 
 def quantize_nvfp4(x: torch.Tensor, *, group_offsets=None, num_groups: int = 1,
-                   tensor_scale_in=None, scale_layout: int = LINEAR, scores: bool = False,
+                   tensor_scale_in=None, tensor_amax_in=None, scale_layout: int = LINEAR,
+                   scores: bool = False,
                    row_index=None, rows: Optional[int] = None, workspace=None, out=None,
                    stream=None):
     """x bf16 [rows, cols] -> (QTensor, score partials [ceil(rows/32), cols] or None)."""
@@ -162,7 +167,8 @@ def quantize_nvfp4(x: torch.Tensor, *, group_offsets=None, num_groups: int = 1,
         codes, scales, ts, part = out
     ws = _workspace(workspace_size(OP_QUANTIZE, rows, cols, 0, 0, G), dev, workspace)
     _check(lib.quads_quantize_nvfp4(_ptr(x), rows, cols, x.stride(0), _ptr(row_index),
-                                    _ptr(group_offsets), G, _ptr(tensor_scale_in), _ptr(codes),
+                                    _ptr(group_offsets), G, _ptr(tensor_scale_in),
+                                    _ptr(tensor_amax_in), _ptr(codes),
                                     codes.stride(0), _ptr(scales), scale_layout, _ptr(ts),
                                     _ptr(part), _ptr(ws), ws.numel(), _stream(stream)),
            "quantize_nvfp4")
@@ -207,9 +213,12 @@ def w4a4_gemm_comp(a: QTensor, w: QTensor, r: Optional[QTensor] = None, sel=None
     ws = None
     if r is not None:
         ws = _workspace(workspace_size(OP_GEMM, 0, K, N, k, 1), y.device, workspace)
+    if r is not None and w.codes_t is None:
+        raise QuadsError("compensation needs the weight's column-major copy (weight_columns)")
     _check(lib.quads_w4a4_gemm_comp(
         M, N, K, _ptr(a.codes), _ptr(a.scales), _ptr(a.tensor_scale), _ptr(w.codes),
-        _ptr(w.scales), _ptr(w.tensor_scale), _ptr(r.codes if r else None),
+        _ptr(w.scales), _ptr(w.tensor_scale), _ptr(w.codes_t), _ptr(w.scales_t),
+        _ptr(r.codes if r else None),
         _ptr(r.scales if r else None), _ptr(r.tensor_scale if r else None), _ptr(sel), k,
         _ptr(y), yd, y.stride(0), _ptr(ws), ws.numel() if ws is not None else 0,
         _stream(stream)), "w4a4_gemm_comp")
@@ -220,7 +229,8 @@ def moe_grouped_gemm(plan: dict, a: QTensor, w: QTensor, num_experts: int, n: in
                      r: Optional[QTensor] = None, sel=None, k: int = 0, *,
                      a_scale_per_expert: bool = False, r_scale_per_expert: bool = False,
                      sel_per_expert: bool = False, epilogue: int = EPI_NONE,
-                     out_dtype=torch.bfloat16, workspace=None, out=None, stream=None):
+                     out_dtype=torch.bfloat16, y_amax=None, workspace=None, out=None,
+                     stream=None):
     """Grouped compensated GEMM over the experts of `plan` (from moe_route)."""
     lib = load()
     cap = plan["rows_capacity"]
@@ -231,13 +241,16 @@ def moe_grouped_gemm(plan: dict, a: QTensor, w: QTensor, num_experts: int, n: in
     ws = None
     if r is not None:
         ws = _workspace(workspace_size(OP_MOE_GEMM, 0, K, n, k, num_experts), y.device, workspace)
+    if r is not None and w.codes_t is None:
+        raise QuadsError("compensation needs the weight's column-major copy (weight_columns)")
     _check(lib.quads_moe_grouped_gemm(
         num_experts, cap, n, K, _ptr(plan["offsets"]), _ptr(plan["counts"]), _ptr(a.codes),
         _ptr(a.scales), _ptr(a.tensor_scale), int(a_scale_per_expert), _ptr(w.codes),
-        _ptr(w.scales), _ptr(w.tensor_scale), _ptr(r.codes if r else None),
-        _ptr(r.scales if r else None), _ptr(r.tensor_scale if r else None),
-        int(r_scale_per_expert), _ptr(sel), int(sel_per_expert), k, epilogue, _ptr(y), yd,
-        y.stride(0), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)),
+        _ptr(w.scales), _ptr(w.tensor_scale), _ptr(w.codes_t), _ptr(w.scales_t),
+        _ptr(r.codes if r else None), _ptr(r.scales if r else None),
+        _ptr(r.tensor_scale if r else None), int(r_scale_per_expert), _ptr(sel),
+        int(sel_per_expert), k, epilogue, _ptr(y), yd, y.stride(0), _ptr(y_amax), _ptr(ws),
+        ws.numel() if ws is not None else 0, _stream(stream)),
         "moe_grouped_gemm")
     return y
 
@@ -264,8 +277,21 @@ def moe_rows_capacity(tokens: int, topk: int, experts: int) -> int:
     return (cap + MOE_ROW_ALIGN - 1) // MOE_ROW_ALIGN * MOE_ROW_ALIGN
 
 
+def weight_columns(w: QTensor, num_groups: int = 1, stream=None) -> QTensor:
+    """Attach the column-major copy of an NVFP4 weight (made once per weight update)."""
+    lib = load()
+    rpg = w.rows // num_groups
+    dev = w.codes.device
+    w.codes_t = torch.empty(num_groups * w.cols * (rpg // 2), dtype=torch.uint8, device=dev)
+    w.scales_t = torch.empty(num_groups * (w.cols // 16) * rpg, dtype=torch.uint8, device=dev)
+    _check(lib.quads_weight_columns(_ptr(w.codes), _ptr(w.scales), num_groups, rpg, w.cols,
+                                    _ptr(w.codes_t), _ptr(w.scales_t), _stream(stream)),
+           "weight_columns")
+    return w
+
+
 def moe_route(logits: torch.Tensor, topk: int, *, rows_capacity: Optional[int] = None,
-              out=None, stream=None) -> dict:
+              out=None, workspace=None, stream=None) -> dict:
     lib = load()
     T, E = logits.shape
     cap = rows_capacity or moe_rows_capacity(T, topk, E)
@@ -277,9 +303,11 @@ def moe_route(logits: torch.Tensor, topk: int, *, rows_capacity: Optional[int] =
                    offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
                    row_token=torch.empty(cap, dtype=torch.int32, device=dev),
                    token_row=torch.empty((T, topk), dtype=torch.int32, device=dev))
+    ws = _workspace(workspace_size(OP_MOE_ROUTE, T, E, 0, topk, 1), dev, workspace)
     _check(lib.quads_moe_route(_ptr(logits), T, E, topk, _ptr(out["idx"]), _ptr(out["gates"]),
                                _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["row_token"]),
-                               _ptr(out["token_row"]), cap, _stream(stream)), "moe_route")
+                               _ptr(out["token_row"]), cap, _ptr(ws), ws.numel(),
+                               _stream(stream)), "moe_route")
     out.update(rows_capacity=cap, tokens=T, experts=E, topk=topk)
     return out
 
@@ -330,4 +358,4 @@ def quantize_expert_weights(w: torch.Tensor, *, swiglu_interleave: bool = False,
     ri = swiglu_row_index(E, N // 2, K, w.device) if swiglu_interleave else None
     q, _ = quantize_nvfp4(flat, group_offsets=offs, num_groups=E, scale_layout=TCGEN05,
                           row_index=ri, stream=stream)
-    return q
+    return weight_columns(q, E, stream=stream)

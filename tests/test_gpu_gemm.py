@@ -19,6 +19,7 @@ def _run(lib, xb, wb, k, out_dtype, comp=True):
     x, w = bf16_tensor(xb), bf16_tensor(wb)
     xq, part = lib.quantize_nvfp4(x, scores=True, scale_layout=1)
     wq, _ = lib.quantize_nvfp4(w, scale_layout=1)
+    lib.weight_columns(wq)
     if not comp:
         return lib.w4a4_gemm_comp(xq, wq, out_dtype=out_dtype), None, None
     sel, _, r = lib.select_residual_channels(x, xq, part, k, r_scale_layout=1)

@@ -27,7 +27,8 @@ def test_status_strings_and_sizes(lib):
     assert [lib.quads_kpad(k) for k in (16, 64, 80, 128, 192, 256, 272)] == [64, 64, 128, 128, 256, 256, 512]
     assert lib.quads_workspace_size(quads.OP_QUANTIZE, 10, 64, 0, 0, 3) == 12
     sel = lib.quads_workspace_size(quads.OP_SELECT, 100, 256, 0, 16, 2)
-    assert sel == ((100 * 16 * 4 + 255) // 256) * 256 + 8
+    assert sel == ((100 * 16 * 4 + 255) // 256) * 256 + 256 + 2 * 256 * 4
+    assert lib.quads_workspace_size(quads.OP_MOE_ROUTE, 100, 128, 0, 8, 1) == 100 * 4 * 4 + 16
     g = lib.quads_workspace_size(quads.OP_GEMM, 0, 2048, 6144, 128, 1)
     assert g == ((6144 * 64 + 1023) // 1024) * 1024 + 6144 * 8
 
@@ -38,29 +39,39 @@ def _err(lib):
 
 def test_host_side_argument_checks_need_no_gpu(lib):
     p = ctypes.c_void_p(16)     # never dereferenced: every call below fails validation first
-    st = lib.quads_quantize_nvfp4(p, 8, 15, 16, None, None, 1, None, p, 8, p, 0, p, None, p, 64, None)
+    st = lib.quads_quantize_nvfp4(p, 8, 15, 16, None, None, 1, None, None, p, 8, p, 0, p, None, p, 64, None)
     assert st == 2 and "multiple of 16" in _err(lib)
-    st = lib.quads_quantize_nvfp4(None, 8, 16, 16, None, None, 1, None, p, 8, p, 0, p, None, p, 64, None)
+    st = lib.quads_quantize_nvfp4(None, 8, 16, 16, None, None, 1, None, None, p, 8, p, 0, p, None, p, 64, None)
     assert st == 1
-    st = lib.quads_quantize_nvfp4(p, 8, 32, 16, None, None, 1, None, p, 16, p, 0, p, None, p, 64, None)
+    st = lib.quads_quantize_nvfp4(p, 8, 32, 16, None, None, 1, None, None, p, 16, p, 0, p, None, p, 64, None)
     assert st == 3                                   # ldx < cols
-    st = lib.quads_quantize_nvfp4(p, 8, 32, 32, None, None, 1, None, p, 16, p, 1, p, None, p, 64, None)
+    st = lib.quads_quantize_nvfp4(p, 8, 32, 32, None, None, 1, None, None, p, 16, p, 1, p, None, p, 64, None)
     assert st == 2                                   # tcgen05 layout needs cols % 64
-    st = lib.quads_w4a4_gemm_comp(64, 100, 256, p, p, p, p, p, p, None, None, None, None, 0, p, 0, 100,
-                                  None, 0, None)
+    st = lib.quads_quantize_nvfp4(p, 8, 32, 32, None, None, 1, p, p, p, 16, p, 0, p, None, p, 64, None)
+    assert st == 1                                   # both tensor_scale_in and tensor_amax_in
+    st = lib.quads_w4a4_gemm_comp(64, 100, 256, p, p, p, p, p, p, None, None, None, None, None, None, 0,
+                                  p, 0, 100, None, 0, None)
     assert st == 2 and "N%128" in _err(lib)
-    st = lib.quads_w4a4_gemm_comp(64, 128, 256, p, p, p, p, p, p, p, p, p, p, 8, p, 0, 128, None, 0, None)
+    st = lib.quads_w4a4_gemm_comp(64, 128, 256, p, p, p, p, p, p, p, p, p, p, p, p, 8, p, 0, 128, None, 0,
+                                  None)
     assert st == 1                                   # k not a multiple of 16
+    st = lib.quads_w4a4_gemm_comp(64, 128, 256, p, p, p, p, p, p, None, None, p, p, p, p, 16, p, 0, 128,
+                                  None, 0, None)
+    assert st == 1 and "column-major" in _err(lib)   # compensation without the weight copy
     st = lib.quads_select_residual_channels(p, 64, 256, 256, None, 1, p, 0, p, p, 17, p, None, p, p, 0, p,
                                             p, 1 << 20, None)
     assert st == 2
-    st = lib.quads_moe_route(p, 100, 300, 8, p, p, p, p, p, p, 1 << 20, None)
+    st = lib.quads_moe_route(p, 100, 300, 8, p, p, p, p, p, p, 1 << 20, p, 1 << 20, None)
     assert st == 2                                   # > 256 experts
-    st = lib.quads_moe_route(p, 100, 16, 8, p, p, p, p, p, p, 10, None)
+    st = lib.quads_moe_route(p, 100, 16, 8, p, p, p, p, p, p, 10, p, 1 << 20, None)
     assert st == 1 and "rows_capacity" in _err(lib)
+    st = lib.quads_moe_route(p, 100, 16, 8, p, p, p, p, p, p, 1 << 20, p, 4, None)
+    assert st == 7                                   # workspace too small
     st = lib.quads_moe_grouped_gemm(4, 1000, 256, 256, p, None, p, p, p, 0, p, p, p, None, None, None,
-                                    0, None, 0, 0, 0, p, 1, 256, None, 0, None)
+                                    None, None, 0, None, 0, 0, 0, p, 1, 256, None, None, 0, None)
     assert st == 2                                   # rows_capacity % 128
+    st = lib.quads_weight_columns(p, p, 2, 100, 256, p, p, None)
+    assert st == 2                                   # rows_per_group % 128
     st = lib.quads_trace_round(p, 4, 24, 24, p, 12, p, p, p, None, None)
     assert st == 2
 
