@@ -43,7 +43,9 @@ constexpr int EPI_THREADS = 256;
 constexpr int TMEM_COLS = 512;
 constexpr int ACC2_COL = 256;
 constexpr int SF_COL = 384;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*barriers*/ + 1024 /*align*/;
+constexpr int MAX_GROUPS = 256;                 // experts cached in shared memory
+constexpr int META_BYTES = 1024 + 4 * (MAX_GROUPS + 1) + 4 * 4 * MAX_GROUPS;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + META_BYTES + 1024 /*align*/;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per wait
 
 enum { OUT_F32 = 0, OUT_BF16 = 1, OUT_SWIGLU = 2 };
@@ -213,12 +215,21 @@ struct Tile {
   int64_t row_end;  // rows >= row_end are not real (not stored for OUT_F32/BF16)
 };
 
-__device__ __forceinline__ int64_t total_tiles(const Params& p) {
+// Per-group tables copied to shared memory once per CTA (the tile decode of
+// every role reads them for every tile).
+struct Meta {
+  int32_t* off;    // [E+1]
+  int32_t* cnt;    // [E]
+  float* a1;       // [E] s_a * s_w
+  float* a2;       // [E] s_r * s_w
+};
+
+__device__ __forceinline__ int64_t total_tiles(const Params& p, const Meta& m) {
   if (!p.row_off) return ((p.M + BM - 1) / BM) * p.Nt;
-  return (int64_t)(p.row_off[p.E] / BM) * p.Nt;
+  return (int64_t)(m.off[p.E] / BM) * p.Nt;
 }
 
-__device__ __forceinline__ Tile decode_tile(const Params& p, int64_t t) {
+__device__ __forceinline__ Tile decode_tile(const Params& p, const Meta& m, int64_t t) {
   Tile r;
   if (!p.row_off) {
     const int64_t Mt = (p.M + BM - 1) / BM;
@@ -228,20 +239,20 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, int64_t t) {
     r.row_end = p.M;
     return r;
   }
-  // expert e holds tiles [row_off[e]/128 * Nt, row_off[e+1]/128 * Nt), m fastest
+  // expert e holds tiles [off[e]/128 * Nt, off[e+1]/128 * Nt), m fastest
   int lo = 0, hi = p.E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if ((int64_t)(p.row_off[mid] / BM) * p.Nt <= t) lo = mid; else hi = mid - 1;
+    if ((int64_t)(m.off[mid] / BM) * p.Nt <= t) lo = mid; else hi = mid - 1;
   }
   const int e = lo;
-  const int64_t base = (int64_t)(p.row_off[e] / BM) * p.Nt;
-  const int64_t mt_e = (p.row_off[e + 1] - p.row_off[e]) / BM;
+  const int64_t base = (int64_t)(m.off[e] / BM) * p.Nt;
+  const int64_t mt_e = (m.off[e + 1] - m.off[e]) / BM;
   const int64_t local = t - base;
   r.e = e;
-  r.m0 = p.row_off[e] + (local % mt_e) * BM;
+  r.m0 = m.off[e] + (local % mt_e) * BM;
   r.n0 = (int)(local / mt_e) * BN;
-  r.row_end = p.row_off[e] + (p.row_cnt ? p.row_cnt[e] : (p.row_off[e + 1] - p.row_off[e]));
+  r.row_end = m.off[e] + m.cnt[e];
   return r;
 }
 
@@ -260,9 +271,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* acc_empty = acc_full + 2;    // [2]
   uint32_t* tmem_holder = (uint32_t*)(acc_empty + 2);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
+  Meta meta;
+  meta.off = (int32_t*)(smem + STAGES * STAGE_BYTES + 1024);
+  meta.cnt = meta.off + (MAX_GROUPS + 1);
+  meta.a1 = (float*)(meta.cnt + MAX_GROUPS);
+  meta.a2 = meta.a1 + MAX_GROUPS;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+    const float bts = p.b_ts[e];
+    meta.a1[e] = __fmul_rn(p.a_ts[p.a_ts_pe ? e : 0], bts);
+    meta.a2[e] = p.comp ? __fmul_rn(p.r_ts[p.r_ts_pe ? e : 0], bts) : 0.0f;
+    if (p.row_off) {
+      meta.off[e] = p.row_off[e];
+      meta.cnt[e] = p.row_cnt ? p.row_cnt[e] : (p.row_off[e + 1] - p.row_off[e]);
+    }
+  }
+  if (threadIdx.x == 0 && p.row_off) meta.off[p.E] = p.row_off[p.E];
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
@@ -283,7 +309,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  const int64_t ntiles = total_tiles(p);
+  const int64_t ntiles = total_tiles(p, meta);
   const int KT = (p.K + 255) / 256;
   const int KTc = p.comp ? (p.kpad + 255) / 256 : 0;
   const int64_t a_sf_rb = (int64_t)(p.K / 64) * 512;    // bytes per 128-row block
@@ -294,7 +320,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t it = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-      const Tile tl = decode_tile(p, t);
+      const Tile tl = decode_tile(p, meta, t);
       const int64_t brow = (int64_t)tl.e * p.N + tl.n0;
       for (int kt = 0; kt < KT + KTc && ok; ++kt, ++it) {
         const int s = it % STAGES;
@@ -384,7 +410,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int row_in_tile = quad * 32 + lane;
     uint32_t j = 0;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++j) {
-      const Tile tl = decode_tile(p, t);
+      const Tile tl = decode_tile(p, meta, t);
       const uint32_t b = j & 1;
       // lane 0 waits, the warp follows it (tcgen05.ld needs the whole warp)
       int okw = 0;
@@ -392,9 +418,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       okw = __shfl_sync(0xffffffffu, okw, 0);
       if (!okw) break;
       tc_fence_after();
-      const float bts = p.b_ts[tl.e];
-      const float a1 = __fmul_rn(p.a_ts[p.a_ts_pe ? tl.e : 0], bts);
-      const float a2 = p.comp ? __fmul_rn(p.r_ts[p.r_ts_pe ? tl.e : 0], bts) : 0.0f;
+      const float a1 = meta.a1[tl.e];
+      const float a2 = meta.a2[tl.e];
       const int64_t row = tl.m0 + row_in_tile;
       const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
       const uint32_t t1 = tmem + lane_base + b * BN;
@@ -403,7 +428,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (p.out_mode == OUT_SWIGLU) {
         // tile columns [0,64) are gate rows of W, [64,128) the matching up rows;
         // this warp produces h columns [32*half, 32*half + 32) of the tile
-        const bool store = row < (p.row_off ? (int64_t)p.row_off[tl.e + 1] : p.M);
+        const bool store = row < (p.row_off ? (int64_t)meta.off[tl.e + 1] : p.M);
         __nv_bfloat16* y = (__nv_bfloat16*)p.y + row * p.ldy + tl.n0 / 2;
 #pragma unroll 1
         for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
@@ -519,42 +544,50 @@ __global__ void __launch_bounds__(256) wtrans_kernel(const uint8_t* __restrict__
 // For every weight row r (of every expert) and every 16-block of the selected
 // channels: gather the selected columns of DQ(Q(W)) in units of s_w
 // (level * E4M3 scale, exact), requantize with tensor scale 1 (s_w kept).
-// Reads the column-major copy (consecutive threads = consecutive rows).
-// Output codes [E*N, kpad/2] and TCGEN05 scales over kpad columns.
+// A warp owns 32 consecutive rows (lane = row) of one expert and reads the
+// column-major copy, so every gather of a selected column is one coalesced
+// 16-byte (codes) + 32-byte (scales) access.  Output codes [E*N, kpad/2] and
+// TCGEN05 scales over kpad columns.
 __global__ void __launch_bounds__(256) wsel_kernel(
     const uint8_t* __restrict__ ct, const uint8_t* __restrict__ st, int64_t rows /*E*N*/, int N,
     int K, const int32_t* __restrict__ sel, int sel_pe, int k, int kpad,
     uint8_t* __restrict__ oc, uint8_t* __restrict__ osf) {
+  const int lane = threadIdx.x & 31;
   const int nb = kpad >> 4;
-  const int64_t total = rows * nb;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i % rows;
-    const int blk = (int)(i / rows);
-    uint32_t lo = 0, hi = 0, sbyte = 0;
-    if (blk * 16 < k) {
-      const int64_t e = r / N, n = r % N;
-      const int32_t* s = sel + (sel_pe ? e * k : 0) + blk * 16;
-      const uint8_t* cte = ct + e * (int64_t)K * (N / 2) + n / 2;
-      const uint8_t* ste = st + e * (int64_t)(K / 16) * N + n;
-      const uint32_t sh = (n & 1) * 4;
-      float w[16];
-      float m = 0.0f;
+  const int64_t nwarps = rows >> 5;
+  for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < nwarps;
+       w += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+    const int64_t r = w * 32 + lane;
+    const int64_t e = r / N, n = r % N;
+    const int32_t* s = sel + (sel_pe ? e * k : 0);
+    const uint8_t* cte = ct + e * (int64_t)K * (N / 2) + n / 2;
+    const uint8_t* ste = st + e * (int64_t)(K / 16) * N + n;
+    const uint32_t sh = (n & 1) * 4;
+    for (int blk = 0; blk < nb; ++blk) {
+      uint32_t lo = 0, hi = 0, sbyte = 0;
+      if (blk * 16 < k) {
+        float w16[16];
+        float m = 0.0f;
+        uint32_t codes[16], sbytes[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int c = s[j];
-        const uint32_t code = (cte[(int64_t)c * (N / 2)] >> sh) & 15u;
-        const float sc = e4m3_to_f32(ste[(int64_t)(c >> 4) * N]);
-        w[j] = __fmul_rn(e2m1_to_f32(code), sc);
-        m = fmaxf(m, fabsf(w[j]));
+        for (int j = 0; j < 16; ++j) {
+          const int c = __ldg(s + blk * 16 + j);
+          codes[j] = cte[(int64_t)c * (N / 2)];
+          sbytes[j] = ste[(int64_t)(c >> 4) * N];
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          w16[j] = __fmul_rn(e2m1_to_f32((codes[j] >> sh) & 15u), e4m3_to_f32(sbytes[j]));
+          m = fmaxf(m, fabsf(w16[j]));
+        }
+        const BlockScale bs = block_scale(m, 1.0f);
+        lo = quantize8(w16, bs);
+        hi = quantize8(w16 + 8, bs);
+        sbyte = bs.byte;
       }
-      const BlockScale bs = block_scale(m, 1.0f);
-      lo = quantize8(w, bs);
-      hi = quantize8(w + 8, bs);
-      sbyte = bs.byte;
+      *reinterpret_cast<uint2*>(oc + r * (kpad >> 1) + blk * 8) = make_uint2(lo, hi);
+      osf[sf_tc_offset(r, blk, nb)] = (uint8_t)sbyte;
     }
-    *reinterpret_cast<uint2*>(oc + r * (kpad >> 1) + blk * 8) = make_uint2(lo, hi);
-    osf[sf_tc_offset(r, blk, nb)] = (uint8_t)sbyte;
   }
 }
 
@@ -621,7 +654,7 @@ static quads_status_t launch(const Launch& L) {
       return fail(QUADS_ERR_WORKSPACE, "gemm: workspace needs %zu bytes", need);
     ws_codes = (uint8_t*)L.ws;
     ws_sf = ws_codes + (((size_t)brows * (L.kpad / 2) + 1023) & ~(size_t)1023);
-    const int64_t total = brows * (L.kpad / 16);
+    const int64_t total = brows;  // one thread per weight row (N % 128 == 0)
     int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)num_sms() * 16);
     wsel_kernel<<<blocks, 256, 0, L.stream>>>(L.b_t, L.b_sf_t, brows, L.N, L.K, L.sel, L.sel_pe,
                                                L.k, L.kpad, ws_codes, ws_sf);
@@ -732,7 +765,8 @@ extern "C" quads_status_t quads_moe_grouped_gemm(
   if (!expert_offsets || !a_codes || !a_scales || !a_tensor_scale || !w_codes || !w_scales ||
       !w_tensor_scale || !y)
     return fail(QUADS_ERR_INVALID_ARG, "moe_gemm: null operand pointer");
-  if (num_experts < 1 || rows_capacity < 1 || rows_capacity % 128 || N % 128 || N <= 0 ||
+  if (num_experts < 1 || num_experts > gemm::MAX_GROUPS || rows_capacity < 1 ||
+      rows_capacity % 128 || N % 128 || N <= 0 ||
       K % 64 || K <= 0)
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "moe_gemm: need experts>=1, rows_capacity%%128==0, N%%128==0, K%%64==0");
   if (epilogue != QUADS_EPILOGUE_NONE && epilogue != QUADS_EPILOGUE_SWIGLU)

@@ -30,9 +30,9 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31;
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int words = (E + 31) >> 5;
-  if (t < T) {
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T;
+       t += (gridDim.x * blockDim.x) >> 5) {
     float v[kMaxExperts / 32];
     const int per = words;
 #pragma unroll
@@ -103,56 +103,62 @@ __global__ void plan_kernel(const int32_t* __restrict__ counts, int E, int32_t* 
   }
 }
 
-// One block per expert: scan the tokens in order (one bit of the token's expert
-// mask each); a token routed to the expert gets the next row of its group and
-// its slot is the number of its experts with a lower id.  Padding rows get
-// row_token = -1.
+// One block per expert: thread i covers a contiguous run of tokens, counts the
+// ones routed to the expert (one bit of the token's expert mask each), a block
+// exclusive scan gives each run its first row, and the rows are then written
+// in token order.  A token's slot is the number of its experts with a lower
+// id.  Padding rows get row_token = -1.
 __global__ void __launch_bounds__(1024) assign_kernel(const uint32_t* __restrict__ emask, int T,
                                                       int E, int topk,
                                                       const int32_t* __restrict__ off,
                                                       const int32_t* __restrict__ counts,
                                                       int32_t* __restrict__ row_token,
                                                       int32_t* __restrict__ token_row) {
-  __shared__ int warp_tot[32];
-  __shared__ int base_s;
+  __shared__ int warp_sums[32];
   const int e = blockIdx.x;
   const int words = (E + 31) >> 5;
   const int ew = e >> 5;
   const uint32_t ebit = 1u << (e & 31);
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  if (threadIdx.x == 0) base_s = 0;
+  const int per = (T + blockDim.x - 1) / blockDim.x;
+  const int t0 = min(T, (int)threadIdx.x * per), t1 = min(T, t0 + per);
+  int cnt = 0;
+  for (int t = t0; t < t1; ++t) cnt += (emask[(int64_t)t * words + ew] & ebit) ? 1 : 0;
+  int v = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+  }
+  if (lane == 31) warp_sums[w] = v;
   __syncthreads();
-  const int e0 = off[e];
-  for (int t0 = 0; t0 < T; t0 += blockDim.x) {
-    const int t = t0 + threadIdx.x;
-    const uint32_t word = t < T ? emask[(int64_t)t * words + ew] : 0u;
-    const int f = (word & ebit) ? 1 : 0;
-    const unsigned bal = __ballot_sync(0xffffffffu, f);
-    const int pre = __popc(bal & ((1u << lane) - 1u));
-    if (lane == 0) warp_tot[w] = __popc(bal);
-    __syncthreads();
-    int wbase = 0;
-    for (int i = 0; i < w; ++i) wbase += warp_tot[i];
-    if (f) {
+  if (w == 0) {
+    int x = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += u;
+    }
+    warp_sums[lane] = x;
+  }
+  __syncthreads();
+  int row = off[e] + v - cnt + (w > 0 ? warp_sums[w - 1] : 0);
+  for (int t = t0; t < t1; ++t) {
+    const uint32_t word = emask[(int64_t)t * words + ew];
+    if (word & ebit) {
       int slot = __popc(word & (ebit - 1u));
       for (int i = 0; i < ew; ++i) slot += __popc(emask[(int64_t)t * words + i]);
-      const int row = e0 + base_s + wbase + pre;
       row_token[row] = t;
       token_row[(int64_t)t * topk + slot] = row;
+      ++row;
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int tot = 0;
-      for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += warp_tot[i];
-      base_s += tot;
-    }
-    __syncthreads();
   }
-  for (int r = e0 + counts[e] + threadIdx.x; r < off[e + 1]; r += blockDim.x) row_token[r] = -1;
+  for (int r = off[e] + counts[e] + threadIdx.x; r < off[e + 1]; r += blockDim.x) row_token[r] = -1;
 }
 
-// One warp per output row: codes (16 B per lane-iteration), then the row's
-// scale bytes in groups of 4 (one 64-element atom column each).
+// One warp per 8 consecutive output rows: the 8 source-row indices are loaded
+// at once, then every lane issues all its 16-byte code loads (and 4-byte scale
+// loads) for the 8 rows before storing them; scale bytes go to the TCGEN05 atoms.
 __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__ row_token,
                                                      const int32_t* __restrict__ off, int E,
                                                      int64_t cap, int cols,
@@ -164,18 +170,44 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
   const int64_t nrows = off[E];
   const int cbytes = cols >> 1;
   const int ncols16 = cols >> 4;
-  for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < nrows;
-       r += ((int64_t)gridDim.x * blockDim.x) >> 5) {
-    const int t = row_token[r];
-    for (int b = lane * 16; b < cbytes; b += 512) {
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (t >= 0) v = *reinterpret_cast<const uint4*>(ic + (int64_t)t * cbytes + b);
-      *reinterpret_cast<uint4*>(oc + r * cbytes + b) = v;
+  const int nvec = cbytes >> 4;           // 16-byte vectors per row
+  const int natom = ncols16 >> 2;         // 4-byte scale groups per row
+  for (int64_t r0 = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 8; r0 < nrows;
+       r0 += (((int64_t)gridDim.x * blockDim.x) >> 5) * 8) {
+    const int tl = (lane < 8 && r0 + lane < nrows) ? row_token[r0 + lane] : -1;
+    for (int v0 = 0; v0 < nvec; v0 += 64) {  // up to 64 vectors (1 KB) of every row per pass
+      uint4 buf[8][2];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int t = __shfl_sync(0xffffffffu, tl, q);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int v = v0 + lane + 32 * h;
+          buf[q][h] = make_uint4(0, 0, 0, 0);
+          if (t >= 0 && v < nvec) buf[q][h] = *reinterpret_cast<const uint4*>(ic + (int64_t)t * cbytes + 16 * v);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int64_t r = r0 + q;
+        if (r >= nrows) break;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int v = v0 + lane + 32 * h;
+          if (v < nvec) *reinterpret_cast<uint4*>(oc + r * cbytes + 16 * v) = buf[q][h];
+        }
+      }
     }
-    for (int a = lane; a < (ncols16 >> 2); a += 32) {
-      uint32_t v = 0;
-      if (t >= 0) v = *reinterpret_cast<const uint32_t*>(isf + (int64_t)t * ncols16 + 4 * a);
-      *reinterpret_cast<uint32_t*>(osf + sf_tc_offset(r, 4 * a, ncols16)) = v;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int t = __shfl_sync(0xffffffffu, tl, q);
+      const int64_t r = r0 + q;
+      if (r >= nrows) break;
+      for (int a = lane; a < natom; a += 32) {
+        uint32_t v = 0;
+        if (t >= 0) v = *reinterpret_cast<const uint32_t*>(isf + (int64_t)t * ncols16 + 4 * a);
+        *reinterpret_cast<uint32_t*>(osf + sf_tc_offset(r, 4 * a, ncols16)) = v;
+      }
     }
   }
 }
@@ -236,8 +268,8 @@ extern "C" quads_status_t quads_moe_route(const float* logits, int32_t tokens, i
   cudaStream_t st = (cudaStream_t)stream;
   cudaMemsetAsync(expert_counts, 0, (size_t)num_experts * 4, st);
   if (tokens > 0)
-    route_kernel<<<(tokens * 32 + 255) / 256, 256, 0, st>>>(logits, tokens, num_experts, topk,
-                                                             topk_idx, gates, expert_counts, emask);
+    route_kernel<<<std::min((tokens * 32 + 255) / 256, 2 * num_sms()), 256, 0, st>>>(
+        logits, tokens, num_experts, topk, topk_idx, gates, expert_counts, emask);
   plan_kernel<<<1, kMaxExperts, 0, st>>>(expert_counts, num_experts, expert_offsets);
   assign_kernel<<<num_experts, 1024, 0, st>>>(emask, tokens, num_experts, topk, expert_offsets,
                                               expert_counts, row_token, token_row);
@@ -256,7 +288,7 @@ extern "C" quads_status_t quads_moe_gather(const int32_t* row_token, const int32
   if (((uintptr_t)in_codes | (uintptr_t)out_codes) & 15u || ((uintptr_t)in_scales | (uintptr_t)out_scales) & 3u)
     return fail(QUADS_ERR_MISALIGNED, "moe_gather: alignment");
   cudaStream_t st = (cudaStream_t)stream;
-  const int blocks = (int)std::min<int64_t>((rows_capacity * 32 + 255) / 256, (int64_t)num_sms() * 16);
+  const int blocks = (int)std::min<int64_t>((rows_capacity / 8 * 32 + 255) / 256, (int64_t)num_sms() * 16);
   gather_kernel<<<blocks, 256, 0, st>>>(row_token, expert_offsets, num_experts, rows_capacity,
                                         (int)cols, in_codes, in_scales, out_codes, out_scales);
   return check_launch("moe_gather", 1);

@@ -86,7 +86,7 @@ template <bool kScores>
 __device__ __forceinline__ void quantize_row(const uint4& raw, float s_t, int lane, bool active,
                                              int64_t row, int col, int ncols16, uint8_t* codes,
                                              int64_t ldc, uint8_t* scales, int layout,
-                                             float2* acc) {
+                                             float* acc) {
   float f[8];
   bf16x8_to_f32(raw, f);
   float m = 0.0f;
@@ -102,12 +102,10 @@ __device__ __forceinline__ void quantize_row(const uint4& raw, float s_t, int la
   if (kScores) {
     float lv[8];
     e2m1x8_to_f32(c, lv);
-    const float2 d2 = make_float2(bs.d, bs.d);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 dq = __fmul2_rn(make_float2(lv[2 * j], lv[2 * j + 1]), d2);
-      const float2 R = __fadd2_rn(make_float2(f[2 * j], f[2 * j + 1]), make_float2(-dq.x, -dq.y));
-      acc[j] = __fadd2_rn(acc[j], __fmul2_rn(R, R));
+    for (int j = 0; j < 8; ++j) {
+      const float R = __fsub_rn(f[j], __fmul_rn(lv[j], bs.d));
+      acc[j] = __fadd_rn(acc[j], __fmul_rn(R, R));
     }
   }
 }
@@ -136,9 +134,9 @@ __global__ void __launch_bounds__(256) quantize_kernel(
     int g = goff ? group_of(goff, G, r0) : 0;
     int64_t gend = goff ? (int64_t)goff[g + 1] : end;
     float s_t = st[g];
-    float2 acc[4];
+    float acc[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[j] = make_float2(0.0f, 0.0f);
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
     auto load4 = [&](int64_t r, uint4* u) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -170,114 +168,162 @@ __global__ void __launch_bounds__(256) quantize_kernel(
     }
     if (kScores && active) {
       float4* p = reinterpret_cast<float4*>(partials + chunk * cols + col);
-      p[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
-      p[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+      p[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      p[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
   }
 }
 
 // ---------------------------------------------------------------- select
-// Channel scores: one warp per (group, channel).  The group's chunk partials
-// are added in ascending chunk order starting from 0: lane l holds 8
-// consecutive chunks, adds them to the running total it receives from lane
-// l-1, and hands the total on -- the same sequence of float32 adds as a single
-// loop over the chunks.
-__global__ void __launch_bounds__(256) score_kernel(const float* __restrict__ partials, int cols,
-                                                    const int32_t* __restrict__ goff, int G,
-                                                    int64_t rows, float* __restrict__ scores) {
-  const int lane = threadIdx.x & 31;
-  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (w >= (int64_t)G * cols) return;
-  const int g = (int)(w / cols);
-  const int c = (int)(w % cols);
+// Channel scores = the group's chunk partials added in ascending chunk order
+// starting from 0 (one float32 add per chunk).  Two launch shapes compute the
+// same sequence of adds:
+//  * long groups (many chunks): a block owns 32 channels of one group; each
+//    slice of up to 256 chunks is staged in shared memory (coalesced reads),
+//    then one warp per channel runs the chain: lane l adds chunks 8l..8l+7 to
+//    the running total handed on from lane l-1;
+//  * short groups: one thread per (group, channel) loops over the chunks.
+__global__ void __launch_bounds__(256) score_chain_kernel(const float* __restrict__ partials,
+                                                          int cols,
+                                                          const int32_t* __restrict__ goff,
+                                                          int64_t rows,
+                                                          float* __restrict__ scores) {
+  __shared__ float tile[256][33];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = blockIdx.y;
+  const int cbase = blockIdx.x * 32;
   const int64_t a = goff ? (int64_t)goff[g] : 0;
   const int64_t b = goff ? (int64_t)goff[g + 1] : rows;
-  const int64_t c0 = a / kScoreChunk;
-  const int64_t c1 = (b + kScoreChunk - 1) / kScoreChunk;
-  float t = 0.0f;
+  const int64_t c0 = a / kScoreChunk, c1 = (b + kScoreChunk - 1) / kScoreChunk;
+  float t[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // running totals of this warp's 4 channels
   for (int64_t base = c0; base < c1; base += 256) {
-    float v[8];
-    const int64_t my = base + 8 * lane;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = (my + i < c1) ? partials[(my + i) * cols + c] : 0.0f;
-    const int cnt = (int)max((int64_t)0, min((int64_t)8, c1 - my));
-#pragma unroll 1
-    for (int l = 0; l < 32; ++l) {
-      if (lane == l)
-        for (int i = 0; i < cnt; ++i) t = __fadd_rn(t, v[i]);
-      t = __shfl_sync(0xffffffffu, t, l);
+    const int n = (int)min((int64_t)256, c1 - base);
+    for (int i = warp; i < n; i += 8) {  // row i of the slice: 32 channels, coalesced
+      const int c = cbase + lane;
+      tile[i][lane] = c < cols ? partials[(base + i) * cols + c] : 0.0f;
     }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int ch = warp * 4 + q;  // channel within the block
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = (8 * lane + i < n) ? tile[8 * lane + i][ch] : 0.0f;
+      const int cnt = max(0, min(8, n - 8 * lane));
+      float tt = t[q];
+#pragma unroll 1
+      for (int l = 0; l < 32; ++l) {
+        if (lane == l)
+          for (int i = 0; i < cnt; ++i) tt = __fadd_rn(tt, v[i]);
+        tt = __shfl_sync(0xffffffffu, tt, l);
+      }
+      t[q] = tt;
+    }
+    __syncthreads();
   }
-  if (lane == 0) scores[(int64_t)g * cols + c] = t;
+  if (lane == 0)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int c = cbase + warp * 4 + q;
+      if (c < cols) scores[(int64_t)g * cols + c] = t[q];
+    }
 }
 
-// One block per group: bitonic sort of (score, ~index) keys descending, mark
-// the top k, compact the marked channels in ascending order.
+__global__ void __launch_bounds__(256) score_loop_kernel(const float* __restrict__ partials,
+                                                         int cols,
+                                                         const int32_t* __restrict__ goff,
+                                                         int64_t rows,
+                                                         float* __restrict__ scores) {
+  const int g = blockIdx.y;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  const int64_t a = goff ? (int64_t)goff[g] : 0;
+  const int64_t b = goff ? (int64_t)goff[g + 1] : rows;
+  const int64_t c0 = a / kScoreChunk, c1 = (b + kScoreChunk - 1) / kScoreChunk;
+  float t = 0.0f;
+  for (int64_t ch = c0; ch < c1; ch += 8) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = ch + i < c1 ? partials[(ch + i) * cols + c] : 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (ch + i < c1) t = __fadd_rn(t, v[i]);
+  }
+  scores[(int64_t)g * cols + c] = t;
+}
+
+// Top-k per group by radix selection on the score bit patterns (scores are
+// >= 0, so the unsigned order of the bits is the float order): find the k-th
+// largest key T byte by byte, take every channel with key > T and the
+// lowest-index channels with key == T, and write them in ascending order.
 __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ scores, int cols,
                                                     int k, int32_t* __restrict__ sel) {
-  extern __shared__ unsigned long long keys[];  // [npow2]
+  __shared__ int hist[256];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_need;
   __shared__ int warp_sums[32];
-  __shared__ int mask_words[256];               // cols <= 8192
-  const int g = blockIdx.x;
-  int npow2 = 1;
-  while (npow2 < cols) npow2 <<= 1;
-  for (int c = threadIdx.x; c < npow2; c += blockDim.x) {
-    unsigned long long key = 0ull;
-    if (c < cols)
-      key = ((unsigned long long)__float_as_uint(scores[(int64_t)g * cols + c]) << 32) |
-            (0xFFFFFFFFu - (uint32_t)c);
-    keys[c] = key;
+  const int g = blockIdx.y;
+  const float* sc = scores + (int64_t)g * cols;
+  constexpr int PER = 8;  // cols <= 8192 = 1024 threads x 8
+  uint32_t key[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int c = threadIdx.x + i * blockDim.x;
+    key[i] = c < cols ? __float_as_uint(sc[c]) : 0u;
   }
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) mask_words[i] = 0;
-  __syncthreads();
-  for (int size = 2; size <= npow2; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < npow2; i += blockDim.x) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const bool desc = (i & size) == 0;
-          const unsigned long long ki = keys[i], kj = keys[j];
-          if (desc ? (ki < kj) : (ki > kj)) { keys[i] = kj; keys[j] = ki; }
-        }
+  if (threadIdx.x == 0) { s_prefix = 0u; s_need = k; }
+  uint32_t mask_hi = 0u;  // bits already fixed in s_prefix
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    const uint32_t prefix = s_prefix;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int c = threadIdx.x + i * blockDim.x;
+      if (c < cols && (key[i] & mask_hi) == prefix) atomicAdd(&hist[(key[i] >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int need = s_need, bin = 255;
+      for (; bin > 0; --bin) {
+        if (hist[bin] >= need) break;
+        need -= hist[bin];
       }
-      __syncthreads();
+      s_need = need;
+      s_prefix = prefix | ((uint32_t)bin << shift);
     }
+    mask_hi |= 255u << shift;
+    __syncthreads();
   }
-  for (int i = threadIdx.x; i < k; i += blockDim.x) {
-    const uint32_t c = 0xFFFFFFFFu - (uint32_t)(keys[i] & 0xFFFFFFFFull);
-    atomicOr(&mask_words[c >> 5], 1 << (c & 31));
-  }
-  __syncthreads();
-  const int nwords = (cols + 31) >> 5;
-  int cnt = 0;
-  if (threadIdx.x < nwords) cnt = __popc(mask_words[threadIdx.x]);
-  int v = cnt;
+  const uint32_t T = s_prefix;
+  const int need_eq = s_need;  // how many channels with key == T are taken
+  // ordered pass over channels: selected = key > T, or key == T among the first need_eq
+  // equal keys in index order; chunks of 1024 channels, block-wide exclusive scans.
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int t = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += t;
-  }
-  if (lane == 31) warp_sums[w] = v;
-  __syncthreads();
-  if (w == 0) {
-    int s2 = warp_sums[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int t = __shfl_up_sync(0xffffffffu, s2, o);
-      if (lane >= o) s2 += t;
-    }
-    warp_sums[lane] = s2;
-  }
-  __syncthreads();
-  int base = v - cnt + (w > 0 ? warp_sums[w - 1] : 0);
-  if (threadIdx.x < nwords) {
-    uint32_t word = (uint32_t)mask_words[threadIdx.x];
-    while (word) {
-      const int bit = __ffs(word) - 1;
-      word &= word - 1;
-      sel[(int64_t)g * k + base++] = threadIdx.x * 32 + bit;
-    }
+  int taken_eq = 0, written = 0;
+  for (int i = 0; i < PER && i * (int)blockDim.x < cols; ++i) {
+    const int c = threadIdx.x + i * blockDim.x;
+    const bool eq = c < cols && key[i] == T;
+    const bool gt = c < cols && key[i] > T;
+    // rank among equal keys in this chunk
+    unsigned bal = __ballot_sync(0xffffffffu, eq);
+    int pre_eq = __popc(bal & ((1u << lane) - 1u));
+    if (lane == 0) warp_sums[w] = __popc(bal);
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int j = 0; j < 32; ++j) { if (j < w) before += warp_sums[j]; total += warp_sums[j]; }
+    const bool take = gt || (eq && taken_eq + before + pre_eq < need_eq);
+    __syncthreads();
+    bal = __ballot_sync(0xffffffffu, take);
+    const int pre_t = __popc(bal & ((1u << lane) - 1u));
+    if (lane == 0) warp_sums[w] = __popc(bal);
+    __syncthreads();
+    int before_t = 0, total_t = 0;
+    for (int j = 0; j < 32; ++j) { if (j < w) before_t += warp_sums[j]; total_t += warp_sums[j]; }
+    if (take) sel[(int64_t)g * k + written + before_t + pre_t] = c;
+    written += total_t;
+    taken_eq += total;
+    __syncthreads();
   }
 }
 
@@ -563,20 +609,20 @@ extern "C" quads_status_t quads_select_residual_channels(
     return fail(QUADS_ERR_WORKSPACE, "select: workspace needs %zu bytes", need);
   if (rows == 0) return QUADS_OK;
   cudaStream_t st = (cudaStream_t)stream;
-  int npow2 = 1;
-  while (npow2 < cols) npow2 <<= 1;
-  const size_t smem = (size_t)npow2 * 8;
-  if (smem > 48 * 1024)
-    cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   float* rs = (float*)workspace;
   const size_t rs_bytes = ((size_t)rows * k * 4 + 255) & ~(size_t)255;
   uint32_t* amax = (uint32_t*)((char*)workspace + rs_bytes);
   float* scores = scores_out ? scores_out
                              : (float*)((char*)workspace + rs_bytes + (((size_t)G * 4 + 255) & ~(size_t)255));
-  const int64_t nw = (int64_t)G * cols;
-  score_kernel<<<(int)((nw * 32 + 255) / 256), 256, 0, st>>>(score_partials, (int)cols,
-                                                             group_offsets, G, rows, scores);
-  topk_kernel<<<G, 1024, smem, st>>>(scores, (int)cols, k, sel);
+  // chunks per group on average decides the launch shape (both give the same sums)
+  const int64_t chunks_per_group = (rows + 31) / 32 / G;
+  if (chunks_per_group > 64)
+    score_chain_kernel<<<dim3((unsigned)((cols + 31) / 32), (unsigned)G), 256, 0, st>>>(
+        score_partials, (int)cols, group_offsets, rows, scores);
+  else
+    score_loop_kernel<<<dim3((unsigned)((cols + 255) / 256), (unsigned)G), 256, 0, st>>>(
+        score_partials, (int)cols, group_offsets, rows, scores);
+  topk_kernel<<<dim3(1, (unsigned)G), 1024, 0, st>>>(scores, (int)cols, k, sel);
   cudaMemsetAsync(amax, 0, (size_t)G * 4, st);
   rsel_residual_kernel<<<grid_for((rows + 31) / 32, 1, 16), 256, 0, st>>>(
       (const __nv_bfloat16*)x, rows, (int)cols, ldx, group_offsets, G, scales, scale_layout,
