@@ -9,13 +9,16 @@
 // correction loop into a second one, and the epilogue forms a1*acc1 + a2*acc2.
 //
 // Design (one CTA per SM, 128x128 output tiles, K tiles of 256 FP4 = 128 B):
-//   warp 0     TMA producer: A/B code tiles by tensor-map TMA (128B swizzle),
-//              scale-factor atoms by bulk copy, into a 6-stage smem ring.
-//   warp 1     TMEM allocator + MMA issuer (one thread): tcgen05.cp moves the
-//              stage's scale atoms into TMEM, then tcgen05.mma
-//              .kind::mxf4nvf4.block_scale.scale_vec::4X (M=128, N=128, K=64).
-//   warps 2-9  epilogue: tcgen05.ld of both accumulators, scale, store; two
-//              warps per TMEM lane quadrant, each owning half of the columns.
+//   warp 0      TMA producer: A/B code tiles by tensor-map TMA (128B swizzle),
+//               scale-factor atoms by bulk copy, into a 6-stage smem ring.
+//   warp 1      TMEM allocator + MMA issuer (one thread):
+//               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (M=128, N=128, K=64).
+//   warps 2-5   scale staging: each warp (one TMEM lane quadrant) reads the
+//               stage's scale atoms from smem and writes them into TMEM with
+//               tcgen05.st (issuing tcgen05.cp from the MMA thread instead
+//               costs ~130 cycles of issue latency per copy, 8 per stage).
+//   warps 6-13  epilogue: tcgen05.ld of both accumulators, scale, store; two
+//               warps per TMEM lane quadrant, each owning half of the columns.
 // TMEM columns: acc1 double-buffered (0-127, 128-255), acc2 (256-383),
 // scale-factor ring (384-511, 4 buffers x 32 columns).
 // Every mbarrier wait is bounded; on timeout the kernel latches an error word,
@@ -38,8 +41,10 @@ constexpr int A_TILE = BM * BK_BYTES;         // 16 KB
 constexpr int B_TILE = BN * BK_BYTES;         // 16 KB
 constexpr int SF_TILE = 4 * 512;              // 4 atoms (128 rows x 16 blocks)
 constexpr int STAGE_BYTES = A_TILE + B_TILE + 2 * SF_TILE;
-constexpr int NUM_THREADS = 320;               // 10 warps: producer, MMA, 8 epilogue
+constexpr int NUM_THREADS = 448;  // 14 warps: producer, MMA, 4 scale staging, 8 epilogue
 constexpr int EPI_THREADS = 256;
+constexpr int SF_THREADS = 128;
+constexpr int SF_WARP0 = 2, EPI_WARP0 = 6;
 constexpr int TMEM_COLS = 512;
 constexpr int ACC2_COL = 256;
 constexpr int SF_COL = 384;
@@ -163,25 +168,12 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
   d |= (uint64_t)2 << 61;             // 128-byte swizzle
   return d;
 }
-// Descriptor of one 512-byte scale atom: 32 rows of 16 bytes, no swizzle,
-// 8-row core matrices 128 bytes apart.
-__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)(128 >> 4) << 32;
-  d |= (uint64_t)1 << 46;
-  return d;
-}
-
 // Instruction descriptor: kind::mxf4nvf4, A and B E2M1, K-major, UE4M3 scales,
 // scale-factor ids 0, dense.
 __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
   return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc));
-}
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                        uint32_t sfa, uint32_t sfb, uint32_t acc) {
   asm volatile(
@@ -202,6 +194,14 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float* v) {
       : "r"(taddr));
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
 }
 __device__ __forceinline__ void tc_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -267,7 +267,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* full = bars;                 // [STAGES]
   uint64_t* empty = bars + STAGES;       // [STAGES]
   uint64_t* sf_free = bars + 2 * STAGES; // [4]
-  uint64_t* acc_full = sf_free + 4;      // [2]
+  uint64_t* sf_ready = sf_free + 4;      // [4]
+  uint64_t* acc_full = sf_ready + 4;     // [2]
   uint64_t* acc_empty = acc_full + 2;    // [2]
   uint32_t* tmem_holder = (uint32_t*)(acc_empty + 2);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
-    for (int i = 0; i < 4; ++i) mbar_init(&sf_free[i], 1);
+    for (int i = 0; i < 4; ++i) { mbar_init(&sf_free[i], 1); mbar_init(&sf_ready[i], SF_THREADS); }
     for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], EPI_THREADS); }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -379,19 +380,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t ph = (it / STAGES) & 1;
         if (!wait_bar(&full[s], ph, abort_flag, p.err)) { ok = false; break; }
         const uint32_t sb = it & 3;
-        if (!wait_bar(&sf_free[sb], ((it >> 2) & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
+        // the staging warps have written this stage's scales into TMEM buffer sb
+        if (!wait_bar(&sf_ready[sb], (it >> 2) & 1, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
         const int klen = corr ? p.kpad : p.K;
         const int nsteps = min(4, (klen - kk * 256) / 64);
         uint8_t* st = smem + s * STAGE_BYTES;
         const uint32_t sa = smem_u32(st), sbb = smem_u32(st + A_TILE);
-        const uint32_t ssfa = smem_u32(st + A_TILE + B_TILE);
-        const uint32_t ssfb = ssfa + SF_TILE;
         const uint32_t tsf = tmem + SF_COL + sb * 32;
-        for (int q = 0; q < nsteps; ++q) {
-          tc_cp_sf(tsf + q * 4, desc_sf(ssfa + q * 512));
-          tc_cp_sf(tsf + 16 + q * 4, desc_sf(ssfb + q * 512));
-        }
         const uint32_t dcol = corr ? (tmem + ACC2_COL) : (tmem + b * BN);
         for (int q = 0; q < nsteps; ++q) {
           tc_mma(dcol, desc_sw128(sa + q * 32), desc_sw128(sbb + q * 32), idesc, tsf + q * 4,
@@ -403,10 +399,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       tc_commit(&acc_full[b]);
     }
-  } else if (warp >= 2) {
+  } else if (warp >= SF_WARP0 && warp < EPI_WARP0) {
+    // ------------------------------------------------------------ scale staging
+    // Lane l of every quadrant gets, at column SF_COL + 32*sb + 4*q + j (A) and
+    // +16 (B), the scale word of row l + 32*j for K step q -- row l of the
+    // stage's scale atom q -- the layout the block-scaled MMA reads (row r's
+    // four scales at lane r % 32, column r / 32).
+    const int quad = warp & 3;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      for (int kt = 0; kt < KT + KTc; ++kt, ++it) {
+        const int s = it % STAGES;
+        const uint32_t sb = it & 3;
+        int okw = 1;
+        if (lane == 0) {
+          okw = wait_bar(&full[s], (it / STAGES) & 1, abort_flag, p.err) ? 1 : 0;
+          if (okw) okw = wait_bar(&sf_free[sb], ((it >> 2) & 1) ^ 1, abort_flag, p.err) ? 1 : 0;
+        }
+        okw = __shfl_sync(0xffffffffu, okw, 0);
+        if (!okw) { ok = false; break; }
+        tc_fence_after();
+        const uint8_t* sfa = smem + s * STAGE_BYTES + A_TILE + B_TILE;
+        uint32_t va[16], vb[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 a = *reinterpret_cast<const uint4*>(sfa + q * 512 + lane * 16);
+          const uint4 bq = *reinterpret_cast<const uint4*>(sfa + SF_TILE + q * 512 + lane * 16);
+          va[4 * q] = a.x; va[4 * q + 1] = a.y; va[4 * q + 2] = a.z; va[4 * q + 3] = a.w;
+          vb[4 * q] = bq.x; vb[4 * q + 1] = bq.y; vb[4 * q + 2] = bq.z; vb[4 * q + 3] = bq.w;
+        }
+        const uint32_t taddr = tmem + lane_base + SF_COL + sb * 32;
+        tc_st16(taddr, va);
+        tc_st16(taddr + 16, vb);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        mbar_arrive(&sf_ready[sb]);
+      }
+    }
+  } else if (warp >= EPI_WARP0) {
     // ------------------------------------------------------------ epilogue
-    const int quad = warp & 3;         // TMEM lane quadrant this warp may access
-    const int half = (warp - 2) >> 2;  // which half of the tile's columns
+    const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int half = (warp - EPI_WARP0) >> 2;  // which half of the tile's columns
     const int row_in_tile = quad * 32 + lane;
     uint32_t j = 0;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++j) {
@@ -433,6 +468,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll 1
         for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
           float g1[16], u1[16], g2[16], u2[16];
+          __syncwarp();  // tcgen05.ld is warp-collective: the row-masked stores above diverge
           tc_ld16(t1 + c0, g1);
           tc_ld16(t1 + 64 + c0, u1);
           if (p.comp) { tc_ld16(t2 + c0, g2); tc_ld16(t2 + 64 + c0, u2); }
@@ -464,6 +500,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll 1
         for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
           float v1[16], v2[16];
+          __syncwarp();  // tcgen05.ld is warp-collective: the row-masked stores above diverge
           tc_ld16(t1 + c0, v1);
           if (p.comp) tc_ld16(t2 + c0, v2);
           tc_wait_ld();
@@ -494,6 +531,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
+      __syncwarp();
       tc_fence_before();
       mbar_arrive(&acc_empty[b]);
       if (p.y_amax) {

@@ -19,16 +19,12 @@ constexpr int kMaxTopk = 16;
 // One warp per token.  Lane l holds logits l, l+32, ...; round r takes the
 // warp arg-max (ties -> lower expert id), removes it, and lane r keeps it.
 // The chosen experts are then ranked by id (ascending slot order), gates are
-// exp(l - lmax) / sum over the chosen, the token's expert set is written as a
-// bit mask, and per-expert counts go through a shared-memory histogram.
+// exp(l - lmax) / sum over the chosen, and the token's expert set is written as
+// a bit mask (the plan kernel counts from the masks).
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T,
                                                     int E, int topk, int32_t* __restrict__ idx,
                                                     float* __restrict__ gates,
-                                                    int32_t* __restrict__ counts,
                                                     uint32_t* __restrict__ emask) {
-  __shared__ int hist[kMaxExperts];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
-  __syncthreads();
   const int lane = threadIdx.x & 31;
   const int words = (E + 31) >> 5;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T;
@@ -77,7 +73,6 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
     if (mine) {
       idx[(int64_t)t * topk + rank] = my_e;
       gates[(int64_t)t * topk + rank] = p / s;
-      atomicAdd(&hist[my_e], 1);
     }
     for (int w = 0; w < words; ++w) {
       const uint32_t bit = (mine && (my_e >> 5) == w) ? (1u << (my_e & 31)) : 0u;
@@ -85,22 +80,56 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
       if (lane == 0) emask[(int64_t)t * words + w] = m;
     }
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    if (hist[e]) atomicAdd(&counts[e], hist[e]);
 }
 
-// Padded offsets: off[e+1] = off[e] + roundup(count[e], 128).  One block.
-__global__ void plan_kernel(const int32_t* __restrict__ counts, int E, int32_t* __restrict__ off) {
-  __shared__ int s[kMaxExperts];
-  const int e = threadIdx.x;
-  if (e < E) s[e] = (counts[e] + QUADS_MOE_ROW_ALIGN - 1) / QUADS_MOE_ROW_ALIGN * QUADS_MOE_ROW_ALIGN;
+// Expert counts from the token masks (shared-memory histogram, order-free
+// integer adds), then padded offsets off[e+1] = off[e] + roundup(count[e], 128).
+// One block of 1024 threads.
+__global__ void __launch_bounds__(1024) plan_kernel(const uint32_t* __restrict__ emask, int T,
+                                                    int E, int32_t* __restrict__ counts,
+                                                    int32_t* __restrict__ off) {
+  __shared__ int hist[kMaxExperts];
+  __shared__ int warp_sums[32];
+  const int words = (E + 31) >> 5;
+  for (int e = threadIdx.x; e < kMaxExperts; e += blockDim.x) hist[e] = 0;
   __syncthreads();
-  if (e == 0) {
-    int acc = 0;
-    off[0] = 0;
-    for (int i = 0; i < E; ++i) { acc += s[i]; off[i + 1] = acc; }
+  const int64_t nw = (int64_t)T * words;
+  for (int64_t i = threadIdx.x; i < nw; i += blockDim.x) {
+    uint32_t m = emask[i];
+    const int base = (int)(i % words) * 32;
+    while (m) {
+      const int b = __ffs(m) - 1;
+      m &= m - 1;
+      atomicAdd(&hist[base + b], 1);
+    }
   }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int cnt = threadIdx.x < E ? hist[threadIdx.x] : 0;
+  if (threadIdx.x < E) counts[threadIdx.x] = cnt;
+  int v = (cnt + QUADS_MOE_ROW_ALIGN - 1) / QUADS_MOE_ROW_ALIGN * QUADS_MOE_ROW_ALIGN;
+  const int padded = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+  }
+  if (lane == 31) warp_sums[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    int x = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += u;
+    }
+    warp_sums[lane] = x;
+  }
+  __syncthreads();
+  const int incl = v + (w > 0 ? warp_sums[w - 1] : 0);
+  if (threadIdx.x < E) off[threadIdx.x + 1] = incl;
+  if (threadIdx.x == 0) off[0] = 0;
+  (void)padded;
 }
 
 // One block per expert: thread i covers a contiguous run of tokens, counts the
@@ -266,11 +295,10 @@ extern "C" quads_status_t quads_moe_route(const float* logits, int32_t tokens, i
     return fail(QUADS_ERR_WORKSPACE, "moe_route: workspace needs %zu bytes", need);
   uint32_t* emask = (uint32_t*)workspace;
   cudaStream_t st = (cudaStream_t)stream;
-  cudaMemsetAsync(expert_counts, 0, (size_t)num_experts * 4, st);
   if (tokens > 0)
-    route_kernel<<<std::min((tokens * 32 + 255) / 256, 2 * num_sms()), 256, 0, st>>>(
-        logits, tokens, num_experts, topk, topk_idx, gates, expert_counts, emask);
-  plan_kernel<<<1, kMaxExperts, 0, st>>>(expert_counts, num_experts, expert_offsets);
+    route_kernel<<<(tokens * 32 + 255) / 256, 256, 0, st>>>(logits, tokens, num_experts, topk,
+                                                             topk_idx, gates, emask);
+  plan_kernel<<<1, 1024, 0, st>>>(emask, tokens, num_experts, expert_counts, expert_offsets);
   assign_kernel<<<num_experts, 1024, 0, st>>>(emask, tokens, num_experts, topk, expert_offsets,
                                               expert_counts, row_token, token_row);
   return check_launch("moe_route", tokens > 0 ? 3 : 2);

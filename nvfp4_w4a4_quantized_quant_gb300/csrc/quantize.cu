@@ -283,14 +283,31 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ sc
       if (c < cols && (key[i] & mask_hi) == prefix) atomicAdd(&hist[(key[i] >> shift) & 255u], 1);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int need = s_need, bin = 255;
-      for (; bin > 0; --bin) {
-        if (hist[bin] >= need) break;
-        need -= hist[bin];
+    if (threadIdx.x < 32) {
+      // warp 0: lane l owns bins 255-8l .. 248-8l (descending); find the bin in
+      // which the running count from the top reaches `need`
+      const int lane = threadIdx.x;
+      int c8[8], lsum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) { c8[i] = hist[255 - 8 * lane - i]; lsum += c8[i]; }
+      int incl = lsum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
       }
-      s_need = need;
-      s_prefix = prefix | ((uint32_t)bin << shift);
+      const int need = s_need;
+      const int excl = incl - lsum;
+      const unsigned found = __ballot_sync(0xffffffffu, excl < need && incl >= need);
+      if (lane == __ffs(found) - 1) {
+        int nd = need - excl, i = 0;
+        for (; i < 7; ++i) {
+          if (c8[i] >= nd) break;
+          nd -= c8[i];
+        }
+        s_need = nd;
+        s_prefix = prefix | ((uint32_t)(255 - 8 * lane - i) << shift);
+      }
     }
     mask_hi |= 255u << shift;
     __syncthreads();
@@ -320,7 +337,8 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ sc
     __syncthreads();
     int before_t = 0, total_t = 0;
     for (int j = 0; j < 32; ++j) { if (j < w) before_t += warp_sums[j]; total_t += warp_sums[j]; }
-    if (take) sel[(int64_t)g * k + written + before_t + pre_t] = c;
+    const int pos = written + before_t + pre_t;
+    if (take && pos < k) sel[(int64_t)g * k + pos] = c;
     written += total_t;
     taken_eq += total;
     __syncthreads();
