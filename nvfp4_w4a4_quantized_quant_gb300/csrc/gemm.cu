@@ -127,6 +127,25 @@ __device__ __forceinline__ bool wait_bar(uint64_t* b, uint32_t parity, volatile 
   }
 }
 
+// One lane of the (fully active) warp returns true.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// Bounded wait for a whole warp: lane 0 polls, the warp follows its verdict.
+__device__ __forceinline__ bool warp_wait_bar(uint64_t* b, uint32_t parity,
+                                              volatile int* abort_flag, int* err) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(b, parity, abort_flag, err) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
                                             uint64_t* bar) {
   asm volatile(
@@ -316,8 +335,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int64_t a_sf_rb = (int64_t)(p.K / 64) * 512;    // bytes per 128-row block
   const int64_t r_sf_rb = (int64_t)(p.kpad / 64) * 512;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // The whole warp runs the loop (so addresses and coordinates stay
+    // warp-uniform); one elected lane issues the copies.
     uint32_t it = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
@@ -326,12 +347,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int kt = 0; kt < KT + KTc && ok; ++kt, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
-        if (!wait_bar(&empty[s], ph ^ 1, abort_flag, p.err)) { ok = false; break; }
+        if (!warp_wait_bar(&empty[s], ph ^ 1, abort_flag, p.err)) { ok = false; break; }
         const bool corr = kt >= KT;
         const int kk = corr ? kt - KT : kt;
         const int klen = corr ? p.kpad : p.K;
         const int nsteps = min(4, (klen - kk * 256) / 64);
         uint8_t* st = smem + s * STAGE_BYTES;
+        if (elect_one()) {
         mbar_expect_tx(&full[s], A_TILE + B_TILE + 2 * nsteps * 512);
         if (!corr) {
           tma_load_2d(st, &tmA, kk * BK_BYTES, (int)tl.m0, &full[s]);
@@ -348,40 +370,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           bulk_load(st + A_TILE + B_TILE + SF_TILE, p.ws_sf + (brow / BN) * r_sf_rb + kk * SF_TILE,
                     nsteps * 512, &full[s]);
         }
+        }
+        __syncwarp();
       }
     }
-    if (!ok && it > 0) {
+    if (!ok && it > 0 && lane == 0) {
       // let copies already issued land before the CTA can exit
       const uint32_t last = it - 1;
       wait_bar(&full[last % STAGES], (last / STAGES) & 1, abort_flag, p.err);
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs the loop so descriptors and TMEM addresses are
+    // warp-uniform values; one elected lane issues each tcgen05 instruction.
+    // (Issuing from a lone divergent lane with per-stage operands made every
+    // MMA issue ~2.5x slower.)
     constexpr uint32_t idesc = idesc_nvf4(BM, BN);
     uint32_t it = 0;
     uint32_t j = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++j) {
       const uint32_t b = j & 1;
-      if (!wait_bar(&acc_empty[b], ((j >> 1) & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
+      if (!warp_wait_bar(&acc_empty[b], ((j >> 1) & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
       tc_fence_after();
       for (int kt = 0; kt < KT + KTc && ok; ++kt, ++it) {
         const bool corr = kt >= KT;
         const int kk = corr ? kt - KT : kt;
         if (corr && kk == 0 && j > 0) {
           // acc2 is free once the previous tile's epilogue is done
-          if (!wait_bar(&acc_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.err)) {
+          if (!warp_wait_bar(&acc_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
         }
         const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        if (!wait_bar(&full[s], ph, abort_flag, p.err)) { ok = false; break; }
         const uint32_t sb = it & 3;
-        // the staging warps have written this stage's scales into TMEM buffer sb
-        if (!wait_bar(&sf_ready[sb], (it >> 2) & 1, abort_flag, p.err)) { ok = false; break; }
+        // the staging warps waited for this stage's TMA data (full[s]) and have
+        // written its scales into TMEM buffer sb: one barrier covers both
+        if (!warp_wait_bar(&sf_ready[sb], (it >> 2) & 1, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
         const int klen = corr ? p.kpad : p.K;
         const int nsteps = min(4, (klen - kk * 256) / 64);
@@ -389,15 +416,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t sa = smem_u32(st), sbb = smem_u32(st + A_TILE);
         const uint32_t tsf = tmem + SF_COL + sb * 32;
         const uint32_t dcol = corr ? (tmem + ACC2_COL) : (tmem + b * BN);
-        for (int q = 0; q < nsteps; ++q) {
-          tc_mma(dcol, desc_sw128(sa + q * 32), desc_sw128(sbb + q * 32), idesc, tsf + q * 4,
-                 tsf + 16 + q * 4, (kk > 0 || q > 0) ? 1u : 0u);
+        if (elect_one()) {
+          for (int q = 0; q < nsteps; ++q) {
+            tc_mma(dcol, desc_sw128(sa + q * 32), desc_sw128(sbb + q * 32), idesc, tsf + q * 4,
+                   tsf + 16 + q * 4, (kk > 0 || q > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[s]);
+          tc_commit(&sf_free[sb]);
         }
-        tc_commit(&empty[s]);
-        tc_commit(&sf_free[sb]);
+        __syncwarp();
       }
       if (!ok) break;
-      tc_commit(&acc_full[b]);
+      if (elect_one()) tc_commit(&acc_full[b]);
+      __syncwarp();
     }
   } else if (warp >= SF_WARP0 && warp < EPI_WARP0) {
     // ------------------------------------------------------------ scale staging
