@@ -193,6 +193,37 @@ quads_status_t quads_select_residual_channels(
     size_t workspace_bytes, void* stream);
 
 /*
+ * quads_select_residual_channels_noalloc -- the same computation and outputs as
+ * quads_select_residual_channels, for callers that cannot allocate device
+ * memory and so cannot pass a workspace: e.g. a host runtime that owns every
+ * device buffer and forbids allocation while it runs, a framework capturing a
+ * CUDA graph with its memory pool frozen, or a process that never links an
+ * allocator.  The pages have no counterpart to this call; it only changes where
+ * the scratch lives.
+ *
+ * The scratch is one array compiled into the library (a file-scope __device__
+ * variable of QUADS_NOALLOC_SELECT_SCRATCH_BYTES bytes) that every GPU loading
+ * the library holds until the process exits.  The call allocates nothing
+ * itself: no cudaMalloc/cudaFree and no allocating library routine.
+ *   - Shapes whose scratch, quads_workspace_size(QUADS_OP_SELECT, rows, cols, 0,
+ *     k, num_groups), exceeds the array are rejected with QUADS_ERR_WORKSPACE.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *     first call before any stream capture.
+ *   - Every call on a device uses the same array, which keeps the previous
+ *     call's contents (the parts that must start at zero are cleared by each
+ *     call).  Calls that overlap on the GPU -- on different streams, or from
+ *     different host threads without ordering -- race on it.
+ * Arguments are those of quads_select_residual_channels without the workspace.
+ */
+#define QUADS_NOALLOC_SELECT_SCRATCH_BYTES (32u << 20)
+quads_status_t quads_select_residual_channels_noalloc(
+    const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* group_offsets,
+    int32_t num_groups, const uint8_t* scales, int32_t scale_layout, const float* tensor_scale,
+    const float* score_partials, int32_t k, int32_t* sel, float* scores_out, uint8_t* r_codes,
+    uint8_t* r_scales, int32_t r_scale_layout, float* r_tensor_scale, void* stream);
+
+/*
  * quads_w4a4_gemm_comp -- Y = s_a s_w Q(A) Q(W)^T + s_r s_w Q(R_sel) Q(W_sel)^T
  * in one kernel on the tcgen05 block-scaled tensor cores (two TMEM
  * accumulators summed in the epilogue).  [QUADS] 2.2 B "Mechanism" (correction

@@ -38,6 +38,8 @@ _SIGS = {
                                     _I32, _P, _P, _P, _SZ, _P]),
     "quads_select_residual_channels": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _I32, _P, _P,
                                               _I32, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P]),
+    "quads_select_residual_channels_noalloc": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _I32, _P,
+                                                      _P, _I32, _P, _P, _P, _P, _I32, _P, _P]),
     "quads_w4a4_gemm_comp": (_I32, [_I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                     _P, _P, _I32, _P, _I32, _I64, _P, _SZ, _P]),
     "quads_moe_grouped_gemm": (_I32, [_I32, _I64, _I64, _I64, _P, _P, _P, _P, _P, _I32, _P, _P,
@@ -200,6 +202,33 @@ def select_residual_channels(x: torch.Tensor, q: QTensor, partials: torch.Tensor
         _ptr(q.tensor_scale), _ptr(partials), k, _ptr(sel), _ptr(sc), _ptr(rc), _ptr(rs),
         r_scale_layout, _ptr(rts), _ptr(ws), ws.numel(), _stream(stream)),
         "select_residual_channels")
+    return sel, sc, QTensor(rc, rs, rts, rows, kp, r_scale_layout)
+
+
+def select_residual_channels_noalloc(x: torch.Tensor, q: QTensor, partials: torch.Tensor, k: int, *,
+                                     group_offsets=None, num_groups: int = 1,
+                                     r_scale_layout: int = LINEAR, want_scores: bool = False,
+                                     out=None, stream=None):
+    """As select_residual_channels, with the library's built-in scratch array instead of
+    a workspace (for callers that cannot allocate)."""
+    lib = load()
+    G = num_groups if group_offsets is not None else 1
+    rows, cols = q.rows, q.cols
+    kp = kpad(k)
+    dev = x.device
+    if out is None:
+        sel = torch.empty((G, k), dtype=torch.int32, device=dev)
+        rc = torch.empty((rows, kp // 2), dtype=torch.uint8, device=dev)
+        nsf = sf_tc_bytes(rows, kp) if r_scale_layout == TCGEN05 else rows * (kp // 16)
+        rs = torch.empty(nsf, dtype=torch.uint8, device=dev)
+        rts = torch.empty(G, dtype=torch.float32, device=dev)
+    else:
+        sel, rc, rs, rts = out
+    sc = torch.empty((G, cols), dtype=torch.float32, device=dev) if want_scores else None
+    _check(lib.quads_select_residual_channels_noalloc(
+        _ptr(x), rows, cols, x.stride(0), _ptr(group_offsets), G, _ptr(q.scales), q.layout,
+        _ptr(q.tensor_scale), _ptr(partials), k, _ptr(sel), _ptr(sc), _ptr(rc), _ptr(rs),
+        r_scale_layout, _ptr(rts), _stream(stream)), "select_residual_channels_noalloc")
     return sel, sc, QTensor(rc, rs, rts, rows, kp, r_scale_layout)
 
 
