@@ -8,19 +8,32 @@
 // kernel: the main K loop accumulates into one TMEM accumulator, the k-channel
 // correction loop into a second one, and the epilogue forms a1*acc1 + a2*acc2.
 //
-// Design (one CTA per SM, 128x128 output tiles, K tiles of 256 FP4 = 128 B):
-//   warp 0      TMA producer: A/B code tiles by tensor-map TMA (128B swizzle),
-//               scale-factor atoms by bulk copy, into a 6-stage smem ring.
-//   warp 1      TMEM allocator + MMA issuer (one thread):
+// Design (one CTA per SM, 128x128 output tiles, K tiles of 512 FP4 = 256 B):
+//   warps 0-2   TMA producers: A/B code tiles by tensor-map TMA (128B
+//               swizzle) and scale atoms by bulk copy into a 3-stage x 72 KB
+//               smem ring; a 512-element K tile is four 16 KB boxes (A and B,
+//               two 128-byte sub-tiles each) and two 4 KB atom runs, dealt to
+//               the three warps in turn.  One issuing warp
+//               moves only ~29 B/cycle into its SM (its copies are processed
+//               one after another); three keep up with the ~70 B/cycle/SM
+//               that L2 delivers when every SM is loading.
+//   warp 3      TMEM allocator + MMA issuer.  The warp stays converged: all
+//               lanes poll the barriers and run every tcgen05 instruction,
+//               predicated inside the asm on an elect.sync lane (a branch on
+//               the elected lane plus __syncwarp costs ~200 cycles a stage):
 //               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (M=128, N=128, K=64).
-//   warps 2-5   scale staging: each warp (one TMEM lane quadrant) reads the
-//               stage's scale atoms from smem and writes them into TMEM with
-//               tcgen05.st (issuing tcgen05.cp from the MMA thread instead
-//               costs ~130 cycles of issue latency per copy, 8 per stage).
-//   warps 6-13  epilogue: tcgen05.ld of both accumulators, scale, store; two
+//   warps 4-7   scale staging: once a stage has landed, each warp copies a
+//               quarter of its scale atoms from smem into TMEM with tcgen05.cp
+//               (issued from four warps because each copy holds its issuing
+//               thread for ~100 cycles) and its tcgen05.commit tells the MMA
+//               warp when they are in place.  Reading the atoms with
+//               ld.shared instead stalls for ~1-7K cycles while the MMAs
+//               stream their operands (they take the whole smem bandwidth),
+//               and loading them from global memory exposes L2 latency.
+//   warps 8-15  epilogue: tcgen05.ld of both accumulators, scale, store; two
 //               warps per TMEM lane quadrant, each owning half of the columns.
 // TMEM columns: acc1 double-buffered (0-127, 128-255), acc2 (256-383),
-// scale-factor ring (384-511, 4 buffers x 32 columns).
+// scale-factor ring (384-511, 2 buffers x 64 columns).
 // Every mbarrier wait is bounded; on timeout the kernel latches an error word,
 // stops all roles, and still releases its TMEM.
 #include <cuda.h>
@@ -35,16 +48,26 @@ namespace quads {
 namespace gemm {
 
 constexpr int BM = 128, BN = 128;
-constexpr int BK_BYTES = 128;                 // 256 FP4 elements per K tile
-constexpr int STAGES = 6;
-constexpr int A_TILE = BM * BK_BYTES;         // 16 KB
-constexpr int B_TILE = BN * BK_BYTES;         // 16 KB
-constexpr int SF_TILE = 4 * 512;              // 4 atoms (128 rows x 16 blocks)
-constexpr int STAGE_BYTES = A_TILE + B_TILE + 2 * SF_TILE;
-constexpr int NUM_THREADS = 448;  // 14 warps: producer, MMA, 4 scale staging, 8 epilogue
+constexpr int KSUB = 128;                     // bytes per row of one 128B-swizzled sub-tile (256 FP4)
+constexpr int KSUBS = 2;                      // sub-tiles per stage: K tile = 512 FP4
+constexpr int KSTEPS = 4 * KSUBS;             // K=64 MMA steps per stage
+constexpr int KTILE = 256 * KSUBS;            // FP4 elements per stage
+constexpr int STAGES = 3;
+constexpr int A_SUB = BM * KSUB;              // 16 KB
+constexpr int B_SUB = BN * KSUB;              // 16 KB
+constexpr int A_TILE = A_SUB * KSUBS;
+constexpr int B_TILE = B_SUB * KSUBS;
+constexpr int SF_TILE = KSTEPS * 512;         // scale atoms (128 rows x 4 blocks each) per operand
+constexpr int STAGE_BYTES = A_TILE + B_TILE + 2 * SF_TILE;  // 72 KB
+constexpr int BOXES = 2 * KSUBS;              // TMA boxes per stage: A0, B0, A1, B1
+constexpr int COPIES = BOXES + 2;             // + the SFA and SFB atom runs (bulk copies)
+constexpr int SF_BUFS = 2;                    // TMEM scale buffers
+constexpr int SF_BUF_COLS = 2 * 4 * KSTEPS;   // SFA 32 + SFB 32 columns
+constexpr int PRODUCERS = 3;
+constexpr int NUM_THREADS = 512;  // 16 warps: 3 producers, MMA, 4 scale staging, 8 epilogue
 constexpr int EPI_THREADS = 256;
-constexpr int SF_THREADS = 128;
-constexpr int SF_WARP0 = 2, EPI_WARP0 = 6;
+constexpr int SF_WARPS = 4;
+constexpr int MMA_WARP = 3, SF_WARP0 = 4, EPI_WARP0 = 8;
 constexpr int TMEM_COLS = 512;
 constexpr int ACC2_COL = 256;
 constexpr int SF_COL = 384;
@@ -138,6 +161,29 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// Bounded wait polled by every lane of a converged warp; the warp leaves together.
+__device__ __forceinline__ bool conv_wait_bar(uint64_t* b, uint32_t parity,
+                                              volatile int* abort_flag, int* err) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(b, parity))) return true;
+  const unsigned long long t0 = global_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(b, parity))) return true;
+    if ((++spins & 255u) == 0) {
+      int give_up = *abort_flag ? 1 : 0;
+      if (!give_up && global_ns() - t0 > kTimeoutNs) give_up = 2;
+      give_up = __shfl_sync(0xffffffffu, give_up, 0);
+      if (give_up) {
+        if (give_up == 2 && (threadIdx.x & 31) == 0) {
+          *abort_flag = 1;
+          atomicExch(err, QUADS_ERR_DEVICE_TIMEOUT);
+        }
+        return false;
+      }
+    }
+  }
+}
+
 // Bounded wait for a whole warp: lane 0 polls, the warp follows its verdict.
 __device__ __forceinline__ bool warp_wait_bar(uint64_t* b, uint32_t parity,
                                               volatile int* abort_flag, int* err) {
@@ -169,12 +215,6 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void tc_commit(uint64_t* b) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(b))
-      : "memory");
-}
 
 // Shared-memory matrix descriptor: K-major operand tile, rows of 128 bytes,
 // 128-byte swizzle, 8-row groups 1024 bytes apart.
@@ -193,14 +233,42 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
   return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t sfa, uint32_t sfb, uint32_t acc) {
+// The same MMA executed by the whole (converged) warp, issued by one elected lane.
+__device__ __forceinline__ void tc_mma_el(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t sfa, uint32_t sfb, uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
       " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb));
+}
+__device__ __forceinline__ void tc_commit_el(uint64_t* b) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(b))
+      : "memory");
+}
+// Descriptor of one 512-byte scale atom: 32 rows of 16 bytes, no swizzle,
+// 8-row core matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+// Copy one scale atom into TMEM: row r of the atom (32 rows x 4 words) to lane
+// r of every lane quadrant, columns taddr .. taddr+3.  Executed by the whole
+// (converged) warp, issued by one elected lane.
+__device__ __forceinline__ void tc_cp_sf_el(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+      "l"(sdesc)
+      : "memory");
 }
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, float* v) {
   uint32_t r[16];
@@ -213,14 +281,6 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float* v) {
       : "r"(taddr));
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t* v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-      : "memory");
 }
 __device__ __forceinline__ void tc_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -285,9 +345,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES);
   uint64_t* full = bars;                 // [STAGES]
   uint64_t* empty = bars + STAGES;       // [STAGES]
-  uint64_t* sf_free = bars + 2 * STAGES; // [4]
-  uint64_t* sf_ready = sf_free + 4;      // [4]
-  uint64_t* acc_full = sf_ready + 4;     // [2]
+  uint64_t* sf_free = bars + 2 * STAGES; // [SF_BUFS]
+  uint64_t* sf_ready = sf_free + SF_BUFS; // [SF_BUFS]
+  uint64_t* acc_full = sf_ready + SF_BUFS; // [2]
   uint64_t* acc_empty = acc_full + 2;    // [2]
   uint32_t* tmem_holder = (uint32_t*)(acc_empty + 2);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
@@ -311,14 +371,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0 && p.row_off) meta.off[p.E] = p.row_off[p.E];
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
-    for (int i = 0; i < 4; ++i) { mbar_init(&sf_free[i], 1); mbar_init(&sf_ready[i], SF_THREADS); }
+    for (int i = 0; i < STAGES; ++i) { mbar_init(&full[i], COPIES); mbar_init(&empty[i], 1); }
+    for (int i = 0; i < SF_BUFS; ++i) { mbar_init(&sf_free[i], 1); mbar_init(&sf_ready[i], SF_WARPS); }
     for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], EPI_THREADS); }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (warp == 1) {
+  if (warp == MMA_WARP) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_holder)),
                  "r"(TMEM_COLS));
@@ -330,143 +390,147 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem = *tmem_holder;
 
   const int64_t ntiles = total_tiles(p, meta);
-  const int KT = (p.K + 255) / 256;
-  const int KTc = p.comp ? (p.kpad + 255) / 256 : 0;
+  const int KT = (p.K + KTILE - 1) / KTILE;
+  const int KTc = p.comp ? (p.kpad + KTILE - 1) / KTILE : 0;
   const int64_t a_sf_rb = (int64_t)(p.K / 64) * 512;    // bytes per 128-row block
   const int64_t r_sf_rb = (int64_t)(p.kpad / 64) * 512;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // The whole warp runs the loop (so addresses and coordinates stay
-    // warp-uniform); one elected lane issues the copies.
-    uint32_t it = 0;
-    bool ok = true;
+  if (warp < PRODUCERS) {
+    // ------------------------------------------------------------ producers
+    // Copy g = COPIES * it + b of ring iteration it goes to producer g % 3;
+    // each copy arrives once on full[s] (a code box with its bytes, or without
+    // any when the stage's K range ends before its sub-tile).  The whole warp runs the loop
+    // (so addresses and coordinates stay warp-uniform); one elected lane issues.
+    uint32_t it = 0, last = 0;
+    bool ok = true, any = false;
     for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       const Tile tl = decode_tile(p, meta, t);
       const int64_t brow = (int64_t)tl.e * p.N + tl.n0;
       for (int kt = 0; kt < KT + KTc && ok; ++kt, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
-        if (!warp_wait_bar(&empty[s], ph ^ 1, abort_flag, p.err)) { ok = false; break; }
         const bool corr = kt >= KT;
         const int kk = corr ? kt - KT : kt;
         const int klen = corr ? p.kpad : p.K;
-        const int nsteps = min(4, (klen - kk * 256) / 64);
+        const int ksteps = min(KSTEPS, (klen - kk * KTILE) / 64);
+        const int nsub = (ksteps + 3) >> 2;   // 128-byte sub-tiles holding real columns
         uint8_t* st = smem + s * STAGE_BYTES;
-        if (elect_one()) {
-        mbar_expect_tx(&full[s], A_TILE + B_TILE + 2 * nsteps * 512);
-        if (!corr) {
-          tma_load_2d(st, &tmA, kk * BK_BYTES, (int)tl.m0, &full[s]);
-          tma_load_2d(st + A_TILE, &tmB, kk * BK_BYTES, (int)brow, &full[s]);
-          bulk_load(st + A_TILE + B_TILE, p.a_sf + (tl.m0 / BM) * a_sf_rb + kk * SF_TILE,
-                    nsteps * 512, &full[s]);
-          bulk_load(st + A_TILE + B_TILE + SF_TILE, p.b_sf + (brow / BN) * a_sf_rb + kk * SF_TILE,
-                    nsteps * 512, &full[s]);
-        } else {
-          tma_load_2d(st, &tmR, kk * BK_BYTES, (int)tl.m0, &full[s]);
-          tma_load_2d(st + A_TILE, &tmW, kk * BK_BYTES, (int)brow, &full[s]);
-          bulk_load(st + A_TILE + B_TILE, p.r_sf + (tl.m0 / BM) * r_sf_rb + kk * SF_TILE,
-                    nsteps * 512, &full[s]);
-          bulk_load(st + A_TILE + B_TILE + SF_TILE, p.ws_sf + (brow / BN) * r_sf_rb + kk * SF_TILE,
-                    nsteps * 512, &full[s]);
+        const CUtensorMap* ma = corr ? &tmR : &tmA;
+        const CUtensorMap* mb = corr ? &tmW : &tmB;
+        const uint8_t* sfa = corr ? p.r_sf + (tl.m0 / BM) * r_sf_rb : p.a_sf + (tl.m0 / BM) * a_sf_rb;
+        const uint8_t* sfb = corr ? p.ws_sf + (brow / BN) * r_sf_rb : p.b_sf + (brow / BN) * a_sf_rb;
+        bool waited = false;
+        for (int b = 0; b < COPIES; ++b) {
+          if ((COPIES * it + b) % PRODUCERS != (uint32_t)warp) continue;
+          if (!waited) {
+            if (!warp_wait_bar(&empty[s], ph ^ 1, abort_flag, p.err)) { ok = false; break; }
+            waited = true;
+          }
+          const int u = b >> 1;
+          if (elect_one()) {
+            if (b >= BOXES) {
+              mbar_expect_tx(&full[s], ksteps * 512);
+              if (b == BOXES) bulk_load(st + A_TILE + B_TILE, sfa + kk * SF_TILE, ksteps * 512, &full[s]);
+              else bulk_load(st + A_TILE + B_TILE + SF_TILE, sfb + kk * SF_TILE, ksteps * 512, &full[s]);
+            } else if (u < nsub) {
+              mbar_expect_tx(&full[s], (b & 1) ? B_SUB : A_SUB);
+              const int x = kk * (KSUB * KSUBS) + u * KSUB;
+              if (b & 1) tma_load_2d(st + A_TILE + u * B_SUB, mb, x, (int)brow, &full[s]);
+              else tma_load_2d(st + u * A_SUB, ma, x, (int)tl.m0, &full[s]);
+            } else {
+              mbar_arrive(&full[s]);
+            }
+          }
+          __syncwarp();
+          last = it;
+          any = true;
         }
-        }
-        __syncwarp();
       }
     }
-    if (!ok && it > 0 && lane == 0) {
-      // let copies already issued land before the CTA can exit
-      const uint32_t last = it - 1;
+    if (!ok && any && lane == 0) {
+      // let copies this warp issued land before the CTA can exit
       wait_bar(&full[last % STAGES], (last / STAGES) & 1, abort_flag, p.err);
     }
-  } else if (warp == 1) {
+  } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs the loop so descriptors and TMEM addresses are
-    // warp-uniform values; one elected lane issues each tcgen05 instruction.
-    // (Issuing from a lone divergent lane with per-stage operands made every
-    // MMA issue ~2.5x slower.)
     constexpr uint32_t idesc = idesc_nvf4(BM, BN);
-    uint32_t it = 0;
+    uint32_t s = 0, sb = 0, sph = 0;
     uint32_t j = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++j) {
       const uint32_t b = j & 1;
-      if (!warp_wait_bar(&acc_empty[b], ((j >> 1) & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
+      if (!conv_wait_bar(&acc_empty[b], ((j >> 1) & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
       tc_fence_after();
-      for (int kt = 0; kt < KT + KTc && ok; ++kt, ++it) {
+      for (int kt = 0; kt < KT + KTc; ++kt) {
         const bool corr = kt >= KT;
         const int kk = corr ? kt - KT : kt;
         if (corr && kk == 0 && j > 0) {
           // acc2 is free once the previous tile's epilogue is done
-          if (!warp_wait_bar(&acc_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.err)) {
+          if (!conv_wait_bar(&acc_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
         }
-        const int s = it % STAGES;
-        const uint32_t sb = it & 3;
-        // the staging warps waited for this stage's TMA data (full[s]) and have
+        // the staging warps saw this stage's TMA data land (full[s]) and have
         // written its scales into TMEM buffer sb: one barrier covers both
-        if (!warp_wait_bar(&sf_ready[sb], (it >> 2) & 1, abort_flag, p.err)) { ok = false; break; }
+        if (!conv_wait_bar(&sf_ready[sb], sph, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
         const int klen = corr ? p.kpad : p.K;
-        const int nsteps = min(4, (klen - kk * 256) / 64);
-        uint8_t* st = smem + s * STAGE_BYTES;
-        const uint32_t sa = smem_u32(st), sbb = smem_u32(st + A_TILE);
-        const uint32_t tsf = tmem + SF_COL + sb * 32;
+        const int ksteps = min(KSTEPS, (klen - kk * KTILE) / 64);
+        const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
+        const uint32_t sbb = sa + A_TILE;
+        const uint32_t tsf = tmem + SF_COL + sb * SF_BUF_COLS;
         const uint32_t dcol = corr ? (tmem + ACC2_COL) : (tmem + b * BN);
-        if (elect_one()) {
-          for (int q = 0; q < nsteps; ++q) {
-            tc_mma(dcol, desc_sw128(sa + q * 32), desc_sw128(sbb + q * 32), idesc, tsf + q * 4,
-                   tsf + 16 + q * 4, (kk > 0 || q > 0) ? 1u : 0u);
-          }
-          tc_commit(&empty[s]);
-          tc_commit(&sf_free[sb]);
+        for (int q = 0; q < ksteps; ++q) {
+          const uint32_t off = (q >> 2) * A_SUB + (q & 3) * 32;
+          tc_mma_el(dcol, desc_sw128(sa + off), desc_sw128(sbb + off), idesc, tsf + q * 4,
+                    tsf + 4 * KSTEPS + q * 4, (kk > 0 || q > 0) ? 1u : 0u);
         }
-        __syncwarp();
+        tc_commit_el(&empty[s]);
+        tc_commit_el(&sf_free[sb]);
+        if (++s == STAGES) s = 0;
+        if (++sb == SF_BUFS) { sb = 0; sph ^= 1; }
       }
       if (!ok) break;
-      if (elect_one()) tc_commit(&acc_full[b]);
-      __syncwarp();
+      tc_commit_el(&acc_full[b]);
     }
   } else if (warp >= SF_WARP0 && warp < EPI_WARP0) {
     // ------------------------------------------------------------ scale staging
-    // Lane l of every quadrant gets, at column SF_COL + 32*sb + 4*q + j (A) and
-    // +16 (B), the scale word of row l + 32*j for K step q -- row l of the
-    // stage's scale atom q -- the layout the block-scaled MMA reads (row r's
-    // four scales at lane r % 32, column r / 32).
-    const int quad = warp & 3;
-    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    uint32_t it = 0;
+    // TMEM buffer sb holds, at column SF_COL + 64*sb + 4*q + j (A) and +32 (B),
+    // lane l of every quadrant, the scale word of row l + 32*j for K step q --
+    // row l of scale atom q -- the layout the block-scaled MMA reads (row r's
+    // four scales at lane r % 32, column r / 32).  Warp w copies the atoms of
+    // K steps 2w and 2w+1.  The warps wait for the stage's TMA data, so
+    // sf_ready alone tells the MMA warp that the stage is complete.
+    const int w = warp - SF_WARP0;
+    uint32_t s = 0, ph = 0, sb = 0, sph = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-      for (int kt = 0; kt < KT + KTc; ++kt, ++it) {
-        const int s = it % STAGES;
-        const uint32_t sb = it & 3;
-        int okw = 1;
-        if (lane == 0) {
-          okw = wait_bar(&full[s], (it / STAGES) & 1, abort_flag, p.err) ? 1 : 0;
-          if (okw) okw = wait_bar(&sf_free[sb], ((it >> 2) & 1) ^ 1, abort_flag, p.err) ? 1 : 0;
+      for (int kt = 0; kt < KT + KTc; ++kt) {
+        if (!conv_wait_bar(&full[s], ph, abort_flag, p.err) ||
+            !conv_wait_bar(&sf_free[sb], sph ^ 1, abort_flag, p.err)) {
+          ok = false;
+          break;
         }
-        okw = __shfl_sync(0xffffffffu, okw, 0);
-        if (!okw) { ok = false; break; }
         tc_fence_after();
-        const uint8_t* sfa = smem + s * STAGE_BYTES + A_TILE + B_TILE;
-        uint32_t va[16], vb[16];
+        const bool corr = kt >= KT;
+        const int kk = corr ? kt - KT : kt;
+        const int klen = corr ? p.kpad : p.K;
+        const int ksteps = min(KSTEPS, (klen - kk * KTILE) / 64);
+        const uint32_t ssf = smem_u32(smem + s * STAGE_BYTES + A_TILE + B_TILE);
+        const uint32_t tsf = tmem + SF_COL + sb * SF_BUF_COLS;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 a = *reinterpret_cast<const uint4*>(sfa + q * 512 + lane * 16);
-          const uint4 bq = *reinterpret_cast<const uint4*>(sfa + SF_TILE + q * 512 + lane * 16);
-          va[4 * q] = a.x; va[4 * q + 1] = a.y; va[4 * q + 2] = a.z; va[4 * q + 3] = a.w;
-          vb[4 * q] = bq.x; vb[4 * q + 1] = bq.y; vb[4 * q + 2] = bq.z; vb[4 * q + 3] = bq.w;
+        for (int i = 0; i < KSTEPS / SF_WARPS; ++i) {
+          const int q = w * (KSTEPS / SF_WARPS) + i;
+          if (q < ksteps) {
+            tc_cp_sf_el(tsf + q * 4, desc_sf(ssf + q * 512));
+            tc_cp_sf_el(tsf + 4 * KSTEPS + q * 4, desc_sf(ssf + SF_TILE + q * 512));
+          }
         }
-        const uint32_t taddr = tmem + lane_base + SF_COL + sb * 32;
-        tc_st16(taddr, va);
-        tc_st16(taddr + 16, vb);
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        tc_fence_before();
-        mbar_arrive(&sf_ready[sb]);
+        tc_commit_el(&sf_ready[sb]);
+        if (++s == STAGES) { s = 0; ph ^= 1; }
+        if (++sb == SF_BUFS) { sb = 0; sph ^= 1; }
       }
     }
   } else if (warp >= EPI_WARP0) {
@@ -572,7 +636,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
   __syncthreads();
-  if (warp == 1) {
+  if (warp == MMA_WARP) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(TMEM_COLS));
@@ -682,7 +746,7 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t wid
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)width_bytes, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)ld_bytes};
-  cuuint32_t box[2] = {BK_BYTES, BM};
+  cuuint32_t box[2] = {KSUB, BM};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
