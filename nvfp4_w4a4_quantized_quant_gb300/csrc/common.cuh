@@ -7,6 +7,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -41,11 +42,14 @@ __host__ __device__ __forceinline__ int64_t sf_tc_bytes(int64_t rows, int64_t co
 }
 
 // ------------------------------------------------------------ conversions
-// E4M3 byte -> float, from the format: bias 7, 3 mantissa bits, subnormals.
+// E4M3 byte -> float through the hardware E4M3 -> f16 converter (every E4M3
+// value, subnormals included, is exact in f16, and f16 -> f32 is exact).
 __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
-  uint32_t e = (b >> 3) & 15u, m = b & 7u;
-  if (e == 0) return (float)m * 0.001953125f;  // m * 2^-9, exact
-  return __uint_as_float(((e + 120u) << 23) | (m << 20));
+  uint32_t h;
+  asm("{\n\t.reg .b16 lo;\n\tcvt.u16.u32 lo, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+      : "=r"(h)
+      : "r"(b & 0xFFu));
+  return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
 }
 
 // Non-negative float -> E4M3 byte, nearest/even, saturating at 448.

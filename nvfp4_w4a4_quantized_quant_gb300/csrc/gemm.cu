@@ -677,26 +677,29 @@ __global__ void __launch_bounds__(256) wtrans_kernel(const uint8_t* __restrict__
 // For every weight row r (of every expert) and every 16-block of the selected
 // channels: gather the selected columns of DQ(Q(W)) in units of s_w
 // (level * E4M3 scale, exact), requantize with tensor scale 1 (s_w kept).
-// A warp owns 32 consecutive rows (lane = row) of one expert and reads the
-// column-major copy, so every gather of a selected column is one coalesced
-// 16-byte (codes) + 32-byte (scales) access.  Output codes [E*N, kpad/2] and
-// TCGEN05 scales over kpad columns.
+// A warp owns one 16-column block of 32 consecutive rows (lane = row) of one
+// expert and reads the column-major copy, so every gather of a selected
+// column is one coalesced 16-byte (codes) + 32-byte (scales) access; one warp
+// per block keeps all of a row group's gathers in flight at once.  Output
+// codes [E*N, kpad/2] and TCGEN05 scales over kpad columns.
 __global__ void __launch_bounds__(256) wsel_kernel(
     const uint8_t* __restrict__ ct, const uint8_t* __restrict__ st, int64_t rows /*E*N*/, int N,
     int K, const int32_t* __restrict__ sel, int sel_pe, int k, int kpad,
     uint8_t* __restrict__ oc, uint8_t* __restrict__ osf) {
   const int lane = threadIdx.x & 31;
   const int nb = kpad >> 4;
-  const int64_t nwarps = rows >> 5;
-  for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < nwarps;
-       w += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+  const int64_t nitems = (rows >> 5) * nb;
+  for (int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < nitems;
+       item += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+    const int64_t w = item / nb;
+    const int blk = (int)(item % nb);
     const int64_t r = w * 32 + lane;
     const int64_t e = r / N, n = r % N;
     const int32_t* s = sel + (sel_pe ? e * k : 0);
     const uint8_t* cte = ct + e * (int64_t)K * (N / 2) + n / 2;
     const uint8_t* ste = st + e * (int64_t)(K / 16) * N + n;
     const uint32_t sh = (n & 1) * 4;
-    for (int blk = 0; blk < nb; ++blk) {
+    {
       uint32_t lo = 0, hi = 0, sbyte = 0;
       if (blk * 16 < k) {
         float w16[16];
@@ -787,8 +790,8 @@ static quads_status_t launch(const Launch& L) {
       return fail(QUADS_ERR_WORKSPACE, "gemm: workspace needs %zu bytes", need);
     ws_codes = (uint8_t*)L.ws;
     ws_sf = ws_codes + (((size_t)brows * (L.kpad / 2) + 1023) & ~(size_t)1023);
-    const int64_t total = brows;  // one thread per weight row (N % 128 == 0)
-    int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)num_sms() * 16);
+    const int64_t items = (brows / 32) * (L.kpad / 16);  // one warp per 32 rows x 16 columns
+    int blocks = (int)std::min<int64_t>((items * 32 + 255) / 256, (int64_t)num_sms() * 32);
     wsel_kernel<<<blocks, 256, 0, L.stream>>>(L.b_t, L.b_sf_t, brows, L.N, L.K, L.sel, L.sel_pe,
                                                L.k, L.kpad, ws_codes, ws_sf);
   }

@@ -19,12 +19,14 @@ constexpr int kMaxTopk = 16;
 // One warp per token.  Lane l holds logits l, l+32, ...; round r takes the
 // warp arg-max (ties -> lower expert id), removes it, and lane r keeps it.
 // The chosen experts are then ranked by id (ascending slot order), gates are
-// exp(l - lmax) / sum over the chosen, and the token's expert set is written as
-// a bit mask (the plan kernel counts from the masks).
+// exp(l - lmax) / sum over the chosen, the token's expert set is written as a
+// bit mask (for the row assignment), and each chosen expert's count is bumped
+// (integer atomics: the totals do not depend on their order).
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T,
                                                     int E, int topk, int32_t* __restrict__ idx,
                                                     float* __restrict__ gates,
-                                                    uint32_t* __restrict__ emask) {
+                                                    uint32_t* __restrict__ emask,
+                                                    int32_t* __restrict__ counts) {
   const int lane = threadIdx.x & 31;
   const int words = (E + 31) >> 5;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T;
@@ -73,6 +75,7 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
     if (mine) {
       idx[(int64_t)t * topk + rank] = my_e;
       gates[(int64_t)t * topk + rank] = p / s;
+      atomicAdd(&counts[my_e], 1);
     }
     for (int w = 0; w < words; ++w) {
       const uint32_t bit = (mine && (my_e >> 5) == w) ? (1u << (my_e & 31)) : 0u;
@@ -82,33 +85,14 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
   }
 }
 
-// Expert counts from the token masks (shared-memory histogram, order-free
-// integer adds), then padded offsets off[e+1] = off[e] + roundup(count[e], 128).
-// One block of 1024 threads.
-__global__ void __launch_bounds__(1024) plan_kernel(const uint32_t* __restrict__ emask, int T,
-                                                    int E, int32_t* __restrict__ counts,
-                                                    int32_t* __restrict__ off) {
-  __shared__ int hist[kMaxExperts];
-  __shared__ int warp_sums[32];
-  const int words = (E + 31) >> 5;
-  for (int e = threadIdx.x; e < kMaxExperts; e += blockDim.x) hist[e] = 0;
-  __syncthreads();
-  const int64_t nw = (int64_t)T * words;
-  for (int64_t i = threadIdx.x; i < nw; i += blockDim.x) {
-    uint32_t m = emask[i];
-    const int base = (int)(i % words) * 32;
-    while (m) {
-      const int b = __ffs(m) - 1;
-      m &= m - 1;
-      atomicAdd(&hist[base + b], 1);
-    }
-  }
-  __syncthreads();
+// Padded offsets off[e+1] = off[e] + roundup(count[e], 128): one block of
+// kMaxExperts threads scans the expert counts.
+__global__ void __launch_bounds__(kMaxExperts) plan_kernel(const int32_t* __restrict__ counts,
+                                                           int E, int32_t* __restrict__ off) {
+  __shared__ int warp_sums[kMaxExperts / 32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  int cnt = threadIdx.x < E ? hist[threadIdx.x] : 0;
-  if (threadIdx.x < E) counts[threadIdx.x] = cnt;
+  const int cnt = threadIdx.x < E ? counts[threadIdx.x] : 0;
   int v = (cnt + QUADS_MOE_ROW_ALIGN - 1) / QUADS_MOE_ROW_ALIGN * QUADS_MOE_ROW_ALIGN;
-  const int padded = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int u = __shfl_up_sync(0xffffffffu, v, o);
@@ -116,20 +100,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(const uint32_t* __restrict__
   }
   if (lane == 31) warp_sums[w] = v;
   __syncthreads();
-  if (w == 0) {
-    int x = warp_sums[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += u;
-    }
-    warp_sums[lane] = x;
-  }
-  __syncthreads();
-  const int incl = v + (w > 0 ? warp_sums[w - 1] : 0);
-  if (threadIdx.x < E) off[threadIdx.x + 1] = incl;
+  int before = 0;
+  for (int i = 0; i < w; ++i) before += warp_sums[i];
+  if (threadIdx.x < E) off[threadIdx.x + 1] = v + before;
   if (threadIdx.x == 0) off[0] = 0;
-  (void)padded;
 }
 
 // One block per expert: thread i covers a contiguous run of tokens, counts the
@@ -185,9 +159,11 @@ __global__ void __launch_bounds__(1024) assign_kernel(const uint32_t* __restrict
   for (int r = off[e] + counts[e] + threadIdx.x; r < off[e + 1]; r += blockDim.x) row_token[r] = -1;
 }
 
-// One warp per 8 consecutive output rows: the 8 source-row indices are loaded
-// at once, then every lane issues all its 16-byte code loads (and 4-byte scale
-// loads) for the 8 rows before storing them; scale bytes go to the TCGEN05 atoms.
+// The output is walked as a flat array of 16-byte code vectors (row-major, so
+// consecutive threads copy consecutive vectors whatever the row width), four
+// per thread per pass with all loads issued before the stores; then the
+// 4-byte scale groups, written to their TCGEN05 atom positions.  Padding rows
+// (row_token -1) get zero codes and scales.
 __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__ row_token,
                                                      const int32_t* __restrict__ off, int E,
                                                      int64_t cap, int cols,
@@ -195,48 +171,48 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
                                                      const uint8_t* __restrict__ isf,
                                                      uint8_t* __restrict__ oc,
                                                      uint8_t* __restrict__ osf) {
-  const int lane = threadIdx.x & 31;
   const int64_t nrows = off[E];
   const int cbytes = cols >> 1;
   const int ncols16 = cols >> 4;
   const int nvec = cbytes >> 4;           // 16-byte vectors per row
   const int natom = ncols16 >> 2;         // 4-byte scale groups per row
-  for (int64_t r0 = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 8; r0 < nrows;
-       r0 += (((int64_t)gridDim.x * blockDim.x) >> 5) * 8) {
-    const int tl = (lane < 8 && r0 + lane < nrows) ? row_token[r0 + lane] : -1;
-    for (int v0 = 0; v0 < nvec; v0 += 64) {  // up to 64 vectors (1 KB) of every row per pass
-      uint4 buf[8][2];
+  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t ncode = nrows * nvec;
+  for (int64_t i0 = tid; i0 < ncode; i0 += 4 * nthreads) {
+    uint4 v[4];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int t = __shfl_sync(0xffffffffu, tl, q);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int v = v0 + lane + 32 * h;
-          buf[q][h] = make_uint4(0, 0, 0, 0);
-          if (t >= 0 && v < nvec) buf[q][h] = *reinterpret_cast<const uint4*>(ic + (int64_t)t * cbytes + 16 * v);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int64_t r = r0 + q;
-        if (r >= nrows) break;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int v = v0 + lane + 32 * h;
-          if (v < nvec) *reinterpret_cast<uint4*>(oc + r * cbytes + 16 * v) = buf[q][h];
-        }
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * nthreads;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (i < ncode) {
+        const int t = __ldg(row_token + i / nvec);
+        if (t >= 0) v[u] = __ldg(reinterpret_cast<const uint4*>(ic + (int64_t)t * cbytes) + i % nvec);
       }
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int t = __shfl_sync(0xffffffffu, tl, q);
-      const int64_t r = r0 + q;
-      if (r >= nrows) break;
-      for (int a = lane; a < natom; a += 32) {
-        uint32_t v = 0;
-        if (t >= 0) v = *reinterpret_cast<const uint32_t*>(isf + (int64_t)t * ncols16 + 4 * a);
-        *reinterpret_cast<uint32_t*>(osf + sf_tc_offset(r, 4 * a, ncols16)) = v;
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * nthreads;
+      if (i < ncode) reinterpret_cast<uint4*>(oc)[i] = v[u];
+    }
+  }
+  const int64_t nsc = nrows * natom;
+  for (int64_t i0 = tid; i0 < nsc; i0 += 4 * nthreads) {
+    uint32_t v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * nthreads;
+      v[u] = 0;
+      if (i < nsc) {
+        const int t = __ldg(row_token + i / natom);
+        if (t >= 0) v[u] = __ldg(reinterpret_cast<const uint32_t*>(isf + (int64_t)t * ncols16) + i % natom);
       }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * nthreads;
+      if (i < nsc)
+        *reinterpret_cast<uint32_t*>(osf + sf_tc_offset(i / natom, 4 * (int)(i % natom), ncols16)) = v[u];
     }
   }
 }
@@ -295,10 +271,11 @@ extern "C" quads_status_t quads_moe_route(const float* logits, int32_t tokens, i
     return fail(QUADS_ERR_WORKSPACE, "moe_route: workspace needs %zu bytes", need);
   uint32_t* emask = (uint32_t*)workspace;
   cudaStream_t st = (cudaStream_t)stream;
+  cudaMemsetAsync(expert_counts, 0, (size_t)num_experts * sizeof(int32_t), st);
   if (tokens > 0)
     route_kernel<<<(tokens * 32 + 255) / 256, 256, 0, st>>>(logits, tokens, num_experts, topk,
-                                                             topk_idx, gates, emask);
-  plan_kernel<<<1, 1024, 0, st>>>(emask, tokens, num_experts, expert_counts, expert_offsets);
+                                                             topk_idx, gates, emask, expert_counts);
+  plan_kernel<<<1, kMaxExperts, 0, st>>>(expert_counts, num_experts, expert_offsets);
   assign_kernel<<<num_experts, 1024, 0, st>>>(emask, tokens, num_experts, topk, expert_offsets,
                                               expert_counts, row_token, token_row);
   return check_launch("moe_route", tokens > 0 ? 3 : 2);
@@ -316,7 +293,8 @@ extern "C" quads_status_t quads_moe_gather(const int32_t* row_token, const int32
   if (((uintptr_t)in_codes | (uintptr_t)out_codes) & 15u || ((uintptr_t)in_scales | (uintptr_t)out_scales) & 3u)
     return fail(QUADS_ERR_MISALIGNED, "moe_gather: alignment");
   cudaStream_t st = (cudaStream_t)stream;
-  const int blocks = (int)std::min<int64_t>((rows_capacity / 8 * 32 + 255) / 256, (int64_t)num_sms() * 16);
+  const int64_t vecs = rows_capacity * (cols / 32);   // 16-byte code vectors
+  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((vecs / 4 + 255) / 256, (int64_t)num_sms() * 8));
   gather_kernel<<<blocks, 256, 0, st>>>(row_token, expert_offsets, num_experts, rows_capacity,
                                         (int)cols, in_codes, in_scales, out_codes, out_scales);
   return check_launch("moe_gather", 1);

@@ -77,37 +77,22 @@ __global__ void tensor_scale_kernel(const uint32_t* __restrict__ amax_bits, int 
 }
 
 // ---------------------------------------------------------------- quantize
-// A warp owns one (32-row chunk, 256-column slab) task: lane l holds columns
-// slab*256 + 8l .. +7 and walks the chunk's rows in order, so the residual
-// energy of its 8 columns is summed row by row in float32 (the fixed order the
-// score definition uses).  Lanes 2i and 2i+1 form one 16-element block.  Loads
-// of the next 4 rows are issued before the current 4 are processed.
-template <bool kScores>
-__device__ __forceinline__ void quantize_row(const uint4& raw, float s_t, int lane, bool active,
-                                             int64_t row, int col, int ncols16, uint8_t* codes,
-                                             int64_t ldc, uint8_t* scales, int layout,
-                                             float* acc) {
-  float f[8];
-  bf16x8_to_f32(raw, f);
+// A block owns one (32-row chunk, 256-column slab) task.  Warp w quantizes
+// rows 4w .. 4w+3 of the chunk, two rows at a time: lane l takes the 16-element
+// block (l & 15) of row (l >> 4), so each block scale is computed once.  In
+// score mode every residual square R^2 is parked in shared memory and, after a
+// barrier, thread c adds column c's 32 squares in row order starting from 0 --
+// the fixed float32 order the score definition uses.
+__device__ __forceinline__ void quantize_block16(const uint4& lo, const uint4& hi, float s_t,
+                                                 float* f, BlockScale& bs, uint2& c) {
+  bf16x8_to_f32(lo, f);
+  bf16x8_to_f32(hi, f + 8);
   float m = 0.0f;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
-  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-  const BlockScale bs = block_scale(m, s_t);
-  const uint32_t c = quantize8(f, bs);
-  if (active) {
-    *reinterpret_cast<uint32_t*>(codes + row * ldc + (col >> 1)) = c;
-    if ((lane & 1) == 0) scales[sf_offset(layout, row, col >> 4, ncols16)] = (uint8_t)bs.byte;
-  }
-  if (kScores) {
-    float lv[8];
-    e2m1x8_to_f32(c, lv);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float R = __fsub_rn(f[j], __fmul_rn(lv[j], bs.d));
-      acc[j] = __fadd_rn(acc[j], __fmul_rn(R, R));
-    }
-  }
+  for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(f[j]));
+  bs = block_scale(m, s_t);
+  c.x = quantize8(f, bs);
+  c.y = quantize8(f + 8, bs);
 }
 
 template <bool kScores>
@@ -116,60 +101,90 @@ __global__ void __launch_bounds__(256) quantize_kernel(
     const int32_t* __restrict__ row_index, const int32_t* __restrict__ goff, int G,
     const float* __restrict__ st, uint8_t* __restrict__ codes, int64_t ldc,
     uint8_t* __restrict__ scales, int layout, float* __restrict__ partials) {
-  const int lane = threadIdx.x & 31;
+  __shared__ __align__(16) float sq[kScores ? kScoreChunk * 256 : 4];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t end = goff ? (int64_t)goff[G] : rows;
   const int nslab = (cols + 255) >> 8;
   const int64_t nchunks = (end + kScoreChunk - 1) / kScoreChunk;
   const int64_t ntasks = nchunks * nslab;
   const int ncols16 = cols >> 4;
-  const int64_t warp_global = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t task = warp_global; task < ntasks; task += nwarps) {
+  const int blk = lane & 15;
+  // this thread's two rows of a task, loaded one task ahead
+  auto load_task = [&](int64_t task, uint4 (&raw)[2][2]) {
+    const int64_t chunk = task / nslab;
+    const int col = (int)(task % nslab) * 256 + blk * 16;
+    const int64_t r0 = chunk * kScoreChunk;
+    const int64_t r1 = min(r0 + kScoreChunk, end);
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const int64_t row = r0 + 4 * warp + 2 * it + (lane >> 4);
+      raw[it][0] = raw[it][1] = make_uint4(0, 0, 0, 0);
+      if (task < ntasks && col < cols && row < r1) {
+        const int64_t src = row_index ? (int64_t)row_index[row] : row;
+        const uint4* px = reinterpret_cast<const uint4*>(x + src * ldx + col);
+        raw[it][0] = __ldg(px);
+        raw[it][1] = __ldg(px + 1);
+      }
+    }
+  };
+  uint4 nxt[2][2];
+  load_task(blockIdx.x, nxt);
+  for (int64_t task = blockIdx.x; task < ntasks; task += gridDim.x) {
+    uint4 raw[2][2];
+#pragma unroll
+    for (int it = 0; it < 2; ++it) { raw[it][0] = nxt[it][0]; raw[it][1] = nxt[it][1]; }
+    load_task(task + gridDim.x, nxt);
     const int64_t chunk = task / nslab;
     const int slab = (int)(task % nslab);
-    const int col = slab * 256 + lane * 8;
+    const int col = slab * 256 + blk * 16;
     const bool active = col < cols;
     const int64_t r0 = chunk * kScoreChunk;
     const int64_t r1 = min(r0 + kScoreChunk, end);
-    int g = goff ? group_of(goff, G, r0) : 0;
-    int64_t gend = goff ? (int64_t)goff[g + 1] : end;
-    float s_t = st[g];
-    float acc[8];
+    const int g0 = goff ? group_of(goff, G, r0) : 0;   // same for the whole block
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-    auto load4 = [&](int64_t r, uint4* u) {
+    for (int it = 0; it < 2; ++it) {
+      const int64_t row = r0 + 4 * warp + 2 * it + (lane >> 4);
+      const bool valid = active && row < r1;
+      int g = g0;
+      if (goff && valid)
+        while (g + 1 < G && row >= goff[g + 1]) ++g;
+      float f[16];
+      BlockScale bs;
+      uint2 c;
+      quantize_block16(raw[it][0], raw[it][1], valid ? st[g] : 1.0f, f, bs, c);
+      if (valid) {
+        uint32_t* pc = reinterpret_cast<uint32_t*>(codes + row * ldc + (col >> 1));
+        pc[0] = c.x;
+        pc[1] = c.y;
+        scales[sf_offset(layout, row, col >> 4, ncols16)] = (uint8_t)bs.byte;
+      }
+      if (kScores) {
+        float lv[16];
+        e2m1x8_to_f32(c.x, lv);
+        e2m1x8_to_f32(c.y, lv + 8);
+        float4* ps = reinterpret_cast<float4*>(sq + (row - r0) * 256 + blk * 16);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        u[q] = make_uint4(0, 0, 0, 0);
-        if (active && r + q < r1) {
-          const int64_t src = row_index ? (int64_t)row_index[r + q] : r + q;
-          u[q] = __ldg(reinterpret_cast<const uint4*>(x + src * ldx + col));
+        for (int q = 0; q < 4; ++q) {
+          float v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float R = __fsub_rn(f[4 * q + j], __fmul_rn(lv[4 * q + j], bs.d));
+            v[j] = valid ? __fmul_rn(R, R) : 0.0f;
+          }
+          ps[q] = make_float4(v[0], v[1], v[2], v[3]);
         }
       }
-    };
-    uint4 cur[4], nxt[4];
-    load4(r0, cur);
-    for (int64_t r = r0; r < r1; r += 4) {
-      if (r + 4 < r1) load4(r + 4, nxt);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int64_t row = r + q;
-        if (row >= r1) break;
-        while (row >= gend) {  // (score mode: never; chunks do not straddle groups)
-          ++g;
-          gend = goff[g + 1];
-          s_t = st[g];
-        }
-        quantize_row<kScores>(cur[q], s_t, lane, active, row, col, ncols16, codes, ldc, scales,
-                              layout, acc);
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
     }
-    if (kScores && active) {
-      float4* p = reinterpret_cast<float4*>(partials + chunk * cols + col);
-      p[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      p[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if (kScores) {
+      __syncthreads();
+      const int c = slab * 256 + (int)threadIdx.x;
+      if (c < cols) {
+        float acc = 0.0f;
+        const int nr = (int)(r1 - r0);
+        for (int r = 0; r < nr; ++r) acc = __fadd_rn(acc, sq[r * 256 + threadIdx.x]);
+        partials[chunk * cols + c] = acc;
+      }
+      __syncthreads();
     }
   }
 }
@@ -594,8 +609,8 @@ extern "C" quads_status_t quads_quantize_nvfp4(
     const int64_t start = (rows / 128) * (ncols16 / 4) * 512;
     cudaMemsetAsync(scales + start, 0, (size_t)(sf_tc_bytes(rows, cols) - start), st);
   }
-  const int64_t ntasks = ((rows + 31) / 32) * ((cols + 255) / 256);
-  const int blocks = grid_for(ntasks, 8, 8);
+  const int64_t ntasks = ((rows + 31) / 32) * ((cols + 255) / 256);  // one block per task
+  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(ntasks, (int64_t)num_sms() * 16));
   if (score_partials)
     quantize_kernel<true><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)x, rows, (int)cols, ldx,
                                                   row_index, group_offsets, G, stp, codes,
