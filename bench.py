@@ -51,6 +51,12 @@ def gemm1_bytes(w=WORKLOAD) -> float:
             + E * 2 * F * kp * 0.5625 + rows * F * 2)
 
 
+# DRAM traffic (read + write) of one GEMM1 launch at this workload, from the
+# ncu capture summarised in profiles/gemm1_moe_swiglu_8192tok_ncu.md; reset to
+# None whenever gemm_kernel changes until a new capture is taken.
+GEMM1_TRAFFIC_BYTES = 320.342272e6 + 89.932032e6
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -317,7 +323,7 @@ def run_gpu(args):
             "peak": pk["hbm"],
             "unit": "GB/s",
             "frac": round(g1_bytes / (g1_ms * 1e-3) / 1e9 / pk["hbm"], 4),
-            "traffic": None,
+            "traffic": GEMM1_TRAFFIC_BYTES,
             "ms": round(g1_ms, 4),
             "tflops": round(2.0 * T * WORKLOAD["topk"] * 2 * WORKLOAD["ffn"] * (H + WORKLOAD["k1"]) / (g1_ms * 1e-3) / 1e12, 1),
             "algorithmic_bytes": int(g1_bytes),
