@@ -688,42 +688,40 @@ __global__ void __launch_bounds__(256) wsel_kernel(
     uint8_t* __restrict__ oc, uint8_t* __restrict__ osf) {
   const int lane = threadIdx.x & 31;
   const int nb = kpad >> 4;
-  const int64_t nitems = (rows >> 5) * nb;
-  for (int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < nitems;
-       item += ((int64_t)gridDim.x * blockDim.x) >> 5) {
-    const int64_t w = item / nb;
-    const int blk = (int)(item % nb);
-    const int64_t r = w * 32 + lane;
-    const int64_t e = r / N, n = r % N;
-    const int32_t* s = sel + (sel_pe ? e * k : 0);
-    const uint8_t* cte = ct + e * (int64_t)K * (N / 2) + n / 2;
-    const uint8_t* ste = st + e * (int64_t)(K / 16) * N + n;
-    const uint32_t sh = (n & 1) * 4;
-    {
-      uint32_t lo = 0, hi = 0, sbyte = 0;
-      if (blk * 16 < k) {
-        float w16[16];
-        float m = 0.0f;
-        uint32_t codes[16], sbytes[16];
+  const uint32_t nitems = (uint32_t)(rows >> 5) * (uint32_t)nb;   // < 2^31 (host check)
+  for (uint32_t item = (uint32_t)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+       item < nitems; item += (uint32_t)(((int64_t)gridDim.x * blockDim.x) >> 5)) {
+    const uint32_t w = item / (uint32_t)nb;
+    const int blk = (int)(item - w * (uint32_t)nb);
+    const uint32_t r = w * 32 + lane;
+    const uint32_t e = r / (uint32_t)N, n = r - e * (uint32_t)N;
+    uint32_t lo = 0, hi = 0, sbyte = 0;
+    if (blk * 16 < k) {
+      const int32_t* s = sel + (sel_pe ? (int64_t)e * k : 0) + blk * 16;
+      const uint8_t* cte = ct + (int64_t)e * K * (N / 2) + n / 2;
+      const uint8_t* ste = st + (int64_t)e * (K / 16) * N + n;
+      const uint32_t sh = (n & 1) * 4;
+      uint32_t codes[16], sbytes[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int c = __ldg(s + blk * 16 + j);
-          codes[j] = cte[(int64_t)c * (N / 2)];
-          sbytes[j] = ste[(int64_t)(c >> 4) * N];
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          w16[j] = __fmul_rn(e2m1_to_f32((codes[j] >> sh) & 15u), e4m3_to_f32(sbytes[j]));
-          m = fmaxf(m, fabsf(w16[j]));
-        }
-        const BlockScale bs = block_scale(m, 1.0f);
-        lo = quantize8(w16, bs);
-        hi = quantize8(w16 + 8, bs);
-        sbyte = bs.byte;
+      for (int j = 0; j < 16; ++j) {
+        const int c = __ldg(s + j);   // k % 16 == 0: a started block is full
+        codes[j] = __ldg(cte + (int64_t)c * (N / 2));
+        sbytes[j] = __ldg(ste + (int64_t)(c >> 4) * N);
       }
-      *reinterpret_cast<uint2*>(oc + r * (kpad >> 1) + blk * 8) = make_uint2(lo, hi);
-      osf[sf_tc_offset(r, blk, nb)] = (uint8_t)sbyte;
+      float w16[16];
+      float m = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        w16[j] = __fmul_rn(e2m1_to_f32((codes[j] >> sh) & 15u), e4m3_to_f32(sbytes[j]));
+        m = fmaxf(m, fabsf(w16[j]));
+      }
+      const BlockScale bs = block_scale(m, 1.0f);
+      lo = quantize8(w16, bs);
+      hi = quantize8(w16 + 8, bs);
+      sbyte = bs.byte;
     }
+    *reinterpret_cast<uint2*>(oc + (int64_t)r * (kpad >> 1) + blk * 8) = make_uint2(lo, hi);
+    osf[sf_tc_offset(r, blk, nb)] = (uint8_t)sbyte;
   }
 }
 
@@ -791,6 +789,8 @@ static quads_status_t launch(const Launch& L) {
     ws_codes = (uint8_t*)L.ws;
     ws_sf = ws_codes + (((size_t)brows * (L.kpad / 2) + 1023) & ~(size_t)1023);
     const int64_t items = (brows / 32) * (L.kpad / 16);  // one warp per 32 rows x 16 columns
+    if (items >= ((int64_t)1 << 31) || brows >= ((int64_t)1 << 31))
+      return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "gemm: W_sel extraction needs E*N*kpad/512 < 2^31");
     int blocks = (int)std::min<int64_t>((items * 32 + 255) / 256, (int64_t)num_sms() * 32);
     wsel_kernel<<<blocks, 256, 0, L.stream>>>(L.b_t, L.b_sf_t, brows, L.N, L.K, L.sel, L.sel_pe,
                                                L.k, L.kpad, ws_codes, ws_sf);

@@ -159,11 +159,11 @@ __global__ void __launch_bounds__(1024) assign_kernel(const uint32_t* __restrict
   for (int r = off[e] + counts[e] + threadIdx.x; r < off[e + 1]; r += blockDim.x) row_token[r] = -1;
 }
 
-// The output is walked as a flat array of 16-byte code vectors (row-major, so
-// consecutive threads copy consecutive vectors whatever the row width), four
-// per thread per pass with all loads issued before the stores; then the
-// 4-byte scale groups, written to their TCGEN05 atom positions.  Padding rows
-// (row_token -1) get zero codes and scales.
+// Wide rows (>= 32 code vectors of 16 bytes): a warp copies 4 rows at a time,
+// lane = vector, all loads issued before the stores, and the row's 4-byte
+// scale groups go to their TCGEN05 atom positions.  Narrow rows (the k-channel
+// residual slices): a thread per (row, vector) / (row, scale group), 32-bit
+// index math.  Padding rows (row_token -1) get zero codes and scales.
 __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__ row_token,
                                                      const int32_t* __restrict__ off, int E,
                                                      int64_t cap, int cols,
@@ -178,41 +178,61 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
   const int natom = ncols16 >> 2;         // 4-byte scale groups per row
   const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t ncode = nrows * nvec;
-  for (int64_t i0 = tid; i0 < ncode; i0 += 4 * nthreads) {
-    uint4 v[4];
+  if (nvec >= 32) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = nthreads >> 5;
+    for (int64_t r0 = (tid >> 5) * 4; r0 < nrows; r0 += nwarps * 4) {
+      int t[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int64_t i = i0 + u * nthreads;
-      v[u] = make_uint4(0, 0, 0, 0);
-      if (i < ncode) {
-        const int t = __ldg(row_token + i / nvec);
-        if (t >= 0) v[u] = __ldg(reinterpret_cast<const uint4*>(ic + (int64_t)t * cbytes) + i % nvec);
+      for (int u = 0; u < 4; ++u) t[u] = r0 + u < nrows ? __ldg(row_token + r0 + u) : -2;
+      for (int v0 = lane; v0 < nvec; v0 += 64) {
+        uint4 buf[4][2];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int v = v0 + 32 * h;
+            buf[u][h] = make_uint4(0, 0, 0, 0);
+            if (t[u] >= 0 && v < nvec)
+              buf[u][h] = __ldg(reinterpret_cast<const uint4*>(ic + (int64_t)t[u] * cbytes) + v);
+          }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int v = v0 + 32 * h;
+            if (t[u] != -2 && v < nvec)
+              reinterpret_cast<uint4*>(oc + (r0 + u) * cbytes)[v] = buf[u][h];
+          }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (t[u] == -2) continue;
+        for (int a = lane; a < natom; a += 32) {
+          uint32_t v = 0;
+          if (t[u] >= 0) v = __ldg(reinterpret_cast<const uint32_t*>(isf + (int64_t)t[u] * ncols16) + a);
+          *reinterpret_cast<uint32_t*>(osf + sf_tc_offset(r0 + u, 4 * a, ncols16)) = v;
+        }
       }
     }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int64_t i = i0 + u * nthreads;
-      if (i < ncode) reinterpret_cast<uint4*>(oc)[i] = v[u];
-    }
+    return;
   }
-  const int64_t nsc = nrows * natom;
-  for (int64_t i0 = tid; i0 < nsc; i0 += 4 * nthreads) {
-    uint32_t v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int64_t i = i0 + u * nthreads;
-      v[u] = 0;
-      if (i < nsc) {
-        const int t = __ldg(row_token + i / natom);
-        if (t >= 0) v[u] = __ldg(reinterpret_cast<const uint32_t*>(isf + (int64_t)t * ncols16) + i % natom);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int64_t i = i0 + u * nthreads;
-      if (i < nsc)
-        *reinterpret_cast<uint32_t*>(osf + sf_tc_offset(i / natom, 4 * (int)(i % natom), ncols16)) = v[u];
+  // narrow rows: nvec < 32, natom < 8; rows * nvec fits comfortably in 32 bits
+  const uint32_t ncode = (uint32_t)(nrows * nvec), nsc = (uint32_t)(nrows * natom);
+  for (uint32_t i = (uint32_t)tid; i < ncode + nsc; i += (uint32_t)nthreads) {
+    if (i < ncode) {
+      const uint32_t r = i / (uint32_t)nvec, v = i - r * (uint32_t)nvec;
+      const int t = __ldg(row_token + r);
+      uint4 x = make_uint4(0, 0, 0, 0);
+      if (t >= 0) x = __ldg(reinterpret_cast<const uint4*>(ic + (int64_t)t * cbytes) + v);
+      reinterpret_cast<uint4*>(oc)[i] = x;
+    } else {
+      const uint32_t j = i - ncode;
+      const uint32_t r = j / (uint32_t)natom, a = j - r * (uint32_t)natom;
+      const int t = __ldg(row_token + r);
+      uint32_t x = 0;
+      if (t >= 0) x = __ldg(reinterpret_cast<const uint32_t*>(isf + (int64_t)t * ncols16) + a);
+      *reinterpret_cast<uint32_t*>(osf + sf_tc_offset(r, 4 * a, ncols16)) = x;
     }
   }
 }
@@ -293,6 +313,8 @@ extern "C" quads_status_t quads_moe_gather(const int32_t* row_token, const int32
   if (((uintptr_t)in_codes | (uintptr_t)out_codes) & 15u || ((uintptr_t)in_scales | (uintptr_t)out_scales) & 3u)
     return fail(QUADS_ERR_MISALIGNED, "moe_gather: alignment");
   cudaStream_t st = (cudaStream_t)stream;
+  if (cols / 32 < 32 && rows_capacity * (cols / 32 + cols / 64) >= (int64_t)1 << 31)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "moe_gather: narrow rows need rows * cols / 32 < 2^31");
   const int64_t vecs = rows_capacity * (cols / 32);   // 16-byte code vectors
   const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((vecs / 4 + 255) / 256, (int64_t)num_sms() * 8));
   gather_kernel<<<blocks, 256, 0, st>>>(row_token, expert_offsets, num_experts, rows_capacity,

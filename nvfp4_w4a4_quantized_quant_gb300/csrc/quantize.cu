@@ -194,9 +194,9 @@ __global__ void __launch_bounds__(256) quantize_kernel(
 // starting from 0 (one float32 add per chunk).  Two launch shapes compute the
 // same sequence of adds:
 //  * long groups (many chunks): a block owns 32 channels of one group; each
-//    slice of up to 256 chunks is staged in shared memory (coalesced reads),
-//    then one warp per channel runs the chain: lane l adds chunks 8l..8l+7 to
-//    the running total handed on from lane l-1;
+//    slice of up to 256 chunks is staged in shared memory by all warps
+//    (coalesced reads, 8 in flight per thread), then lane l of warp 0 adds
+//    channel l's chunks in order;
 //  * short groups: one thread per (group, channel) loops over the chunks.
 __global__ void __launch_bounds__(256) score_chain_kernel(const float* __restrict__ partials,
                                                           int cols,
@@ -206,42 +206,31 @@ __global__ void __launch_bounds__(256) score_chain_kernel(const float* __restric
   __shared__ float tile[256][33];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = blockIdx.y;
-  const int cbase = blockIdx.x * 32;
+  const int c = blockIdx.x * 32 + lane;
   const int64_t a = goff ? (int64_t)goff[g] : 0;
   const int64_t b = goff ? (int64_t)goff[g + 1] : rows;
   const int64_t c0 = a / kScoreChunk, c1 = (b + kScoreChunk - 1) / kScoreChunk;
-  float t[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // running totals of this warp's 4 channels
+  float t = 0.0f;  // warp 0: running total of channel c
   for (int64_t base = c0; base < c1; base += 256) {
     const int n = (int)min((int64_t)256, c1 - base);
-    for (int i = warp; i < n; i += 8) {  // row i of the slice: 32 channels, coalesced
-      const int c = cbase + lane;
-      tile[i][lane] = c < cols ? partials[(base + i) * cols + c] : 0.0f;
-    }
-    __syncthreads();
+    // every thread stages rows warp, warp+8, ... of the slice, 8 loads in flight
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int ch = warp * 4 + q;  // channel within the block
+    for (int j0 = 0; j0 < 32; j0 += 8) {
       float v[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = (8 * lane + i < n) ? tile[8 * lane + i][ch] : 0.0f;
-      const int cnt = max(0, min(8, n - 8 * lane));
-      float tt = t[q];
-#pragma unroll 1
-      for (int l = 0; l < 32; ++l) {
-        if (lane == l)
-          for (int i = 0; i < cnt; ++i) tt = __fadd_rn(tt, v[i]);
-        tt = __shfl_sync(0xffffffffu, tt, l);
+      for (int j = 0; j < 8; ++j) {
+        const int i = warp + 8 * (j0 + j);
+        v[j] = (i < n && c < cols) ? __ldg(partials + (base + i) * cols + c) : 0.0f;
       }
-      t[q] = tt;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) tile[warp + 8 * (j0 + j)][lane] = v[j];
     }
     __syncthreads();
+    if (warp == 0)
+      for (int i = 0; i < n; ++i) t = __fadd_rn(t, tile[i][lane]);
+    __syncthreads();
   }
-  if (lane == 0)
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int c = cbase + warp * 4 + q;
-      if (c < cols) scores[(int64_t)g * cols + c] = t[q];
-    }
+  if (warp == 0 && c < cols) scores[(int64_t)g * cols + c] = t;
 }
 
 __global__ void __launch_bounds__(256) score_loop_kernel(const float* __restrict__ partials,
