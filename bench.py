@@ -187,6 +187,78 @@ def build_layer(torch, seed=0):
     return layer, x_host, l_host
 
 
+def secondary(torch, Q, steps, flush, stream):
+    """The other configurations of the scope table, each captured in a CUDA
+    graph and timed like the step (L2 flushed before every replay):
+    dense projection 4096x2048 x W 6144x2048 (k=128, bf16 Y) compensated and
+    plain, the 512-token decode layer, and TRACE rounding of 16384x2048."""
+    import numpy as np
+    from nvfp4_w4a4_quantized_quant_gb300 import inputs
+    from nvfp4_w4a4_quantized_quant_gb300.layer import CompensatedLinear, MoEExpertLayer
+
+    def graph_ms(fn):
+        with torch.cuda.stream(stream):
+            fn()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            torch.cuda.synchronize()
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            return timed(torch, g.replay, steps, flush, stream) / steps
+
+    out = {}
+    d = inputs.dense_projection(0)
+    x = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).cuda()
+    w = torch.from_numpy(d["w"].view(np.int16)).view(torch.bfloat16).cuda()
+    M, K = x.shape
+    N = w.shape[0]
+    k = 128
+    dense = {}
+    for comp in (True, False):
+        lin = CompensatedLinear(w, k, M, compensate=comp)
+        ms = graph_ms(lambda: lin.forward(x, stream=stream))
+        fl = 2.0 * M * N * (K + (k if comp else 0))
+        dense["comp" if comp else "plain"] = {"ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 1)}
+        del lin
+    dense["overhead_pct"] = round(100.0 * (dense["comp"]["ms"] / dense["plain"]["ms"] - 1.0), 1)
+    dense["shape"] = {"M": M, "K": K, "N": N, "k": k, "y": "bf16"}
+    out["dense_projection"] = dense
+    del x, w
+
+    wl = dict(WORKLOAD, tokens=512)
+    dd = inputs.moe_layer(0, tokens=512, hidden=wl["hidden"], experts=wl["experts"], topk=wl["topk"],
+                          ffn=wl["ffn"], k=wl["k1"], with_weights=False)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1)
+    E, H, F = wl["experts"], wl["hidden"], wl["ffn"]
+    w1 = (torch.randn((E, 2 * F, H), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    w2 = (torch.randn((E, H, F), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    layer = MoEExpertLayer(w1, w2, wl["topk"], wl["k1"], wl["k2"], 512)
+    del w1, w2
+    xd = torch.from_numpy(dd["x"].view(np.int16)).view(torch.bfloat16).cuda()
+    ld = torch.from_numpy(dd["logits"]).cuda()
+    ms = graph_ms(lambda: layer.forward(xd, ld, stream=stream))
+    wbytes = E * (2 * F * H + H * F) * (0.5 + 1.0 / 16)
+    out["moe_decode_512"] = {"ms": round(ms, 4), "weight_gbs": round(wbytes / (ms * 1e-3) / 1e9, 1),
+                             "weight_bytes": int(wbytes), "frac_hbm": None}
+    del layer
+
+    t = inputs.trace_rounding(0)
+    xr = torch.from_numpy(t["x_rollout"].view(np.int16)).view(torch.bfloat16).cuda()
+    xt = torch.from_numpy(t["x_train"].view(np.int16)).view(torch.bfloat16).cuda()
+    rq, _ = Q.quantize_nvfp4(xr)
+    codes = torch.empty((xt.shape[0], xt.shape[1] // 2), dtype=torch.uint8, device="cuda")
+    cnt = torch.zeros(3, dtype=torch.int64, device="cuda")
+    ms = graph_ms(lambda: Q.trace_round(xt, rq, counters=cnt, out=codes, stream=stream))
+    tb = xt.numel() * (2 + 0.5 + 0.5 + 1.0 / 16)
+    out["trace_16384x2048"] = {"ms": round(ms, 4), "gbs": round(tb / (ms * 1e-3) / 1e9, 1),
+                               "algorithmic_bytes": int(tb)}
+    return out
+
+
 def timed(torch, fn, steps, flush, stream):
     """Sum of per-step device times (ms) with an L2 flush before each step."""
     tot = 0.0
@@ -282,6 +354,7 @@ def run_gpu(args):
             out_host.copy_(layer.b["out"], non_blocking=True)
         e2e_ms = timed(torch, e2e, args.steps, flush, stream)
     torch.cuda.synchronize()
+    sec = secondary(torch, Q, args.steps, flush, stream) if rank == 0 else None
 
     ms = t_ms / args.steps
     e_ms = e2e_ms / args.steps
@@ -291,6 +364,11 @@ def run_gpu(args):
         ms, e_ms = t.tolist()
     if rank != 0:
         return
+    if sec:
+        dec = sec["moe_decode_512"]
+        dec["frac_hbm"] = round(dec["weight_bytes"] / (dec["ms"] * 1e-3) / 1e9 / pk["hbm"], 4)
+        tr = sec["trace_16384x2048"]
+        tr["frac_hbm"] = round(tr["gbs"] / pk["hbm"], 4)
     fl = moe_flops()
     value = world * fl / (ms * 1e-3) / 1e12
     e2e_val = world * fl / (e_ms * 1e-3) / 1e12
@@ -329,6 +407,7 @@ def run_gpu(args):
             "algorithmic_bytes": int(g1_bytes),
             "peak_source": pk["src"],
         },
+        "secondary": sec,
         "quantizer": {"gbs": round(q_bytes / (q_ms * 1e-3) / 1e9, 1), "frac_hbm": round(q_bytes / (q_ms * 1e-3) / 1e9 / pk["hbm"], 4),
                       "ms": round(q_ms, 4), "shape": [T, H], "algorithmic_bytes": int(q_bytes)},
         "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s",

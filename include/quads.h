@@ -314,6 +314,7 @@ quads_status_t quads_weight_columns(const uint8_t* w_codes, const uint8_t* w_sca
  *   counters nullable device uint64 [3], ADDED to: #(RTN code != rollout code),
  *   #(TRACE code != rollout code), #(RTN mismatches one signed level away),
  *   codes compared by value (+0 == -0).
+ *   rows * cols / 8 < 2^31 (else QUADS_ERR_UNSUPPORTED_SHAPE).
  */
 quads_status_t quads_trace_round(const void* x_train, int64_t rows, int64_t cols, int64_t ldx,
                                  const uint8_t* rollout_codes, int64_t ld_codes,

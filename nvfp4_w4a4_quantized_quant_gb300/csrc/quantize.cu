@@ -440,74 +440,58 @@ __global__ void __launch_bounds__(256) rsel_quantize_kernel(
 }
 
 // ---------------------------------------------------------------- TRACE
-// Signed E2M1 levels ascending, +0 and -0 merged: index 0..14 = -6 .. 6.
-__device__ __forceinline__ int signed_level_index(float q) {
-  const float a = fabsf(q);
-  // magnitude index 0..7 of an exact level
-  int mi = a == 0.f ? 0 : a == 0.5f ? 1 : a == 1.f ? 2 : a == 1.5f ? 3 : a == 2.f ? 4
-         : a == 3.f ? 5 : a == 4.f ? 6 : 7;
-  return q < 0.f ? 7 - mi : 7 + mi;
+// Signed level index of an E2M1 code: the 3 magnitude bits are the index of
+// the level among {0, .5, 1, 1.5, 2, 3, 4, 6}; negative codes count down, and
+// -0 and +0 share index 0.
+__device__ __forceinline__ int signed_index(uint32_t c) {
+  const int m = (int)(c & 7u);
+  return (c & 8u) ? -m : m;
 }
 
-__device__ __forceinline__ float level_of_index(int i) {
-  const int mi = i >= 7 ? i - 7 : 7 - i;
-  const float mag = e2m1_to_f32((uint32_t)mi);
-  return i < 7 ? -mag : mag;
-}
-
+// One thread per 8 consecutive elements of a row (one half of a 16-block).
+// Neighbours and the choice are taken on signed level indices: the RTN level
+// sn is one neighbour of v and the other is sn - 1 (RTN level above v) or
+// sn + 1 (below v); of two adjacent levels the one nearer the rollout level
+// sr is the lower one exactly when sr <= the lower index.
 __global__ void __launch_bounds__(256) trace_kernel(
     const __nv_bfloat16* __restrict__ xt, int64_t rows, int cols, int64_t ldx,
     const uint8_t* __restrict__ rcodes, int64_t ldc, const uint8_t* __restrict__ rscales,
     const float* __restrict__ rst, uint8_t* __restrict__ out,
     unsigned long long* __restrict__ counters) {
-  const int vec_per_row = cols >> 3;
-  const int64_t total = rows * vec_per_row;
+  const uint32_t vec_per_row = (uint32_t)cols >> 3;
+  const uint32_t total = (uint32_t)(rows * vec_per_row);   // < 2^31 (host check)
   const float s_t = rst[0];
   unsigned int n_rtn = 0, n_tr = 0, n_adj = 0;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / vec_per_row;
-    const int col = (int)(i % vec_per_row) * 8;
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const uint32_t r = i / vec_per_row;
+    const int col = (int)(i - r * vec_per_row) * 8;
     float f[8];
-    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(xt + r * ldx + col)), f);
-    const uint32_t rc = *reinterpret_cast<const uint32_t*>(rcodes + r * ldc + (col >> 1));
-    const BlockScale bs = block_scale_from_byte(rscales[r * (cols >> 4) + (col >> 4)], s_t);
+    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(xt + (int64_t)r * ldx + col)), f);
+    const uint32_t rc = __ldg(reinterpret_cast<const uint32_t*>(rcodes + (int64_t)r * ldc + (col >> 1)));
+    const BlockScale bs =
+        block_scale_from_byte(__ldg(rscales + (int64_t)r * (cols >> 4) + (col >> 4)), s_t);
     float v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = bs.zero ? 0.0f : __fmul_rn(f[j], bs.r);
+    for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(f[j], bs.r);
     const uint32_t rtn = bs.zero ? 0u : f32x8_to_e2m1(v);
+    float qn[8];
+    e2m1x8_to_f32(rtn, qn);
     uint32_t outw = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const float qr = e2m1_to_f32((rc >> (4 * j)) & 15u);
-      const float qn = e2m1_to_f32((rtn >> (4 * j)) & 15u);
-      uint32_t code;
-      float qt;
-      if (bs.zero) {
-        code = 0u;
-        qt = 0.0f;
-      } else {
-        // neighbours of v: the RTN level is one of them; the other is the next
-        // level on the far side of v (or the same when v is a level / clamped)
-        const float vc = fminf(fmaxf(v[j], -6.0f), 6.0f);
-        const int in_ = signed_level_index(qn);
-        int ilo = in_, ihi = in_;
-        if (qn > vc) ilo = in_ - 1;
-        else if (qn < vc) ihi = in_ + 1;
-        const float qlo = level_of_index(ilo), qhi = level_of_index(ihi);
-        qt = fabsf(qlo - qr) <= fabsf(qhi - qr) ? qlo : qhi;
-        const uint32_t mag = (uint32_t)(signed_level_index(fabsf(qt)) - 7);
-        const bool neg = qt < 0.0f || (qt == 0.0f && signbit(v[j]));
-        code = mag | (neg ? 8u : 0u);
-      }
-      outw |= code << (4 * j);
-      if (qn != qr) {
-        ++n_rtn;
-        if (abs(signed_level_index(qn) - signed_level_index(qr)) == 1) ++n_adj;
-      }
-      if (qt != qr) ++n_tr;
+      const int sn = signed_index((rtn >> (4 * j)) & 15u);
+      const int sr = signed_index((rc >> (4 * j)) & 15u);
+      const float vc = fminf(fmaxf(v[j], -6.0f), 6.0f);
+      const int ilo = sn - (qn[j] > vc ? 1 : 0);
+      const int ihi = sn + (qn[j] < vc ? 1 : 0);
+      const int stc = bs.zero ? 0 : (sr <= ilo ? ilo : ihi);
+      const bool neg = !bs.zero && (stc < 0 || (stc == 0 && signbit(v[j])));
+      outw |= ((uint32_t)abs(stc) | (neg ? 8u : 0u)) << (4 * j);
+      n_rtn += sn != sr ? 1u : 0u;
+      n_adj += (sn != sr && abs(sn - sr) == 1) ? 1u : 0u;
+      n_tr += stc != sr ? 1u : 0u;
     }
-    *reinterpret_cast<uint32_t*>(out + r * ldc + (col >> 1)) = outw;
+    *reinterpret_cast<uint32_t*>(out + (int64_t)r * ldc + (col >> 1)) = outw;
   }
   if (counters) {
 #pragma unroll
@@ -669,6 +653,8 @@ extern "C" quads_status_t quads_trace_round(const void* x_train, int64_t rows, i
   if (ldx < cols || ldx % 8 || ld_codes < cols / 2 || ld_codes % 4 || !aligned16(x_train))
     return fail(QUADS_ERR_MISALIGNED, "trace_round: leading dimensions / alignment");
   if (rows == 0) return QUADS_OK;
+  if (rows * (cols / 8) >= ((int64_t)1 << 31))
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "trace_round: rows * cols / 8 must be < 2^31");
   cudaStream_t st = (cudaStream_t)stream;
   trace_kernel<<<grid_for(rows * (cols / 8), 256), 256, 0, st>>>(
       (const __nv_bfloat16*)x_train, rows, (int)cols, ldx, rollout_codes, ld_codes,
