@@ -568,6 +568,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_ld16(t1 + 64 + c0, u1);
           if (p.comp) { tc_ld16(t2 + c0, g2); tc_ld16(t2 + 64 + c0, u2); }
           tc_wait_ld();
+          if (c0 + 16 == half * 32 + 32) {
+            // the last TMEM read of this tile is done: release the accumulators
+            // before the math and the stores, so the next MMAs can start
+            tc_fence_before();
+            mbar_arrive(&acc_empty[b]);
+          }
           uint32_t packed[8];
 #pragma unroll
           for (int i = 0; i < 16; i += 2) {
@@ -599,6 +605,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_ld16(t1 + c0, v1);
           if (p.comp) tc_ld16(t2 + c0, v2);
           tc_wait_ld();
+          if (c0 + 16 == half * 64 + 64) {
+            // the last TMEM read of this tile is done: release the accumulators
+            tc_fence_before();
+            mbar_arrive(&acc_empty[b]);
+          }
           float o[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) o[i] = p.comp ? fmaf(a2, v2[i], a1 * v1[i]) : a1 * v1[i];
@@ -627,8 +638,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       __syncwarp();
-      tc_fence_before();
-      mbar_arrive(&acc_empty[b]);
       if (p.y_amax) {
         amax = warp_max(amax);
         if (lane == 0 && amax > 0.0f) atomicMax(&p.y_amax[tl.e], __float_as_uint(amax));
