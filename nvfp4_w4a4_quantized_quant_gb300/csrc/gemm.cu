@@ -683,54 +683,65 @@ __global__ void __launch_bounds__(256) wtrans_kernel(const uint8_t* __restrict__
   }
 }
 
-// For every weight row r (of every expert) and every 16-block of the selected
-// channels: gather the selected columns of DQ(Q(W)) in units of s_w
-// (level * E4M3 scale, exact), requantize with tensor scale 1 (s_w kept).
-// A warp owns one 16-column block of 32 consecutive rows (lane = row) of one
-// expert and reads the column-major copy, so every gather of a selected
-// column is one coalesced 16-byte (codes) + 32-byte (scales) access; one warp
-// per block keeps all of a row group's gathers in flight at once.  Output
-// codes [E*N, kpad/2] and TCGEN05 scales over kpad columns.
-__global__ void __launch_bounds__(256) wsel_kernel(
-    const uint8_t* __restrict__ ct, const uint8_t* __restrict__ st, int64_t rows /*E*N*/, int N,
-    int K, const int32_t* __restrict__ sel, int sel_pe, int k, int kpad,
-    uint8_t* __restrict__ oc, uint8_t* __restrict__ osf) {
-  const int lane = threadIdx.x & 31;
-  const int nb = kpad >> 4;
-  const uint32_t nitems = (uint32_t)(rows >> 5) * (uint32_t)nb;   // < 2^31 (host check)
-  for (uint32_t item = (uint32_t)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-       item < nitems; item += (uint32_t)(((int64_t)gridDim.x * blockDim.x) >> 5)) {
-    const uint32_t w = item / (uint32_t)nb;
-    const int blk = (int)(item - w * (uint32_t)nb);
-    const uint32_t r = w * 32 + lane;
-    const uint32_t e = r / (uint32_t)N, n = r - e * (uint32_t)N;
-    uint32_t lo = 0, hi = 0, sbyte = 0;
-    if (blk * 16 < k) {
-      const int32_t* s = sel + (sel_pe ? (int64_t)e * k : 0) + blk * 16;
-      const uint8_t* cte = ct + (int64_t)e * K * (N / 2) + n / 2;
-      const uint8_t* ste = st + (int64_t)e * (K / 16) * N + n;
-      const uint32_t sh = (n & 1) * 4;
-      uint32_t codes[16], sbytes[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int c = __ldg(s + j);   // k % 16 == 0: a started block is full
-        codes[j] = __ldg(cte + (int64_t)c * (N / 2));
-        sbytes[j] = __ldg(ste + (int64_t)(c >> 4) * N);
-      }
-      float w16[16];
-      float m = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        w16[j] = __fmul_rn(e2m1_to_f32((codes[j] >> sh) & 15u), e4m3_to_f32(sbytes[j]));
-        m = fmaxf(m, fabsf(w16[j]));
-      }
-      const BlockScale bs = block_scale(m, 1.0f);
-      lo = quantize8(w16, bs);
-      hi = quantize8(w16 + 8, bs);
-      sbyte = bs.byte;
+// Q(W_sel): for every weight row r (of every expert) and every 16-block of the
+// selected channels, gather the selected columns of DQ(Q(W)) in units of s_w
+// (level * E4M3 scale, exact) and requantize with tensor scale 1 (s_w kept).
+// Output codes [E*N, kpad/2] and TCGEN05 scales over kpad columns.
+// One CTA per (16-column block of the selection, group, chunk of NC rows):
+// the chunk's codes (NC/2 bytes) and scale bytes (NC) of
+// the block's 16 selected columns -- contiguous runs in the column-major copy
+// -- are staged in shared memory with 16-byte loads, then each thread
+// requantizes rows from there.  Long runs keep DRAM and L2 busy, where
+// per-row 16/32-byte gathers wait on latency.  Padding blocks (>= k) get zero
+// codes and scales.
+__global__ void __launch_bounds__(256) wsel_cols_kernel(
+    const uint8_t* __restrict__ ct, const uint8_t* __restrict__ st, int N, int K, int NC,
+    const int32_t* __restrict__ sel, int sel_pe, int k, int kpad, uint8_t* __restrict__ oc,
+    uint8_t* __restrict__ osf) {
+  extern __shared__ __align__(16) uint8_t wsm[];
+  uint8_t* sc = wsm;                   // [16][NC/2] codes
+  uint8_t* ss = wsm + 16 * (NC / 2);   // [16][NC] scale bytes
+  const int blk = blockIdx.x, e = blockIdx.y, n0 = blockIdx.z * NC, nb = kpad >> 4;
+  const int64_t r0 = (int64_t)e * N + n0;
+  if (blk * 16 >= k) {
+    for (int n = threadIdx.x; n < NC; n += blockDim.x) {
+      *reinterpret_cast<uint2*>(oc + (r0 + n) * (kpad >> 1) + blk * 8) = make_uint2(0, 0);
+      osf[sf_tc_offset(r0 + n, blk, nb)] = 0;
     }
-    *reinterpret_cast<uint2*>(oc + (int64_t)r * (kpad >> 1) + blk * 8) = make_uint2(lo, hi);
-    osf[sf_tc_offset(r, blk, nb)] = (uint8_t)sbyte;
+    return;
+  }
+  const int32_t* s = sel + (sel_pe ? (int64_t)e * k : 0) + blk * 16;
+  const uint8_t* cte = ct + (int64_t)e * K * (N / 2) + n0 / 2;
+  const uint8_t* ste = st + (int64_t)e * (K / 16) * N + n0;
+  const int cv = NC >> 5, sv = NC >> 4;   // 16-byte vectors per code run / scale run
+  for (int i = threadIdx.x; i < 16 * (cv + sv); i += blockDim.x) {
+    if (i < 16 * cv) {
+      const int j = i / cv, v = i - j * cv;
+      const int c = __ldg(s + j);
+      reinterpret_cast<uint4*>(sc + j * (NC / 2))[v] =
+          __ldg(reinterpret_cast<const uint4*>(cte + (int64_t)c * (N / 2)) + v);
+    } else {
+      const int i2 = i - 16 * cv, j = i2 / sv, v = i2 - j * sv;
+      const int c = __ldg(s + j);
+      reinterpret_cast<uint4*>(ss + j * NC)[v] =
+          __ldg(reinterpret_cast<const uint4*>(ste + (int64_t)(c >> 4) * N) + v);
+    }
+  }
+  __syncthreads();
+  for (int n = threadIdx.x; n < NC; n += blockDim.x) {
+    const uint32_t sh = (n & 1) * 4;
+    float w16[16];
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t code = (sc[j * (NC / 2) + (n >> 1)] >> sh) & 15u;
+      w16[j] = __fmul_rn(e2m1_to_f32(code), e4m3_to_f32(ss[j * NC + n]));
+      m = fmaxf(m, fabsf(w16[j]));
+    }
+    const BlockScale bs = block_scale(m, 1.0f);
+    *reinterpret_cast<uint2*>(oc + (r0 + n) * (kpad >> 1) + blk * 8) =
+        make_uint2(quantize8(w16, bs), quantize8(w16 + 8, bs));
+    osf[sf_tc_offset(r0 + n, blk, nb)] = (uint8_t)bs.byte;
   }
 }
 
@@ -797,12 +808,14 @@ static quads_status_t launch(const Launch& L) {
       return fail(QUADS_ERR_WORKSPACE, "gemm: workspace needs %zu bytes", need);
     ws_codes = (uint8_t*)L.ws;
     ws_sf = ws_codes + (((size_t)brows * (L.kpad / 2) + 1023) & ~(size_t)1023);
-    const int64_t items = (brows / 32) * (L.kpad / 16);  // one warp per 32 rows x 16 columns
-    if (items >= ((int64_t)1 << 31) || brows >= ((int64_t)1 << 31))
-      return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "gemm: W_sel extraction needs E*N*kpad/512 < 2^31");
-    int blocks = (int)std::min<int64_t>((items * 32 + 255) / 256, (int64_t)num_sms() * 32);
-    wsel_kernel<<<blocks, 256, 0, L.stream>>>(L.b_t, L.b_sf_t, brows, L.N, L.K, L.sel, L.sel_pe,
-                                               L.k, L.kpad, ws_codes, ws_sf);
+    // row chunks of 512 (or 128) rows: N is a multiple of 128
+    const int NC = L.N % 512 == 0 ? 512 : 128;
+    {
+      const size_t cols_smem = (size_t)24 * NC;   // 16 columns x (NC/2 code + NC scale bytes)
+      wsel_cols_kernel<<<dim3((unsigned)(L.kpad / 16), (unsigned)L.E, (unsigned)(L.N / NC)), 256,
+                         cols_smem, L.stream>>>(L.b_t, L.b_sf_t, L.N, L.K, NC, L.sel, L.sel_pe,
+                                                L.k, L.kpad, ws_codes, ws_sf);
+    }
   }
   CUtensorMap tA, tB, tR, tW;
   const int64_t arows = L.row_off ? L.rows_cap : L.M;
