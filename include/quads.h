@@ -115,7 +115,7 @@ quads_status_t quads_device_status(void* stream, int32_t* device_code);
  *   QUADS_OP_GEMM:     the requantized selected weight columns Q(W_sel):
  *                      n*kpad/2 code bytes + n*kpad/16 scale bytes (+ alignment).
  *   QUADS_OP_MOE_GEMM: the same for num_groups experts.
- *   QUADS_OP_MOE_ROUTE: one bit per (token, expert): rows = tokens, cols = experts.
+ *   QUADS_OP_MOE_ROUTE: two int32 per (32-token block, expert): rows = tokens, cols = experts.
  * `cols` is the channel count (K) and `n` the output width (N, unused for the
  * activation-side ops).  kpad = k rounded up to 64 (k <= 256) or to 256. */
 size_t quads_workspace_size(int32_t op, int64_t rows, int64_t cols, int64_t n, int32_t k,

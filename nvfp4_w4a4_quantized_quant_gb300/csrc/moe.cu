@@ -4,8 +4,8 @@
 // combine.  [TRACE digest] "MoE 专家路由敏感性": the router sends every token to a
 // few experts by gate score.
 //
-// Determinism: counts use integer atomics (order-free); every row position is
-// a prefix count over tokens, so the plan is identical from run to run.
+// Determinism: counts and row positions are prefix counts over tokens (no
+// atomics), so the plan is identical from run to run.
 #include <algorithm>
 #include <cstdio>
 
@@ -16,30 +16,37 @@ namespace quads {
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopk = 16;
 
-// One warp per token.  Lane l holds logits l, l+32, ...; round r takes the
-// warp arg-max (ties -> lower expert id), removes it, and lane r keeps it.
-// The chosen experts are then ranked by id (ascending slot order), gates are
-// exp(l - lmax) / sum over the chosen, the token's expert set is written as a
-// bit mask (for the row assignment), and each chosen expert's count is bumped
-// (integer atomics: the totals do not depend on their order).
-__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T,
-                                                    int E, int topk, int32_t* __restrict__ idx,
-                                                    float* __restrict__ gates,
-                                                    uint32_t* __restrict__ emask,
-                                                    int32_t* __restrict__ counts) {
-  const int lane = threadIdx.x & 31;
+constexpr int kRouteTokens = 32;   // tokens per routing block: one warp each
+
+// One block of 32 warps per 32 consecutive tokens, one warp per token.  Lane l
+// holds logits l, l+32, ...; round r takes the warp arg-max (ties -> lower
+// expert id), removes it, and lane r keeps it.  The chosen experts are ranked
+// by id (ascending slot order) and gates are exp(l - lmax) / sum over the
+// chosen.  Then, from the block's per-token expert bit masks in shared
+// memory: each (token, slot) gets its rank among the block's earlier tokens
+// routed to the same expert (stored in token_row, turned into a row by
+// assign_kernel), and each expert its count of the block's tokens, written to
+// bcount[e][block] -- no atomics, so every number is independent of
+// scheduling.
+__global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ logits, int T,
+                                                     int E, int topk, int32_t* __restrict__ idx,
+                                                     float* __restrict__ gates,
+                                                     int32_t* __restrict__ bcount,
+                                                     int32_t* __restrict__ local_rank) {
+  __shared__ uint32_t smask[kRouteTokens][kMaxExperts / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t = blockIdx.x * kRouteTokens + warp;
   const int words = (E + 31) >> 5;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T;
-       t += (gridDim.x * blockDim.x) >> 5) {
+  const bool live = t < T;
+  int my_e = 0x7fffffff, rank = 0;
+  if (live) {
     float v[kMaxExperts / 32];
-    const int per = words;
 #pragma unroll
     for (int i = 0; i < kMaxExperts / 32; ++i) {
       const int e = lane + 32 * i;
-      v[i] = (i < per && e < E) ? logits[(int64_t)t * E + e] : -INFINITY;
+      v[i] = (i < words && e < E) ? logits[(int64_t)t * E + e] : -INFINITY;
     }
     uint32_t taken = 0;
-    int my_e = 0x7fffffff;
     float my_l = -INFINITY, lmax = -INFINITY;
     for (int r = 0; r < topk; ++r) {
       float bv = -INFINITY;
@@ -47,7 +54,7 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
 #pragma unroll
       for (int i = 0; i < kMaxExperts / 32; ++i) {
         const int e = lane + 32 * i;
-        if (i < per && e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
+        if (i < words && e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
           bv = v[i];
           be = e;
         }
@@ -67,7 +74,6 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
     float s = p;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    int rank = 0;
     for (int j = 0; j < topk; ++j) {
       const int ej = __shfl_sync(0xffffffffu, my_e, j);
       rank += (ej < my_e) ? 1 : 0;
@@ -75,88 +81,115 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
     if (mine) {
       idx[(int64_t)t * topk + rank] = my_e;
       gates[(int64_t)t * topk + rank] = p / s;
-      atomicAdd(&counts[my_e], 1);
     }
     for (int w = 0; w < words; ++w) {
       const uint32_t bit = (mine && (my_e >> 5) == w) ? (1u << (my_e & 31)) : 0u;
       const uint32_t m = __reduce_or_sync(0xffffffffu, bit);
-      if (lane == 0) emask[(int64_t)t * words + w] = m;
+      if (lane == 0) smask[warp][w] = m;
     }
+  }
+  __syncthreads();
+  const int nlive = min(kRouteTokens, T - (int)blockIdx.x * kRouteTokens);
+  if (live && lane < topk) {
+    const int mw = my_e >> 5;
+    const uint32_t mb = 1u << (my_e & 31);
+    int r = 0;
+    for (int i = 0; i < warp; ++i) r += (smask[i][mw] & mb) ? 1 : 0;
+    local_rank[(int64_t)t * topk + rank] = r;
+  }
+  if ((int)threadIdx.x < E) {
+    const int mw = threadIdx.x >> 5;
+    const uint32_t mb = 1u << (threadIdx.x & 31);
+    int c = 0;
+    for (int i = 0; i < nlive; ++i) c += (smask[i][mw] & mb) ? 1 : 0;
+    bcount[(int64_t)threadIdx.x * gridDim.x + blockIdx.x] = c;
   }
 }
 
-// Padded offsets off[e+1] = off[e] + roundup(count[e], 128): one block of
-// kMaxExperts threads scans the expert counts.
-__global__ void __launch_bounds__(kMaxExperts) plan_kernel(const int32_t* __restrict__ counts,
-                                                           int E, int32_t* __restrict__ off) {
+// One block: warp w scans the per-block counts of experts w, w+32, ... over the
+// routing blocks (block_prefix[e][b] = tokens of expert e in blocks < b, and
+// the expert's total count; each expert's counts are contiguous, loaded 8 per
+// lane at once), then the padded offsets
+// off[e+1] = off[e] + roundup(count[e], 128) by a scan over the experts.
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ bcount, int nb,
+                                                    int E, int32_t* __restrict__ bprefix,
+                                                    int32_t* __restrict__ counts,
+                                                    int32_t* __restrict__ off) {
+  __shared__ int cnt[kMaxExperts];
   __shared__ int warp_sums[kMaxExperts / 32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int cnt = threadIdx.x < E ? counts[threadIdx.x] : 0;
-  int v = (cnt + QUADS_MOE_ROW_ALIGN - 1) / QUADS_MOE_ROW_ALIGN * QUADS_MOE_ROW_ALIGN;
+  for (int e = w; e < E; e += 32) {
+    const int32_t* bc = bcount + (int64_t)e * nb;
+    int32_t* bp = bprefix + (int64_t)e * nb;
+    int running = 0;
+    for (int b0 = 0; b0 < nb; b0 += 256) {   // lane l: blocks b0 + 8l .. b0 + 8l + 7
+      int v[8], sum = 0;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += u;
-  }
-  if (lane == 31) warp_sums[w] = v;
-  __syncthreads();
-  int before = 0;
-  for (int i = 0; i < w; ++i) before += warp_sums[i];
-  if (threadIdx.x < E) off[threadIdx.x + 1] = v + before;
-  if (threadIdx.x == 0) off[0] = 0;
-}
-
-// One block per expert: thread i covers a contiguous run of tokens, counts the
-// ones routed to the expert (one bit of the token's expert mask each), a block
-// exclusive scan gives each run its first row, and the rows are then written
-// in token order.  A token's slot is the number of its experts with a lower
-// id.  Padding rows get row_token = -1.
-__global__ void __launch_bounds__(1024) assign_kernel(const uint32_t* __restrict__ emask, int T,
-                                                      int E, int topk,
-                                                      const int32_t* __restrict__ off,
-                                                      const int32_t* __restrict__ counts,
-                                                      int32_t* __restrict__ row_token,
-                                                      int32_t* __restrict__ token_row) {
-  __shared__ int warp_sums[32];
-  const int e = blockIdx.x;
-  const int words = (E + 31) >> 5;
-  const int ew = e >> 5;
-  const uint32_t ebit = 1u << (e & 31);
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int per = (T + blockDim.x - 1) / blockDim.x;
-  const int t0 = min(T, (int)threadIdx.x * per), t1 = min(T, t0 + per);
-  int cnt = 0;
-  for (int t = t0; t < t1; ++t) cnt += (emask[(int64_t)t * words + ew] & ebit) ? 1 : 0;
-  int v = cnt;
+      for (int i = 0; i < 8; ++i) {
+        const int b = b0 + 8 * lane + i;
+        v[i] = b < nb ? bc[b] : 0;
+        sum += v[i];
+      }
+      int incl = sum;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += u;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      int x = running + incl - sum;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int b = b0 + 8 * lane + i;
+        if (b < nb) bp[b] = x;
+        x += v[i];
+      }
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) { cnt[e] = running; counts[e] = running; }
   }
-  if (lane == 31) warp_sums[w] = v;
   __syncthreads();
-  if (w == 0) {
-    int x = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+  int v = 0;   // inclusive padded count of experts <= threadIdx.x within the warp
+  if (threadIdx.x < kMaxExperts) {
+    const int c = (int)threadIdx.x < E ? cnt[threadIdx.x] : 0;
+    v = (c + QUADS_MOE_ROW_ALIGN - 1) / QUADS_MOE_ROW_ALIGN * QUADS_MOE_ROW_ALIGN;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += u;
+      const int u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
     }
-    warp_sums[lane] = x;
+    if (lane == 31) warp_sums[w] = v;
   }
   __syncthreads();
-  int row = off[e] + v - cnt + (w > 0 ? warp_sums[w - 1] : 0);
-  for (int t = t0; t < t1; ++t) {
-    const uint32_t word = emask[(int64_t)t * words + ew];
-    if (word & ebit) {
-      int slot = __popc(word & (ebit - 1u));
-      for (int i = 0; i < ew; ++i) slot += __popc(emask[(int64_t)t * words + i]);
-      row_token[row] = t;
-      token_row[(int64_t)t * topk + slot] = row;
-      ++row;
-    }
+  if (threadIdx.x < kMaxExperts) {
+    int before = 0;
+    for (int i = 0; i < w; ++i) before += warp_sums[i];
+    if ((int)threadIdx.x < E) off[threadIdx.x + 1] = v + before;
+    if (threadIdx.x == 0) off[0] = 0;
   }
-  for (int r = off[e] + counts[e] + threadIdx.x; r < off[e + 1]; r += blockDim.x) row_token[r] = -1;
+}
+
+// Rows of the plan: slot (t, j) routed to expert e goes to row
+// off[e] + block_prefix[e][t / 32] + its rank within the routing block, so
+// each expert's rows hold its tokens in ascending token order.  Padding rows
+// get row_token = -1.
+__global__ void __launch_bounds__(256) assign_kernel(const int32_t* __restrict__ idx, int T, int E,
+                                                     int topk, int nb,
+                                                     const int32_t* __restrict__ bprefix,
+                                                     const int32_t* __restrict__ off,
+                                                     const int32_t* __restrict__ counts,
+                                                     int32_t* __restrict__ row_token,
+                                                     int32_t* __restrict__ token_row) {
+  const int total = T * topk;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const int t = i / topk;
+    const int e = idx[i];
+    const int row = off[e] + bprefix[(int64_t)e * nb + t / kRouteTokens] + token_row[i];
+    token_row[i] = row;
+    row_token[row] = t;
+  }
+  for (int e = blockIdx.x; e < E; e += gridDim.x)
+    for (int r = off[e] + counts[e] + (int)threadIdx.x; r < off[e + 1]; r += blockDim.x)
+      row_token[r] = -1;
 }
 
 // Wide rows (>= 32 code vectors of 16 bytes): a warp copies 4 rows at a time,
@@ -289,15 +322,17 @@ extern "C" quads_status_t quads_moe_route(const float* logits, int32_t tokens, i
   const size_t need = quads_workspace_size(QUADS_OP_MOE_ROUTE, tokens, num_experts, 0, topk, 1);
   if (!workspace || workspace_bytes < need)
     return fail(QUADS_ERR_WORKSPACE, "moe_route: workspace needs %zu bytes", need);
-  uint32_t* emask = (uint32_t*)workspace;
+  const int nb = (tokens + kRouteTokens - 1) / kRouteTokens;
+  int32_t* bcount = (int32_t*)workspace;                       // [E, nb]
+  int32_t* bprefix = bcount + (size_t)nb * num_experts;         // [E, nb]
   cudaStream_t st = (cudaStream_t)stream;
-  cudaMemsetAsync(expert_counts, 0, (size_t)num_experts * sizeof(int32_t), st);
   if (tokens > 0)
-    route_kernel<<<(tokens * 32 + 255) / 256, 256, 0, st>>>(logits, tokens, num_experts, topk,
-                                                             topk_idx, gates, emask, expert_counts);
-  plan_kernel<<<1, kMaxExperts, 0, st>>>(expert_counts, num_experts, expert_offsets);
-  assign_kernel<<<num_experts, 1024, 0, st>>>(emask, tokens, num_experts, topk, expert_offsets,
-                                              expert_counts, row_token, token_row);
+    route_kernel<<<nb, 32 * kRouteTokens, 0, st>>>(logits, tokens, num_experts, topk, topk_idx,
+                                                    gates, bcount, token_row);
+  plan_kernel<<<1, 1024, 0, st>>>(bcount, nb, num_experts, bprefix, expert_counts, expert_offsets);
+  assign_kernel<<<std::max(1, std::min(num_sms() * 4, (tokens * topk + 255) / 256)), 256, 0, st>>>(
+      topk_idx, tokens, num_experts, topk, nb, bprefix, expert_offsets, expert_counts, row_token,
+      token_row);
   return check_launch("moe_route", tokens > 0 ? 3 : 2);
 }
 

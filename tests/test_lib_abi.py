@@ -28,7 +28,7 @@ def test_status_strings_and_sizes(lib):
     assert lib.quads_workspace_size(quads.OP_QUANTIZE, 10, 64, 0, 0, 3) == 12
     sel = lib.quads_workspace_size(quads.OP_SELECT, 100, 256, 0, 16, 2)
     assert sel == ((100 * 16 * 4 + 255) // 256) * 256 + 256 + 2 * 256 * 4
-    assert lib.quads_workspace_size(quads.OP_MOE_ROUTE, 100, 128, 0, 8, 1) == 100 * 4 * 4 + 16
+    assert lib.quads_workspace_size(quads.OP_MOE_ROUTE, 100, 128, 0, 8, 1) == 4 * 128 * 8 + 16
     g = lib.quads_workspace_size(quads.OP_GEMM, 0, 2048, 6144, 128, 1)
     assert g == ((6144 * 64 + 1023) // 1024) * 1024 + 6144 * 8
 
