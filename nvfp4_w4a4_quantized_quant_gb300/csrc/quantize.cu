@@ -70,12 +70,6 @@ __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restri
   }
 }
 
-__global__ void tensor_scale_kernel(const uint32_t* __restrict__ amax_bits, int G,
-                                    float* __restrict__ st_out) {
-  for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < G; g += gridDim.x * blockDim.x)
-    st_out[g] = tensor_scale_from_amax(__uint_as_float(amax_bits[g]));
-}
-
 // ---------------------------------------------------------------- quantize
 // A block owns one (32-row chunk, 256-column slab) task.  Warp w quantizes
 // rows 4w .. 4w+3 of the chunk, two rows at a time: lane l takes the 16-element
@@ -99,9 +93,17 @@ template <bool kScores>
 __global__ void __launch_bounds__(256) quantize_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
     const int32_t* __restrict__ row_index, const int32_t* __restrict__ goff, int G,
-    const float* __restrict__ st, uint8_t* __restrict__ codes, int64_t ldc,
-    uint8_t* __restrict__ scales, int layout, float* __restrict__ partials) {
+    const float* __restrict__ st, const uint32_t* __restrict__ amax_bits, float* __restrict__ st_out,
+    uint8_t* __restrict__ codes, int64_t ldc, uint8_t* __restrict__ scales, int layout,
+    float* __restrict__ partials) {
+  // tensor scales: given (st), or derived here from the groups' amax bits
+  // (then block 0 also stores them to st_out)
   __shared__ __align__(16) float sq[kScores ? kScoreChunk * 256 : 4];
+  auto scale_of = [&](int g) {
+    return amax_bits ? tensor_scale_from_amax(__uint_as_float(__ldg(amax_bits + g))) : __ldg(st + g);
+  };
+  if (amax_bits && blockIdx.x == 0)
+    for (int g = threadIdx.x; g < G; g += blockDim.x) st_out[g] = scale_of(g);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t end = goff ? (int64_t)goff[G] : rows;
   const int nslab = (cols + 255) >> 8;
@@ -141,6 +143,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(
     const int64_t r0 = chunk * kScoreChunk;
     const int64_t r1 = min(r0 + kScoreChunk, end);
     const int g0 = goff ? group_of(goff, G, r0) : 0;   // same for the whole block
+    const float s_t0 = scale_of(g0);
 #pragma unroll
     for (int it = 0; it < 2; ++it) {
       const int64_t row = r0 + 4 * warp + 2 * it + (lane >> 4);
@@ -151,7 +154,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(
       float f[16];
       BlockScale bs;
       uint2 c;
-      quantize_block16(raw[it][0], raw[it][1], valid ? st[g] : 1.0f, f, bs, c);
+      quantize_block16(raw[it][0], raw[it][1], !valid ? 1.0f : g == g0 ? s_t0 : scale_of(g), f, bs,
+                       c);
       if (valid) {
         uint32_t* pc = reinterpret_cast<uint32_t*>(codes + row * ldc + (col >> 1));
         pc[0] = c.x;
@@ -559,20 +563,17 @@ extern "C" quads_status_t quads_quantize_nvfp4(
   if (rows == 0) return QUADS_OK;
   cudaStream_t st = (cudaStream_t)stream;
   const float* stp = tensor_scale_in;
+  const uint32_t* amax_bits = nullptr;   // set: the quantize kernel derives the tensor scales
   int launched = 1;
   if (tensor_amax_in) {
-    tensor_scale_kernel<<<(G + 255) / 256, 256, 0, st>>>((const uint32_t*)tensor_amax_in, G,
-                                                          tensor_scale_out);
-    stp = tensor_scale_out;
-    launched = 2;
+    amax_bits = (const uint32_t*)tensor_amax_in;
   } else if (!tensor_scale_in) {
-    launched = 3;
+    launched = 2;
     uint32_t* amax = (uint32_t*)workspace;
     cudaMemsetAsync(amax, 0, (size_t)G * 4, st);
     amax_kernel<<<grid_for((rows + 31) / 32, 1, 16), 256, 0, st>>>(
         (const __nv_bfloat16*)x, rows, (int)cols, ldx, row_index, group_offsets, G, amax);
-    tensor_scale_kernel<<<(G + 255) / 256, 256, 0, st>>>(amax, G, tensor_scale_out);
-    stp = tensor_scale_out;
+    amax_bits = amax;
   } else if (tensor_scale_in != tensor_scale_out) {
     cudaMemcpyAsync(tensor_scale_out, tensor_scale_in, (size_t)G * 4, cudaMemcpyDeviceToDevice, st);
   }
@@ -586,11 +587,13 @@ extern "C" quads_status_t quads_quantize_nvfp4(
   const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(ntasks, (int64_t)num_sms() * 16));
   if (score_partials)
     quantize_kernel<true><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)x, rows, (int)cols, ldx,
-                                                  row_index, group_offsets, G, stp, codes,
+                                                  row_index, group_offsets, G, stp, amax_bits,
+                                                  tensor_scale_out, codes,
                                                   ld_codes, scales, scale_layout, score_partials);
   else
     quantize_kernel<false><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)x, rows, (int)cols, ldx,
-                                                   row_index, group_offsets, G, stp, codes,
+                                                   row_index, group_offsets, G, stp, amax_bits,
+                                                   tensor_scale_out, codes,
                                                    ld_codes, scales, scale_layout, nullptr);
   return check_launch("quantize", launched);
 }
