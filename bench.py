@@ -273,6 +273,17 @@ def timed(torch, fn, steps, flush, stream):
     return tot
 
 
+def max_over_ranks(dist, values, device="cuda"):
+    """Element-wise max of per-rank timings (the slowest rank sets the job
+    time).  `dist` is torch.distributed (initialised) or None for one process."""
+    if dist is None:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def run_gpu(args):
     import torch
     from nvfp4_w4a4_quantized_quant_gb300 import quads as Q
@@ -358,10 +369,7 @@ def run_gpu(args):
 
     ms = t_ms / args.steps
     e_ms = e2e_ms / args.steps
-    if dist:
-        t = torch.tensor([ms, e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e_ms = t.tolist()
+    ms, e_ms = max_over_ranks(dist, [ms, e_ms])
     if rank != 0:
         return
     if sec:
