@@ -657,29 +657,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // g (rows g*N .. g*N+N-1), codes_t[g][c][n/2] holds the codes of rows n, n+1 at
 // column c (n even -> low nibble) and scales_t[g][c/16][n] the block scale, so
 // the k selected columns are read as k contiguous runs.
+// One CTA per (group, 128-row block, 64-column group): the block's codes
+// (128 rows x 32 bytes) are staged in shared memory and written back as 64
+// columns x 64 bytes; the block's one scale atom (128 rows x 4 scale columns,
+// 512 contiguous bytes) becomes 4 scale rows of 128 bytes.  Every global
+// access is a coalesced run.
 __global__ void __launch_bounds__(256) wtrans_kernel(const uint8_t* __restrict__ wc,
                                                      const uint8_t* __restrict__ wsf, int G, int N,
                                                      int K, uint8_t* __restrict__ ct,
                                                      uint8_t* __restrict__ st) {
-  const int64_t nbytes = (int64_t)G * K * (N / 2);
-  const int64_t nsc = (int64_t)G * (K / 16) * N;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nbytes + nsc;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    if (i < nbytes) {
-      const int64_t np = i % (N / 2);
-      const int64_t c = (i / (N / 2)) % K;
-      const int64_t g = i / ((int64_t)(N / 2) * K);
-      const int64_t r0 = g * N + 2 * np;
-      const uint32_t b0 = wc[r0 * (K / 2) + c / 2], b1 = wc[(r0 + 1) * (K / 2) + c / 2];
-      const uint32_t sh = (c & 1) * 4;
-      ct[i] = (uint8_t)(((b0 >> sh) & 15u) | (((b1 >> sh) & 15u) << 4));
-    } else {
-      const int64_t j = i - nbytes;
-      const int64_t n = j % N;
-      const int64_t cb = (j / N) % (K / 16);
-      const int64_t g = j / ((int64_t)N * (K / 16));
-      st[j] = wsf[sf_tc_offset(g * N + n, cb, K / 16)];
+  __shared__ __align__(16) uint8_t tile[128][32];
+  const int ncg = K / 64, nrb = N / 128;
+  const int64_t id = blockIdx.x;
+  const int cg = (int)(id % ncg);
+  const int rb = (int)((id / ncg) % nrb);
+  const int g = (int)(id / ((int64_t)ncg * nrb));
+  const int t = threadIdx.x;
+  const int64_t row0 = (int64_t)g * N + (int64_t)rb * 128;   // first weight row of the block
+  {
+    const int r = t >> 1, h = t & 1;
+    reinterpret_cast<uint4*>(tile[r])[h] =
+        __ldg(reinterpret_cast<const uint4*>(wc + (row0 + r) * (K / 2) + cg * 32) + h);
+  }
+  __syncthreads();
+  {
+    const int cc = t >> 2, part = t & 3;           // column cg*64 + cc, row pairs part*16 ..
+    const uint32_t sh = (cc & 1) * 4;
+    uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int np = part * 16 + i;
+      const uint32_t lo = (tile[2 * np][cc >> 1] >> sh) & 15u;
+      const uint32_t hi = (tile[2 * np + 1][cc >> 1] >> sh) & 15u;
+      w[i >> 2] |= (lo | (hi << 4)) << (8 * (i & 3));
     }
+    uint8_t* dst = ct + (int64_t)g * K * (N / 2) + (int64_t)(cg * 64 + cc) * (N / 2) + rb * 64 + part * 16;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  if (t < 128) {
+    const uint8_t* atom = wsf + ((row0 / 128) * (K / 64) + cg) * 512;
+    const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(atom + (t & 31) * 16 + ((t >> 5) & 3) * 4));
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      st[((int64_t)g * (K / 16) + cg * 4 + j) * N + rb * 128 + t] = (uint8_t)(v >> (8 * j));
   }
 }
 
@@ -964,9 +984,10 @@ extern "C" quads_status_t quads_weight_columns(const uint8_t* w_codes, const uin
     return fail(QUADS_ERR_INVALID_ARG, "weight_columns: null pointer argument");
   if (num_groups < 1 || rows_per_group <= 0 || rows_per_group % 128 || cols <= 0 || cols % 64)
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "weight_columns: rows_per_group %% 128 and cols %% 64");
-  const int64_t total = (int64_t)num_groups * cols * (rows_per_group / 2 + rows_per_group / 16);
-  const int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)num_sms() * 32);
-  gemm::wtrans_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(
+  const int64_t blocks = (int64_t)num_groups * (rows_per_group / 128) * (cols / 64);
+  if (blocks >= ((int64_t)1 << 31))
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "weight_columns: too many 128x64 blocks");
+  gemm::wtrans_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
       w_codes, w_scales, num_groups, (int)rows_per_group, (int)cols, codes_t, scales_t);
   return check_launch("weight_columns", 1);
 }
