@@ -20,8 +20,11 @@ namespace quads {
 static __device__ int g_quant_error;  // device-side argument check failures
 
 // ---------------------------------------------------------------- amax
-// One block per 32-row chunk (inside one group), threads over (row, 8-col
-// vector), eight 16-byte loads in flight per thread.
+// One block per 8-row slice (inside one group), threads over (row, 8-col
+// vector), eight 16-byte loads in flight per thread; the absolute maximum is
+// taken on packed bf16 pairs (exact: the maximum of bf16 values is one of
+// them) and converted to float once per thread.
+constexpr int kAmaxRows = 8;
 __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restrict__ x,
                                                    int64_t rows, int cols, int64_t ldx,
                                                    const int32_t* __restrict__ row_index,
@@ -29,14 +32,14 @@ __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restri
                                                    uint32_t* __restrict__ amax_bits) {
   const int64_t end = goff ? (int64_t)goff[G] : rows;
   const int vec_per_row = cols >> 3;
-  const int64_t nchunks = (end + kScoreChunk - 1) / kScoreChunk;
+  const int64_t nslices = (end + kAmaxRows - 1) / kAmaxRows;
   __shared__ float red[8];
-  for (int64_t chunk = blockIdx.x; chunk < nchunks; chunk += gridDim.x) {
-    const int64_t r0 = chunk * kScoreChunk;
-    const int64_t r1 = min(r0 + kScoreChunk, end);
+  for (int64_t slice = blockIdx.x; slice < nslices; slice += gridDim.x) {
+    const int64_t r0 = slice * kAmaxRows;
+    const int64_t r1 = min(r0 + kAmaxRows, end);
     const int g = goff ? group_of(goff, G, r0) : 0;
     if (goff && r1 > goff[g + 1]) atomicExch(&g_quant_error, QUADS_ERR_DEVICE_CHECK);
-    float m = 0.0f;
+    __nv_bfloat162 m2 = __floats2bfloat162_rn(0.0f, 0.0f);
     const int total = (int)(r1 - r0) * vec_per_row;
     for (int i0 = threadIdx.x; i0 < total; i0 += 8 * blockDim.x) {
       uint4 u[8];
@@ -45,19 +48,21 @@ __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restri
         const int i = i0 + q * blockDim.x;
         u[q] = make_uint4(0, 0, 0, 0);
         if (i < total) {
-          const int64_t r = r0 + i / vec_per_row;
-          const int64_t src = row_index ? (int64_t)row_index[r] : r;
-          u[q] = __ldg(reinterpret_cast<const uint4*>(x + src * ldx) + (i % vec_per_row));
+          const int rr = i / vec_per_row;
+          const int64_t src = row_index ? (int64_t)row_index[r0 + rr] : r0 + rr;
+          u[q] = __ldg(reinterpret_cast<const uint4*>(x + src * ldx) + (i - rr * vec_per_row));
         }
       }
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        float f[8];
-        bf16x8_to_f32(u[q], f);
+        const uint32_t w[4] = {u[q].x, u[q].y, u[q].z, u[q].w};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
+        for (int j = 0; j < 4; ++j)
+          m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[j])));
       }
     }
+    const float2 mf = __bfloat1622float2(m2);
+    float m = fmaxf(mf.x, mf.y);
     m = warp_max(m);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
     __syncthreads();
@@ -172,8 +177,9 @@ __global__ void __launch_bounds__(256) quantize_kernel(
           float v[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
+            // rows past the end were loaded as zeros: their codes and R are 0
             const float R = __fsub_rn(f[4 * q + j], __fmul_rn(lv[4 * q + j], bs.d));
-            v[j] = valid ? __fmul_rn(R, R) : 0.0f;
+            v[j] = __fmul_rn(R, R);
           }
           ps[q] = make_float4(v[0], v[1], v[2], v[3]);
         }
@@ -571,7 +577,7 @@ extern "C" quads_status_t quads_quantize_nvfp4(
     launched = 2;
     uint32_t* amax = (uint32_t*)workspace;
     cudaMemsetAsync(amax, 0, (size_t)G * 4, st);
-    amax_kernel<<<grid_for((rows + 31) / 32, 1, 16), 256, 0, st>>>(
+    amax_kernel<<<grid_for((rows + kAmaxRows - 1) / kAmaxRows, 1, 8), 256, 0, st>>>(
         (const __nv_bfloat16*)x, rows, (int)cols, ldx, row_index, group_offsets, G, amax);
     amax_bits = amax;
   } else if (tensor_scale_in != tensor_scale_out) {
