@@ -207,7 +207,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(
 //    slice of up to 256 chunks is staged in shared memory by all warps
 //    (coalesced reads, 8 in flight per thread), then lane l of warp 0 adds
 //    channel l's chunks in order;
-//  * short groups: one thread per (group, channel) loops over the chunks.
+//  * short groups: inside the top-k kernel, one thread per (group, channel)
+//    loops over the chunks.
 __global__ void __launch_bounds__(256) score_chain_kernel(const float* __restrict__ partials,
                                                           int cols,
                                                           const int32_t* __restrict__ goff,
@@ -243,47 +244,55 @@ __global__ void __launch_bounds__(256) score_chain_kernel(const float* __restric
   if (warp == 0 && c < cols) scores[(int64_t)g * cols + c] = t;
 }
 
-__global__ void __launch_bounds__(256) score_loop_kernel(const float* __restrict__ partials,
-                                                         int cols,
-                                                         const int32_t* __restrict__ goff,
-                                                         int64_t rows,
-                                                         float* __restrict__ scores) {
-  const int g = blockIdx.y;
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= cols) return;
-  const int64_t a = goff ? (int64_t)goff[g] : 0;
-  const int64_t b = goff ? (int64_t)goff[g + 1] : rows;
-  const int64_t c0 = a / kScoreChunk, c1 = (b + kScoreChunk - 1) / kScoreChunk;
-  float t = 0.0f;
-  for (int64_t ch = c0; ch < c1; ch += 8) {
-    float v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = ch + i < c1 ? partials[(ch + i) * cols + c] : 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (ch + i < c1) t = __fadd_rn(t, v[i]);
-  }
-  scores[(int64_t)g * cols + c] = t;
-}
 
 // Top-k per group by radix selection on the score bit patterns (scores are
 // >= 0, so the unsigned order of the bits is the float order): find the k-th
 // largest key T byte by byte, take every channel with key > T and the
 // lowest-index channels with key == T, and write them in ascending order.
-__global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ scores, int cols,
-                                                    int k, int32_t* __restrict__ sel) {
+// With `partials` (short groups) the block first forms its group's scores
+// itself -- the chunk partials added in ascending chunk order from 0 -- and
+// stores them to `scores`; otherwise it reads the scores score_chain_kernel
+// left there.
+__global__ void __launch_bounds__(1024) topk_kernel(float* __restrict__ scores, int cols,
+                                                    int k, int32_t* __restrict__ sel,
+                                                    const float* __restrict__ partials,
+                                                    const int32_t* __restrict__ goff,
+                                                    int64_t rows) {
   __shared__ int hist[256];
   __shared__ uint32_t s_prefix;
   __shared__ int s_need;
   __shared__ int warp_sums[32];
   const int g = blockIdx.y;
-  const float* sc = scores + (int64_t)g * cols;
+  float* sc = scores + (int64_t)g * cols;
   constexpr int PER = 8;  // cols <= 8192 = 1024 threads x 8
   uint32_t key[PER];
+  if (partials) {
+    const int64_t a = goff ? (int64_t)goff[g] : 0;
+    const int64_t b = goff ? (int64_t)goff[g + 1] : rows;
+    const int64_t c0 = a / kScoreChunk, c1 = (b + kScoreChunk - 1) / kScoreChunk;
 #pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int c = threadIdx.x + i * blockDim.x;
-    key[i] = c < cols ? __float_as_uint(sc[c]) : 0u;
+    for (int i = 0; i < PER; ++i) {
+      const int c = threadIdx.x + i * blockDim.x;
+      float t = 0.0f;
+      if (c < cols) {
+        for (int64_t ch = c0; ch < c1; ch += 8) {
+          float v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v[u] = ch + u < c1 ? __ldg(partials + (ch + u) * cols + c) : 0.0f;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (ch + u < c1) t = __fadd_rn(t, v[u]);
+        }
+        sc[c] = t;
+      }
+      key[i] = c < cols ? __float_as_uint(t) : 0u;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int c = threadIdx.x + i * blockDim.x;
+      key[i] = c < cols ? __float_as_uint(sc[c]) : 0u;
+    }
   }
   if (threadIdx.x == 0) { s_prefix = 0u; s_need = k; }
   uint32_t mask_hi = 0u;  // bits already fixed in s_prefix
@@ -629,15 +638,16 @@ extern "C" quads_status_t quads_select_residual_channels(
   uint32_t* amax = (uint32_t*)((char*)workspace + rs_bytes);
   float* scores = scores_out ? scores_out
                              : (float*)((char*)workspace + rs_bytes + (((size_t)G * 4 + 255) & ~(size_t)255));
-  // chunks per group on average decides the launch shape (both give the same sums)
+  // chunks per group on average decides the launch shape (both give the same
+  // sums); for short groups the top-k block also forms the scores
   const int64_t chunks_per_group = (rows + 31) / 32 / G;
-  if (chunks_per_group > 64)
+  const bool long_groups = chunks_per_group > 64;
+  if (long_groups)
     score_chain_kernel<<<dim3((unsigned)((cols + 31) / 32), (unsigned)G), 256, 0, st>>>(
         score_partials, (int)cols, group_offsets, rows, scores);
-  else
-    score_loop_kernel<<<dim3((unsigned)((cols + 255) / 256), (unsigned)G), 256, 0, st>>>(
-        score_partials, (int)cols, group_offsets, rows, scores);
-  topk_kernel<<<dim3(1, (unsigned)G), 1024, 0, st>>>(scores, (int)cols, k, sel);
+  topk_kernel<<<dim3(1, (unsigned)G), 1024, 0, st>>>(scores, (int)cols, k, sel,
+                                                     long_groups ? nullptr : score_partials,
+                                                     group_offsets, rows);
   cudaMemsetAsync(amax, 0, (size_t)G * 4, st);
   rsel_residual_kernel<<<grid_for((rows + 31) / 32, 1, 16), 256, 0, st>>>(
       (const __nv_bfloat16*)x, rows, (int)cols, ldx, group_offsets, G, scales, scale_layout,
@@ -648,7 +658,7 @@ extern "C" quads_status_t quads_select_residual_channels(
   }
   rsel_quantize_kernel<<<grid_for(rows * (kpad / 8), 256), 256, 0, st>>>(
       rs, rows, k, kpad, group_offsets, G, amax, r_codes, r_scales, r_scale_layout, r_tensor_scale);
-  return check_launch("select", 4);
+  return check_launch("select", long_groups ? 4 : 3);
 }
 
 extern "C" quads_status_t quads_trace_round(const void* x_train, int64_t rows, int64_t cols,
