@@ -345,8 +345,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES);
   uint64_t* full = bars;                 // [STAGES]
   uint64_t* empty = bars + STAGES;       // [STAGES]
-  uint64_t* sf_free = bars + 2 * STAGES; // [SF_BUFS]
-  uint64_t* sf_ready = sf_free + SF_BUFS; // [SF_BUFS]
+  uint64_t* sf_ready = bars + 2 * STAGES; // [SF_BUFS]
   uint64_t* acc_full = sf_ready + SF_BUFS; // [2]
   uint64_t* acc_empty = acc_full + 2;    // [2]
   uint32_t* tmem_holder = (uint32_t*)(acc_empty + 2);
@@ -372,7 +371,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) { mbar_init(&full[i], COPIES); mbar_init(&empty[i], 1); }
-    for (int i = 0; i < SF_BUFS; ++i) { mbar_init(&sf_free[i], 1); mbar_init(&sf_ready[i], SF_WARPS); }
+    for (int i = 0; i < SF_BUFS; ++i) mbar_init(&sf_ready[i], SF_WARPS);
     for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], EPI_THREADS); }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -487,8 +486,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_mma_el(dcol, desc_sw128(sa + off), desc_sw128(sbb + off), idesc, tsf + q * 4,
                     tsf + 4 * KSTEPS + q * 4, (kk > 0 || q > 0) ? 1u : 0u);
         }
-        tc_commit_el(&empty[s]);
-        tc_commit_el(&sf_free[sb]);
+        tc_commit_el(&empty[s]);   // also frees this stage's scale buffer
         if (++s == STAGES) s = 0;
         if (++sb == SF_BUFS) { sb = 0; sph ^= 1; }
       }
@@ -503,13 +501,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // four scales at lane r % 32, column r / 32).  Warp w copies the atoms of
     // K steps 2w and 2w+1.  The warps wait for the stage's TMA data, so
     // sf_ready alone tells the MMA warp that the stage is complete.
+    // Scale buffer sb was last read by the MMAs of ring iteration it - SF_BUFS,
+    // whose completion the MMA warp signals on that stage's empty barrier.
     const int w = warp - SF_WARP0;
-    uint32_t s = 0, ph = 0, sb = 0, sph = 0;
+    uint32_t s = 0, ph = 0, sb = 0, it = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-      for (int kt = 0; kt < KT + KTc; ++kt) {
-        if (!conv_wait_bar(&full[s], ph, abort_flag, p.err) ||
-            !conv_wait_bar(&sf_free[sb], sph ^ 1, abort_flag, p.err)) {
+      for (int kt = 0; kt < KT + KTc; ++kt, ++it) {
+        bool okw = conv_wait_bar(&full[s], ph, abort_flag, p.err);
+        if (okw && it >= (uint32_t)SF_BUFS) {
+          const uint32_t prev = it - SF_BUFS;
+          okw = conv_wait_bar(&empty[prev % STAGES], (prev / STAGES) & 1, abort_flag, p.err);
+        }
+        if (!okw) {
           ok = false;
           break;
         }
@@ -530,7 +534,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_commit_el(&sf_ready[sb]);
         if (++s == STAGES) { s = 0; ph ^= 1; }
-        if (++sb == SF_BUFS) { sb = 0; sph ^= 1; }
+        if (++sb == SF_BUFS) sb = 0;
       }
     }
   } else if (warp >= EPI_WARP0) {
