@@ -109,16 +109,25 @@ class MoEExpertLayer:
             s2=e(Q.workspace_size(Q.OP_SELECT, cap, F, 0, k2, E)),
             g2=e(Q.workspace_size(Q.OP_MOE_GEMM, 0, F, H, k2, E)),
         )
+        # routing does not depend on X's quantization: it runs on a side stream
+        # (joined before the gathers), also inside a captured graph
+        self.side = torch.cuda.Stream(device=dev)
+        self.ev_fork, self.ev_plan = torch.cuda.Event(), torch.cuda.Event()
 
     def forward(self, x: torch.Tensor, logits: torch.Tensor, stream=None) -> dict:
         b, ws, T = self.b, self.ws, x.shape[0]
         assert T == self.max_tokens, "buffers are sized for a fixed token count"
         E, H, F = self.E, self.H, self.F
         comp = self.compensate
+        main = torch.cuda.current_stream() if stream is None else stream
+        self.ev_fork.record(main)
+        self.side.wait_event(self.ev_fork)
         plan = Q.moe_route(logits, self.topk, rows_capacity=self.cap, out=b["route"],
-                           workspace=ws["rt"], stream=stream)
+                           workspace=ws["rt"], stream=self.side)
+        self.ev_plan.record(self.side)
         xq, xpart = Q.quantize_nvfp4(x, scores=comp, workspace=ws["q1"], stream=stream,
                                      out=(b["xc"], b["xs"], b["xts"], b["xpart"] if comp else None))
+        main.wait_event(self.ev_plan)
         a1 = Q.moe_gather(plan, xq, out=(b["a1c"], b["a1s"]), stream=stream)
         r1 = sel1 = None
         if comp:
