@@ -339,7 +339,7 @@ def run_gpu(args):
         def g1():
             Q.moe_grouped_gemm(dict(plan, rows_capacity=layer.cap, experts=layer.E), layer._a1,
                                layer.w1q, layer.E, 2 * layer.F, layer._r1, layer.b["sel1"],
-                               layer.k1, epilogue=Q.EPI_SWIGLU, workspace=layer.ws["g1"],
+                               layer.k1, epilogue=Q.EPI_SWIGLU, w_sel=layer._w1sel,
                                out=layer.b["h"], stream=stream)
         # captured in a graph so that host-side launch work stays out of the timing
         g1_graph = torch.cuda.CUDAGraph()

@@ -183,6 +183,12 @@ quads_status_t quads_quantize_nvfp4(const void* x, int64_t rows, int64_t cols, i
  *                  columns, padding blocks 0.
  *   r_tensor_scale device float [num_groups].
  *   workspace      >= quads_workspace_size(QUADS_OP_SELECT, rows, cols, 0, k, num_groups).
+ *   sel_ready_event nullable cudaEvent_t (caller-owned, created): recorded on
+ *                  `stream` as soon as sel is written, before the residual
+ *                  slice is formed, so that work on another stream needing only
+ *                  sel (quads_select_weight_channels) can wait on it and
+ *                  overlap the rest of this call.  A failed record returns
+ *                  QUADS_ERR_CUDA.
  * Requires cols <= 8192.
  */
 quads_status_t quads_select_residual_channels(
@@ -190,7 +196,7 @@ quads_status_t quads_select_residual_channels(
     int32_t num_groups, const uint8_t* scales, int32_t scale_layout, const float* tensor_scale,
     const float* score_partials, int32_t k, int32_t* sel, float* scores_out, uint8_t* r_codes,
     uint8_t* r_scales, int32_t r_scale_layout, float* r_tensor_scale, void* workspace,
-    size_t workspace_bytes, void* stream);
+    size_t workspace_bytes, void* sel_ready_event, void* stream);
 
 /*
  * quads_select_residual_channels_noalloc -- the same computation and outputs as
@@ -214,7 +220,8 @@ quads_status_t quads_select_residual_channels(
  *     call's contents (the parts that must start at zero are cleared by each
  *     call).  Calls that overlap on the GPU -- on different streams, or from
  *     different host threads without ordering -- race on it.
- * Arguments are those of quads_select_residual_channels without the workspace.
+ * Arguments are those of quads_select_residual_channels without the workspace
+ * and the sel_ready_event.
  */
 #define QUADS_NOALLOC_SELECT_SCRATCH_BYTES (32u << 20)
 quads_status_t quads_select_residual_channels_noalloc(
@@ -228,14 +235,19 @@ quads_status_t quads_select_residual_channels_noalloc(
  * in one kernel on the tcgen05 block-scaled tensor cores (two TMEM
  * accumulators summed in the epilogue).  [QUADS] 2.2 B "Mechanism" (correction
  * added back to the quantized output) and section 1 (native W4A4 GEMM).
- * Q(W_sel) is built inside the call (into `workspace`) from the column-major
- * copy of the packed weight (quads_weight_columns): the selected columns of
- * DQ(Q(W)) in units of s_w, requantized in 16-blocks along the selection with
- * s_w kept.
+ * Q(W_sel) is either given (w_sel_codes / w_sel_scales, from
+ * quads_select_weight_channels, e.g. made on another stream while R_sel is
+ * being formed) or built inside the call (into `workspace`) from the
+ * column-major copy of the packed weight (quads_weight_columns): the selected
+ * columns of DQ(Q(W)) in units of s_w, requantized in 16-blocks along the
+ * selection with s_w kept.
  *
  *   A: a_codes [M, K/2], a_scales TCGEN05 (ceil(M/128)*128 rows), a_tensor_scale device [1].
  *   W: w_codes [N, K/2], w_scales TCGEN05, w_tensor_scale device [1];
- *   w_codes_t / w_scales_t: its column-major copy (required with compensation).
+ *   w_codes_t / w_scales_t: its column-major copy (needed with compensation
+ *   unless Q(W_sel) is given; then not read, nor is the workspace).
+ *   w_sel_codes [N, kpad/2] / w_sel_scales TCGEN05 over kpad columns: both or
+ *   neither (nullable), 16-byte aligned.
  *   r_codes NULL -> plain W4A4 (sel, r_* ignored); else r_codes [M, kpad/2],
  *   r_scales TCGEN05 over kpad columns, r_tensor_scale [1], sel [k] ascending.
  *   y [M, ldy] float32 or bf16 (y_dtype).
@@ -245,7 +257,8 @@ quads_status_t quads_w4a4_gemm_comp(int64_t M, int64_t N, int64_t K, const uint8
                                     const uint8_t* a_scales, const float* a_tensor_scale,
                                     const uint8_t* w_codes, const uint8_t* w_scales,
                                     const float* w_tensor_scale, const uint8_t* w_codes_t,
-                                    const uint8_t* w_scales_t, const uint8_t* r_codes,
+                                    const uint8_t* w_scales_t, const uint8_t* w_sel_codes,
+                                    const uint8_t* w_sel_scales, const uint8_t* r_codes,
                                     const uint8_t* r_scales, const float* r_tensor_scale,
                                     const int32_t* sel, int32_t k, void* y, int32_t y_dtype,
                                     int64_t ldy, void* workspace, size_t workspace_bytes,
@@ -262,7 +275,10 @@ quads_status_t quads_w4a4_gemm_comp(int64_t M, int64_t N, int64_t K, const uint8
  *     [num_experts] (a_scale_per_expert).
  *   w_codes [num_experts * N, K/2] (expert e's rows e*N..), w_scales TCGEN05 over
  *     the same num_experts*N rows, w_tensor_scale [num_experts]; w_codes_t /
- *     w_scales_t its column-major copy per expert (required with compensation).
+ *     w_scales_t its column-major copy per expert (needed with compensation
+ *     unless w_sel_codes / w_sel_scales [num_experts*N rows over kpad columns,
+ *     as quads_select_weight_channels writes them] are given, as in
+ *     quads_w4a4_gemm_comp).
  *   r_codes NULL -> plain; else [rows_capacity, kpad/2] + TCGEN05 scales,
  *     r_tensor_scale [1] or [num_experts] (r_scale_per_expert); sel [k] shared
  *     (sel_per_expert = 0) or [num_experts, k].
@@ -280,8 +296,9 @@ quads_status_t quads_moe_grouped_gemm(
     const int32_t* expert_offsets, const int32_t* expert_counts, const uint8_t* a_codes,
     const uint8_t* a_scales, const float* a_tensor_scale, int32_t a_scale_per_expert,
     const uint8_t* w_codes, const uint8_t* w_scales, const float* w_tensor_scale,
-    const uint8_t* w_codes_t, const uint8_t* w_scales_t, const uint8_t* r_codes,
-    const uint8_t* r_scales, const float* r_tensor_scale, int32_t r_scale_per_expert,
+    const uint8_t* w_codes_t, const uint8_t* w_scales_t, const uint8_t* w_sel_codes,
+    const uint8_t* w_sel_scales, const uint8_t* r_codes, const uint8_t* r_scales,
+    const float* r_tensor_scale, int32_t r_scale_per_expert,
     const int32_t* sel, int32_t sel_per_expert, int32_t k, int32_t epilogue, void* y,
     int32_t y_dtype, int64_t ldy, float* y_amax, void* workspace, size_t workspace_bytes,
     void* stream);
@@ -300,6 +317,35 @@ quads_status_t quads_moe_grouped_gemm(
 quads_status_t quads_weight_columns(const uint8_t* w_codes, const uint8_t* w_scales,
                                     int32_t num_groups, int64_t rows_per_group, int64_t cols,
                                     uint8_t* codes_t, uint8_t* scales_t, void* stream);
+
+/*
+ * quads_select_weight_channels -- Q(W_sel), the weight side of the correction
+ * term ([QUADS] 2.2 B "Mechanism": the selected input channels of the weight,
+ * paired with R_sel).  For each of num_groups stacked matrices of
+ * rows_per_group rows and each weight row: the selected columns of DQ(Q(W)),
+ * exact in units of the group's tensor scale s_w (E2M1 level x E4M3 block
+ * scale), requantized in 16-blocks along the selection with tensor scale 1 --
+ * the group's s_w is applied by the GEMM.  The same operand the GEMMs build
+ * when no Q(W_sel) is given to them; made by its own call so that it can run
+ * on another stream while R_sel is formed.
+ *
+ *   codes_t / scales_t: the column-major copy from quads_weight_columns
+ *     (16-byte aligned).
+ *   sel [k] shared by every group (sel_per_group = 0) or [num_groups, k];
+ *     entries are column indices in [0, cols) (ascending, as
+ *     quads_select_residual_channels writes them).
+ *   w_sel_codes [num_groups*rows_per_group, kpad/2] (16-byte aligned),
+ *   w_sel_scales TCGEN05 over kpad columns, kpad = quads_kpad(k); columns
+ *     k..kpad-1 get zero codes and scales.  Caller-owned.
+ * rows_per_group % 128 == 0, cols % 64 == 0, 16 <= k <= cols, k % 16 == 0,
+ * num_groups <= 65535.
+ */
+quads_status_t quads_select_weight_channels(int32_t num_groups, int64_t rows_per_group,
+                                            int64_t cols, const uint8_t* codes_t,
+                                            const uint8_t* scales_t, const int32_t* sel,
+                                            int32_t sel_per_group, int32_t k,
+                                            uint8_t* w_sel_codes, uint8_t* w_sel_scales,
+                                            void* stream);
 
 /*
  * quads_trace_round -- TRACE rollout-guided rounding ([TRACE] "核心方法", Eq. (3)):

@@ -807,6 +807,7 @@ struct Launch {
   const int32_t* row_off;
   const int32_t* row_cnt;
   const uint8_t *a, *a_sf, *b, *b_sf, *b_t, *b_sf_t, *r, *r_sf;
+  const uint8_t *wsel, *wsel_sf;   // prebuilt Q(W_sel), or null: built into ws
   const float *a_ts, *b_ts, *r_ts;
   int a_pe, r_pe;
   const int32_t* sel;
@@ -820,26 +821,37 @@ struct Launch {
   cudaStream_t stream;
 };
 
+// Q(W_sel) of E groups of N rows: codes [E*N, kpad/2], TCGEN05 scales.
+static void launch_wsel(const uint8_t* b_t, const uint8_t* b_sf_t, int E, int N, int K,
+                        const int32_t* sel, int sel_pe, int k, int kpad, uint8_t* codes,
+                        uint8_t* sf, cudaStream_t stream) {
+  // row chunks of 512 (or 128) rows: N is a multiple of 128
+  const int NC = N % 512 == 0 ? 512 : 128;
+  const size_t cols_smem = (size_t)24 * NC;   // 16 columns x (NC/2 code + NC scale bytes)
+  wsel_cols_kernel<<<dim3((unsigned)(kpad / 16), (unsigned)E, (unsigned)(N / NC)), 256, cols_smem,
+                     stream>>>(b_t, b_sf_t, N, K, NC, sel, sel_pe, k, kpad, codes, sf);
+}
+
 static quads_status_t launch(const Launch& L) {
   const bool comp = L.r != nullptr;
   const int64_t brows = (int64_t)L.E * L.N;
-  uint8_t* ws_codes = nullptr;
-  uint8_t* ws_sf = nullptr;
-  if (comp) {
+  const uint8_t* ws_codes = nullptr;
+  const uint8_t* ws_sf = nullptr;
+  int launches = comp ? 2 : 1;
+  if (comp && L.wsel) {
+    ws_codes = L.wsel;
+    ws_sf = L.wsel_sf;
+    launches = 1;
+  } else if (comp) {
     const size_t need = quads_workspace_size(L.row_off ? QUADS_OP_MOE_GEMM : QUADS_OP_GEMM, 0,
                                              L.K, L.N, L.k, L.E);
     if (!L.ws || L.ws_bytes < need)
       return fail(QUADS_ERR_WORKSPACE, "gemm: workspace needs %zu bytes", need);
-    ws_codes = (uint8_t*)L.ws;
-    ws_sf = ws_codes + (((size_t)brows * (L.kpad / 2) + 1023) & ~(size_t)1023);
-    // row chunks of 512 (or 128) rows: N is a multiple of 128
-    const int NC = L.N % 512 == 0 ? 512 : 128;
-    {
-      const size_t cols_smem = (size_t)24 * NC;   // 16 columns x (NC/2 code + NC scale bytes)
-      wsel_cols_kernel<<<dim3((unsigned)(L.kpad / 16), (unsigned)L.E, (unsigned)(L.N / NC)), 256,
-                         cols_smem, L.stream>>>(L.b_t, L.b_sf_t, L.N, L.K, NC, L.sel, L.sel_pe,
-                                                L.k, L.kpad, ws_codes, ws_sf);
-    }
+    uint8_t* c = (uint8_t*)L.ws;
+    uint8_t* f = c + (((size_t)brows * (L.kpad / 2) + 1023) & ~(size_t)1023);
+    launch_wsel(L.b_t, L.b_sf_t, L.E, L.N, L.K, L.sel, L.sel_pe, L.k, L.kpad, c, f, L.stream);
+    ws_codes = c;
+    ws_sf = f;
   }
   CUtensorMap tA, tB, tR, tW;
   const int64_t arows = L.row_off ? L.rows_cap : L.M;
@@ -874,7 +886,7 @@ static quads_status_t launch(const Launch& L) {
   int64_t grid = num_sms();
   if (!L.row_off) grid = std::min<int64_t>(grid, ((L.M + BM - 1) / BM) * (L.N / BN));
   gemm_kernel<<<(int)grid, NUM_THREADS, SMEM_BYTES, L.stream>>>(tA, tB, tR, tW, p);
-  return check_launch("gemm", comp ? 2 : 1);
+  return check_launch("gemm", launches);
 }
 
 }  // namespace gemm
@@ -893,11 +905,32 @@ using namespace quads;
 
 static bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Compensation operands: R_sel and sel, and either a prebuilt Q(W_sel) or the
+// column-major weight copy it is built from.
+static quads_status_t check_wsel_args(const char* who, const uint8_t* r_codes,
+                                      const uint8_t* r_scales, const float* r_tensor_scale,
+                                      const int32_t* sel, const uint8_t* w_codes_t,
+                                      const uint8_t* w_scales_t, const uint8_t* w_sel_codes,
+                                      const uint8_t* w_sel_scales, int32_t k, int64_t K) {
+  if (!r_codes) return QUADS_OK;
+  if (!r_scales || !r_tensor_scale || !sel || k <= 0 || k % 16 || k > K)
+    return fail(QUADS_ERR_INVALID_ARG, "%s: compensation needs r_scales, r_tensor_scale, sel and 16<=k<=K, k%%16==0", who);
+  if (!w_sel_codes != !w_sel_scales)
+    return fail(QUADS_ERR_INVALID_ARG, "%s: give both w_sel_codes and w_sel_scales, or neither", who);
+  if (w_sel_codes && (!al16(w_sel_codes) || !al16(w_sel_scales)))
+    return fail(QUADS_ERR_MISALIGNED, "%s: Q(W_sel) must be 16-byte aligned", who);
+  if (!w_sel_codes && (!w_codes_t || !w_scales_t))
+    return fail(QUADS_ERR_INVALID_ARG, "%s: without a prebuilt Q(W_sel), compensation needs the column-major weight copy", who);
+  return QUADS_OK;
+}
+
 extern "C" quads_status_t quads_w4a4_gemm_comp(int64_t M, int64_t N, int64_t K,
                                                const uint8_t* a_codes, const uint8_t* a_scales,
                                                const float* a_tensor_scale, const uint8_t* w_codes,
                                                const uint8_t* w_scales, const float* w_tensor_scale,
                                                const uint8_t* w_codes_t, const uint8_t* w_scales_t,
+                                               const uint8_t* w_sel_codes,
+                                               const uint8_t* w_sel_scales,
                                                const uint8_t* r_codes, const uint8_t* r_scales,
                                                const float* r_tensor_scale, const int32_t* sel,
                                                int32_t k, void* y, int32_t y_dtype, int64_t ldy,
@@ -916,15 +949,16 @@ extern "C" quads_status_t quads_w4a4_gemm_comp(int64_t M, int64_t N, int64_t K,
   if (!al16(a_codes) || !al16(w_codes) || !al16(a_scales) || !al16(w_scales) || !al16(y) ||
       (r_codes && (!al16(r_codes) || !al16(r_scales))))
     return fail(QUADS_ERR_MISALIGNED, "gemm: operands must be 16-byte aligned");
-  if (r_codes && (!r_scales || !r_tensor_scale || !sel || !w_codes_t || !w_scales_t || k <= 0 ||
-                  k % 16 || k > K))
-    return fail(QUADS_ERR_INVALID_ARG, "gemm: compensation needs r_scales, r_tensor_scale, sel, the column-major weight copy and 16<=k<=K, k%%16==0");
+  if (quads_status_t st = check_wsel_args("gemm", r_codes, r_scales, r_tensor_scale, sel,
+                                          w_codes_t, w_scales_t, w_sel_codes, w_sel_scales, k, K))
+    return st;
   gemm::Launch L{};
   L.M = M; L.rows_cap = M; L.E = 1; L.N = (int)N; L.K = (int)K; L.k = k;
   L.kpad = r_codes ? quads_kpad(k) : 0;
   L.row_off = nullptr; L.row_cnt = nullptr;
   L.a = a_codes; L.a_sf = a_scales; L.b = w_codes; L.b_sf = w_scales;
   L.b_t = w_codes_t; L.b_sf_t = w_scales_t;
+  L.wsel = w_sel_codes; L.wsel_sf = w_sel_scales;
   L.r = r_codes; L.r_sf = r_scales;
   L.a_ts = a_tensor_scale; L.b_ts = w_tensor_scale; L.r_ts = r_tensor_scale;
   L.a_pe = 0; L.r_pe = 0; L.sel = sel; L.sel_pe = 0;
@@ -939,9 +973,9 @@ extern "C" quads_status_t quads_moe_grouped_gemm(
     const int32_t* expert_offsets, const int32_t* expert_counts, const uint8_t* a_codes,
     const uint8_t* a_scales, const float* a_tensor_scale, int32_t a_scale_per_expert,
     const uint8_t* w_codes, const uint8_t* w_scales, const float* w_tensor_scale,
-    const uint8_t* w_codes_t, const uint8_t* w_scales_t,
-    const uint8_t* r_codes, const uint8_t* r_scales, const float* r_tensor_scale,
-    int32_t r_scale_per_expert, const int32_t* sel, int32_t sel_per_expert, int32_t k,
+    const uint8_t* w_codes_t, const uint8_t* w_scales_t, const uint8_t* w_sel_codes,
+    const uint8_t* w_sel_scales, const uint8_t* r_codes, const uint8_t* r_scales,
+    const float* r_tensor_scale, int32_t r_scale_per_expert, const int32_t* sel, int32_t sel_per_expert, int32_t k,
     int32_t epilogue, void* y, int32_t y_dtype, int64_t ldy, float* y_amax, void* workspace,
     size_t workspace_bytes, void* stream) {
   if (!expert_offsets || !a_codes || !a_scales || !a_tensor_scale || !w_codes || !w_scales ||
@@ -961,15 +995,16 @@ extern "C" quads_status_t quads_moe_grouped_gemm(
   if (!al16(a_codes) || !al16(w_codes) || !al16(a_scales) || !al16(w_scales) || !al16(y) ||
       (r_codes && (!al16(r_codes) || !al16(r_scales))))
     return fail(QUADS_ERR_MISALIGNED, "moe_gemm: operands must be 16-byte aligned");
-  if (r_codes && (!r_scales || !r_tensor_scale || !sel || !w_codes_t || !w_scales_t || k <= 0 ||
-                  k % 16 || k > K))
-    return fail(QUADS_ERR_INVALID_ARG, "moe_gemm: compensation needs r_scales, r_tensor_scale, sel, the column-major weight copy and valid k");
+  if (quads_status_t st = check_wsel_args("moe_gemm", r_codes, r_scales, r_tensor_scale, sel,
+                                          w_codes_t, w_scales_t, w_sel_codes, w_sel_scales, k, K))
+    return st;
   gemm::Launch L{};
   L.M = rows_capacity; L.rows_cap = rows_capacity; L.E = num_experts; L.N = (int)N; L.K = (int)K;
   L.k = k; L.kpad = r_codes ? quads_kpad(k) : 0;
   L.row_off = expert_offsets; L.row_cnt = expert_counts;
   L.a = a_codes; L.a_sf = a_scales; L.b = w_codes; L.b_sf = w_scales;
   L.b_t = w_codes_t; L.b_sf_t = w_scales_t;
+  L.wsel = w_sel_codes; L.wsel_sf = w_sel_scales;
   L.r = r_codes; L.r_sf = r_scales;
   L.a_ts = a_tensor_scale; L.b_ts = w_tensor_scale; L.r_ts = r_tensor_scale;
   L.a_pe = a_scale_per_expert; L.r_pe = r_scale_per_expert; L.sel = sel; L.sel_pe = sel_per_expert;
@@ -994,4 +1029,23 @@ extern "C" quads_status_t quads_weight_columns(const uint8_t* w_codes, const uin
   gemm::wtrans_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
       w_codes, w_scales, num_groups, (int)rows_per_group, (int)cols, codes_t, scales_t);
   return check_launch("weight_columns", 1);
+}
+
+extern "C" quads_status_t quads_select_weight_channels(
+    int32_t num_groups, int64_t rows_per_group, int64_t cols, const uint8_t* codes_t,
+    const uint8_t* scales_t, const int32_t* sel, int32_t sel_per_group, int32_t k,
+    uint8_t* w_sel_codes, uint8_t* w_sel_scales, void* stream) {
+  if (!codes_t || !scales_t || !sel || !w_sel_codes || !w_sel_scales)
+    return fail(QUADS_ERR_INVALID_ARG, "select_weight_channels: null pointer argument");
+  if (num_groups < 1 || num_groups > 65535 || rows_per_group <= 0 || rows_per_group % 128 ||
+      rows_per_group > (1 << 30) || cols <= 0 || cols % 64 || cols > (1 << 30))
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "select_weight_channels: rows_per_group %% 128, cols %% 64, groups <= 65535");
+  if (k <= 0 || k % 16 || k > cols)
+    return fail(QUADS_ERR_INVALID_ARG, "select_weight_channels: need 16 <= k <= cols, k %% 16 == 0");
+  if (!al16(w_sel_codes) || !al16(codes_t) || !al16(scales_t))
+    return fail(QUADS_ERR_MISALIGNED, "select_weight_channels: codes_t, scales_t and w_sel_codes must be 16-byte aligned");
+  const int kpad = quads_kpad(k);
+  gemm::launch_wsel(codes_t, scales_t, num_groups, (int)rows_per_group, (int)cols, sel,
+                    sel_per_group, k, kpad, w_sel_codes, w_sel_scales, (cudaStream_t)stream);
+  return check_launch("select_weight_channels", 1);
 }

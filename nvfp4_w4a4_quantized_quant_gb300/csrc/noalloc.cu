@@ -72,5 +72,6 @@ extern "C" quads_status_t quads_select_residual_channels_noalloc(
                                         scale_layout, tensor_scale, score_partials, k, sel,
                                         scores_out, r_codes, r_scales, r_scale_layout,
                                         r_tensor_scale, scratch,
-                                        (size_t)QUADS_NOALLOC_SELECT_SCRATCH_BYTES, stream);
+                                        (size_t)QUADS_NOALLOC_SELECT_SCRATCH_BYTES, nullptr,
+                                        stream);
 }

@@ -618,7 +618,7 @@ extern "C" quads_status_t quads_select_residual_channels(
     int32_t num_groups, const uint8_t* scales, int32_t scale_layout, const float* tensor_scale,
     const float* score_partials, int32_t k, int32_t* sel, float* scores_out, uint8_t* r_codes,
     uint8_t* r_scales, int32_t r_scale_layout, float* r_tensor_scale, void* workspace,
-    size_t workspace_bytes, void* stream) {
+    size_t workspace_bytes, void* sel_ready_event, void* stream) {
   if (!x || !scales || !tensor_scale || !score_partials || !sel || !r_codes || !r_scales || !r_tensor_scale)
     return fail(QUADS_ERR_INVALID_ARG, "select: null pointer argument");
   if (cols <= 0 || cols % 16 || cols > 8192)
@@ -631,8 +631,14 @@ extern "C" quads_status_t quads_select_residual_channels(
   const size_t need = quads_workspace_size(QUADS_OP_SELECT, rows, cols, 0, k, G);
   if (!workspace || workspace_bytes < need)
     return fail(QUADS_ERR_WORKSPACE, "select: workspace needs %zu bytes", need);
-  if (rows == 0) return QUADS_OK;
   cudaStream_t st = (cudaStream_t)stream;
+  auto sel_ready = [&]() -> quads_status_t {
+    if (!sel_ready_event) return QUADS_OK;
+    const cudaError_t e = cudaEventRecord((cudaEvent_t)sel_ready_event, st);
+    return e == cudaSuccess ? QUADS_OK
+                            : fail(QUADS_ERR_CUDA, "select: cudaEventRecord: %s", cudaGetErrorString(e));
+  };
+  if (rows == 0) return sel_ready();
   float* rs = (float*)workspace;
   const size_t rs_bytes = ((size_t)rows * k * 4 + 255) & ~(size_t)255;
   uint32_t* amax = (uint32_t*)((char*)workspace + rs_bytes);
@@ -648,6 +654,7 @@ extern "C" quads_status_t quads_select_residual_channels(
   topk_kernel<<<dim3(1, (unsigned)G), 1024, 0, st>>>(scores, (int)cols, k, sel,
                                                      long_groups ? nullptr : score_partials,
                                                      group_offsets, rows);
+  if (quads_status_t s = sel_ready()) return s;
   cudaMemsetAsync(amax, 0, (size_t)G * 4, st);
   rsel_residual_kernel<<<grid_for((rows + 31) / 32, 1, 16), 256, 0, st>>>(
       (const __nv_bfloat16*)x, rows, (int)cols, ldx, group_offsets, G, scales, scale_layout,

@@ -99,20 +99,25 @@ class MoEExpertLayer:
             sel2=e((E, k2), dt=i32), r2c=e((cap, kp2 // 2)), r2s=e(Q.sf_tc_bytes(cap, kp2)),
             r2ts=e(E, dt=f32), hamax=e(E, dt=f32),
             y=e((cap, H), dt=torch.bfloat16), out=e((T, H), dt=torch.bfloat16),
+            w1sc=e((E * 2 * F, kp1 // 2)), w1ss=e(Q.sf_tc_bytes(E * 2 * F, kp1)),
+            w2sc=e((E * H, kp2 // 2)), w2ss=e(Q.sf_tc_bytes(E * H, kp2)),
         )
         self.ws = dict(
             rt=e(Q.workspace_size(Q.OP_MOE_ROUTE, T, E, 0, topk)),
             q1=e(Q.workspace_size(Q.OP_QUANTIZE, T, H)),
             s1=e(Q.workspace_size(Q.OP_SELECT, T, H, 0, k1)),
-            g1=e(Q.workspace_size(Q.OP_MOE_GEMM, 0, H, 2 * F, k1, E)),
             q2=e(Q.workspace_size(Q.OP_QUANTIZE, cap, F, 0, 0, E)),
             s2=e(Q.workspace_size(Q.OP_SELECT, cap, F, 0, k2, E)),
-            g2=e(Q.workspace_size(Q.OP_MOE_GEMM, 0, F, H, k2, E)),
         )
-        # routing does not depend on X's quantization: it runs on a side stream
-        # (joined before the gathers), also inside a captured graph
+        # Work that does not wait on its neighbours runs on two side streams,
+        # forked and joined by events (so this also holds inside a captured
+        # graph): routing, then the gather of X's rows (needs only X's codes),
+        # on `side`; Q(W_sel) of each GEMM (needs only the selection, not
+        # R_sel) on `wside`.
         self.side = torch.cuda.Stream(device=dev)
-        self.ev_fork, self.ev_plan = torch.cuda.Event(), torch.cuda.Event()
+        self.wside = torch.cuda.Stream(device=dev)
+        (self.ev_fork, self.ev_xq, self.ev_a1, self.ev_sel1, self.ev_w1, self.ev_sel2,
+         self.ev_w2) = (torch.cuda.Event() for _ in range(7))
 
     def forward(self, x: torch.Tensor, logits: torch.Tensor, stream=None) -> dict:
         b, ws, T = self.b, self.ws, x.shape[0]
@@ -124,37 +129,50 @@ class MoEExpertLayer:
         self.side.wait_event(self.ev_fork)
         plan = Q.moe_route(logits, self.topk, rows_capacity=self.cap, out=b["route"],
                            workspace=ws["rt"], stream=self.side)
-        self.ev_plan.record(self.side)
         xq, xpart = Q.quantize_nvfp4(x, scores=comp, workspace=ws["q1"], stream=stream,
                                      out=(b["xc"], b["xs"], b["xts"], b["xpart"] if comp else None))
-        main.wait_event(self.ev_plan)
-        a1 = Q.moe_gather(plan, xq, out=(b["a1c"], b["a1s"]), stream=stream)
-        r1 = sel1 = None
+        self.ev_xq.record(main)
+        self.side.wait_event(self.ev_xq)
+        a1 = Q.moe_gather(plan, xq, out=(b["a1c"], b["a1s"]), stream=self.side)
+        self.ev_a1.record(self.side)
+        r1 = sel1 = w1sel = None
         if comp:
             sel1, _, xr = Q.select_residual_channels(x, xq, xpart, self.k1, workspace=ws["s1"],
-                                                     stream=stream,
+                                                     sel_ready_event=self.ev_sel1, stream=stream,
                                                      out=(b["sel1"], b["r1c"], b["r1s"], b["r1ts"]))
+            self.wside.wait_event(self.ev_sel1)
+            w1sel = Q.select_weight_channels(self.w1q, sel1, self.k1, E, stream=self.wside,
+                                             out=(b["w1sc"], b["w1ss"]))
+            self.ev_w1.record(self.wside)
+        main.wait_event(self.ev_a1)
+        if comp:
             r1 = Q.moe_gather(plan, xr, out=(b["g1c"], b["g1s"]), stream=stream)
+            main.wait_event(self.ev_w1)
         # GEMM1's epilogue also leaves each expert's max |h| for h's tensor scale
         h = Q.moe_grouped_gemm(plan, a1, self.w1q, E, 2 * F, r1, sel1, self.k1,
-                               epilogue=Q.EPI_SWIGLU, y_amax=b["hamax"], workspace=ws["g1"],
+                               epilogue=Q.EPI_SWIGLU, y_amax=b["hamax"], w_sel=w1sel,
                                out=b["h"], stream=stream)
         hq, hpart = Q.quantize_nvfp4(h, group_offsets=plan["offsets"], num_groups=E,
                                      tensor_amax_in=b["hamax"], scale_layout=Q.TCGEN05,
                                      scores=comp, rows=self.cap,
                                      workspace=ws["q2"], stream=stream,
                                      out=(b["hc"], b["hs"], b["hts"], b["hpart"] if comp else None))
-        r2 = sel2 = None
+        r2 = sel2 = w2sel = None
         if comp:
             sel2, _, r2 = Q.select_residual_channels(h, hq, hpart, self.k2,
                                                      group_offsets=plan["offsets"], num_groups=E,
                                                      r_scale_layout=Q.TCGEN05, workspace=ws["s2"],
-                                                     stream=stream,
+                                                     sel_ready_event=self.ev_sel2, stream=stream,
                                                      out=(b["sel2"], b["r2c"], b["r2s"], b["r2ts"]))
+            self.wside.wait_event(self.ev_sel2)
+            w2sel = Q.select_weight_channels(self.w2q, sel2, self.k2, E, sel_per_group=True,
+                                             stream=self.wside, out=(b["w2sc"], b["w2ss"]))
+            self.ev_w2.record(self.wside)
+            main.wait_event(self.ev_w2)
         y = Q.moe_grouped_gemm(plan, hq, self.w2q, E, H, r2, sel2, self.k2,
                                a_scale_per_expert=True, r_scale_per_expert=True,
-                               sel_per_expert=True, workspace=ws["g2"], out=b["y"], stream=stream)
+                               sel_per_expert=True, w_sel=w2sel, out=b["y"], stream=stream)
         out = Q.moe_combine(y, plan, out=b["out"], stream=stream)
-        self._a1, self._r1 = a1, r1
+        self._a1, self._r1, self._w1sel = a1, r1, w1sel
         return dict(out=out, plan=plan, xq=xq, sel1=sel1, a1=a1, r1=r1, h=h, hq=hq, sel2=sel2,
                     r2=r2, y=y)

@@ -37,15 +37,17 @@ _SIGS = {
     "quads_quantize_nvfp4": (_I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P, _I64, _P,
                                     _I32, _P, _P, _P, _SZ, _P]),
     "quads_select_residual_channels": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _I32, _P, _P,
-                                              _I32, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P]),
+                                              _I32, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P, _P]),
     "quads_select_residual_channels_noalloc": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _I32, _P,
                                                       _P, _I32, _P, _P, _P, _P, _I32, _P, _P]),
     "quads_w4a4_gemm_comp": (_I32, [_I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                                    _P, _P, _I32, _P, _I32, _I64, _P, _SZ, _P]),
+                                    _P, _P, _P, _P, _I32, _P, _I32, _I64, _P, _SZ, _P]),
     "quads_moe_grouped_gemm": (_I32, [_I32, _I64, _I64, _I64, _P, _P, _P, _P, _P, _I32, _P, _P,
-                                      _P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _P,
-                                      _I32, _I64, _P, _P, _SZ, _P]),
+                                      _P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32,
+                                      _P, _I32, _I64, _P, _P, _SZ, _P]),
     "quads_weight_columns": (_I32, [_P, _P, _I32, _I64, _I64, _P, _P, _P]),
+    "quads_select_weight_channels": (_I32, [_I32, _I64, _I64, _P, _P, _P, _I32, _I32, _P, _P,
+                                            _P]),
     "quads_trace_round": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _P, _P]),
     "quads_moe_route": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _I64, _P, _SZ, _P]),
     "quads_moe_gather": (_I32, [_P, _P, _I32, _I64, _I64, _P, _P, _P, _P, _P]),
@@ -96,9 +98,12 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _torch_stream(stream=None):
+    return torch.cuda.current_stream() if stream is None else stream
+
+
 def _stream(stream=None):
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    return ctypes.c_void_p(_torch_stream(stream).cuda_stream)
 
 
 def kpad(k: int) -> int:
@@ -177,11 +182,21 @@ def quantize_nvfp4(x: torch.Tensor, *, group_offsets=None, num_groups: int = 1,
     return QTensor(codes, scales, ts, rows, cols, scale_layout), part
 
 
+def _event(ev, stream):
+    """Raw cudaEvent_t of a torch.cuda.Event (created by a first record if needed)."""
+    if ev is None:
+        return None
+    if not ev.cuda_event:
+        ev.record(_torch_stream(stream))
+    return ctypes.c_void_p(ev.cuda_event)
+
+
 def select_residual_channels(x: torch.Tensor, q: QTensor, partials: torch.Tensor, k: int, *,
                              group_offsets=None, num_groups: int = 1,
                              r_scale_layout: int = LINEAR, want_scores: bool = False,
-                             workspace=None, out=None, stream=None):
-    """-> (sel int32 [G, k], scores [G, cols] or None, QTensor of Q(R_sel) [rows, kpad])."""
+                             sel_ready_event=None, workspace=None, out=None, stream=None):
+    """-> (sel int32 [G, k], scores [G, cols] or None, QTensor of Q(R_sel) [rows, kpad]).
+    sel_ready_event (torch.cuda.Event): recorded once sel is written, before R_sel."""
     lib = load()
     G = num_groups if group_offsets is not None else 1
     rows, cols = q.rows, q.cols
@@ -200,8 +215,8 @@ def select_residual_channels(x: torch.Tensor, q: QTensor, partials: torch.Tensor
     _check(lib.quads_select_residual_channels(
         _ptr(x), rows, cols, x.stride(0), _ptr(group_offsets), G, _ptr(q.scales), q.layout,
         _ptr(q.tensor_scale), _ptr(partials), k, _ptr(sel), _ptr(sc), _ptr(rc), _ptr(rs),
-        r_scale_layout, _ptr(rts), _ptr(ws), ws.numel(), _stream(stream)),
-        "select_residual_channels")
+        r_scale_layout, _ptr(rts), _ptr(ws), ws.numel(), _event(sel_ready_event, stream),
+        _stream(stream)), "select_residual_channels")
     return sel, sc, QTensor(rc, rs, rts, rows, kp, r_scale_layout)
 
 
@@ -232,21 +247,30 @@ def select_residual_channels_noalloc(x: torch.Tensor, q: QTensor, partials: torc
     return sel, sc, QTensor(rc, rs, rts, rows, kp, r_scale_layout)
 
 
+def _wsel_args(r, w, w_sel, size_args, dev, workspace):
+    """Workspace and Q(W_sel) pointers of a compensated GEMM call."""
+    if r is None:
+        return None, None, None
+    if w_sel is not None:
+        return None, _ptr(w_sel.codes), _ptr(w_sel.scales)
+    if w.codes_t is None:
+        raise QuadsError("compensation needs the weight's column-major copy (weight_columns)")
+    return _workspace(workspace_size(*size_args), dev, workspace), None, None
+
+
 def w4a4_gemm_comp(a: QTensor, w: QTensor, r: Optional[QTensor] = None, sel=None, k: int = 0, *,
-                   out_dtype=torch.bfloat16, workspace=None, out=None, stream=None):
-    """Y [M, N] = Q(A) Q(W)^T (+ Q(R_sel) Q(W_sel)^T when r is given)."""
+                   out_dtype=torch.bfloat16, w_sel: Optional[QTensor] = None, workspace=None,
+                   out=None, stream=None):
+    """Y [M, N] = Q(A) Q(W)^T (+ Q(R_sel) Q(W_sel)^T when r is given; Q(W_sel) is
+    built by the call unless given, from select_weight_channels)."""
     lib = load()
     M, K, N = a.rows, a.cols, w.rows
     y = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=a.codes.device)
     yd = OUT_F32 if y.dtype == torch.float32 else OUT_BF16
-    ws = None
-    if r is not None:
-        ws = _workspace(workspace_size(OP_GEMM, 0, K, N, k, 1), y.device, workspace)
-    if r is not None and w.codes_t is None:
-        raise QuadsError("compensation needs the weight's column-major copy (weight_columns)")
+    ws, wsc, wss = _wsel_args(r, w, w_sel, (OP_GEMM, 0, K, N, k, 1), y.device, workspace)
     _check(lib.quads_w4a4_gemm_comp(
         M, N, K, _ptr(a.codes), _ptr(a.scales), _ptr(a.tensor_scale), _ptr(w.codes),
-        _ptr(w.scales), _ptr(w.tensor_scale), _ptr(w.codes_t), _ptr(w.scales_t),
+        _ptr(w.scales), _ptr(w.tensor_scale), _ptr(w.codes_t), _ptr(w.scales_t), wsc, wss,
         _ptr(r.codes if r else None),
         _ptr(r.scales if r else None), _ptr(r.tensor_scale if r else None), _ptr(sel), k,
         _ptr(y), yd, y.stride(0), _ptr(ws), ws.numel() if ws is not None else 0,
@@ -258,8 +282,8 @@ def moe_grouped_gemm(plan: dict, a: QTensor, w: QTensor, num_experts: int, n: in
                      r: Optional[QTensor] = None, sel=None, k: int = 0, *,
                      a_scale_per_expert: bool = False, r_scale_per_expert: bool = False,
                      sel_per_expert: bool = False, epilogue: int = EPI_NONE,
-                     out_dtype=torch.bfloat16, y_amax=None, workspace=None, out=None,
-                     stream=None):
+                     out_dtype=torch.bfloat16, y_amax=None, w_sel: Optional[QTensor] = None,
+                     workspace=None, out=None, stream=None):
     """Grouped compensated GEMM over the experts of `plan` (from moe_route)."""
     lib = load()
     cap = plan["rows_capacity"]
@@ -267,15 +291,12 @@ def moe_grouped_gemm(plan: dict, a: QTensor, w: QTensor, num_experts: int, n: in
     ycols = n // 2 if epilogue == EPI_SWIGLU else n
     y = out if out is not None else torch.empty((cap, ycols), dtype=out_dtype, device=a.codes.device)
     yd = OUT_F32 if y.dtype == torch.float32 else OUT_BF16
-    ws = None
-    if r is not None:
-        ws = _workspace(workspace_size(OP_MOE_GEMM, 0, K, n, k, num_experts), y.device, workspace)
-    if r is not None and w.codes_t is None:
-        raise QuadsError("compensation needs the weight's column-major copy (weight_columns)")
+    ws, wsc, wss = _wsel_args(r, w, w_sel, (OP_MOE_GEMM, 0, K, n, k, num_experts), y.device,
+                              workspace)
     _check(lib.quads_moe_grouped_gemm(
         num_experts, cap, n, K, _ptr(plan["offsets"]), _ptr(plan["counts"]), _ptr(a.codes),
         _ptr(a.scales), _ptr(a.tensor_scale), int(a_scale_per_expert), _ptr(w.codes),
-        _ptr(w.scales), _ptr(w.tensor_scale), _ptr(w.codes_t), _ptr(w.scales_t),
+        _ptr(w.scales), _ptr(w.tensor_scale), _ptr(w.codes_t), _ptr(w.scales_t), wsc, wss,
         _ptr(r.codes if r else None), _ptr(r.scales if r else None),
         _ptr(r.tensor_scale if r else None), int(r_scale_per_expert), _ptr(sel),
         int(sel_per_expert), k, epilogue, _ptr(y), yd, y.stride(0), _ptr(y_amax), _ptr(ws),
@@ -317,6 +338,25 @@ def weight_columns(w: QTensor, num_groups: int = 1, stream=None) -> QTensor:
                                     _ptr(w.codes_t), _ptr(w.scales_t), _stream(stream)),
            "weight_columns")
     return w
+
+
+def select_weight_channels(w: QTensor, sel: torch.Tensor, k: int, num_groups: int = 1, *,
+                           sel_per_group: bool = False, out=None, stream=None) -> QTensor:
+    """Q(W_sel): the selected columns of the weight (per group), requantized with
+    the group's s_w kept aside; TCGEN05 scales over kpad columns."""
+    lib = load()
+    if w.codes_t is None:
+        raise QuadsError("select_weight_channels needs the column-major copy (weight_columns)")
+    rpg, kp, dev = w.rows // num_groups, kpad(k), w.codes.device
+    if out is None:
+        out = (torch.empty((w.rows, kp // 2), dtype=torch.uint8, device=dev),
+               torch.empty(sf_tc_bytes(w.rows, kp), dtype=torch.uint8, device=dev))
+    codes, scales = out
+    _check(lib.quads_select_weight_channels(num_groups, rpg, w.cols, _ptr(w.codes_t),
+                                            _ptr(w.scales_t), _ptr(sel), int(sel_per_group), k,
+                                            _ptr(codes), _ptr(scales), _stream(stream)),
+           "select_weight_channels")
+    return QTensor(codes, scales, None, w.rows, kp, TCGEN05)
 
 
 def moe_route(logits: torch.Tensor, topk: int, *, rows_capacity: Optional[int] = None,

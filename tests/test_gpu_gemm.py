@@ -120,3 +120,49 @@ def test_repeat_calls_are_deterministic(lib):
     y1, _, _ = _run(lib, d["x"], d["w"], d["k"], torch.float32)
     y2, _, _ = _run(lib, d["x"], d["w"], d["k"], torch.float32)
     assert torch.equal(y1, y2)
+
+
+def test_prebuilt_w_sel_matches_oracle_and_the_built_in_path(lib):
+    """select_weight_channels gives the oracle's Q(W_sel) bit for bit, and a GEMM
+    fed that operand returns exactly the output of one that builds it itself."""
+    d = inputs.single_linear(0)
+    y_in, sel, _ = _run(lib, d["x"], d["w"], d["k"], torch.float32)
+    wq, _ = lib.quantize_nvfp4(bf16_tensor(d["w"]), scale_layout=1)
+    lib.weight_columns(wq)
+    k, N = d["k"], d["w"].shape[0]
+    wsel = lib.select_weight_channels(wq, sel, k)
+    x = bf16_tensor(d["x"])
+    xq, part = lib.quantize_nvfp4(x, scores=True, scale_layout=1)
+    sel2, _, r = lib.select_residual_channels(x, xq, part, k, r_scale_layout=1)
+    y_pre = lib.w4a4_gemm_comp(xq, wq, r, sel2, k, out_dtype=torch.float32, w_sel=wsel)
+    torch.cuda.synchronize()
+    assert torch.equal(sel, sel2) and torch.equal(y_in, y_pre)
+    _, _, ref, (wsc, wss) = _oracle(d["x"], d["w"], k)
+    c = codes_np(wsel.codes, wsel.cols)
+    s = unswizzle(wsel.scales, N, wsel.cols)
+    assert np.array_equal(c[:, :k], wsc) and not c[:, k:].any()
+    assert np.array_equal(s[:, : k // 16], wss) and not s[:, k // 16:].any()
+
+
+@pytest.mark.parametrize("G,N,K,k", [(3, 256, 512, 48), (2, 640, 320, 320)])
+def test_select_weight_channels_per_group(lib, G, N, K, k):
+    """Grouped weights with one selection per group (the MoE GEMM2 case), against
+    the oracle group by group; k == K takes every column."""
+    rng = inputs.make_rng(G * N + K + k)
+    wb = inputs.f32_to_bf16_bits(rng.standard_normal((G * N, K), dtype=np.float32) * np.float32(0.02))
+    sel = np.stack([np.sort(rng.choice(K, k, replace=False)) for _ in range(G)]).astype(np.int32)
+    wq, _ = lib.quantize_nvfp4(bf16_tensor(wb), scale_layout=1, group_offsets=None)
+    lib.weight_columns(wq, num_groups=G)
+    out = lib.select_weight_channels(wq, torch.from_numpy(sel).cuda(), k, num_groups=G,
+                                     sel_per_group=True)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    c = codes_np(out.codes, out.cols)
+    s = unswizzle(out.scales, G * N, out.cols)
+    wf = f32(wb)
+    wc, ws, _ = Q.quantize_groups(wf)
+    for g in range(G):
+        rows = slice(g * N, (g + 1) * N)
+        wsc, wss = Q.requantize_weight_columns(wc[rows], ws[rows], sel[g])
+        assert np.array_equal(c[rows, :k], wsc) and not c[rows, k:].any()
+        assert np.array_equal(s[rows, : k // 16], wss) and not s[rows, k // 16:].any()

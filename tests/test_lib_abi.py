@@ -49,17 +49,24 @@ def test_host_side_argument_checks_need_no_gpu(lib):
     assert st == 2                                   # tcgen05 layout needs cols % 64
     st = lib.quads_quantize_nvfp4(p, 8, 32, 32, None, None, 1, p, p, p, 16, p, 0, p, None, p, 64, None)
     assert st == 1                                   # both tensor_scale_in and tensor_amax_in
-    st = lib.quads_w4a4_gemm_comp(64, 100, 256, p, p, p, p, p, p, None, None, None, None, None, None, 0,
-                                  p, 0, 100, None, 0, None)
+    st = lib.quads_w4a4_gemm_comp(64, 100, 256, p, p, p, p, p, p, None, None, None, None, None, None,
+                                  None, None, 0, p, 0, 100, None, 0, None)
     assert st == 2 and "N%128" in _err(lib)
-    st = lib.quads_w4a4_gemm_comp(64, 128, 256, p, p, p, p, p, p, p, p, p, p, p, p, 8, p, 0, 128, None, 0,
-                                  None)
+    st = lib.quads_w4a4_gemm_comp(64, 128, 256, p, p, p, p, p, p, p, p, None, None, p, p, p, p, 8, p, 0,
+                                  128, None, 0, None)
     assert st == 1                                   # k not a multiple of 16
-    st = lib.quads_w4a4_gemm_comp(64, 128, 256, p, p, p, p, p, p, None, None, p, p, p, p, 16, p, 0, 128,
-                                  None, 0, None)
-    assert st == 1 and "column-major" in _err(lib)   # compensation without the weight copy
+    st = lib.quads_w4a4_gemm_comp(64, 128, 256, p, p, p, p, p, p, None, None, None, None, p, p, p, p, 16,
+                                  p, 0, 128, None, 0, None)
+    assert st == 1 and "column-major" in _err(lib)   # compensation without the weight copy or Q(W_sel)
+    st = lib.quads_w4a4_gemm_comp(64, 128, 256, p, p, p, p, p, p, None, None, p, None, p, p, p, p, 16,
+                                  p, 0, 128, None, 0, None)
+    assert st == 1 and "both" in _err(lib)           # Q(W_sel) codes without its scales
+    q = ctypes.c_void_p(24)
+    st = lib.quads_w4a4_gemm_comp(64, 128, 256, p, p, p, p, p, p, None, None, q, p, p, p, p, p, 16,
+                                  p, 0, 128, None, 0, None)
+    assert st == 3                                   # Q(W_sel) not 16-byte aligned
     st = lib.quads_select_residual_channels(p, 64, 256, 256, None, 1, p, 0, p, p, 17, p, None, p, p, 0, p,
-                                            p, 1 << 20, None)
+                                            p, 1 << 20, None, None)
     assert st == 2
     st = lib.quads_moe_route(p, 100, 300, 8, p, p, p, p, p, p, 1 << 20, p, 1 << 20, None)
     assert st == 2                                   # > 256 experts
@@ -68,10 +75,19 @@ def test_host_side_argument_checks_need_no_gpu(lib):
     st = lib.quads_moe_route(p, 100, 16, 8, p, p, p, p, p, p, 1 << 20, p, 4, None)
     assert st == 7                                   # workspace too small
     st = lib.quads_moe_grouped_gemm(4, 1000, 256, 256, p, None, p, p, p, 0, p, p, p, None, None, None,
-                                    None, None, 0, None, 0, 0, 0, p, 1, 256, None, None, 0, None)
+                                    None, None, None, None, 0, None, 0, 0, 0, p, 1, 256, None, None, 0,
+                                    None)
     assert st == 2                                   # rows_capacity % 128
     st = lib.quads_weight_columns(p, p, 2, 100, 256, p, p, None)
     assert st == 2                                   # rows_per_group % 128
+    st = lib.quads_select_weight_channels(2, 100, 256, p, p, p, 0, 16, p, p, None)
+    assert st == 2                                   # rows_per_group % 128
+    st = lib.quads_select_weight_channels(2, 128, 256, p, p, p, 0, 24, p, p, None)
+    assert st == 1                                   # k % 16
+    st = lib.quads_select_weight_channels(2, 128, 256, p, p, p, 0, 272, p, p, None)
+    assert st == 1                                   # k > cols
+    st = lib.quads_select_weight_channels(2, 128, 256, p, p, None, 0, 16, p, p, None)
+    assert st == 1                                   # no selection
     st = lib.quads_trace_round(p, 4, 24, 24, p, 12, p, p, p, None, None)
     assert st == 2
 
