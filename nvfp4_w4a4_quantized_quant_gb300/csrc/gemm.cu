@@ -11,9 +11,9 @@
 // Design (one CTA per SM, 128x128 output tiles, K tiles of 512 FP4 = 256 B):
 //   warps 0-2   TMA producers: A/B code tiles by tensor-map TMA (128B
 //               swizzle) and scale atoms by bulk copy into a 3-stage x 72 KB
-//               smem ring; a 512-element K tile is four 16 KB boxes (A and B,
-//               two 128-byte sub-tiles each) and two 4 KB atom runs, dealt to
-//               the three warps in turn.  One issuing warp
+//               smem ring; a 512-element K tile is eight 8 KB boxes (A and B,
+//               two 128-byte sub-tiles of two 64-row halves each) and two 4 KB
+//               atom runs, 24 KB per warp.  One issuing warp
 //               moves only ~29 B/cycle into its SM (its copies are processed
 //               one after another); three keep up with the ~70 B/cycle/SM
 //               that L2 delivers when every SM is loading.
@@ -59,7 +59,9 @@ constexpr int A_TILE = A_SUB * KSUBS;
 constexpr int B_TILE = B_SUB * KSUBS;
 constexpr int SF_TILE = KSTEPS * 512;         // scale atoms (128 rows x 4 blocks each) per operand
 constexpr int STAGE_BYTES = A_TILE + B_TILE + 2 * SF_TILE;  // 72 KB
-constexpr int BOXES = 2 * KSUBS;              // TMA boxes per stage: A0, B0, A1, B1
+constexpr int BOX_ROWS = 64;                  // rows per TMA box: half a 128-row sub-tile
+constexpr int BOX_BYTES = BOX_ROWS * KSUB;    // 8 KB
+constexpr int BOXES = 2 * KSUBS * 2;          // per stage: (A, B) x sub-tiles x halves
 constexpr int COPIES = BOXES + 2;             // + the SFA and SFB atom runs (bulk copies)
 constexpr int SF_BUFS = 2;                    // TMEM scale buffers
 constexpr int SF_BUF_COLS = 2 * 4 * KSTEPS;   // SFA 32 + SFB 32 columns
@@ -396,10 +398,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp < PRODUCERS) {
     // ------------------------------------------------------------ producers
-    // Copy g = COPIES * it + b of ring iteration it goes to producer g % 3;
-    // each copy arrives once on full[s] (a code box with its bytes, or without
-    // any when the stage's K range ends before its sub-tile).  The whole warp runs the loop
-    // (so addresses and coordinates stay warp-uniform); one elected lane issues.
+    // A stage is ten copies: eight 8 KB code boxes (A/B x two 128-byte
+    // sub-tiles x two 64-row halves) and two 4 KB scale-atom runs, dealt as
+    // 3 + 3 + 4 copies so that each producer warp moves 24 KB (one warp's
+    // copies are processed one after another, so the most loaded warp sets
+    // the stage's pace).  Each copy arrives once on full[s] (a box with its
+    // bytes, or without any when the stage's K range ends before its
+    // sub-tile).  The whole warp runs the loop (so addresses and coordinates
+    // stay warp-uniform); one elected lane issues.
+    const int b_lo = warp == 0 ? 0 : (warp == 1 ? 3 : 6);
+    const int b_hi = warp == 0 ? 3 : (warp == 1 ? 6 : COPIES);
     uint32_t it = 0, last = 0;
     bool ok = true, any = false;
     for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
@@ -418,32 +426,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const CUtensorMap* mb = corr ? &tmW : &tmB;
         const uint8_t* sfa = corr ? p.r_sf + (tl.m0 / BM) * r_sf_rb : p.a_sf + (tl.m0 / BM) * a_sf_rb;
         const uint8_t* sfb = corr ? p.ws_sf + (brow / BN) * r_sf_rb : p.b_sf + (brow / BN) * a_sf_rb;
-        bool waited = false;
-        for (int b = 0; b < COPIES; ++b) {
-          if ((COPIES * it + b) % PRODUCERS != (uint32_t)warp) continue;
-          if (!waited) {
-            if (!warp_wait_bar(&empty[s], ph ^ 1, abort_flag, p.err)) { ok = false; break; }
-            waited = true;
-          }
-          const int u = b >> 1;
-          if (elect_one()) {
+        if (!warp_wait_bar(&empty[s], ph ^ 1, abort_flag, p.err)) { ok = false; break; }
+        if (elect_one()) {
+          for (int b = b_lo; b < b_hi; ++b) {
             if (b >= BOXES) {
               mbar_expect_tx(&full[s], ksteps * 512);
               if (b == BOXES) bulk_load(st + A_TILE + B_TILE, sfa + kk * SF_TILE, ksteps * 512, &full[s]);
               else bulk_load(st + A_TILE + B_TILE + SF_TILE, sfb + kk * SF_TILE, ksteps * 512, &full[s]);
-            } else if (u < nsub) {
-              mbar_expect_tx(&full[s], (b & 1) ? B_SUB : A_SUB);
+              continue;
+            }
+            const int u = b >> 2, isb = (b >> 1) & 1, hf = b & 1;
+            if (u < nsub) {
+              mbar_expect_tx(&full[s], BOX_BYTES);
               const int x = kk * (KSUB * KSUBS) + u * KSUB;
-              if (b & 1) tma_load_2d(st + A_TILE + u * B_SUB, mb, x, (int)brow, &full[s]);
-              else tma_load_2d(st + u * A_SUB, ma, x, (int)tl.m0, &full[s]);
+              if (isb)
+                tma_load_2d(st + A_TILE + u * B_SUB + hf * BOX_BYTES, mb, x,
+                            (int)(brow + hf * BOX_ROWS), &full[s]);
+              else
+                tma_load_2d(st + u * A_SUB + hf * BOX_BYTES, ma, x, (int)(tl.m0 + hf * BOX_ROWS),
+                            &full[s]);
             } else {
               mbar_arrive(&full[s]);
             }
           }
-          __syncwarp();
-          last = it;
-          any = true;
         }
+        __syncwarp();
+        last = it;
+        any = true;
       }
     }
     if (!ok && any && lane == 0) {
@@ -783,7 +792,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D byte tensor [rows, width_bytes] (row pitch ld_bytes), box 128 B x 128 rows,
+// 2-D byte tensor [rows, width_bytes] (row pitch ld_bytes), box 128 B x 64 rows,
 // 128-byte swizzle, out-of-range elements read as zero.
 static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t width_bytes,
                      int64_t ld_bytes) {
@@ -791,7 +800,7 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t wid
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)width_bytes, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)ld_bytes};
-  cuuint32_t box[2] = {KSUB, BM};
+  cuuint32_t box[2] = {KSUB, BOX_ROWS};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
