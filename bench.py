@@ -191,7 +191,8 @@ def secondary(torch, Q, steps, flush, stream):
     """The other configurations of the scope table, each captured in a CUDA
     graph and timed like the step (L2 flushed before every replay):
     dense projection 4096x2048 x W 6144x2048 (k=128, bf16 Y) compensated and
-    plain, the 512-token decode layer, and TRACE rounding of 16384x2048."""
+    plain, the 512-token decode layer, TRACE rounding of 16384x2048 and the
+    trainer-side W4A16 fake quantization of the expert gate/up weights."""
     import numpy as np
     from nvfp4_w4a4_quantized_quant_gb300 import inputs
     from nvfp4_w4a4_quantized_quant_gb300.layer import CompensatedLinear, MoEExpertLayer
@@ -256,6 +257,24 @@ def secondary(torch, Q, steps, flush, stream):
     tb = xt.numel() * (2 + 0.5 + 0.5 + 1.0 / 16)
     out["trace_16384x2048"] = {"ms": round(ms, 4), "gbs": round(tb / (ms * 1e-3) / 1e9, 1),
                                "algorithmic_bytes": int(tb)}
+    del xr, xt, rq, codes
+
+    # trainer-side W4A16 fake quantization of the 128 experts' gate/up weights
+    # (one tensor scale per expert; codes and scales written for the rollout copy)
+    E, H, F = WORKLOAD["experts"], WORKLOAD["hidden"], WORKLOAD["ffn"]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(2)
+    wq = (torch.randn((E * 2 * F, H), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    offs = torch.arange(0, E * 2 * F + 1, 2 * F, dtype=torch.int32, device="cuda")
+    yq = torch.empty_like(wq)
+    ws = torch.empty(Q.workspace_size(Q.OP_QUANTIZE, wq.shape[0], H, 0, 0, E), dtype=torch.uint8,
+                     device="cuda")
+    ms = graph_ms(lambda: Q.qdq_nvfp4(wq, group_offsets=offs, num_groups=E, want_codes=True,
+                                      workspace=ws, out=yq, stream=stream))
+    qb = wq.numel() * (2 + 2 + 0.5 + 1.0 / 16)
+    out["w4a16_qdq_w1"] = {"ms": round(ms, 4), "gbs": round(qb / (ms * 1e-3) / 1e9, 1),
+                           "algorithmic_bytes": int(qb), "shape": [E * 2 * F, H],
+                           "note": "bytes: x read once, bf16 y, codes + scales; the amax pass re-reads x"}
     return out
 
 
@@ -411,6 +430,8 @@ def run_gpu(args):
         dec["frac_hbm"] = round(dec["weight_bytes"] / (dec["ms"] * 1e-3) / 1e9 / pk["hbm"], 4)
         tr = sec["trace_16384x2048"]
         tr["frac_hbm"] = round(tr["gbs"] / pk["hbm"], 4)
+        wq = sec["w4a16_qdq_w1"]
+        wq["frac_hbm"] = round(wq["gbs"] / pk["hbm"], 4)
     fl = moe_flops()
     value = world * fl / (ms * 1e-3) / 1e12
     e2e_val = world * fl / (e_ms * 1e-3) / 1e12

@@ -162,6 +162,33 @@ quads_status_t quads_quantize_nvfp4(const void* x, int64_t rows, int64_t cols, i
                                     size_t workspace_bytes, void* stream);
 
 /*
+ * quads_qdq_nvfp4 -- the trainer side's W4A16 fake quantization ([QUADS] 2.2 A
+ * "Asymmetric Quantization-Aware Training" and 2.1 "Weights": the trainer runs
+ * the same quantize-dequantize path as the rollout engine, so every forward
+ * pass sees the weights the rollout uses while activations stay bf16).
+ * y = bf16(fl(level * d_b)) with the codes, block scales d_b and tensor scale
+ * that quads_quantize_nvfp4 produces for the same input (same rules, same
+ * bits); the codes and scales can be written in the same pass, for the copy
+ * synchronised to the rollout engine.  The backward pass of fake quantization
+ * is the identity (straight-through) and needs no call.
+ *
+ *   x [rows, cols] bf16 (ldx); group_offsets / num_groups / tensor_scale_in as
+ *     for quads_quantize_nvfp4 (one tensor scale per group, e.g. per expert).
+ *   y [rows, ldy] bf16 (ldy >= cols, multiple of 8; 16-byte aligned).
+ *   codes nullable ([rows, ld_codes]); scales (scale_layout) required when
+ *     codes is given; tensor_scale_out device float [num_groups].
+ *   workspace >= quads_workspace_size(QUADS_OP_QUANTIZE, rows, cols, 0, 0,
+ *     num_groups) unless tensor_scale_in is given.
+ * cols % 16 == 0.
+ */
+quads_status_t quads_qdq_nvfp4(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                               const int32_t* group_offsets, int32_t num_groups,
+                               const float* tensor_scale_in, void* y, int64_t ldy,
+                               uint8_t* codes, int64_t ld_codes, uint8_t* scales,
+                               int32_t scale_layout, float* tensor_scale_out, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/*
  * quads_select_residual_channels -- per row group: channel score = sum of the
  * group's score-partial rows in ascending order (float32); the k channels with
  * the largest score (ties -> lower channel index) returned ascending in

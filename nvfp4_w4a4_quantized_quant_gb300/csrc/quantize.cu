@@ -81,7 +81,10 @@ __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restri
 // block (l & 15) of row (l >> 4), so each block scale is computed once.  In
 // score mode every residual square R^2 is parked in shared memory and, after a
 // barrier, thread c adds column c's 32 squares in row order starting from 0 --
-// the fixed float32 order the score definition uses.
+// the fixed float32 order the score definition uses.  In QDQ mode (the
+// trainer's W4A16 fake quantization, [QUADS] 2.2 A) each element's dequantized
+// value fl(level * d_b) is also stored, rounded to bf16; codes and scales may
+// then be skipped (codes == nullptr).
 __device__ __forceinline__ void quantize_block16(const uint4& lo, const uint4& hi, float s_t,
                                                  float* f, BlockScale& bs, uint2& c) {
   bf16x8_to_f32(lo, f);
@@ -94,13 +97,13 @@ __device__ __forceinline__ void quantize_block16(const uint4& lo, const uint4& h
   c.y = quantize8(f + 8, bs);
 }
 
-template <bool kScores>
+template <bool kScores, bool kQdq>
 __global__ void __launch_bounds__(256) quantize_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
     const int32_t* __restrict__ row_index, const int32_t* __restrict__ goff, int G,
     const float* __restrict__ st, const uint32_t* __restrict__ amax_bits, float* __restrict__ st_out,
     uint8_t* __restrict__ codes, int64_t ldc, uint8_t* __restrict__ scales, int layout,
-    float* __restrict__ partials) {
+    float* __restrict__ partials, __nv_bfloat16* __restrict__ qdq, int64_t ldq) {
   // tensor scales: given (st), or derived here from the groups' amax bits
   // (then block 0 also stores them to st_out)
   __shared__ __align__(16) float sq[kScores ? kScoreChunk * 256 : 4];
@@ -161,11 +164,26 @@ __global__ void __launch_bounds__(256) quantize_kernel(
       uint2 c;
       quantize_block16(raw[it][0], raw[it][1], !valid ? 1.0f : g == g0 ? s_t0 : scale_of(g), f, bs,
                        c);
-      if (valid) {
+      if (valid && (!kQdq || codes)) {
         uint32_t* pc = reinterpret_cast<uint32_t*>(codes + row * ldc + (col >> 1));
         pc[0] = c.x;
         pc[1] = c.y;
         scales[sf_offset(layout, row, col >> 4, ncols16)] = (uint8_t)bs.byte;
+      }
+      if (kQdq && valid) {
+        float lv[16];
+        e2m1x8_to_f32(c.x, lv);
+        e2m1x8_to_f32(c.y, lv + 8);
+        uint32_t packed[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(lv[2 * j], bs.d),
+                                                   __fmul_rn(lv[2 * j + 1], bs.d));
+          packed[j] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        uint4* pq = reinterpret_cast<uint4*>(qdq + row * ldq + col);
+        pq[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        pq[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
       }
       if (kScores) {
         float lv[16];
@@ -550,15 +568,19 @@ int read_quant_device_error(cudaStream_t) {
 
 using namespace quads;
 
-extern "C" quads_status_t quads_quantize_nvfp4(
+// Shared by the quantizer and the W4A16 QDQ entry points (qdq == nullptr:
+// codes and scales only; codes == nullptr: bf16 QDQ values only).
+static quads_status_t quantize_impl(
     const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* row_index,
     const int32_t* group_offsets, int32_t num_groups, const float* tensor_scale_in,
     const float* tensor_amax_in, uint8_t* codes, int64_t ld_codes, uint8_t* scales,
-    int32_t scale_layout,
-    float* tensor_scale_out, float* score_partials, void* workspace, size_t workspace_bytes,
-    void* stream) {
-  if (!x || !codes || !scales || !tensor_scale_out)
+    int32_t scale_layout, float* tensor_scale_out, float* score_partials,
+    __nv_bfloat16* qdq, int64_t ldq, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!x || (!codes && !qdq) || (codes && !scales) || !tensor_scale_out)
     return fail(QUADS_ERR_INVALID_ARG, "quantize: null x/codes/scales/tensor_scale_out");
+  if (qdq && (ldq < cols || ldq % 8 || !aligned16(qdq)))
+    return fail(QUADS_ERR_MISALIGNED, "qdq: y must be 16-byte aligned with ldy >= cols, ldy %% 8 == 0");
+  if (!codes) ld_codes = cols / 2;
   if (rows < 0 || cols <= 0 || cols % 16)
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "quantize: cols=%lld must be a positive multiple of 16", (long long)cols);
   if (scale_layout == QUADS_SCALES_TCGEN05 && cols % 64)
@@ -567,7 +589,8 @@ extern "C" quads_status_t quads_quantize_nvfp4(
     return fail(QUADS_ERR_INVALID_ARG, "quantize: bad scale_layout %d", scale_layout);
   if (ldx < cols || ldx % 8 || ld_codes < cols / 2 || ld_codes % 4)
     return fail(QUADS_ERR_MISALIGNED, "quantize: ldx=%lld (>=cols, %%8) ld_codes=%lld (>=cols/2, %%4)", (long long)ldx, (long long)ld_codes);
-  if (!aligned16(x) || !aligned16(codes) || (score_partials && !aligned16(score_partials)))
+  if (!aligned16(x) || (codes && !aligned16(codes)) ||
+      (score_partials && !aligned16(score_partials)))
     return fail(QUADS_ERR_MISALIGNED, "quantize: x/codes/score_partials must be 16-byte aligned");
   const int G = group_offsets ? num_groups : 1;
   if (group_offsets && num_groups < 1) return fail(QUADS_ERR_INVALID_ARG, "quantize: num_groups < 1");
@@ -592,7 +615,7 @@ extern "C" quads_status_t quads_quantize_nvfp4(
   } else if (tensor_scale_in != tensor_scale_out) {
     cudaMemcpyAsync(tensor_scale_out, tensor_scale_in, (size_t)G * 4, cudaMemcpyDeviceToDevice, st);
   }
-  if (scale_layout == QUADS_SCALES_TCGEN05 && rows % 128) {
+  if (codes && scale_layout == QUADS_SCALES_TCGEN05 && rows % 128) {
     // padding rows of the last 128-row block must read as scale 0
     const int64_t ncols16 = cols / 16;
     const int64_t start = (rows / 128) * (ncols16 / 4) * 512;
@@ -600,17 +623,44 @@ extern "C" quads_status_t quads_quantize_nvfp4(
   }
   const int64_t ntasks = ((rows + 31) / 32) * ((cols + 255) / 256);  // one block per task
   const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(ntasks, (int64_t)num_sms() * 16));
-  if (score_partials)
-    quantize_kernel<true><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)x, rows, (int)cols, ldx,
-                                                  row_index, group_offsets, G, stp, amax_bits,
-                                                  tensor_scale_out, codes,
-                                                  ld_codes, scales, scale_layout, score_partials);
+  const __nv_bfloat16* xb = (const __nv_bfloat16*)x;
+  if (qdq)
+    quantize_kernel<false, true><<<blocks, 256, 0, st>>>(
+        xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
+        codes, ld_codes, scales, scale_layout, nullptr, qdq, ldq);
+  else if (score_partials)
+    quantize_kernel<true, false><<<blocks, 256, 0, st>>>(
+        xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
+        codes, ld_codes, scales, scale_layout, score_partials, nullptr, 0);
   else
-    quantize_kernel<false><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)x, rows, (int)cols, ldx,
-                                                   row_index, group_offsets, G, stp, amax_bits,
-                                                   tensor_scale_out, codes,
-                                                   ld_codes, scales, scale_layout, nullptr);
-  return check_launch("quantize", launched);
+    quantize_kernel<false, false><<<blocks, 256, 0, st>>>(
+        xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
+        codes, ld_codes, scales, scale_layout, nullptr, nullptr, 0);
+  return check_launch(qdq ? "qdq" : "quantize", launched);
+}
+
+extern "C" quads_status_t quads_quantize_nvfp4(
+    const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* row_index,
+    const int32_t* group_offsets, int32_t num_groups, const float* tensor_scale_in,
+    const float* tensor_amax_in, uint8_t* codes, int64_t ld_codes, uint8_t* scales,
+    int32_t scale_layout,
+    float* tensor_scale_out, float* score_partials, void* workspace, size_t workspace_bytes,
+    void* stream) {
+  if (!codes) return fail(QUADS_ERR_INVALID_ARG, "quantize: null codes");
+  return quantize_impl(x, rows, cols, ldx, row_index, group_offsets, num_groups, tensor_scale_in,
+                       tensor_amax_in, codes, ld_codes, scales, scale_layout, tensor_scale_out,
+                       score_partials, nullptr, 0, workspace, workspace_bytes, stream);
+}
+
+extern "C" quads_status_t quads_qdq_nvfp4(
+    const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* group_offsets,
+    int32_t num_groups, const float* tensor_scale_in, void* y, int64_t ldy, uint8_t* codes,
+    int64_t ld_codes, uint8_t* scales, int32_t scale_layout, float* tensor_scale_out,
+    void* workspace, size_t workspace_bytes, void* stream) {
+  if (!y) return fail(QUADS_ERR_INVALID_ARG, "qdq: null y");
+  return quantize_impl(x, rows, cols, ldx, nullptr, group_offsets, num_groups, tensor_scale_in,
+                       nullptr, codes, ld_codes, scales, scale_layout, tensor_scale_out, nullptr,
+                       (__nv_bfloat16*)y, ldy, workspace, workspace_bytes, stream);
 }
 
 extern "C" quads_status_t quads_select_residual_channels(

@@ -36,6 +36,8 @@ _SIGS = {
     "quads_kpad": (_I32, [_I32]),
     "quads_quantize_nvfp4": (_I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P, _I64, _P,
                                     _I32, _P, _P, _P, _SZ, _P]),
+    "quads_qdq_nvfp4": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _I64, _P, _I64, _P, _I32,
+                               _P, _P, _SZ, _P]),
     "quads_select_residual_channels": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _I32, _P, _P,
                                               _I32, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P, _P]),
     "quads_select_residual_channels_noalloc": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _I32, _P,
@@ -180,6 +182,33 @@ def quantize_nvfp4(x: torch.Tensor, *, group_offsets=None, num_groups: int = 1,
                                     _ptr(part), _ptr(ws), ws.numel(), _stream(stream)),
            "quantize_nvfp4")
     return QTensor(codes, scales, ts, rows, cols, scale_layout), part
+
+
+def qdq_nvfp4(x: torch.Tensor, *, group_offsets=None, num_groups: int = 1,
+              tensor_scale_in=None, want_codes: bool = False, scale_layout: int = LINEAR,
+              workspace=None, out=None, stream=None):
+    """W4A16 fake quantization: -> (y bf16 = DQ(Q(x)), QTensor of the codes or None)."""
+    lib = load()
+    assert x.dtype == torch.bfloat16 and x.dim() == 2
+    rows, cols = x.shape
+    G = num_groups if group_offsets is not None else 1
+    dev = x.device
+    y = out if out is not None else torch.empty((rows, cols), dtype=torch.bfloat16, device=dev)
+    codes = scales = None
+    if want_codes:
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+        nsf = sf_tc_bytes(rows, cols) if scale_layout == TCGEN05 else rows * (cols // 16)
+        scales = torch.empty(nsf, dtype=torch.uint8, device=dev)
+    ts = torch.empty(G, dtype=torch.float32, device=dev)
+    ws = None
+    if tensor_scale_in is None:
+        ws = _workspace(workspace_size(OP_QUANTIZE, rows, cols, 0, 0, G), dev, workspace)
+    _check(lib.quads_qdq_nvfp4(
+        _ptr(x), rows, cols, x.stride(0), _ptr(group_offsets), G, _ptr(tensor_scale_in), _ptr(y),
+        y.stride(0), _ptr(codes), cols // 2, _ptr(scales), scale_layout, _ptr(ts), _ptr(ws),
+        ws.numel() if ws is not None else 0, _stream(stream)), "qdq_nvfp4")
+    q = QTensor(codes, scales, ts, rows, cols, scale_layout) if want_codes else None
+    return y, q
 
 
 def _event(ev, stream):

@@ -213,3 +213,26 @@ def quantize_full(x: np.ndarray, k: int, group_offsets=None, tensor_scales=None)
     rcodes, rscales, rst = quantize_residual_slice(R, sel, group_offsets)
     return dict(codes=codes, scales=scales, s_t=st, R=R, scores=scores, sel=sel,
                 r_codes=rcodes, r_scales=rscales, r_s_t=rst)
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit pattern (uint16), rounded to nearest, ties to even."""
+    b = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((b + np.uint64(0x7FFF) + ((b >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)).astype(np.uint16)
+
+
+def qdq(x: np.ndarray, group_offsets=None, tensor_scales=None):
+    """Trainer-side W4A16 fake quantization ([QUADS] 2.2 A, asymmetric QAT; 2.1
+    "Weights": the trainer applies the rollout's quantize-dequantize path).
+    Per row group: the NVFP4 codes and scales of `quantize`, their dequantized
+    values fl(level * d_b) (`dequantize`), rounded to bf16.
+
+    Returns (bf16 bits uint16 [rows, cols], codes, scale bytes, s_t [G])."""
+    x = np.asarray(x, dtype=np.float32)
+    rows, cols = x.shape
+    codes, scales, st = quantize_groups(x, group_offsets, tensor_scales)
+    dq = np.zeros((rows, cols), np.float32)
+    for g, (a, b) in enumerate(group_bounds(rows, group_offsets)):
+        if b > a:
+            dq[a:b] = dequantize(codes[a:b], scales[a:b], st[g])
+    return bf16_bits(dq), codes, scales, st

@@ -192,3 +192,43 @@ def test_block_scale_encoding_exhaustive(lib):
     oc, osc = Q.quantize(f32(bits), np.float32(1.0))
     assert np.array_equal(linear_scales(q), osc)
     assert np.array_equal(codes_np(q.codes, 16), oc)
+
+
+@pytest.mark.parametrize("name", ["single_linear", "ragged", "edge", "zeros"])
+def test_w4a16_qdq_bit_exact(lib, name):
+    """Trainer-side fake quantization: bf16 output, codes and scales bit for bit."""
+    bits = _case(name)
+    rows, cols = bits.shape
+    x = bf16_tensor(bits)
+    y, q = lib.qdq_nvfp4(x, want_codes=True)
+    y_only, _ = lib.qdq_nvfp4(x)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    oy, oc, osc, ost = Q.qdq(f32(bits))
+    got = y.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, oy)
+    assert torch.equal(y, y_only)
+    assert q.tensor_scale.cpu().numpy()[0] == ost[0]
+    assert np.array_equal(codes_np(q.codes, cols), oc)
+    assert np.array_equal(linear_scales(q), osc)
+
+
+def test_w4a16_qdq_per_expert_groups_and_given_scale(lib):
+    """Expert-stacked weights (one tensor scale per expert) and a given scale."""
+    rng = inputs.make_rng(21)
+    w = rng.standard_normal((3 * 128, 192), dtype=np.float32) * np.float32(0.02)
+    w[128:256] *= np.float32(7.0)
+    bits = inputs.f32_to_bf16_bits(w)
+    offs = np.array([0, 128, 256, 384], np.int32)
+    x = bf16_tensor(bits)
+    y, q = lib.qdq_nvfp4(x, group_offsets=torch.from_numpy(offs).cuda(), num_groups=3,
+                         want_codes=True, scale_layout=1)
+    ts = torch.tensor([2.0 ** -9], dtype=torch.float32, device="cuda")
+    y2, _ = lib.qdq_nvfp4(x, tensor_scale_in=ts)
+    torch.cuda.synchronize()
+    oy, oc, osc, ost = Q.qdq(f32(bits), group_offsets=offs)
+    assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), oy)
+    assert np.array_equal(q.tensor_scale.cpu().numpy(), ost)
+    assert np.array_equal(linear_scales(q), osc)
+    oy2 = Q.qdq(f32(bits), tensor_scales=[2.0 ** -9])[0]
+    assert np.array_equal(y2.view(torch.int16).cpu().numpy().view(np.uint16), oy2)
