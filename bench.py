@@ -257,7 +257,19 @@ def secondary(torch, Q, steps, flush, stream):
     tb = xt.numel() * (2 + 0.5 + 0.5 + 1.0 / 16)
     out["trace_16384x2048"] = {"ms": round(ms, 4), "gbs": round(tb / (ms * 1e-3) / 1e9, 1),
                                "algorithmic_bytes": int(tb)}
-    del xr, xt, rq, codes
+    # mantissa-only mode: pack the 1.5-bit record, then round from it
+    bits = Q.trace_pack_record(rq)
+    cnt1 = torch.zeros(2, dtype=torch.int64, device="cuda")
+    ms_p = graph_ms(lambda: Q.trace_pack_record(rq, out=bits, stream=stream))
+    ms_r = graph_ms(lambda: Q.trace_round_1bit(xt, bits, rq, counters=cnt1, out=codes,
+                                               stream=stream))
+    n = xt.numel()
+    pb, rb = n * (0.5 + 1.0 / 8), n * (2 + 1.0 / 8 + 1.0 / 16 + 0.5)
+    out["trace_1bit_16384x2048"] = {
+        "pack_ms": round(ms_p, 4), "pack_gbs": round(pb / (ms_p * 1e-3) / 1e9, 1),
+        "round_ms": round(ms_r, 4), "gbs": round(rb / (ms_r * 1e-3) / 1e9, 1),
+        "algorithmic_bytes": int(rb), "record_bits_per_value": 1.5}
+    del xr, xt, rq, codes, bits
 
     # trainer-side W4A16 fake quantization of the 128 experts' gate/up weights
     # (one tensor scale per expert; codes and scales written for the rollout copy)
@@ -430,6 +442,8 @@ def run_gpu(args):
         dec["frac_hbm"] = round(dec["weight_bytes"] / (dec["ms"] * 1e-3) / 1e9 / pk["hbm"], 4)
         tr = sec["trace_16384x2048"]
         tr["frac_hbm"] = round(tr["gbs"] / pk["hbm"], 4)
+        t1 = sec["trace_1bit_16384x2048"]
+        t1["frac_hbm"] = round(t1["gbs"] / pk["hbm"], 4)
         wq = sec["w4a16_qdq_w1"]
         wq["frac_hbm"] = round(wq["gbs"] / pk["hbm"], 4)
     fl = moe_flops()

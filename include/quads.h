@@ -396,6 +396,48 @@ quads_status_t quads_trace_round(const void* x_train, int64_t rows, int64_t cols
                                  unsigned long long* counters, void* stream);
 
 /*
+ * quads_trace_pack_record -- the compact rollout record of TRACE's
+ * mantissa-only mode ([TRACE] "核心方法" second innovation, "方法步骤详情"
+ * step 2): of each rollout E2M1 code only its mantissa bit (the low bit of the
+ * magnitude) is kept; with the E4M3 block scales (kept as they are, 8 bits per
+ * 16 values) the record costs 1.5 bits per value.
+ *
+ *   rollout_codes [rows, ld_codes] packed codes (4-byte aligned, ld_codes >=
+ *     cols/2, multiple of 4).
+ *   mantissa_bits [rows, ld_bits] bytes (ld_bits >= cols/8): bit j of byte i of
+ *     a row is the mantissa bit of element 8i+j.
+ * cols % 16 == 0, rows * cols / 8 < 2^31.
+ */
+quads_status_t quads_trace_pack_record(const uint8_t* rollout_codes, int64_t rows, int64_t cols,
+                                       int64_t ld_codes, uint8_t* mantissa_bits, int64_t ld_bits,
+                                       void* stream);
+
+/*
+ * quads_trace_round_1bit -- TRACE rounding from the 1-bit record: v = x_train *
+ * (1/d_b) under the rollout block's d_b; of the two neighbouring signed E2M1
+ * levels of v (clamped to +-6) pick the one whose mantissa bit equals the
+ * record's -- adjacent levels have opposite mantissa bits, so this is the
+ * rollout's code whenever that code is one of the two neighbours, the
+ * off-by-one case that makes one bit enough ([TRACE] "核心方法": over 99% of
+ * mismatched values differ by one adjacent code).  v on a level has that level
+ * alone; a zero result takes the sign of v; a rollout block with d_b == 0
+ * gives 0x0.
+ *
+ *   x_train [rows, cols] bf16 (ldx, 16-byte aligned); mantissa_bits as written
+ *   by quads_trace_pack_record; rollout_scales LINEAR [rows, cols/16];
+ *   rollout_tensor_scale device [1]; codes_out [rows, ld_codes] (4-byte aligned).
+ *   counters nullable device uint64 [2], ADDED to: #(result != RTN code under
+ *   the rollout scale), #(result's mantissa bit != record bit).
+ * cols % 16 == 0, rows * cols / 8 < 2^31.
+ */
+quads_status_t quads_trace_round_1bit(const void* x_train, int64_t rows, int64_t cols,
+                                      int64_t ldx, const uint8_t* mantissa_bits, int64_t ld_bits,
+                                      const uint8_t* rollout_scales,
+                                      const float* rollout_tensor_scale, uint8_t* codes_out,
+                                      int64_t ld_codes, unsigned long long* counters,
+                                      void* stream);
+
+/*
  * quads_moe_route -- router top-k and the token -> expert dispatch plan
  * ([TRACE] "MoE 专家路由敏感性").  Per token: the topk largest logits (ties ->
  * lower expert id), kept in ascending expert order; gate = exp(l - lmax) /

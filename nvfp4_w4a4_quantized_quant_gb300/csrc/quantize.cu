@@ -545,6 +545,88 @@ __global__ void __launch_bounds__(256) trace_kernel(
   }
 }
 
+// ---------------------------------------------------------------- TRACE records
+// Compact rollout record ([TRACE] "核心方法", "方法步骤详情" step 2): of each
+// rollout code only its mantissa bit (the low bit of the 3 magnitude bits) is
+// kept, 8 per byte, element 8i+j in bit j of byte i; with the E4M3 block scale
+// (8 bits per 16 values) that is the pages' 1.5 bits per value.
+// One thread per 8 codes: a 4-byte read, a 1-byte write.
+__global__ void __launch_bounds__(256) trace_pack_kernel(const uint8_t* __restrict__ codes,
+                                                         int64_t rows, int cols, int64_t ldc,
+                                                         uint8_t* __restrict__ bits,
+                                                         int64_t ldb) {
+  const uint32_t per_row = (uint32_t)cols >> 3;
+  const uint32_t total = (uint32_t)(rows * per_row);   // < 2^31 (host check)
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const uint32_t r = i / per_row, v = i - r * per_row;
+    const uint32_t c = __ldg(reinterpret_cast<const uint32_t*>(codes + (int64_t)r * ldc) + v);
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m |= ((c >> (4 * j)) & 1u) << j;
+    bits[(int64_t)r * ldb + v] = (uint8_t)m;
+  }
+}
+
+// Rounding guided by the 1-bit record: of the two E2M1 neighbours of v =
+// x_train / d_b (rollout scale), adjacent levels have opposite mantissa bits,
+// so the record bit names one of them -- the rollout's own code whenever it
+// is one of the two (the off-by-one case the pages find in over 99% of
+// mismatches).  A v on a level (or clamped at +-6) has that level alone.
+// Counters (nullable, added to): #(result != RTN code), #(result's mantissa
+// bit != record bit).
+__global__ void __launch_bounds__(256) trace_1bit_kernel(
+    const __nv_bfloat16* __restrict__ xt, int64_t rows, int cols, int64_t ldx,
+    const uint8_t* __restrict__ mbits, int64_t ldb, const uint8_t* __restrict__ rscales,
+    const float* __restrict__ rst, uint8_t* __restrict__ out, int64_t ldc,
+    unsigned long long* __restrict__ counters) {
+  const uint32_t vec_per_row = (uint32_t)cols >> 3;
+  const uint32_t total = (uint32_t)(rows * vec_per_row);   // < 2^31 (host check)
+  const float s_t = rst[0];
+  unsigned int n_chg = 0, n_bit = 0;
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const uint32_t r = i / vec_per_row;
+    const uint32_t vi = i - r * vec_per_row;
+    const int col = (int)vi * 8;
+    float f[8];
+    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(xt + (int64_t)r * ldx + col)), f);
+    const uint32_t mb = __ldg(mbits + (int64_t)r * ldb + vi);
+    const BlockScale bs =
+        block_scale_from_byte(__ldg(rscales + (int64_t)r * (cols >> 4) + (col >> 4)), s_t);
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(f[j], bs.r);
+    const uint32_t rtn = bs.zero ? 0u : f32x8_to_e2m1(v);
+    float qn[8];
+    e2m1x8_to_f32(rtn, qn);
+    uint32_t outw = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int sn = signed_index((rtn >> (4 * j)) & 15u);
+      const float vc = fminf(fmaxf(v[j], -6.0f), 6.0f);
+      const int ilo = sn - (qn[j] > vc ? 1 : 0);
+      const int ihi = sn + (qn[j] < vc ? 1 : 0);
+      const int bit = (int)((mb >> j) & 1u);
+      const int stc = bs.zero ? 0 : ((abs(ilo) & 1) == bit ? ilo : ihi);
+      const bool neg = !bs.zero && (stc < 0 || (stc == 0 && signbit(v[j])));
+      outw |= ((uint32_t)abs(stc) | (neg ? 8u : 0u)) << (4 * j);
+      n_chg += stc != sn ? 1u : 0u;
+      n_bit += (abs(stc) & 1) != bit ? 1u : 0u;
+    }
+    *reinterpret_cast<uint32_t*>(out + (int64_t)r * ldc + (col >> 1)) = outw;
+  }
+  if (counters) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      n_chg += __shfl_xor_sync(0xffffffffu, n_chg, o);
+      n_bit += __shfl_xor_sync(0xffffffffu, n_bit, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+      if (n_chg) atomicAdd(&counters[0], (unsigned long long)n_chg);
+      if (n_bit) atomicAdd(&counters[1], (unsigned long long)n_bit);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- host side
 static int grid_for(int64_t work_items, int per_block, int max_blocks_per_sm = 8) {
   int64_t b = (work_items + per_block - 1) / per_block;
@@ -736,4 +818,45 @@ extern "C" quads_status_t quads_trace_round(const void* x_train, int64_t rows, i
       (const __nv_bfloat16*)x_train, rows, (int)cols, ldx, rollout_codes, ld_codes,
       rollout_scales, rollout_tensor_scale, codes_out, counters);
   return check_launch("trace_round", 1);
+}
+
+extern "C" quads_status_t quads_trace_pack_record(const uint8_t* rollout_codes, int64_t rows,
+                                                  int64_t cols, int64_t ld_codes,
+                                                  uint8_t* mantissa_bits, int64_t ld_bits,
+                                                  void* stream) {
+  if (!rollout_codes || !mantissa_bits)
+    return fail(QUADS_ERR_INVALID_ARG, "trace_pack_record: null pointer argument");
+  if (rows < 0 || cols <= 0 || cols % 16 || ld_codes < cols / 2 || ld_codes % 4 ||
+      ld_bits < cols / 8)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "trace_pack_record: cols %% 16, ld_codes >= cols/2 (%% 4), ld_bits >= cols/8");
+  if (((uintptr_t)rollout_codes & 3u) != 0)
+    return fail(QUADS_ERR_MISALIGNED, "trace_pack_record: rollout_codes must be 4-byte aligned");
+  if (rows * (cols / 8) >= ((int64_t)1 << 31))
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "trace_pack_record: rows * cols / 8 must be < 2^31");
+  if (rows == 0) return QUADS_OK;
+  trace_pack_kernel<<<grid_for(rows * (cols / 8), 256), 256, 0, (cudaStream_t)stream>>>(
+      rollout_codes, rows, (int)cols, ld_codes, mantissa_bits, ld_bits);
+  return check_launch("trace_pack_record", 1);
+}
+
+extern "C" quads_status_t quads_trace_round_1bit(const void* x_train, int64_t rows, int64_t cols,
+                                                 int64_t ldx, const uint8_t* mantissa_bits,
+                                                 int64_t ld_bits, const uint8_t* rollout_scales,
+                                                 const float* rollout_tensor_scale,
+                                                 uint8_t* codes_out, int64_t ld_codes,
+                                                 unsigned long long* counters, void* stream) {
+  if (!x_train || !mantissa_bits || !rollout_scales || !rollout_tensor_scale || !codes_out)
+    return fail(QUADS_ERR_INVALID_ARG, "trace_round_1bit: null pointer argument");
+  if (rows < 0 || cols <= 0 || cols % 16 || ld_bits < cols / 8 || ld_codes < cols / 2 ||
+      ld_codes % 4)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "trace_round_1bit: cols %% 16, ld_bits >= cols/8, ld_codes >= cols/2 (%% 4)");
+  if (ldx < cols || ldx % 8 || !aligned16(x_train) || ((uintptr_t)codes_out & 3u) != 0)
+    return fail(QUADS_ERR_MISALIGNED, "trace_round_1bit: x_train 16-byte aligned (ldx >= cols, %% 8), codes_out 4-byte aligned");
+  if (rows * (cols / 8) >= ((int64_t)1 << 31))
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "trace_round_1bit: rows * cols / 8 must be < 2^31");
+  if (rows == 0) return QUADS_OK;
+  trace_1bit_kernel<<<grid_for(rows * (cols / 8), 256), 256, 0, (cudaStream_t)stream>>>(
+      (const __nv_bfloat16*)x_train, rows, (int)cols, ldx, mantissa_bits, ld_bits,
+      rollout_scales, rollout_tensor_scale, codes_out, ld_codes, counters);
+  return check_launch("trace_round_1bit", 1);
 }

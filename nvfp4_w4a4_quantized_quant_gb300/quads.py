@@ -51,6 +51,8 @@ _SIGS = {
     "quads_select_weight_channels": (_I32, [_I32, _I64, _I64, _P, _P, _P, _I32, _I32, _P, _P,
                                             _P]),
     "quads_trace_round": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _P, _P]),
+    "quads_trace_pack_record": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P]),
+    "quads_trace_round_1bit": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _I64, _P, _P]),
     "quads_moe_route": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _I64, _P, _SZ, _P]),
     "quads_moe_gather": (_I32, [_P, _P, _I32, _I64, _I64, _P, _P, _P, _P, _P]),
     "quads_moe_combine": (_I32, [_P, _I64, _P, _P, _I32, _I32, _I64, _P, _I64, _P]),
@@ -348,6 +350,38 @@ def trace_round(x_train: torch.Tensor, rollout: QTensor, *, counters=None, out=N
                                  _ptr(rollout.codes), rollout.codes.stride(0),
                                  _ptr(rollout.scales), _ptr(rollout.tensor_scale), _ptr(codes),
                                  _ptr(counters), _stream(stream)), "trace_round")
+    return codes, counters
+
+
+def trace_pack_record(rollout: QTensor, *, out=None, stream=None) -> torch.Tensor:
+    """Mantissa bits of the rollout codes, [rows, cols/8] bytes (element 8i+j in bit j)."""
+    lib = load()
+    rows, cols = rollout.rows, rollout.cols
+    bits = out if out is not None else torch.empty((rows, cols // 8), dtype=torch.uint8,
+                                                   device=rollout.codes.device)
+    _check(lib.quads_trace_pack_record(_ptr(rollout.codes), rows, cols, rollout.codes.stride(0),
+                                       _ptr(bits), bits.stride(0), _stream(stream)),
+           "trace_pack_record")
+    return bits
+
+
+def trace_round_1bit(x_train: torch.Tensor, mantissa_bits: torch.Tensor, rollout: QTensor, *,
+                     counters=None, out=None, stream=None):
+    """-> (codes [rows, cols/2], counters int64 [2]: changed vs RTN, record-bit mismatches).
+    Uses the rollout's LINEAR scales and tensor scale; its codes are not read."""
+    lib = load()
+    rows, cols = x_train.shape
+    if rollout.layout != LINEAR:
+        raise QuadsError("trace_round_1bit takes LINEAR rollout scales")
+    codes = out if out is not None else torch.empty((rows, cols // 2), dtype=torch.uint8,
+                                                    device=x_train.device)
+    if counters is None:
+        counters = torch.zeros(2, dtype=torch.int64, device=x_train.device)
+    _check(lib.quads_trace_round_1bit(_ptr(x_train), rows, cols, x_train.stride(0),
+                                      _ptr(mantissa_bits), mantissa_bits.stride(0),
+                                      _ptr(rollout.scales), _ptr(rollout.tensor_scale),
+                                      _ptr(codes), codes.stride(0), _ptr(counters),
+                                      _stream(stream)), "trace_round_1bit")
     return codes, counters
 
 

@@ -89,3 +89,45 @@ def cross_path_difference(codes_a, codes_b, scales, s_t) -> float:
     da = e2m1_decode(codes_a).reshape(d_b.shape[0], -1, BLOCK) * d_b[:, :, None]
     db = e2m1_decode(codes_b).reshape(d_b.shape[0], -1, BLOCK) * d_b[:, :, None]
     return float(np.sqrt(np.sum((da - db) ** 2)))
+
+
+def _mantissa(q: np.ndarray) -> np.ndarray:
+    """Mantissa bit of an E2M1 value: the low bit of its magnitude code."""
+    return (np.searchsorted(E2M1_LEVELS, np.abs(q)) & 1).astype(np.uint8)
+
+
+def pack_record(rollout_codes) -> np.ndarray:
+    """[TRACE] "核心方法" / "方法步骤详情" step 2: the compact record keeps one
+    mantissa bit per value (plus the block scales, kept as they are).
+    Returns bytes [rows, cols/8], element 8i+j in bit j of byte i."""
+    c = np.asarray(rollout_codes, dtype=np.uint8)
+    rows, cols = c.shape
+    m = (c & 1).reshape(rows, cols // 8, 8).astype(np.uint16)
+    return (m << np.arange(8, dtype=np.uint16)).sum(axis=2).astype(np.uint8)
+
+
+def unpack_record(bits, cols: int) -> np.ndarray:
+    b = np.asarray(bits, dtype=np.uint8)[:, : cols // 8]
+    return ((b[:, :, None] >> np.arange(8, dtype=np.uint8)) & 1).reshape(b.shape[0], cols)
+
+
+def trace_round_1bit(x_train, mantissa_bits, rollout_scales, s_t):
+    """TRACE with the 1-bit record: of the neighbours {q-, q+} of v take the one
+    whose mantissa bit equals the record's (adjacent signed E2M1 levels have
+    opposite mantissa bits, so one bit names one of them -- the rollout's code
+    whenever it is a neighbour; "核心方法": over 99% of mismatches are one code
+    apart).  Same v, clamping, zero sign and zero-block rules as trace_round.
+
+    Returns (codes uint8 [rows, cols], counters dict: changed vs RTN,
+    record-bit mismatches)."""
+    v, zero_el = _scaled(x_train, rollout_scales, s_t)
+    rows, cols = v.shape
+    bit = unpack_record(mantissa_bits, cols)
+    q_lo, q_hi = neighbours(v)
+    pick_lo = (q_lo == q_hi) | (_mantissa(q_lo) == bit)
+    q = np.where(pick_lo, q_lo, q_hi)
+    codes = np.where(zero_el, np.uint8(0), _value_to_code(q, v)).astype(np.uint8)
+    q_rtn = e2m1_decode(np.where(zero_el, np.uint8(0), e2m1_encode(v)))
+    q_out = e2m1_decode(codes)
+    return codes, dict(changed=int((q_out != q_rtn).sum()),
+                       bit_mismatch=int((_mantissa(q_out) != bit).sum()))

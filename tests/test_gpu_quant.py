@@ -232,3 +232,35 @@ def test_w4a16_qdq_per_expert_groups_and_given_scale(lib):
     assert np.array_equal(linear_scales(q), osc)
     oy2 = Q.qdq(f32(bits), tensor_scales=[2.0 ** -9])[0]
     assert np.array_equal(y2.view(torch.int16).cpu().numpy().view(np.uint16), oy2)
+
+
+@pytest.mark.parametrize("rows,cols", [(64, 256), (389, 320), (16384, 2048)])
+def test_trace_record_and_1bit_round_bit_exact(lib, rows, cols):
+    """Mantissa-only record and the rounding it guides, against the oracle; the
+    16384x2048 case is the benchmark's TRACE workload."""
+    d = inputs.trace_rounding(1, rows, cols)
+    xr, xt = bf16_tensor(d["x_rollout"]), bf16_tensor(d["x_train"])
+    rq, _ = lib.quantize_nvfp4(xr)
+    bits = lib.trace_pack_record(rq)
+    codes, cnt = lib.trace_round_1bit(xt, bits, rq)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    xrf, xtf = f32(d["x_rollout"]), f32(d["x_train"])
+    rc, rs, st = Q.quantize_groups(xrf)
+    obits = T.pack_record(rc)
+    assert np.array_equal(bits.cpu().numpy(), obits)
+    oc, ocnt = T.trace_round_1bit(xtf, obits, rs, st[0])
+    assert np.array_equal(codes_np(codes, cols), oc)
+    assert cnt.cpu().numpy().tolist() == [ocnt["changed"], ocnt["bit_mismatch"]]
+
+
+def test_trace_1bit_worked_example_on_gpu(lib):
+    xr = np.zeros((1, 16), np.float32)
+    xr[0, 0], xr[0, 1] = 59.75, 144.0
+    xt = xr.copy()
+    xt[0, 0] = 60.25
+    rq, _ = lib.quantize_nvfp4(bf16_tensor(inputs.f32_to_bf16_bits(xr)))
+    bits = lib.trace_pack_record(rq)
+    codes, cnt = lib.trace_round_1bit(bf16_tensor(inputs.f32_to_bf16_bits(xt)), bits, rq)
+    assert F.e2m1_decode(codes_np(codes, 16)[0, 0]) == 2.0
+    assert cnt.cpu().tolist() == [1, 0]

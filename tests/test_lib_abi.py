@@ -90,6 +90,16 @@ def test_host_side_argument_checks_need_no_gpu(lib):
     assert st == 1                                   # no selection
     st = lib.quads_trace_round(p, 4, 24, 24, p, 12, p, p, p, None, None)
     assert st == 2
+    st = lib.quads_trace_pack_record(p, 4, 24, 12, p, 3, None)
+    assert st == 2                                   # cols % 16
+    st = lib.quads_trace_pack_record(p, 4, 32, 16, p, 3, None)
+    assert st == 2                                   # ld_bits < cols / 8
+    st = lib.quads_trace_round_1bit(p, 4, 32, 24, p, 4, p, p, p, 16, None, None)
+    assert st == 3                                   # ldx < cols
+    st = lib.quads_qdq_nvfp4(p, 4, 32, 32, None, 1, p, None, 32, None, 16, None, 0, p, None, 0, None)
+    assert st == 1                                   # null y
+    st = lib.quads_qdq_nvfp4(p, 4, 32, 32, None, 1, p, p, 24, None, 16, None, 0, p, None, 0, None)
+    assert st == 3                                   # ldy < cols
 
 
 def test_product_path_never_imports_the_oracle():
