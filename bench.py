@@ -227,7 +227,20 @@ def secondary(torch, Q, steps, flush, stream):
     dense["overhead_pct"] = round(100.0 * (dense["comp"]["ms"] / dense["plain"]["ms"] - 1.0), 1)
     dense["shape"] = {"M": M, "K": K, "N": N, "k": k, "y": "bf16"}
     out["dense_projection"] = dense
-    del x, w
+
+    # MXFP4 variant on the same shapes: quantizer of X, plain W4A4 GEMM
+    wx, _ = Q.mx_quantize(w, scale_layout=Q.TCGEN05)
+    ax, _ = Q.mx_quantize(x, scale_layout=Q.TCGEN05)
+    ymx = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    ms_q = graph_ms(lambda: Q.mx_quantize(x, scale_layout=Q.TCGEN05, out=(ax.codes, ax.scales),
+                                          stream=stream))
+    ms_g = graph_ms(lambda: Q.mx_gemm(ax, wx, out=ymx, stream=stream))
+    qb = M * K * (2 + 0.5 + 1.0 / 32)
+    out["mxfp4_dense_projection"] = {
+        "quantize_ms": round(ms_q, 4), "quantize_gbs": round(qb / (ms_q * 1e-3) / 1e9, 1),
+        "gemm_ms": round(ms_g, 4), "gemm_tflops": round(2.0 * M * N * K / (ms_g * 1e-3) / 1e12, 1),
+        "shape": {"M": M, "K": K, "N": N, "y": "bf16"}}
+    del x, w, wx, ax, ymx
 
     wl = dict(WORKLOAD, tokens=512)
     dd = inputs.moe_layer(0, tokens=512, hidden=wl["hidden"], experts=wl["experts"], topk=wl["topk"],

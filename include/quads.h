@@ -438,6 +438,51 @@ quads_status_t quads_trace_round_1bit(const void* x_train, int64_t rows, int64_t
                                       void* stream);
 
 /*
+ * MXFP4 variant ([TRACE] "技术新颖性", "实验结果": the method also runs on
+ * MXFP4 W4A4 / W4A8 rollouts).  The pages do not define the format; these calls
+ * follow the OCP microscaling definition: blocks of 32 consecutive elements of
+ * a row share a power-of-two scale 2^e stored as an E8M0 byte (e + 127), with
+ * e = floor(log2(block max)) - 2 clamped to >= -127; elements are the E2M1
+ * codes (round to nearest even, saturating at +-6) of x / 2^e.  No tensor
+ * scale.  The residual compensation stays NVFP4-only.
+ *
+ * quads_mx_quantize -- x [rows, cols] bf16 (ldx; 16-byte aligned) -> codes
+ *   [rows, ld_codes] (8-byte aligned, ld_codes >= cols/2, multiple of 8) and
+ *   E8M0 scale bytes: LINEAR [rows, cols/32] or TCGEN05 (the same 128-row x
+ *   4-column atoms as NVFP4, a column being a 32-element block; cols % 128;
+ *   padding rows 0).  y_qdq nullable: bf16 [rows, ldy] = level * 2^e (the
+ *   trainer's fake quantization in this format).
+ *   cols % 32 == 0, rows * cols / 16 < 2^31.
+ */
+quads_status_t quads_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                                 uint8_t* codes, int64_t ld_codes, uint8_t* scales,
+                                 int32_t scale_layout, void* y_qdq, int64_t ldy, void* stream);
+
+/*
+ * quads_mx_gemm -- Y = DQ(A) DQ(W)^T for MXFP4 operands on the block-scaled
+ * tensor cores (tcgen05.mma kind::mxf4, E8M0 scales, float32 accumulation).
+ *   a_codes [M, K/2], a_scales TCGEN05 (ceil(M/128)*128 rows); w_codes [N, K/2],
+ *   w_scales TCGEN05; y [M, ldy] float32 or bf16 (y_dtype).
+ *   M >= 1, N % 128 == 0, K % 128 == 0; operands 16-byte aligned.
+ */
+quads_status_t quads_mx_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* a_codes,
+                             const uint8_t* a_scales, const uint8_t* w_codes,
+                             const uint8_t* w_scales, void* y, int32_t y_dtype, int64_t ldy,
+                             void* stream);
+
+/*
+ * quads_trace_round_mx -- TRACE rounding (as quads_trace_round) under an MXFP4
+ * rollout: v = x_train / 2^e with the rollout block's E8M0 scale
+ * (rollout_scales LINEAR [rows, cols/32]); codes 4-byte aligned.  counters
+ * nullable device uint64 [3] as in quads_trace_round.
+ *   cols % 32 == 0, rows * cols / 8 < 2^31.
+ */
+quads_status_t quads_trace_round_mx(const void* x_train, int64_t rows, int64_t cols, int64_t ldx,
+                                    const uint8_t* rollout_codes, int64_t ld_codes,
+                                    const uint8_t* rollout_scales, uint8_t* codes_out,
+                                    unsigned long long* counters, void* stream);
+
+/*
  * quads_moe_route -- router top-k and the token -> expert dispatch plan
  * ([TRACE] "MoE 专家路由敏感性").  Per token: the topk largest logits (ties ->
  * lower expert id), kept in ascending expert order; gate = exp(l - lmax) /

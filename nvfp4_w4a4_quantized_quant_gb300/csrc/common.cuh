@@ -146,6 +146,22 @@ __device__ __forceinline__ BlockScale block_scale_from_byte(uint32_t byte, float
   return b;
 }
 
+// MXFP4 block scale (OCP microscaling): 2^e with e = floor(log2 m) - 2 for the
+// 32-block maximum m (2 = exponent of the largest E2M1 level), clamped at
+// -127, stored as the E8M0 byte e + 127.  From the float's exponent field:
+// floor(log2 m) = field - 127 for normal m; m below 2^-125 (field < 2) clamps.
+__device__ __forceinline__ uint32_t e8m0_scale_byte(float m) {
+  const uint32_t field = (__float_as_uint(m) >> 23) & 0xFFu;
+  return field >= 2u ? field - 2u : 0u;
+}
+// 2^e and 2^-e of an E8M0 byte (e in [-127, 125] here: both are floats).
+__device__ __forceinline__ float e8m0_value(uint32_t byte) {
+  return byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);
+}
+__device__ __forceinline__ float e8m0_inverse(uint32_t byte) {
+  return __uint_as_float((254u - byte) << 23);
+}
+
 // Quantize 8 values of one block: returns packed codes; writes levels*d residuals
 // when want_residual.
 __device__ __forceinline__ uint32_t quantize8(const float* x, const BlockScale& bs) {

@@ -94,6 +94,7 @@ struct Params {
   const float* r_ts;
   int a_ts_pe, r_ts_pe;
   int comp;
+  int mx;                       // MXFP4 operands: E8M0 scale per 32 elements, no tensor scales
   void* y;
   int64_t ldy;
   int out_mode;
@@ -235,6 +236,13 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
   return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// MXFP4: E8M0 scales (instruction-descriptor bit 23); each 32-bit TMEM scale
+// word holds four 32-element block scales, the scale-factor id (byte 0 or 2,
+// bits 29-30 for A and 4-5 for B) picks the pair a K=64 MMA uses.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, uint32_t sf_id) {
+  return idesc_nvf4(M, N) | (1u << 23) | (sf_id << 29) | (sf_id << 4);
+}
+
 // The same MMA executed by the whole (converged) warp, issued by one elected lane.
 __device__ __forceinline__ void tc_mma_el(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                           uint32_t sfa, uint32_t sfb, uint32_t acc) {
@@ -243,6 +251,16 @@ __device__ __forceinline__ void tc_mma_el(uint32_t d, uint64_t a, uint64_t b, ui
       "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb));
+}
+__device__ __forceinline__ void tc_mma_mx_el(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                             uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X"
       " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb));
 }
@@ -361,8 +379,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
-    const float bts = p.b_ts[e];
-    meta.a1[e] = __fmul_rn(p.a_ts[p.a_ts_pe ? e : 0], bts);
+    const float bts = p.mx ? 1.0f : p.b_ts[e];
+    meta.a1[e] = p.mx ? 1.0f : __fmul_rn(p.a_ts[p.a_ts_pe ? e : 0], bts);
     meta.a2[e] = p.comp ? __fmul_rn(p.r_ts[p.r_ts_pe ? e : 0], bts) : 0.0f;
     if (p.row_off) {
       meta.off[e] = p.row_off[e];
@@ -393,7 +411,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int64_t ntiles = total_tiles(p, meta);
   const int KT = (p.K + KTILE - 1) / KTILE;
   const int KTc = p.comp ? (p.kpad + KTILE - 1) / KTILE : 0;
-  const int64_t a_sf_rb = (int64_t)(p.K / 64) * 512;    // bytes per 128-row block
+  // scale bytes per 128-row block and per stage (MXFP4: one scale per 32 elements)
+  const int64_t a_sf_rb = (int64_t)(p.K / (p.mx ? 128 : 64)) * 512;
+  const int sf_stage = p.mx ? SF_TILE / 2 : SF_TILE;
   const int64_t r_sf_rb = (int64_t)(p.kpad / 64) * 512;
 
   if (warp < PRODUCERS) {
@@ -430,9 +450,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (elect_one()) {
           for (int b = b_lo; b < b_hi; ++b) {
             if (b >= BOXES) {
-              mbar_expect_tx(&full[s], ksteps * 512);
-              if (b == BOXES) bulk_load(st + A_TILE + B_TILE, sfa + kk * SF_TILE, ksteps * 512, &full[s]);
-              else bulk_load(st + A_TILE + B_TILE + SF_TILE, sfb + kk * SF_TILE, ksteps * 512, &full[s]);
+              const uint32_t sfbytes = (p.mx ? ksteps / 2 : ksteps) * 512;
+              mbar_expect_tx(&full[s], sfbytes);
+              if (b == BOXES) bulk_load(st + A_TILE + B_TILE, sfa + kk * sf_stage, sfbytes, &full[s]);
+              else bulk_load(st + A_TILE + B_TILE + SF_TILE, sfb + kk * sf_stage, sfbytes, &full[s]);
               continue;
             }
             const int u = b >> 2, isb = (b >> 1) & 1, hf = b & 1;
@@ -490,10 +511,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t sbb = sa + A_TILE;
         const uint32_t tsf = tmem + SF_COL + sb * SF_BUF_COLS;
         const uint32_t dcol = corr ? (tmem + ACC2_COL) : (tmem + b * BN);
-        for (int q = 0; q < ksteps; ++q) {
-          const uint32_t off = (q >> 2) * A_SUB + (q & 3) * 32;
-          tc_mma_el(dcol, desc_sw128(sa + off), desc_sw128(sbb + off), idesc, tsf + q * 4,
-                    tsf + 4 * KSTEPS + q * 4, (kk > 0 || q > 0) ? 1u : 0u);
+        if (p.mx) {
+          for (int q = 0; q < ksteps; ++q) {
+            const uint32_t off = (q >> 2) * A_SUB + (q & 3) * 32;
+            const uint32_t id = (q & 1) ? idesc_mxf4(BM, BN, 2) : idesc_mxf4(BM, BN, 0);
+            tc_mma_mx_el(dcol, desc_sw128(sa + off), desc_sw128(sbb + off), id,
+                         tsf + (q >> 1) * 4, tsf + 4 * KSTEPS + (q >> 1) * 4,
+                         (kk > 0 || q > 0) ? 1u : 0u);
+          }
+        } else {
+          for (int q = 0; q < ksteps; ++q) {
+            const uint32_t off = (q >> 2) * A_SUB + (q & 3) * 32;
+            tc_mma_el(dcol, desc_sw128(sa + off), desc_sw128(sbb + off), idesc, tsf + q * 4,
+                      tsf + 4 * KSTEPS + q * 4, (kk > 0 || q > 0) ? 1u : 0u);
+          }
         }
         tc_commit_el(&empty[s]);   // also frees this stage's scale buffer
         if (++s == STAGES) s = 0;
@@ -533,12 +564,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int ksteps = min(KSTEPS, (klen - kk * KTILE) / 64);
         const uint32_t ssf = smem_u32(smem + s * STAGE_BYTES + A_TILE + B_TILE);
         const uint32_t tsf = tmem + SF_COL + sb * SF_BUF_COLS;
+        if (p.mx) {
+          // MXFP4: one atom covers two K steps; warp w copies atom w
+          if (2 * w < ksteps) {
+            tc_cp_sf_el(tsf + w * 4, desc_sf(ssf + w * 512));
+            tc_cp_sf_el(tsf + 4 * KSTEPS + w * 4, desc_sf(ssf + SF_TILE + w * 512));
+          }
+        } else {
 #pragma unroll
-        for (int i = 0; i < KSTEPS / SF_WARPS; ++i) {
-          const int q = w * (KSTEPS / SF_WARPS) + i;
-          if (q < ksteps) {
-            tc_cp_sf_el(tsf + q * 4, desc_sf(ssf + q * 512));
-            tc_cp_sf_el(tsf + 4 * KSTEPS + q * 4, desc_sf(ssf + SF_TILE + q * 512));
+          for (int i = 0; i < KSTEPS / SF_WARPS; ++i) {
+            const int q = w * (KSTEPS / SF_WARPS) + i;
+            if (q < ksteps) {
+              tc_cp_sf_el(tsf + q * 4, desc_sf(ssf + q * 512));
+              tc_cp_sf_el(tsf + 4 * KSTEPS + q * 4, desc_sf(ssf + SF_TILE + q * 512));
+            }
           }
         }
         tc_commit_el(&sf_ready[sb]);
@@ -824,6 +863,7 @@ struct Launch {
   void* y;
   int64_t ldy;
   int out_mode;
+  int mx;
   float* y_amax;
   void* ws;
   size_t ws_bytes;
@@ -880,6 +920,7 @@ static quads_status_t launch(const Launch& L) {
   p.a_sf = L.a_sf; p.b_sf = L.b_sf; p.r_sf = L.r_sf; p.ws_sf = ws_sf;
   p.a_ts = L.a_ts; p.b_ts = L.b_ts; p.r_ts = L.r_ts; p.a_ts_pe = L.a_pe; p.r_ts_pe = L.r_pe;
   p.comp = comp ? 1 : 0;
+  p.mx = L.mx;
   p.y = L.y; p.ldy = L.ldy; p.out_mode = L.out_mode;
   p.y_amax = (uint32_t*)L.y_amax;
   if (L.y_amax) cudaMemsetAsync(L.y_amax, 0, (size_t)L.E * 4, L.stream);
@@ -1021,6 +1062,35 @@ extern "C" quads_status_t quads_moe_grouped_gemm(
   L.out_mode = epilogue == QUADS_EPILOGUE_SWIGLU ? gemm::OUT_SWIGLU
                : (y_dtype == QUADS_OUT_F32 ? gemm::OUT_F32 : gemm::OUT_BF16);
   L.ws = workspace; L.ws_bytes = workspace_bytes; L.stream = (cudaStream_t)stream;
+  return gemm::launch(L);
+}
+
+extern "C" quads_status_t quads_mx_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* a_codes,
+                                        const uint8_t* a_scales, const uint8_t* w_codes,
+                                        const uint8_t* w_scales, void* y, int32_t y_dtype,
+                                        int64_t ldy, void* stream) {
+  if (!a_codes || !a_scales || !w_codes || !w_scales || !y)
+    return fail(QUADS_ERR_INVALID_ARG, "mx_gemm: null operand pointer");
+  if (M < 1 || N % 128 || N <= 0 || K % 128 || K <= 0)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "mx_gemm: need M>=1, N%%128==0, K%%128==0 (M=%lld N=%lld K=%lld)", (long long)M, (long long)N, (long long)K);
+  if (M > (1ll << 31) - 256 || (int64_t)N * K / 2 > (1ll << 40))
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "mx_gemm: shape too large");
+  if (y_dtype != QUADS_OUT_F32 && y_dtype != QUADS_OUT_BF16)
+    return fail(QUADS_ERR_INVALID_ARG, "mx_gemm: y_dtype");
+  if (ldy < N || (y_dtype == QUADS_OUT_F32 ? ldy % 4 : ldy % 8))
+    return fail(QUADS_ERR_MISALIGNED, "mx_gemm: ldy must be >= N and keep 16-byte rows");
+  if (!al16(a_codes) || !al16(w_codes) || !al16(a_scales) || !al16(w_scales) || !al16(y))
+    return fail(QUADS_ERR_MISALIGNED, "mx_gemm: operands must be 16-byte aligned");
+  gemm::Launch L{};
+  L.M = M; L.rows_cap = M; L.E = 1; L.N = (int)N; L.K = (int)K; L.k = 0; L.kpad = 0;
+  L.row_off = nullptr; L.row_cnt = nullptr;
+  L.a = a_codes; L.a_sf = a_scales; L.b = w_codes; L.b_sf = w_scales;
+  L.a_ts = nullptr; L.b_ts = nullptr; L.r_ts = nullptr;
+  L.a_pe = 0; L.r_pe = 0; L.sel = nullptr; L.sel_pe = 0;
+  L.y = y; L.ldy = ldy; L.out_mode = y_dtype == QUADS_OUT_F32 ? gemm::OUT_F32 : gemm::OUT_BF16;
+  L.mx = 1;
+  L.y_amax = nullptr;
+  L.stream = (cudaStream_t)stream;
   return gemm::launch(L);
 }
 

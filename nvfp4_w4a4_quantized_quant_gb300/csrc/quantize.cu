@@ -490,6 +490,9 @@ __device__ __forceinline__ int signed_index(uint32_t c) {
 // sn is one neighbour of v and the other is sn - 1 (RTN level above v) or
 // sn + 1 (below v); of two adjacent levels the one nearer the rollout level
 // sr is the lower one exactly when sr <= the lower index.
+// kMx: MXFP4 rollout (E8M0 scale per 32 elements, no tensor scale): the
+// scaled value is x * 2^-e and no block is a zero block.
+template <bool kMx>
 __global__ void __launch_bounds__(256) trace_kernel(
     const __nv_bfloat16* __restrict__ xt, int64_t rows, int cols, int64_t ldx,
     const uint8_t* __restrict__ rcodes, int64_t ldc, const uint8_t* __restrict__ rscales,
@@ -497,7 +500,7 @@ __global__ void __launch_bounds__(256) trace_kernel(
     unsigned long long* __restrict__ counters) {
   const uint32_t vec_per_row = (uint32_t)cols >> 3;
   const uint32_t total = (uint32_t)(rows * vec_per_row);   // < 2^31 (host check)
-  const float s_t = rst[0];
+  const float s_t = kMx ? 1.0f : rst[0];
   unsigned int n_rtn = 0, n_tr = 0, n_adj = 0;
   for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
     const uint32_t r = i / vec_per_row;
@@ -505,8 +508,14 @@ __global__ void __launch_bounds__(256) trace_kernel(
     float f[8];
     bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(xt + (int64_t)r * ldx + col)), f);
     const uint32_t rc = __ldg(reinterpret_cast<const uint32_t*>(rcodes + (int64_t)r * ldc + (col >> 1)));
-    const BlockScale bs =
-        block_scale_from_byte(__ldg(rscales + (int64_t)r * (cols >> 4) + (col >> 4)), s_t);
+    BlockScale bs;
+    if (kMx) {
+      bs.byte = __ldg(rscales + (int64_t)r * (cols >> 5) + (col >> 5));
+      bs.r = e8m0_inverse(bs.byte);
+      bs.zero = false;
+    } else {
+      bs = block_scale_from_byte(__ldg(rscales + (int64_t)r * (cols >> 4) + (col >> 4)), s_t);
+    }
     float v[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(f[j], bs.r);
@@ -541,6 +550,68 @@ __global__ void __launch_bounds__(256) trace_kernel(
       if (n_rtn) atomicAdd(&counters[0], (unsigned long long)n_rtn);
       if (n_tr) atomicAdd(&counters[1], (unsigned long long)n_tr);
       if (n_adj) atomicAdd(&counters[2], (unsigned long long)n_adj);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- MXFP4
+// MXFP4 quantization (32-element blocks, E8M0 power-of-two scales, no tensor
+// scale).  A thread takes 16 elements, half a block; the block maximum comes
+// from one shuffle with the partner lane (the even lane writes the scale
+// byte).  Scaling by 2^-e is exact, so the codes are the E2M1 rounding
+// (ties to even, saturating) of x * 2^-e.  Optional bf16 QDQ output
+// level * 2^e (exact in float32).  The loop runs on warp-uniform bases so
+// both partners of a block are always active together.
+__global__ void __launch_bounds__(256) mx_quantize_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
+    uint8_t* __restrict__ codes, int64_t ldc, uint8_t* __restrict__ scales, int layout,
+    __nv_bfloat16* __restrict__ qdq, int64_t ldq) {
+  const uint32_t per_row = (uint32_t)cols >> 4;              // even: cols % 32 == 0
+  const uint32_t total = (uint32_t)(rows * per_row);         // < 2^31 (host check)
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t base = blockIdx.x * blockDim.x + (threadIdx.x & ~31u); base < total; base += stride) {
+    const uint32_t i = base + lane;
+    const bool valid = i < total;
+    float f[16];
+    uint32_t r = 0, h = 0;
+    if (valid) {
+      r = i / per_row;
+      h = i - r * per_row;
+      const uint4* px = reinterpret_cast<const uint4*>(x + (int64_t)r * ldx + h * 16);
+      bf16x8_to_f32(__ldg(px), f);
+      bf16x8_to_f32(__ldg(px + 1), f + 8);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) f[j] = 0.0f;
+    }
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(f[j]));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    if (!valid) continue;
+    const uint32_t byte = e8m0_scale_byte(m);
+    const float inv = e8m0_inverse(byte);
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(f[j], inv);
+    const uint32_t c0 = f32x8_to_e2m1(v), c1 = f32x8_to_e2m1(v + 8);
+    *reinterpret_cast<uint2*>(codes + (int64_t)r * ldc + h * 8) = make_uint2(c0, c1);
+    if ((h & 1) == 0) scales[sf_offset(layout, r, h >> 1, cols >> 5)] = (uint8_t)byte;
+    if (qdq) {
+      const float d = e8m0_value(byte);
+      float lv[16];
+      e2m1x8_to_f32(c0, lv);
+      e2m1x8_to_f32(c1, lv + 8);
+      uint32_t packed[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(lv[2 * j], d), __fmul_rn(lv[2 * j + 1], d));
+        packed[j] = *reinterpret_cast<uint32_t*>(&b2);
+      }
+      uint4* pq = reinterpret_cast<uint4*>(qdq + (int64_t)r * ldq + h * 16);
+      pq[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      pq[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
     }
   }
 }
@@ -814,10 +885,61 @@ extern "C" quads_status_t quads_trace_round(const void* x_train, int64_t rows, i
   if (rows * (cols / 8) >= ((int64_t)1 << 31))
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "trace_round: rows * cols / 8 must be < 2^31");
   cudaStream_t st = (cudaStream_t)stream;
-  trace_kernel<<<grid_for(rows * (cols / 8), 256), 256, 0, st>>>(
+  trace_kernel<false><<<grid_for(rows * (cols / 8), 256), 256, 0, st>>>(
       (const __nv_bfloat16*)x_train, rows, (int)cols, ldx, rollout_codes, ld_codes,
       rollout_scales, rollout_tensor_scale, codes_out, counters);
   return check_launch("trace_round", 1);
+}
+
+extern "C" quads_status_t quads_trace_round_mx(const void* x_train, int64_t rows, int64_t cols,
+                                               int64_t ldx, const uint8_t* rollout_codes,
+                                               int64_t ld_codes, const uint8_t* rollout_scales,
+                                               uint8_t* codes_out, unsigned long long* counters,
+                                               void* stream) {
+  if (!x_train || !rollout_codes || !rollout_scales || !codes_out)
+    return fail(QUADS_ERR_INVALID_ARG, "trace_round_mx: null pointer argument");
+  if (cols <= 0 || cols % 32) return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "trace_round_mx: cols %% 32");
+  if (ldx < cols || ldx % 8 || ld_codes < cols / 2 || ld_codes % 4 || !aligned16(x_train) ||
+      ((uintptr_t)rollout_codes & 3u) || ((uintptr_t)codes_out & 3u))
+    return fail(QUADS_ERR_MISALIGNED, "trace_round_mx: leading dimensions / alignment");
+  if (rows < 0 || rows * (cols / 8) >= ((int64_t)1 << 31))
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "trace_round_mx: rows * cols / 8 must be < 2^31");
+  if (rows == 0) return QUADS_OK;
+  trace_kernel<true><<<grid_for(rows * (cols / 8), 256), 256, 0, (cudaStream_t)stream>>>(
+      (const __nv_bfloat16*)x_train, rows, (int)cols, ldx, rollout_codes, ld_codes,
+      rollout_scales, nullptr, codes_out, counters);
+  return check_launch("trace_round_mx", 1);
+}
+
+extern "C" quads_status_t quads_mx_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                                            uint8_t* codes, int64_t ld_codes, uint8_t* scales,
+                                            int32_t scale_layout, void* y_qdq, int64_t ldy,
+                                            void* stream) {
+  if (!x || !codes || !scales) return fail(QUADS_ERR_INVALID_ARG, "mx_quantize: null x/codes/scales");
+  if (rows < 0 || cols <= 0 || cols % 32)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "mx_quantize: cols %% 32 == 0");
+  if (scale_layout != QUADS_SCALES_LINEAR && scale_layout != QUADS_SCALES_TCGEN05)
+    return fail(QUADS_ERR_INVALID_ARG, "mx_quantize: bad scale_layout %d", scale_layout);
+  if (scale_layout == QUADS_SCALES_TCGEN05 && cols % 128)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "mx_quantize: TCGEN05 scale layout needs cols %% 128 == 0");
+  if (ldx < cols || ldx % 8 || !aligned16(x) || ld_codes < cols / 2 || ld_codes % 8 ||
+      ((uintptr_t)codes & 7u))
+    return fail(QUADS_ERR_MISALIGNED, "mx_quantize: x 16-byte aligned (ldx >= cols, %% 8), codes 8-byte aligned (ld_codes >= cols/2, %% 8)");
+  if (y_qdq && (ldy < cols || ldy % 8 || !aligned16(y_qdq)))
+    return fail(QUADS_ERR_MISALIGNED, "mx_quantize: y 16-byte aligned, ldy >= cols, %% 8");
+  if (rows * (cols / 16) >= ((int64_t)1 << 31))
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "mx_quantize: rows * cols / 16 must be < 2^31");
+  if (rows == 0) return QUADS_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (scale_layout == QUADS_SCALES_TCGEN05 && rows % 128) {
+    const int64_t start = (rows / 128) * (cols / 128) * 512;
+    const int64_t bytes = ((rows + 127) / 128) * 128 * (cols / 32);
+    cudaMemsetAsync(scales + start, 0, (size_t)(bytes - start), st);
+  }
+  mx_quantize_kernel<<<grid_for(rows * (cols / 16), 256), 256, 0, st>>>(
+      (const __nv_bfloat16*)x, rows, (int)cols, ldx, codes, ld_codes, scales, scale_layout,
+      (__nv_bfloat16*)y_qdq, ldy);
+  return check_launch("mx_quantize", 1);
 }
 
 extern "C" quads_status_t quads_trace_pack_record(const uint8_t* rollout_codes, int64_t rows,

@@ -53,6 +53,9 @@ _SIGS = {
     "quads_trace_round": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _P, _P]),
     "quads_trace_pack_record": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P]),
     "quads_trace_round_1bit": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _I64, _P, _P]),
+    "quads_mx_quantize": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _I32, _P, _I64, _P]),
+    "quads_mx_gemm": (_I32, [_I64, _I64, _I64, _P, _P, _P, _P, _P, _I32, _I64, _P]),
+    "quads_trace_round_mx": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _P]),
     "quads_moe_route": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _I64, _P, _SZ, _P]),
     "quads_moe_gather": (_I32, [_P, _P, _I32, _I64, _I64, _P, _P, _P, _P, _P]),
     "quads_moe_combine": (_I32, [_P, _I64, _P, _P, _I32, _I32, _I64, _P, _I64, _P]),
@@ -382,6 +385,57 @@ def trace_round_1bit(x_train: torch.Tensor, mantissa_bits: torch.Tensor, rollout
                                       _ptr(rollout.scales), _ptr(rollout.tensor_scale),
                                       _ptr(codes), codes.stride(0), _ptr(counters),
                                       _stream(stream)), "trace_round_1bit")
+    return codes, counters
+
+
+def mx_quantize(x: torch.Tensor, *, scale_layout: int = LINEAR, want_qdq: bool = False,
+                out=None, stream=None):
+    """MXFP4 (32-element blocks, E8M0 scales) -> (QTensor with tensor_scale None, bf16 QDQ or None)."""
+    lib = load()
+    assert x.dtype == torch.bfloat16 and x.dim() == 2
+    rows, cols = x.shape
+    dev = x.device
+    if out is None:
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+        nsf = ((rows + 127) // 128 * 128 if scale_layout == TCGEN05 else rows) * (cols // 32)
+        scales = torch.empty(nsf, dtype=torch.uint8, device=dev)
+    else:
+        codes, scales = out
+    y = torch.empty((rows, cols), dtype=torch.bfloat16, device=dev) if want_qdq else None
+    _check(lib.quads_mx_quantize(_ptr(x), rows, cols, x.stride(0), _ptr(codes), codes.stride(0),
+                                 _ptr(scales), scale_layout, _ptr(y), cols, _stream(stream)),
+           "mx_quantize")
+    return QTensor(codes, scales, None, rows, cols, scale_layout), y
+
+
+def mx_gemm(a: QTensor, w: QTensor, *, out_dtype=torch.bfloat16, out=None, stream=None):
+    """Y [M, N] = DQ(A) DQ(W)^T for MXFP4 operands (TCGEN05 scale layout)."""
+    lib = load()
+    if a.layout != TCGEN05 or w.layout != TCGEN05:
+        raise QuadsError("mx_gemm takes TCGEN05 scale layouts")
+    M, K, N = a.rows, a.cols, w.rows
+    y = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=a.codes.device)
+    yd = OUT_F32 if y.dtype == torch.float32 else OUT_BF16
+    _check(lib.quads_mx_gemm(M, N, K, _ptr(a.codes), _ptr(a.scales), _ptr(w.codes),
+                             _ptr(w.scales), _ptr(y), yd, y.stride(0), _stream(stream)), "mx_gemm")
+    return y
+
+
+def trace_round_mx(x_train: torch.Tensor, rollout: QTensor, *, counters=None, out=None,
+                   stream=None):
+    """TRACE rounding under an MXFP4 rollout (LINEAR E8M0 scales)."""
+    lib = load()
+    rows, cols = x_train.shape
+    if rollout.layout != LINEAR:
+        raise QuadsError("trace_round_mx takes LINEAR rollout scales")
+    codes = out if out is not None else torch.empty((rows, cols // 2), dtype=torch.uint8,
+                                                    device=x_train.device)
+    if counters is None:
+        counters = torch.zeros(3, dtype=torch.int64, device=x_train.device)
+    _check(lib.quads_trace_round_mx(_ptr(x_train), rows, cols, x_train.stride(0),
+                                    _ptr(rollout.codes), rollout.codes.stride(0),
+                                    _ptr(rollout.scales), _ptr(codes), _ptr(counters),
+                                    _stream(stream)), "trace_round_mx")
     return codes, counters
 
 

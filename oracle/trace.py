@@ -131,3 +131,19 @@ def trace_round_1bit(x_train, mantissa_bits, rollout_scales, s_t):
     q_out = e2m1_decode(codes)
     return codes, dict(changed=int((q_out != q_rtn).sum()),
                        bit_mismatch=int((_mantissa(q_out) != bit).sum()))
+
+
+def trace_round_mx(x_train, rollout_codes, rollout_e8m0):
+    """trace_round under an MXFP4 rollout: v = x_train / 2^e with the rollout
+    block's E8M0 scale (32-element blocks, no tensor scale, never a zero block)."""
+    x = np.asarray(x_train, dtype=np.float32)
+    rows, cols = x.shape
+    e = np.asarray(rollout_e8m0, dtype=np.int64) - 127
+    v = np.ldexp(x.reshape(rows, cols // 32, 32).astype(np.float64), -e[:, :, None])
+    v = v.astype(np.float32).reshape(rows, cols)
+    q_roll = e2m1_decode(rollout_codes)
+    q_lo, q_hi = neighbours(v)
+    pick_lo = np.abs(q_lo - q_roll) <= np.abs(q_hi - q_roll)
+    codes = _value_to_code(np.where(pick_lo, q_lo, q_hi), v)
+    q_rtn = e2m1_decode(e2m1_encode(v))
+    return codes, mismatch_counters(q_rtn, e2m1_decode(codes), q_roll)

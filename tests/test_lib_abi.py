@@ -96,6 +96,14 @@ def test_host_side_argument_checks_need_no_gpu(lib):
     assert st == 2                                   # ld_bits < cols / 8
     st = lib.quads_trace_round_1bit(p, 4, 32, 24, p, 4, p, p, p, 16, None, None)
     assert st == 3                                   # ldx < cols
+    st = lib.quads_mx_quantize(p, 4, 48, 48, p, 24, p, 0, None, 0, None)
+    assert st == 2                                   # cols % 32
+    st = lib.quads_mx_quantize(p, 4, 96, 96, p, 48, p, 1, None, 0, None)
+    assert st == 2                                   # TCGEN05 layout needs cols % 128
+    st = lib.quads_mx_gemm(64, 128, 192, p, p, p, p, p, 0, 128, None)
+    assert st == 2                                   # K % 128
+    st = lib.quads_trace_round_mx(p, 4, 48, 48, p, 24, p, p, None, None)
+    assert st == 2                                   # cols % 32
     st = lib.quads_qdq_nvfp4(p, 4, 32, 32, None, 1, p, None, 32, None, 16, None, 0, p, None, 0, None)
     assert st == 1                                   # null y
     st = lib.quads_qdq_nvfp4(p, 4, 32, 32, None, 1, p, p, 24, None, 16, None, 0, p, None, 0, None)
