@@ -106,79 +106,87 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
   }
 }
 
-// One block: warp w scans the per-block counts of experts w, w+32, ... over the
-// routing blocks (block_prefix[e][b] = tokens of expert e in blocks < b, and
-// the expert's total count; each expert's counts are contiguous, loaded 8 per
-// lane at once), then the padded offsets
-// off[e+1] = off[e] + roundup(count[e], 128) by a scan over the experts.
-__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ bcount, int nb,
-                                                    int E, int32_t* __restrict__ bprefix,
-                                                    int32_t* __restrict__ counts,
-                                                    int32_t* __restrict__ off) {
-  __shared__ int cnt[kMaxExperts];
-  __shared__ int warp_sums[kMaxExperts / 32];
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  for (int e = w; e < E; e += 32) {
-    const int32_t* bc = bcount + (int64_t)e * nb;
-    int32_t* bp = bprefix + (int64_t)e * nb;
-    int running = 0;
-    for (int b0 = 0; b0 < nb; b0 += 256) {   // lane l: blocks b0 + 8l .. b0 + 8l + 7
-      int v[8], sum = 0;
+// One block per expert: block_prefix[e][b] = tokens of expert e in routing
+// blocks < b and the expert's total count, by a block-wide scan (thread t
+// takes 8 consecutive routing blocks per pass).  The padded offsets are formed
+// by assign_kernel from the counts.
+__global__ void __launch_bounds__(256) plan_kernel(const int32_t* __restrict__ bcount, int nb,
+                                                   int32_t* __restrict__ bprefix,
+                                                   int32_t* __restrict__ counts) {
+  __shared__ int warp_sums[8];
+  const int e = blockIdx.x, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int32_t* bc = bcount + (int64_t)e * nb;
+  int32_t* bp = bprefix + (int64_t)e * nb;
+  int running = 0;
+  for (int b0 = 0; b0 < nb; b0 += 256 * 8) {
+    int v[8], sum = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int b = b0 + 8 * lane + i;
-        v[i] = b < nb ? bc[b] : 0;
-        sum += v[i];
-      }
-      int incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
-      }
-      int x = running + incl - sum;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int b = b0 + 8 * lane + i;
-        if (b < nb) bp[b] = x;
-        x += v[i];
-      }
-      running += __shfl_sync(0xffffffffu, incl, 31);
+    for (int i = 0; i < 8; ++i) {
+      const int b = b0 + 8 * (int)threadIdx.x + i;
+      v[i] = b < nb ? bc[b] : 0;
+      sum += v[i];
     }
-    if (lane == 0) { cnt[e] = running; counts[e] = running; }
-  }
-  __syncthreads();
-  int v = 0;   // inclusive padded count of experts <= threadIdx.x within the warp
-  if (threadIdx.x < kMaxExperts) {
-    const int c = (int)threadIdx.x < E ? cnt[threadIdx.x] : 0;
-    v = (c + QUADS_MOE_ROW_ALIGN - 1) / QUADS_MOE_ROW_ALIGN * QUADS_MOE_ROW_ALIGN;
+    int incl = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += u;
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
     }
-    if (lane == 31) warp_sums[w] = v;
+    if (lane == 31) warp_sums[w] = incl;
+    __syncthreads();
+    int before = running, total = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      total += warp_sums[i];
+      if (i < w) before += warp_sums[i];
+    }
+    int x = before + incl - sum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int b = b0 + 8 * (int)threadIdx.x + i;
+      if (b < nb) bp[b] = x;
+      x += v[i];
+    }
+    running += total;
+    __syncthreads();
   }
-  __syncthreads();
-  if (threadIdx.x < kMaxExperts) {
-    int before = 0;
-    for (int i = 0; i < w; ++i) before += warp_sums[i];
-    if ((int)threadIdx.x < E) off[threadIdx.x + 1] = v + before;
-    if (threadIdx.x == 0) off[0] = 0;
-  }
+  if (threadIdx.x == 0) counts[e] = running;
 }
 
 // Rows of the plan: slot (t, j) routed to expert e goes to row
 // off[e] + block_prefix[e][t / 32] + its rank within the routing block, so
 // each expert's rows hold its tokens in ascending token order.  Padding rows
-// get row_token = -1.
+// get row_token = -1.  Every block forms the padded offsets
+// off[e+1] = off[e] + roundup(count[e], 128) itself (a scan over <= 256
+// experts); block 0 stores them.
 __global__ void __launch_bounds__(256) assign_kernel(const int32_t* __restrict__ idx, int T, int E,
                                                      int topk, int nb,
                                                      const int32_t* __restrict__ bprefix,
-                                                     const int32_t* __restrict__ off,
+                                                     int32_t* __restrict__ off_out,
                                                      const int32_t* __restrict__ counts,
                                                      int32_t* __restrict__ row_token,
                                                      int32_t* __restrict__ token_row) {
+  __shared__ int off[kMaxExperts + 1];
+  __shared__ int warp_sums[8];
+  {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int c = (int)threadIdx.x < E ? counts[threadIdx.x] : 0;
+    const int pc = (c + QUADS_MOE_ROW_ALIGN - 1) / QUADS_MOE_ROW_ALIGN * QUADS_MOE_ROW_ALIGN;
+    int incl = pc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) warp_sums[w] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int i = 0; i < w; ++i) before += warp_sums[i];
+    if ((int)threadIdx.x < E) off[threadIdx.x + 1] = before + incl;
+    if (threadIdx.x == 0) off[0] = 0;
+    __syncthreads();
+    if (blockIdx.x == 0 && (int)threadIdx.x <= E) off_out[threadIdx.x] = off[threadIdx.x];
+  }
   const int total = T * topk;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
     const int t = i / topk;
@@ -329,7 +337,7 @@ extern "C" quads_status_t quads_moe_route(const float* logits, int32_t tokens, i
   if (tokens > 0)
     route_kernel<<<nb, 32 * kRouteTokens, 0, st>>>(logits, tokens, num_experts, topk, topk_idx,
                                                     gates, bcount, token_row);
-  plan_kernel<<<1, 1024, 0, st>>>(bcount, nb, num_experts, bprefix, expert_counts, expert_offsets);
+  plan_kernel<<<num_experts, 256, 0, st>>>(bcount, nb, bprefix, expert_counts);
   assign_kernel<<<std::max(1, std::min(num_sms() * 4, (tokens * topk + 255) / 256)), 256, 0, st>>>(
       topk_idx, tokens, num_experts, topk, nb, bprefix, expert_offsets, expert_counts, row_token,
       token_row);
