@@ -31,6 +31,10 @@
  *     are latched in a device word read by quads_device_status().
  *   - bf16 tensors are row-major with a leading dimension in elements that is
  *     a multiple of 8; pointers are 16-byte aligned.
+ *   - An empty input (rows, tokens or M of 0) is valid: after the shape
+ *     checks the call returns QUADS_OK without enqueueing anything, and its
+ *     data pointers may then be NULL (as PyTorch gives for empty tensors).
+ *     Nothing is written, not even tensor scales.
  *
  * NVFP4 storage:
  *   codes   uint8 [rows, ld_codes]: two E2M1 codes per byte, element 2i of a row
@@ -278,7 +282,7 @@ quads_status_t quads_select_residual_channels_noalloc(
  *   r_codes NULL -> plain W4A4 (sel, r_* ignored); else r_codes [M, kpad/2],
  *   r_scales TCGEN05 over kpad columns, r_tensor_scale [1], sel [k] ascending.
  *   y [M, ldy] float32 or bf16 (y_dtype).
- * K % 64 == 0, N % 128 == 0, M >= 1.
+ * K % 64 == 0, N % 128 == 0, M >= 0 (M == 0: nothing is enqueued).
  */
 quads_status_t quads_w4a4_gemm_comp(int64_t M, int64_t N, int64_t K, const uint8_t* a_codes,
                                     const uint8_t* a_scales, const float* a_tensor_scale,
@@ -463,7 +467,8 @@ quads_status_t quads_mx_quantize(const void* x, int64_t rows, int64_t cols, int6
  * tensor cores (tcgen05.mma kind::mxf4, E8M0 scales, float32 accumulation).
  *   a_codes [M, K/2], a_scales TCGEN05 (ceil(M/128)*128 rows); w_codes [N, K/2],
  *   w_scales TCGEN05; y [M, ldy] float32 or bf16 (y_dtype).
- *   M >= 1, N % 128 == 0, K % 128 == 0; operands 16-byte aligned.
+ *   M >= 0 (0: nothing is enqueued), N % 128 == 0, K % 128 == 0; operands
+ *   16-byte aligned.
  */
 quads_status_t quads_mx_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* a_codes,
                              const uint8_t* a_scales, const uint8_t* w_codes,

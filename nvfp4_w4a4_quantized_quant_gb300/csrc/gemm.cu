@@ -986,10 +986,11 @@ extern "C" quads_status_t quads_w4a4_gemm_comp(int64_t M, int64_t N, int64_t K,
                                                int32_t k, void* y, int32_t y_dtype, int64_t ldy,
                                                void* workspace, size_t workspace_bytes,
                                                void* stream) {
+  if (M < 0 || N % 128 || N <= 0 || K % 64 || K <= 0)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "gemm: need M>=0, N%%128==0, K%%64==0 (M=%lld N=%lld K=%lld)", (long long)M, (long long)N, (long long)K);
+  if (M == 0) return QUADS_OK;
   if (!a_codes || !a_scales || !a_tensor_scale || !w_codes || !w_scales || !w_tensor_scale || !y)
     return fail(QUADS_ERR_INVALID_ARG, "gemm: null operand pointer");
-  if (M < 1 || N % 128 || N <= 0 || K % 64 || K <= 0)
-    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "gemm: need M>=1, N%%128==0, K%%64==0 (M=%lld N=%lld K=%lld)", (long long)M, (long long)N, (long long)K);
   if (M > (1ll << 31) - 256 || (int64_t)N * K / 2 > (1ll << 40))
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "gemm: shape too large");
   if (y_dtype != QUADS_OUT_F32 && y_dtype != QUADS_OUT_BF16)
@@ -1069,10 +1070,11 @@ extern "C" quads_status_t quads_mx_gemm(int64_t M, int64_t N, int64_t K, const u
                                         const uint8_t* a_scales, const uint8_t* w_codes,
                                         const uint8_t* w_scales, void* y, int32_t y_dtype,
                                         int64_t ldy, void* stream) {
+  if (M < 0 || N % 128 || N <= 0 || K % 128 || K <= 0)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "mx_gemm: need M>=0, N%%128==0, K%%128==0 (M=%lld N=%lld K=%lld)", (long long)M, (long long)N, (long long)K);
+  if (M == 0) return QUADS_OK;
   if (!a_codes || !a_scales || !w_codes || !w_scales || !y)
     return fail(QUADS_ERR_INVALID_ARG, "mx_gemm: null operand pointer");
-  if (M < 1 || N % 128 || N <= 0 || K % 128 || K <= 0)
-    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "mx_gemm: need M>=1, N%%128==0, K%%128==0 (M=%lld N=%lld K=%lld)", (long long)M, (long long)N, (long long)K);
   if (M > (1ll << 31) - 256 || (int64_t)N * K / 2 > (1ll << 40))
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "mx_gemm: shape too large");
   if (y_dtype != QUADS_OUT_F32 && y_dtype != QUADS_OUT_BF16)

@@ -320,7 +320,8 @@ extern "C" quads_status_t quads_moe_route(const float* logits, int32_t tokens, i
                                           int32_t* row_token, int32_t* token_row,
                                           int64_t rows_capacity, void* workspace,
                                           size_t workspace_bytes, void* stream) {
-  if (!logits || !topk_idx || !gates || !expert_counts || !expert_offsets || !row_token || !token_row)
+  if (!expert_counts || !expert_offsets || !row_token ||
+      (tokens > 0 && (!logits || !topk_idx || !gates || !token_row)))
     return fail(QUADS_ERR_INVALID_ARG, "moe_route: null pointer argument");
   if (tokens < 0 || num_experts < 1 || num_experts > kMaxExperts || topk < 1 ||
       topk > kMaxTopk || topk > num_experts)
@@ -368,7 +369,8 @@ extern "C" quads_status_t quads_moe_gather(const int32_t* row_token, const int32
 extern "C" quads_status_t quads_moe_combine(const void* y, int64_t ldy, const int32_t* token_row,
                                             const float* gates, int32_t tokens, int32_t topk,
                                             int64_t hidden, void* out, int64_t ldo, void* stream) {
-  if (!y || !token_row || !gates || !out) return fail(QUADS_ERR_INVALID_ARG, "moe_combine: null pointer");
+  if (tokens > 0 && (!y || !token_row || !gates || !out))
+    return fail(QUADS_ERR_INVALID_ARG, "moe_combine: null pointer");
   if (hidden <= 0 || hidden % 8 || ldy % 8 || ldo % 8 || ldy < hidden || ldo < hidden)
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "moe_combine: hidden/ld must be multiples of 8");
   if (tokens == 0) return QUADS_OK;

@@ -737,7 +737,7 @@ static quads_status_t quantize_impl(
     const float* tensor_amax_in, uint8_t* codes, int64_t ld_codes, uint8_t* scales,
     int32_t scale_layout, float* tensor_scale_out, float* score_partials,
     __nv_bfloat16* qdq, int64_t ldq, void* workspace, size_t workspace_bytes, void* stream) {
-  if (!x || (!codes && !qdq) || (codes && !scales) || !tensor_scale_out)
+  if (rows > 0 && (!x || (!codes && !qdq) || (codes && !scales) || !tensor_scale_out))
     return fail(QUADS_ERR_INVALID_ARG, "quantize: null x/codes/scales/tensor_scale_out");
   if (qdq && (ldq < cols || ldq % 8 || !aligned16(qdq)))
     return fail(QUADS_ERR_MISALIGNED, "qdq: y must be 16-byte aligned with ldy >= cols, ldy %% 8 == 0");
@@ -757,9 +757,9 @@ static quads_status_t quantize_impl(
   if (group_offsets && num_groups < 1) return fail(QUADS_ERR_INVALID_ARG, "quantize: num_groups < 1");
   if (tensor_scale_in && tensor_amax_in)
     return fail(QUADS_ERR_INVALID_ARG, "quantize: give tensor_scale_in or tensor_amax_in, not both");
+  if (rows == 0) return QUADS_OK;
   if (!tensor_scale_in && !tensor_amax_in && (workspace_bytes < (size_t)G * 4 || !workspace))
     return fail(QUADS_ERR_WORKSPACE, "quantize: workspace needs %d bytes", G * 4);
-  if (rows == 0) return QUADS_OK;
   cudaStream_t st = (cudaStream_t)stream;
   const float* stp = tensor_scale_in;
   const uint32_t* amax_bits = nullptr;   // set: the quantize kernel derives the tensor scales
@@ -807,7 +807,7 @@ extern "C" quads_status_t quads_quantize_nvfp4(
     int32_t scale_layout,
     float* tensor_scale_out, float* score_partials, void* workspace, size_t workspace_bytes,
     void* stream) {
-  if (!codes) return fail(QUADS_ERR_INVALID_ARG, "quantize: null codes");
+  if (!codes && rows > 0) return fail(QUADS_ERR_INVALID_ARG, "quantize: null codes");
   return quantize_impl(x, rows, cols, ldx, row_index, group_offsets, num_groups, tensor_scale_in,
                        tensor_amax_in, codes, ld_codes, scales, scale_layout, tensor_scale_out,
                        score_partials, nullptr, 0, workspace, workspace_bytes, stream);
@@ -818,7 +818,7 @@ extern "C" quads_status_t quads_qdq_nvfp4(
     int32_t num_groups, const float* tensor_scale_in, void* y, int64_t ldy, uint8_t* codes,
     int64_t ld_codes, uint8_t* scales, int32_t scale_layout, float* tensor_scale_out,
     void* workspace, size_t workspace_bytes, void* stream) {
-  if (!y) return fail(QUADS_ERR_INVALID_ARG, "qdq: null y");
+  if (!y && rows > 0) return fail(QUADS_ERR_INVALID_ARG, "qdq: null y");
   return quantize_impl(x, rows, cols, ldx, nullptr, group_offsets, num_groups, tensor_scale_in,
                        nullptr, codes, ld_codes, scales, scale_layout, tensor_scale_out, nullptr,
                        (__nv_bfloat16*)y, ldy, workspace, workspace_bytes, stream);
@@ -830,17 +830,18 @@ extern "C" quads_status_t quads_select_residual_channels(
     const float* score_partials, int32_t k, int32_t* sel, float* scores_out, uint8_t* r_codes,
     uint8_t* r_scales, int32_t r_scale_layout, float* r_tensor_scale, void* workspace,
     size_t workspace_bytes, void* sel_ready_event, void* stream) {
-  if (!x || !scales || !tensor_scale || !score_partials || !sel || !r_codes || !r_scales || !r_tensor_scale)
+  if (rows > 0 && (!x || !scales || !tensor_scale || !score_partials || !sel || !r_codes ||
+                   !r_scales || !r_tensor_scale))
     return fail(QUADS_ERR_INVALID_ARG, "select: null pointer argument");
-  if (cols <= 0 || cols % 16 || cols > 8192)
-    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "select: cols=%lld must be a multiple of 16 and <= 8192", (long long)cols);
+  if (rows < 0 || cols <= 0 || cols % 16 || cols > 8192)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "select: cols=%lld must be a multiple of 16 and <= 8192 (rows >= 0)", (long long)cols);
   if (k <= 0 || k % 16 || k > cols)
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "select: k=%d must be a multiple of 16 in [16, cols]", k);
   if (ldx < cols) return fail(QUADS_ERR_MISALIGNED, "select: ldx < cols");
   const int G = group_offsets ? num_groups : 1;
   const int kpad = quads_kpad(k);
   const size_t need = quads_workspace_size(QUADS_OP_SELECT, rows, cols, 0, k, G);
-  if (!workspace || workspace_bytes < need)
+  if (rows > 0 && (!workspace || workspace_bytes < need))
     return fail(QUADS_ERR_WORKSPACE, "select: workspace needs %zu bytes", need);
   cudaStream_t st = (cudaStream_t)stream;
   auto sel_ready = [&]() -> quads_status_t {
@@ -884,7 +885,7 @@ extern "C" quads_status_t quads_trace_round(const void* x_train, int64_t rows, i
                                             int64_t ld_codes, const uint8_t* rollout_scales,
                                             const float* rollout_tensor_scale, uint8_t* codes_out,
                                             unsigned long long* counters, void* stream) {
-  if (!x_train || !rollout_codes || !rollout_scales || !rollout_tensor_scale || !codes_out)
+  if (rows > 0 && (!x_train || !rollout_codes || !rollout_scales || !rollout_tensor_scale || !codes_out))
     return fail(QUADS_ERR_INVALID_ARG, "trace_round: null pointer argument");
   if (cols <= 0 || cols % 16) return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "trace_round: cols %% 16");
   if (ldx < cols || ldx % 8 || ld_codes < cols / 2 || ld_codes % 4 || !aligned16(x_train))
@@ -904,7 +905,7 @@ extern "C" quads_status_t quads_trace_round_mx(const void* x_train, int64_t rows
                                                int64_t ld_codes, const uint8_t* rollout_scales,
                                                uint8_t* codes_out, unsigned long long* counters,
                                                void* stream) {
-  if (!x_train || !rollout_codes || !rollout_scales || !codes_out)
+  if (rows > 0 && (!x_train || !rollout_codes || !rollout_scales || !codes_out))
     return fail(QUADS_ERR_INVALID_ARG, "trace_round_mx: null pointer argument");
   if (cols <= 0 || cols % 32) return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "trace_round_mx: cols %% 32");
   if (ldx < cols || ldx % 8 || ld_codes < cols / 2 || ld_codes % 4 || !aligned16(x_train) ||
@@ -923,7 +924,8 @@ extern "C" quads_status_t quads_mx_quantize(const void* x, int64_t rows, int64_t
                                             uint8_t* codes, int64_t ld_codes, uint8_t* scales,
                                             int32_t scale_layout, void* y_qdq, int64_t ldy,
                                             void* stream) {
-  if (!x || !codes || !scales) return fail(QUADS_ERR_INVALID_ARG, "mx_quantize: null x/codes/scales");
+  if (rows > 0 && (!x || !codes || !scales))
+    return fail(QUADS_ERR_INVALID_ARG, "mx_quantize: null x/codes/scales");
   if (rows < 0 || cols <= 0 || cols % 32)
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "mx_quantize: cols %% 32 == 0");
   if (scale_layout != QUADS_SCALES_LINEAR && scale_layout != QUADS_SCALES_TCGEN05)
@@ -954,7 +956,7 @@ extern "C" quads_status_t quads_trace_pack_record(const uint8_t* rollout_codes, 
                                                   int64_t cols, int64_t ld_codes,
                                                   uint8_t* mantissa_bits, int64_t ld_bits,
                                                   void* stream) {
-  if (!rollout_codes || !mantissa_bits)
+  if (rows > 0 && (!rollout_codes || !mantissa_bits))
     return fail(QUADS_ERR_INVALID_ARG, "trace_pack_record: null pointer argument");
   if (rows < 0 || cols <= 0 || cols % 16 || ld_codes < cols / 2 || ld_codes % 4 ||
       ld_bits < cols / 8)
@@ -975,7 +977,7 @@ extern "C" quads_status_t quads_trace_round_1bit(const void* x_train, int64_t ro
                                                  const float* rollout_tensor_scale,
                                                  uint8_t* codes_out, int64_t ld_codes,
                                                  unsigned long long* counters, void* stream) {
-  if (!x_train || !mantissa_bits || !rollout_scales || !rollout_tensor_scale || !codes_out)
+  if (rows > 0 && (!x_train || !mantissa_bits || !rollout_scales || !rollout_tensor_scale || !codes_out))
     return fail(QUADS_ERR_INVALID_ARG, "trace_round_1bit: null pointer argument");
   if (rows < 0 || cols <= 0 || cols % 16 || ld_bits < cols / 8 || ld_codes < cols / 2 ||
       ld_codes % 4)
