@@ -395,35 +395,55 @@ __global__ void __launch_bounds__(1024) topk_kernel(float* __restrict__ scores, 
 }
 
 // ---------------------------------------------------------------- residual slice
-// R[:, sel] recomputed from x and the stored block scales; one block per 32-row
-// chunk (one group), per-group amax of |R| by atomicMax on the float bits.
+// R[:, sel] recomputed from x and the stored block scales; one block per
+// slice of `rb` rows (8 or 32: group offsets are multiples of 32, so a slice
+// is inside one group; 8 when 32-row slices would leave the GPU short of
+// blocks), four independent gathers in flight per thread; per-group amax of
+// |R| by atomicMax on the float bits.
 __global__ void __launch_bounds__(256) rsel_residual_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
     const int32_t* __restrict__ goff, int G, const uint8_t* __restrict__ scales, int layout,
     const float* __restrict__ st, const int32_t* __restrict__ sel, int k,
-    float* __restrict__ rs, uint32_t* __restrict__ amax_bits) {
+    float* __restrict__ rs, uint32_t* __restrict__ amax_bits, int rb) {
   __shared__ float red[8];
   const int64_t end = goff ? (int64_t)goff[G] : rows;
-  const int64_t nchunks = (end + kScoreChunk - 1) / kScoreChunk;
+  const int64_t nblk = (end + rb - 1) / rb;
   const int ncols16 = cols >> 4;
-  for (int64_t chunk = blockIdx.x; chunk < nchunks; chunk += gridDim.x) {
-    const int64_t r0 = chunk * kScoreChunk, r1 = min(r0 + kScoreChunk, end);
+  for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+    const int64_t r0 = blk * rb, r1 = min(r0 + rb, end);
     const int g = goff ? group_of(goff, G, r0) : 0;
     const float s_t = st[g];
     const int32_t* sg = sel + (int64_t)g * k;
     float m = 0.0f;
     const int total = (int)(r1 - r0) * k;
-    for (int i = threadIdx.x; i < total; i += blockDim.x) {
-      const int64_t r = r0 + i / k;
-      const int j = i % k;
-      const int c = sg[j];
-      const float xv = __bfloat162float(x[r * ldx + c]);
-      const BlockScale bs = block_scale_from_byte(scales[sf_offset(layout, r, c >> 4, ncols16)], s_t);
-      float v[8] = {__fmul_rn(xv, bs.r), 0, 0, 0, 0, 0, 0, 0};
-      const uint32_t code = bs.zero ? 0u : (f32x8_to_e2m1(v) & 15u);
-      const float R = __fsub_rn(xv, __fmul_rn(e2m1_to_f32(code), bs.d));
-      rs[r * k + j] = R;
-      m = fmaxf(m, fabsf(R));
+    for (int i0 = threadIdx.x; i0 < total; i0 += 4 * blockDim.x) {
+      int64_t r[4];
+      int j[4], c[4];
+      float xv[4];
+      uint32_t sb[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * (int)blockDim.x;
+        r[u] = r0 + (i < total ? i / k : 0);
+        j[u] = i < total ? i % k : 0;
+        c[u] = sg[j[u]];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        xv[u] = __bfloat162float(x[r[u] * ldx + c[u]]);
+        sb[u] = scales[sf_offset(layout, r[u], c[u] >> 4, ncols16)];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * (int)blockDim.x;
+        if (i >= total) continue;
+        const BlockScale bs = block_scale_from_byte(sb[u], s_t);
+        float v[8] = {__fmul_rn(xv[u], bs.r), 0, 0, 0, 0, 0, 0, 0};
+        const uint32_t code = bs.zero ? 0u : (f32x8_to_e2m1(v) & 15u);
+        const float R = __fsub_rn(xv[u], __fmul_rn(e2m1_to_f32(code), bs.d));
+        rs[r[u] * k + j[u]] = R;
+        m = fmaxf(m, fabsf(R));
+      }
     }
     m = warp_max(m);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
@@ -868,9 +888,10 @@ extern "C" quads_status_t quads_select_residual_channels(
                                                      group_offsets, rows);
   if (quads_status_t s = sel_ready()) return s;
   cudaMemsetAsync(amax, 0, (size_t)G * 4, st);
-  rsel_residual_kernel<<<grid_for((rows + 31) / 32, 1, 16), 256, 0, st>>>(
+  const int rb = (rows + 31) / 32 < 2 * (int64_t)num_sms() ? 8 : 32;
+  rsel_residual_kernel<<<grid_for((rows + rb - 1) / rb, 1, 16), 256, 0, st>>>(
       (const __nv_bfloat16*)x, rows, (int)cols, ldx, group_offsets, G, scales, scale_layout,
-      tensor_scale, sel, k, rs, amax);
+      tensor_scale, sel, k, rs, amax, rb);
   if (r_scale_layout == QUADS_SCALES_TCGEN05 && rows % 128) {
     const int64_t start = (rows / 128) * (kpad / 64) * 512;
     cudaMemsetAsync(r_scales + start, 0, (size_t)(sf_tc_bytes(rows, kpad) - start), st);
