@@ -40,13 +40,17 @@ class CompensatedLinear:
             rs=torch.empty(Q.sf_tc_bytes(max_rows, kp), dtype=torch.uint8, device=dev),
             rts=torch.empty(1, dtype=torch.float32, device=dev),
             y=torch.empty((max_rows, self.N), dtype=out_dtype, device=dev),
+            wsc=torch.empty((self.N, kp // 2), dtype=torch.uint8, device=dev),
+            wss=torch.empty(Q.sf_tc_bytes(self.N, kp), dtype=torch.uint8, device=dev),
         )
         self.ws_q = torch.empty(Q.workspace_size(Q.OP_QUANTIZE, max_rows, self.K), dtype=torch.uint8,
                                 device=dev)
         self.ws_s = torch.empty(Q.workspace_size(Q.OP_SELECT, max_rows, self.K, 0, k),
                                 dtype=torch.uint8, device=dev)
-        self.ws_g = torch.empty(Q.workspace_size(Q.OP_GEMM, 0, self.K, self.N, k), dtype=torch.uint8,
-                                device=dev)
+        # Q(W_sel) is built on a side stream as soon as the selection is known,
+        # next to the residual slice (forked and joined by events)
+        self.side = torch.cuda.Stream(device=dev)
+        self.ev_sel, self.ev_w = torch.cuda.Event(), torch.cuda.Event()
 
     def forward(self, x: torch.Tensor, stream=None) -> torch.Tensor:
         b = self.bufs
@@ -59,11 +63,17 @@ class CompensatedLinear:
         y = b["y"][:M]
         if not self.compensate:
             return Q.w4a4_gemm_comp(xq, self.wq, out=y, stream=stream)
+        main = torch.cuda.current_stream() if stream is None else stream
         sel, _, r = Q.select_residual_channels(x, xq, part, self.k, r_scale_layout=Q.TCGEN05,
-                                               workspace=self.ws_s, stream=stream,
+                                               workspace=self.ws_s, sel_ready_event=self.ev_sel,
+                                               stream=stream,
                                                out=(b["sel"], b["rc"][:M], b["rs"], b["rts"]))
-        return Q.w4a4_gemm_comp(xq, self.wq, r, sel, self.k, out=y, workspace=self.ws_g,
-                                stream=stream)
+        self.side.wait_event(self.ev_sel)
+        wsel = Q.select_weight_channels(self.wq, sel, self.k, stream=self.side,
+                                        out=(b["wsc"], b["wss"]))
+        self.ev_w.record(self.side)
+        main.wait_event(self.ev_w)
+        return Q.w4a4_gemm_comp(xq, self.wq, r, sel, self.k, out=y, w_sel=wsel, stream=stream)
 
 
 class MoEExpertLayer:
