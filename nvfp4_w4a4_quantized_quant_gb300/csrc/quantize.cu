@@ -19,6 +19,8 @@ namespace quads {
 
 static __device__ int g_quant_error;  // device-side argument check failures
 
+constexpr int kRselGroupMin = 32;     // groups from which the per-group R_sel kernel is used
+
 // ---------------------------------------------------------------- amax
 // One block per 8-row slice (inside one group), threads over (row, 8-col
 // vector), eight 16-byte loads in flight per thread; the absolute maximum is
@@ -457,6 +459,113 @@ __global__ void __launch_bounds__(256) rsel_residual_kernel(
   }
 }
 
+// Per-group path (many groups, e.g. one per expert): one block per group does
+// both steps -- R for the group's rows into the float32 workspace, the
+// group's amax by a block reduction, then the second quantization of those
+// rows (the arithmetic of rsel_residual_kernel and rsel_quantize_kernel) --
+// so no grid-wide maximum and no second launch are needed.  Blocks past the
+// groups zero the rows after the last offset.
+constexpr int kRselGroupThreads = 1024;
+__global__ void __launch_bounds__(kRselGroupThreads) rsel_group_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
+    const int32_t* __restrict__ goff, int G, const uint8_t* __restrict__ scales, int layout,
+    const float* __restrict__ st, const int32_t* __restrict__ sel, int k, int kpad,
+    float* __restrict__ rs, uint8_t* __restrict__ rcodes, uint8_t* __restrict__ rscales,
+    int rlayout, float* __restrict__ rst) {
+  __shared__ float red[kRselGroupThreads / 32];
+  const int ncols16 = cols >> 4, rcols16 = kpad >> 4;
+  const int vpr = kpad >> 3;   // 8-element vectors per residual row (even)
+  if ((int)blockIdx.x >= G) {
+    // rows past the last offset: zero codes and scales
+    const int64_t end = goff[G];
+    const int64_t total = (rows - end) * vpr;
+    for (int64_t i = (int64_t)(blockIdx.x - G) * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)(gridDim.x - G) * blockDim.x) {
+      const int64_t r = end + i / vpr;
+      const int col = (int)(i % vpr) * 8;
+      *reinterpret_cast<uint32_t*>(rcodes + r * (kpad >> 1) + (col >> 1)) = 0u;
+      if (((col >> 3) & 1) == 0) rscales[sf_offset(rlayout, r, col >> 4, rcols16)] = 0;
+    }
+    return;
+  }
+  const int g = blockIdx.x;
+  const int64_t r0 = goff[g], r1 = goff[g + 1];
+  const float s_t = st[g];
+  const int32_t* sg = sel + (int64_t)g * k;
+  const int total = (int)(r1 - r0) * k;
+  float m = 0.0f;
+  for (int i0 = threadIdx.x; i0 < total; i0 += 4 * blockDim.x) {
+    int64_t r[4];
+    int j[4], c[4];
+    float xv[4];
+    uint32_t sb[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * (int)blockDim.x;
+      r[u] = r0 + (i < total ? i / k : 0);
+      j[u] = i < total ? i % k : 0;
+      c[u] = sg[j[u]];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      xv[u] = __bfloat162float(x[r[u] * ldx + c[u]]);
+      sb[u] = scales[sf_offset(layout, r[u], c[u] >> 4, ncols16)];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * (int)blockDim.x;
+      if (i >= total) continue;
+      const BlockScale bs = block_scale_from_byte(sb[u], s_t);
+      float v[8] = {__fmul_rn(xv[u], bs.r), 0, 0, 0, 0, 0, 0, 0};
+      const uint32_t code = bs.zero ? 0u : (f32x8_to_e2m1(v) & 15u);
+      const float R = __fsub_rn(xv[u], __fmul_rn(e2m1_to_f32(code), bs.d));
+      rs[r[u] * k + j[u]] = R;
+      m = fmaxf(m, fabsf(R));
+    }
+  }
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();   // also makes this block's rs writes visible to the block
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+    v = warp_max(v);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float rs_t = tensor_scale_from_amax(red[0]);
+  if (threadIdx.x == 0) rst[g] = rs_t;
+  const int64_t nvec = (r1 - r0) * vpr;
+  // warp-uniform loop: lanes 2i / 2i+1 hold the two halves of one 16-block
+  for (int64_t base = (threadIdx.x & ~31); base < nvec; base += blockDim.x) {
+    const int64_t i = base + (threadIdx.x & 31);
+    const bool in = i < nvec;
+    const int64_t r = r0 + (in ? i / vpr : 0);
+    const int col = in ? (int)(i % vpr) * 8 : 0;
+    const bool live = in && col < k;
+    float f[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) f[jj] = 0.0f;
+    if (live) {
+      const float4* p = reinterpret_cast<const float4*>(rs + r * k + col);
+      const float4 a = p[0], b = p[1];
+      f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+      f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    }
+    float mm = 0.0f;
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) mm = fmaxf(mm, fabsf(f[jj]));
+    mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, 1));
+    const BlockScale bs = block_scale(mm, rs_t);
+    uint32_t cw = quantize8(f, bs);
+    uint32_t sbyte = bs.byte;
+    if (!live) { cw = 0u; sbyte = 0u; }
+    if (in) {
+      *reinterpret_cast<uint32_t*>(rcodes + r * (kpad >> 1) + (col >> 1)) = cw;
+      if (((col >> 3) & 1) == 0) rscales[sf_offset(rlayout, r, col >> 4, rcols16)] = (uint8_t)sbyte;
+    }
+  }
+}
+
 // Quantize the float32 residual slice [rows, k] (16-blocks along the selection)
 // into codes [rows, kpad/2] and scales (kpad columns, padding blocks 0).
 // One thread per 8 elements; lanes 2i/2i+1 share a block.
@@ -887,6 +996,16 @@ extern "C" quads_status_t quads_select_residual_channels(
                                                      long_groups ? nullptr : score_partials,
                                                      group_offsets, rows);
   if (quads_status_t s = sel_ready()) return s;
+  if (group_offsets && G >= kRselGroupMin) {
+    if (r_scale_layout == QUADS_SCALES_TCGEN05 && rows % 128) {
+      const int64_t start = (rows / 128) * (kpad / 64) * 512;
+      cudaMemsetAsync(r_scales + start, 0, (size_t)(sf_tc_bytes(rows, kpad) - start), st);
+    }
+    rsel_group_kernel<<<G + 2 * num_sms(), kRselGroupThreads, 0, st>>>(
+        (const __nv_bfloat16*)x, rows, (int)cols, ldx, group_offsets, G, scales, scale_layout,
+        tensor_scale, sel, k, kpad, rs, r_codes, r_scales, r_scale_layout, r_tensor_scale);
+    return check_launch("select", long_groups ? 3 : 2);
+  }
   cudaMemsetAsync(amax, 0, (size_t)G * 4, st);
   const int rb = (rows + 31) / 32 < 2 * (int64_t)num_sms() ? 8 : 32;
   rsel_residual_kernel<<<grid_for((rows + rb - 1) / rb, 1, 16), 256, 0, st>>>(

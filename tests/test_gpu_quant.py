@@ -264,3 +264,33 @@ def test_trace_1bit_worked_example_on_gpu(lib):
     codes, cnt = lib.trace_round_1bit(bf16_tensor(inputs.f32_to_bf16_bits(xt)), bits, rq)
     assert F.e2m1_decode(codes_np(codes, 16)[0, 0]) == 2.0
     assert cnt.cpu().tolist() == [1, 0]
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+def test_select_many_groups_one_block_per_group(lib, layout):
+    """40 row groups (the per-expert shape: one selection and one R_sel tensor
+    scale per group), with empty groups, uneven sizes and capacity rows past the
+    last offset, which must come out as zero codes and scales."""
+    rng = inputs.make_rng(9)
+    sizes = rng.choice([0, 32, 64, 96, 160, 256], size=40)
+    sizes[[3, 17]] = 0
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    end, cap = int(offs[-1]), int(offs[-1]) + 200
+    x = inputs.student_t4(rng, (cap, 256))
+    x[:, 11] *= 25
+    bits = inputs.f32_to_bf16_bits(x)
+    ot = torch.from_numpy(offs).cuda()
+    xt = bf16_tensor(bits)
+    q, part = lib.quantize_nvfp4(xt, group_offsets=ot, num_groups=40, scores=True, scale_layout=layout)
+    sel, _, r = lib.select_residual_channels(xt, q, part, 32, group_offsets=ot, num_groups=40,
+                                             r_scale_layout=layout)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    ref = Q.quantize_full(f32(bits[:end]), 32, offs)
+    assert np.array_equal(sel.cpu().numpy(), ref["sel"])
+    assert np.array_equal(r.tensor_scale.cpu().numpy(), ref["r_s_t"])
+    rc = codes_np(r.codes, 64)
+    rsc = linear_scales(r, cap, 64)
+    assert np.array_equal(rc[:end, :32], ref["r_codes"]) and not rc[:end, 32:].any()
+    assert np.array_equal(rsc[:end, :2], ref["r_scales"]) and not rsc[:end, 2:].any()
+    assert not rc[end:].any() and not rsc[end:].any()
