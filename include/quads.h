@@ -365,8 +365,8 @@ quads_status_t quads_weight_columns(const uint8_t* w_codes, const uint8_t* w_sca
  *   sel [k] shared by every group (sel_per_group = 0) or [num_groups, k];
  *     entries are column indices in [0, cols) (ascending, as
  *     quads_select_residual_channels writes them).
- *   w_sel_codes [num_groups*rows_per_group, kpad/2] (16-byte aligned),
- *   w_sel_scales TCGEN05 over kpad columns, kpad = quads_kpad(k); columns
+ *   w_sel_codes [num_groups*rows_per_group, kpad/2], w_sel_scales TCGEN05
+ *     over kpad columns (both 16-byte aligned), kpad = quads_kpad(k); columns
  *     k..kpad-1 get zero codes and scales.  Caller-owned.
  * rows_per_group % 128 == 0, cols % 64 == 0, 16 <= k <= cols, k % 16 == 0,
  * num_groups <= 65535.

@@ -1123,8 +1123,8 @@ extern "C" quads_status_t quads_select_weight_channels(
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "select_weight_channels: rows_per_group %% 128, cols %% 64, groups <= 65535");
   if (k <= 0 || k % 16 || k > cols)
     return fail(QUADS_ERR_INVALID_ARG, "select_weight_channels: need 16 <= k <= cols, k %% 16 == 0");
-  if (!al16(w_sel_codes) || !al16(codes_t) || !al16(scales_t))
-    return fail(QUADS_ERR_MISALIGNED, "select_weight_channels: codes_t, scales_t and w_sel_codes must be 16-byte aligned");
+  if (!al16(w_sel_codes) || !al16(w_sel_scales) || !al16(codes_t) || !al16(scales_t))
+    return fail(QUADS_ERR_MISALIGNED, "select_weight_channels: codes_t, scales_t, w_sel_codes and w_sel_scales must be 16-byte aligned");
   const int kpad = quads_kpad(k);
   gemm::launch_wsel(codes_t, scales_t, num_groups, (int)rows_per_group, (int)cols, sel,
                     sel_per_group, k, kpad, w_sel_codes, w_sel_scales, (cudaStream_t)stream);
