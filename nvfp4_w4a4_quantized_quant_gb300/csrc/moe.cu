@@ -279,6 +279,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
 }
 
 // out[t, :] = bf16(sum_j gate[t, j] * y[row(t, j), :]), float32, j ascending.
+// kTopk > 0: the slot count is known at compile time, so every slot's row
+// index and then every slot's y vector are loaded before the sum (kTopk
+// loads in flight per thread); the sum itself keeps the same order.
+template <int kTopk>
 __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __restrict__ y,
                                                       int64_t ldy,
                                                       const int32_t* __restrict__ token_row,
@@ -292,13 +296,33 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
     const int t = (int)(i / vec);
     const int c = (int)(i % vec) * 8;
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int j = 0; j < topk; ++j) {
-      const int r = token_row[(int64_t)t * topk + j];
-      const float g = gates[(int64_t)t * topk + j];
-      float f[8];
-      bf16x8_to_f32(*reinterpret_cast<const uint4*>(y + (int64_t)r * ldy + c), f);
+    if (kTopk > 0) {
+      int r[kTopk > 0 ? kTopk : 1];
+      float g[kTopk > 0 ? kTopk : 1];
+      uint4 v[kTopk > 0 ? kTopk : 1];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = fmaf(g, f[q], acc[q]);
+      for (int j = 0; j < kTopk; ++j) {
+        r[j] = token_row[(int64_t)t * kTopk + j];
+        g[j] = gates[(int64_t)t * kTopk + j];
+      }
+#pragma unroll
+      for (int j = 0; j < kTopk; ++j) v[j] = *reinterpret_cast<const uint4*>(y + (int64_t)r[j] * ldy + c);
+#pragma unroll
+      for (int j = 0; j < kTopk; ++j) {
+        float f[8];
+        bf16x8_to_f32(v[j], f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = fmaf(g[j], f[q], acc[q]);
+      }
+    } else {
+      for (int j = 0; j < topk; ++j) {
+        const int r = token_row[(int64_t)t * topk + j];
+        const float g = gates[(int64_t)t * topk + j];
+        float f[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(y + (int64_t)r * ldy + c), f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = fmaf(g, f[q], acc[q]);
+      }
     }
     uint32_t pk[4];
 #pragma unroll
@@ -377,7 +401,12 @@ extern "C" quads_status_t quads_moe_combine(const void* y, int64_t ldy, const in
   cudaStream_t st = (cudaStream_t)stream;
   const int64_t work = (int64_t)tokens * (hidden / 8);
   const int blocks = (int)std::min<int64_t>((work + 255) / 256, (int64_t)num_sms() * 8);
-  combine_kernel<<<blocks, 256, 0, st>>>((const __nv_bfloat16*)y, ldy, token_row, gates, tokens,
+  auto kernel = topk == 8   ? combine_kernel<8>
+                : topk == 4 ? combine_kernel<4>
+                : topk == 2 ? combine_kernel<2>
+                : topk == 1 ? combine_kernel<1>
+                            : combine_kernel<0>;
+  kernel<<<blocks, 256, 0, st>>>((const __nv_bfloat16*)y, ldy, token_row, gates, tokens,
                                          topk, (int)hidden, (__nv_bfloat16*)out, ldo);
   return check_launch("moe_combine", 1);
 }
