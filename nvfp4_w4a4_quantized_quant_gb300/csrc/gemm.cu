@@ -98,6 +98,7 @@ struct Params {
   void* y;
   int64_t ldy;
   int out_mode;
+  int st32;                     // y rows and base 32-byte aligned: one 32-byte store per 16 bf16
   uint32_t* y_amax;             // nullable [E]: max |stored y| per group (float bits)
   int* err;
 };
@@ -210,6 +211,13 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
           "r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// One 32-byte store (a whole sector) from eight 32-bit words.
+__device__ __forceinline__ void st_global_32B(void* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -642,9 +650,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             amax = fmaxf(amax, fmaxf(fabsf(hr.x), fabsf(hr.y)));
           }
           if (store) {
-            uint4* dst = reinterpret_cast<uint4*>(y + c0);
-            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            if (p.st32) {
+              st_global_32B(y + c0, packed);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(y + c0);
+              dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+              dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            }
           }
         }
         if (!store) amax = 0.0f;
@@ -667,10 +679,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int i = 0; i < 16; ++i) o[i] = p.comp ? fmaf(a2, v2[i], a1 * v1[i]) : a1 * v1[i];
           if (store) {
             if (p.out_mode == OUT_F32) {
-              float4* dst = reinterpret_cast<float4*>((float*)p.y + row * p.ldy + tl.n0 + c0);
+              float* yrow = (float*)p.y + row * p.ldy + tl.n0 + c0;
+              if (p.st32) {
+                st_global_32B(yrow, reinterpret_cast<const uint32_t*>(o));
+                st_global_32B(yrow + 8, reinterpret_cast<const uint32_t*>(o + 8));
+              } else {
+                float4* dst = reinterpret_cast<float4*>(yrow);
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                for (int i = 0; i < 4; ++i)
+                  dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+              }
 #pragma unroll
               for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(o[i]));
             } else {
@@ -682,9 +700,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float2 hr = __bfloat1622float2(hb);
                 amax = fmaxf(amax, fmaxf(fabsf(hr.x), fabsf(hr.y)));
               }
-              uint4* dst = reinterpret_cast<uint4*>((__nv_bfloat16*)p.y + row * p.ldy + tl.n0 + c0);
-              dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-              dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+              __nv_bfloat16* yrow = (__nv_bfloat16*)p.y + row * p.ldy + tl.n0 + c0;
+              if (p.st32) {
+                st_global_32B(yrow, packed);
+              } else {
+                uint4* dst = reinterpret_cast<uint4*>(yrow);
+                dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+              }
             }
           }
         }
@@ -941,6 +964,12 @@ static quads_status_t launch(const Launch& L) {
   p.comp = comp ? 1 : 0;
   p.mx = L.mx;
   p.y = L.y; p.ldy = L.ldy; p.out_mode = L.out_mode;
+  {
+    // 32-byte stores need every row start and column offset on a 32-byte
+    // boundary: tiles start at multiples of 128 columns (64 for SwiGLU output)
+    const int64_t esz = L.out_mode == OUT_F32 ? 4 : 2;
+    p.st32 = ((uintptr_t)L.y % 32 == 0 && (L.ldy * esz) % 32 == 0) ? 1 : 0;
+  }
   p.y_amax = (uint32_t*)L.y_amax;
   if (L.y_amax) cudaMemsetAsync(L.y_amax, 0, (size_t)L.E * 4, L.stream);
   static int* errp = nullptr;
