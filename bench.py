@@ -54,7 +54,7 @@ def gemm1_bytes(w=WORKLOAD) -> float:
 # DRAM traffic (read + write) of one GEMM1 launch at this workload, from the
 # ncu capture summarised in profiles/gemm1_moe_swiglu_8192tok_ncu.md; reset to
 # None whenever gemm_kernel changes until a new capture is taken.
-GEMM1_TRAFFIC_BYTES = 320.427776e6 + 89.476608e6
+GEMM1_TRAFFIC_BYTES = 320.36224e6 + 91.823616e6
 
 
 def peaks():
