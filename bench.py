@@ -23,6 +23,7 @@ import json
 import math
 import os
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -77,7 +78,7 @@ class ClockSampler:
 
     def start(self):
         try:
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+            self.path = os.path.join(tempfile.gettempdir(), f"quads_clocks_{os.getpid()}.csv")
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
