@@ -1,16 +1,21 @@
 // Activation-side kernels: tensor amax, NVFP4 RTN quantization with fused
-// residual-energy partials, top-k residual channel selection, the second
-// quantization of the residual slice, and TRACE rollout-guided rounding.
+// residual-energy partials (and the trainer's W4A16 fake quantization), top-k
+// residual channel selection, the second quantization of the residual slice,
+// TRACE rollout-guided rounding (full rollout codes or the 1-bit record), and
+// the MXFP4 quantizer.
 //
 // [TRACE digest] "NVFP4 与 E2M1 码本": per-tensor scale + per-block scale, RTN.
-// [QUADS technical summary] 2.1: Delta X_q = X - DQ(Q(X)); 2.2 B "Mechanism":
+// [QUADS technical summary] 2.1: Delta X_q = X - DQ(Q(X)); 2.2 A: asymmetric
+// W4A16 QAT (weights fake-quantized on the trainer); 2.2 B "Mechanism":
 // second-pass quantization of the channels with the largest FP4 error;
 // "Implementation": a channel mask picks the top channels by residual magnitude.
-// [TRACE digest] "核心方法", Eq. (3): q_TRACE = argmin_{q in {q-, q+}} |q - q_rollout|.
+// [TRACE digest] "核心方法", Eq. (3): q_TRACE = argmin_{q in {q-, q+}} |q - q_rollout|;
+// the mantissa-only record; "技术新颖性": also validated on MXFP4.
 //
-// All of these are HBM-bound: 16-byte vector loads (8 bf16 per lane), warp
-// shuffles for the 16-element block maximum, no shared-memory staging needed
-// because every byte is read once and used in registers.
+// The streaming kernels read every byte once with 16-byte vector loads (8 bf16
+// per lane) and take 16-element block maxima with warp shuffles; shared memory
+// is used where values must be re-ordered: the residual squares summed per
+// column in row order, and the top-k histograms.
 #include <cstdio>
 
 #include "common.cuh"
