@@ -30,8 +30,12 @@
 //               ld.shared instead stalls for ~1-7K cycles while the MMAs
 //               stream their operands (they take the whole smem bandwidth),
 //               and loading them from global memory exposes L2 latency.
-//   warps 8-15  epilogue: tcgen05.ld of both accumulators, scale, store; two
-//               warps per TMEM lane quadrant, each owning half of the columns.
+//   warps 8-15  epilogue: tcgen05.ld of both accumulators, scale, store (one
+//               32-byte store per 16 bf16 outputs of a row when the rows are
+//               32-byte aligned); two warps per TMEM lane quadrant, each owning
+//               half of the columns.
+// MXFP4 operands (E8M0 scale per 32 elements, no tensor scales) run through the
+// same kernel with kind::mxf4 MMAs and one scale atom per two K steps.
 // TMEM columns: acc1 double-buffered (0-127, 128-255), acc2 (256-383),
 // scale-factor ring (384-511, 2 buffers x 64 columns).
 // Every mbarrier wait is bounded; on timeout the kernel latches an error word,
