@@ -116,3 +116,13 @@ def test_product_path_never_imports_the_oracle():
     for f in list(pkg.glob("*.py")) + list(pkg.glob("csrc/*")):
         text = f.read_text()
         assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
+    """No CPU fallback: with the shared library absent the binding raises
+    before any computation instead of answering from another code path."""
+    import pytest
+    from nvfp4_w4a4_quantized_quant_gb300 import quads as Q
+    monkeypatch.setattr(Q, "_lib", None)     # restored after the test
+    with pytest.raises(RuntimeError, match="not built"):
+        Q.load(str(tmp_path / "missing.so"))
