@@ -294,3 +294,25 @@ def test_select_many_groups_one_block_per_group(lib, layout):
     assert np.array_equal(rc[:end, :32], ref["r_codes"]) and not rc[:end, 32:].any()
     assert np.array_equal(rsc[:end, :2], ref["r_scales"]) and not rsc[:end, 2:].any()
     assert not rc[end:].any() and not rsc[end:].any()
+
+
+def test_w4a16_qdq_full_expert_stack_sampled_experts(lib):
+    """The benchmark's QDQ configuration: the 128 experts' gate/up weights
+    (196608 x 2048, one tensor scale per expert); three experts checked bit for
+    bit (their groups are quantized independently of the others)."""
+    E, R, H = 128, 1536, 2048
+    g = torch.Generator(device="cuda")
+    g.manual_seed(2)
+    w = (torch.randn((E * R, H), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    offs = torch.arange(0, E * R + 1, R, dtype=torch.int32, device="cuda")
+    y, q = lib.qdq_nvfp4(w, group_offsets=offs, num_groups=E, want_codes=True)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    ts = q.tensor_scale.cpu().numpy()
+    for e in (0, 63, 127):
+        rows = slice(e * R, (e + 1) * R)
+        bits = w[rows].view(torch.int16).cpu().numpy().view(np.uint16)
+        oy, oc, osc, ost = Q.qdq(f32(bits))
+        assert ts[e] == ost[0]
+        assert np.array_equal(y[rows].view(torch.int16).cpu().numpy().view(np.uint16), oy)
+        assert np.array_equal(codes_np(q.codes[rows], H), oc)
