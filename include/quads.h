@@ -246,7 +246,12 @@ quads_status_t quads_select_residual_channels(
  *     k, num_groups), exceeds the array are rejected with QUADS_ERR_WORKSPACE.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make that
- *     first call before any stream capture.
+ *     first call before any stream capture.  The cached address belongs to the
+ *     device's context at that time: calls after cudaDeviceReset (or anything
+ *     else that replaces the device's primary context) are not supported.
+ *   - Argument checks and their status codes are those of
+ *     quads_select_residual_channels; a valid shape whose scratch does not fit
+ *     the array then returns QUADS_ERR_WORKSPACE.
  *   - Every call on a device uses the same array, which keeps the previous
  *     call's contents (the parts that must start at zero are cleared by each
  *     call).  Calls that overlap on the GPU -- on different streams, or from

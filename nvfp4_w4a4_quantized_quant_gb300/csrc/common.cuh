@@ -25,6 +25,12 @@ void set_detail(const char* fmt, ...);
 quads_status_t fail(quads_status_t s, const char* fmt, ...);
 quads_status_t check_launch(const char* what, int kernels_launched);
 int num_sms();
+quads_status_t select_check_args(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                                 const int32_t* group_offsets, int32_t num_groups,
+                                 const uint8_t* scales, const float* tensor_scale,
+                                 const float* score_partials, int32_t k, const int32_t* sel,
+                                 const uint8_t* r_codes, const uint8_t* r_scales,
+                                 const float* r_tensor_scale, size_t* need);
 
 // ------------------------------------------------------------ scale layouts
 // Byte offset of scale column c (a 16-element block) of row r in the

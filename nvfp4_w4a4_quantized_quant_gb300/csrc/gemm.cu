@@ -45,6 +45,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -977,17 +978,28 @@ static quads_status_t launch(const Launch& L) {
   p.y_amax = (uint32_t*)L.y_amax;
   if (L.y_amax) cudaMemsetAsync(L.y_amax, 0, (size_t)L.E * 4, L.stream);
   // the error word's address and the shared-memory attribute are per device
-  static int* errp[64] = {nullptr};
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return fail(QUADS_ERR_CUDA, "gemm: device ordinal %d out of range", dev);
-  if (!errp[dev] && cudaGetSymbolAddress((void**)&errp[dev], g_gemm_error) != cudaSuccess)
-    return fail(QUADS_ERR_CUDA, "gemm: cannot resolve the device error word");
-  p.err = errp[dev];
-  if (!attr_set[dev]) {
-    cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    attr_set[dev] = true;
+  // (resolved on the first launch on a device; calls after cudaDeviceReset
+  // are not supported)
+  {
+    static std::mutex mu;
+    static int* errp[64] = {nullptr};
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+      return fail(QUADS_ERR_CUDA, "gemm: no usable current device (ordinal %d)", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!errp[dev] && cudaGetSymbolAddress((void**)&errp[dev], g_gemm_error) != cudaSuccess) {
+      errp[dev] = nullptr;
+      return fail(QUADS_ERR_CUDA, "gemm: cannot resolve the device error word");
+    }
+    p.err = errp[dev];
+    if (!attr_set[dev]) {
+      const cudaError_t e =
+          cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+      if (e != cudaSuccess)
+        return fail(QUADS_ERR_CUDA, "gemm: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+      attr_set[dev] = true;
+    }
   }
   int64_t grid = num_sms();
   if (!L.row_off) grid = std::min<int64_t>(grid, ((L.M + BM - 1) / BM) * (L.N / BN));

@@ -52,11 +52,13 @@ extern "C" quads_status_t quads_select_residual_channels_noalloc(
     int32_t num_groups, const uint8_t* scales, int32_t scale_layout, const float* tensor_scale,
     const float* score_partials, int32_t k, int32_t* sel, float* scores_out, uint8_t* r_codes,
     uint8_t* r_scales, int32_t r_scale_layout, float* r_tensor_scale, void* stream) {
-  const int G = group_offsets ? num_groups : 1;
-  if (rows < 0 || cols <= 0 || k <= 0 || G < 1)
-    return fail(QUADS_ERR_INVALID_ARG, "select_noalloc: bad shape");
-  const size_t need = quads_workspace_size(QUADS_OP_SELECT, rows, cols, 0, k, G);
-  if (need > (size_t)QUADS_NOALLOC_SELECT_SCRATCH_BYTES)
+  // the same argument checks, in the same order, as the workspace entry point
+  size_t need = 0;
+  if (quads_status_t s = select_check_args(x, rows, cols, ldx, group_offsets, num_groups, scales,
+                                           tensor_scale, score_partials, k, sel, r_codes,
+                                           r_scales, r_tensor_scale, &need))
+    return s;
+  if (rows > 0 && need > (size_t)QUADS_NOALLOC_SELECT_SCRATCH_BYTES)
     return fail(QUADS_ERR_WORKSPACE,
                 "select_noalloc: this shape needs %zu bytes of scratch, the built-in array holds %zu "
                 "(rows*k*4 + per-group maxima + groups*cols*4 must fit)",

@@ -958,12 +958,16 @@ extern "C" quads_status_t quads_qdq_nvfp4(
                        (__nv_bfloat16*)y, ldy, workspace, workspace_bytes, stream);
 }
 
-extern "C" quads_status_t quads_select_residual_channels(
-    const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* group_offsets,
-    int32_t num_groups, const uint8_t* scales, int32_t scale_layout, const float* tensor_scale,
-    const float* score_partials, int32_t k, int32_t* sel, float* scores_out, uint8_t* r_codes,
-    uint8_t* r_scales, int32_t r_scale_layout, float* r_tensor_scale, void* workspace,
-    size_t workspace_bytes, void* sel_ready_event, void* stream) {
+namespace quads {
+// Argument checks of the selection call (shared by the workspace and the
+// allocation-free entry points, so that both report the same status for the
+// same arguments); on success *need is the scratch the call uses.
+quads_status_t select_check_args(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                                 const int32_t* group_offsets, int32_t num_groups,
+                                 const uint8_t* scales, const float* tensor_scale,
+                                 const float* score_partials, int32_t k, const int32_t* sel,
+                                 const uint8_t* r_codes, const uint8_t* r_scales,
+                                 const float* r_tensor_scale, size_t* need) {
   if (rows > 0 && (!x || !scales || !tensor_scale || !score_partials || !sel || !r_codes ||
                    !r_scales || !r_tensor_scale))
     return fail(QUADS_ERR_INVALID_ARG, "select: null pointer argument");
@@ -972,9 +976,25 @@ extern "C" quads_status_t quads_select_residual_channels(
   if (k <= 0 || k % 16 || k > cols)
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "select: k=%d must be a multiple of 16 in [16, cols]", k);
   if (ldx < cols) return fail(QUADS_ERR_MISALIGNED, "select: ldx < cols");
+  if (group_offsets && num_groups < 1) return fail(QUADS_ERR_INVALID_ARG, "select: num_groups < 1");
+  *need = quads_workspace_size(QUADS_OP_SELECT, rows, cols, 0, k, group_offsets ? num_groups : 1);
+  return QUADS_OK;
+}
+}  // namespace quads
+
+extern "C" quads_status_t quads_select_residual_channels(
+    const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* group_offsets,
+    int32_t num_groups, const uint8_t* scales, int32_t scale_layout, const float* tensor_scale,
+    const float* score_partials, int32_t k, int32_t* sel, float* scores_out, uint8_t* r_codes,
+    uint8_t* r_scales, int32_t r_scale_layout, float* r_tensor_scale, void* workspace,
+    size_t workspace_bytes, void* sel_ready_event, void* stream) {
+  size_t need = 0;
+  if (quads_status_t s = select_check_args(x, rows, cols, ldx, group_offsets, num_groups, scales,
+                                           tensor_scale, score_partials, k, sel, r_codes,
+                                           r_scales, r_tensor_scale, &need))
+    return s;
   const int G = group_offsets ? num_groups : 1;
   const int kpad = quads_kpad(k);
-  const size_t need = quads_workspace_size(QUADS_OP_SELECT, rows, cols, 0, k, G);
   if (rows > 0 && (!workspace || workspace_bytes < need))
     return fail(QUADS_ERR_WORKSPACE, "select: workspace needs %zu bytes", need);
   cudaStream_t st = (cudaStream_t)stream;

@@ -95,6 +95,10 @@ class MoEExpertLayer:
         kp1, kp2 = Q.kpad(k1), Q.kpad(k2)
         u8, f32, i32 = torch.uint8, torch.float32, torch.int32
         e = lambda *s, dt=u8: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
+        # h and y: rows past the last expert's group (and y's padding rows) are
+        # never written by the kernels; zeroed once here so that whole-buffer
+        # reads see zeros rather than stale memory
+        z = lambda *s, dt: torch.zeros(*s, dtype=dt, device=dev)  # noqa: E731
         self.b = dict(
             route=dict(idx=e((T, topk), dt=i32), gates=e((T, topk), dt=f32), counts=e(E, dt=i32),
                        offsets=e(E + 1, dt=i32), row_token=e(cap, dt=i32),
@@ -103,12 +107,12 @@ class MoEExpertLayer:
             sel1=e((1, k1), dt=i32), r1c=e((T, kp1 // 2)), r1s=e(T * (kp1 // 16)), r1ts=e(1, dt=f32),
             a1c=e((cap, H // 2)), a1s=e(Q.sf_tc_bytes(cap, H)),
             g1c=e((cap, kp1 // 2)), g1s=e(Q.sf_tc_bytes(cap, kp1)),
-            h=e((cap, F), dt=torch.bfloat16),
+            h=z((cap, F), dt=torch.bfloat16),
             hc=e((cap, F // 2)), hs=e(Q.sf_tc_bytes(cap, F)), hts=e(E, dt=f32),
             hpart=e((cap // 32, F), dt=f32),
             sel2=e((E, k2), dt=i32), r2c=e((cap, kp2 // 2)), r2s=e(Q.sf_tc_bytes(cap, kp2)),
             r2ts=e(E, dt=f32), hamax=e(E, dt=f32),
-            y=e((cap, H), dt=torch.bfloat16), out=e((T, H), dt=torch.bfloat16),
+            y=z((cap, H), dt=torch.bfloat16), out=e((T, H), dt=torch.bfloat16),
             w1sc=e((E * 2 * F, kp1 // 2)), w1ss=e(Q.sf_tc_bytes(E * 2 * F, kp1)),
             w2sc=e((E * H, kp2 // 2)), w2ss=e(Q.sf_tc_bytes(E * H, kp2)),
         )

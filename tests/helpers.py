@@ -48,3 +48,17 @@ def swizzle_np(lin: np.ndarray, rows: int, cols: int) -> np.ndarray:
     off = ((r // 128) * (n16 // 4) + c // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + c % 4
     out[off] = lin
     return out
+
+
+def check_combine(out, idx, gates, y_slots):
+    """The GPU's combined output against the oracle's combine on the same gates
+    and expert outputs.  Both sides round to bf16, the GPU after a float32 sum,
+    the oracle after a float64 one, so an element may land one bf16 step away
+    (2^-7 of its magnitude) where the float32 sum crosses a rounding boundary;
+    such flips must be rare."""
+    from oracle import moe as M
+    ref = M.combine(idx, gates, y_slots)
+    out = np.asarray(out, np.float64)
+    mag = np.abs(y_slots.astype(np.float64)).sum(1)
+    assert np.all(np.abs(out - ref) <= 2.0 ** -7 * np.abs(ref) + 1e-5 * mag + 1e-30)
+    assert np.mean(out == ref) >= 0.999

@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import codes_np, f32, unswizzle
+from helpers import check_combine, codes_np, f32, unswizzle
 from nvfp4_w4a4_quantized_quant_gb300 import inputs
 from oracle import moe as M
 from test_gpu_moe import _h_tol, _layer
@@ -111,14 +111,12 @@ def _sampled_check(lib, d, k1, k2, experts):
         Y2, B2 = ref2["y2"][e], ref2["b2"][e]
         assert np.all(np.abs(y[rows].astype(np.float64) - Y2) <= 1e-3 * B2 + 2.0 ** -8 * np.abs(Y2) + 1e-30)
 
-    # --- combine over every token, on the GPU's y
+    # --- combine over every token (the oracle's, on the GPU's gates and y)
     out = res["out"].float().cpu().numpy()
-    gates = plan["gates"].cpu().numpy().astype(np.float64)
+    gates = plan["gates"].cpu().numpy()
     for t0 in range(0, T, 512):
         ts = slice(t0, min(T, t0 + 512))
-        ysl = y[trow[ts]].astype(np.float64)                 # [t, topk, H]
-        exp = np.einsum("tj,tjh->th", gates[ts], ysl)
-        assert np.all(np.abs(out[ts] - exp) <= 2.0 ** -8 * np.abs(exp) + 1e-5 * np.abs(ysl).sum(1) + 1e-30)
+        check_combine(out[ts], oidx[ts], gates[ts], y[trow[ts]])
 
 
 def test_moe_prefill_8192_tokens_sampled_experts(lib):

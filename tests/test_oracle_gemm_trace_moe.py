@@ -217,3 +217,68 @@ def test_dispatch_covers_every_slot_once():
     assert sum(len(t) for t in toks) == 150
     for e, t in enumerate(toks):
         assert np.all(np.diff(t) > 0) and all(e in idx[i] for i in t)
+
+
+def test_silu_mul_matches_torch_silu_and_closed_forms():
+    # an independent library: torch's SiLU in float64, on a dense grid out to +-80
+    g = np.concatenate([np.linspace(-80.0, 80.0, 4001), [-1e-300, 0.0, 1e-300, 1e-3, -1e-3]])
+    u = np.linspace(-3.0, 5.0, g.size)
+    ref = torch.nn.functional.silu(torch.from_numpy(g)).numpy() * u
+    assert np.allclose(M.silu_mul(g, u), ref, rtol=1e-14, atol=1e-300)
+    one = np.ones(1)
+    assert M.silu_mul(np.zeros(1), one)[0] == 0.0                       # silu(0) = 0
+    assert M.silu_mul(np.array([40.0]), one)[0] / 40.0 == 1.0           # silu(g)/g -> 1
+    neg = M.silu_mul(np.array([-40.0]), one)[0]                         # silu(g) -> 0 from below
+    assert -1e-15 < neg < 0.0
+    assert abs(neg - (-40.0 * np.exp(-40.0))) <= 1e-12 * abs(neg)
+    # sigma(-g) = 1 - sigma(g)  =>  silu(-g) = silu(g) - g
+    gg = np.linspace(-12.0, 12.0, 97)
+    assert np.allclose(M.silu_mul(-gg, np.ones_like(gg)), M.silu_mul(gg, np.ones_like(gg)) - gg,
+                       rtol=0, atol=1e-13)
+    # the second operand multiplies: silu(g) * u, not silu(u) * g
+    assert np.isclose(M.silu_mul(np.array([2.0]), np.array([-3.0]))[0],
+                      -3.0 * 2.0 / (1.0 + np.exp(-2.0)), rtol=1e-15)
+
+
+def test_w1_rows_are_gate_then_up():
+    # W1 of one expert with F = 16: rows [0, 16) (gate) pick -4 * x0, rows
+    # [16, 32) (up) pick +4 * x0.  With x0 = 2 the gate is -8 and the up value
+    # 8, so h = silu(-8) * 8 ~ -0.0215; the swapped reading silu(8) * (-8)
+    # would give ~ -7.997.  +-4 is the matrix's absolute maximum, so it is
+    # represented exactly up to the float32 rounding of the scales.
+    T_, H, Fd = 8, 32, 16
+    x = np.zeros((T_, H), np.float32)
+    x[:, 0] = 2.0
+    x[:, 1] = 1.0                     # a second non-zero channel keeps the blocks non-trivial
+    w1 = np.zeros((1, 2 * Fd, H), np.float32)
+    w1[0, :Fd, 0] = -4.0
+    w1[0, Fd:, 0] = 4.0
+    w2 = np.zeros((1, H, Fd), np.float32)
+    w2[0, :, 0] = 1.0
+    w1q, w2q = M.quantize_weights(w1), M.quantize_weights(w2)
+    res = M.moe_layer(x, np.zeros((T_, 1), np.float32), w1q, w2q, 16, 16, topk=1)
+    y1 = res["y1"][0]
+    assert np.allclose(y1[:, :Fd], -8.0, rtol=1e-5) and np.allclose(y1[:, Fd:], 8.0, rtol=1e-5)
+    want = -8.0 / (1.0 + np.exp(8.0)) * 8.0
+    assert np.allclose(res["h"][0], want, rtol=2e-2)
+
+
+def test_chunk_partials_add_up_to_channel_scores():
+    # groups starting at multiples of the 32-row chunk: adding a group's chunk
+    # partials in ascending chunk order from 0 in float32 is the score, bit for bit
+    rng = np.random.default_rng(11)
+    rows, cols = 221, 48
+    R = (rng.standard_normal((rows, cols)) * 10.0 ** rng.integers(-3, 3, (rows, cols))).astype(np.float32)
+    offs = np.array([0, 64, 96, 192, rows], np.int32)
+    part = Q.chunk_partials(R)
+    assert part.shape == ((rows + 31) // 32, cols)
+    scores = Q.channel_scores(R, offs)
+    for g in range(len(offs) - 1):
+        a, b = int(offs[g]), int(offs[g + 1])
+        acc = np.zeros(cols, np.float32)
+        for c in range(a // 32, (b + 31) // 32):
+            acc = (acc + part[c]).astype(np.float32)
+        assert np.array_equal(acc.view(np.uint32), scores[g].view(np.uint32))
+    # and each partial is its own rows' sum of squares (float64 agreement)
+    ref = np.add.reduceat((R.astype(np.float64) ** 2), np.arange(0, rows, 32), axis=0)
+    assert np.allclose(part, ref, rtol=1e-5)

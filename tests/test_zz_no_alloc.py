@@ -65,3 +65,16 @@ def test_noalloc_rejects_shapes_beyond_the_builtin_scratch(lib):
     st = raw.quads_select_residual_channels_noalloc(p, rows, cols, cols, None, 1, p, 0, p, p, k,
                                                     p, None, p, p, 0, p, None)
     assert st == 7 and b"built-in array" in raw.quads_last_error_detail()
+
+
+def test_noalloc_reports_the_same_status_as_the_workspace_entry_point(lib):
+    # bad shapes are refused before the scratch is considered, with the codes
+    # the workspace entry point returns for the same arguments
+    raw = lib.load()
+    p = ctypes.c_void_p(256)
+    for rows, cols, k in [(64, 256, 0), (64, 256, 24), (64, 250, 16), (64, 256, 512)]:
+        st_ws = raw.quads_select_residual_channels(p, rows, cols, cols, None, 1, p, 0, p, p, k,
+                                                   p, None, p, p, 0, p, p, 1 << 20, None, None)
+        st_na = raw.quads_select_residual_channels_noalloc(p, rows, cols, cols, None, 1, p, 0, p,
+                                                           p, k, p, None, p, p, 0, p, None)
+        assert st_ws == st_na != 0, (rows, cols, k, st_ws, st_na)
