@@ -198,6 +198,12 @@ def secondary(torch, Q, steps, flush, stream):
     from nvfp4_w4a4_quantized_quant_gb300 import inputs
     from nvfp4_w4a4_quantized_quant_gb300.layer import CompensatedLinear, MoEExpertLayer
 
+    def check(tag):
+        code = Q.device_status(stream)
+        if code:
+            raise RuntimeError(f"{tag}: device status {code}: "
+                               f"{Q.load().quads_last_error_detail().decode()}")
+
     def graph_ms(fn):
         with torch.cuda.stream(stream):
             fn()
@@ -209,7 +215,9 @@ def secondary(torch, Q, steps, flush, stream):
             for _ in range(3):
                 g.replay()
             torch.cuda.synchronize()
-            return timed(torch, g.replay, steps, flush, stream) / steps
+            ms = timed(torch, g.replay, steps, flush, stream) / steps
+        check("secondary")
+        return ms
 
     out = {}
     d = inputs.dense_projection(0)
@@ -280,9 +288,17 @@ def secondary(torch, Q, steps, flush, stream):
         ms = graph_ms(lambda: Q.quantize_nvfp4(xq_in, scores=True, workspace=wsq,
                                                out=(qo.codes, qo.scales, qo.tensor_scale, po),
                                                stream=stream))
+        # the quantize pass alone, with the tensor scale given (as when the
+        # producer already knows the amax): x is read once
+        ms1 = graph_ms(lambda: Q.quantize_nvfp4(xq_in, scores=True, workspace=wsq,
+                                                tensor_scale_in=qo.tensor_scale,
+                                                out=(qo.codes, qo.scales, qo.tensor_scale, po),
+                                                stream=stream))
         qb = rows_q * Hq * (2 + 0.5 + 1.0 / 16) + (rows_q // 32) * Hq * 4
         sweep.append({"rows": rows_q, "cols": Hq, "input_mib": rows_q * Hq * 2 >> 20,
-                      "ms": round(ms, 4), "gbs": round(qb / (ms * 1e-3) / 1e9, 1)})
+                      "ms": round(ms, 4), "gbs": round(qb / (ms * 1e-3) / 1e9, 1),
+                      "ms_scale_given": round(ms1, 4),
+                      "gbs_scale_given": round(qb / (ms1 * 1e-3) / 1e9, 1)})
         del xq_in, wsq, qo, po
     out["quantizer_sweep"] = sweep
 
@@ -404,7 +420,8 @@ def run_gpu(args):
         with torch.cuda.graph(graph, stream=stream):
             layer.forward(x, logits)
         torch.cuda.synchronize()
-        assert Q.device_status(stream) == 0
+        code = Q.device_status(stream)
+        assert code == 0, f"device status {code}: {Q.load().quads_last_error_detail().decode()}"
 
     def step():
         graph.replay()
@@ -505,6 +522,7 @@ def run_gpu(args):
         wq["frac_hbm"] = round(wq["gbs"] / pk["hbm"], 4)
         for row in sec["quantizer_sweep"]:
             row["frac_hbm"] = round(row["gbs"] / pk["hbm"], 4)
+            row["frac_hbm_scale_given"] = round(row["gbs_scale_given"] / pk["hbm"], 4)
     fl = moe_flops()
     value = world * fl / (ms * 1e-3) / 1e12
     e2e_val = world * fl / (e_ms * 1e-3) / 1e12
@@ -564,20 +582,43 @@ def run_gpu(args):
 
 
 def run_profile(args):
-    """A plain sequence of eager forward passes (no graph, no flush, no clock
-    sampling) for an ncu launch list or a single-kernel capture."""
+    """Plain sequences of eager calls (no graph, no flush, no clock sampling)
+    for an ncu launch list or a single-kernel capture:
+      moe     the MoE expert layer step (8192 tokens)
+      dense   the compensated dense projection 4096x2048 x 6144x2048, k = 128
+      decode  the MoE expert layer on 512 tokens"""
+    import numpy as np
     import torch
+    from nvfp4_w4a4_quantized_quant_gb300 import inputs
     from nvfp4_w4a4_quantized_quant_gb300 import quads as Q
+    from nvfp4_w4a4_quantized_quant_gb300.layer import CompensatedLinear, MoEExpertLayer
     torch.cuda.set_device(0)
     Q.load()
-    layer, x_host, l_host = build_layer(torch)
-    x, logits = x_host.cuda(), l_host.cuda()
+    if args.profile == "dense":
+        d = inputs.dense_projection(0)
+        x = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).cuda()
+        w = torch.from_numpy(d["w"].view(np.int16)).view(torch.bfloat16).cuda()
+        lin = CompensatedLinear(w, 128, x.shape[0])
+        step = lambda: lin.forward(x)  # noqa: E731
+    else:
+        w = dict(WORKLOAD, tokens=512) if args.profile == "decode" else WORKLOAD
+        d = inputs.moe_layer(0, tokens=w["tokens"], hidden=w["hidden"], experts=w["experts"],
+                             topk=w["topk"], ffn=w["ffn"], k=w["k1"], with_weights=False)
+        g = torch.Generator(device="cuda")
+        g.manual_seed(0)
+        E, H, F = w["experts"], w["hidden"], w["ffn"]
+        w1 = (torch.randn((E, 2 * F, H), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+        w2 = (torch.randn((E, H, F), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+        layer = MoEExpertLayer(w1, w2, w["topk"], w["k1"], w["k2"], w["tokens"])
+        x = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).cuda()
+        logits = torch.from_numpy(d["logits"]).cuda()
+        step = lambda: layer.forward(x, logits)  # noqa: E731
     torch.cuda.synchronize()
     for _ in range(args.warmup + args.steps):
-        layer.forward(x, logits)
+        step()
     torch.cuda.synchronize()
     assert Q.device_status() == 0
-    print(json.dumps({"profile_steps": args.warmup + args.steps,
+    print(json.dumps({"profile": args.profile, "profile_steps": args.warmup + args.steps,
                       "launches": Q.kernel_launch_count()}))
 
 
@@ -613,8 +654,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="libquads", choices=["libquads", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", action="store_true",
-                    help="eager steps only, for ncu launch lists / captures")
+    ap.add_argument("--profile", nargs="?", const="moe", default=None,
+                    choices=["moe", "dense", "decode"],
+                    help="eager steps only (MoE step, dense projection or decode layer), for ncu")
     args = ap.parse_args()
     if args.warmup < 3 and not args.profile:
         args.warmup = 3

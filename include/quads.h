@@ -112,6 +112,19 @@ const char* quads_last_error_detail(void);
  */
 quads_status_t quads_device_status(void* stream, int32_t* device_code);
 
+/*
+ * Test hook for the GEMM's failure path (no counterpart on the pages).  With
+ * enable != 0, the next GEMM launch on any device (quads_w4a4_gemm_comp,
+ * quads_moe_grouped_gemm or quads_mx_gemm) runs with a 1 ms wait limit and an
+ * MMA issuer that issues nothing: its producers fill the ring and their waits
+ * for a free stage run out, as do the epilogue's waits for a full
+ * accumulator.  The kernel then latches QUADS_ERR_DEVICE_TIMEOUT, lets its
+ * copies in flight land, releases its tensor memory and returns; its output
+ * is unspecified.  The switch clears itself at that launch.  Nothing faults,
+ * traps or hangs: every wait of the kernel is bounded.
+ */
+void quads_test_gemm_wait_timeout(int32_t enable);
+
 /* Bytes of scratch the call `op` needs for the given shape (0 if none).
  *   QUADS_OP_QUANTIZE: num_groups floats of tensor amax.
  *   QUADS_OP_SELECT:   rows*k floats (the residual slice) + num_groups floats

@@ -1,6 +1,12 @@
 """Builds libquads.so in-tree with nvcc for sm_103a (one -gencode, sources compiled in parallel).
 
-    python -m nvfp4_w4a4_quantized_quant_gb300.build
+    python -m nvfp4_w4a4_quantized_quant_gb300.build            # release library
+    python -m nvfp4_w4a4_quantized_quant_gb300.build --debug    # bounds-checked library
+
+The bounds-checked build (-DQUADS_DEBUG, in _build/debug/) guards every
+access whose index comes from data or tile arithmetic; a failed guard is
+skipped and reported by quads_device_status.  The binding loads it when
+QUADS_DEBUG_LIB=1.
 """
 from __future__ import annotations
 
@@ -15,6 +21,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libquads.so")
+DEBUG_BUILD = os.path.join(BUILD, "debug")
+DEBUG_LIB = os.path.join(DEBUG_BUILD, "libquads.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -37,36 +45,39 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src):
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+def _compile(src, out_dir, defines):
+    obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
     if not _stale(obj, [src] + _headers()):
         return obj, ""
-    cmd = [NVCC] + ARCH + FLAGS + ["-c", src, "-o", obj]
+    cmd = [NVCC] + ARCH + FLAGS + defines + ["-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
     return obj, r.stderr
 
 
-def build(verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, debug: bool = False) -> str:
+    out_dir = DEBUG_BUILD if debug else BUILD
+    lib = DEBUG_LIB if debug else LIB
+    defines = ["-DQUADS_DEBUG"] if debug else []
+    os.makedirs(out_dir, exist_ok=True)
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        results = list(ex.map(_compile, srcs))
+        results = list(ex.map(lambda src: _compile(src, out_dir, defines), srcs))
     objs = [o for o, _ in results]
     if verbose:
         for _, log in results:
             if log.strip():
                 print(log, file=sys.stderr)
-    if _stale(LIB, objs):
-        tmp = LIB + ".tmp"
+    if _stale(lib, objs):
+        tmp = lib + ".tmp"
         cmd = [NVCC] + ARCH + ["-shared", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose=True))
+    print(build(verbose=True, debug="--debug" in sys.argv[1:]))

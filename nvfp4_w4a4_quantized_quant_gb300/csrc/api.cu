@@ -49,6 +49,9 @@ int num_sms() {
 
 int read_quant_device_error(cudaStream_t);
 int read_gemm_device_error();
+int debug_line_quantize();
+int debug_line_gemm();
+int debug_line_moe();
 
 }  // namespace quads
 
@@ -111,5 +114,11 @@ extern "C" quads_status_t quads_device_status(void* stream, int32_t* device_code
   int g = read_gemm_device_error();
   int q = read_quant_device_error((cudaStream_t)stream);
   *device_code = g ? g : q;
+  // bounds-checked builds: the first failed guard of each source file
+  const int lq = debug_line_quantize(), lg = debug_line_gemm(), lm = debug_line_moe();
+  if (lq || lg || lm) {
+    *device_code = QUADS_ERR_DEVICE_CHECK;
+    set_detail("bounds check failed: quantize.cu:%d gemm.cu:%d moe.cu:%d (0 = none)", lq, lg, lm);
+  }
   return QUADS_OK;
 }

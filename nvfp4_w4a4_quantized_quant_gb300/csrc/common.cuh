@@ -32,6 +32,31 @@ quads_status_t select_check_args(const void* x, int64_t rows, int64_t cols, int6
                                  const uint8_t* r_codes, const uint8_t* r_scales,
                                  const float* r_tensor_scale, size_t* need);
 
+// ------------------------------------------------------------ debug checks
+// Bounds-checked builds (-DQUADS_DEBUG): an access whose index comes from
+// data or from tile arithmetic is guarded by QDBG(index in range); a failed
+// guard latches its source line in this translation unit's debug word (read
+// by quads_device_status) and the access is skipped.  Release builds compile
+// the guards away.
+#ifdef QUADS_DEBUG
+static __device__ int g_debug_line;
+__device__ __forceinline__ bool quads_dbg(bool ok, int line) {
+  if (!ok) atomicCAS(&g_debug_line, 0, line);
+  return ok;
+}
+#define QDBG(cond) quads_dbg((cond), __LINE__)
+// Host side: read and clear this translation unit's debug word.
+[[maybe_unused]] static int take_debug_line() {
+  int v = 0, z = 0;
+  cudaMemcpyFromSymbol(&v, g_debug_line, sizeof(int));
+  cudaMemcpyToSymbol(g_debug_line, &z, sizeof(int));
+  return v;
+}
+#else
+#define QDBG(cond) true
+[[maybe_unused]] static int take_debug_line() { return 0; }
+#endif
+
 // ------------------------------------------------------------ scale layouts
 // Byte offset of scale column c (a 16-element block) of row r in the
 // tensor-core layout: 128-row x 4-column blocks of 512 bytes, row-block major.

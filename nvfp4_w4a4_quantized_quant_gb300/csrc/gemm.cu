@@ -44,7 +44,9 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -106,6 +108,8 @@ struct Params {
   int st32;                     // y rows and base 32-byte aligned: one 32-byte store per 16 bf16
   uint32_t* y_amax;             // nullable [E]: max |stored y| per group (float bits)
   int* err;
+  // extents for the bounds-checked build: scale buffer bytes and output rows
+  int64_t a_sf_bytes, b_sf_bytes, r_sf_bytes, ws_sf_bytes, y_rows;
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -464,9 +468,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int b = b_lo; b < b_hi; ++b) {
             if (b >= BOXES) {
               const uint32_t sfbytes = (p.mx ? ksteps / 2 : ksteps) * 512;
+              const uint8_t* src = (b == BOXES ? sfa : sfb) + kk * sf_stage;
+              const uint8_t* base = b == BOXES ? (corr ? p.r_sf : p.a_sf) : (corr ? p.ws_sf : p.b_sf);
+              const int64_t lim = b == BOXES ? (corr ? p.r_sf_bytes : p.a_sf_bytes)
+                                             : (corr ? p.ws_sf_bytes : p.b_sf_bytes);
+              if (!QDBG(src >= base && src - base + sfbytes <= lim)) {
+                mbar_arrive(&full[s]);   // skipped copy: the stage still completes
+                continue;
+              }
               mbar_expect_tx(&full[s], sfbytes);
-              if (b == BOXES) bulk_load(st + A_TILE + B_TILE, sfa + kk * sf_stage, sfbytes, &full[s]);
-              else bulk_load(st + A_TILE + B_TILE + SF_TILE, sfb + kk * sf_stage, sfbytes, &full[s]);
+              if (b == BOXES) bulk_load(st + A_TILE + B_TILE, src, sfbytes, &full[s]);
+              else bulk_load(st + A_TILE + B_TILE + SF_TILE, src, sfbytes, &full[s]);
               continue;
             }
             const int u = b >> 2, isb = (b >> 1) & 1, hf = b & 1;
@@ -623,7 +635,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (p.out_mode == OUT_SWIGLU) {
         // tile columns [0,64) are gate rows of W, [64,128) the matching up rows;
         // this warp produces h columns [32*half, 32*half + 32) of the tile
-        const bool store = row < (p.row_off ? (int64_t)meta.off[tl.e + 1] : p.M);
+        const bool store = row < (p.row_off ? (int64_t)meta.off[tl.e + 1] : p.M) && QDBG(row < p.y_rows);
         __nv_bfloat16* y = (__nv_bfloat16*)p.y + row * p.ldy + tl.n0 / 2;
 #pragma unroll 1
         for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
@@ -666,7 +678,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (!store) amax = 0.0f;
       } else {
-        const bool store = row < tl.row_end;
+        const bool store = row < tl.row_end && QDBG(row < p.y_rows);
 #pragma unroll 1
         for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
           float v1[16], v2[16];
@@ -731,6 +743,717 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                  "r"(TMEM_COLS));
   }
 }
+
+// ---------------------------------------------------------------- CTA-pair kernel
+// The same product on pairs of SMs: a 2-CTA cluster issues
+// tcgen05.mma.cta_group::2 with M = 256 (each CTA holds 128 rows of A and
+// the accumulator rows of its half) and N = 128 (each CTA holds 64 of the
+// 128 rows of B; the tensor cores read both halves).  Per SM that is the
+// work of a 128 x 128 tile for 3/4 of the operand bytes, so each 512-element
+// K stage is 56 KB and four stages fit where three did.
+//
+// A tile's K stream is a sequence of 256-element sub-tiles -- the main K
+// range, then the k-channel correction -- packed two per ring stage, so the
+// correction shares a stage with the main loop's last sub-tile when there is
+// room (K = 768: two stages per tile instead of three).
+//
+// Roles (16 warps per CTA):
+//   warps 0-3  TMA producers of this CTA's operands (A rows, its 64 rows of
+//              B, the scale atoms), each arriving on its own per-stage
+//              barrier so that it can wait for exactly its own copies when a
+//              pipeline wait gives up.
+//   warp 4     leader: TMEM allocation (both CTAs) and the MMA issuer.
+//   warps 5-6  leader: scale atoms of a stage into TMEM of both CTAs
+//              (tcgen05.cp.cta_group::2), one sub-tile each.
+//   warp 5     peer: forwards "this CTA's stage has landed" to the leader.
+//   warps 8-15 epilogue of this CTA's 128 rows (two warps per lane quadrant).
+// The leader's MMA commits free a stage in both CTAs and announce a full
+// accumulator to both; both CTAs' epilogues arrive on the leader's
+// accumulator-empty barrier.  Every wait is bounded; on a timeout a CTA stops
+// its roles, waits (bounded) for its own copies and tensor-core work in
+// flight, meets its peer at the cluster barrier and frees its TMEM.
+namespace pair {
+
+constexpr int BM = 128;                       // rows of A per CTA (M = 256 per pair)
+constexpr int BN = 128;                       // output columns of a pair tile
+constexpr int BNH = 64;                       // rows of B held by each CTA
+constexpr int KSUB = 128;                     // bytes per row of a 128B-swizzled sub-tile (256 FP4)
+constexpr int SLOTS = 2;                      // sub-tiles per stage
+constexpr int STAGES = 4;
+constexpr int A_SUB = BM * KSUB;              // 16 KB
+constexpr int B_SUB = BNH * KSUB;             // 8 KB
+constexpr int SF_SUB = 4 * 512;               // four 128-row scale atoms (one per K = 64 step)
+constexpr int OFF_B = SLOTS * A_SUB;
+constexpr int OFF_SFA = OFF_B + SLOTS * B_SUB;
+constexpr int OFF_SFB = OFF_SFA + SLOTS * SF_SUB;
+constexpr int STAGE_BYTES = OFF_SFB + SLOTS * SF_SUB;   // 56 KB
+constexpr int BOX_ROWS = 64;
+constexpr int BOX_BYTES = BOX_ROWS * KSUB;    // 8 KB
+constexpr int PRODUCERS = 4;
+constexpr int MMA_WARP = 4, SF_WARP0 = 5, SF_WARPS = 2, EPI_WARP0 = 8;
+constexpr int NUM_THREADS = 512;
+constexpr int EPI_WARPS = 8;
+constexpr int TMEM_COLS = 512;
+constexpr int ACC2_COL = 256;
+constexpr int SF_COL = 384;
+constexpr int SF_BUFS = 2;
+constexpr int SF_BUF_COLS = 64;               // A atoms at +4a, B atoms at +32+4a (a < 8)
+constexpr int MAX_GROUPS = 256;
+constexpr int NBARS = PRODUCERS * STAGES + 2 * STAGES + SF_BUFS + 4 + 2;
+constexpr int BAR_BYTES = NBARS * 8 + 16;     // + TMEM holder and abort flag
+constexpr int META_BYTES = 4 * (MAX_GROUPS + 1);
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + META_BYTES + 1024 /*align*/;
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+// copies (arrivals) per stage of producer warp w: A slot 0, A slot 1, B, scales
+__host__ __device__ constexpr int copies_of(int w) { return w == 3 ? 4 : 2; }
+
+struct Params {
+  int E, N, K, kpad, Nt;
+  int64_t M;                    // dense rows (row_off == nullptr)
+  const int32_t* row_off;       // [E+1] padded row offsets (multiples of 128) or null
+  const int32_t* row_cnt;       // [E] real rows (null: whole groups)
+  const uint8_t* a_sf;
+  const uint8_t* b_sf;
+  const uint8_t* r_sf;
+  const uint8_t* ws_sf;
+  const float* a_ts;
+  const float* b_ts;
+  const float* r_ts;
+  int a_ts_pe, r_ts_pe;
+  int comp;
+  int mx;
+  void* y;
+  int64_t ldy;
+  int out_mode;
+  int st32;
+  uint32_t* y_amax;
+  int* err;
+  unsigned long long timeout_ns;
+  int skip_mma;                 // test hook: the MMA warp issues nothing (waits then run out)
+  // extents for the bounds-checked build: scale buffer bytes and output rows
+  int64_t a_sf_bytes, b_sf_bytes, r_sf_bytes, ws_sf_bytes, y_rows;
+};
+
+struct Sync {
+  volatile int* abort_flag;
+  int* err;
+  unsigned long long tmo;
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ bool try_wait_cluster(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait by one thread; `cluster` waits with cluster-scope acquire (for
+// barriers another CTA arrives on).  `drain`: ignore the abort flag (used to
+// let work in flight finish after an abort), still bounded by the timeout.
+__device__ __forceinline__ bool wait1(uint64_t* b, uint32_t parity, const Sync& s,
+                                      bool cluster = false, bool drain = false) {
+  auto probe = [&]() { return cluster ? try_wait_cluster(b, parity) : mbar_try_wait(b, parity); };
+  if (probe()) return true;
+  const unsigned long long t0 = global_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (probe()) return true;
+    if ((++spins & 255u) == 0) {
+      if (!drain && *s.abort_flag) return false;
+      if (global_ns() - t0 > s.tmo) {
+        if (!drain) {
+          *s.abort_flag = 1;
+          atomicExch(s.err, QUADS_ERR_DEVICE_TIMEOUT);
+        }
+        return false;
+      }
+    }
+  }
+}
+// Bounded wait for a whole warp: lane 0 polls, the warp follows its verdict.
+__device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, const Sync& s,
+                                          bool cluster = false) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait1(b, parity, s, cluster) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+// Bounded wait polled by every lane of a converged warp (the MMA warp stays
+// converged for its elect-predicated tcgen05 instructions).
+__device__ __forceinline__ bool conv_wait(uint64_t* b, uint32_t parity, const Sync& s,
+                                          bool cluster = false) {
+  auto probe = [&]() { return cluster ? try_wait_cluster(b, parity) : mbar_try_wait(b, parity); };
+  if (__all_sync(0xffffffffu, probe())) return true;
+  const unsigned long long t0 = global_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (__all_sync(0xffffffffu, probe())) return true;
+    if ((++spins & 255u) == 0) {
+      int give_up = *s.abort_flag ? 1 : 0;
+      if (!give_up && global_ns() - t0 > s.tmo) give_up = 2;
+      give_up = __shfl_sync(0xffffffffu, give_up, 0);
+      if (give_up) {
+        if (give_up == 2 && (threadIdx.x & 31) == 0) {
+          *s.abort_flag = 1;
+          atomicExch(s.err, QUADS_ERR_DEVICE_TIMEOUT);
+        }
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void mma_nvf4_cg2(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                             uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb));
+}
+__device__ __forceinline__ void mma_mxf4_cg2(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                             uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb));
+}
+// Commit of the executing thread's earlier tcgen05 work: arrive on the
+// barrier at the same offset in every CTA of `mask`.
+__device__ __forceinline__ void commit_mc_cg2(uint64_t* b, uint16_t mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}" ::"r"(smem_u32(b)),
+      "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void cp_sf_cg2(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+      "l"(sdesc)
+      : "memory");
+}
+
+// A pair tile: rows [m0, m0 + 256) (the peer's half starts at m0 + 128) x
+// output columns [n0, n0 + 128) of group e.
+struct Tile {
+  int e;
+  int64_t m0;
+  int n0;
+  int64_t row_end;   // rows >= row_end are not stored (plain / f32 outputs)
+  int64_t grp_end;   // end of the group's padded rows (SwiGLU stores up to here)
+  int64_t blk_lim;   // 128-row blocks >= blk_lim hold none of the group's rows
+};
+
+__device__ __forceinline__ int64_t total_tiles(const Params& p, const int32_t* poff) {
+  if (!p.row_off) return ((p.M + 2 * BM - 1) / (2 * BM)) * p.Nt;
+  return (int64_t)poff[p.E] * p.Nt;
+}
+
+__device__ __forceinline__ Tile decode_tile(const Params& p, const int32_t* poff, int64_t t) {
+  Tile r;
+  if (!p.row_off) {
+    const int64_t Mt = (p.M + 2 * BM - 1) / (2 * BM);
+    r.e = 0;
+    r.m0 = (t % Mt) * 2 * BM;
+    r.n0 = (int)(t / Mt) * BN;
+    r.row_end = p.M;
+    r.grp_end = p.M;
+    r.blk_lim = (p.M + BM - 1) / BM;
+    return r;
+  }
+  // group e holds pair tiles [poff[e] * Nt, poff[e+1] * Nt), m fastest
+  int lo = 0, hi = p.E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)poff[mid] * p.Nt <= t) lo = mid; else hi = mid - 1;
+  }
+  const int e = lo;
+  const int64_t pairs = poff[e + 1] - poff[e];
+  const int64_t local = t - (int64_t)poff[e] * p.Nt;
+  const int64_t o0 = __ldg(p.row_off + e), o1 = __ldg(p.row_off + e + 1);
+  r.e = e;
+  r.m0 = o0 + (local % pairs) * 2 * BM;
+  r.n0 = (int)(local / pairs) * BN;
+  r.row_end = o0 + (p.row_cnt ? __ldg(p.row_cnt + e) : (o1 - o0));
+  r.grp_end = o1;
+  r.blk_lim = o1 / BM;
+  return r;
+}
+
+// Sub-tile j of a tile's K stream: main K sub-tiles first, then the
+// correction's.  Returns the number of K = 64 steps it holds (0: empty slot).
+struct Sub {
+  int ksteps;
+  bool corr;
+  int kk;        // sub-tile index inside its own K range
+};
+__device__ __forceinline__ Sub sub_of(const Params& p, int j, int nmain, int ncorr) {
+  Sub s;
+  if (j < nmain) {
+    s.corr = false;
+    s.kk = j;
+    s.ksteps = min(4, (p.K - j * 256) / 64);
+  } else if (j < nmain + ncorr) {
+    s.corr = true;
+    s.kk = j - nmain;
+    s.ksteps = min(4, (p.kpad - s.kk * 256) / 64);
+  } else {
+    s.corr = false;
+    s.kk = 0;
+    s.ksteps = 0;
+  }
+  return s;
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmR,
+                     const __grid_constant__ CUtensorMap tmW, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES);
+  uint64_t* fullw = bars;                                // [PRODUCERS][STAGES]
+  uint64_t* full_peer = fullw + PRODUCERS * STAGES;      // [STAGES] (leader)
+  uint64_t* empty = full_peer + STAGES;                  // [STAGES]
+  uint64_t* sf_ready = empty + STAGES;                   // [SF_BUFS] (leader)
+  uint64_t* acc_full = sf_ready + SF_BUFS;               // [2]
+  uint64_t* acc_empty = acc_full + 2;                    // [2] (leader)
+  uint64_t* drain_mma = acc_empty + 2;                   // leader
+  uint64_t* drain_sf = drain_mma + 1;                    // leader
+  uint32_t* tmem_holder = (uint32_t*)(drain_sf + 1);
+  volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
+  int32_t* poff = (int32_t*)(smem + STAGES * STAGE_BYTES + BAR_BYTES);   // [E+1] pair prefix
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const Sync sy{abort_flag, p.err, p.timeout_ns};
+
+  // pair prefix of the groups: pairs_e = ceil(blocks_e / 2), exclusive scan
+  if (p.row_off && warp < 8) {
+    __shared__ int wsum[8];
+    const int e = threadIdx.x;   // warps 0-7 cover up to 256 groups
+    int v = 0;
+    if (e < p.E) {
+      const int blocks = (__ldg(p.row_off + e + 1) - __ldg(p.row_off + e)) / BM;
+      v = (blocks + 1) >> 1;
+    }
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    int before = 0;
+    for (int i = 0; i < warp; ++i) before += wsum[i];
+    if (e < p.E) poff[e + 1] = before + incl;
+    if (e == 0) poff[0] = 0;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < PRODUCERS; ++i)
+      for (int s = 0; s < STAGES; ++s) mbar_init(&fullw[i * STAGES + s], copies_of(i));
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_peer[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < SF_BUFS; ++i) mbar_init(&sf_ready[i], SF_WARPS);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 2 * EPI_WARPS);
+    }
+    mbar_init(drain_mma, 1);
+    mbar_init(drain_sf, SF_WARPS);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == MMA_WARP) {
+    // one warp of each CTA of the pair allocates, collectively
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_holder)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // both CTAs' barriers are initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  const int64_t ntiles = total_tiles(p, poff);
+  const int64_t cid = cluster_id(), ncl = cluster_count();
+  const int nmain = (p.K + 255) / 256;
+  const int ncorr = p.comp ? (p.kpad + 255) / 256 : 0;
+  const int nst = (nmain + ncorr + SLOTS - 1) / SLOTS;   // ring stages per tile
+  // scale bytes per 128-row block and per 256-element sub-tile
+  const int64_t a_sf_rb = (int64_t)(p.K / (p.mx ? 128 : 64)) * 512;
+  const int64_t r_sf_rb = (int64_t)(p.kpad / 64) * 512;
+  const int sf_sub = p.mx ? SF_SUB / 2 : SF_SUB;
+
+  if (warp < PRODUCERS) {
+    // ---------------------------------------------------------- producers
+    // warp 0: A boxes of slot 0, warp 1: A boxes of slot 1, warp 2: the B box
+    // of both slots, warp 3: the scale atoms (A and B) of both slots.  A copy
+    // of an empty slot is a plain arrival.
+    uint64_t* myfull = fullw + warp * STAGES;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int64_t t = cid; t < ntiles && ok; t += ncl) {
+      const Tile tl = decode_tile(p, poff, t);
+      const int64_t mrow = tl.m0 + (int64_t)rank * BM;          // this CTA's A rows
+      int64_t blk = mrow / BM;                                  // its scale rows
+      if (blk >= tl.blk_lim) blk = tl.m0 / BM;                  // no rows of the group: any valid block
+      const int64_t bbase = (int64_t)tl.e * p.N + tl.n0;        // the pair's 128 B rows
+      const int64_t brow = bbase + (int64_t)rank * BNH;         // this CTA's 64 of them
+      for (int kt = 0; kt < nst && ok; ++kt, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!warp_wait(&empty[s], ph ^ 1, sy)) { ok = false; break; }
+        uint8_t* st = smem + s * STAGE_BYTES;
+        if (elect_one()) {
+          for (int u = 0; u < SLOTS; ++u) {
+            const Sub sb = sub_of(p, kt * SLOTS + u, nmain, ncorr);
+            const CUtensorMap* ma = sb.corr ? &tmR : &tmA;
+            const CUtensorMap* mb = sb.corr ? &tmW : &tmB;
+            const int x = sb.kk * KSUB;
+            if (warp == u) {            // A: two 64-row boxes
+              for (int h = 0; h < 2; ++h) {
+                if (sb.ksteps) {
+                  mbar_expect_tx(&myfull[s], BOX_BYTES);
+                  tma_load_2d(st + u * A_SUB + h * BOX_BYTES, ma, x, (int)(mrow + h * BOX_ROWS),
+                              &myfull[s]);
+                } else {
+                  mbar_arrive(&myfull[s]);
+                }
+              }
+            } else if (warp == 2) {     // B: this CTA's 64 rows
+              if (sb.ksteps) {
+                mbar_expect_tx(&myfull[s], BOX_BYTES);
+                tma_load_2d(st + OFF_B + u * B_SUB, mb, x, (int)brow, &myfull[s]);
+              } else {
+                mbar_arrive(&myfull[s]);
+              }
+            } else if (warp == 3) {     // scale atoms of A and of the pair's B
+              const uint32_t bytes = (p.mx ? (sb.ksteps + 1) / 2 : sb.ksteps) * 512;
+              if (sb.ksteps) {
+                const int64_t oa = sb.corr ? blk * r_sf_rb + (int64_t)sb.kk * SF_SUB
+                                           : blk * a_sf_rb + (int64_t)sb.kk * sf_sub;
+                const int64_t ow = sb.corr ? (bbase / BM) * r_sf_rb + (int64_t)sb.kk * SF_SUB
+                                           : (bbase / BM) * a_sf_rb + (int64_t)sb.kk * sf_sub;
+                if (QDBG(oa >= 0 && oa + bytes <= (sb.corr ? p.r_sf_bytes : p.a_sf_bytes))) {
+                  mbar_expect_tx(&myfull[s], bytes);
+                  bulk_load(st + OFF_SFA + u * SF_SUB, (sb.corr ? p.r_sf : p.a_sf) + oa, bytes,
+                            &myfull[s]);
+                } else {
+                  mbar_arrive(&myfull[s]);
+                }
+                if (QDBG(ow >= 0 && ow + bytes <= (sb.corr ? p.ws_sf_bytes : p.b_sf_bytes))) {
+                  mbar_expect_tx(&myfull[s], bytes);
+                  bulk_load(st + OFF_SFB + u * SF_SUB, (sb.corr ? p.ws_sf : p.b_sf) + ow, bytes,
+                            &myfull[s]);
+                } else {
+                  mbar_arrive(&myfull[s]);
+                }
+              } else {
+                mbar_arrive(&myfull[s]);
+                mbar_arrive(&myfull[s]);
+              }
+            }
+          }
+        }
+        __syncwarp();
+      }
+    }
+    // let every copy this warp issued land (at most the last STAGES
+    // iterations can still be in flight) before the CTA can exit
+    if (lane == 0) {
+      const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
+      for (uint32_t j = first; j < it; ++j) wait1(&myfull[j % STAGES], (j / STAGES) & 1, sy, false, true);
+    }
+  } else if (warp == MMA_WARP && leader) {
+    // ---------------------------------------------------------- MMA issuer
+    const uint32_t idesc = idesc_nvf4(2 * BM, BN);
+    uint32_t s = 0, sb = 0, sph = 0, j = 0;
+    bool ok = !p.skip_mma;
+    for (int64_t t = cid; t < ntiles && ok; t += ncl, ++j) {
+      const uint32_t b = j & 1;
+      if (!conv_wait(&acc_empty[b], ((j >> 1) & 1) ^ 1, sy, true)) { ok = false; break; }
+      tc_fence_after();
+      for (int kt = 0; kt < nst; ++kt) {
+        if (!conv_wait(&sf_ready[sb], sph, sy)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
+        const uint32_t tsf = tmem + SF_COL + sb * SF_BUF_COLS;
+        for (int u = 0; u < SLOTS; ++u) {
+          const int jj = kt * SLOTS + u;
+          const Sub sub = sub_of(p, jj, nmain, ncorr);
+          if (!sub.ksteps) continue;
+          if (sub.corr && sub.kk == 0 && j > 0) {
+            // acc2 is free once the previous tile's epilogues are done
+            if (!conv_wait(&acc_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, sy, true)) { ok = false; break; }
+            tc_fence_after();
+          }
+          const uint32_t dcol = sub.corr ? (tmem + ACC2_COL) : (tmem + b * BN);
+          const bool first_sub = sub.corr ? (sub.kk == 0) : (jj == 0);
+          const uint32_t a0 = sa + u * A_SUB, b0 = sa + OFF_B + u * B_SUB;
+          for (int q = 0; q < sub.ksteps; ++q) {
+            const uint32_t acc = (first_sub && q == 0) ? 0u : 1u;
+            if (p.mx) {
+              const uint32_t at = 2 * u + (q >> 1);
+              const uint32_t id = (q & 1) ? idesc_mxf4(2 * BM, BN, 2) : idesc_mxf4(2 * BM, BN, 0);
+              mma_mxf4_cg2(dcol, desc_sw128(a0 + q * 32), desc_sw128(b0 + q * 32), id,
+                           tsf + 4 * at, tsf + 32 + 4 * at, acc);
+            } else {
+              const uint32_t at = 4 * u + q;
+              mma_nvf4_cg2(dcol, desc_sw128(a0 + q * 32), desc_sw128(b0 + q * 32), idesc,
+                           tsf + 4 * at, tsf + 32 + 4 * at, acc);
+            }
+          }
+        }
+        if (!ok) break;
+        commit_mc_cg2(&empty[s], 0x3);   // frees the stage in both CTAs (and the scale buffer)
+        if (++s == STAGES) s = 0;
+        if (++sb == SF_BUFS) { sb = 0; sph ^= 1; }
+      }
+      if (!ok) break;
+      commit_mc_cg2(&acc_full[b], 0x3);
+    }
+    // every MMA this thread issued has completed before TMEM or shared memory go away
+    commit_mc_cg2(drain_mma, 0x1);
+    if (lane == 0) wait1(drain_mma, 0, sy, false, true);
+    __syncwarp();
+  } else if (warp >= SF_WARP0 && warp < SF_WARP0 + SF_WARPS && leader) {
+    // ---------------------------------------------------------- scale staging
+    // Warp w copies slot w's scale atoms of a stage once both CTAs' copies
+    // have landed; scale buffer sb was last read by the MMAs of ring
+    // iteration it - SF_BUFS (signalled on that stage's empty barrier).
+    const int w = warp - SF_WARP0;
+    uint32_t s = 0, ph = 0, sb = 0, it = 0;
+    bool ok = true;
+    for (int64_t t = cid; t < ntiles && ok; t += ncl) {
+      for (int kt = 0; kt < nst; ++kt, ++it) {
+        bool okw = true;
+        for (int i = 0; i < PRODUCERS && okw; ++i) okw = conv_wait(&fullw[i * STAGES + s], ph, sy);
+        if (okw) okw = conv_wait(&full_peer[s], ph, sy, true);
+        if (okw && it >= (uint32_t)SF_BUFS) {
+          const uint32_t prev = it - SF_BUFS;
+          okw = conv_wait(&empty[prev % STAGES], (prev / STAGES) & 1, sy);
+        }
+        if (!okw) { ok = false; break; }
+        tc_fence_after();
+        const Sub sub = sub_of(p, kt * SLOTS + w, nmain, ncorr);
+        const uint32_t ssa = smem_u32(smem + s * STAGE_BYTES + OFF_SFA + w * SF_SUB);
+        const uint32_t ssb = smem_u32(smem + s * STAGE_BYTES + OFF_SFB + w * SF_SUB);
+        const uint32_t tsf = tmem + SF_COL + sb * SF_BUF_COLS;
+        const int natoms = p.mx ? (sub.ksteps + 1) / 2 : sub.ksteps;
+        const int abase = p.mx ? 2 * w : 4 * w;
+        for (int a = 0; a < natoms; ++a) {
+          cp_sf_cg2(tsf + 4 * (abase + a), desc_sf(ssa + a * 512));
+          cp_sf_cg2(tsf + 32 + 4 * (abase + a), desc_sf(ssb + a * 512));
+        }
+        commit_mc_cg2(&sf_ready[sb], 0x1);
+        if (++s == STAGES) { s = 0; ph ^= 1; }
+        if (++sb == SF_BUFS) sb = 0;
+      }
+    }
+    commit_mc_cg2(drain_sf, 0x1);
+    if (lane == 0) wait1(drain_sf, 0, sy, false, true);
+    __syncwarp();
+  } else if (warp == SF_WARP0 && !leader) {
+    // ---------------------------------------------------------- peer: forward
+    // "this CTA's stage has landed" to the leader's full_peer barrier
+    uint32_t s = 0, ph = 0;
+    bool ok = true;
+    const uint32_t remote = peer_addr(&full_peer[0], 0);
+    for (int64_t t = cid; t < ntiles && ok; t += ncl) {
+      for (int kt = 0; kt < nst && ok; ++kt) {
+        for (int i = 0; i < PRODUCERS && ok; ++i) ok = warp_wait(&fullw[i * STAGES + s], ph, sy);
+        if (!ok) break;
+        if (lane == 0) arrive_cluster(remote + 8u * s);
+        __syncwarp();
+        if (++s == STAGES) { s = 0; ph ^= 1; }
+      }
+    }
+  } else if (warp >= EPI_WARP0) {
+    // ---------------------------------------------------------- epilogue
+    const int quad = warp & 3;
+    const int half = (warp - EPI_WARP0) >> 2;
+    const int row_in_tile = (int)rank * BM + quad * 32 + lane;
+    const uint32_t acc_empty_leader = peer_addr(&acc_empty[0], 0);
+    uint32_t j = 0;
+    for (int64_t t = cid; t < ntiles; t += ncl, ++j) {
+      const Tile tl = decode_tile(p, poff, t);
+      const uint32_t b = j & 1;
+      if (!warp_wait(&acc_full[b], (j >> 1) & 1, sy, true)) break;
+      tc_fence_after();
+      const float bts = p.mx ? 1.0f : __ldg(p.b_ts + tl.e);
+      const float a1 = p.mx ? 1.0f : __fmul_rn(__ldg(p.a_ts + (p.a_ts_pe ? tl.e : 0)), bts);
+      const float a2 = p.comp ? __fmul_rn(__ldg(p.r_ts + (p.r_ts_pe ? tl.e : 0)), bts) : 0.0f;
+      const int64_t row = tl.m0 + row_in_tile;
+      const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+      const uint32_t t1 = tmem + lane_base + b * BN;
+      const uint32_t t2 = tmem + lane_base + ACC2_COL;
+      auto release = [&]() {
+        // this warp's last TMEM read of the tile is done: tell the leader
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(&acc_empty[b]);
+          else arrive_cluster(acc_empty_leader + 8u * b);
+        }
+      };
+      float amax = 0.0f;
+      if (p.out_mode == OUT_SWIGLU) {
+        // tile columns [0,64) are gate rows of W, [64,128) the matching up rows;
+        // this warp produces h columns [32*half, 32*half + 32) of the tile
+        const bool store = row < tl.grp_end && QDBG(row < p.y_rows);
+        __nv_bfloat16* y = (__nv_bfloat16*)p.y + row * p.ldy + tl.n0 / 2;
+#pragma unroll 1
+        for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
+          float g1[16], u1[16], g2[16], u2[16];
+          __syncwarp();
+          tc_ld16(t1 + c0, g1);
+          tc_ld16(t1 + 64 + c0, u1);
+          if (p.comp) { tc_ld16(t2 + c0, g2); tc_ld16(t2 + 64 + c0, u2); }
+          tc_wait_ld();
+          if (c0 + 16 == half * 32 + 32) release();
+          uint32_t packed[8];
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            float h[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              float g = a1 * g1[i + q], u = a1 * u1[i + q];
+              if (p.comp) { g = fmaf(a2, g2[i + q], g); u = fmaf(a2, u2[i + q], u); }
+              h[q] = __fdividef(g * u, 1.0f + __expf(-g));   // silu(g) * u
+            }
+            __nv_bfloat162 hb = __floats2bfloat162_rn(h[0], h[1]);
+            packed[i / 2] = *reinterpret_cast<uint32_t*>(&hb);
+            const float2 hr = __bfloat1622float2(hb);
+            amax = fmaxf(amax, fmaxf(fabsf(hr.x), fabsf(hr.y)));
+          }
+          if (store) {
+            if (p.st32) {
+              st_global_32B(y + c0, packed);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(y + c0);
+              dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+              dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            }
+          }
+        }
+        if (!store) amax = 0.0f;
+      } else {
+        const bool store = row < tl.row_end && QDBG(row < p.y_rows);
+#pragma unroll 1
+        for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
+          float v1[16], v2[16];
+          __syncwarp();
+          tc_ld16(t1 + c0, v1);
+          if (p.comp) tc_ld16(t2 + c0, v2);
+          tc_wait_ld();
+          if (c0 + 16 == half * 64 + 64) release();
+          float o[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] = p.comp ? fmaf(a2, v2[i], a1 * v1[i]) : a1 * v1[i];
+          if (store) {
+            if (p.out_mode == OUT_F32) {
+              float* yrow = (float*)p.y + row * p.ldy + tl.n0 + c0;
+              if (p.st32) {
+                st_global_32B(yrow, reinterpret_cast<const uint32_t*>(o));
+                st_global_32B(yrow + 8, reinterpret_cast<const uint32_t*>(o + 8));
+              } else {
+                float4* dst = reinterpret_cast<float4*>(yrow);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+              }
+#pragma unroll
+              for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(o[i]));
+            } else {
+              uint32_t packed[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                __nv_bfloat162 hb = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+                packed[i] = *reinterpret_cast<uint32_t*>(&hb);
+                const float2 hr = __bfloat1622float2(hb);
+                amax = fmaxf(amax, fmaxf(fabsf(hr.x), fabsf(hr.y)));
+              }
+              __nv_bfloat16* yrow = (__nv_bfloat16*)p.y + row * p.ldy + tl.n0 + c0;
+              if (p.st32) {
+                st_global_32B(yrow, packed);
+              } else {
+                uint4* dst = reinterpret_cast<uint4*>(yrow);
+                dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+              }
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (p.y_amax) {
+        amax = warp_max(amax);
+        if (lane == 0 && amax > 0.0f) atomicMax(&p.y_amax[tl.e], __float_as_uint(amax));
+      }
+    }
+  }
+  // both CTAs: no MMA reads this CTA's shared memory or writes its TMEM any
+  // more, and no arrival on its barriers is pending, past this point
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == MMA_WARP)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+}
+
+}  // namespace pair
 
 // ---------------------------------------------------------------- Q(W_sel)
 // Column-major copy of an NVFP4 weight, made once per weight update: for group
@@ -817,12 +1540,14 @@ __global__ void __launch_bounds__(256) wsel_cols_kernel(
   for (int i = threadIdx.x; i < 16 * (cv + sv); i += blockDim.x) {
     if (i < 16 * cv) {
       const int j = i / cv, v = i - j * cv;
-      const int c = __ldg(s + j);
+      int c = __ldg(s + j);
+      if (!QDBG(c >= 0 && c < K)) c = 0;
       reinterpret_cast<uint4*>(sc + j * (NC / 2))[v] =
           __ldg(reinterpret_cast<const uint4*>(cte + (int64_t)c * (N / 2)) + v);
     } else {
       const int i2 = i - 16 * cv, j = i2 / sv, v = i2 - j * sv;
-      const int c = __ldg(s + j);
+      int c = __ldg(s + j);
+      if (!QDBG(c >= 0 && c < K)) c = 0;
       reinterpret_cast<uint4*>(ss + j * NC)[v] =
           __ldg(reinterpret_cast<const uint4*>(ste + (int64_t)(c >> 4) * N) + v);
     }
@@ -896,6 +1621,15 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t wid
 
 static __device__ int g_gemm_error;
 
+// Test hook (quads_test_gemm_wait_timeout): the next GEMM launch gets a 1 ms
+// wait limit and an MMA warp that issues nothing, so its waits run out.
+static std::atomic<int> g_wait_test{0};
+// The earlier one-CTA kernel, selectable for comparison (QUADS_GEMM_ONE_CTA=1).
+static const bool g_one_cta_kernel = [] {
+  const char* v = getenv("QUADS_GEMM_ONE_CTA");
+  return v && v[0] == '1';
+}();
+
 struct Launch {
   int64_t M, rows_cap;
   int E, N, K, k, kpad;
@@ -961,52 +1695,130 @@ static quads_status_t launch(const Launch& L) {
     tR = tA;
     tW = tB;
   }
-  Params p;
-  p.E = L.E; p.N = L.N; p.K = L.K; p.kpad = comp ? L.kpad : 0; p.Nt = L.N / BN;
+  // 32-byte stores need every row start and column offset on a 32-byte
+  // boundary: tiles start at multiples of 128 columns (64 for SwiGLU output)
+  const int64_t esz = L.out_mode == OUT_F32 ? 4 : 2;
+  const int st32 = ((uintptr_t)L.y % 32 == 0 && (L.ldy * esz) % 32 == 0) ? 1 : 0;
+  // scale buffer sizes implied by the shapes (checked in bounds-checked builds)
+  struct { int64_t a, b, r, w; } ext;
+  {
+    const int64_t per = L.mx ? 32 : 16;
+    ext.a = (arows + 127) / 128 * 128 * (L.K / per);
+    ext.b = (brows + 127) / 128 * 128 * (L.K / per);
+    ext.r = comp ? (arows + 127) / 128 * 128 * (L.kpad / 16) : 0;
+    ext.w = comp ? (brows + 127) / 128 * 128 * (L.kpad / 16) : 0;
+  }
+  if (L.y_amax) cudaMemsetAsync(L.y_amax, 0, (size_t)L.E * 4, L.stream);
+  // per device, resolved on the first launch there (calls after
+  // cudaDeviceReset are not supported): the error word's address, the
+  // shared-memory attributes and how many CTA pairs can be resident at once
+  int* errp = nullptr;
+  int max_pairs = 0;
+  {
+    static std::mutex mu;
+    static int* errp_dev[64] = {nullptr};
+    static int pairs_dev[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+      return fail(QUADS_ERR_CUDA, "gemm: no usable current device (ordinal %d)", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!errp_dev[dev]) {
+      if (cudaGetSymbolAddress((void**)&errp_dev[dev], g_gemm_error) != cudaSuccess) {
+        errp_dev[dev] = nullptr;
+        return fail(QUADS_ERR_CUDA, "gemm: cannot resolve the device error word");
+      }
+      cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           SMEM_BYTES);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(pair::pair_gemm_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
+      if (e != cudaSuccess) {
+        errp_dev[dev] = nullptr;
+        return fail(QUADS_ERR_CUDA, "gemm: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+      }
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute at;
+      at.id = cudaLaunchAttributeClusterDimension;
+      at.val.clusterDim.x = 2;
+      at.val.clusterDim.y = 1;
+      at.val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2 * (unsigned)num_sms(), 1, 1);
+      cfg.blockDim = dim3(pair::NUM_THREADS, 1, 1);
+      cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+      cfg.attrs = &at;
+      cfg.numAttrs = 1;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, pair::pair_gemm_kernel, &cfg);
+      if (e != cudaSuccess || n < 1) {
+        errp_dev[dev] = nullptr;
+        return fail(QUADS_ERR_CUDA, "gemm: no resident CTA pair possible (%s)",
+                    e == cudaSuccess ? "0 clusters" : cudaGetErrorString(e));
+      }
+      pairs_dev[dev] = n;
+    }
+    errp = errp_dev[dev];
+    max_pairs = pairs_dev[dev];
+  }
+  if (g_one_cta_kernel) {
+    Params p;
+    p.E = L.E; p.N = L.N; p.K = L.K; p.kpad = comp ? L.kpad : 0; p.Nt = L.N / BN;
+    p.M = L.M; p.row_off = L.row_off; p.row_cnt = L.row_cnt;
+    p.a_sf = L.a_sf; p.b_sf = L.b_sf; p.r_sf = L.r_sf; p.ws_sf = ws_sf;
+    p.a_ts = L.a_ts; p.b_ts = L.b_ts; p.r_ts = L.r_ts; p.a_ts_pe = L.a_pe; p.r_ts_pe = L.r_pe;
+    p.comp = comp ? 1 : 0;
+    p.mx = L.mx;
+    p.y = L.y; p.ldy = L.ldy; p.out_mode = L.out_mode;
+    p.st32 = st32;
+    p.y_amax = (uint32_t*)L.y_amax;
+    p.err = errp;
+    p.a_sf_bytes = ext.a; p.b_sf_bytes = ext.b; p.r_sf_bytes = ext.r; p.ws_sf_bytes = ext.w;
+    p.y_rows = arows;
+    int64_t grid = num_sms();
+    if (!L.row_off) grid = std::min<int64_t>(grid, ((L.M + BM - 1) / BM) * (L.N / BN));
+    gemm_kernel<<<(int)grid, NUM_THREADS, SMEM_BYTES, L.stream>>>(tA, tB, tR, tW, p);
+    return check_launch("gemm", launches);
+  }
+  pair::Params p;
+  p.E = L.E; p.N = L.N; p.K = L.K; p.kpad = comp ? L.kpad : 0; p.Nt = L.N / pair::BN;
   p.M = L.M; p.row_off = L.row_off; p.row_cnt = L.row_cnt;
   p.a_sf = L.a_sf; p.b_sf = L.b_sf; p.r_sf = L.r_sf; p.ws_sf = ws_sf;
   p.a_ts = L.a_ts; p.b_ts = L.b_ts; p.r_ts = L.r_ts; p.a_ts_pe = L.a_pe; p.r_ts_pe = L.r_pe;
   p.comp = comp ? 1 : 0;
   p.mx = L.mx;
   p.y = L.y; p.ldy = L.ldy; p.out_mode = L.out_mode;
-  {
-    // 32-byte stores need every row start and column offset on a 32-byte
-    // boundary: tiles start at multiples of 128 columns (64 for SwiGLU output)
-    const int64_t esz = L.out_mode == OUT_F32 ? 4 : 2;
-    p.st32 = ((uintptr_t)L.y % 32 == 0 && (L.ldy * esz) % 32 == 0) ? 1 : 0;
-  }
+  p.st32 = st32;
   p.y_amax = (uint32_t*)L.y_amax;
-  if (L.y_amax) cudaMemsetAsync(L.y_amax, 0, (size_t)L.E * 4, L.stream);
-  // the error word's address and the shared-memory attribute are per device
-  // (resolved on the first launch on a device; calls after cudaDeviceReset
-  // are not supported)
-  {
-    static std::mutex mu;
-    static int* errp[64] = {nullptr};
-    static bool attr_set[64] = {false};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-      return fail(QUADS_ERR_CUDA, "gemm: no usable current device (ordinal %d)", dev);
-    std::lock_guard<std::mutex> lock(mu);
-    if (!errp[dev] && cudaGetSymbolAddress((void**)&errp[dev], g_gemm_error) != cudaSuccess) {
-      errp[dev] = nullptr;
-      return fail(QUADS_ERR_CUDA, "gemm: cannot resolve the device error word");
-    }
-    p.err = errp[dev];
-    if (!attr_set[dev]) {
-      const cudaError_t e =
-          cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-      if (e != cudaSuccess)
-        return fail(QUADS_ERR_CUDA, "gemm: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-      attr_set[dev] = true;
-    }
+  p.err = errp;
+  p.a_sf_bytes = ext.a; p.b_sf_bytes = ext.b; p.r_sf_bytes = ext.r; p.ws_sf_bytes = ext.w;
+  p.y_rows = arows;
+  const bool wait_test = g_wait_test.exchange(0) != 0;
+  p.timeout_ns = wait_test ? 1000000ull : kTimeoutNs;
+  p.skip_mma = wait_test ? 1 : 0;
+  // one CTA pair per pair of SMs, persistent over the tiles
+  int64_t pairs = max_pairs;
+  if (!L.row_off)
+    pairs = std::min<int64_t>(pairs, ((L.M + 2 * pair::BM - 1) / (2 * pair::BM)) * (L.N / pair::BN));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeClusterDimension;
+  at.val.clusterDim.x = 2;
+  at.val.clusterDim.y = 1;
+  at.val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(pair::NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+  cfg.stream = L.stream;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, pair::pair_gemm_kernel, tA, tB, tR, tW, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(QUADS_ERR_CUDA, "gemm: launch of the CTA-pair kernel: %s", cudaGetErrorString(e));
   }
-  int64_t grid = num_sms();
-  if (!L.row_off) grid = std::min<int64_t>(grid, ((L.M + BM - 1) / BM) * (L.N / BN));
-  gemm_kernel<<<(int)grid, NUM_THREADS, SMEM_BYTES, L.stream>>>(tA, tB, tR, tW, p);
   return check_launch("gemm", launches);
 }
 
+void gemm_wait_test(int enable) { g_wait_test.store(enable ? 1 : 0); }
 }  // namespace gemm
 
 int read_gemm_device_error() {
@@ -1016,6 +1828,8 @@ int read_gemm_device_error() {
   cudaMemcpyToSymbol(gemm::g_gemm_error, &zero, sizeof(int));
   return v;
 }
+
+int debug_line_gemm() { return take_debug_line(); }
 
 }  // namespace quads
 
@@ -1163,6 +1977,8 @@ extern "C" quads_status_t quads_mx_gemm(int64_t M, int64_t N, int64_t K, const u
   L.stream = (cudaStream_t)stream;
   return gemm::launch(L);
 }
+
+extern "C" void quads_test_gemm_wait_timeout(int32_t enable) { gemm::gemm_wait_test(enable); }
 
 extern "C" quads_status_t quads_weight_columns(const uint8_t* w_codes, const uint8_t* w_scales,
                                                int32_t num_groups, int64_t rows_per_group,

@@ -44,7 +44,8 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
 #pragma unroll
     for (int i = 0; i < kMaxExperts / 32; ++i) {
       const int e = lane + 32 * i;
-      v[i] = (i < words && e < E) ? logits[(int64_t)t * E + e] : -INFINITY;
+      const float l = (i < words && e < E) ? logits[(int64_t)t * E + e] : -INFINITY;
+      v[i] = isnan(l) ? -INFINITY : l;   // a NaN logit ranks lowest: every pick is a real expert
     }
     uint32_t taken = 0;
     float my_l = -INFINITY, lmax = -INFINITY;
@@ -165,7 +166,8 @@ __global__ void __launch_bounds__(256) assign_kernel(const int32_t* __restrict__
                                                      int32_t* __restrict__ off_out,
                                                      const int32_t* __restrict__ counts,
                                                      int32_t* __restrict__ row_token,
-                                                     int32_t* __restrict__ token_row) {
+                                                     int32_t* __restrict__ token_row,
+                                                     int64_t cap) {
   __shared__ int off[kMaxExperts + 1];
   __shared__ int warp_sums[8];
   {
@@ -191,13 +193,14 @@ __global__ void __launch_bounds__(256) assign_kernel(const int32_t* __restrict__
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
     const int t = i / topk;
     const int e = idx[i];
+    if (!QDBG(e >= 0 && e < E)) continue;
     const int row = off[e] + bprefix[(int64_t)e * nb + t / kRouteTokens] + token_row[i];
     token_row[i] = row;
-    row_token[row] = t;
+    if (QDBG(row >= 0 && row < cap)) row_token[row] = t;
   }
   for (int e = blockIdx.x; e < E; e += gridDim.x)
     for (int r = off[e] + counts[e] + (int)threadIdx.x; r < off[e + 1]; r += blockDim.x)
-      row_token[r] = -1;
+      if (QDBG(r < cap)) row_token[r] = -1;
 }
 
 // Wide rows (>= 32 code vectors of 16 bytes): a warp copies 4 rows at a time,
@@ -212,7 +215,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
                                                      const uint8_t* __restrict__ isf,
                                                      uint8_t* __restrict__ oc,
                                                      uint8_t* __restrict__ osf) {
-  const int64_t nrows = off[E];
+  int64_t nrows = off[E];
+  if (!QDBG(nrows >= 0 && nrows <= cap)) nrows = 0;
   const int cbytes = cols >> 1;
   const int ncols16 = cols >> 4;
   const int nvec = cbytes >> 4;           // 16-byte vectors per row
@@ -234,7 +238,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
           for (int h = 0; h < 2; ++h) {
             const int v = v0 + 32 * h;
             buf[u][h] = make_uint4(0, 0, 0, 0);
-            if (t[u] >= 0 && v < nvec)
+            if (t[u] >= 0 && v < nvec && QDBG(t[u] < (1 << 30)))
               buf[u][h] = __ldg(reinterpret_cast<const uint4*>(ic + (int64_t)t[u] * cbytes) + v);
           }
 #pragma unroll
@@ -306,7 +310,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
         g[j] = gates[(int64_t)t * kTopk + j];
       }
 #pragma unroll
-      for (int j = 0; j < kTopk; ++j) v[j] = *reinterpret_cast<const uint4*>(y + (int64_t)r[j] * ldy + c);
+      for (int j = 0; j < kTopk; ++j)
+        v[j] = QDBG(r[j] >= 0) ? *reinterpret_cast<const uint4*>(y + (int64_t)r[j] * ldy + c)
+                               : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int j = 0; j < kTopk; ++j) {
         float f[8];
@@ -333,6 +339,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
     *reinterpret_cast<uint4*>(out + (int64_t)t * ldo + c) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   }
 }
+
+int debug_line_moe() { return take_debug_line(); }
 
 }  // namespace quads
 
@@ -365,7 +373,7 @@ extern "C" quads_status_t quads_moe_route(const float* logits, int32_t tokens, i
   plan_kernel<<<num_experts, 256, 0, st>>>(bcount, nb, bprefix, expert_counts);
   assign_kernel<<<std::max(1, std::min(num_sms() * 4, (tokens * topk + 255) / 256)), 256, 0, st>>>(
       topk_idx, tokens, num_experts, topk, nb, bprefix, expert_offsets, expert_counts, row_token,
-      token_row);
+      token_row, rows_capacity);
   return check_launch("moe_route", tokens > 0 ? 3 : 2);
 }
 

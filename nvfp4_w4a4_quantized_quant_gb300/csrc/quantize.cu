@@ -83,151 +83,134 @@ __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restri
 }
 
 // ---------------------------------------------------------------- quantize
-// A block owns one (32-row chunk, 256-column slab) task.  Warp w quantizes
-// rows 4w .. 4w+3 of the chunk, two rows at a time: lane l takes the 16-element
-// block (l & 15) of row (l >> 4), so each block scale is computed once.  In
-// score mode every residual square R^2 is parked in shared memory and, after a
-// barrier, thread c adds column c's 32 squares in row order starting from 0 --
-// the fixed float32 order the score definition uses.  In QDQ mode (the
-// trainer's W4A16 fake quantization, [QUADS] 2.2 A) each element's dequantized
-// value fl(level * d_b) is also stored, rounded to bf16; codes and scales may
-// then be skipped (codes == nullptr).
-__device__ __forceinline__ void quantize_block16(const uint4& lo, const uint4& hi, float s_t,
-                                                 float* f, BlockScale& bs, uint2& c) {
-  bf16x8_to_f32(lo, f);
-  bf16x8_to_f32(hi, f + 8);
-  float m = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(f[j]));
-  bs = block_scale(m, s_t);
-  c.x = quantize8(f, bs);
-  c.y = quantize8(f + 8, bs);
-}
+// One warp per task = (32-row chunk, 256-column slab).  Lane l owns the eight
+// columns slab*256 + 8l .. +7, half of a 16-element block whose other half is
+// on lane l^1 (the block maximum takes one shuffle; both lanes then derive the
+// same block scale), and walks the chunk's rows in order with the next eight
+// rows' loads in flight (a register ring, unrolled so its indices are static).
+// In score mode the residual energy R^2 of each of its columns is added to a
+// register accumulator row by row from 0 -- the fixed float32 order of the
+// score definition -- and stored as the chunk's partials at the end: no shared
+// memory, no barrier.  Codes go out as one 4-byte word per lane (128 bytes per
+// warp and row), block scales as one 4-byte word per four blocks.  In QDQ mode
+// (the trainer's W4A16 fake quantization, [QUADS] 2.2 A) each element's
+// dequantized value fl(level * d_b) is also stored, rounded to bf16, as one
+// 16-byte vector per lane; codes and scales may then be skipped
+// (codes == nullptr).
+constexpr int kQAhead = 8;   // rows loaded ahead per warp
 
-// Score mode runs four blocks per SM (64 registers, no spills): measured
-// faster than three blocks at the unconstrained register count.
 template <bool kScores, bool kQdq>
-__global__ void __launch_bounds__(256, kScores ? 4 : 1) quantize_kernel(
+__global__ void __launch_bounds__(256, 2) quantize_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
     const int32_t* __restrict__ row_index, const int32_t* __restrict__ goff, int G,
     const float* __restrict__ st, const uint32_t* __restrict__ amax_bits, float* __restrict__ st_out,
     uint8_t* __restrict__ codes, int64_t ldc, uint8_t* __restrict__ scales, int layout,
-    float* __restrict__ partials, __nv_bfloat16* __restrict__ qdq, int64_t ldq) {
+    int sf_words, float* __restrict__ partials, __nv_bfloat16* __restrict__ qdq, int64_t ldq) {
   // tensor scales: given (st), or derived here from the groups' amax bits
   // (then block 0 also stores them to st_out)
-  __shared__ __align__(16) float sq[kScores ? kScoreChunk * 256 : 4];
   auto scale_of = [&](int g) {
     return amax_bits ? tensor_scale_from_amax(__uint_as_float(__ldg(amax_bits + g))) : __ldg(st + g);
   };
   if (amax_bits && blockIdx.x == 0)
     for (int g = threadIdx.x; g < G; g += blockDim.x) st_out[g] = scale_of(g);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t end = goff ? (int64_t)goff[G] : rows;
+  const int lane = threadIdx.x & 31;
+  int64_t end = goff ? (int64_t)goff[G] : rows;
+  if (!QDBG(end >= 0 && end <= rows)) end = 0;
   const int nslab = (cols + 255) >> 8;
   const int64_t nchunks = (end + kScoreChunk - 1) / kScoreChunk;
   const int64_t ntasks = nchunks * nslab;
   const int ncols16 = cols >> 4;
-  const int blk = lane & 15;
-  // this thread's two rows of a task, loaded one task ahead
-  auto load_task = [&](int64_t task, uint4 (&raw)[2][2]) {
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < ntasks;
+       task += nwarps) {
     const int64_t chunk = task / nslab;
-    const int col = (int)(task % nslab) * 256 + blk * 16;
-    const int64_t r0 = chunk * kScoreChunk;
-    const int64_t r1 = min(r0 + kScoreChunk, end);
-#pragma unroll
-    for (int it = 0; it < 2; ++it) {
-      const int64_t row = r0 + 4 * warp + 2 * it + (lane >> 4);
-      raw[it][0] = raw[it][1] = make_uint4(0, 0, 0, 0);
-      if (task < ntasks && col < cols && row < r1) {
-        const int64_t src = row_index ? (int64_t)row_index[row] : row;
-        const uint4* px = reinterpret_cast<const uint4*>(x + src * ldx + col);
-        raw[it][0] = __ldg(px);
-        raw[it][1] = __ldg(px + 1);
-      }
-    }
-  };
-  uint4 nxt[2][2];
-  load_task(blockIdx.x, nxt);
-  for (int64_t task = blockIdx.x; task < ntasks; task += gridDim.x) {
-    uint4 raw[2][2];
-#pragma unroll
-    for (int it = 0; it < 2; ++it) { raw[it][0] = nxt[it][0]; raw[it][1] = nxt[it][1]; }
-    load_task(task + gridDim.x, nxt);
-    const int64_t chunk = task / nslab;
-    const int slab = (int)(task % nslab);
-    const int col = slab * 256 + blk * 16;
+    const int col = (int)(task - chunk * nslab) * 256 + lane * 8;
     const bool active = col < cols;
     const int64_t r0 = chunk * kScoreChunk;
-    const int64_t r1 = min(r0 + kScoreChunk, end);
-    const int g0 = goff ? group_of(goff, G, r0) : 0;   // same for the whole block
-    const float s_t0 = scale_of(g0);
-#pragma unroll
-    for (int it = 0; it < 2; ++it) {
-      const int64_t row = r0 + 4 * warp + 2 * it + (lane >> 4);
-      const bool valid = active && row < r1;
-      int g = g0;
-      if (goff && valid)
-        while (g + 1 < G && row >= goff[g + 1]) ++g;
-      float f[16];
-      BlockScale bs;
-      uint2 c;
-      quantize_block16(raw[it][0], raw[it][1], !valid ? 1.0f : g == g0 ? s_t0 : scale_of(g), f, bs,
-                       c);
-      if (valid && (!kQdq || codes)) {
-        uint32_t* pc = reinterpret_cast<uint32_t*>(codes + row * ldc + (col >> 1));
-        pc[0] = c.x;
-        pc[1] = c.y;
-        scales[sf_offset(layout, row, col >> 4, ncols16)] = (uint8_t)bs.byte;
+    const int nr = (int)min((int64_t)kScoreChunk, end - r0);   // warp-uniform
+    auto load_row = [&](int i) {
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (active && i < nr) {
+        const int64_t src = row_index ? (int64_t)__ldg(row_index + r0 + i) : r0 + i;
+        v = __ldg(reinterpret_cast<const uint4*>(x + src * ldx + col));
       }
-      if (kQdq && valid) {
-        float lv[16];
-        e2m1x8_to_f32(c.x, lv);
-        e2m1x8_to_f32(c.y, lv + 8);
-        uint32_t packed[8];
+      return v;
+    };
+    uint4 ring[kQAhead];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(lv[2 * j], bs.d),
-                                                   __fmul_rn(lv[2 * j + 1], bs.d));
-          packed[j] = *reinterpret_cast<uint32_t*>(&h);
-        }
-        uint4* pq = reinterpret_cast<uint4*>(qdq + row * ldq + col);
-        pq[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        pq[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-      }
-      if (kScores) {
-        float lv[16];
-        e2m1x8_to_f32(c.x, lv);
-        e2m1x8_to_f32(c.y, lv + 8);
-        float4* ps = reinterpret_cast<float4*>(sq + (row - r0) * 256 + blk * 16);
+    for (int u = 0; u < kQAhead; ++u) ring[u] = load_row(u);
+    int g = goff ? group_of(goff, G, r0) : 0;
+    int64_t gnext = goff ? (int64_t)__ldg(goff + g + 1) : end;
+    float s_t = scale_of(g);
+    float acc[8];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float v[4];
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int i0 = 0; i0 < nr; i0 += kQAhead) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            // rows past the end were loaded as zeros: their codes and R are 0
-            const float R = __fsub_rn(f[4 * q + j], __fmul_rn(lv[4 * q + j], bs.d));
-            v[j] = __fmul_rn(R, R);
+      for (int u = 0; u < kQAhead; ++u) {
+        const int i = i0 + u;
+        const uint4 cur = ring[u];
+        ring[u] = load_row(i + kQAhead);
+        if (i < nr) {   // warp-uniform
+          const int64_t row = r0 + i;
+          while (row >= gnext) {   // a group boundary inside the chunk
+            // the partials of a chunk must belong to one group
+            if (kScores && lane == 0) atomicExch(&g_quant_error, QUADS_ERR_DEVICE_CHECK);
+            ++g;
+            gnext = __ldg(goff + g + 1);
+            s_t = scale_of(g);
           }
-          // 16-byte chunk q of this block lands at chunk q ^ ((blk >> 1) & 3): the
-          // eight lanes of a store phase then cover all 32 banks
-          ps[q ^ ((blk >> 1) & 3)] = make_float4(v[0], v[1], v[2], v[3]);
+          float f[8];
+          bf16x8_to_f32(cur, f);
+          float m = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+          const BlockScale bs = block_scale(m, s_t);
+          const uint32_t c = quantize8(f, bs);
+          if (!kQdq || codes) {
+            if (active) *reinterpret_cast<uint32_t*>(codes + row * ldc + (col >> 1)) = c;
+            if (sf_words) {
+              // blocks 4q .. 4q+3 of the slab sit on lanes 8q, 8q+2, 8q+4, 8q+6
+              const uint32_t b1 = __shfl_down_sync(0xffffffffu, bs.byte, 2);
+              const uint32_t b2 = __shfl_down_sync(0xffffffffu, bs.byte, 4);
+              const uint32_t b3 = __shfl_down_sync(0xffffffffu, bs.byte, 6);
+              if ((lane & 7) == 0 && active)
+                *reinterpret_cast<uint32_t*>(scales + sf_offset(layout, row, col >> 4, ncols16)) =
+                    bs.byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+            } else if ((lane & 1) == 0 && active) {
+              scales[sf_offset(layout, row, col >> 4, ncols16)] = (uint8_t)bs.byte;
+            }
+          }
+          if (kQdq || kScores) {
+            float lv[8];
+            e2m1x8_to_f32(c, lv);
+            if (kQdq && active) {
+              uint32_t packed[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(lv[2 * j], bs.d),
+                                                         __fmul_rn(lv[2 * j + 1], bs.d));
+                packed[j] = *reinterpret_cast<uint32_t*>(&h);
+              }
+              *reinterpret_cast<uint4*>(qdq + row * ldq + col) =
+                  make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            }
+            if (kScores) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float R = __fsub_rn(f[j], __fmul_rn(lv[j], bs.d));
+                acc[j] = __fadd_rn(acc[j], __fmul_rn(R, R));
+              }
+            }
+          }
         }
       }
     }
-    if (kScores) {
-      __syncthreads();
-      const int c = slab * 256 + (int)threadIdx.x;
-      if (c < cols) {
-        float acc = 0.0f;
-        const int nr = (int)(r1 - r0);
-        // column c sits at its swizzled position (chunk of 4 within its 16-block)
-        const int cb = (int)threadIdx.x >> 4;
-        const int pc = ((int)threadIdx.x & ~15) | (((((int)threadIdx.x >> 2) & 3) ^ ((cb >> 1) & 3)) << 2) |
-                       ((int)threadIdx.x & 3);
-        for (int r = 0; r < nr; ++r) acc = __fadd_rn(acc, sq[r * 256 + pc]);
-        partials[chunk * cols + c] = acc;
-      }
-      __syncthreads();
+    if (kScores && active) {
+      float4* pp = reinterpret_cast<float4*>(partials + chunk * cols + col);
+      pp[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      pp[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
   }
 }
@@ -434,6 +417,7 @@ __global__ void __launch_bounds__(256) rsel_residual_kernel(
         r[u] = r0 + (i < total ? i / k : 0);
         j[u] = i < total ? i % k : 0;
         c[u] = sg[j[u]];
+        if (!QDBG(c[u] >= 0 && c[u] < cols)) c[u] = 0;
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -510,6 +494,7 @@ __global__ void __launch_bounds__(kRselGroupThreads) rsel_group_kernel(
       r[u] = r0 + (i < total ? i / k : 0);
       j[u] = i < total ? i % k : 0;
       c[u] = sg[j[u]];
+      if (!QDBG(c[u] >= 0 && c[u] < cols)) c[u] = 0;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -627,59 +612,98 @@ __device__ __forceinline__ int signed_index(uint32_t c) {
   return (c & 8u) ? -m : m;
 }
 
-// One thread per 8 consecutive elements of a row (one half of a 16-block).
-// Neighbours and the choice are taken on signed level indices: the RTN level
-// sn is one neighbour of v and the other is sn - 1 (RTN level above v) or
-// sn + 1 (below v); of two adjacent levels the one nearer the rollout level
-// sr is the lower one exactly when sr <= the lower index.
+// One thread per 16-element block of a row per step (kMx: per 16 elements of
+// a 32-element block), with the next step's loads (x, rollout codes, scale)
+// issued before the current block is computed, so that loads stay in flight
+// across the arithmetic.  Neighbours and the choice are taken on signed level
+// indices: the RTN level sn is one neighbour of v and the other is sn - 1
+// (RTN level above v) or sn + 1 (below v); the level of {ilo, ihi} nearer the
+// rollout level sr is sr clamped to [ilo, ihi] (the two are adjacent, so sr
+// cannot fall strictly between them).
 // kMx: MXFP4 rollout (E8M0 scale per 32 elements, no tensor scale): the
 // scaled value is x * 2^-e and no block is a zero block.
+struct TraceItem {
+  uint4 x0, x1;     // 16 bf16
+  uint2 rc;         // 16 rollout codes
+  uint32_t sbyte;   // block scale byte
+};
+
+template <bool kMx>
+__device__ __forceinline__ void trace_load(TraceItem& it, uint32_t i, uint32_t total,
+                                           uint32_t blk_per_row, const __nv_bfloat16* xt,
+                                           int64_t ldx, const uint8_t* rcodes, int64_t ldc,
+                                           const uint8_t* rscales, int cols) {
+  if (i >= total) return;
+  const uint32_t r = i / blk_per_row;
+  const int col = (int)(i - r * blk_per_row) * 16;
+  const uint4* px = reinterpret_cast<const uint4*>(xt + (int64_t)r * ldx + col);
+  it.x0 = __ldg(px);
+  it.x1 = __ldg(px + 1);
+  const uint32_t* pc = reinterpret_cast<const uint32_t*>(rcodes + (int64_t)r * ldc + (col >> 1));
+  it.rc = make_uint2(__ldg(pc), __ldg(pc + 1));   // 4-byte aligned (ldc % 4 == 0)
+  it.sbyte = kMx ? __ldg(rscales + (int64_t)r * (cols >> 5) + (col >> 5))
+                 : __ldg(rscales + (int64_t)r * (cols >> 4) + (col >> 4));
+}
+
 template <bool kMx>
 __global__ void __launch_bounds__(256) trace_kernel(
     const __nv_bfloat16* __restrict__ xt, int64_t rows, int cols, int64_t ldx,
     const uint8_t* __restrict__ rcodes, int64_t ldc, const uint8_t* __restrict__ rscales,
     const float* __restrict__ rst, uint8_t* __restrict__ out,
     unsigned long long* __restrict__ counters) {
-  const uint32_t vec_per_row = (uint32_t)cols >> 3;
-  const uint32_t total = (uint32_t)(rows * vec_per_row);   // < 2^31 (host check)
+  const uint32_t blk_per_row = (uint32_t)cols >> 4;
+  const uint32_t total = (uint32_t)(rows * blk_per_row);   // < 2^31 (host check)
+  const uint32_t stride = gridDim.x * blockDim.x;
   const float s_t = kMx ? 1.0f : rst[0];
   unsigned int n_rtn = 0, n_tr = 0, n_adj = 0;
-  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
-    const uint32_t r = i / vec_per_row;
-    const int col = (int)(i - r * vec_per_row) * 8;
-    float f[8];
-    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(xt + (int64_t)r * ldx + col)), f);
-    const uint32_t rc = __ldg(reinterpret_cast<const uint32_t*>(rcodes + (int64_t)r * ldc + (col >> 1)));
+  uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  TraceItem nxt;
+  trace_load<kMx>(nxt, i, total, blk_per_row, xt, ldx, rcodes, ldc, rscales, cols);
+  for (; i < total; i += stride) {
+    const TraceItem cur = nxt;
+    trace_load<kMx>(nxt, i + stride, total, blk_per_row, xt, ldx, rcodes, ldc, rscales, cols);
+    const uint32_t r = i / blk_per_row;
+    const int col = (int)(i - r * blk_per_row) * 16;
     BlockScale bs;
     if (kMx) {
-      bs.byte = __ldg(rscales + (int64_t)r * (cols >> 5) + (col >> 5));
-      bs.r = e8m0_inverse(bs.byte);
+      bs.r = e8m0_inverse(cur.sbyte);
       bs.zero = false;
     } else {
-      bs = block_scale_from_byte(__ldg(rscales + (int64_t)r * (cols >> 4) + (col >> 4)), s_t);
+      bs = block_scale_from_byte(cur.sbyte, s_t);
     }
-    float v[8];
+    uint32_t outw[2];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(f[j], bs.r);
-    const uint32_t rtn = bs.zero ? 0u : f32x8_to_e2m1(v);
-    float qn[8];
-    e2m1x8_to_f32(rtn, qn);
-    uint32_t outw = 0;
+    for (int h = 0; h < 2; ++h) {
+      float f[8];
+      bf16x8_to_f32(h ? cur.x1 : cur.x0, f);
+      const uint32_t rc = h ? cur.rc.y : cur.rc.x;
+      float v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int sn = signed_index((rtn >> (4 * j)) & 15u);
-      const int sr = signed_index((rc >> (4 * j)) & 15u);
-      const float vc = fminf(fmaxf(v[j], -6.0f), 6.0f);
-      const int ilo = sn - (qn[j] > vc ? 1 : 0);
-      const int ihi = sn + (qn[j] < vc ? 1 : 0);
-      const int stc = bs.zero ? 0 : (sr <= ilo ? ilo : ihi);
-      const bool neg = !bs.zero && (stc < 0 || (stc == 0 && signbit(v[j])));
-      outw |= ((uint32_t)abs(stc) | (neg ? 8u : 0u)) << (4 * j);
-      n_rtn += sn != sr ? 1u : 0u;
-      n_adj += (sn != sr && abs(sn - sr) == 1) ? 1u : 0u;
-      n_tr += stc != sr ? 1u : 0u;
+      for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(f[j], bs.r);
+      const uint32_t rtn = bs.zero ? 0u : f32x8_to_e2m1(v);
+      float qn[8];
+      e2m1x8_to_f32(rtn, qn);
+      uint32_t w = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int sn = signed_index((rtn >> (4 * j)) & 15u);
+        const int sr = signed_index((rc >> (4 * j)) & 15u);
+        const float vc = fminf(fmaxf(v[j], -6.0f), 6.0f);
+        const int ilo = sn - (qn[j] > vc ? 1 : 0);
+        const int ihi = sn + (qn[j] < vc ? 1 : 0);
+        const int stc = bs.zero ? 0 : min(max(sr, ilo), ihi);
+        const bool neg = !bs.zero && (stc < 0 || (stc == 0 && signbit(v[j])));
+        w |= ((uint32_t)abs(stc) | (neg ? 8u : 0u)) << (4 * j);
+        const int dd = sn - sr;
+        n_rtn += dd != 0 ? 1u : 0u;
+        n_adj += (dd == 1 || dd == -1) ? 1u : 0u;
+        n_tr += stc != sr ? 1u : 0u;
+      }
+      outw[h] = w;
     }
-    *reinterpret_cast<uint32_t*>(out + (int64_t)r * ldc + (col >> 1)) = outw;
+    uint32_t* po = reinterpret_cast<uint32_t*>(out + (int64_t)r * ldc + (col >> 1));
+    po[0] = outw[0];
+    po[1] = outw[1];
   }
   if (counters) {
 #pragma unroll
@@ -792,40 +816,66 @@ __global__ void __launch_bounds__(256) trace_1bit_kernel(
     const uint8_t* __restrict__ mbits, int64_t ldb, const uint8_t* __restrict__ rscales,
     const float* __restrict__ rst, uint8_t* __restrict__ out, int64_t ldc,
     unsigned long long* __restrict__ counters) {
-  const uint32_t vec_per_row = (uint32_t)cols >> 3;
-  const uint32_t total = (uint32_t)(rows * vec_per_row);   // < 2^31 (host check)
+  // one 16-element block per thread and step, the next step's loads issued
+  // before the current block is computed (as in trace_kernel)
+  const uint32_t blk_per_row = (uint32_t)cols >> 4;
+  const uint32_t total = (uint32_t)(rows * blk_per_row);   // < 2^31 (host check)
+  const uint32_t stride = gridDim.x * blockDim.x;
   const float s_t = rst[0];
   unsigned int n_chg = 0, n_bit = 0;
-  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
-    const uint32_t r = i / vec_per_row;
-    const uint32_t vi = i - r * vec_per_row;
-    const int col = (int)vi * 8;
-    float f[8];
-    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(xt + (int64_t)r * ldx + col)), f);
-    const uint32_t mb = __ldg(mbits + (int64_t)r * ldb + vi);
-    const BlockScale bs =
-        block_scale_from_byte(__ldg(rscales + (int64_t)r * (cols >> 4) + (col >> 4)), s_t);
-    float v[8];
+  auto load = [&](uint32_t i, uint4& x0, uint4& x1, uint32_t& mb, uint32_t& sb) {
+    if (i >= total) return;
+    const uint32_t r = i / blk_per_row;
+    const uint32_t bi = i - r * blk_per_row;
+    const uint4* px = reinterpret_cast<const uint4*>(xt + (int64_t)r * ldx + bi * 16);
+    x0 = __ldg(px);
+    x1 = __ldg(px + 1);
+    const uint8_t* pb = mbits + (int64_t)r * ldb + bi * 2;
+    mb = (uint32_t)__ldg(pb) | ((uint32_t)__ldg(pb + 1) << 8);
+    sb = __ldg(rscales + (int64_t)r * (cols >> 4) + bi);
+  };
+  uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  uint4 nx0 = make_uint4(0, 0, 0, 0), nx1 = nx0;
+  uint32_t nmb = 0, nsb = 0;
+  load(i, nx0, nx1, nmb, nsb);
+  for (; i < total; i += stride) {
+    const uint4 x0 = nx0, x1 = nx1;
+    const uint32_t mb16 = nmb, sbyte = nsb;
+    load(i + stride, nx0, nx1, nmb, nsb);
+    const uint32_t r = i / blk_per_row;
+    const uint32_t bi = i - r * blk_per_row;
+    const BlockScale bs = block_scale_from_byte(sbyte, s_t);
+    uint32_t outw[2];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(f[j], bs.r);
-    const uint32_t rtn = bs.zero ? 0u : f32x8_to_e2m1(v);
-    float qn[8];
-    e2m1x8_to_f32(rtn, qn);
-    uint32_t outw = 0;
+    for (int h = 0; h < 2; ++h) {
+      float f[8];
+      bf16x8_to_f32(h ? x1 : x0, f);
+      const uint32_t mb = (mb16 >> (8 * h)) & 0xFFu;
+      float v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int sn = signed_index((rtn >> (4 * j)) & 15u);
-      const float vc = fminf(fmaxf(v[j], -6.0f), 6.0f);
-      const int ilo = sn - (qn[j] > vc ? 1 : 0);
-      const int ihi = sn + (qn[j] < vc ? 1 : 0);
-      const int bit = (int)((mb >> j) & 1u);
-      const int stc = bs.zero ? 0 : ((abs(ilo) & 1) == bit ? ilo : ihi);
-      const bool neg = !bs.zero && (stc < 0 || (stc == 0 && signbit(v[j])));
-      outw |= ((uint32_t)abs(stc) | (neg ? 8u : 0u)) << (4 * j);
-      n_chg += stc != sn ? 1u : 0u;
-      n_bit += (abs(stc) & 1) != bit ? 1u : 0u;
+      for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(f[j], bs.r);
+      const uint32_t rtn = bs.zero ? 0u : f32x8_to_e2m1(v);
+      float qn[8];
+      e2m1x8_to_f32(rtn, qn);
+      uint32_t w = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int sn = signed_index((rtn >> (4 * j)) & 15u);
+        const float vc = fminf(fmaxf(v[j], -6.0f), 6.0f);
+        const int ilo = sn - (qn[j] > vc ? 1 : 0);
+        const int ihi = sn + (qn[j] < vc ? 1 : 0);
+        const int bit = (int)((mb >> j) & 1u);
+        const int stc = bs.zero ? 0 : ((abs(ilo) & 1) == bit ? ilo : ihi);
+        const bool neg = !bs.zero && (stc < 0 || (stc == 0 && signbit(v[j])));
+        w |= ((uint32_t)abs(stc) | (neg ? 8u : 0u)) << (4 * j);
+        n_chg += stc != sn ? 1u : 0u;
+        n_bit += (abs(stc) & 1) != bit ? 1u : 0u;
+      }
+      outw[h] = w;
     }
-    *reinterpret_cast<uint32_t*>(out + (int64_t)r * ldc + (col >> 1)) = outw;
+    uint32_t* po = reinterpret_cast<uint32_t*>(out + (int64_t)r * ldc + bi * 8);
+    po[0] = outw[0];
+    po[1] = outw[1];
   }
   if (counters) {
 #pragma unroll
@@ -916,21 +966,25 @@ static quads_status_t quantize_impl(
     const int64_t start = (rows / 128) * (ncols16 / 4) * 512;
     cudaMemsetAsync(scales + start, 0, (size_t)(sf_tc_bytes(rows, cols) - start), st);
   }
-  const int64_t ntasks = ((rows + 31) / 32) * ((cols + 255) / 256);  // one block per task
-  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(ntasks, (int64_t)num_sms() * 16));
+  // one warp per (32-row chunk, 256-column slab) task, eight warps per block
+  const int64_t ntasks = ((rows + 31) / 32) * ((cols + 255) / 256);
+  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((ntasks + 7) / 8, (int64_t)num_sms() * 8));
+  // four consecutive block scales of a row are contiguous (and word-aligned)
+  // in both layouts when cols % 64 == 0
+  const int sf_words = (cols % 64 == 0 && ((uintptr_t)scales & 3u) == 0) ? 1 : 0;
   const __nv_bfloat16* xb = (const __nv_bfloat16*)x;
   if (qdq)
     quantize_kernel<false, true><<<blocks, 256, 0, st>>>(
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
-        codes, ld_codes, scales, scale_layout, nullptr, qdq, ldq);
+        codes, ld_codes, scales, scale_layout, sf_words, nullptr, qdq, ldq);
   else if (score_partials)
     quantize_kernel<true, false><<<blocks, 256, 0, st>>>(
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
-        codes, ld_codes, scales, scale_layout, score_partials, nullptr, 0);
+        codes, ld_codes, scales, scale_layout, sf_words, score_partials, nullptr, 0);
   else
     quantize_kernel<false, false><<<blocks, 256, 0, st>>>(
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
-        codes, ld_codes, scales, scale_layout, nullptr, nullptr, 0);
+        codes, ld_codes, scales, scale_layout, sf_words, nullptr, nullptr, 0);
   return check_launch(qdq ? "qdq" : "quantize", launched);
 }
 
@@ -980,6 +1034,8 @@ quads_status_t select_check_args(const void* x, int64_t rows, int64_t cols, int6
   *need = quads_workspace_size(QUADS_OP_SELECT, rows, cols, 0, k, group_offsets ? num_groups : 1);
   return QUADS_OK;
 }
+int debug_line_quantize() { return take_debug_line(); }
+
 }  // namespace quads
 
 extern "C" quads_status_t quads_select_residual_channels(
@@ -1053,13 +1109,14 @@ extern "C" quads_status_t quads_trace_round(const void* x_train, int64_t rows, i
   if (rows > 0 && (!x_train || !rollout_codes || !rollout_scales || !rollout_tensor_scale || !codes_out))
     return fail(QUADS_ERR_INVALID_ARG, "trace_round: null pointer argument");
   if (cols <= 0 || cols % 16) return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "trace_round: cols %% 16");
-  if (ldx < cols || ldx % 8 || ld_codes < cols / 2 || ld_codes % 4 || !aligned16(x_train))
+  if (ldx < cols || ldx % 8 || ld_codes < cols / 2 || ld_codes % 4 || !aligned16(x_train) ||
+      ((uintptr_t)rollout_codes & 3u) || ((uintptr_t)codes_out & 3u))
     return fail(QUADS_ERR_MISALIGNED, "trace_round: leading dimensions / alignment");
   if (rows == 0) return QUADS_OK;
   if (rows * (cols / 8) >= ((int64_t)1 << 31))
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "trace_round: rows * cols / 8 must be < 2^31");
   cudaStream_t st = (cudaStream_t)stream;
-  trace_kernel<false><<<grid_for(rows * (cols / 8), 256), 256, 0, st>>>(
+  trace_kernel<false><<<grid_for(rows * (cols / 16), 256), 256, 0, st>>>(
       (const __nv_bfloat16*)x_train, rows, (int)cols, ldx, rollout_codes, ld_codes,
       rollout_scales, rollout_tensor_scale, codes_out, counters);
   return check_launch("trace_round", 1);
@@ -1079,7 +1136,7 @@ extern "C" quads_status_t quads_trace_round_mx(const void* x_train, int64_t rows
   if (rows < 0 || rows * (cols / 8) >= ((int64_t)1 << 31))
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "trace_round_mx: rows * cols / 8 must be < 2^31");
   if (rows == 0) return QUADS_OK;
-  trace_kernel<true><<<grid_for(rows * (cols / 8), 256), 256, 0, (cudaStream_t)stream>>>(
+  trace_kernel<true><<<grid_for(rows * (cols / 16), 256), 256, 0, (cudaStream_t)stream>>>(
       (const __nv_bfloat16*)x_train, rows, (int)cols, ldx, rollout_codes, ld_codes,
       rollout_scales, nullptr, codes_out, counters);
   return check_launch("trace_round_mx", 1);
@@ -1152,7 +1209,7 @@ extern "C" quads_status_t quads_trace_round_1bit(const void* x_train, int64_t ro
   if (rows * (cols / 8) >= ((int64_t)1 << 31))
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "trace_round_1bit: rows * cols / 8 must be < 2^31");
   if (rows == 0) return QUADS_OK;
-  trace_1bit_kernel<<<grid_for(rows * (cols / 8), 256), 256, 0, (cudaStream_t)stream>>>(
+  trace_1bit_kernel<<<grid_for(rows * (cols / 16), 256), 256, 0, (cudaStream_t)stream>>>(
       (const __nv_bfloat16*)x_train, rows, (int)cols, ldx, mantissa_bits, ld_bits,
       rollout_scales, rollout_tensor_scale, codes_out, ld_codes, counters);
   return check_launch("trace_round_1bit", 1);

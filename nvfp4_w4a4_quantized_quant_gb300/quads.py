@@ -15,7 +15,7 @@ from typing import Optional
 
 import torch
 
-from .build import LIB, ROOT
+from .build import DEBUG_LIB, LIB, ROOT
 
 LINEAR, TCGEN05 = 0, 1
 OUT_F32, OUT_BF16 = 0, 1
@@ -32,6 +32,7 @@ _SIGS = {
     "quads_status_string": (ctypes.c_char_p, [_I32]),
     "quads_last_error_detail": (ctypes.c_char_p, []),
     "quads_device_status": (_I32, [_P, ctypes.POINTER(_I32)]),
+    "quads_test_gemm_wait_timeout": (None, [_I32]),
     "quads_workspace_size": (_SZ, [_I32, _I64, _I64, _I64, _I32, _I32]),
     "quads_kpad": (_I32, [_I32]),
     "quads_quantize_nvfp4": (_I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P, _I64, _P,
@@ -71,9 +72,12 @@ def header_symbols() -> list[str]:
     return sorted(set(re.findall(r"\b(quads_[a-z0-9_]+)\s*\(", text)))
 
 
-def load(path: str = LIB):
-    """Load libquads.so (no CUDA device needed for loading)."""
+def load(path: Optional[str] = None):
+    """Load libquads.so (no CUDA device needed for loading); the bounds-checked
+    build when QUADS_DEBUG_LIB=1."""
     global _lib
+    if path is None:
+        path = DEBUG_LIB if os.environ.get("QUADS_DEBUG_LIB") == "1" else LIB
     if _lib is None:
         if not os.path.exists(path):
             raise RuntimeError(f"libquads is not built ({path}); run "
@@ -142,6 +146,12 @@ def device_status(stream=None) -> int:
     code = _I32(0)
     _check(load().quads_device_status(_stream(stream), ctypes.byref(code)), "device_status")
     return int(code.value)
+
+
+def test_gemm_wait_timeout(enable: bool = True) -> None:
+    """Test hook: the next GEMM launch runs with a 1 ms wait limit and an MMA
+    issuer that issues nothing, so that its bounded waits run out."""
+    load().quads_test_gemm_wait_timeout(1 if enable else 0)
 
 
 @dataclass

@@ -166,3 +166,46 @@ def test_select_weight_channels_per_group(lib, G, N, K, k):
         wsc, wss = Q.requantize_weight_columns(wc[rows], ws[rows], sel[g])
         assert np.array_equal(c[rows, :k], wsc) and not c[rows, k:].any()
         assert np.array_equal(s[rows, : k // 16], wss) and not s[rows, k // 16:].any()
+
+
+@pytest.mark.parametrize("M,N,K,k", [(384, 256, 768, 64), (64, 128, 64, 64)])
+def test_correction_shares_the_last_stage(lib, M, N, K, k):
+    """K = 768 (three 256-element sub-tiles): the k-channel correction rides in
+    the second slot of the last stage; K = 64: main and correction sub-tiles
+    share the only stage.  M = 384 leaves the second CTA pair half-empty."""
+    rng = inputs.make_rng(M * 7 + K)
+    xb = inputs.f32_to_bf16_bits(inputs.student_t4(rng, (M, K)))
+    wb = inputs.f32_to_bf16_bits(rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02))
+    y, sel, ws = _run(lib, xb, wb, k, torch.float32)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    Y, B, ref, wsel = _oracle(xb, wb, k)
+    assert np.array_equal(sel.cpu().numpy(), ref["sel"])
+    _check(y, Y, B, False)
+
+
+def test_gemm_wait_timeout_is_reported_and_the_device_stays_usable(lib):
+    """The test hook makes the next GEMM's MMA issuer issue nothing under a 1 ms
+    wait limit: its producers' and epilogue's bounded waits run out, the kernel
+    reports QUADS_ERR_DEVICE_TIMEOUT and returns.  The next call is normal and
+    matches the oracle."""
+    # K = 4096: eight ring stages per tile, more than the ring holds, so the
+    # producers also block on a free stage with their copies landed
+    rng = inputs.make_rng(5)
+    x = bf16_tensor(inputs.f32_to_bf16_bits(inputs.student_t4(rng, (256, 4096))))
+    w = bf16_tensor(inputs.f32_to_bf16_bits(rng.standard_normal((256, 4096), dtype=np.float32)))
+    xq, _ = lib.quantize_nvfp4(x, scale_layout=1)
+    wq, _ = lib.quantize_nvfp4(w, scale_layout=1)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    lib.test_gemm_wait_timeout(True)
+    lib.w4a4_gemm_comp(xq, wq, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 5          # QUADS_ERR_DEVICE_TIMEOUT, read and cleared
+    assert lib.device_status() == 0
+    d = inputs.single_linear(0)
+    y, _, _ = _run(lib, d["x"], d["w"], d["k"], torch.float32, comp=False)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    Y, B, _, _ = _oracle(d["x"], d["w"], d["k"], comp=False)
+    _check(y, Y, B, False)

@@ -10,6 +10,7 @@ import torch
 
 from helpers import bf16_tensor, check_combine, codes_np, f32, unswizzle
 from nvfp4_w4a4_quantized_quant_gb300 import inputs
+from oracle import gemm as G
 from oracle import moe as M
 from oracle import nvfp4 as Q
 
@@ -147,3 +148,50 @@ def test_moe_layer_decode_shaped_with_empty_experts(lib):
 def test_moe_layer_ragged_tokens_three_tiles(lib):
     d = inputs.moe_layer(2, tokens=300, hidden=512, experts=4, topk=2, ffn=256, k=64)
     _check_layer(lib, d, 64, 64)
+
+
+def _check_plain_layer(lib, d, experts=None):
+    """The layer without compensation (plain W4A4 both GEMMs): routing, A rows,
+    h within the GEMM1 tolerance of the oracle's plain product, h's per-expert
+    codes bit for bit (teacher-forced on the GPU's h), y within tolerance of the
+    plain GEMM2 on those codes, and the combine."""
+    layer, res = _layer(lib, d, 16, 16, compensate=False)
+    E, twoF, H = d["w1"].shape
+    F, topk = twoF // 2, d["topk"]
+    plan = res["plan"]
+    xf = f32(d["x"])
+    w1q, w2q = M.quantize_weights(f32(d["w1"])), M.quantize_weights(f32(d["w2"]))
+    oidx, _ = M.route(d["logits"], topk)
+    assert np.array_equal(plan["idx"].cpu().numpy(), oidx)
+    toks = M.dispatch(oidx, E)
+    cnt = plan["counts"].cpu().numpy()
+    off = plan["offsets"].cpu().numpy()
+    trow = plan["token_row"].cpu().numpy()
+    xc, xs, xst = Q.quantize_groups(xf)
+    h = res["h"].float().cpu().numpy().astype(np.float64)
+    y = res["y"].float().cpu().numpy().astype(np.float64)
+    hqc = codes_np(res["hq"].codes, F)
+    hqs = unswizzle(res["hq"].scales, layer.cap, F)
+    hts = res["hq"].tensor_scale.cpu().numpy()
+    for e in (range(E) if experts is None else experts):
+        n = cnt[e]
+        if n == 0:
+            continue
+        rows = slice(off[e], off[e] + n)
+        t = toks[e]
+        Y1, B1 = G.gemm_comp(xc[t], xs[t], xst[0], w1q[0][e], w1q[1][e], w1q[2][e])
+        href = M.bf16_round(M.silu_mul(Y1[:, :F], Y1[:, F:]))
+        assert np.all(np.abs(h[rows] - href) <= _h_tol(Y1, B1, F))
+        hc, hs, hst = Q.quantize_groups(h[rows].astype(np.float32))
+        assert hts[e] == hst[0]
+        assert np.array_equal(hqc[rows], hc) and np.array_equal(hqs[rows], hs)
+        Y2, B2 = G.gemm_comp(hc, hs, hst[0], w2q[0][e], w2q[1][e], w2q[2][e])
+        assert np.all(np.abs(y[rows] - Y2) <= 1e-3 * B2 + 2.0 ** -8 * np.abs(Y2) + 1e-30)
+    if experts is None:
+        check_combine(res["out"].float().cpu().numpy(), oidx, plan["gates"].cpu().numpy(),
+                      res["y"].float().cpu().numpy()[trow])
+
+
+def test_moe_layer_plain_w4a4(lib):
+    d = inputs.moe_layer(2, tokens=300, hidden=512, experts=4, topk=2, ffn=256, k=64)
+    _check_plain_layer(lib, d)
