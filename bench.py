@@ -205,6 +205,9 @@ def secondary(torch, Q, steps, flush, stream):
                                f"{Q.load().quads_last_error_detail().decode()}")
 
     def graph_ms(fn):
+        # inputs prepared on the default stream must be complete before `stream`
+        # (which does not wait for the default stream) uses them
+        torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             fn()
             torch.cuda.synchronize()

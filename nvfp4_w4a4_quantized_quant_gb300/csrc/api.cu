@@ -49,9 +49,9 @@ int num_sms() {
 
 int read_quant_device_error(cudaStream_t);
 int read_gemm_device_error();
-int debug_line_quantize();
-int debug_line_gemm();
-int debug_line_moe();
+int debug_line_quantize(long long* value);
+int debug_line_gemm(long long* value);
+int debug_line_moe(long long* value);
 
 }  // namespace quads
 
@@ -115,10 +115,13 @@ extern "C" quads_status_t quads_device_status(void* stream, int32_t* device_code
   int q = read_quant_device_error((cudaStream_t)stream);
   *device_code = g ? g : q;
   // bounds-checked builds: the first failed guard of each source file
-  const int lq = debug_line_quantize(), lg = debug_line_gemm(), lm = debug_line_moe();
+  long long vq = 0, vg = 0, vm = 0;
+  const int lq = debug_line_quantize(&vq), lg = debug_line_gemm(&vg), lm = debug_line_moe(&vm);
   if (lq || lg || lm) {
     *device_code = QUADS_ERR_DEVICE_CHECK;
-    set_detail("bounds check failed: quantize.cu:%d gemm.cu:%d moe.cu:%d (0 = none)", lq, lg, lm);
+    set_detail("bounds check failed: quantize.cu:%d (%lld) gemm.cu:%d (%lld) moe.cu:%d (%lld) "
+               "(line 0 = none; the value recorded with the first failure)",
+               lq, vq, lg, vg, lm, vm);
   }
   return QUADS_OK;
 }

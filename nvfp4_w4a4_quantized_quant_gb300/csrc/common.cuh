@@ -40,21 +40,32 @@ quads_status_t select_check_args(const void* x, int64_t rows, int64_t cols, int6
 // the guards away.
 #ifdef QUADS_DEBUG
 static __device__ int g_debug_line;
-__device__ __forceinline__ bool quads_dbg(bool ok, int line) {
-  if (!ok) atomicCAS(&g_debug_line, 0, line);
+static __device__ long long g_debug_value;
+__device__ __forceinline__ bool quads_dbg(bool ok, int line, long long value) {
+  if (!ok && atomicCAS(&g_debug_line, 0, line) == 0) g_debug_value = value;
   return ok;
 }
-#define QDBG(cond) quads_dbg((cond), __LINE__)
-// Host side: read and clear this translation unit's debug word.
-[[maybe_unused]] static int take_debug_line() {
+#define QDBG(cond) quads_dbg((cond), __LINE__, 0)
+#define QDBGV(cond, value) quads_dbg((cond), __LINE__, (long long)(value))
+// Host side: read and clear this translation unit's debug word (and the
+// value recorded with it).
+[[maybe_unused]] static int take_debug_line(long long* value) {
   int v = 0, z = 0;
+  long long val = 0, zz = 0;
   cudaMemcpyFromSymbol(&v, g_debug_line, sizeof(int));
+  cudaMemcpyFromSymbol(&val, g_debug_value, sizeof(long long));
   cudaMemcpyToSymbol(g_debug_line, &z, sizeof(int));
+  cudaMemcpyToSymbol(g_debug_value, &zz, sizeof(long long));
+  *value = val;
   return v;
 }
 #else
 #define QDBG(cond) true
-[[maybe_unused]] static int take_debug_line() { return 0; }
+#define QDBGV(cond, value) true
+[[maybe_unused]] static int take_debug_line(long long* value) {
+  *value = 0;
+  return 0;
+}
 #endif
 
 // ------------------------------------------------------------ scale layouts

@@ -469,10 +469,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (b >= BOXES) {
               const uint32_t sfbytes = (p.mx ? ksteps / 2 : ksteps) * 512;
               const uint8_t* src = (b == BOXES ? sfa : sfb) + kk * sf_stage;
-              const uint8_t* base = b == BOXES ? (corr ? p.r_sf : p.a_sf) : (corr ? p.ws_sf : p.b_sf);
-              const int64_t lim = b == BOXES ? (corr ? p.r_sf_bytes : p.a_sf_bytes)
-                                             : (corr ? p.ws_sf_bytes : p.b_sf_bytes);
-              if (!QDBG(src >= base && src - base + sfbytes <= lim)) {
+              [[maybe_unused]] const uint8_t* base =
+                  b == BOXES ? (corr ? p.r_sf : p.a_sf) : (corr ? p.ws_sf : p.b_sf);
+              [[maybe_unused]] const int64_t lim = b == BOXES ? (corr ? p.r_sf_bytes : p.a_sf_bytes)
+                                                              : (corr ? p.ws_sf_bytes : p.b_sf_bytes);
+              if (!QDBGV(src >= base && src - base + sfbytes <= lim,
+                         (tl.m0 << 20) | ((int64_t)tl.e << 8) | (corr ? 2 : 0) | (b == BOXES ? 0 : 4))) {
                 mbar_arrive(&full[s]);   // skipped copy: the stage still completes
                 continue;
               }
@@ -1012,6 +1014,7 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const int32_t* poff
   const int64_t pairs = poff[e + 1] - poff[e];
   const int64_t local = t - (int64_t)poff[e] * p.Nt;
   const int64_t o0 = __ldg(p.row_off + e), o1 = __ldg(p.row_off + e + 1);
+  (void)QDBGV(o0 >= 0 && o0 <= o1 && o1 <= p.y_rows && pairs > 0, (o1 << 16) | e);
   r.e = e;
   r.m0 = o0 + (local % pairs) * 2 * BM;
   r.n0 = (int)(local / pairs) * BN;
@@ -1185,14 +1188,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                            : blk * a_sf_rb + (int64_t)sb.kk * sf_sub;
                 const int64_t ow = sb.corr ? (bbase / BM) * r_sf_rb + (int64_t)sb.kk * SF_SUB
                                            : (bbase / BM) * a_sf_rb + (int64_t)sb.kk * sf_sub;
-                if (QDBG(oa >= 0 && oa + bytes <= (sb.corr ? p.r_sf_bytes : p.a_sf_bytes))) {
+                if (QDBGV(oa >= 0 && oa + bytes <= (sb.corr ? p.r_sf_bytes : p.a_sf_bytes),
+                          (tl.m0 << 20) | ((int64_t)tl.e << 8) | (sb.corr ? 2 : 0) | (int)rank)) {
                   mbar_expect_tx(&myfull[s], bytes);
                   bulk_load(st + OFF_SFA + u * SF_SUB, (sb.corr ? p.r_sf : p.a_sf) + oa, bytes,
                             &myfull[s]);
                 } else {
                   mbar_arrive(&myfull[s]);
                 }
-                if (QDBG(ow >= 0 && ow + bytes <= (sb.corr ? p.ws_sf_bytes : p.b_sf_bytes))) {
+                if (QDBGV(ow >= 0 && ow + bytes <= (sb.corr ? p.ws_sf_bytes : p.b_sf_bytes),
+                          (bbase << 20) | ((int64_t)tl.e << 8) | (sb.corr ? 2 : 0) | 4 | (int)rank)) {
                   mbar_expect_tx(&myfull[s], bytes);
                   bulk_load(st + OFF_SFB + u * SF_SUB, (sb.corr ? p.ws_sf : p.b_sf) + ow, bytes,
                             &myfull[s]);
@@ -1829,7 +1834,7 @@ int read_gemm_device_error() {
   return v;
 }
 
-int debug_line_gemm() { return take_debug_line(); }
+int debug_line_gemm(long long* value) { return take_debug_line(value); }
 
 }  // namespace quads
 

@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
   }
 }
 
-int debug_line_moe() { return take_debug_line(); }
+int debug_line_moe(long long* value) { return take_debug_line(value); }
 
 }  // namespace quads
 

@@ -99,20 +99,20 @@ __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restri
 // (codes == nullptr).
 constexpr int kQAhead = 8;   // rows loaded ahead per warp
 
+// The task loop of one warp (warp `wid` of `nwarps`), shared by the
+// quantizer kernel and the fused activation-side kernel.
 template <bool kScores, bool kQdq>
-__global__ void __launch_bounds__(256, 2) quantize_kernel(
+__device__ __forceinline__ void quantize_tasks(
     const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
     const int32_t* __restrict__ row_index, const int32_t* __restrict__ goff, int G,
-    const float* __restrict__ st, const uint32_t* __restrict__ amax_bits, float* __restrict__ st_out,
+    const float* __restrict__ st, const uint32_t* __restrict__ amax_bits,
     uint8_t* __restrict__ codes, int64_t ldc, uint8_t* __restrict__ scales, int layout,
-    int sf_words, float* __restrict__ partials, __nv_bfloat16* __restrict__ qdq, int64_t ldq) {
-  // tensor scales: given (st), or derived here from the groups' amax bits
-  // (then block 0 also stores them to st_out)
+    int sf_words, float* __restrict__ partials, __nv_bfloat16* __restrict__ qdq, int64_t ldq,
+    int64_t wid, int64_t nwarps) {
+  // tensor scales: given (st), or derived from the groups' amax bits
   auto scale_of = [&](int g) {
     return amax_bits ? tensor_scale_from_amax(__uint_as_float(__ldg(amax_bits + g))) : __ldg(st + g);
   };
-  if (amax_bits && blockIdx.x == 0)
-    for (int g = threadIdx.x; g < G; g += blockDim.x) st_out[g] = scale_of(g);
   const int lane = threadIdx.x & 31;
   int64_t end = goff ? (int64_t)goff[G] : rows;
   if (!QDBG(end >= 0 && end <= rows)) end = 0;
@@ -120,9 +120,7 @@ __global__ void __launch_bounds__(256, 2) quantize_kernel(
   const int64_t nchunks = (end + kScoreChunk - 1) / kScoreChunk;
   const int64_t ntasks = nchunks * nslab;
   const int ncols16 = cols >> 4;
-  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < ntasks;
-       task += nwarps) {
+  for (int64_t task = wid; task < ntasks; task += nwarps) {
     const int64_t chunk = task / nslab;
     const int col = (int)(task - chunk * nslab) * 256 + lane * 8;
     const bool active = col < cols;
@@ -215,6 +213,23 @@ __global__ void __launch_bounds__(256, 2) quantize_kernel(
   }
 }
 
+template <bool kScores, bool kQdq>
+__global__ void __launch_bounds__(256, 2) quantize_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
+    const int32_t* __restrict__ row_index, const int32_t* __restrict__ goff, int G,
+    const float* __restrict__ st, const uint32_t* __restrict__ amax_bits, float* __restrict__ st_out,
+    uint8_t* __restrict__ codes, int64_t ldc, uint8_t* __restrict__ scales, int layout,
+    int sf_words, float* __restrict__ partials, __nv_bfloat16* __restrict__ qdq, int64_t ldq) {
+  // tensor scales derived from the groups' amax bits are also stored by block 0
+  if (amax_bits && blockIdx.x == 0)
+    for (int g = threadIdx.x; g < G; g += blockDim.x)
+      st_out[g] = tensor_scale_from_amax(__uint_as_float(__ldg(amax_bits + g)));
+  quantize_tasks<kScores, kQdq>(x, rows, cols, ldx, row_index, goff, G, st, amax_bits, codes, ldc,
+                                scales, layout, sf_words, partials, qdq, ldq,
+                                (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5),
+                                (int64_t)gridDim.x * (blockDim.x >> 5));
+}
+
 // ---------------------------------------------------------------- select
 // Channel scores = the group's chunk partials added in ascending chunk order
 // starting from 0 (one float32 add per chunk).  Two launch shapes compute the
@@ -261,6 +276,91 @@ __global__ void __launch_bounds__(256) score_chain_kernel(const float* __restric
 }
 
 
+// Top-k of `cols` keys held PER per thread by a block of NT threads (key i of
+// thread t is channel t + i*NT): radix selection on the bit patterns (scores
+// are >= 0, so the unsigned order of the bits is the float order) finds the
+// k-th largest key T byte by byte; the channels with key > T and the
+// lowest-index channels with key == T are written to sel_out in ascending
+// order.  Shared scratch: hist[256], *s_prefix, *s_need, warp_sums[NT/32].
+template <int NT, int PER>
+__device__ __forceinline__ void block_topk(const uint32_t (&key)[PER], int cols, int k,
+                                           int32_t* sel_out, int* hist, uint32_t* s_prefix,
+                                           int* s_need, int* warp_sums) {
+  constexpr int NW = NT / 32;
+  if (threadIdx.x == 0) { *s_prefix = 0u; *s_need = k; }
+  uint32_t mask_hi = 0u;  // bits already fixed in *s_prefix
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += NT) hist[i] = 0;
+    __syncthreads();
+    const uint32_t prefix = *s_prefix;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int c = threadIdx.x + i * NT;
+      if (c < cols && (key[i] & mask_hi) == prefix) atomicAdd(&hist[(key[i] >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      // warp 0: lane l owns bins 255-8l .. 248-8l (descending); find the bin in
+      // which the running count from the top reaches `need`
+      const int lane = threadIdx.x;
+      int c8[8], lsum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) { c8[i] = hist[255 - 8 * lane - i]; lsum += c8[i]; }
+      int incl = lsum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      const int need = *s_need;
+      const int excl = incl - lsum;
+      const unsigned found = __ballot_sync(0xffffffffu, excl < need && incl >= need);
+      if (lane == __ffs(found) - 1) {
+        int nd = need - excl, i = 0;
+        for (; i < 7; ++i) {
+          if (c8[i] >= nd) break;
+          nd -= c8[i];
+        }
+        *s_need = nd;
+        *s_prefix = prefix | ((uint32_t)(255 - 8 * lane - i) << shift);
+      }
+    }
+    mask_hi |= 255u << shift;
+    __syncthreads();
+  }
+  const uint32_t T = *s_prefix;
+  const int need_eq = *s_need;  // how many channels with key == T are taken
+  // ordered pass over channels: selected = key > T, or key == T among the first need_eq
+  // equal keys in index order; chunks of NT channels, block-wide exclusive scans.
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int taken_eq = 0, written = 0;
+  for (int i = 0; i < PER && i * NT < cols; ++i) {
+    const int c = threadIdx.x + i * NT;
+    const bool eq = c < cols && key[i] == T;
+    const bool gt = c < cols && key[i] > T;
+    // rank among equal keys in this chunk
+    unsigned bal = __ballot_sync(0xffffffffu, eq);
+    int pre_eq = __popc(bal & ((1u << lane) - 1u));
+    if (lane == 0) warp_sums[w] = __popc(bal);
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int j = 0; j < NW; ++j) { if (j < w) before += warp_sums[j]; total += warp_sums[j]; }
+    const bool take = gt || (eq && taken_eq + before + pre_eq < need_eq);
+    __syncthreads();
+    bal = __ballot_sync(0xffffffffu, take);
+    const int pre_t = __popc(bal & ((1u << lane) - 1u));
+    if (lane == 0) warp_sums[w] = __popc(bal);
+    __syncthreads();
+    int before_t = 0, total_t = 0;
+    for (int j = 0; j < NW; ++j) { if (j < w) before_t += warp_sums[j]; total_t += warp_sums[j]; }
+    const int pos = written + before_t + pre_t;
+    if (take && pos < k) sel_out[pos] = c;
+    written += total_t;
+    taken_eq += total;
+    __syncthreads();
+  }
+}
+
 // Top-k per group by radix selection on the score bit patterns (scores are
 // >= 0, so the unsigned order of the bits is the float order): find the k-th
 // largest key T byte by byte, take every channel with key > T and the
@@ -277,7 +377,7 @@ __global__ void __launch_bounds__(1024) topk_kernel(float* __restrict__ scores, 
   __shared__ int hist[256];
   __shared__ uint32_t s_prefix;
   __shared__ int s_need;
-  __shared__ int warp_sums[32];
+  __shared__ int warp_sums[32];   // one per warp of the 1024-thread block
   const int g = blockIdx.y;
   float* sc = scores + (int64_t)g * cols;
   constexpr int PER = 8;  // cols <= 8192 = 1024 threads x 8
@@ -310,78 +410,7 @@ __global__ void __launch_bounds__(1024) topk_kernel(float* __restrict__ scores, 
       key[i] = c < cols ? __float_as_uint(sc[c]) : 0u;
     }
   }
-  if (threadIdx.x == 0) { s_prefix = 0u; s_need = k; }
-  uint32_t mask_hi = 0u;  // bits already fixed in s_prefix
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    const uint32_t prefix = s_prefix;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int c = threadIdx.x + i * blockDim.x;
-      if (c < cols && (key[i] & mask_hi) == prefix) atomicAdd(&hist[(key[i] >> shift) & 255u], 1);
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      // warp 0: lane l owns bins 255-8l .. 248-8l (descending); find the bin in
-      // which the running count from the top reaches `need`
-      const int lane = threadIdx.x;
-      int c8[8], lsum = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) { c8[i] = hist[255 - 8 * lane - i]; lsum += c8[i]; }
-      int incl = lsum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
-      }
-      const int need = s_need;
-      const int excl = incl - lsum;
-      const unsigned found = __ballot_sync(0xffffffffu, excl < need && incl >= need);
-      if (lane == __ffs(found) - 1) {
-        int nd = need - excl, i = 0;
-        for (; i < 7; ++i) {
-          if (c8[i] >= nd) break;
-          nd -= c8[i];
-        }
-        s_need = nd;
-        s_prefix = prefix | ((uint32_t)(255 - 8 * lane - i) << shift);
-      }
-    }
-    mask_hi |= 255u << shift;
-    __syncthreads();
-  }
-  const uint32_t T = s_prefix;
-  const int need_eq = s_need;  // how many channels with key == T are taken
-  // ordered pass over channels: selected = key > T, or key == T among the first need_eq
-  // equal keys in index order; chunks of 1024 channels, block-wide exclusive scans.
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  int taken_eq = 0, written = 0;
-  for (int i = 0; i < PER && i * (int)blockDim.x < cols; ++i) {
-    const int c = threadIdx.x + i * blockDim.x;
-    const bool eq = c < cols && key[i] == T;
-    const bool gt = c < cols && key[i] > T;
-    // rank among equal keys in this chunk
-    unsigned bal = __ballot_sync(0xffffffffu, eq);
-    int pre_eq = __popc(bal & ((1u << lane) - 1u));
-    if (lane == 0) warp_sums[w] = __popc(bal);
-    __syncthreads();
-    int before = 0, total = 0;
-    for (int j = 0; j < 32; ++j) { if (j < w) before += warp_sums[j]; total += warp_sums[j]; }
-    const bool take = gt || (eq && taken_eq + before + pre_eq < need_eq);
-    __syncthreads();
-    bal = __ballot_sync(0xffffffffu, take);
-    const int pre_t = __popc(bal & ((1u << lane) - 1u));
-    if (lane == 0) warp_sums[w] = __popc(bal);
-    __syncthreads();
-    int before_t = 0, total_t = 0;
-    for (int j = 0; j < 32; ++j) { if (j < w) before_t += warp_sums[j]; total_t += warp_sums[j]; }
-    const int pos = written + before_t + pre_t;
-    if (take && pos < k) sel[(int64_t)g * k + pos] = c;
-    written += total_t;
-    taken_eq += total;
-    __syncthreads();
-  }
+  block_topk<1024, PER>(key, cols, k, sel + (int64_t)g * k, hist, &s_prefix, &s_need, warp_sums);
 }
 
 // ---------------------------------------------------------------- residual slice
@@ -1034,7 +1063,7 @@ quads_status_t select_check_args(const void* x, int64_t rows, int64_t cols, int6
   *need = quads_workspace_size(QUADS_OP_SELECT, rows, cols, 0, k, group_offsets ? num_groups : 1);
   return QUADS_OK;
 }
-int debug_line_quantize() { return take_debug_line(); }
+int debug_line_quantize(long long* value) { return take_debug_line(value); }
 
 }  // namespace quads
 

@@ -51,6 +51,10 @@ class CompensatedLinear:
         # next to the residual slice (forked and joined by events)
         self.side = torch.cuda.Stream(device=dev)
         self.ev_sel, self.ev_w = torch.cuda.Event(), torch.cuda.Event()
+        # the weight preparation above ran on the current stream; forward() may
+        # run on other streams that do not wait for it (and the allocator may
+        # already hand its freed scratch to other buffers), so finish it here
+        torch.cuda.current_stream(dev).synchronize()
 
     def forward(self, x: torch.Tensor, stream=None) -> torch.Tensor:
         b = self.bufs
@@ -132,6 +136,11 @@ class MoEExpertLayer:
         self.wside = torch.cuda.Stream(device=dev)
         (self.ev_fork, self.ev_xq, self.ev_a1, self.ev_sel1, self.ev_w1, self.ev_sel2,
          self.ev_w2) = (torch.cuda.Event() for _ in range(7))
+        # the weight preparation and buffer fills above ran on the current
+        # stream; forward() runs on streams that do not wait for it (and the
+        # allocator may already have handed that work's freed scratch to the
+        # routing buffers), so finish it here
+        torch.cuda.current_stream(dev).synchronize()
 
     def forward(self, x: torch.Tensor, logits: torch.Tensor, stream=None) -> dict:
         b, ws, T = self.b, self.ws, x.shape[0]

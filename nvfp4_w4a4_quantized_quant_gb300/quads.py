@@ -125,12 +125,16 @@ def workspace_size(op, rows=0, cols=0, n=0, k=0, groups=1) -> int:
     return int(load().quads_workspace_size(op, rows, cols, n, k, groups))
 
 
-def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]):
+def _workspace(nbytes: int, device, ws: Optional[torch.Tensor], stream=None):
+    """The caller's workspace, or a temporary one allocated on the stream the
+    kernels run on (so that the caching allocator does not hand it to another
+    stream's allocation while those kernels may still use it)."""
     if ws is not None:
         if ws.numel() < nbytes:
             raise QuadsError(f"workspace of {ws.numel()} bytes < {nbytes}")
         return ws
-    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+    with torch.cuda.stream(_torch_stream(stream)):
+        return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
 
 
 def sf_tc_bytes(rows: int, cols: int) -> int:
@@ -189,7 +193,7 @@ def quantize_nvfp4(x: torch.Tensor, *, group_offsets=None, num_groups: int = 1,
                 if scores else None)
     else:
         codes, scales, ts, part = out
-    ws = _workspace(workspace_size(OP_QUANTIZE, rows, cols, 0, 0, G), dev, workspace)
+    ws = _workspace(workspace_size(OP_QUANTIZE, rows, cols, 0, 0, G), dev, workspace, stream)
     _check(lib.quads_quantize_nvfp4(_ptr(x), rows, cols, x.stride(0), _ptr(row_index),
                                     _ptr(group_offsets), G, _ptr(tensor_scale_in),
                                     _ptr(tensor_amax_in), _ptr(codes),
@@ -217,7 +221,7 @@ def qdq_nvfp4(x: torch.Tensor, *, group_offsets=None, num_groups: int = 1,
     ts = torch.empty(G, dtype=torch.float32, device=dev)
     ws = None
     if tensor_scale_in is None:
-        ws = _workspace(workspace_size(OP_QUANTIZE, rows, cols, 0, 0, G), dev, workspace)
+        ws = _workspace(workspace_size(OP_QUANTIZE, rows, cols, 0, 0, G), dev, workspace, stream)
     _check(lib.quads_qdq_nvfp4(
         _ptr(x), rows, cols, x.stride(0), _ptr(group_offsets), G, _ptr(tensor_scale_in), _ptr(y),
         y.stride(0), _ptr(codes), cols // 2, _ptr(scales), scale_layout, _ptr(ts), _ptr(ws),
@@ -255,7 +259,7 @@ def select_residual_channels(x: torch.Tensor, q: QTensor, partials: torch.Tensor
     else:
         sel, rc, rs, rts = out
     sc = torch.empty((G, cols), dtype=torch.float32, device=dev) if want_scores else None
-    ws = _workspace(workspace_size(OP_SELECT, rows, cols, 0, k, G), dev, workspace)
+    ws = _workspace(workspace_size(OP_SELECT, rows, cols, 0, k, G), dev, workspace, stream)
     _check(lib.quads_select_residual_channels(
         _ptr(x), rows, cols, x.stride(0), _ptr(group_offsets), G, _ptr(q.scales), q.layout,
         _ptr(q.tensor_scale), _ptr(partials), k, _ptr(sel), _ptr(sc), _ptr(rc), _ptr(rs),
@@ -291,7 +295,7 @@ def select_residual_channels_noalloc(x: torch.Tensor, q: QTensor, partials: torc
     return sel, sc, QTensor(rc, rs, rts, rows, kp, r_scale_layout)
 
 
-def _wsel_args(r, w, w_sel, size_args, dev, workspace):
+def _wsel_args(r, w, w_sel, size_args, dev, workspace, stream=None):
     """Workspace and Q(W_sel) pointers of a compensated GEMM call."""
     if r is None:
         return None, None, None
@@ -299,7 +303,7 @@ def _wsel_args(r, w, w_sel, size_args, dev, workspace):
         return None, _ptr(w_sel.codes), _ptr(w_sel.scales)
     if w.codes_t is None:
         raise QuadsError("compensation needs the weight's column-major copy (weight_columns)")
-    return _workspace(workspace_size(*size_args), dev, workspace), None, None
+    return _workspace(workspace_size(*size_args), dev, workspace, stream), None, None
 
 
 def w4a4_gemm_comp(a: QTensor, w: QTensor, r: Optional[QTensor] = None, sel=None, k: int = 0, *,
@@ -311,7 +315,7 @@ def w4a4_gemm_comp(a: QTensor, w: QTensor, r: Optional[QTensor] = None, sel=None
     M, K, N = a.rows, a.cols, w.rows
     y = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=a.codes.device)
     yd = OUT_F32 if y.dtype == torch.float32 else OUT_BF16
-    ws, wsc, wss = _wsel_args(r, w, w_sel, (OP_GEMM, 0, K, N, k, 1), y.device, workspace)
+    ws, wsc, wss = _wsel_args(r, w, w_sel, (OP_GEMM, 0, K, N, k, 1), y.device, workspace, stream)
     _check(lib.quads_w4a4_gemm_comp(
         M, N, K, _ptr(a.codes), _ptr(a.scales), _ptr(a.tensor_scale), _ptr(w.codes),
         _ptr(w.scales), _ptr(w.tensor_scale), _ptr(w.codes_t), _ptr(w.scales_t), wsc, wss,
@@ -336,7 +340,7 @@ def moe_grouped_gemm(plan: dict, a: QTensor, w: QTensor, num_experts: int, n: in
     y = out if out is not None else torch.empty((cap, ycols), dtype=out_dtype, device=a.codes.device)
     yd = OUT_F32 if y.dtype == torch.float32 else OUT_BF16
     ws, wsc, wss = _wsel_args(r, w, w_sel, (OP_MOE_GEMM, 0, K, n, k, num_experts), y.device,
-                              workspace)
+                              workspace, stream)
     _check(lib.quads_moe_grouped_gemm(
         num_experts, cap, n, K, _ptr(plan["offsets"]), _ptr(plan["counts"]), _ptr(a.codes),
         _ptr(a.scales), _ptr(a.tensor_scale), int(a_scale_per_expert), _ptr(w.codes),
@@ -499,7 +503,7 @@ def moe_route(logits: torch.Tensor, topk: int, *, rows_capacity: Optional[int] =
                    offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
                    row_token=torch.empty(cap, dtype=torch.int32, device=dev),
                    token_row=torch.empty((T, topk), dtype=torch.int32, device=dev))
-    ws = _workspace(workspace_size(OP_MOE_ROUTE, T, E, 0, topk, 1), dev, workspace)
+    ws = _workspace(workspace_size(OP_MOE_ROUTE, T, E, 0, topk, 1), dev, workspace, stream)
     _check(lib.quads_moe_route(_ptr(logits), T, E, topk, _ptr(out["idx"]), _ptr(out["gates"]),
                                _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["row_token"]),
                                _ptr(out["token_row"]), cap, _ptr(ws), ws.numel(),
