@@ -267,10 +267,12 @@ def secondary(torch, Q, steps, flush, stream):
     xm = torch.from_numpy(dm["x"].view(np.int16)).view(torch.bfloat16).cuda()
     lm = torch.from_numpy(dm["logits"]).cuda()
     moe = {}
-    for comp in (False, True):
-        lay = MoEExpertLayer(w1, w2, wm["topk"], wm["k1"], wm["k2"], wm["tokens"], compensate=comp)
+    for name, comp, fused in (("plain", False, False), ("comp", True, False),
+                              ("comp_fused_activation_side", True, True)):
+        lay = MoEExpertLayer(w1, w2, wm["topk"], wm["k1"], wm["k2"], wm["tokens"], compensate=comp,
+                             fused_activation_side=fused)
         ms = graph_ms(lambda: lay.forward(xm, lm, stream=stream))
-        moe["comp" if comp else "plain"] = {"ms": round(ms, 4)}
+        moe[name] = {"ms": round(ms, 4)}
         del lay
     rows = wm["tokens"] * wm["topk"]
     fl_plain = 2.0 * rows * (2 * F) * H + 2.0 * rows * H * F
@@ -456,13 +458,26 @@ def run_gpu(args):
         g1_ms = timed(torch, g1_graph.replay, args.steps, flush, stream) / args.steps
 
         # quantizer alone on the layer input (scores on): algorithmic bytes
-        xq_out = (layer.b["xc"], layer.b["xs"], layer.b["xts"], layer.b["xpart"])
+        xpart = torch.empty(((x.shape[0] + 31) // 32, x.shape[1]), dtype=torch.float32, device="cuda")
+        xq_out = (layer.b["xc"], layer.b["xs"], layer.b["xts"], xpart)
         def qx():
             Q.quantize_nvfp4(x, scores=True, workspace=layer.ws["q1"], out=xq_out, stream=stream)
         q_graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(q_graph, stream=stream):
             qx()
         q_ms = timed(torch, q_graph.replay, args.steps, flush, stream) / args.steps
+
+        # GEMM1's whole activation side (quantize + select) in one cooperative launch
+        b = layer.b
+        qs_out = (b["xc"], b["xs"], b["xts"], b["sel1"], b["r1c"], b["r1s"], b["r1ts"])
+        qs_ws = torch.empty(Q.workspace_size(Q.OP_QUANTIZE_SELECT, x.shape[0], x.shape[1], 0, layer.k1),
+                            dtype=torch.uint8, device="cuda")
+        def qs():
+            Q.quantize_select_nvfp4(x, layer.k1, workspace=qs_ws, out=qs_out, stream=stream)
+        qs_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(qs_graph, stream=stream):
+            qs()
+        qs_ms = timed(torch, qs_graph.replay, args.steps, flush, stream) / args.steps
 
         # end to end: every step copies its inputs from pinned host memory and
         # its output back; the copies of step i+1 (in) and i (out) run on their
@@ -531,6 +546,8 @@ def run_gpu(args):
     e2e_val = world * fl / (e_ms * 1e-3) / 1e12
     T, H, E = WORKLOAD["tokens"], WORKLOAD["hidden"], WORKLOAD["experts"]
     q_bytes = T * H * 2 + T * H * 0.5 + T * H / 16 + (T // 32) * H * 4
+    kp1 = 64 if WORKLOAD["k1"] <= 64 else 128
+    qs_bytes = T * H * 2 + T * H * 0.5625 + T * kp1 * 0.5625     # x once, Q(X), Q(R_sel)
     # the timed region is a series of sub-millisecond graph replays, not a
     # seconds-long loop: the burst peak applies
     fp4_peak = pk["bf16"] * FP4_OVER_BF16
@@ -568,7 +585,12 @@ def run_gpu(args):
         },
         "secondary": sec,
         "quantizer": {"gbs": round(q_bytes / (q_ms * 1e-3) / 1e9, 1), "frac_hbm": round(q_bytes / (q_ms * 1e-3) / 1e9 / pk["hbm"], 4),
-                      "ms": round(q_ms, 4), "shape": [T, H], "algorithmic_bytes": int(q_bytes)},
+                      "ms": round(q_ms, 4), "shape": [T, H], "algorithmic_bytes": int(q_bytes),
+                      "note": "amax pass + quantize pass with score partials (two launches)",
+                      "fused_quantize_select_ms": round(qs_ms, 4),
+                      "fused_quantize_select_gbs": round(qs_bytes / (qs_ms * 1e-3) / 1e9, 1),
+                      "fused_note": "amax, quantization, scores, top-k, R_sel and its quantization in one "
+                                    "cooperative launch (GEMM1's activation side; x read from HBM once)"},
         "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(x_host.numel() * 2 + l_host.numel() * 4),
                 "d2h_bytes_per_step": int(out_host[0].numel() * 2), "ms_per_step": round(e_ms, 4),

@@ -85,7 +85,8 @@ enum {
   QUADS_OP_SELECT = 1,
   QUADS_OP_GEMM = 2,
   QUADS_OP_MOE_GEMM = 3,
-  QUADS_OP_MOE_ROUTE = 4
+  QUADS_OP_MOE_ROUTE = 4,
+  QUADS_OP_QUANTIZE_SELECT = 5
 };
 
 /* Rows of the score-partial array are chunks of this many consecutive rows. */
@@ -125,6 +126,18 @@ quads_status_t quads_device_status(void* stream, int32_t* device_code);
  */
 void quads_test_gemm_wait_timeout(int32_t enable);
 
+/*
+ * Profiling hook (no counterpart on the pages): the next GEMM launch records
+ * the stage timeline of its first CTA -- %globaltimer nanoseconds -- into
+ * device_buffer, 7 events x 64 entries of uint64 (event e, iteration i at
+ * [e*64 + i]): 0 producer got a free stage, 1 scale warp saw the stage's
+ * data, 2 scale warp committed its copies, 3 MMA issuer saw the scales,
+ * 4 MMA issuer committed the stage, 5 epilogue saw a full accumulator (per
+ * tile), 6 epilogue finished a tile.  Unwritten entries keep their contents.
+ * The hook clears itself at that launch.
+ */
+void quads_test_gemm_timeline(uint64_t* device_buffer);
+
 /* Bytes of scratch the call `op` needs for the given shape (0 if none).
  *   QUADS_OP_QUANTIZE: num_groups floats of tensor amax.
  *   QUADS_OP_SELECT:   rows*k floats (the residual slice) + num_groups floats
@@ -133,6 +146,9 @@ void quads_test_gemm_wait_timeout(int32_t enable);
  *                      n*kpad/2 code bytes + n*kpad/16 scale bytes (+ alignment).
  *   QUADS_OP_MOE_GEMM: the same for num_groups experts.
  *   QUADS_OP_MOE_ROUTE: two int32 per (32-token block, expert): rows = tokens, cols = experts.
+ *   QUADS_OP_QUANTIZE_SELECT: 256 bytes of control words + the score partials
+ *                      (ceil(rows/32)*cols floats) + cols floats of scores +
+ *                      rows*k floats (the residual slice), each 256-byte aligned.
  * `cols` is the channel count (K) and `n` the output width (N, unused for the
  * activation-side ops).  kpad = k rounded up to 64 (k <= 256) or to 256. */
 size_t quads_workspace_size(int32_t op, int64_t rows, int64_t cols, int64_t n, int32_t k,
@@ -278,6 +294,31 @@ quads_status_t quads_select_residual_channels_noalloc(
     int32_t num_groups, const uint8_t* scales, int32_t scale_layout, const float* tensor_scale,
     const float* score_partials, int32_t k, int32_t* sel, float* scores_out, uint8_t* r_codes,
     uint8_t* r_scales, int32_t r_scale_layout, float* r_tensor_scale, void* stream);
+
+/*
+ * quads_quantize_select_nvfp4 -- quads_quantize_nvfp4 (one group, tensor
+ * scale from the amax, score partials) followed by
+ * quads_select_residual_channels, in one cooperative launch whose five
+ * phases (tensor amax; quantization with the residual-energy partials;
+ * channel scores; top-k selection and the residual slice R[:, sel]; the
+ * second quantization of that slice) are separated by grid-wide barriers, so
+ * x is read from HBM once and the second pass over it is served by L2 when x
+ * fits there.  [QUADS] 2.2 B "Mechanism" and "Implementation" (the
+ * high-residual channels chosen online; the correction path fused).
+ * Outputs are those of the two calls, bit for bit: codes, scales
+ * (scale_layout), tensor_scale_out[1], sel[k] ascending, scores_out (nullable,
+ * [cols]), R_sel codes [rows, kpad/2], scales (r_scale_layout), r_tensor_scale[1].
+ * cols % 16 == 0 and cols <= 8192 (cols % 64 for TCGEN05 scales); 16 <= k <=
+ * min(cols, 1024), k % 16 == 0.  All blocks must be resident at once (one per
+ * SM): the launch is cooperative, and fails with QUADS_ERR_CUDA when the
+ * device cannot hold the grid.  A grid barrier that does not complete within
+ * 2 s latches QUADS_ERR_DEVICE_TIMEOUT (quads_device_status).
+ */
+quads_status_t quads_quantize_select_nvfp4(
+    const void* x, int64_t rows, int64_t cols, int64_t ldx, int32_t k, uint8_t* codes,
+    int64_t ld_codes, uint8_t* scales, int32_t scale_layout, float* tensor_scale_out, int32_t* sel,
+    float* scores_out, uint8_t* r_codes, uint8_t* r_scales, int32_t r_scale_layout,
+    float* r_tensor_scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * quads_w4a4_gemm_comp -- Y = s_a s_w Q(A) Q(W)^T + s_r s_w Q(R_sel) Q(W_sel)^T

@@ -93,6 +93,12 @@ extern "C" size_t quads_workspace_size(int32_t op, int64_t rows, int64_t cols, i
     case QUADS_OP_SELECT:  // residual slice, per-group amax, per-group channel scores
       return (((size_t)rows * (size_t)k * 4 + 255) & ~(size_t)255) + ((G * 4 + 255) & ~(size_t)255) +
              G * (size_t)cols * 4;
+    case QUADS_OP_QUANTIZE_SELECT: {  // control words, partials, scores, residual slice
+      const size_t r = rows > 0 ? (size_t)rows : 0, c = cols > 0 ? (size_t)cols : 0;
+      const size_t kk = k > 0 ? (size_t)k : 0;
+      auto al = [](size_t b) { return (b + 255) & ~(size_t)255; };
+      return 256 + al((r + 31) / 32 * c * 4) + al(c * 4) + al(r * kk * 4);
+    }
     case QUADS_OP_MOE_ROUTE:  // per-32-token-block expert counts and prefixes: rows = tokens, cols = experts
       return (size_t)((rows > 0 ? rows : 0) + 31) / 32 * (size_t)(cols > 0 ? cols : 0) * 8 + 16;
     case QUADS_OP_GEMM:

@@ -38,8 +38,11 @@
 // same kernel with kind::mxf4 MMAs and one scale atom per two K steps.
 // TMEM columns: acc1 double-buffered (0-127, 128-255), acc2 (256-383),
 // scale-factor ring (384-511, 2 buffers x 64 columns).
-// Every mbarrier wait is bounded; on timeout the kernel latches an error word,
-// stops all roles, and still releases its TMEM.
+// Every mbarrier wait is bounded (2 s); on a timeout the kernel latches an
+// error word and every role stops.  Each producer warp then waits (bounded)
+// for its own copies in flight -- its per-stage barriers count its copies only,
+// so they complete whatever the other roles did -- the MMA and scale warps
+// commit and wait for their tensor-core work, and TMEM is released.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -54,12 +57,23 @@
 namespace quads {
 namespace gemm {
 
+// Stage geometry (sub-tiles per stage, ring stages, TMEM scale buffers); the
+// build may override it to compare variants.
+#ifndef QUADS_GEMM_KSUBS
+#define QUADS_GEMM_KSUBS 2
+#endif
+#ifndef QUADS_GEMM_STAGES
+#define QUADS_GEMM_STAGES 3
+#endif
+#ifndef QUADS_GEMM_SF_BUFS
+#define QUADS_GEMM_SF_BUFS 2
+#endif
 constexpr int BM = 128, BN = 128;
 constexpr int KSUB = 128;                     // bytes per row of one 128B-swizzled sub-tile (256 FP4)
-constexpr int KSUBS = 2;                      // sub-tiles per stage: K tile = 512 FP4
+constexpr int KSUBS = QUADS_GEMM_KSUBS;       // sub-tiles per stage: K tile = 256 * KSUBS FP4
 constexpr int KSTEPS = 4 * KSUBS;             // K=64 MMA steps per stage
 constexpr int KTILE = 256 * KSUBS;            // FP4 elements per stage
-constexpr int STAGES = 3;
+constexpr int STAGES = QUADS_GEMM_STAGES;
 constexpr int A_SUB = BM * KSUB;              // 16 KB
 constexpr int B_SUB = BN * KSUB;              // 16 KB
 constexpr int A_TILE = A_SUB * KSUBS;
@@ -70,8 +84,9 @@ constexpr int BOX_ROWS = 64;                  // rows per TMA box: half a 128-ro
 constexpr int BOX_BYTES = BOX_ROWS * KSUB;    // 8 KB
 constexpr int BOXES = 2 * KSUBS * 2;          // per stage: (A, B) x sub-tiles x halves
 constexpr int COPIES = BOXES + 2;             // + the SFA and SFB atom runs (bulk copies)
-constexpr int SF_BUFS = 2;                    // TMEM scale buffers
-constexpr int SF_BUF_COLS = 2 * 4 * KSTEPS;   // SFA 32 + SFB 32 columns
+constexpr int SF_BUFS = QUADS_GEMM_SF_BUFS;   // TMEM scale buffers
+constexpr int SF_BUF_COLS = 2 * 4 * KSTEPS;   // SFA and SFB: four columns per K step each
+static_assert(SF_BUFS * SF_BUF_COLS <= 128, "scale buffers fit the 128 TMEM columns left");
 constexpr int PRODUCERS = 3;
 constexpr int NUM_THREADS = 512;  // 16 warps: 3 producers, MMA, 4 scale staging, 8 epilogue
 constexpr int EPI_THREADS = 256;
@@ -84,6 +99,9 @@ constexpr int MAX_GROUPS = 256;                 // experts cached in shared memo
 constexpr int META_BYTES = 1024 + 4 * (MAX_GROUPS + 1) + 4 * 4 * MAX_GROUPS;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + META_BYTES + 1024 /*align*/;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per wait
+// the stage's copies dealt to the producer warps: warp w issues [first, first + count)
+__host__ __device__ constexpr int copies_first(int w) { return w * COPIES / PRODUCERS; }
+__host__ __device__ constexpr int copies_of(int w) { return copies_first(w + 1) - copies_first(w); }
 
 enum { OUT_F32 = 0, OUT_BF16 = 1, OUT_SWIGLU = 2 };
 
@@ -110,7 +128,11 @@ struct Params {
   int* err;
   // extents for the bounds-checked build: scale buffer bytes and output rows
   int64_t a_sf_bytes, b_sf_bytes, r_sf_bytes, ws_sf_bytes, y_rows;
+  unsigned long long timeout_ns;
+  int skip_mma;                 // test hook: the MMA warp issues nothing (waits then run out)
+  unsigned long long* trace;    // nullable: stage timeline of CTA 0 (kTraceSlots per event)
 };
+constexpr int kTraceSlots = 64;
 
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -143,24 +165,10 @@ __device__ __forceinline__ unsigned long long global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-
-// Bounded wait: false when the wait gave up (error latched) or another role aborted.
-__device__ __forceinline__ bool wait_bar(uint64_t* b, uint32_t parity, volatile int* abort_flag,
-                                         int* err) {
-  if (mbar_try_wait(b, parity)) return true;
-  const unsigned long long t0 = global_ns();
-  uint32_t spins = 0;
-  while (true) {
-    if (mbar_try_wait(b, parity)) return true;
-    if ((++spins & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (global_ns() - t0 > kTimeoutNs) {
-        *abort_flag = 1;
-        atomicExch(err, QUADS_ERR_DEVICE_TIMEOUT);
-        return false;
-      }
-    }
-  }
+// Stage timeline (CTA 0 only, first kTraceSlots iterations of each event).
+__device__ __forceinline__ void trace_mark(unsigned long long* trace, int event, uint32_t i) {
+  if (trace && blockIdx.x == 0 && i < (uint32_t)kTraceSlots && (threadIdx.x & 31) == 0)
+    trace[event * kTraceSlots + i] = global_ns();
 }
 
 // One lane of the (fully active) warp returns true.
@@ -172,37 +180,6 @@ __device__ __forceinline__ bool elect_one() {
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(pred));
   return pred != 0;
-}
-
-// Bounded wait polled by every lane of a converged warp; the warp leaves together.
-__device__ __forceinline__ bool conv_wait_bar(uint64_t* b, uint32_t parity,
-                                              volatile int* abort_flag, int* err) {
-  if (__all_sync(0xffffffffu, mbar_try_wait(b, parity))) return true;
-  const unsigned long long t0 = global_ns();
-  uint32_t spins = 0;
-  while (true) {
-    if (__all_sync(0xffffffffu, mbar_try_wait(b, parity))) return true;
-    if ((++spins & 255u) == 0) {
-      int give_up = *abort_flag ? 1 : 0;
-      if (!give_up && global_ns() - t0 > kTimeoutNs) give_up = 2;
-      give_up = __shfl_sync(0xffffffffu, give_up, 0);
-      if (give_up) {
-        if (give_up == 2 && (threadIdx.x & 31) == 0) {
-          *abort_flag = 1;
-          atomicExch(err, QUADS_ERR_DEVICE_TIMEOUT);
-        }
-        return false;
-      }
-    }
-  }
-}
-
-// Bounded wait for a whole warp: lane 0 polls, the warp follows its verdict.
-__device__ __forceinline__ bool warp_wait_bar(uint64_t* b, uint32_t parity,
-                                              volatile int* abort_flag, int* err) {
-  int ok = 0;
-  if ((threadIdx.x & 31) == 0) ok = wait_bar(b, parity, abort_flag, err) ? 1 : 0;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
@@ -323,6 +300,111 @@ __device__ __forceinline__ void tc_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- bounded waits
+constexpr unsigned long long kDrainNs = 50000000ull;   // bound on waits for work in flight after an abort
+
+struct Sync {
+  volatile int* abort_flag;
+  int* err;
+  unsigned long long tmo;
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ bool try_wait_cluster(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait by one thread; `cluster` waits with cluster-scope acquire (for
+// barriers another CTA arrives on).  `drain`: ignore the abort flag (used to
+// let work in flight finish after an abort), still bounded by the timeout.
+__device__ __forceinline__ bool wait1(uint64_t* b, uint32_t parity, const Sync& s,
+                                      bool cluster = false, bool drain = false) {
+  auto probe = [&]() { return cluster ? try_wait_cluster(b, parity) : mbar_try_wait(b, parity); };
+  if (probe()) return true;
+  const unsigned long long t0 = global_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (probe()) return true;
+    if ((++spins & 255u) == 0) {
+      if (!drain && *s.abort_flag) return false;
+      if (global_ns() - t0 > s.tmo) {
+        if (!drain) {
+          *s.abort_flag = 1;
+          atomicExch(s.err, QUADS_ERR_DEVICE_TIMEOUT);
+        }
+        return false;
+      }
+    }
+  }
+}
+// Bounded wait for a whole warp: lane 0 polls, the warp follows its verdict.
+__device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, const Sync& s,
+                                          bool cluster = false) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait1(b, parity, s, cluster) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+// Bounded wait polled by every lane of a converged warp (the MMA warp stays
+// converged for its elect-predicated tcgen05 instructions).
+__device__ __forceinline__ bool conv_wait(uint64_t* b, uint32_t parity, const Sync& s,
+                                          bool cluster = false) {
+  auto probe = [&]() { return cluster ? try_wait_cluster(b, parity) : mbar_try_wait(b, parity); };
+  if (__all_sync(0xffffffffu, probe())) return true;
+  const unsigned long long t0 = global_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (__all_sync(0xffffffffu, probe())) return true;
+    if ((++spins & 255u) == 0) {
+      int give_up = *s.abort_flag ? 1 : 0;
+      if (!give_up && global_ns() - t0 > s.tmo) give_up = 2;
+      give_up = __shfl_sync(0xffffffffu, give_up, 0);
+      if (give_up) {
+        if (give_up == 2 && (threadIdx.x & 31) == 0) {
+          *s.abort_flag = 1;
+          atomicExch(s.err, QUADS_ERR_DEVICE_TIMEOUT);
+        }
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- tile schedule
 struct Tile {
   int e;
@@ -380,12 +462,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES);
-  uint64_t* full = bars;                 // [STAGES]
-  uint64_t* empty = bars + STAGES;       // [STAGES]
-  uint64_t* sf_ready = bars + 2 * STAGES; // [SF_BUFS]
-  uint64_t* acc_full = sf_ready + SF_BUFS; // [2]
-  uint64_t* acc_empty = acc_full + 2;    // [2]
-  uint32_t* tmem_holder = (uint32_t*)(acc_empty + 2);
+  uint64_t* fullw = bars;                          // [PRODUCERS][STAGES]: each producer's copies
+  uint64_t* empty = fullw + PRODUCERS * STAGES;    // [STAGES]
+  uint64_t* sf_ready = empty + STAGES;             // [SF_BUFS]
+  uint64_t* acc_full = sf_ready + SF_BUFS;         // [2]
+  uint64_t* acc_empty = acc_full + 2;              // [2]
+  uint64_t* drain_mma = acc_empty + 2;
+  uint64_t* drain_sf = drain_mma + 1;
+  uint32_t* tmem_holder = (uint32_t*)(drain_sf + 1);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
   Meta meta;
   meta.off = (int32_t*)(smem + STAGES * STAGE_BYTES + 1024);
@@ -407,9 +491,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0 && p.row_off) meta.off[p.E] = p.row_off[p.E];
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) { mbar_init(&full[i], COPIES); mbar_init(&empty[i], 1); }
+    for (int w = 0; w < PRODUCERS; ++w)
+      for (int i = 0; i < STAGES; ++i) mbar_init(&fullw[w * STAGES + i], copies_of(w));
+    for (int i = 0; i < STAGES; ++i) mbar_init(&empty[i], 1);
     for (int i = 0; i < SF_BUFS; ++i) mbar_init(&sf_ready[i], SF_WARPS);
     for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], EPI_THREADS); }
+    mbar_init(drain_mma, 1);
+    mbar_init(drain_sf, SF_WARPS);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -424,6 +512,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  const Sync sy{abort_flag, p.err, p.timeout_ns};
+  const Sync dr{abort_flag, p.err, kDrainNs};
 
   const int64_t ntiles = total_tiles(p, meta);
   const int KT = (p.K + KTILE - 1) / KTILE;
@@ -443,10 +533,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // bytes, or without any when the stage's K range ends before its
     // sub-tile).  The whole warp runs the loop (so addresses and coordinates
     // stay warp-uniform); one elected lane issues.
-    const int b_lo = warp == 0 ? 0 : (warp == 1 ? 3 : 6);
-    const int b_hi = warp == 0 ? 3 : (warp == 1 ? 6 : COPIES);
-    uint32_t it = 0, last = 0;
-    bool ok = true, any = false;
+    const int b_lo = copies_first(warp);
+    const int b_hi = copies_first(warp + 1);
+    uint64_t* full = fullw + warp * STAGES;   // this warp's own barriers
+    uint32_t it = 0;
+    bool ok = true;
     for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       const Tile tl = decode_tile(p, meta, t);
       const int64_t brow = (int64_t)tl.e * p.N + tl.n0;
@@ -463,7 +554,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const CUtensorMap* mb = corr ? &tmW : &tmB;
         const uint8_t* sfa = corr ? p.r_sf + (tl.m0 / BM) * r_sf_rb : p.a_sf + (tl.m0 / BM) * a_sf_rb;
         const uint8_t* sfb = corr ? p.ws_sf + (brow / BN) * r_sf_rb : p.b_sf + (brow / BN) * a_sf_rb;
-        if (!warp_wait_bar(&empty[s], ph ^ 1, abort_flag, p.err)) { ok = false; break; }
+        if (!warp_wait(&empty[s], ph ^ 1, sy)) { ok = false; break; }
+        if (warp == 0) trace_mark(p.trace, 0, it);
         if (elect_one()) {
           for (int b = b_lo; b < b_hi; ++b) {
             if (b >= BOXES) {
@@ -499,30 +591,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         __syncwarp();
-        last = it;
-        any = true;
       }
     }
-    if (!ok && any && lane == 0) {
-      // let copies this warp issued land before the CTA can exit
-      wait_bar(&full[last % STAGES], (last / STAGES) & 1, abort_flag, p.err);
+    if (!ok && lane == 0) {
+      // every copy this warp issued (at most the last STAGES iterations can
+      // still be in flight) lands before the CTA can exit: the barriers count
+      // this warp's copies only, so they complete whatever the others did
+      const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
+      for (uint32_t j = first; j < it; ++j) wait1(&full[j % STAGES], (j / STAGES) & 1, dr, false, true);
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc = idesc_nvf4(BM, BN);
     uint32_t s = 0, sb = 0, sph = 0;
-    uint32_t j = 0;
-    bool ok = true;
+    uint32_t j = 0, mit = 0;
+    bool ok = !p.skip_mma;
     for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++j) {
       const uint32_t b = j & 1;
-      if (!conv_wait_bar(&acc_empty[b], ((j >> 1) & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
+      if (!conv_wait(&acc_empty[b], ((j >> 1) & 1) ^ 1, sy)) { ok = false; break; }
       tc_fence_after();
       for (int kt = 0; kt < KT + KTc; ++kt) {
         const bool corr = kt >= KT;
         const int kk = corr ? kt - KT : kt;
         if (corr && kk == 0 && j > 0) {
           // acc2 is free once the previous tile's epilogue is done
-          if (!conv_wait_bar(&acc_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.err)) {
+          if (!conv_wait(&acc_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, sy)) {
             ok = false;
             break;
           }
@@ -530,7 +623,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         // the staging warps saw this stage's TMA data land (full[s]) and have
         // written its scales into TMEM buffer sb: one barrier covers both
-        if (!conv_wait_bar(&sf_ready[sb], sph, abort_flag, p.err)) { ok = false; break; }
+        if (!conv_wait(&sf_ready[sb], sph, sy)) { ok = false; break; }
+        trace_mark(p.trace, 3, mit);
         tc_fence_after();
         const int klen = corr ? p.kpad : p.K;
         const int ksteps = min(KSTEPS, (klen - kk * KTILE) / 64);
@@ -554,12 +648,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         tc_commit_el(&empty[s]);   // also frees this stage's scale buffer
+        trace_mark(p.trace, 4, mit++);
         if (++s == STAGES) s = 0;
         if (++sb == SF_BUFS) { sb = 0; sph ^= 1; }
       }
       if (!ok) break;
       tc_commit_el(&acc_full[b]);
     }
+    // every MMA this warp issued completes before TMEM or shared memory go away
+    tc_commit_el(drain_mma);
+    if (lane == 0) wait1(drain_mma, 0, dr, false, true);
+    __syncwarp();
   } else if (warp >= SF_WARP0 && warp < EPI_WARP0) {
     // ------------------------------------------------------------ scale staging
     // TMEM buffer sb holds, at column SF_COL + 64*sb + 4*q + j (A) and +32 (B),
@@ -575,15 +674,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       for (int kt = 0; kt < KT + KTc; ++kt, ++it) {
-        bool okw = conv_wait_bar(&full[s], ph, abort_flag, p.err);
+        bool okw = true;
+        for (int w2 = 0; w2 < PRODUCERS && okw; ++w2) okw = conv_wait(&fullw[w2 * STAGES + s], ph, sy);
         if (okw && it >= (uint32_t)SF_BUFS) {
           const uint32_t prev = it - SF_BUFS;
-          okw = conv_wait_bar(&empty[prev % STAGES], (prev / STAGES) & 1, abort_flag, p.err);
+          okw = conv_wait(&empty[prev % STAGES], (prev / STAGES) & 1, sy);
         }
         if (!okw) {
           ok = false;
           break;
         }
+        if (w == 0) trace_mark(p.trace, 1, it);
         tc_fence_after();
         const bool corr = kt >= KT;
         const int kk = corr ? kt - KT : kt;
@@ -608,10 +709,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         tc_commit_el(&sf_ready[sb]);
+        if (w == 0) trace_mark(p.trace, 2, it);
         if (++s == STAGES) { s = 0; ph ^= 1; }
         if (++sb == SF_BUFS) sb = 0;
       }
     }
+    // the scale copies this warp issued complete before TMEM goes away
+    tc_commit_el(drain_sf);
+    if (lane == 0) wait1(drain_sf, 0, dr, false, true);
+    __syncwarp();
   } else if (warp >= EPI_WARP0) {
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
@@ -622,10 +728,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const Tile tl = decode_tile(p, meta, t);
       const uint32_t b = j & 1;
       // lane 0 waits, the warp follows it (tcgen05.ld needs the whole warp)
-      int okw = 0;
-      if (lane == 0) okw = wait_bar(&acc_full[b], (j >> 1) & 1, abort_flag, p.err) ? 1 : 0;
-      okw = __shfl_sync(0xffffffffu, okw, 0);
-      if (!okw) break;
+      if (!warp_wait(&acc_full[b], (j >> 1) & 1, sy)) break;
+      if (warp == EPI_WARP0) trace_mark(p.trace, 5, j);
       tc_fence_after();
       const float a1 = meta.a1[tl.e];
       const float a2 = meta.a2[tl.e];
@@ -732,6 +836,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       __syncwarp();
+      if (warp == EPI_WARP0) trace_mark(p.trace, 6, j);
       if (p.y_amax) {
         amax = warp_max(amax);
         if (lane == 0 && amax > 0.0f) atomicMax(&p.y_amax[tl.e], __float_as_uint(amax));
@@ -761,19 +866,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //
 // Roles (16 warps per CTA):
 //   warps 0-3  TMA producers of this CTA's operands (A rows, its 64 rows of
-//              B, the scale atoms), each arriving on its own per-stage
-//              barrier so that it can wait for exactly its own copies when a
-//              pipeline wait gives up.
-//   warp 4     leader: TMEM allocation (both CTAs) and the MMA issuer.
+//              B, the scale atoms).  Every copy of both CTAs completes on the
+//              leader's full barrier of the stage (cp.async.bulk.tensor
+//              .cta_group::2 names the leader's barrier); the leader's first
+//              producer expects the bytes of both CTAs, so no CTA has to
+//              forward anything to the other.
+//   warp 4     TMEM allocation (both CTAs); leader: the MMA issuer.
 //   warps 5-6  leader: scale atoms of a stage into TMEM of both CTAs
 //              (tcgen05.cp.cta_group::2), one sub-tile each.
-//   warp 5     peer: forwards "this CTA's stage has landed" to the leader.
 //   warps 8-15 epilogue of this CTA's 128 rows (two warps per lane quadrant).
 // The leader's MMA commits free a stage in both CTAs and announce a full
 // accumulator to both; both CTAs' epilogues arrive on the leader's
 // accumulator-empty barrier.  Every wait is bounded; on a timeout a CTA stops
-// its roles, waits (bounded) for its own copies and tensor-core work in
-// flight, meets its peer at the cluster barrier and frees its TMEM.
+// its roles, lets its copies and tensor-core work in flight finish (the
+// leader waits for them on its barriers, with a bound; the peer, whose copies
+// complete on the leader's barriers, waits a fixed bounded time), meets its
+// peer at the cluster barrier and frees its TMEM.
 namespace pair {
 
 constexpr int BM = 128;                       // rows of A per CTA (M = 256 per pair)
@@ -792,6 +900,7 @@ constexpr int STAGE_BYTES = OFF_SFB + SLOTS * SF_SUB;   // 56 KB
 constexpr int BOX_ROWS = 64;
 constexpr int BOX_BYTES = BOX_ROWS * KSUB;    // 8 KB
 constexpr int PRODUCERS = 4;
+constexpr int SF_BOX_ROWS = SF_SUB / 128;     // a sub-tile's atoms as 128-byte rows (TMA box)
 constexpr int MMA_WARP = 4, SF_WARP0 = 5, SF_WARPS = 2, EPI_WARP0 = 8;
 constexpr int NUM_THREADS = 512;
 constexpr int EPI_WARPS = 8;
@@ -801,13 +910,11 @@ constexpr int SF_COL = 384;
 constexpr int SF_BUFS = 2;
 constexpr int SF_BUF_COLS = 64;               // A atoms at +4a, B atoms at +32+4a (a < 8)
 constexpr int MAX_GROUPS = 256;
-constexpr int NBARS = PRODUCERS * STAGES + 2 * STAGES + SF_BUFS + 4 + 2;
+constexpr int NBARS = 2 * STAGES + SF_BUFS + 4 + 2;
 constexpr int BAR_BYTES = NBARS * 8 + 16;     // + TMEM holder and abort flag
 constexpr int META_BYTES = 4 * (MAX_GROUPS + 1);
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + META_BYTES + 1024 /*align*/;
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
-// copies (arrivals) per stage of producer warp w: A slot 0, A slot 1, B, scales
-__host__ __device__ constexpr int copies_of(int w) { return w == 3 ? 4 : 2; }
 
 struct Params {
   int E, N, K, kpad, Nt;
@@ -835,108 +942,6 @@ struct Params {
   // extents for the bounds-checked build: scale buffer bytes and output rows
   int64_t a_sf_bytes, b_sf_bytes, r_sf_bytes, ws_sf_bytes, y_rows;
 };
-
-struct Sync {
-  volatile int* abort_flag;
-  int* err;
-  unsigned long long tmo;
-};
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_id() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_count() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
-                   "memory");
-}
-// Address of the same shared-memory object in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-__device__ __forceinline__ bool try_wait_cluster(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(b)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait by one thread; `cluster` waits with cluster-scope acquire (for
-// barriers another CTA arrives on).  `drain`: ignore the abort flag (used to
-// let work in flight finish after an abort), still bounded by the timeout.
-__device__ __forceinline__ bool wait1(uint64_t* b, uint32_t parity, const Sync& s,
-                                      bool cluster = false, bool drain = false) {
-  auto probe = [&]() { return cluster ? try_wait_cluster(b, parity) : mbar_try_wait(b, parity); };
-  if (probe()) return true;
-  const unsigned long long t0 = global_ns();
-  uint32_t spins = 0;
-  while (true) {
-    if (probe()) return true;
-    if ((++spins & 255u) == 0) {
-      if (!drain && *s.abort_flag) return false;
-      if (global_ns() - t0 > s.tmo) {
-        if (!drain) {
-          *s.abort_flag = 1;
-          atomicExch(s.err, QUADS_ERR_DEVICE_TIMEOUT);
-        }
-        return false;
-      }
-    }
-  }
-}
-// Bounded wait for a whole warp: lane 0 polls, the warp follows its verdict.
-__device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, const Sync& s,
-                                          bool cluster = false) {
-  int ok = 0;
-  if ((threadIdx.x & 31) == 0) ok = wait1(b, parity, s, cluster) ? 1 : 0;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-// Bounded wait polled by every lane of a converged warp (the MMA warp stays
-// converged for its elect-predicated tcgen05 instructions).
-__device__ __forceinline__ bool conv_wait(uint64_t* b, uint32_t parity, const Sync& s,
-                                          bool cluster = false) {
-  auto probe = [&]() { return cluster ? try_wait_cluster(b, parity) : mbar_try_wait(b, parity); };
-  if (__all_sync(0xffffffffu, probe())) return true;
-  const unsigned long long t0 = global_ns();
-  uint32_t spins = 0;
-  while (true) {
-    if (__all_sync(0xffffffffu, probe())) return true;
-    if ((++spins & 255u) == 0) {
-      int give_up = *s.abort_flag ? 1 : 0;
-      if (!give_up && global_ns() - t0 > s.tmo) give_up = 2;
-      give_up = __shfl_sync(0xffffffffu, give_up, 0);
-      if (give_up) {
-        if (give_up == 2 && (threadIdx.x & 31) == 0) {
-          *s.abort_flag = 1;
-          atomicExch(s.err, QUADS_ERR_DEVICE_TIMEOUT);
-        }
-        return false;
-      }
-    }
-  }
-}
 
 __device__ __forceinline__ void mma_nvf4_cg2(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                              uint32_t sfa, uint32_t sfb, uint32_t acc) {
@@ -973,6 +978,17 @@ __device__ __forceinline__ void cp_sf_cg2(uint32_t taddr, uint64_t sdesc) {
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
       "l"(sdesc)
+      : "memory");
+}
+
+// TMA load into this CTA's shared memory that completes on the barrier at
+// cluster address `bar` (the leader's).
+__device__ __forceinline__ void tma_load_2d_cg2(void* dst, const CUtensorMap* map, int x, int y,
+                                                uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
 
@@ -1053,13 +1069,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmR,
-                     const __grid_constant__ CUtensorMap tmW, const Params p) {
+                     const __grid_constant__ CUtensorMap tmW,
+                     const __grid_constant__ CUtensorMap tsA,
+                     const __grid_constant__ CUtensorMap tsB,
+                     const __grid_constant__ CUtensorMap tsR,
+                     const __grid_constant__ CUtensorMap tsW, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES);
-  uint64_t* fullw = bars;                                // [PRODUCERS][STAGES]
-  uint64_t* full_peer = fullw + PRODUCERS * STAGES;      // [STAGES] (leader)
-  uint64_t* empty = full_peer + STAGES;                  // [STAGES]
+  uint64_t* full = bars;                                 // [STAGES] (leader's: both CTAs' copies)
+  uint64_t* empty = full + STAGES;                       // [STAGES]
   uint64_t* sf_ready = empty + STAGES;                   // [SF_BUFS] (leader)
   uint64_t* acc_full = sf_ready + SF_BUFS;               // [2]
   uint64_t* acc_empty = acc_full + 2;                    // [2] (leader)
@@ -1098,10 +1117,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (e == 0) poff[0] = 0;
   }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < PRODUCERS; ++i)
-      for (int s = 0; s < STAGES; ++s) mbar_init(&fullw[i * STAGES + s], copies_of(i));
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full_peer[s], 1);
+      mbar_init(&full[s], 1);   // the leader's expect_tx; the copies complete the bytes
       mbar_init(&empty[s], 1);
     }
     for (int i = 0; i < SF_BUFS; ++i) mbar_init(&sf_ready[i], SF_WARPS);
@@ -1141,9 +1158,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp < PRODUCERS) {
     // ---------------------------------------------------------- producers
     // warp 0: A boxes of slot 0, warp 1: A boxes of slot 1, warp 2: the B box
-    // of both slots, warp 3: the scale atoms (A and B) of both slots.  A copy
-    // of an empty slot is a plain arrival.
-    uint64_t* myfull = fullw + warp * STAGES;
+    // of both slots, warp 3: the scale atoms (A and B) of both slots.  The
+    // leader's warp 0 expects the stage's bytes of both CTAs before its own
+    // copies; the other copies may land first (the barrier's transaction
+    // count then runs ahead, which it allows).
+    const uint32_t full0 = peer_addr(&full[0], 0);
+    const uint32_t sf_box = (p.mx ? SF_BOX_ROWS / 2 : SF_BOX_ROWS) * 128;
     uint32_t it = 0;
     bool ok = true;
     for (int64_t t = cid; t < ntiles && ok; t += ncl) {
@@ -1158,67 +1178,56 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t ph = (it / STAGES) & 1;
         if (!warp_wait(&empty[s], ph ^ 1, sy)) { ok = false; break; }
         uint8_t* st = smem + s * STAGE_BYTES;
+        const uint32_t bar = full0 + 8u * s;
         if (elect_one()) {
+          if (leader && warp == 0) {
+            uint32_t bytes = 0;
+            for (int u = 0; u < SLOTS; ++u)
+              if (sub_of(p, kt * SLOTS + u, nmain, ncorr).ksteps)
+                bytes += A_SUB + B_SUB + 2 * sf_box;
+            mbar_expect_tx(&full[s], 2 * bytes);   // both CTAs
+          }
           for (int u = 0; u < SLOTS; ++u) {
             const Sub sb = sub_of(p, kt * SLOTS + u, nmain, ncorr);
+            if (!sb.ksteps) continue;
             const CUtensorMap* ma = sb.corr ? &tmR : &tmA;
             const CUtensorMap* mb = sb.corr ? &tmW : &tmB;
             const int x = sb.kk * KSUB;
             if (warp == u) {            // A: two 64-row boxes
-              for (int h = 0; h < 2; ++h) {
-                if (sb.ksteps) {
-                  mbar_expect_tx(&myfull[s], BOX_BYTES);
-                  tma_load_2d(st + u * A_SUB + h * BOX_BYTES, ma, x, (int)(mrow + h * BOX_ROWS),
-                              &myfull[s]);
-                } else {
-                  mbar_arrive(&myfull[s]);
-                }
-              }
+              for (int h = 0; h < 2; ++h)
+                tma_load_2d_cg2(st + u * A_SUB + h * BOX_BYTES, ma, x, (int)(mrow + h * BOX_ROWS), bar);
             } else if (warp == 2) {     // B: this CTA's 64 rows
-              if (sb.ksteps) {
-                mbar_expect_tx(&myfull[s], BOX_BYTES);
-                tma_load_2d(st + OFF_B + u * B_SUB, mb, x, (int)brow, &myfull[s]);
-              } else {
-                mbar_arrive(&myfull[s]);
-              }
-            } else if (warp == 3) {     // scale atoms of A and of the pair's B
-              const uint32_t bytes = (p.mx ? (sb.ksteps + 1) / 2 : sb.ksteps) * 512;
-              if (sb.ksteps) {
-                const int64_t oa = sb.corr ? blk * r_sf_rb + (int64_t)sb.kk * SF_SUB
-                                           : blk * a_sf_rb + (int64_t)sb.kk * sf_sub;
-                const int64_t ow = sb.corr ? (bbase / BM) * r_sf_rb + (int64_t)sb.kk * SF_SUB
-                                           : (bbase / BM) * a_sf_rb + (int64_t)sb.kk * sf_sub;
-                if (QDBGV(oa >= 0 && oa + bytes <= (sb.corr ? p.r_sf_bytes : p.a_sf_bytes),
-                          (tl.m0 << 20) | ((int64_t)tl.e << 8) | (sb.corr ? 2 : 0) | (int)rank)) {
-                  mbar_expect_tx(&myfull[s], bytes);
-                  bulk_load(st + OFF_SFA + u * SF_SUB, (sb.corr ? p.r_sf : p.a_sf) + oa, bytes,
-                            &myfull[s]);
-                } else {
-                  mbar_arrive(&myfull[s]);
-                }
-                if (QDBGV(ow >= 0 && ow + bytes <= (sb.corr ? p.ws_sf_bytes : p.b_sf_bytes),
-                          (bbase << 20) | ((int64_t)tl.e << 8) | (sb.corr ? 2 : 0) | 4 | (int)rank)) {
-                  mbar_expect_tx(&myfull[s], bytes);
-                  bulk_load(st + OFF_SFB + u * SF_SUB, (sb.corr ? p.ws_sf : p.b_sf) + ow, bytes,
-                            &myfull[s]);
-                } else {
-                  mbar_arrive(&myfull[s]);
-                }
-              } else {
-                mbar_arrive(&myfull[s]);
-                mbar_arrive(&myfull[s]);
-              }
+              tma_load_2d_cg2(st + OFF_B + u * B_SUB, mb, x, (int)brow, bar);
+            } else if (warp == 3) {     // scale atoms of A and of the pair's B, as 128-byte rows
+              const int64_t oa = sb.corr ? blk * r_sf_rb + (int64_t)sb.kk * SF_SUB
+                                         : blk * a_sf_rb + (int64_t)sb.kk * sf_sub;
+              const int64_t ow = sb.corr ? (bbase / BM) * r_sf_rb + (int64_t)sb.kk * SF_SUB
+                                         : (bbase / BM) * a_sf_rb + (int64_t)sb.kk * sf_sub;
+              (void)QDBGV(oa >= 0 && oa + sf_box <= (sb.corr ? p.r_sf_bytes : p.a_sf_bytes) + 3 * 512,
+                          (tl.m0 << 20) | ((int64_t)tl.e << 8) | (sb.corr ? 2 : 0) | (int)rank);
+              (void)QDBGV(ow >= 0 && ow + sf_box <= (sb.corr ? p.ws_sf_bytes : p.b_sf_bytes) + 3 * 512,
+                          (bbase << 20) | ((int64_t)tl.e << 8) | (sb.corr ? 2 : 0) | 4 | (int)rank);
+              tma_load_2d_cg2(st + OFF_SFA + u * SF_SUB, sb.corr ? &tsR : &tsA, 0, (int)(oa / 128), bar);
+              tma_load_2d_cg2(st + OFF_SFB + u * SF_SUB, sb.corr ? &tsW : &tsB, 0, (int)(ow / 128), bar);
             }
           }
         }
         __syncwarp();
       }
     }
-    // let every copy this warp issued land (at most the last STAGES
-    // iterations can still be in flight) before the CTA can exit
-    if (lane == 0) {
-      const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
-      for (uint32_t j = first; j < it; ++j) wait1(&myfull[j % STAGES], (j / STAGES) & 1, sy, false, true);
+    if (!ok && lane == 0) {
+      // let the copies this CTA issued land before it can exit: the leader
+      // waits for the stages' barriers (bounded); the peer, whose copies
+      // complete on the leader's barriers, waits a fixed bounded time
+      if (leader) {
+        const Sync dr{abort_flag, p.err, kDrainNs};
+        const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
+        for (uint32_t j = first; j < it; ++j) wait1(&full[j % STAGES], (j / STAGES) & 1, dr, false, true);
+      } else {
+        const unsigned long long t0 = global_ns();
+        while (global_ns() - t0 < 100000ull) {
+        }
+      }
     }
   } else if (warp == MMA_WARP && leader) {
     // ---------------------------------------------------------- MMA issuer
@@ -1270,7 +1279,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     // every MMA this thread issued has completed before TMEM or shared memory go away
     commit_mc_cg2(drain_mma, 0x1);
-    if (lane == 0) wait1(drain_mma, 0, sy, false, true);
+    if (lane == 0) wait1(drain_mma, 0, Sync{abort_flag, p.err, kDrainNs}, false, true);
     __syncwarp();
   } else if (warp >= SF_WARP0 && warp < SF_WARP0 + SF_WARPS && leader) {
     // ---------------------------------------------------------- scale staging
@@ -1282,9 +1291,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     for (int64_t t = cid; t < ntiles && ok; t += ncl) {
       for (int kt = 0; kt < nst; ++kt, ++it) {
-        bool okw = true;
-        for (int i = 0; i < PRODUCERS && okw; ++i) okw = conv_wait(&fullw[i * STAGES + s], ph, sy);
-        if (okw) okw = conv_wait(&full_peer[s], ph, sy, true);
+        bool okw = conv_wait(&full[s], ph, sy, true);
         if (okw && it >= (uint32_t)SF_BUFS) {
           const uint32_t prev = it - SF_BUFS;
           okw = conv_wait(&empty[prev % STAGES], (prev / STAGES) & 1, sy);
@@ -1307,23 +1314,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     commit_mc_cg2(drain_sf, 0x1);
-    if (lane == 0) wait1(drain_sf, 0, sy, false, true);
+    if (lane == 0) wait1(drain_sf, 0, Sync{abort_flag, p.err, kDrainNs}, false, true);
     __syncwarp();
-  } else if (warp == SF_WARP0 && !leader) {
-    // ---------------------------------------------------------- peer: forward
-    // "this CTA's stage has landed" to the leader's full_peer barrier
-    uint32_t s = 0, ph = 0;
-    bool ok = true;
-    const uint32_t remote = peer_addr(&full_peer[0], 0);
-    for (int64_t t = cid; t < ntiles && ok; t += ncl) {
-      for (int kt = 0; kt < nst && ok; ++kt) {
-        for (int i = 0; i < PRODUCERS && ok; ++i) ok = warp_wait(&fullw[i * STAGES + s], ph, sy);
-        if (!ok) break;
-        if (lane == 0) arrive_cluster(remote + 8u * s);
-        __syncwarp();
-        if (++s == STAGES) { s = 0; ph ^= 1; }
-      }
-    }
   } else if (warp >= EPI_WARP0) {
     // ---------------------------------------------------------- epilogue
     const int quad = warp & 3;
@@ -1624,14 +1616,34 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t wid
   return r == CUDA_SUCCESS;
 }
 
+// Scale atoms as rows of 128 bytes (a 512-byte atom is four rows), box of
+// `box_rows` rows, no swizzle: the pair kernel loads a sub-tile's atoms with
+// one TMA copy that can complete on the leader CTA's barrier.
+static bool make_sf_map(CUtensorMap* m, const void* base, int64_t bytes, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn || bytes < 128 || bytes % 128) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)(bytes / 128)};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 static __device__ int g_gemm_error;
 
 // Test hook (quads_test_gemm_wait_timeout): the next GEMM launch gets a 1 ms
 // wait limit and an MMA warp that issues nothing, so its waits run out.
 static std::atomic<int> g_wait_test{0};
-// The earlier one-CTA kernel, selectable for comparison (QUADS_GEMM_ONE_CTA=1).
-static const bool g_one_cta_kernel = [] {
-  const char* v = getenv("QUADS_GEMM_ONE_CTA");
+// Profiling hook (quads_test_gemm_timeline): the next one-CTA GEMM launch
+// records CTA 0's stage timeline into this device buffer.
+static std::atomic<unsigned long long*> g_trace{nullptr};
+// The CTA-pair kernel, selectable for comparison (QUADS_GEMM_PAIR=1); the
+// one-CTA kernel measured faster on every benchmark shape and is the default.
+static const bool g_pair_kernel = [] {
+  const char* v = getenv("QUADS_GEMM_PAIR");
   return v && v[0] == '1';
 }();
 
@@ -1764,7 +1776,8 @@ static quads_status_t launch(const Launch& L) {
     errp = errp_dev[dev];
     max_pairs = pairs_dev[dev];
   }
-  if (g_one_cta_kernel) {
+  const bool wait_test = g_wait_test.exchange(0) != 0;
+  if (!g_pair_kernel) {
     Params p;
     p.E = L.E; p.N = L.N; p.K = L.K; p.kpad = comp ? L.kpad : 0; p.Nt = L.N / BN;
     p.M = L.M; p.row_off = L.row_off; p.row_cnt = L.row_cnt;
@@ -1778,6 +1791,9 @@ static quads_status_t launch(const Launch& L) {
     p.err = errp;
     p.a_sf_bytes = ext.a; p.b_sf_bytes = ext.b; p.r_sf_bytes = ext.r; p.ws_sf_bytes = ext.w;
     p.y_rows = arows;
+    p.timeout_ns = wait_test ? 1000000ull : kTimeoutNs;
+    p.skip_mma = wait_test ? 1 : 0;
+    p.trace = g_trace.exchange(nullptr);
     int64_t grid = num_sms();
     if (!L.row_off) grid = std::min<int64_t>(grid, ((L.M + BM - 1) / BM) * (L.N / BN));
     gemm_kernel<<<(int)grid, NUM_THREADS, SMEM_BYTES, L.stream>>>(tA, tB, tR, tW, p);
@@ -1796,7 +1812,6 @@ static quads_status_t launch(const Launch& L) {
   p.err = errp;
   p.a_sf_bytes = ext.a; p.b_sf_bytes = ext.b; p.r_sf_bytes = ext.r; p.ws_sf_bytes = ext.w;
   p.y_rows = arows;
-  const bool wait_test = g_wait_test.exchange(0) != 0;
   p.timeout_ns = wait_test ? 1000000ull : kTimeoutNs;
   p.skip_mma = wait_test ? 1 : 0;
   // one CTA pair per pair of SMs, persistent over the tiles
@@ -1815,7 +1830,20 @@ static quads_status_t launch(const Launch& L) {
   cfg.stream = L.stream;
   cfg.attrs = &at;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, pair::pair_gemm_kernel, tA, tB, tR, tW, p);
+  CUtensorMap sA, sB, sR, sW;
+  const int sf_rows = L.mx ? pair::SF_BOX_ROWS / 2 : pair::SF_BOX_ROWS;
+  if (!make_sf_map(&sA, L.a_sf, ext.a, sf_rows) || !make_sf_map(&sB, L.b_sf, ext.b, sf_rows))
+    return fail(QUADS_ERR_CUDA, "gemm: cuTensorMapEncodeTiled failed for the scale atoms");
+  if (comp) {
+    if (!make_sf_map(&sR, L.r_sf, ext.r, pair::SF_BOX_ROWS) ||
+        !make_sf_map(&sW, ws_sf, ext.w, pair::SF_BOX_ROWS))
+      return fail(QUADS_ERR_CUDA, "gemm: cuTensorMapEncodeTiled failed for the correction scales");
+  } else {
+    sR = sA;
+    sW = sB;
+  }
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, pair::pair_gemm_kernel, tA, tB, tR, tW, sA, sB, sR, sW, p);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return fail(QUADS_ERR_CUDA, "gemm: launch of the CTA-pair kernel: %s", cudaGetErrorString(e));
@@ -1824,6 +1852,7 @@ static quads_status_t launch(const Launch& L) {
 }
 
 void gemm_wait_test(int enable) { g_wait_test.store(enable ? 1 : 0); }
+void gemm_timeline(unsigned long long* buf) { g_trace.store(buf); }
 }  // namespace gemm
 
 int read_gemm_device_error() {
@@ -1984,6 +2013,10 @@ extern "C" quads_status_t quads_mx_gemm(int64_t M, int64_t N, int64_t K, const u
 }
 
 extern "C" void quads_test_gemm_wait_timeout(int32_t enable) { gemm::gemm_wait_test(enable); }
+
+extern "C" void quads_test_gemm_timeline(uint64_t* device_buffer) {
+  gemm::gemm_timeline(reinterpret_cast<unsigned long long*>(device_buffer));
+}
 
 extern "C" quads_status_t quads_weight_columns(const uint8_t* w_codes, const uint8_t* w_scales,
                                                int32_t num_groups, int64_t rows_per_group,

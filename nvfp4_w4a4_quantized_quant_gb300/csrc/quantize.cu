@@ -25,6 +25,7 @@ namespace quads {
 static __device__ int g_quant_error;  // device-side argument check failures
 
 constexpr int kRselGroupMin = 32;     // groups from which the per-group R_sel kernel is used
+constexpr int kFusedMaxK = 1024;      // selected channels of the fused activation-side kernel
 
 // ---------------------------------------------------------------- amax
 // One block per 8-row slice (inside one group), threads over (row, 8-col
@@ -83,151 +84,172 @@ __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restri
 }
 
 // ---------------------------------------------------------------- quantize
-// One warp per task = (32-row chunk, 256-column slab).  Lane l owns the eight
-// columns slab*256 + 8l .. +7, half of a 16-element block whose other half is
-// on lane l^1 (the block maximum takes one shuffle; both lanes then derive the
-// same block scale), and walks the chunk's rows in order with the next eight
-// rows' loads in flight (a register ring, unrolled so its indices are static).
-// In score mode the residual energy R^2 of each of its columns is added to a
-// register accumulator row by row from 0 -- the fixed float32 order of the
-// score definition -- and stored as the chunk's partials at the end: no shared
-// memory, no barrier.  Codes go out as one 4-byte word per lane (128 bytes per
-// warp and row), block scales as one 4-byte word per four blocks.  In QDQ mode
-// (the trainer's W4A16 fake quantization, [QUADS] 2.2 A) each element's
-// dequantized value fl(level * d_b) is also stored, rounded to bf16, as one
-// 16-byte vector per lane; codes and scales may then be skipped
-// (codes == nullptr).
-constexpr int kQAhead = 8;   // rows loaded ahead per warp
+// A block owns one (32-row chunk, 256-column slab) task.  Warp w quantizes
+// rows 4w .. 4w+3 of the chunk, two rows at a time: lane l takes the 16-element
+// block (l & 15) of row (l >> 4), so each block scale is computed once.  In
+// score mode every residual square R^2 is parked in shared memory and, after a
+// barrier, thread c adds column c's 32 squares in row order starting from 0 --
+// the fixed float32 order the score definition uses.  In QDQ mode (the
+// trainer's W4A16 fake quantization, [QUADS] 2.2 A) each element's dequantized
+// value fl(level * d_b) is also stored, rounded to bf16; codes and scales may
+// then be skipped (codes == nullptr).
+__device__ __forceinline__ void quantize_block16(const uint4& lo, const uint4& hi, float s_t,
+                                                 float* f, BlockScale& bs, uint2& c) {
+  bf16x8_to_f32(lo, f);
+  bf16x8_to_f32(hi, f + 8);
+  float m = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(f[j]));
+  bs = block_scale(m, s_t);
+  c.x = quantize8(f, bs);
+  c.y = quantize8(f + 8, bs);
+}
 
-// The task loop of one warp (warp `wid` of `nwarps`), shared by the
-// quantizer kernel and the fused activation-side kernel.
+// The task loop of one 256-thread block (tasks first, first + stride, ...),
+// shared by the quantizer kernel and the fused activation-side kernel; `sq`
+// is 32 x 256 floats of shared memory in score mode.
 template <bool kScores, bool kQdq>
-__device__ __forceinline__ void quantize_tasks(
+__device__ __forceinline__ void quantize_block_tasks(
     const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
     const int32_t* __restrict__ row_index, const int32_t* __restrict__ goff, int G,
     const float* __restrict__ st, const uint32_t* __restrict__ amax_bits,
     uint8_t* __restrict__ codes, int64_t ldc, uint8_t* __restrict__ scales, int layout,
-    int sf_words, float* __restrict__ partials, __nv_bfloat16* __restrict__ qdq, int64_t ldq,
-    int64_t wid, int64_t nwarps) {
-  // tensor scales: given (st), or derived from the groups' amax bits
+    float* __restrict__ partials, __nv_bfloat16* __restrict__ qdq, int64_t ldq, float* sq,
+    int64_t first, int64_t stride) {
+  // tensor scales: given (st), or derived from the groups' amax bits (read
+  // through L2: the fused kernel produces them earlier in the same launch)
   auto scale_of = [&](int g) {
-    return amax_bits ? tensor_scale_from_amax(__uint_as_float(__ldg(amax_bits + g))) : __ldg(st + g);
+    return amax_bits ? tensor_scale_from_amax(__uint_as_float(__ldcg(amax_bits + g))) : __ldcg(st + g);
   };
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int64_t end = goff ? (int64_t)goff[G] : rows;
   if (!QDBG(end >= 0 && end <= rows)) end = 0;
   const int nslab = (cols + 255) >> 8;
   const int64_t nchunks = (end + kScoreChunk - 1) / kScoreChunk;
   const int64_t ntasks = nchunks * nslab;
   const int ncols16 = cols >> 4;
-  for (int64_t task = wid; task < ntasks; task += nwarps) {
+  const int blk = lane & 15;
+  // this thread's two rows of a task, loaded one task ahead
+  auto load_task = [&](int64_t task, uint4 (&raw)[2][2]) {
     const int64_t chunk = task / nslab;
-    const int col = (int)(task - chunk * nslab) * 256 + lane * 8;
+    const int col = (int)(task % nslab) * 256 + blk * 16;
+    const int64_t r0 = chunk * kScoreChunk;
+    const int64_t r1 = min(r0 + kScoreChunk, end);
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const int64_t row = r0 + 4 * warp + 2 * it + (lane >> 4);
+      raw[it][0] = raw[it][1] = make_uint4(0, 0, 0, 0);
+      if (task < ntasks && col < cols && row < r1) {
+        const int64_t src = row_index ? (int64_t)row_index[row] : row;
+        const uint4* px = reinterpret_cast<const uint4*>(x + src * ldx + col);
+        raw[it][0] = __ldg(px);
+        raw[it][1] = __ldg(px + 1);
+      }
+    }
+  };
+  uint4 nxt[2][2];
+  load_task(first, nxt);
+  for (int64_t task = first; task < ntasks; task += stride) {
+    uint4 raw[2][2];
+#pragma unroll
+    for (int it = 0; it < 2; ++it) { raw[it][0] = nxt[it][0]; raw[it][1] = nxt[it][1]; }
+    load_task(task + stride, nxt);
+    const int64_t chunk = task / nslab;
+    const int slab = (int)(task % nslab);
+    const int col = slab * 256 + blk * 16;
     const bool active = col < cols;
     const int64_t r0 = chunk * kScoreChunk;
-    const int nr = (int)min((int64_t)kScoreChunk, end - r0);   // warp-uniform
-    auto load_row = [&](int i) {
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (active && i < nr) {
-        const int64_t src = row_index ? (int64_t)__ldg(row_index + r0 + i) : r0 + i;
-        v = __ldg(reinterpret_cast<const uint4*>(x + src * ldx + col));
+    const int64_t r1 = min(r0 + kScoreChunk, end);
+    const int g0 = goff ? group_of(goff, G, r0) : 0;   // same for the whole block
+    const float s_t0 = scale_of(g0);
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const int64_t row = r0 + 4 * warp + 2 * it + (lane >> 4);
+      const bool valid = active && row < r1;
+      int g = g0;
+      if (goff && valid)
+        while (g + 1 < G && row >= goff[g + 1]) ++g;
+      float f[16];
+      BlockScale bs;
+      uint2 c;
+      quantize_block16(raw[it][0], raw[it][1], !valid ? 1.0f : g == g0 ? s_t0 : scale_of(g), f, bs,
+                       c);
+      if (valid && (!kQdq || codes)) {
+        uint32_t* pc = reinterpret_cast<uint32_t*>(codes + row * ldc + (col >> 1));
+        pc[0] = c.x;
+        pc[1] = c.y;
+        scales[sf_offset(layout, row, col >> 4, ncols16)] = (uint8_t)bs.byte;
       }
-      return v;
-    };
-    uint4 ring[kQAhead];
+      if (kQdq && valid) {
+        float lv[16];
+        e2m1x8_to_f32(c.x, lv);
+        e2m1x8_to_f32(c.y, lv + 8);
+        uint32_t packed[8];
 #pragma unroll
-    for (int u = 0; u < kQAhead; ++u) ring[u] = load_row(u);
-    int g = goff ? group_of(goff, G, r0) : 0;
-    int64_t gnext = goff ? (int64_t)__ldg(goff + g + 1) : end;
-    float s_t = scale_of(g);
-    float acc[8];
+        for (int j = 0; j < 8; ++j) {
+          __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(lv[2 * j], bs.d),
+                                                   __fmul_rn(lv[2 * j + 1], bs.d));
+          packed[j] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        uint4* pq = reinterpret_cast<uint4*>(qdq + row * ldq + col);
+        pq[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        pq[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+      }
+      if (kScores) {
+        float lv[16];
+        e2m1x8_to_f32(c.x, lv);
+        e2m1x8_to_f32(c.y, lv + 8);
+        float4* ps = reinterpret_cast<float4*>(sq + (row - r0) * 256 + blk * 16);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-    for (int i0 = 0; i0 < nr; i0 += kQAhead) {
+        for (int q = 0; q < 4; ++q) {
+          float v[4];
 #pragma unroll
-      for (int u = 0; u < kQAhead; ++u) {
-        const int i = i0 + u;
-        const uint4 cur = ring[u];
-        ring[u] = load_row(i + kQAhead);
-        if (i < nr) {   // warp-uniform
-          const int64_t row = r0 + i;
-          while (row >= gnext) {   // a group boundary inside the chunk
-            // the partials of a chunk must belong to one group
-            if (kScores && lane == 0) atomicExch(&g_quant_error, QUADS_ERR_DEVICE_CHECK);
-            ++g;
-            gnext = __ldg(goff + g + 1);
-            s_t = scale_of(g);
+          for (int j = 0; j < 4; ++j) {
+            // rows past the end were loaded as zeros: their codes and R are 0
+            const float R = __fsub_rn(f[4 * q + j], __fmul_rn(lv[4 * q + j], bs.d));
+            v[j] = __fmul_rn(R, R);
           }
-          float f[8];
-          bf16x8_to_f32(cur, f);
-          float m = 0.0f;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
-          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-          const BlockScale bs = block_scale(m, s_t);
-          const uint32_t c = quantize8(f, bs);
-          if (!kQdq || codes) {
-            if (active) *reinterpret_cast<uint32_t*>(codes + row * ldc + (col >> 1)) = c;
-            if (sf_words) {
-              // blocks 4q .. 4q+3 of the slab sit on lanes 8q, 8q+2, 8q+4, 8q+6
-              const uint32_t b1 = __shfl_down_sync(0xffffffffu, bs.byte, 2);
-              const uint32_t b2 = __shfl_down_sync(0xffffffffu, bs.byte, 4);
-              const uint32_t b3 = __shfl_down_sync(0xffffffffu, bs.byte, 6);
-              if ((lane & 7) == 0 && active)
-                *reinterpret_cast<uint32_t*>(scales + sf_offset(layout, row, col >> 4, ncols16)) =
-                    bs.byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
-            } else if ((lane & 1) == 0 && active) {
-              scales[sf_offset(layout, row, col >> 4, ncols16)] = (uint8_t)bs.byte;
-            }
-          }
-          if (kQdq || kScores) {
-            float lv[8];
-            e2m1x8_to_f32(c, lv);
-            if (kQdq && active) {
-              uint32_t packed[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(lv[2 * j], bs.d),
-                                                         __fmul_rn(lv[2 * j + 1], bs.d));
-                packed[j] = *reinterpret_cast<uint32_t*>(&h);
-              }
-              *reinterpret_cast<uint4*>(qdq + row * ldq + col) =
-                  make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            }
-            if (kScores) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float R = __fsub_rn(f[j], __fmul_rn(lv[j], bs.d));
-                acc[j] = __fadd_rn(acc[j], __fmul_rn(R, R));
-              }
-            }
-          }
+          // 16-byte chunk q of this block lands at chunk q ^ ((blk >> 1) & 3): the
+          // eight lanes of a store phase then cover all 32 banks
+          ps[q ^ ((blk >> 1) & 3)] = make_float4(v[0], v[1], v[2], v[3]);
         }
       }
     }
-    if (kScores && active) {
-      float4* pp = reinterpret_cast<float4*>(partials + chunk * cols + col);
-      pp[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      pp[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if (kScores) {
+      __syncthreads();
+      const int c = slab * 256 + (int)threadIdx.x;
+      if (c < cols) {
+        float acc = 0.0f;
+        const int nr = (int)(r1 - r0);
+        // column c sits at its swizzled position (chunk of 4 within its 16-block)
+        const int cb = (int)threadIdx.x >> 4;
+        const int pc = ((int)threadIdx.x & ~15) | (((((int)threadIdx.x >> 2) & 3) ^ ((cb >> 1) & 3)) << 2) |
+                       ((int)threadIdx.x & 3);
+        for (int r = 0; r < nr; ++r) acc = __fadd_rn(acc, sq[r * 256 + pc]);
+        partials[chunk * cols + c] = acc;
+      }
+      __syncthreads();
     }
   }
 }
 
+
+// Score mode runs four blocks per SM (64 registers, no spills).
 template <bool kScores, bool kQdq>
-__global__ void __launch_bounds__(256, 2) quantize_kernel(
+__global__ void __launch_bounds__(256, kScores ? 4 : 1) quantize_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
     const int32_t* __restrict__ row_index, const int32_t* __restrict__ goff, int G,
     const float* __restrict__ st, const uint32_t* __restrict__ amax_bits, float* __restrict__ st_out,
     uint8_t* __restrict__ codes, int64_t ldc, uint8_t* __restrict__ scales, int layout,
-    int sf_words, float* __restrict__ partials, __nv_bfloat16* __restrict__ qdq, int64_t ldq) {
+    float* __restrict__ partials, __nv_bfloat16* __restrict__ qdq, int64_t ldq) {
+  __shared__ __align__(16) float sq[kScores ? kScoreChunk * 256 : 4];
   // tensor scales derived from the groups' amax bits are also stored by block 0
   if (amax_bits && blockIdx.x == 0)
     for (int g = threadIdx.x; g < G; g += blockDim.x)
       st_out[g] = tensor_scale_from_amax(__uint_as_float(__ldg(amax_bits + g)));
-  quantize_tasks<kScores, kQdq>(x, rows, cols, ldx, row_index, goff, G, st, amax_bits, codes, ldc,
-                                scales, layout, sf_words, partials, qdq, ldq,
-                                (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5),
-                                (int64_t)gridDim.x * (blockDim.x >> 5));
+  quantize_block_tasks<kScores, kQdq>(x, rows, cols, ldx, row_index, goff, G, st, amax_bits, codes,
+                                      ldc, scales, layout, partials, qdq, ldq, sq, blockIdx.x,
+                                      gridDim.x);
 }
 
 // ---------------------------------------------------------------- select
@@ -632,6 +654,230 @@ __global__ void __launch_bounds__(256) rsel_quantize_kernel(
   }
 }
 
+// ---------------------------------------------------------------- fused activation side
+// The whole activation side of one compensated GEMM in one cooperative
+// kernel: tensor amax, RTN quantization with the residual-energy partials,
+// channel scores, top-k selection, the residual slice R[:, sel] and its second
+// quantization -- five phases separated by four grid-wide barriers.  X is read
+// from HBM once: the second (quantizing) pass and the gather of the selected
+// columns find it in L2 when it fits there (a 8192 x 2048 bf16 activation is
+// 32 MiB of the 129 MB L2).  Every block computes the same top-k from the
+// same scores, so the selection needs no further barrier.  The barrier waits
+// are bounded; a barrier that does not complete latches
+// QUADS_ERR_DEVICE_TIMEOUT and the kernel returns.
+struct FusedCtl {
+  uint32_t amax_x;    // float bits of max |x|
+  uint32_t amax_r;    // float bits of max |R_sel|
+  uint32_t count;     // barrier arrivals
+  uint32_t gen;       // barrier generation
+};
+constexpr int kFusedThreads = 256;
+
+__device__ __forceinline__ bool grid_barrier(FusedCtl* ctl, unsigned long long tmo, int* err) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const uint32_t g = *reinterpret_cast<volatile uint32_t*>(&ctl->gen);
+    __threadfence();
+    if (atomicAdd(&ctl->count, 1u) == gridDim.x - 1) {
+      atomicExch(&ctl->count, 0u);
+      __threadfence();
+      atomicAdd(&ctl->gen, 1u);
+    } else {
+      unsigned long long t0 = 0;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+      while (*reinterpret_cast<volatile uint32_t*>(&ctl->gen) == g) {
+        unsigned long long t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if (t - t0 > tmo) {
+          ok = 0;
+          atomicExch(err, QUADS_ERR_DEVICE_TIMEOUT);
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+template <int PER>
+__global__ void __launch_bounds__(kFusedThreads, 4) quantize_select_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
+    uint8_t* __restrict__ codes, int64_t ldc, uint8_t* __restrict__ scales, int layout,
+    float* __restrict__ st_out, float* __restrict__ partials,
+    float* __restrict__ scores, int k, int kpad, int32_t* __restrict__ sel, float* __restrict__ rs,
+    uint8_t* __restrict__ rcodes, uint8_t* __restrict__ rscales, int rlayout,
+    float* __restrict__ rst, FusedCtl* ctl, unsigned long long tmo) {
+  // phase B's residual squares (32 x 256) and phase C's partial tile (256 x 33)
+  // share one buffer
+  __shared__ __align__(16) float sbuf[256 * 33];
+  float (*tile)[33] = reinterpret_cast<float (*)[33]>(sbuf);
+  __shared__ int hist[256];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_need;
+  __shared__ int warp_sums[kFusedThreads / 32];
+  __shared__ int32_t s_sel[kFusedMaxK];
+  __shared__ float red[kFusedThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int NW = kFusedThreads / 32;
+  const int ncols16 = cols >> 4;
+
+  // ---- A: tensor amax (exact maximum of bf16 magnitudes)
+  {
+    const int vpr = cols >> 3;
+    const int64_t nvec = rows * vpr;
+    __nv_bfloat162 m2 = __floats2bfloat162_rn(0.0f, 0.0f);
+    const int64_t stride = (int64_t)gridDim.x * kFusedThreads;
+    for (int64_t i0 = (int64_t)blockIdx.x * kFusedThreads + threadIdx.x; i0 < nvec; i0 += 4 * stride) {
+      uint4 u[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int64_t i = i0 + q * stride;
+        u[q] = make_uint4(0, 0, 0, 0);
+        if (i < nvec) {
+          const int64_t r = i / vpr;
+          u[q] = __ldg(reinterpret_cast<const uint4*>(x + r * ldx) + (i - r * vpr));
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t w[4] = {u[q].x, u[q].y, u[q].z, u[q].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[j])));
+      }
+    }
+    const float2 mf = __bfloat1622float2(m2);
+    float m = warp_max(fmaxf(mf.x, mf.y));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+      float v = lane < NW ? red[lane] : 0.0f;
+      v = warp_max(v);
+      if (lane == 0 && v > 0.0f) atomicMax(&ctl->amax_x, __float_as_uint(v));
+    }
+  }
+  if (!grid_barrier(ctl, tmo, &g_quant_error)) return;
+
+  // ---- B: quantization and residual-energy partials
+  if (blockIdx.x == 0 && threadIdx.x == 0)
+    st_out[0] = tensor_scale_from_amax(__uint_as_float(*reinterpret_cast<volatile uint32_t*>(&ctl->amax_x)));
+  quantize_block_tasks<true, false>(x, rows, cols, ldx, nullptr, nullptr, 1, nullptr, &ctl->amax_x,
+                                    codes, ldc, scales, layout, partials, nullptr, 0, sbuf,
+                                    blockIdx.x, gridDim.x);
+  if (!grid_barrier(ctl, tmo, &g_quant_error)) return;
+
+  // ---- C: channel scores = chunk partials added in ascending chunk order
+  {
+    const int64_t nchunks = (rows + kScoreChunk - 1) / kScoreChunk;
+    for (int cg = blockIdx.x; cg * 32 < cols; cg += gridDim.x) {
+      const int c = cg * 32 + lane;
+      float t = 0.0f;
+      for (int64_t base = 0; base < nchunks; base += 256) {
+        const int n = (int)min((int64_t)256, nchunks - base);
+#pragma unroll
+        for (int j = 0; j < 256 / NW; ++j) {
+          const int i = warp + NW * j;
+          tile[i][lane] = (i < n && c < cols) ? __ldcg(partials + (base + i) * cols + c) : 0.0f;
+        }
+        __syncthreads();
+        if (warp == 0)
+          for (int i = 0; i < n; ++i) t = __fadd_rn(t, tile[i][lane]);
+        __syncthreads();
+      }
+      if (warp == 0 && c < cols) scores[c] = t;
+    }
+  }
+  if (!grid_barrier(ctl, tmo, &g_quant_error)) return;
+
+  // ---- D: every block selects the same top-k; R[:, sel] of this block's rows
+  {
+    uint32_t key[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int c = threadIdx.x + i * kFusedThreads;
+      key[i] = c < cols ? __float_as_uint(__ldcg(scores + c)) : 0u;
+    }
+    block_topk<kFusedThreads, PER>(key, cols, k, s_sel, hist, &s_prefix, &s_need, warp_sums);
+    __syncthreads();
+    if (blockIdx.x == 0)
+      for (int j = threadIdx.x; j < k; j += kFusedThreads) sel[j] = s_sel[j];
+    const float s_t = tensor_scale_from_amax(__uint_as_float(*reinterpret_cast<volatile uint32_t*>(&ctl->amax_x)));
+    const int64_t rpb = (rows + gridDim.x - 1) / gridDim.x;
+    const int64_t r0 = min(rows, (int64_t)blockIdx.x * rpb), r1 = min(rows, r0 + rpb);
+    const int64_t total = (r1 - r0) * k;
+    float m = 0.0f;
+    for (int64_t i = threadIdx.x; i < total; i += kFusedThreads) {
+      const int64_t r = r0 + i / k;
+      const int j = (int)(i % k);
+      int c = s_sel[j];
+      if (!QDBG(c >= 0 && c < cols)) c = 0;
+      const float xv = __bfloat162float(x[r * ldx + c]);
+      const BlockScale bs =
+          block_scale_from_byte(__ldcg(scales + sf_offset(layout, r, c >> 4, ncols16)), s_t);
+      float v[8] = {__fmul_rn(xv, bs.r), 0, 0, 0, 0, 0, 0, 0};
+      const uint32_t code = bs.zero ? 0u : (f32x8_to_e2m1(v) & 15u);
+      const float R = __fsub_rn(xv, __fmul_rn(e2m1_to_f32(code), bs.d));
+      rs[r * k + j] = R;
+      m = fmaxf(m, fabsf(R));
+    }
+    m = warp_max(m);
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+      float v = lane < NW ? red[lane] : 0.0f;
+      v = warp_max(v);
+      if (lane == 0 && v > 0.0f) atomicMax(&ctl->amax_r, __float_as_uint(v));
+    }
+  }
+  if (!grid_barrier(ctl, tmo, &g_quant_error)) return;
+
+  // ---- E: second quantization of this block's rows of R_sel (own tensor scale)
+  {
+    const float rs_t = tensor_scale_from_amax(__uint_as_float(*reinterpret_cast<volatile uint32_t*>(&ctl->amax_r)));
+    if (blockIdx.x == 0 && threadIdx.x == 0) rst[0] = rs_t;
+    const int rcols16 = kpad >> 4;
+    const int vpr = kpad >> 3;   // 8-element vectors per residual row (even)
+    const int64_t rpb = (rows + gridDim.x - 1) / gridDim.x;
+    const int64_t r0 = min(rows, (int64_t)blockIdx.x * rpb), r1 = min(rows, r0 + rpb);
+    const int64_t nvec = (r1 - r0) * vpr;
+    // warp-uniform loop: lanes 2i / 2i+1 hold the two halves of one 16-block
+    for (int64_t base = (int64_t)warp * 32; base < nvec; base += kFusedThreads) {
+      const int64_t i = base + lane;
+      const bool in = i < nvec;
+      const int64_t r = r0 + (in ? i / vpr : 0);
+      const int col = in ? (int)(i % vpr) * 8 : 0;
+      const bool live = in && col < k;
+      float f[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) f[jj] = 0.0f;
+      if (live) {
+        const float4* pp = reinterpret_cast<const float4*>(rs + r * k + col);
+        const float4 a = __ldcg(pp), b = __ldcg(pp + 1);
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+      }
+      float mm = 0.0f;
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) mm = fmaxf(mm, fabsf(f[jj]));
+      mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, 1));
+      const BlockScale bs = block_scale(mm, rs_t);
+      uint32_t cw = quantize8(f, bs);
+      uint32_t sbyte = bs.byte;
+      if (!live) { cw = 0u; sbyte = 0u; }
+      if (in) {
+        *reinterpret_cast<uint32_t*>(rcodes + r * (kpad >> 1) + (col >> 1)) = cw;
+        if (((col >> 3) & 1) == 0) rscales[sf_offset(rlayout, r, col >> 4, rcols16)] = (uint8_t)sbyte;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- TRACE
 // Signed level index of an E2M1 code: the 3 magnitude bits are the index of
 // the level among {0, .5, 1, 1.5, 2, 3, 4, 6}; negative codes count down, and
@@ -995,25 +1241,21 @@ static quads_status_t quantize_impl(
     const int64_t start = (rows / 128) * (ncols16 / 4) * 512;
     cudaMemsetAsync(scales + start, 0, (size_t)(sf_tc_bytes(rows, cols) - start), st);
   }
-  // one warp per (32-row chunk, 256-column slab) task, eight warps per block
-  const int64_t ntasks = ((rows + 31) / 32) * ((cols + 255) / 256);
-  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((ntasks + 7) / 8, (int64_t)num_sms() * 8));
-  // four consecutive block scales of a row are contiguous (and word-aligned)
-  // in both layouts when cols % 64 == 0
-  const int sf_words = (cols % 64 == 0 && ((uintptr_t)scales & 3u) == 0) ? 1 : 0;
+  const int64_t ntasks = ((rows + 31) / 32) * ((cols + 255) / 256);  // one block per task
+  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(ntasks, (int64_t)num_sms() * 16));
   const __nv_bfloat16* xb = (const __nv_bfloat16*)x;
   if (qdq)
     quantize_kernel<false, true><<<blocks, 256, 0, st>>>(
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
-        codes, ld_codes, scales, scale_layout, sf_words, nullptr, qdq, ldq);
+        codes, ld_codes, scales, scale_layout, nullptr, qdq, ldq);
   else if (score_partials)
     quantize_kernel<true, false><<<blocks, 256, 0, st>>>(
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
-        codes, ld_codes, scales, scale_layout, sf_words, score_partials, nullptr, 0);
+        codes, ld_codes, scales, scale_layout, score_partials, nullptr, 0);
   else
     quantize_kernel<false, false><<<blocks, 256, 0, st>>>(
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
-        codes, ld_codes, scales, scale_layout, sf_words, nullptr, nullptr, 0);
+        codes, ld_codes, scales, scale_layout, nullptr, nullptr, 0);
   return check_launch(qdq ? "qdq" : "quantize", launched);
 }
 
@@ -1128,6 +1370,79 @@ extern "C" quads_status_t quads_select_residual_channels(
   rsel_quantize_kernel<<<grid_for(rows * (kpad / 8), 256), 256, 0, st>>>(
       rs, rows, k, kpad, group_offsets, G, amax, r_codes, r_scales, r_scale_layout, r_tensor_scale);
   return check_launch("select", long_groups ? 4 : 3);
+}
+
+extern "C" quads_status_t quads_quantize_select_nvfp4(
+    const void* x, int64_t rows, int64_t cols, int64_t ldx, int32_t k, uint8_t* codes,
+    int64_t ld_codes, uint8_t* scales, int32_t scale_layout, float* tensor_scale_out, int32_t* sel,
+    float* scores_out, uint8_t* r_codes, uint8_t* r_scales, int32_t r_scale_layout,
+    float* r_tensor_scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (rows > 0 && (!x || !codes || !scales || !tensor_scale_out || !sel || !r_codes || !r_scales ||
+                   !r_tensor_scale))
+    return fail(QUADS_ERR_INVALID_ARG, "quantize_select: null pointer argument");
+  if (rows < 0 || cols <= 0 || cols % 16 || cols > 8192)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "quantize_select: cols=%lld must be a multiple of 16 and <= 8192", (long long)cols);
+  if (k <= 0 || k % 16 || k > cols || k > kFusedMaxK)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "quantize_select: k=%d must be a multiple of 16 in [16, min(cols, %d)]", k, kFusedMaxK);
+  if ((scale_layout != QUADS_SCALES_LINEAR && scale_layout != QUADS_SCALES_TCGEN05) ||
+      (r_scale_layout != QUADS_SCALES_LINEAR && r_scale_layout != QUADS_SCALES_TCGEN05))
+    return fail(QUADS_ERR_INVALID_ARG, "quantize_select: bad scale layout");
+  if (scale_layout == QUADS_SCALES_TCGEN05 && cols % 64)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "quantize_select: TCGEN05 scale layout needs cols %% 64 == 0");
+  if (ldx < cols || ldx % 8 || ld_codes < cols / 2 || ld_codes % 4 || !aligned16(x) ||
+      !aligned16(codes))
+    return fail(QUADS_ERR_MISALIGNED, "quantize_select: x and codes 16-byte aligned, ldx >= cols (%% 8), ld_codes >= cols/2 (%% 4)");
+  const size_t need = quads_workspace_size(QUADS_OP_QUANTIZE_SELECT, rows, cols, 0, k, 1);
+  if (rows > 0 && (!workspace || workspace_bytes < need))
+    return fail(QUADS_ERR_WORKSPACE, "quantize_select: workspace needs %zu bytes", need);
+  if (rows == 0) return QUADS_OK;
+  const int kpad = quads_kpad(k);
+  cudaStream_t st = (cudaStream_t)stream;
+  char* ws = (char*)workspace;
+  auto al = [](size_t b) { return (b + 255) & ~(size_t)255; };
+  FusedCtl* ctl = (FusedCtl*)ws;
+  float* partials = (float*)(ws + 256);
+  float* scores = (float*)(ws + 256 + al((size_t)((rows + 31) / 32) * cols * 4));
+  float* rs = (float*)((char*)scores + al((size_t)cols * 4));
+  if (scores_out) scores = scores_out;
+  cudaMemsetAsync(ctl, 0, sizeof(FusedCtl), st);
+  if (scale_layout == QUADS_SCALES_TCGEN05 && rows % 128) {
+    const int64_t start = (rows / 128) * (cols / 64) * 512;
+    cudaMemsetAsync(scales + start, 0, (size_t)(sf_tc_bytes(rows, cols) - start), st);
+  }
+  if (r_scale_layout == QUADS_SCALES_TCGEN05 && rows % 128) {
+    const int64_t start = (rows / 128) * (kpad / 64) * 512;
+    cudaMemsetAsync(r_scales + start, 0, (size_t)(sf_tc_bytes(rows, kpad) - start), st);
+  }
+  auto kernel = cols <= 2048 ? quantize_select_kernel<8>
+                : cols <= 4096 ? quantize_select_kernel<16>
+                               : quantize_select_kernel<32>;
+  // every block must be resident at once (grid-wide barriers): one per SM
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kFusedThreads, 0);
+  if (e != cudaSuccess || per_sm < 1)
+    return fail(QUADS_ERR_CUDA, "quantize_select: occupancy query: %s", cudaGetErrorString(e));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeCooperative;
+  at.val.cooperative = 1;
+  // several small blocks per SM (the quantization phase needs the warps to
+  // hide its load latency), all resident at once
+  cfg.gridDim = dim3((unsigned)(num_sms() * std::min(per_sm, 4)), 1, 1);
+  cfg.blockDim = dim3(kFusedThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, (const __nv_bfloat16*)x, rows, (int)cols, ldx, codes,
+                         ld_codes, scales, (int)scale_layout, tensor_scale_out, partials,
+                         scores, (int)k, kpad, sel, rs, r_codes, r_scales, (int)r_scale_layout,
+                         r_tensor_scale, ctl, 2000000000ull);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(QUADS_ERR_CUDA, "quantize_select: cooperative launch: %s", cudaGetErrorString(e));
+  }
+  return check_launch("quantize_select", 1);
 }
 
 extern "C" quads_status_t quads_trace_round(const void* x_train, int64_t rows, int64_t cols,

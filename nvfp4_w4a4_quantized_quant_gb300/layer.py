@@ -85,11 +85,17 @@ class MoEExpertLayer:
     residual compensation on both GEMMs."""
 
     def __init__(self, w1: torch.Tensor, w2: torch.Tensor, topk: int, k1: int, k2: int,
-                 max_tokens: int, compensate: bool = True):
+                 max_tokens: int, compensate: bool = True, fused_activation_side: bool = False):
+        """fused_activation_side: GEMM1's activation side (quantization,
+        selection, R_sel) as one cooperative launch (quantize_select_nvfp4)
+        instead of the quantizer and the selection call.  Off by default: the
+        cooperative grid holds every SM while it runs, so the routing on the
+        side stream cannot overlap it."""
         self.E, twoF, self.H = w1.shape
         self.F = twoF // 2
         assert w2.shape == (self.E, self.H, self.F)
         self.topk, self.k1, self.k2, self.compensate = topk, k1, k2, compensate
+        self.fused = fused_activation_side
         dev = w1.device
         self.w1q = Q.quantize_expert_weights(w1, swiglu_interleave=True)
         self.w2q = Q.quantize_expert_weights(w2)
@@ -124,6 +130,7 @@ class MoEExpertLayer:
             rt=e(Q.workspace_size(Q.OP_MOE_ROUTE, T, E, 0, topk)),
             q1=e(Q.workspace_size(Q.OP_QUANTIZE, T, H)),
             s1=e(Q.workspace_size(Q.OP_SELECT, T, H, 0, k1)),
+            qs1=e(Q.workspace_size(Q.OP_QUANTIZE_SELECT, T, H, 0, k1) if fused_activation_side else 16),
             q2=e(Q.workspace_size(Q.OP_QUANTIZE, cap, F, 0, 0, E)),
             s2=e(Q.workspace_size(Q.OP_SELECT, cap, F, 0, k2, E)),
         )
@@ -152,17 +159,26 @@ class MoEExpertLayer:
         self.side.wait_event(self.ev_fork)
         plan = Q.moe_route(logits, self.topk, rows_capacity=self.cap, out=b["route"],
                            workspace=ws["rt"], stream=self.side)
-        xq, xpart = Q.quantize_nvfp4(x, scores=comp, workspace=ws["q1"], stream=stream,
-                                     out=(b["xc"], b["xs"], b["xts"], b["xpart"] if comp else None))
+        r1 = sel1 = w1sel = xr = None
+        if comp and self.fused:
+            # X's activation side in one cooperative launch: quantization,
+            # channel scores, top-k and the second quantization of R_sel
+            xq, sel1, _, xr = Q.quantize_select_nvfp4(
+                x, self.k1, workspace=ws["qs1"], stream=stream,
+                out=(b["xc"], b["xs"], b["xts"], b["sel1"], b["r1c"], b["r1s"], b["r1ts"]))
+            self.ev_sel1.record(main)
+        else:
+            xq, xpart = Q.quantize_nvfp4(x, scores=comp, workspace=ws["q1"], stream=stream,
+                                         out=(b["xc"], b["xs"], b["xts"], b["xpart"] if comp else None))
         self.ev_xq.record(main)
         self.side.wait_event(self.ev_xq)
         a1 = Q.moe_gather(plan, xq, out=(b["a1c"], b["a1s"]), stream=self.side)
         self.ev_a1.record(self.side)
-        r1 = sel1 = w1sel = None
-        if comp:
+        if comp and not self.fused:
             sel1, _, xr = Q.select_residual_channels(x, xq, xpart, self.k1, workspace=ws["s1"],
                                                      sel_ready_event=self.ev_sel1, stream=stream,
                                                      out=(b["sel1"], b["r1c"], b["r1s"], b["r1ts"]))
+        if comp:
             self.wside.wait_event(self.ev_sel1)
             w1sel = Q.select_weight_channels(self.w1q, sel1, self.k1, E, stream=self.wside,
                                              out=(b["w1sc"], b["w1ss"]))

@@ -20,7 +20,7 @@ from .build import DEBUG_LIB, LIB, ROOT
 LINEAR, TCGEN05 = 0, 1
 OUT_F32, OUT_BF16 = 0, 1
 EPI_NONE, EPI_SWIGLU = 0, 1
-OP_QUANTIZE, OP_SELECT, OP_GEMM, OP_MOE_GEMM, OP_MOE_ROUTE = 0, 1, 2, 3, 4
+OP_QUANTIZE, OP_SELECT, OP_GEMM, OP_MOE_GEMM, OP_MOE_ROUTE, OP_QUANTIZE_SELECT = 0, 1, 2, 3, 4, 5
 SCORE_CHUNK_ROWS = 32
 MOE_ROW_ALIGN = 128
 
@@ -33,6 +33,7 @@ _SIGS = {
     "quads_last_error_detail": (ctypes.c_char_p, []),
     "quads_device_status": (_I32, [_P, ctypes.POINTER(_I32)]),
     "quads_test_gemm_wait_timeout": (None, [_I32]),
+    "quads_test_gemm_timeline": (None, [_P]),
     "quads_workspace_size": (_SZ, [_I32, _I64, _I64, _I64, _I32, _I32]),
     "quads_kpad": (_I32, [_I32]),
     "quads_quantize_nvfp4": (_I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P, _I64, _P,
@@ -43,6 +44,8 @@ _SIGS = {
                                               _I32, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P, _P]),
     "quads_select_residual_channels_noalloc": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _I32, _P,
                                                       _P, _I32, _P, _P, _P, _P, _I32, _P, _P]),
+    "quads_quantize_select_nvfp4": (_I32, [_P, _I64, _I64, _I64, _I32, _P, _I64, _P, _I32, _P, _P,
+                                           _P, _P, _P, _I32, _P, _P, _SZ, _P]),
     "quads_w4a4_gemm_comp": (_I32, [_I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                     _P, _P, _P, _P, _I32, _P, _I32, _I64, _P, _SZ, _P]),
     "quads_moe_grouped_gemm": (_I32, [_I32, _I64, _I64, _I64, _P, _P, _P, _P, _P, _I32, _P, _P,
@@ -74,10 +77,11 @@ def header_symbols() -> list[str]:
 
 def load(path: Optional[str] = None):
     """Load libquads.so (no CUDA device needed for loading); the bounds-checked
-    build when QUADS_DEBUG_LIB=1."""
+    build when QUADS_DEBUG_LIB=1, or the library at QUADS_LIB when set."""
     global _lib
     if path is None:
-        path = DEBUG_LIB if os.environ.get("QUADS_DEBUG_LIB") == "1" else LIB
+        path = os.environ.get("QUADS_LIB") or (
+            DEBUG_LIB if os.environ.get("QUADS_DEBUG_LIB") == "1" else LIB)
     if _lib is None:
         if not os.path.exists(path):
             raise RuntimeError(f"libquads is not built ({path}); run "
@@ -156,6 +160,13 @@ def test_gemm_wait_timeout(enable: bool = True) -> None:
     """Test hook: the next GEMM launch runs with a 1 ms wait limit and an MMA
     issuer that issues nothing, so that its bounded waits run out."""
     load().quads_test_gemm_wait_timeout(1 if enable else 0)
+
+
+def test_gemm_timeline(buf: torch.Tensor) -> None:
+    """Profiling hook: the next GEMM launch writes its first CTA's stage
+    timeline (int64 [7, 64], %globaltimer ns) into `buf`."""
+    assert buf.dtype == torch.int64 and buf.numel() >= 7 * 64 and buf.is_cuda
+    load().quads_test_gemm_timeline(_ptr(buf))
 
 
 @dataclass
@@ -237,6 +248,39 @@ def _event(ev, stream):
     if not ev.cuda_event:
         ev.record(_torch_stream(stream))
     return ctypes.c_void_p(ev.cuda_event)
+
+
+def quantize_select_nvfp4(x: torch.Tensor, k: int, *, scale_layout: int = LINEAR,
+                          r_scale_layout: int = LINEAR, want_scores: bool = False,
+                          workspace=None, out=None, stream=None):
+    """quantize_nvfp4 (tensor scale from the amax, one group) and
+    select_residual_channels in one cooperative launch.
+    -> (QTensor of Q(X), sel int32 [1, k], scores [1, cols] or None, QTensor of Q(R_sel))."""
+    lib = load()
+    assert x.dtype == torch.bfloat16 and x.dim() == 2
+    rows, cols = x.shape
+    kp = kpad(k)
+    dev = x.device
+    if out is None:
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+        nsf = sf_tc_bytes(rows, cols) if scale_layout == TCGEN05 else rows * (cols // 16)
+        scales = torch.empty(nsf, dtype=torch.uint8, device=dev)
+        ts = torch.empty(1, dtype=torch.float32, device=dev)
+        sel = torch.empty((1, k), dtype=torch.int32, device=dev)
+        rc = torch.empty((rows, kp // 2), dtype=torch.uint8, device=dev)
+        nrs = sf_tc_bytes(rows, kp) if r_scale_layout == TCGEN05 else rows * (kp // 16)
+        rs = torch.empty(nrs, dtype=torch.uint8, device=dev)
+        rts = torch.empty(1, dtype=torch.float32, device=dev)
+    else:
+        codes, scales, ts, sel, rc, rs, rts = out
+    sc = torch.empty((1, cols), dtype=torch.float32, device=dev) if want_scores else None
+    ws = _workspace(workspace_size(OP_QUANTIZE_SELECT, rows, cols, 0, k, 1), dev, workspace, stream)
+    _check(lib.quads_quantize_select_nvfp4(
+        _ptr(x), rows, cols, x.stride(0), k, _ptr(codes), codes.stride(0), _ptr(scales),
+        scale_layout, _ptr(ts), _ptr(sel), _ptr(sc), _ptr(rc), _ptr(rs), r_scale_layout, _ptr(rts),
+        _ptr(ws), ws.numel(), _stream(stream)), "quantize_select_nvfp4")
+    return (QTensor(codes, scales, ts, rows, cols, scale_layout), sel, sc,
+            QTensor(rc, rs, rts, rows, kp, r_scale_layout))
 
 
 def select_residual_channels(x: torch.Tensor, q: QTensor, partials: torch.Tensor, k: int, *,

@@ -195,3 +195,23 @@ def _check_plain_layer(lib, d, experts=None):
 def test_moe_layer_plain_w4a4(lib):
     d = inputs.moe_layer(2, tokens=300, hidden=512, experts=4, topk=2, ffn=256, k=64)
     _check_plain_layer(lib, d)
+
+
+def test_moe_layer_fused_activation_side_gives_the_same_outputs(lib):
+    """GEMM1's activation side as one cooperative launch gives the layer the
+    same outputs, bit for bit, as the quantizer and selection calls."""
+    from nvfp4_w4a4_quantized_quant_gb300.layer import MoEExpertLayer
+    d = inputs.moe_layer(2, tokens=300, hidden=512, experts=4, topk=2, ffn=256, k=64)
+    E, twoF, H = d["w1"].shape
+    w1 = bf16_tensor(d["w1"].reshape(E * twoF, H)).reshape(E, twoF, H)
+    w2 = bf16_tensor(d["w2"].reshape(E * H, twoF // 2)).reshape(E, H, twoF // 2)
+    x, lg = bf16_tensor(d["x"]), torch.from_numpy(d["logits"]).cuda()
+    res = []
+    for fused in (False, True):
+        layer = MoEExpertLayer(w1, w2, d["topk"], 64, 64, d["x"].shape[0], fused_activation_side=fused)
+        r = layer.forward(x, lg)
+        torch.cuda.synchronize()
+        assert lib.device_status() == 0
+        res.append({k: r[k].clone() for k in ("out", "h", "y")} | {"sel1": r["sel1"].clone()})
+    for k in res[0]:
+        assert torch.equal(res[0][k], res[1][k]), k

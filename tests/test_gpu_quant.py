@@ -316,3 +316,29 @@ def test_w4a16_qdq_full_expert_stack_sampled_experts(lib):
         assert ts[e] == ost[0]
         assert np.array_equal(y[rows].view(torch.int16).cpu().numpy().view(np.uint16), oy)
         assert np.array_equal(codes_np(q.codes[rows], H), oc)
+
+
+@pytest.mark.parametrize("rows,cols,k,layout", [(8192, 2048, 64, 0), (4096, 2048, 128, 1),
+                                                (300, 256, 16, 0), (77, 512, 64, 1)])
+def test_fused_quantize_select_matches_the_two_calls(lib, rows, cols, k, layout):
+    """The cooperative quantize + select kernel gives exactly the outputs of
+    quantize_nvfp4 (scores on) followed by select_residual_channels."""
+    rng = inputs.make_rng(rows + cols + k)
+    xf = inputs.student_t4(rng, (rows, cols))
+    xf[:, rng.choice(cols, max(1, cols // 100), replace=False)] *= np.float32(20.0)
+    x = bf16_tensor(inputs.f32_to_bf16_bits(xf))
+    q, part = lib.quantize_nvfp4(x, scores=True, scale_layout=layout)
+    sel, sc, r = lib.select_residual_channels(x, q, part, k, r_scale_layout=layout, want_scores=True)
+    fq, fsel, fsc, fr = lib.quantize_select_nvfp4(x, k, scale_layout=layout, r_scale_layout=layout,
+                                                  want_scores=True)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    assert torch.equal(fq.codes, q.codes) and torch.equal(fq.scales, q.scales)
+    assert torch.equal(fq.tensor_scale, q.tensor_scale)
+    assert torch.equal(fsc, sc) and torch.equal(fsel, sel)
+    assert torch.equal(fr.codes, r.codes) and torch.equal(fr.scales, r.scales)
+    assert torch.equal(fr.tensor_scale, r.tensor_scale)
+    if rows <= 300:
+        ref = Q.quantize_full(f32(inputs.f32_to_bf16_bits(xf)), k)
+        assert np.array_equal(fsel.cpu().numpy(), ref["sel"])
+        assert np.array_equal(codes_np(fr.codes, lib.kpad(k))[:, :k], ref["r_codes"])
