@@ -299,11 +299,19 @@ def secondary(torch, Q, steps, flush, stream):
                                                 tensor_scale_in=qo.tensor_scale,
                                                 out=(qo.codes, qo.scales, qo.tensor_scale, po),
                                                 stream=stream))
+        # plain quantization (no residual-energy partials), tensor scale given
+        ms0 = graph_ms(lambda: Q.quantize_nvfp4(xq_in, workspace=wsq,
+                                                tensor_scale_in=qo.tensor_scale,
+                                                out=(qo.codes, qo.scales, qo.tensor_scale, None),
+                                                stream=stream))
         qb = rows_q * Hq * (2 + 0.5 + 1.0 / 16) + (rows_q // 32) * Hq * 4
+        qb0 = rows_q * Hq * (2 + 0.5 + 1.0 / 16)
         sweep.append({"rows": rows_q, "cols": Hq, "input_mib": rows_q * Hq * 2 >> 20,
                       "ms": round(ms, 4), "gbs": round(qb / (ms * 1e-3) / 1e9, 1),
                       "ms_scale_given": round(ms1, 4),
-                      "gbs_scale_given": round(qb / (ms1 * 1e-3) / 1e9, 1)})
+                      "gbs_scale_given": round(qb / (ms1 * 1e-3) / 1e9, 1),
+                      "ms_no_scores_scale_given": round(ms0, 4),
+                      "gbs_no_scores_scale_given": round(qb0 / (ms0 * 1e-3) / 1e9, 1)})
         del xq_in, wsq, qo, po
     out["quantizer_sweep"] = sweep
 
@@ -541,6 +549,7 @@ def run_gpu(args):
         for row in sec["quantizer_sweep"]:
             row["frac_hbm"] = round(row["gbs"] / pk["hbm"], 4)
             row["frac_hbm_scale_given"] = round(row["gbs_scale_given"] / pk["hbm"], 4)
+            row["frac_hbm_no_scores_scale_given"] = round(row["gbs_no_scores_scale_given"] / pk["hbm"], 4)
     fl = moe_flops()
     value = world * fl / (ms * 1e-3) / 1e12
     e2e_val = world * fl / (e_ms * 1e-3) / 1e12

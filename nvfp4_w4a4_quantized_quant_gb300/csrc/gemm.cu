@@ -39,10 +39,9 @@
 // TMEM columns: acc1 double-buffered (0-127, 128-255), acc2 (256-383),
 // scale-factor ring (384-511, 2 buffers x 64 columns).
 // Every mbarrier wait is bounded (2 s); on a timeout the kernel latches an
-// error word and every role stops.  Each producer warp then waits (bounded)
-// for its own copies in flight -- its per-stage barriers count its copies only,
-// so they complete whatever the other roles did -- the MMA and scale warps
-// commit and wait for their tensor-core work, and TMEM is released.
+// error word and every role stops.  Each producer warp then waits a fixed
+// bounded time (200 us) for its copies in flight, the MMA and scale warps
+// commit and wait (bounded) for their tensor-core work, and TMEM is released.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -101,7 +100,6 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + META_BYTES + 1024 /*align*/;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per wait
 // the stage's copies dealt to the producer warps: warp w issues [first, first + count)
 __host__ __device__ constexpr int copies_first(int w) { return w * COPIES / PRODUCERS; }
-__host__ __device__ constexpr int copies_of(int w) { return copies_first(w + 1) - copies_first(w); }
 
 enum { OUT_F32 = 0, OUT_BF16 = 1, OUT_SWIGLU = 2 };
 
@@ -302,6 +300,7 @@ __device__ __forceinline__ void tc_wait_ld() {
 
 // ---------------------------------------------------------------- bounded waits
 constexpr unsigned long long kDrainNs = 50000000ull;   // bound on waits for work in flight after an abort
+constexpr unsigned long long kCopyDrainNs = 200000ull;  // producers' wait for their copies after an abort
 
 struct Sync {
   volatile int* abort_flag;
@@ -462,8 +461,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES);
-  uint64_t* fullw = bars;                          // [PRODUCERS][STAGES]: each producer's copies
-  uint64_t* empty = fullw + PRODUCERS * STAGES;    // [STAGES]
+  uint64_t* full = bars;                           // [STAGES]
+  uint64_t* empty = full + STAGES;                 // [STAGES]
   uint64_t* sf_ready = empty + STAGES;             // [SF_BUFS]
   uint64_t* acc_full = sf_ready + SF_BUFS;         // [2]
   uint64_t* acc_empty = acc_full + 2;              // [2]
@@ -491,9 +490,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0 && p.row_off) meta.off[p.E] = p.row_off[p.E];
 
   if (threadIdx.x == 0) {
-    for (int w = 0; w < PRODUCERS; ++w)
-      for (int i = 0; i < STAGES; ++i) mbar_init(&fullw[w * STAGES + i], copies_of(w));
-    for (int i = 0; i < STAGES; ++i) mbar_init(&empty[i], 1);
+    for (int i = 0; i < STAGES; ++i) { mbar_init(&full[i], COPIES); mbar_init(&empty[i], 1); }
     for (int i = 0; i < SF_BUFS; ++i) mbar_init(&sf_ready[i], SF_WARPS);
     for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], EPI_THREADS); }
     mbar_init(drain_mma, 1);
@@ -535,7 +532,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // stay warp-uniform); one elected lane issues.
     const int b_lo = copies_first(warp);
     const int b_hi = copies_first(warp + 1);
-    uint64_t* full = fullw + warp * STAGES;   // this warp's own barriers
     uint32_t it = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
@@ -594,11 +590,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     if (!ok && lane == 0) {
-      // every copy this warp issued (at most the last STAGES iterations can
-      // still be in flight) lands before the CTA can exit: the barriers count
-      // this warp's copies only, so they complete whatever the others did
-      const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
-      for (uint32_t j = first; j < it; ++j) wait1(&full[j % STAGES], (j / STAGES) & 1, dr, false, true);
+      // the copies this warp issued land before the CTA can exit.  A stage's
+      // barrier may never complete once another producer stopped before its
+      // share, so the wait is a fixed bounded time (copies from L2 or HBM take
+      // microseconds)
+      const unsigned long long t0 = global_ns();
+      while (global_ns() - t0 < kCopyDrainNs) {
+      }
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
@@ -674,8 +672,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       for (int kt = 0; kt < KT + KTc; ++kt, ++it) {
-        bool okw = true;
-        for (int w2 = 0; w2 < PRODUCERS && okw; ++w2) okw = conv_wait(&fullw[w2 * STAGES + s], ph, sy);
+        bool okw = conv_wait(&full[s], ph, sy);
         if (okw && it >= (uint32_t)SF_BUFS) {
           const uint32_t prev = it - SF_BUFS;
           okw = conv_wait(&empty[prev % STAGES], (prev / STAGES) & 1, sy);
