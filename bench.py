@@ -620,7 +620,11 @@ def run_profile(args):
     for an ncu launch list or a single-kernel capture:
       moe     the MoE expert layer step (8192 tokens)
       dense   the compensated dense projection 4096x2048 x 6144x2048, k = 128
-      decode  the MoE expert layer on 512 tokens"""
+      decode  the MoE expert layer on 512 tokens
+      streams the streaming kernels: TRACE rounding, record packing and 1-bit
+              rounding on 16384x2048; quantization of 8192x2048 with score
+              partials (amax + quantize); plain quantization of 262144x2048
+              with the tensor scale given"""
     import numpy as np
     import torch
     from nvfp4_w4a4_quantized_quant_gb300 import inputs
@@ -634,6 +638,32 @@ def run_profile(args):
         w = torch.from_numpy(d["w"].view(np.int16)).view(torch.bfloat16).cuda()
         lin = CompensatedLinear(w, 128, x.shape[0])
         step = lambda: lin.forward(x)  # noqa: E731
+    elif args.profile == "streams":
+        t = inputs.trace_rounding(0)
+        xr = torch.from_numpy(t["x_rollout"].view(np.int16)).view(torch.bfloat16).cuda()
+        xt = torch.from_numpy(t["x_train"].view(np.int16)).view(torch.bfloat16).cuda()
+        rq, _ = Q.quantize_nvfp4(xr)
+        codes = torch.empty((xt.shape[0], xt.shape[1] // 2), dtype=torch.uint8, device="cuda")
+        cnt = torch.zeros(3, dtype=torch.int64, device="cuda")
+        bits = Q.trace_pack_record(rq)
+        cnt1 = torch.zeros(2, dtype=torch.int64, device="cuda")
+        g = torch.Generator(device="cuda")
+        g.manual_seed(3)
+        xs = torch.randn((8192, 2048), generator=g, device="cuda").to(torch.bfloat16)
+        xl = torch.randn((262144, 2048), generator=g, device="cuda").to(torch.bfloat16)
+        ws = torch.empty(Q.workspace_size(Q.OP_QUANTIZE, 262144, 2048), dtype=torch.uint8,
+                         device="cuda")
+        qs, ps = Q.quantize_nvfp4(xs, scores=True, workspace=ws)
+        ql, _ = Q.quantize_nvfp4(xl, workspace=ws)
+
+        def step():
+            Q.trace_round(xt, rq, counters=cnt, out=codes)
+            Q.trace_pack_record(rq, out=bits)
+            Q.trace_round_1bit(xt, bits, rq, counters=cnt1, out=codes)
+            Q.quantize_nvfp4(xs, scores=True, workspace=ws,
+                             out=(qs.codes, qs.scales, qs.tensor_scale, ps))
+            Q.quantize_nvfp4(xl, workspace=ws, tensor_scale_in=ql.tensor_scale,
+                             out=(ql.codes, ql.scales, ql.tensor_scale, None))
     else:
         w = dict(WORKLOAD, tokens=512) if args.profile == "decode" else WORKLOAD
         d = inputs.moe_layer(0, tokens=w["tokens"], hidden=w["hidden"], experts=w["experts"],
@@ -689,8 +719,9 @@ def main():
     ap.add_argument("--impl", default="libquads", choices=["libquads", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", nargs="?", const="moe", default=None,
-                    choices=["moe", "dense", "decode"],
-                    help="eager steps only (MoE step, dense projection or decode layer), for ncu")
+                    choices=["moe", "dense", "decode", "streams"],
+                    help="eager steps only (MoE step, dense projection, decode layer or the "
+                         "streaming kernels), for ncu")
     args = ap.parse_args()
     if args.warmup < 3 and not args.profile:
         args.warmup = 3

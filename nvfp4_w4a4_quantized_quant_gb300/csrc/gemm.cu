@@ -256,6 +256,36 @@ __device__ __forceinline__ void tc_mma_mx_el(uint32_t d, uint64_t a, uint64_t b,
       " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb));
 }
+// A whole 512-element K stage (eight K = 64 MMAs over two 128-byte sub-tiles
+// of A and B, 16 KB apart) issued by one elected lane in straight-line code:
+// one elect for the eight MMAs (an elect per MMA costs about as much issue
+// time as the MMA itself).  Descriptor start addresses advance by 32 bytes
+// per K step (2 in descriptor units) and by a sub-tile (1024) after four;
+// the scale columns advance by 4 per K step.
+__device__ __forceinline__ void tc_mma_stage8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 a1, b1;\n\t.reg .b32 fa, fb;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\tadd.u32 fa, %5, 4;\n\tadd.u32 fb, %6, 4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [fa], [fb], 1;\n\t"
+      "add.s64 a1, %1, 4;\n\tadd.s64 b1, %2, 4;\n\tadd.u32 fa, %5, 8;\n\tadd.u32 fb, %6, 8;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [fa], [fb], 1;\n\t"
+      "add.s64 a1, %1, 6;\n\tadd.s64 b1, %2, 6;\n\tadd.u32 fa, %5, 12;\n\tadd.u32 fb, %6, 12;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [fa], [fb], 1;\n\t"
+      "add.s64 a1, %1, 1024;\n\tadd.s64 b1, %2, 1024;\n\tadd.u32 fa, %5, 16;\n\tadd.u32 fb, %6, 16;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [fa], [fb], 1;\n\t"
+      "add.s64 a1, %1, 1026;\n\tadd.s64 b1, %2, 1026;\n\tadd.u32 fa, %5, 20;\n\tadd.u32 fb, %6, 20;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [fa], [fb], 1;\n\t"
+      "add.s64 a1, %1, 1028;\n\tadd.s64 b1, %2, 1028;\n\tadd.u32 fa, %5, 24;\n\tadd.u32 fb, %6, 24;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [fa], [fb], 1;\n\t"
+      "add.s64 a1, %1, 1030;\n\tadd.s64 b1, %2, 1030;\n\tadd.u32 fa, %5, 28;\n\tadd.u32 fb, %6, 28;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [fa], [fb], 1;\n\t"
+      "}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb));
+}
 __device__ __forceinline__ void tc_commit_el(uint64_t* b) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
@@ -280,6 +310,22 @@ __device__ __forceinline__ void tc_cp_sf_el(uint32_t taddr, uint64_t sdesc) {
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
       "l"(sdesc)
+      : "memory");
+}
+// Scale atoms of two consecutive K steps (A and B) in one elected block:
+// atom q to columns t, atom q+1 to t+4; B's atoms 32 columns further.  An
+// atom descriptor advances by 512 bytes (32 in descriptor units) per K step.
+__device__ __forceinline__ void tc_cp_sf_pair_el(uint32_t t, uint64_t da, uint64_t db) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b64 a1, b1;\n\t.reg .b32 t1, t2, t3;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "add.s64 a1, %1, 32;\n\tadd.s64 b1, %2, 32;\n\t"
+      "add.u32 t1, %0, 4;\n\tadd.u32 t2, %0, 32;\n\tadd.u32 t3, %0, 36;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [t1], a1;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [t2], %2;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [t3], b1;\n\t}" ::"r"(t),
+      "l"(da), "l"(db)
       : "memory");
 }
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, float* v) {
@@ -638,6 +684,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                          tsf + (q >> 1) * 4, tsf + 4 * KSTEPS + (q >> 1) * 4,
                          (kk > 0 || q > 0) ? 1u : 0u);
           }
+        } else if (KSTEPS == 8 && ksteps == 8) {
+          tc_mma_stage8(dcol, desc_sw128(sa), desc_sw128(sbb), idesc, tsf, tsf + 4 * KSTEPS,
+                        kk > 0 ? 1u : 0u);
         } else {
           for (int q = 0; q < ksteps; ++q) {
             const uint32_t off = (q >> 2) * A_SUB + (q & 3) * 32;
@@ -695,6 +744,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_cp_sf_el(tsf + w * 4, desc_sf(ssf + w * 512));
             tc_cp_sf_el(tsf + 4 * KSTEPS + w * 4, desc_sf(ssf + SF_TILE + w * 512));
           }
+        } else if (KSTEPS == 2 * SF_WARPS && 4 * KSTEPS == 32 && 2 * w + 1 < ksteps) {
+          const int q = 2 * w;
+          tc_cp_sf_pair_el(tsf + q * 4, desc_sf(ssf + q * 512), desc_sf(ssf + SF_TILE + q * 512));
         } else {
 #pragma unroll
           for (int i = 0; i < KSTEPS / SF_WARPS; ++i) {
@@ -938,6 +990,7 @@ struct Params {
   int skip_mma;                 // test hook: the MMA warp issues nothing (waits then run out)
   // extents for the bounds-checked build: scale buffer bytes and output rows
   int64_t a_sf_bytes, b_sf_bytes, r_sf_bytes, ws_sf_bytes, y_rows;
+  unsigned long long* trace;    // nullable: stage timeline of the first pair's leader
 };
 
 __device__ __forceinline__ void mma_nvf4_cg2(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
@@ -959,6 +1012,41 @@ __device__ __forceinline__ void mma_mxf4_cg2(uint32_t d, uint64_t a, uint64_t b,
       "@e tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X"
       " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb));
+}
+// The four K = 64 MMAs of one 256-element sub-tile under one elect (see
+// tc_mma_stage8): descriptors +2 per K step, scale columns +4.
+__device__ __forceinline__ void mma_nvf4_cg2_x4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                                uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 a1, b1;\n\t.reg .b32 fa, fb;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\tadd.u32 fa, %5, 4;\n\tadd.u32 fb, %6, 4;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [fa], [fb], 1;\n\t"
+      "add.s64 a1, %1, 4;\n\tadd.s64 b1, %2, 4;\n\tadd.u32 fa, %5, 8;\n\tadd.u32 fb, %6, 8;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [fa], [fb], 1;\n\t"
+      "add.s64 a1, %1, 6;\n\tadd.s64 b1, %2, 6;\n\tadd.u32 fa, %5, 12;\n\tadd.u32 fb, %6, 12;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [fa], [fb], 1;\n\t"
+      "}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb));
+}
+// Four scale atoms of A (columns ta + 4a) and four of B (tb + 4a), atom
+// descriptors +32 per atom, under one elect.
+__device__ __forceinline__ void cp_sf_cg2_x4(uint32_t ta, uint32_t tb, uint64_t da, uint64_t db) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b64 x;\n\t.reg .b32 t;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %2;\n\t"
+      "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%1], %3;\n\t"
+      "add.s64 x, %2, 32;\n\tadd.u32 t, %0, 4;\n\t@e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], x;\n\t"
+      "add.s64 x, %3, 32;\n\tadd.u32 t, %1, 4;\n\t@e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], x;\n\t"
+      "add.s64 x, %2, 64;\n\tadd.u32 t, %0, 8;\n\t@e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], x;\n\t"
+      "add.s64 x, %3, 64;\n\tadd.u32 t, %1, 8;\n\t@e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], x;\n\t"
+      "add.s64 x, %2, 96;\n\tadd.u32 t, %0, 12;\n\t@e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], x;\n\t"
+      "add.s64 x, %3, 96;\n\tadd.u32 t, %1, 12;\n\t@e tcgen05.cp.cta_group::2.32x128b.warpx4 [t], x;\n\t}"
+      ::"r"(ta), "r"(tb), "l"(da), "l"(db)
+      : "memory");
 }
 // Commit of the executing thread's earlier tcgen05 work: arrive on the
 // barrier at the same offset in every CTA of `mask`.
@@ -1174,6 +1262,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
         if (!warp_wait(&empty[s], ph ^ 1, sy)) { ok = false; break; }
+        if (warp == 0) trace_mark(p.trace, 0, it);
         uint8_t* st = smem + s * STAGE_BYTES;
         const uint32_t bar = full0 + 8u * s;
         if (elect_one()) {
@@ -1229,7 +1318,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == MMA_WARP && leader) {
     // ---------------------------------------------------------- MMA issuer
     const uint32_t idesc = idesc_nvf4(2 * BM, BN);
-    uint32_t s = 0, sb = 0, sph = 0, j = 0;
+    uint32_t s = 0, sb = 0, sph = 0, j = 0, mit = 0;
     bool ok = !p.skip_mma;
     for (int64_t t = cid; t < ntiles && ok; t += ncl, ++j) {
       const uint32_t b = j & 1;
@@ -1237,6 +1326,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       for (int kt = 0; kt < nst; ++kt) {
         if (!conv_wait(&sf_ready[sb], sph, sy)) { ok = false; break; }
+        trace_mark(p.trace, 3, mit);
         tc_fence_after();
         const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
         const uint32_t tsf = tmem + SF_COL + sb * SF_BUF_COLS;
@@ -1252,6 +1342,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t dcol = sub.corr ? (tmem + ACC2_COL) : (tmem + b * BN);
           const bool first_sub = sub.corr ? (sub.kk == 0) : (jj == 0);
           const uint32_t a0 = sa + u * A_SUB, b0 = sa + OFF_B + u * B_SUB;
+          if (!p.mx && sub.ksteps == 4) {
+            mma_nvf4_cg2_x4(dcol, desc_sw128(a0), desc_sw128(b0), idesc, tsf + 16 * u,
+                            tsf + 32 + 16 * u, first_sub ? 0u : 1u);
+            continue;
+          }
           for (int q = 0; q < sub.ksteps; ++q) {
             const uint32_t acc = (first_sub && q == 0) ? 0u : 1u;
             if (p.mx) {
@@ -1268,6 +1363,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (!ok) break;
         commit_mc_cg2(&empty[s], 0x3);   // frees the stage in both CTAs (and the scale buffer)
+        trace_mark(p.trace, 4, mit++);
         if (++s == STAGES) s = 0;
         if (++sb == SF_BUFS) { sb = 0; sph ^= 1; }
       }
@@ -1294,6 +1390,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           okw = conv_wait(&empty[prev % STAGES], (prev / STAGES) & 1, sy);
         }
         if (!okw) { ok = false; break; }
+        if (w == 0) trace_mark(p.trace, 1, it);
         tc_fence_after();
         const Sub sub = sub_of(p, kt * SLOTS + w, nmain, ncorr);
         const uint32_t ssa = smem_u32(smem + s * STAGE_BYTES + OFF_SFA + w * SF_SUB);
@@ -1301,11 +1398,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t tsf = tmem + SF_COL + sb * SF_BUF_COLS;
         const int natoms = p.mx ? (sub.ksteps + 1) / 2 : sub.ksteps;
         const int abase = p.mx ? 2 * w : 4 * w;
+        if (natoms == 4) {
+          cp_sf_cg2_x4(tsf + 4 * abase, tsf + 32 + 4 * abase, desc_sf(ssa), desc_sf(ssb));
+        } else
         for (int a = 0; a < natoms; ++a) {
           cp_sf_cg2(tsf + 4 * (abase + a), desc_sf(ssa + a * 512));
           cp_sf_cg2(tsf + 32 + 4 * (abase + a), desc_sf(ssb + a * 512));
         }
         commit_mc_cg2(&sf_ready[sb], 0x1);
+        if (w == 0) trace_mark(p.trace, 2, it);
         if (++s == STAGES) { s = 0; ph ^= 1; }
         if (++sb == SF_BUFS) sb = 0;
       }
@@ -1324,6 +1425,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const Tile tl = decode_tile(p, poff, t);
       const uint32_t b = j & 1;
       if (!warp_wait(&acc_full[b], (j >> 1) & 1, sy, true)) break;
+      if (warp == EPI_WARP0) trace_mark(p.trace, 5, j);
       tc_fence_after();
       const float bts = p.mx ? 1.0f : __ldg(p.b_ts + tl.e);
       const float a1 = p.mx ? 1.0f : __fmul_rn(__ldg(p.a_ts + (p.a_ts_pe ? tl.e : 0)), bts);
@@ -1431,6 +1533,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       __syncwarp();
+      if (warp == EPI_WARP0) trace_mark(p.trace, 6, j);
       if (p.y_amax) {
         amax = warp_max(amax);
         if (lane == 0 && amax > 0.0f) atomicMax(&p.y_amax[tl.e], __float_as_uint(amax));
@@ -1811,6 +1914,7 @@ static quads_status_t launch(const Launch& L) {
   p.y_rows = arows;
   p.timeout_ns = wait_test ? 1000000ull : kTimeoutNs;
   p.skip_mma = wait_test ? 1 : 0;
+  p.trace = g_trace.exchange(nullptr);
   // one CTA pair per pair of SMs, persistent over the tiles
   int64_t pairs = max_pairs;
   if (!L.row_off)
