@@ -126,13 +126,17 @@ __device__ __forceinline__ void quantize_block_tasks(
   if (!QDBG(end >= 0 && end <= rows)) end = 0;
   const int nslab = (cols + 255) >> 8;
   const int64_t nchunks = (end + kScoreChunk - 1) / kScoreChunk;
-  const int64_t ntasks = nchunks * nslab;
+  const int64_t ntasks = nchunks * nslab;   // < 2^31 (host check)
   const int ncols16 = cols >> 4;
   const int blk = lane & 15;
-  // this thread's two rows of a task, loaded one task ahead
+  // tensor scale of a single group, once per block
+  const float s_single = G == 1 ? scale_of(0) : 0.0f;
+  // this thread's two rows of a task, loaded one task ahead (task indices fit
+  // in 32 bits: the division is a 32-bit one)
   auto load_task = [&](int64_t task, uint4 (&raw)[2][2]) {
-    const int64_t chunk = task / nslab;
-    const int col = (int)(task % nslab) * 256 + blk * 16;
+    const uint32_t tk = (uint32_t)task;
+    const int64_t chunk = tk / (uint32_t)nslab;
+    const int col = (int)(tk - (uint32_t)chunk * (uint32_t)nslab) * 256 + blk * 16;
     const int64_t r0 = chunk * kScoreChunk;
     const int64_t r1 = min(r0 + kScoreChunk, end);
 #pragma unroll
@@ -154,14 +158,14 @@ __device__ __forceinline__ void quantize_block_tasks(
 #pragma unroll
     for (int it = 0; it < 2; ++it) { raw[it][0] = nxt[it][0]; raw[it][1] = nxt[it][1]; }
     load_task(task + stride, nxt);
-    const int64_t chunk = task / nslab;
-    const int slab = (int)(task % nslab);
+    const int64_t chunk = (uint32_t)task / (uint32_t)nslab;
+    const int slab = (int)((uint32_t)task - (uint32_t)chunk * (uint32_t)nslab);
     const int col = slab * 256 + blk * 16;
     const bool active = col < cols;
     const int64_t r0 = chunk * kScoreChunk;
     const int64_t r1 = min(r0 + kScoreChunk, end);
     const int g0 = goff ? group_of(goff, G, r0) : 0;   // same for the whole block
-    const float s_t0 = scale_of(g0);
+    const float s_t0 = G == 1 ? s_single : scale_of(g0);
 #pragma unroll
     for (int it = 0; it < 2; ++it) {
       const int64_t row = r0 + 4 * warp + 2 * it + (lane >> 4);
@@ -234,9 +238,10 @@ __device__ __forceinline__ void quantize_block_tasks(
 }
 
 
-// Score mode runs four blocks per SM (64 registers, no spills).
+// Score mode: four blocks per SM (64 registers, no spills); the others
+// three (85 registers, no spills at 64).
 template <bool kScores, bool kQdq>
-__global__ void __launch_bounds__(256, kScores ? 4 : 1) quantize_kernel(
+__global__ void __launch_bounds__(256, kScores ? 4 : 3) quantize_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
     const int32_t* __restrict__ row_index, const int32_t* __restrict__ goff, int G,
     const float* __restrict__ st, const uint32_t* __restrict__ amax_bits, float* __restrict__ st_out,
@@ -879,22 +884,77 @@ __global__ void __launch_bounds__(kFusedThreads, 4) quantize_select_kernel(
 }
 
 // ---------------------------------------------------------------- TRACE
-// Signed level index of an E2M1 code: the 3 magnitude bits are the index of
-// the level among {0, .5, 1, 1.5, 2, 3, 4, 6}; negative codes count down, and
-// -0 and +0 share index 0.
-__device__ __forceinline__ int signed_index(uint32_t c) {
-  const int m = (int)(c & 7u);
-  return (c & 8u) ? -m : m;
+// Word-parallel form of the rule.  With n = the RTN code of v (same sign as v;
+// a zero result keeps the sign of v) and its magnitude level m_n, the two
+// neighbours of v are n itself and, when v is not a level, the code one
+// magnitude step away from zero (|v| > |q_n|) or toward zero (|v| < |q_n|),
+// with the same sign (a step toward zero from magnitude 1 gives a zero that
+// keeps the sign of v).  Nearest to the rollout code r (values compared, +0 ==
+// -0) is the neighbour step when
+//   away from zero:  r has the sign of n and a larger magnitude;
+//   toward zero:     r has the other sign, or a smaller magnitude,
+// else n.  (|v| > 6 rounds to 6 and no magnitude is larger; |v| < |q_n| needs
+// m_n >= 1.)  Eight 4-bit codes are handled at once in a 32-bit word with
+// per-nibble arithmetic that never carries across nibbles.
+
+// Per element, whether |v| lies beyond its RTN level (away) or inside it
+// (toward): bit 4j of the returned masks.  |v| - |q| is exact whenever the
+// two are within a factor of two (Sterbenz) and otherwise far from zero, so
+// its sign decides; equal magnitudes give +0 in both differences.
+__device__ __forceinline__ void trace_dirs8(const float* v, const float* qn, uint32_t& away,
+                                            uint32_t& toward) {
+  away = 0;
+  toward = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float a = __fsub_rn(fabsf(v[j]), fabsf(qn[j]));   // < 0: toward zero
+    const float b = __fsub_rn(fabsf(qn[j]), fabsf(v[j]));   // < 0: away from zero
+    toward |= (__float_as_uint(a) >> (31 - 4 * j)) & (1u << (4 * j));
+    away |= (__float_as_uint(b) >> (31 - 4 * j)) & (1u << (4 * j));
+  }
+}
+
+constexpr uint32_t kNib1 = 0x11111111u, kNib7 = 0x77777777u, kNib8 = 0x88888888u;
+
+// Nibbles of x that are zero, as bit 4j.
+__device__ __forceinline__ uint32_t zero_nibbles(uint32_t x) {
+  x |= x >> 2;
+  x |= x >> 1;
+  return ~x & kNib1;
+}
+
+// TRACE codes of eight elements (rtn: RTN codes, rc: rollout codes, dirs from
+// trace_dirs8), and the counter contributions: values of RTN != rollout,
+// TRACE != rollout, and RTN mismatches one signed level from the rollout.
+__device__ __forceinline__ uint32_t trace_word(uint32_t rtn, uint32_t rc, uint32_t away,
+                                               uint32_t toward, unsigned& n_rtn, unsigned& n_tr,
+                                               unsigned& n_adj) {
+  const uint32_t mn = rtn & kNib7, mr = rc & kNib7;
+  const uint32_t same = ~((rtn ^ rc) >> 3) & kNib1;          // equal sign bits
+  const uint32_t ge_r = (((mr | kNib8) - mn) >> 3) & kNib1;  // m_r >= m_n
+  const uint32_t ge_n = (((mn | kNib8) - mr) >> 3) & kNib1;  // m_n >= m_r
+  const uint32_t up = away & same & ~ge_n;                   // same sign, m_r > m_n
+  const uint32_t dn = toward & (~same | ~ge_r) & kNib1;      // other sign, or m_r < m_n
+  const uint32_t out = rtn + up - dn;
+  // value mismatch: magnitudes differ, or signs differ on a nonzero magnitude
+  const uint32_t nz_n = ((mn + kNib7) >> 3) & kNib1;
+  const uint32_t neq = (~zero_nibbles(mn ^ mr) & kNib1) | (~same & nz_n & kNib1);
+  // one signed level apart: same sign and |m_n - m_r| == 1, or other signs and
+  // m_n + m_r == 1
+  const uint32_t e = ((mr | kNib8) - mn) ^ kNib8;            // m_r - m_n mod 16
+  const uint32_t neg = (e >> 3) & kNib1;
+  const uint32_t absd = (e ^ (neg * 15u)) + neg;             // |m_r - m_n| <= 7
+  const uint32_t adj = (same & zero_nibbles(absd ^ kNib1)) | (~same & zero_nibbles((mn + mr) ^ kNib1));
+  n_rtn += __popc(neq);
+  n_adj += __popc(adj & kNib1);
+  n_tr += __popc(neq) - __popc((up | dn) & adj);   // a step onto an adjacent rollout level matches it
+  return out;
 }
 
 // One thread per 16-element block of a row per step (kMx: per 16 elements of
 // a 32-element block), with the next step's loads (x, rollout codes, scale)
 // issued before the current block is computed, so that loads stay in flight
-// across the arithmetic.  Neighbours and the choice are taken on signed level
-// indices: the RTN level sn is one neighbour of v and the other is sn - 1
-// (RTN level above v) or sn + 1 (below v); the level of {ilo, ihi} nearer the
-// rollout level sr is sr clamped to [ilo, ihi] (the two are adjacent, so sr
-// cannot fall strictly between them).
+// across the arithmetic.
 // kMx: MXFP4 rollout (E8M0 scale per 32 elements, no tensor scale): the
 // scaled value is x * 2^-e and no block is a zero block.
 struct TraceItem {
@@ -951,30 +1011,16 @@ __global__ void __launch_bounds__(256) trace_kernel(
     for (int h = 0; h < 2; ++h) {
       float f[8];
       bf16x8_to_f32(h ? cur.x1 : cur.x0, f);
-      const uint32_t rc = h ? cur.rc.y : cur.rc.x;
       float v[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(f[j], bs.r);
-      const uint32_t rtn = bs.zero ? 0u : f32x8_to_e2m1(v);
+      uint32_t rtn = f32x8_to_e2m1(v);
       float qn[8];
       e2m1x8_to_f32(rtn, qn);
-      uint32_t w = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int sn = signed_index((rtn >> (4 * j)) & 15u);
-        const int sr = signed_index((rc >> (4 * j)) & 15u);
-        const float vc = fminf(fmaxf(v[j], -6.0f), 6.0f);
-        const int ilo = sn - (qn[j] > vc ? 1 : 0);
-        const int ihi = sn + (qn[j] < vc ? 1 : 0);
-        const int stc = bs.zero ? 0 : min(max(sr, ilo), ihi);
-        const bool neg = !bs.zero && (stc < 0 || (stc == 0 && signbit(v[j])));
-        w |= ((uint32_t)abs(stc) | (neg ? 8u : 0u)) << (4 * j);
-        const int dd = sn - sr;
-        n_rtn += dd != 0 ? 1u : 0u;
-        n_adj += (dd == 1 || dd == -1) ? 1u : 0u;
-        n_tr += stc != sr ? 1u : 0u;
-      }
-      outw[h] = w;
+      uint32_t away, toward;
+      trace_dirs8(v, qn, away, toward);
+      if (bs.zero) rtn = away = toward = 0u;   // a zero block gives 0x0 codes
+      outw[h] = trace_word(rtn, h ? cur.rc.y : cur.rc.x, away, toward, n_rtn, n_tr, n_adj);
     }
     uint32_t* po = reinterpret_cast<uint32_t*>(out + (int64_t)r * ldc + (col >> 1));
     po[0] = outw[0];
@@ -1086,6 +1132,18 @@ __global__ void __launch_bounds__(256) trace_pack_kernel(const uint8_t* __restri
 // mismatches).  A v on a level (or clamped at +-6) has that level alone.
 // Counters (nullable, added to): #(result != RTN code), #(result's mantissa
 // bit != record bit).
+// Eight record bits (element j in bit j) spread to bit 4j.
+__device__ __forceinline__ uint32_t spread_bits8(uint32_t b) {
+  b = (b | (b << 12)) & 0x000F000Fu;
+  b = (b | (b << 6)) & 0x03030303u;
+  b = (b | (b << 3)) & 0x11111111u;
+  return b;
+}
+
+// TRACE from the 1-bit record: the two neighbours of v (when v is not a
+// level) are adjacent signed levels with opposite mantissa bits, so the one
+// named by the record bit is the RTN code n when n's mantissa bit matches,
+// else the neighbour step (away from or toward zero, as in trace_word).
 __global__ void __launch_bounds__(256) trace_1bit_kernel(
     const __nv_bfloat16* __restrict__ xt, int64_t rows, int cols, int64_t ldx,
     const uint8_t* __restrict__ mbits, int64_t ldb, const uint8_t* __restrict__ rscales,
@@ -1125,27 +1183,23 @@ __global__ void __launch_bounds__(256) trace_1bit_kernel(
     for (int h = 0; h < 2; ++h) {
       float f[8];
       bf16x8_to_f32(h ? x1 : x0, f);
-      const uint32_t mb = (mb16 >> (8 * h)) & 0xFFu;
       float v[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(f[j], bs.r);
-      const uint32_t rtn = bs.zero ? 0u : f32x8_to_e2m1(v);
+      uint32_t rtn = f32x8_to_e2m1(v);
       float qn[8];
       e2m1x8_to_f32(rtn, qn);
-      uint32_t w = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int sn = signed_index((rtn >> (4 * j)) & 15u);
-        const float vc = fminf(fmaxf(v[j], -6.0f), 6.0f);
-        const int ilo = sn - (qn[j] > vc ? 1 : 0);
-        const int ihi = sn + (qn[j] < vc ? 1 : 0);
-        const int bit = (int)((mb >> j) & 1u);
-        const int stc = bs.zero ? 0 : ((abs(ilo) & 1) == bit ? ilo : ihi);
-        const bool neg = !bs.zero && (stc < 0 || (stc == 0 && signbit(v[j])));
-        w |= ((uint32_t)abs(stc) | (neg ? 8u : 0u)) << (4 * j);
-        n_chg += stc != sn ? 1u : 0u;
-        n_bit += (abs(stc) & 1) != bit ? 1u : 0u;
-      }
+      uint32_t away, toward;
+      trace_dirs8(v, qn, away, toward);
+      if (bs.zero) rtn = away = toward = 0u;   // a zero block gives 0x0 codes
+      const uint32_t bits = spread_bits8((mb16 >> (8 * h)) & 0xFFu);
+      const uint32_t flip = (rtn ^ bits) & kNib1;   // RTN's mantissa bit is not the record's
+      // |v| beyond 6 rounds to magnitude 7 and has no level further out
+      const uint32_t top = rtn & (rtn >> 1) & (rtn >> 2) & kNib1;
+      const uint32_t up = away & flip & ~top, dn = toward & flip;
+      const uint32_t w = rtn + up - dn;
+      n_chg += __popc(up | dn);
+      n_bit += __popc((w ^ bits) & kNib1);
       outw[h] = w;
     }
     uint32_t* po = reinterpret_cast<uint32_t*>(out + (int64_t)r * ldc + bi * 8);
@@ -1242,6 +1296,8 @@ static quads_status_t quantize_impl(
     cudaMemsetAsync(scales + start, 0, (size_t)(sf_tc_bytes(rows, cols) - start), st);
   }
   const int64_t ntasks = ((rows + 31) / 32) * ((cols + 255) / 256);  // one block per task
+  if (ntasks >= (1ll << 31))
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "quantize: more than 2^31 32x256 tasks");
   const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(ntasks, (int64_t)num_sms() * 16));
   const __nv_bfloat16* xb = (const __nv_bfloat16*)x;
   if (qdq)
