@@ -897,21 +897,36 @@ __global__ void __launch_bounds__(kFusedThreads, 4) quantize_select_kernel(
 // m_n >= 1.)  Eight 4-bit codes are handled at once in a 32-bit word with
 // per-nibble arithmetic that never carries across nibbles.
 
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+// Sign bits of eight floats to bit 4j: the top bytes of the even and of the
+// odd elements are gathered into one word each (byte permutes), whose sign
+// bits then sit at 8k + 7 for elements 2k and 2k + 1.
+__device__ __forceinline__ uint32_t sign_nibbles8(const float* d) {
+  const uint32_t e = prmt(prmt(__float_as_uint(d[0]), __float_as_uint(d[2]), 0x0073u),
+                          prmt(__float_as_uint(d[4]), __float_as_uint(d[6]), 0x0073u), 0x5410u);
+  const uint32_t o = prmt(prmt(__float_as_uint(d[1]), __float_as_uint(d[3]), 0x0073u),
+                          prmt(__float_as_uint(d[5]), __float_as_uint(d[7]), 0x0073u), 0x5410u);
+  return ((e >> 7) & 0x01010101u) | ((o >> 3) & 0x10101010u);
+}
+
 // Per element, whether |v| lies beyond its RTN level (away) or inside it
 // (toward): bit 4j of the returned masks.  |v| - |q| is exact whenever the
 // two are within a factor of two (Sterbenz) and otherwise far from zero, so
 // its sign decides; equal magnitudes give +0 in both differences.
 __device__ __forceinline__ void trace_dirs8(const float* v, const float* qn, uint32_t& away,
                                             uint32_t& toward) {
-  away = 0;
-  toward = 0;
+  float a[8], b[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const float a = __fsub_rn(fabsf(v[j]), fabsf(qn[j]));   // < 0: toward zero
-    const float b = __fsub_rn(fabsf(qn[j]), fabsf(v[j]));   // < 0: away from zero
-    toward |= (__float_as_uint(a) >> (31 - 4 * j)) & (1u << (4 * j));
-    away |= (__float_as_uint(b) >> (31 - 4 * j)) & (1u << (4 * j));
+    a[j] = __fsub_rn(fabsf(v[j]), fabsf(qn[j]));   // < 0: toward zero
+    b[j] = __fsub_rn(fabsf(qn[j]), fabsf(v[j]));   // < 0: away from zero
   }
+  toward = sign_nibbles8(a);
+  away = sign_nibbles8(b);
 }
 
 constexpr uint32_t kNib1 = 0x11111111u, kNib7 = 0x77777777u, kNib8 = 0x88888888u;
