@@ -26,6 +26,7 @@ static __device__ int g_quant_error;  // device-side argument check failures
 
 constexpr int kRselGroupMin = 32;     // groups from which the per-group R_sel kernel is used
 constexpr int kFusedMaxK = 1024;      // selected channels of the fused activation-side kernel
+constexpr int kSmemGroups = 256;      // groups whose offsets and scales a quantizer block caches
 
 // ---------------------------------------------------------------- amax
 // One block per 8-row slice (inside one group), threads over (row, 8-col
@@ -115,10 +116,12 @@ __device__ __forceinline__ void quantize_block_tasks(
     const float* __restrict__ st, const uint32_t* __restrict__ amax_bits,
     uint8_t* __restrict__ codes, int64_t ldc, uint8_t* __restrict__ scales, int layout,
     float* __restrict__ partials, __nv_bfloat16* __restrict__ qdq, int64_t ldq, float* sq,
-    int64_t first, int64_t stride) {
-  // tensor scales: given (st), or derived from the groups' amax bits (read
-  // through L2: the fused kernel produces them earlier in the same launch)
+    int64_t first, int64_t stride, const float* gscale = nullptr) {
+  // tensor scales: a per-block table (gscale, shared memory), given (st), or
+  // derived from the groups' amax bits (read through L2: the fused kernel
+  // produces them earlier in the same launch)
   auto scale_of = [&](int g) {
+    if (gscale) return gscale[g];
     return amax_bits ? tensor_scale_from_amax(__uint_as_float(__ldcg(amax_bits + g))) : __ldcg(st + g);
   };
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -248,13 +251,24 @@ __global__ void __launch_bounds__(256, kScores ? 4 : 3) quantize_kernel(
     uint8_t* __restrict__ codes, int64_t ldc, uint8_t* __restrict__ scales, int layout,
     float* __restrict__ partials, __nv_bfloat16* __restrict__ qdq, int64_t ldq) {
   __shared__ __align__(16) float sq[kScores ? kScoreChunk * 256 : 4];
+  // groups (up to kSmemGroups): offsets and tensor scales once per block in
+  // shared memory, so the per-task group search and scale reads stay on chip
+  __shared__ int32_t s_goff[kSmemGroups + 1];
+  __shared__ float s_scale[kSmemGroups];
   // tensor scales derived from the groups' amax bits are also stored by block 0
   if (amax_bits && blockIdx.x == 0)
     for (int g = threadIdx.x; g < G; g += blockDim.x)
       st_out[g] = tensor_scale_from_amax(__uint_as_float(__ldg(amax_bits + g)));
-  quantize_block_tasks<kScores, kQdq>(x, rows, cols, ldx, row_index, goff, G, st, amax_bits, codes,
-                                      ldc, scales, layout, partials, qdq, ldq, sq, blockIdx.x,
-                                      gridDim.x);
+  const bool cache = goff && G <= kSmemGroups;
+  if (cache) {
+    for (int g = threadIdx.x; g <= G; g += blockDim.x) s_goff[g] = goff[g];
+    for (int g = threadIdx.x; g < G; g += blockDim.x)
+      s_scale[g] = amax_bits ? tensor_scale_from_amax(__uint_as_float(__ldg(amax_bits + g))) : __ldg(st + g);
+    __syncthreads();
+  }
+  quantize_block_tasks<kScores, kQdq>(x, rows, cols, ldx, row_index, cache ? s_goff : goff, G, st,
+                                      amax_bits, codes, ldc, scales, layout, partials, qdq, ldq, sq,
+                                      blockIdx.x, gridDim.x, cache ? s_scale : nullptr);
 }
 
 // ---------------------------------------------------------------- select
@@ -1124,19 +1138,33 @@ __global__ void __launch_bounds__(256) mx_quantize_kernel(
 // kept, 8 per byte, element 8i+j in bit j of byte i; with the E4M3 block scale
 // (8 bits per 16 values) that is the pages' 1.5 bits per value.
 // One thread per 8 codes: a 4-byte read, a 1-byte write.
+// Bit 0 of each of the eight nibbles of c, as bits 0..7.
+__device__ __forceinline__ uint32_t gather_nibble_bit0(uint32_t c) {
+  c &= 0x11111111u;
+  c = (c | (c >> 3)) & 0x03030303u;
+  c = (c | (c >> 6)) & 0x000F000Fu;
+  return (c | (c >> 12)) & 0xFFu;
+}
+
+// One thread per 32 codes (a 16-byte read, a 4-byte write) when the row
+// length allows it (vec), else per 8 codes (a 4-byte read, a 1-byte write).
 __global__ void __launch_bounds__(256) trace_pack_kernel(const uint8_t* __restrict__ codes,
                                                          int64_t rows, int cols, int64_t ldc,
                                                          uint8_t* __restrict__ bits,
-                                                         int64_t ldb) {
-  const uint32_t per_row = (uint32_t)cols >> 3;
+                                                         int64_t ldb, int vec) {
+  const uint32_t per_row = (uint32_t)cols >> (vec ? 5 : 3);
   const uint32_t total = (uint32_t)(rows * per_row);   // < 2^31 (host check)
   for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
     const uint32_t r = i / per_row, v = i - r * per_row;
-    const uint32_t c = __ldg(reinterpret_cast<const uint32_t*>(codes + (int64_t)r * ldc) + v);
-    uint32_t m = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) m |= ((c >> (4 * j)) & 1u) << j;
-    bits[(int64_t)r * ldb + v] = (uint8_t)m;
+    if (vec) {
+      const uint4 c = __ldg(reinterpret_cast<const uint4*>(codes + (int64_t)r * ldc) + v);
+      const uint32_t m = gather_nibble_bit0(c.x) | (gather_nibble_bit0(c.y) << 8) |
+                         (gather_nibble_bit0(c.z) << 16) | (gather_nibble_bit0(c.w) << 24);
+      *reinterpret_cast<uint32_t*>(bits + (int64_t)r * ldb + 4 * v) = m;
+    } else {
+      const uint32_t c = __ldg(reinterpret_cast<const uint32_t*>(codes + (int64_t)r * ldc) + v);
+      bits[(int64_t)r * ldb + v] = (uint8_t)gather_nibble_bit0(c);
+    }
   }
 }
 
@@ -1603,8 +1631,12 @@ extern "C" quads_status_t quads_trace_pack_record(const uint8_t* rollout_codes, 
   if (rows * (cols / 8) >= ((int64_t)1 << 31))
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "trace_pack_record: rows * cols / 8 must be < 2^31");
   if (rows == 0) return QUADS_OK;
-  trace_pack_kernel<<<grid_for(rows * (cols / 8), 256), 256, 0, (cudaStream_t)stream>>>(
-      rollout_codes, rows, (int)cols, ld_codes, mantissa_bits, ld_bits);
+  // 32 codes per thread when rows are 16-byte aligned runs of codes and the
+  // record rows take aligned 4-byte stores
+  const int vec = cols % 32 == 0 && ld_codes % 16 == 0 && ld_bits % 4 == 0 &&
+                  ((uintptr_t)rollout_codes & 15) == 0 && ((uintptr_t)mantissa_bits & 3) == 0;
+  trace_pack_kernel<<<grid_for(rows * (cols / (vec ? 32 : 8)), 256), 256, 0, (cudaStream_t)stream>>>(
+      rollout_codes, rows, (int)cols, ld_codes, mantissa_bits, ld_bits, vec);
   return check_launch("trace_pack_record", 1);
 }
 
