@@ -271,6 +271,91 @@ __global__ void __launch_bounds__(256, kScores ? 4 : 3) quantize_kernel(
                                       blockIdx.x, gridDim.x, cache ? s_scale : nullptr);
 }
 
+// Score mode with one thread per (32-row chunk, 16-column block): the thread
+// walks its chunk's rows in order (the next two rows' loads in flight), writes
+// each row's codes and block scale, and adds each column's residual square to
+// a register in row order from 0 -- the same float32 sequence the shared-
+// memory column sums form -- so the partials need no shared memory and no
+// barrier.  Chunks never straddle a group (group offsets are multiples of 32
+// in score mode).  Used when there are enough (chunk, block) pairs to fill
+// the GPU.
+__global__ void __launch_bounds__(256, 3) quantize_chunk_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
+    const int32_t* __restrict__ row_index, const int32_t* __restrict__ goff, int G,
+    const float* __restrict__ st, const uint32_t* __restrict__ amax_bits, float* __restrict__ st_out,
+    uint8_t* __restrict__ codes, int64_t ldc, uint8_t* __restrict__ scales, int layout,
+    float* __restrict__ partials) {
+  __shared__ int32_t s_goff[kSmemGroups + 1];
+  __shared__ float s_scale[kSmemGroups];
+  if (amax_bits && blockIdx.x == 0)
+    for (int g = threadIdx.x; g < G; g += blockDim.x)
+      st_out[g] = tensor_scale_from_amax(__uint_as_float(__ldg(amax_bits + g)));
+  const bool cache = G <= kSmemGroups;
+  if (cache) {
+    if (goff)
+      for (int g = threadIdx.x; g <= G; g += blockDim.x) s_goff[g] = goff[g];
+    for (int g = threadIdx.x; g < G; g += blockDim.x)
+      s_scale[g] = amax_bits ? tensor_scale_from_amax(__uint_as_float(__ldg(amax_bits + g))) : __ldg(st + g);
+    __syncthreads();
+  }
+  const int32_t* go = cache ? s_goff : goff;
+  auto scale_of = [&](int g) {
+    if (cache) return s_scale[g];
+    return amax_bits ? tensor_scale_from_amax(__uint_as_float(__ldcg(amax_bits + g))) : __ldg(st + g);
+  };
+  int64_t end = goff ? (int64_t)go[G] : rows;
+  if (!QDBG(end >= 0 && end <= rows)) end = 0;
+  const uint32_t nblk = (uint32_t)cols >> 4;
+  const uint32_t total = (uint32_t)(((end + kScoreChunk - 1) / kScoreChunk) * nblk);   // < 2^31 (host check)
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const uint32_t chunk = i / nblk, cb = i - chunk * nblk;
+    const int64_t r0 = (int64_t)chunk * kScoreChunk;
+    const int nr = (int)min((int64_t)kScoreChunk, end - r0);
+    const int g = goff ? group_of(go, G, r0) : 0;
+    if (goff && r0 + nr > (int64_t)go[g + 1]) atomicExch(&g_quant_error, QUADS_ERR_DEVICE_CHECK);
+    const float s_t = scale_of(g);
+    auto load = [&](int r, uint4& lo, uint4& hi) {
+      if (r < nr) {
+        const int64_t src = row_index ? (int64_t)row_index[r0 + r] : r0 + r;
+        const uint4* px = reinterpret_cast<const uint4*>(x + src * ldx + cb * 16);
+        lo = __ldg(px);
+        hi = __ldg(px + 1);
+      }
+    };
+    uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, b0 = a0, b1 = a0;
+    load(0, a0, a1);
+    load(1, b0, b1);
+    float acc[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+#pragma unroll 1
+    for (int r = 0; r < nr; ++r) {
+      const uint4 lo = a0, hi = a1;
+      a0 = b0;
+      a1 = b1;
+      load(r + 2, b0, b1);
+      const int64_t row = r0 + r;
+      float f[16];
+      BlockScale bs;
+      uint2 c;
+      quantize_block16(lo, hi, s_t, f, bs, c);
+      *reinterpret_cast<uint2*>(codes + row * ldc + cb * 8) = c;
+      scales[sf_offset(layout, row, cb, nblk)] = (uint8_t)bs.byte;
+      float lv[16];
+      e2m1x8_to_f32(c.x, lv);
+      e2m1x8_to_f32(c.y, lv + 8);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float R = __fsub_rn(f[j], __fmul_rn(lv[j], bs.d));
+        acc[j] = __fadd_rn(acc[j], __fmul_rn(R, R));
+      }
+    }
+    float4* pp = reinterpret_cast<float4*>(partials + (int64_t)chunk * cols + cb * 16);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) pp[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+  }
+}
+
 // ---------------------------------------------------------------- select
 // Channel scores = the group's chunk partials added in ascending chunk order
 // starting from 0 (one float32 add per chunk).  Two launch shapes compute the
@@ -1347,6 +1432,12 @@ static quads_status_t quantize_impl(
     quantize_kernel<false, true><<<blocks, 256, 0, st>>>(
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
         codes, ld_codes, scales, scale_layout, nullptr, qdq, ldq);
+  else if (score_partials && ((rows + 31) / 32) * (cols / 16) >= (int64_t)num_sms() * 512 &&
+           ((rows + 31) / 32) * (cols / 16) < (1ll << 31))
+    // enough (chunk, block) pairs for a thread each: about two blocks per SM
+    quantize_chunk_kernel<<<grid_for(((rows + 31) / 32) * (cols / 16), 256, 3), 256, 0, st>>>(
+        xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
+        codes, ld_codes, scales, scale_layout, score_partials);
   else if (score_partials)
     quantize_kernel<true, false><<<blocks, 256, 0, st>>>(
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,

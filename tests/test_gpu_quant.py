@@ -82,6 +82,40 @@ def test_quantize_groups_and_row_index(lib):
     assert np.array_equal(part.cpu().numpy(), Q.chunk_partials(R))
 
 
+@pytest.mark.parametrize("layout", [0, 1])
+def test_quantize_scores_per_expert_groups_sampled_chunks(lib, layout):
+    # 128 groups of 12-25 chunks of 32 rows x 768 columns: enough (chunk,
+    # 16-column block) pairs for the thread-per-pair score kernel (the shape
+    # of the per-expert h quantization); every tensor scale checked, codes,
+    # scales and partials on 48 sampled chunks
+    rng = inputs.make_rng(21)
+    sizes = 32 * rng.integers(12, 26, 128)
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    rows, cols = int(offs[-1]), 768
+    x = inputs.student_t4(rng, (rows, cols))
+    x *= np.repeat(np.float32(2.0) ** rng.integers(-3, 4, 128).astype(np.float32), sizes)[:, None]
+    bits = inputs.f32_to_bf16_bits(x)
+    q, part = lib.quantize_nvfp4(bf16_tensor(bits), group_offsets=torch.from_numpy(offs).cuda(),
+                                 num_groups=128, scale_layout=layout, scores=True)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    xf = f32(bits)
+    ts = q.tensor_scale.cpu().numpy()
+    for g in range(128):
+        assert ts[g] == Q.tensor_scale(xf[offs[g]:offs[g + 1]])
+    codes = codes_np(q.codes, cols)
+    scales = linear_scales(q)
+    pc = part.cpu().numpy()
+    for ch in rng.choice(rows // 32, 48, replace=False):
+        a, b = 32 * ch, 32 * ch + 32
+        g = int(np.searchsorted(offs, a, side="right") - 1)
+        oc, osc = Q.quantize(xf[a:b], ts[g])
+        assert np.array_equal(codes[a:b], oc)
+        assert np.array_equal(scales[a:b], osc)
+        R = Q.residual(xf[a:b], oc, osc, ts[g])
+        assert np.array_equal(pc[ch:ch + 1], Q.chunk_partials(R))
+
+
 def test_quantize_given_tensor_scale(lib):
     bits = _case("ragged")
     x = bf16_tensor(bits)
