@@ -495,18 +495,21 @@ __device__ __forceinline__ void block_topk(const uint32_t (&key)[PER], int cols,
 // itself -- the chunk partials added in ascending chunk order from 0 -- and
 // stores them to `scores`; otherwise it reads the scores score_chain_kernel
 // left there.
-__global__ void __launch_bounds__(1024) topk_kernel(float* __restrict__ scores, int cols,
-                                                    int k, int32_t* __restrict__ sel,
-                                                    const float* __restrict__ partials,
-                                                    const int32_t* __restrict__ goff,
-                                                    int64_t rows) {
+// NT threads x PER channels per thread cover cols (256 x 8 up to 2048
+// channels: fewer warps per block barrier; 1024 x 8 up to 8192).
+template <int NT>
+__global__ void __launch_bounds__(NT) topk_kernel(float* __restrict__ scores, int cols,
+                                                  int k, int32_t* __restrict__ sel,
+                                                  const float* __restrict__ partials,
+                                                  const int32_t* __restrict__ goff,
+                                                  int64_t rows) {
   __shared__ int hist[256];
   __shared__ uint32_t s_prefix;
   __shared__ int s_need;
-  __shared__ int warp_sums[32];   // one per warp of the 1024-thread block
+  __shared__ int warp_sums[NT / 32];   // one per warp
   const int g = blockIdx.y;
   float* sc = scores + (int64_t)g * cols;
-  constexpr int PER = 8;  // cols <= 8192 = 1024 threads x 8
+  constexpr int PER = 8;
   uint32_t key[PER];
   if (partials) {
     const int64_t a = goff ? (int64_t)goff[g] : 0;
@@ -536,7 +539,7 @@ __global__ void __launch_bounds__(1024) topk_kernel(float* __restrict__ scores, 
       key[i] = c < cols ? __float_as_uint(sc[c]) : 0u;
     }
   }
-  block_topk<1024, PER>(key, cols, k, sel + (int64_t)g * k, hist, &s_prefix, &s_need, warp_sums);
+  block_topk<NT, PER>(key, cols, k, sel + (int64_t)g * k, hist, &s_prefix, &s_need, warp_sums);
 }
 
 // ---------------------------------------------------------------- residual slice
@@ -1534,9 +1537,14 @@ extern "C" quads_status_t quads_select_residual_channels(
   if (long_groups)
     score_chain_kernel<<<dim3((unsigned)((cols + 31) / 32), (unsigned)G), 256, 0, st>>>(
         score_partials, (int)cols, group_offsets, rows, scores);
-  topk_kernel<<<dim3(1, (unsigned)G), 1024, 0, st>>>(scores, (int)cols, k, sel,
-                                                     long_groups ? nullptr : score_partials,
-                                                     group_offsets, rows);
+  if (cols <= 2048 && long_groups)   // scores precomputed: only the selection
+    topk_kernel<256><<<dim3(1, (unsigned)G), 256, 0, st>>>(scores, (int)cols, k, sel,
+                                                          long_groups ? nullptr : score_partials,
+                                                          group_offsets, rows);
+  else
+    topk_kernel<1024><<<dim3(1, (unsigned)G), 1024, 0, st>>>(scores, (int)cols, k, sel,
+                                                            long_groups ? nullptr : score_partials,
+                                                            group_offsets, rows);
   if (quads_status_t s = sel_ready()) return s;
   if (group_offsets && G >= kRselGroupMin) {
     if (r_scale_layout == QUADS_SCALES_TCGEN05 && rows % 128) {
