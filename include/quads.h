@@ -138,6 +138,23 @@ void quads_test_gemm_wait_timeout(int32_t enable);
  */
 void quads_test_gemm_timeline(uint64_t* device_buffer);
 
+/*
+ * GEMM output tile width (no counterpart on the pages: a tuning choice), set
+ * process-wide for quads_w4a4_gemm_comp and quads_moe_grouped_gemm.
+ *   QUADS_GEMM_TILES_AUTO (default): 128 x 256 tiles for plain products (no
+ *     correction) whose N is a multiple of 256, 128 x 128 otherwise;
+ *   QUADS_GEMM_TILES_128: always 128 x 128;
+ *   QUADS_GEMM_TILES_256: 128 x 256 wherever N is a multiple of 256,
+ *     compensated products included (their k-channel correction is then
+ *     folded into the single accumulator: its partial sum is scaled by
+ *     s_R / s_X in tensor memory before the main MMAs accumulate on top).
+ * MXFP4 products always use 128 x 128 tiles.  Results agree within the GEMM
+ * tolerance, not bit for bit, across policies.  Returns the previous policy,
+ * or -1 (and changes nothing) for an unknown value.
+ */
+enum { QUADS_GEMM_TILES_AUTO = 0, QUADS_GEMM_TILES_128 = 1, QUADS_GEMM_TILES_256 = 2 };
+int32_t quads_set_gemm_tile_policy(int32_t policy);
+
 /* Bytes of scratch the call `op` needs for the given shape (0 if none).
  *   QUADS_OP_QUANTIZE: num_groups floats of tensor amax.
  *   QUADS_OP_SELECT:   rows*k floats (the residual slice) + num_groups floats

@@ -1552,6 +1552,504 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 }  // namespace pair
 
+// ---------------------------------------------------------------- 256-column tiles
+// The same product with 128 x 256 output tiles on one SM: a 256-element K
+// stage is 54 KB (A 16 KB, B 32 KB, scale atoms 6 KB) and a stage's four
+// 128x256x64 MMAs do twice the work of a 128x128 stage for 3/4 of its bytes,
+// so the four-stage ring keeps more work in flight per byte.  The accumulator
+// takes 256 TMEM columns and the scale buffers the rest, which leaves no room
+// for a second accumulator: the k-channel correction is folded into the main
+// one.  Its MMAs run first (the correction's stages lead each tile), the
+// epilogue warps scale that partial sum by s_R / s_X in TMEM (tcgen05.ld,
+// multiply, tcgen05.st), and the main MMAs then accumulate on top, so the
+// epilogue forms s_X s_W (acc_main + fl(s_R / s_X * acc_corr)).
+//
+// Roles (24 warps):
+//   warps 0-2   TMA producers (A box, B box and a scale run each; the third
+//               warp two B boxes and a scale run: 18 KB per warp and stage)
+//   warp 3      MMA issuer (four MMAs of a stage under one elect)
+//   warps 4-7   scale atoms into TMEM: warp w the A atom and the two B atoms
+//               of K step w
+//   warps 8-23  epilogue: four warps per TMEM lane quadrant, 64 accumulator
+//               columns each; they read their columns into registers, release
+//               the accumulator, then compute and store
+namespace wide {
+
+constexpr int BM = 128, BN = 256;
+constexpr int KSUB = 128;                        // bytes of a row per stage (256 FP4)
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * KSUB;               // 16 KB
+constexpr int B_BYTES = BN * KSUB;               // 32 KB
+constexpr int OFF_B = A_BYTES;
+constexpr int OFF_SFA = OFF_B + B_BYTES;         // A's atoms, one per K step
+constexpr int OFF_SFB = OFF_SFA + 4 * 512;       // B rows 0-127: one atom per K step; rows 128-255 at +2 KB
+constexpr int STAGE_BYTES = OFF_SFB + 8 * 512;   // 54 KB
+constexpr int BOX_ROWS = 64;
+constexpr int BOX_BYTES = BOX_ROWS * KSUB;       // 8 KB
+constexpr int COPIES = 9;
+constexpr int MMA_WARP = 3, SF_WARP0 = 4, SF_WARPS = 4, EPI_WARP0 = 8, EPI_WARPS = 16;
+constexpr int NUM_THREADS = 32 * (EPI_WARP0 + EPI_WARPS);   // 768
+constexpr int TMEM_COLS = 512;
+constexpr int SF_COL = 256;                      // the accumulator holds columns 0-255
+constexpr int SF_BUF_COLS = 48;                  // per K step q: A at 4q, B's two atoms at 16 + 8q
+constexpr int SF_BUFS = 4;
+static_assert(SF_COL + SF_BUFS * SF_BUF_COLS <= TMEM_COLS, "scale buffers fit beside the accumulator");
+constexpr int MAX_GROUPS = 256;
+constexpr int BAR_BYTES = 1024;
+constexpr int META_BYTES = 4 * (MAX_GROUPS + 1) + 3 * 4 * MAX_GROUPS;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + META_BYTES + 1024 /*align*/;
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+
+struct Meta {
+  int32_t* off;    // [E+1]
+  int32_t* cnt;    // [E]
+  float* a1;       // [E] s_a * s_w
+  float* ratio;    // [E] s_r / s_a
+};
+
+__device__ __forceinline__ int64_t total_tiles(const Params& p, const Meta& m) {
+  if (!p.row_off) return ((p.M + BM - 1) / BM) * p.Nt;
+  return (int64_t)(m.off[p.E] / BM) * p.Nt;
+}
+
+__device__ __forceinline__ Tile decode_tile(const Params& p, const Meta& m, int64_t t) {
+  Tile r;
+  if (!p.row_off) {
+    const int64_t Mt = (p.M + BM - 1) / BM;
+    r.e = 0;
+    r.m0 = (t % Mt) * BM;
+    r.n0 = (int)(t / Mt) * BN;
+    r.row_end = p.M;
+    return r;
+  }
+  int lo = 0, hi = p.E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)(m.off[mid] / BM) * p.Nt <= t) lo = mid; else hi = mid - 1;
+  }
+  const int e = lo;
+  const int64_t base = (int64_t)(m.off[e] / BM) * p.Nt;
+  const int64_t mt_e = (m.off[e + 1] - m.off[e]) / BM;
+  const int64_t local = t - base;
+  r.e = e;
+  r.m0 = m.off[e] + (local % mt_e) * BM;
+  r.n0 = (int)(local / mt_e) * BN;
+  r.row_end = m.off[e] + m.cnt[e];
+  return r;
+}
+
+// Stage j of a tile: the correction's stages first, then the main range's.
+struct Stage {
+  int ksteps;
+  bool corr;
+  int kk;       // stage index inside its own K range
+};
+__device__ __forceinline__ Stage stage_of(const Params& p, int j, int ncorr) {
+  Stage s;
+  s.corr = j < ncorr;
+  s.kk = s.corr ? j : j - ncorr;
+  s.ksteps = min(4, ((s.corr ? p.kpad : p.K) - s.kk * 256) / 64);
+  return s;
+}
+
+// Four 128x256x64 MMAs of a stage under one elect: descriptors +2 per K
+// step, A's scale columns +4, B's +8.
+__device__ __forceinline__ void mma_x4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 a1, b1;\n\t.reg .b32 fa, fb;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\tadd.u32 fa, %5, 4;\n\tadd.u32 fb, %6, 8;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [fa], [fb], 1;\n\t"
+      "add.s64 a1, %1, 4;\n\tadd.s64 b1, %2, 4;\n\tadd.u32 fa, %5, 8;\n\tadd.u32 fb, %6, 16;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [fa], [fb], 1;\n\t"
+      "add.s64 a1, %1, 6;\n\tadd.s64 b1, %2, 6;\n\tadd.u32 fa, %5, 12;\n\tadd.u32 fb, %6, 24;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [fa], [fb], 1;\n\t"
+      "}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb));
+}
+
+// K step q's atoms: A to column t, B rows 0-127 to t + 16 + 4q... (caller
+// passes both targets), under one elect.
+__device__ __forceinline__ void cp_atoms3(uint32_t ta, uint64_t da, uint32_t tb, uint64_t db0,
+                                          uint64_t db1) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 t1;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "add.u32 t1, %2, 4;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%2], %3;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [t1], %4;\n\t}" ::"r"(ta),
+      "l"(da), "r"(tb), "l"(db0), "l"(db1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+__device__ __forceinline__ void tc_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmW,
+                     const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = bars;                           // [STAGES]
+  uint64_t* empty = full + STAGES;                 // [STAGES]
+  uint64_t* sf_ready = empty + STAGES;             // [SF_BUFS]
+  uint64_t* acc_full = sf_ready + SF_BUFS;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* corr_full = acc_empty + 1;
+  uint64_t* prescaled = corr_full + 1;
+  uint64_t* drain_mma = prescaled + 1;
+  uint64_t* drain_sf = drain_mma + 1;
+  uint32_t* tmem_holder = (uint32_t*)(drain_sf + 1);
+  volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
+  Meta meta;
+  meta.off = (int32_t*)(smem + STAGES * STAGE_BYTES + BAR_BYTES);
+  meta.cnt = meta.off + (MAX_GROUPS + 1);
+  meta.a1 = (float*)(meta.cnt + MAX_GROUPS);
+  meta.ratio = meta.a1 + MAX_GROUPS;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+    const float ats = __ldg(p.a_ts + (p.a_ts_pe ? e : 0));
+    meta.a1[e] = __fmul_rn(ats, __ldg(p.b_ts + e));
+    meta.ratio[e] = p.comp ? __fdiv_rn(__ldg(p.r_ts + (p.r_ts_pe ? e : 0)), ats) : 0.0f;
+    if (p.row_off) {
+      meta.off[e] = p.row_off[e];
+      meta.cnt[e] = p.row_cnt ? p.row_cnt[e] : (p.row_off[e + 1] - p.row_off[e]);
+    }
+  }
+  if (threadIdx.x == 0 && p.row_off) meta.off[p.E] = p.row_off[p.E];
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) { mbar_init(&full[i], COPIES); mbar_init(&empty[i], 1); }
+    for (int i = 0; i < SF_BUFS; ++i) mbar_init(&sf_ready[i], SF_WARPS);
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, EPI_WARPS);
+    mbar_init(corr_full, 1);
+    mbar_init(prescaled, EPI_WARPS);
+    mbar_init(drain_mma, 1);
+    mbar_init(drain_sf, SF_WARPS);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == MMA_WARP) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_holder)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const Sync sy{abort_flag, p.err, p.timeout_ns};
+  const Sync dr{abort_flag, p.err, kDrainNs};
+
+  const int64_t ntiles = total_tiles(p, meta);
+  const int nmain = (p.K + 255) / 256;
+  const int ncorr = p.comp ? (p.kpad + 255) / 256 : 0;
+  const int nst = ncorr + nmain;
+  const int64_t a_sf_rb = (int64_t)(p.K / 64) * 512;   // scale bytes per 128-row block
+  const int64_t r_sf_rb = (int64_t)(p.kpad / 64) * 512;
+
+  if (warp < 3) {
+    // ------------------------------------------------------------ producers
+    uint32_t it = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      const Tile tl = decode_tile(p, meta, t);
+      const int64_t brow = (int64_t)tl.e * p.N + tl.n0;
+      for (int j = 0; j < nst && ok; ++j, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        const Stage sg = stage_of(p, j, ncorr);
+        uint8_t* st = smem + s * STAGE_BYTES;
+        if (!warp_wait(&empty[s], ph ^ 1, sy)) { ok = false; break; }
+        if (warp == 0) trace_mark(p.trace, 0, it);
+        if (elect_one()) {
+          const int x = sg.kk * KSUB;
+          const CUtensorMap* ma = sg.corr ? &tmR : &tmA;
+          const CUtensorMap* mb = sg.corr ? &tmW : &tmB;
+          const int64_t rb = sg.corr ? r_sf_rb : a_sf_rb;
+          const uint32_t sfbytes = sg.ksteps * 512;
+          // warp 0: A rows 0-63, B rows 0-63, A's atoms; warp 1: A rows 64-127,
+          // B rows 64-127, B's atoms of rows 0-127; warp 2: B rows 128-255 and
+          // their atoms
+          for (int c = 0; c < 3; ++c) {
+            const int kind = warp == 2 ? (c < 2 ? 1 : 2) : c;   // 0: A box, 1: B box, 2: atoms
+            if (kind == 0) {
+              mbar_expect_tx(&full[s], BOX_BYTES);
+              tma_load_2d(st + warp * BOX_BYTES, ma, x, (int)(tl.m0 + warp * BOX_ROWS), &full[s]);
+            } else if (kind == 1) {
+              const int bb = warp == 2 ? 2 + c : warp;
+              mbar_expect_tx(&full[s], BOX_BYTES);
+              tma_load_2d(st + OFF_B + bb * BOX_BYTES, mb, x, (int)(brow + bb * BOX_ROWS), &full[s]);
+            } else {
+              const uint8_t* base = warp == 0 ? (sg.corr ? p.r_sf : p.a_sf) : (sg.corr ? p.ws_sf : p.b_sf);
+              const int64_t blk = warp == 0 ? tl.m0 / BM : brow / BM + (warp == 2 ? 1 : 0);
+              const uint8_t* src = base + blk * rb + (int64_t)sg.kk * 2048;
+              [[maybe_unused]] const int64_t lim = warp == 0 ? (sg.corr ? p.r_sf_bytes : p.a_sf_bytes)
+                                                              : (sg.corr ? p.ws_sf_bytes : p.b_sf_bytes);
+              if (!QDBGV(src - base + sfbytes <= lim,
+                         (tl.m0 << 20) | ((int64_t)tl.e << 8) | (sg.corr ? 2 : 0) | warp)) {
+                mbar_arrive(&full[s]);   // skipped copy: the stage still completes
+                continue;
+              }
+              mbar_expect_tx(&full[s], sfbytes);
+              bulk_load(st + (warp == 0 ? OFF_SFA : OFF_SFB + (warp == 2 ? 2048 : 0)), src, sfbytes,
+                        &full[s]);
+            }
+          }
+        }
+        __syncwarp();
+      }
+    }
+    if (!ok && lane == 0) {
+      // the copies this warp issued land before the CTA can exit (a fixed
+      // bounded time: a stage's barrier may never complete once another
+      // producer stopped before its share)
+      const unsigned long long t0 = global_ns();
+      while (global_ns() - t0 < kCopyDrainNs) {
+      }
+    }
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_nvf4(BM, BN);
+    uint32_t s = 0, sb = 0, sph = 0, mit = 0;
+    uint32_t j = 0;
+    bool ok = !p.skip_mma;
+    for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++j) {
+      // the epilogue has read the previous tile's accumulator
+      if (!conv_wait(acc_empty, (j & 1) ^ 1, sy)) { ok = false; break; }
+      tc_fence_after();
+      for (int q = 0; q < nst; ++q) {
+        const Stage sg = stage_of(p, q, ncorr);
+        if (q == ncorr && ncorr > 0) {
+          // the correction's partial sum is complete: the epilogue scales it
+          // by s_R / s_X in place before the main range accumulates on top
+          tc_commit_el(corr_full);
+          if (!conv_wait(prescaled, j & 1, sy)) { ok = false; break; }
+          tc_fence_after();
+        }
+        if (!conv_wait(&sf_ready[sb], sph, sy)) { ok = false; break; }
+        trace_mark(p.trace, 3, mit);
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
+        const uint32_t tsf = tmem + SF_COL + sb * SF_BUF_COLS;
+        // accumulate onto earlier stages, the prescaled correction included
+        const uint32_t acc = (q > 0) ? 1u : 0u;
+        if (sg.ksteps == 4) {
+          mma_x4(tmem, desc_sw128(sa), desc_sw128(sa + OFF_B), idesc, tsf, tsf + 16, acc);
+        } else {
+          for (int k = 0; k < sg.ksteps; ++k)
+            tc_mma_el(tmem, desc_sw128(sa + 32 * k), desc_sw128(sa + OFF_B + 32 * k), idesc,
+                      tsf + 4 * k, tsf + 16 + 8 * k, (acc || k > 0) ? 1u : 0u);
+        }
+        tc_commit_el(&empty[s]);   // also frees this stage's scale buffer
+        trace_mark(p.trace, 4, mit++);
+        if (++s == STAGES) s = 0;
+        if (++sb == SF_BUFS) { sb = 0; sph ^= 1; }
+      }
+      if (!ok) break;
+      tc_commit_el(acc_full);
+    }
+    tc_commit_el(drain_mma);
+    if (lane == 0) wait1(drain_mma, 0, dr, false, true);
+    __syncwarp();
+  } else if (warp >= SF_WARP0 && warp < EPI_WARP0) {
+    // ------------------------------------------------------------ scale staging
+    // TMEM buffer sb: K step q's A atom at column SF_COL + 48*sb + 4q, B's
+    // atoms of rows 0-127 and 128-255 at +16 + 8q and +20 + 8q (row r of an
+    // operand at lane r % 32, column r / 32, as the block-scaled MMA reads
+    // them).  Warp w copies K step w's three atoms once the stage has landed;
+    // buffer sb was last read by the MMAs of ring iteration it - SF_BUFS.
+    const int w = warp - SF_WARP0;
+    uint32_t s = 0, ph = 0, sb = 0, it = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      for (int q = 0; q < nst; ++q, ++it) {
+        bool okw = conv_wait(&full[s], ph, sy);
+        if (okw && it >= (uint32_t)SF_BUFS) {
+          const uint32_t prev = it - SF_BUFS;
+          okw = conv_wait(&empty[prev % STAGES], (prev / STAGES) & 1, sy);
+        }
+        if (!okw) { ok = false; break; }
+        if (w == 0) trace_mark(p.trace, 1, it);
+        tc_fence_after();
+        const Stage sg = stage_of(p, q, ncorr);
+        if (w < sg.ksteps) {
+          const uint32_t ss = smem_u32(smem + s * STAGE_BYTES);
+          const uint32_t tsf = tmem + SF_COL + sb * SF_BUF_COLS;
+          cp_atoms3(tsf + 4 * w, desc_sf(ss + OFF_SFA + 512 * w), tsf + 16 + 8 * w,
+                    desc_sf(ss + OFF_SFB + 512 * w), desc_sf(ss + OFF_SFB + 2048 + 512 * w));
+        }
+        tc_commit_el(&sf_ready[sb]);
+        if (w == 0) trace_mark(p.trace, 2, it);
+        if (++s == STAGES) { s = 0; ph ^= 1; }
+        if (++sb == SF_BUFS) sb = 0;
+      }
+    }
+    tc_commit_el(drain_sf);
+    if (lane == 0) wait1(drain_sf, 0, dr, false, true);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - EPI_WARP0;
+    const int quad = warp & 3;               // TMEM lane quadrant this warp may access
+    const int sub = ew >> 2;                 // which 64 of the tile's 256 columns
+    const int row_in_tile = quad * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const bool swiglu = p.out_mode == OUT_SWIGLU;
+    // this warp's accumulator columns: SwiGLU: 32 gate columns and the
+    // matching 32 up columns (tile columns [128b, 128b + 64) are gate rows of
+    // W, the next 64 the up rows); otherwise 64 consecutive columns
+    const int c_lo = swiglu ? 128 * (sub >> 1) + 32 * (sub & 1) : 64 * sub;
+    const int c_hi = swiglu ? c_lo + 64 : c_lo + 32;   // second half of the 64
+    uint32_t j = 0;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++j) {
+      const Tile tl = decode_tile(p, meta, t);
+      if (p.comp) {
+        if (!warp_wait(corr_full, j & 1, sy)) break;
+        tc_fence_after();
+        // all four loads, one wait, all four stores, one wait
+        const float ratio = meta.ratio[tl.e];
+        float w[64];
+        tc_ld16(tmem + lane_base + c_lo, w);
+        tc_ld16(tmem + lane_base + c_lo + 16, w + 16);
+        tc_ld16(tmem + lane_base + c_hi, w + 32);
+        tc_ld16(tmem + lane_base + c_hi + 16, w + 48);
+        tc_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 64; ++i) w[i] = __fmul_rn(ratio, w[i]);
+        tc_st16(tmem + lane_base + c_lo, w);
+        tc_st16(tmem + lane_base + c_lo + 16, w + 16);
+        tc_st16(tmem + lane_base + c_hi, w + 32);
+        tc_st16(tmem + lane_base + c_hi + 16, w + 48);
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(prescaled);
+      }
+      if (!warp_wait(acc_full, j & 1, sy)) break;
+      if (warp == EPI_WARP0) trace_mark(p.trace, 5, j);
+      tc_fence_after();
+      float v[64];
+      tc_ld16(tmem + lane_base + c_lo, v);
+      tc_ld16(tmem + lane_base + c_lo + 16, v + 16);
+      tc_ld16(tmem + lane_base + c_hi, v + 32);
+      tc_ld16(tmem + lane_base + c_hi + 16, v + 48);
+      tc_wait_ld();
+      // the accumulator is read: release it before the math and the stores
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+      const float a1 = meta.a1[tl.e];
+      const int64_t row = tl.m0 + row_in_tile;
+      float amax = 0.0f;
+      if (swiglu) {
+        const bool store = row < (p.row_off ? (int64_t)meta.off[tl.e + 1] : p.M) && QDBG(row < p.y_rows);
+        // v[0..31]: gate columns, v[32..63]: the matching up columns
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float h[2];
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const float g = a1 * v[i + q], u = a1 * v[32 + i + q];
+            h[q] = __fdividef(g * u, 1.0f + __expf(-g));   // silu(g) * u
+          }
+          __nv_bfloat162 hb = __floats2bfloat162_rn(h[0], h[1]);
+          packed[i / 2] = *reinterpret_cast<uint32_t*>(&hb);
+          const float2 hr = __bfloat1622float2(hb);
+          amax = fmaxf(amax, fmaxf(fabsf(hr.x), fabsf(hr.y)));
+        }
+        if (store) {
+          __nv_bfloat16* y = (__nv_bfloat16*)p.y + row * p.ldy + tl.n0 / 2 + 64 * (sub >> 1) + 32 * (sub & 1);
+          if (p.st32) {
+            st_global_32B(y, packed);
+            st_global_32B(y + 16, packed + 8);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(y);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+          }
+        } else {
+          amax = 0.0f;
+        }
+      } else {
+        const bool store = row < tl.row_end && QDBG(row < p.y_rows);
+        if (store) {
+          if (p.out_mode == OUT_F32) {
+            float* yrow = (float*)p.y + row * p.ldy + tl.n0 + 64 * sub;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) v[i] = a1 * v[i];
+            if (p.st32) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) st_global_32B(yrow + 8 * i, reinterpret_cast<const uint32_t*>(v + 8 * i));
+            } else {
+              float4* dst = reinterpret_cast<float4*>(yrow);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            }
+#pragma unroll
+            for (int i = 0; i < 64; ++i) amax = fmaxf(amax, fabsf(v[i]));
+          } else {
+            uint32_t packed[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              __nv_bfloat162 hb = __floats2bfloat162_rn(a1 * v[2 * i], a1 * v[2 * i + 1]);
+              packed[i] = *reinterpret_cast<uint32_t*>(&hb);
+              const float2 hr = __bfloat1622float2(hb);
+              amax = fmaxf(amax, fmaxf(fabsf(hr.x), fabsf(hr.y)));
+            }
+            __nv_bfloat16* yrow = (__nv_bfloat16*)p.y + row * p.ldy + tl.n0 + 64 * sub;
+            if (p.st32) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) st_global_32B(yrow + 16 * i, packed + 8 * i);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(yrow);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (warp == EPI_WARP0) trace_mark(p.trace, 6, j);
+      if (p.y_amax) {
+        amax = warp_max(amax);
+        if (lane == 0 && amax > 0.0f) atomicMax(&p.y_amax[tl.e], __float_as_uint(amax));
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+  }
+}
+
+}  // namespace wide
+
 // ---------------------------------------------------------------- Q(W_sel)
 // Column-major copy of an NVFP4 weight, made once per weight update: for group
 // g (rows g*N .. g*N+N-1), codes_t[g][c][n/2] holds the codes of rows n, n+1 at
@@ -1742,6 +2240,8 @@ static std::atomic<int> g_wait_test{0};
 static std::atomic<unsigned long long*> g_trace{nullptr};
 // The CTA-pair kernel, selectable for comparison (QUADS_GEMM_PAIR=1); the
 // one-CTA kernel measured faster on every benchmark shape and is the default.
+// Tile width policy (quads_set_gemm_tile_policy).
+static std::atomic<int> g_tile_policy{QUADS_GEMM_TILES_AUTO};
 static const bool g_pair_kernel = [] {
   const char* v = getenv("QUADS_GEMM_PAIR");
   return v && v[0] == '1';
@@ -1849,6 +2349,9 @@ static quads_status_t launch(const Launch& L) {
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(pair::pair_gemm_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(wide::wide_gemm_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, wide::SMEM_BYTES);
       if (e != cudaSuccess) {
         errp_dev[dev] = nullptr;
         return fail(QUADS_ERR_CUDA, "gemm: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -1877,6 +2380,30 @@ static quads_status_t launch(const Launch& L) {
     max_pairs = pairs_dev[dev];
   }
   const bool wait_test = g_wait_test.exchange(0) != 0;
+  const int policy = g_tile_policy.load();
+  if (!g_pair_kernel && !L.mx && L.N % wide::BN == 0 &&
+      (policy == QUADS_GEMM_TILES_256 || (policy == QUADS_GEMM_TILES_AUTO && !comp))) {
+    Params p;
+    p.E = L.E; p.N = L.N; p.K = L.K; p.kpad = comp ? L.kpad : 0; p.Nt = L.N / wide::BN;
+    p.M = L.M; p.row_off = L.row_off; p.row_cnt = L.row_cnt;
+    p.a_sf = L.a_sf; p.b_sf = L.b_sf; p.r_sf = L.r_sf; p.ws_sf = ws_sf;
+    p.a_ts = L.a_ts; p.b_ts = L.b_ts; p.r_ts = L.r_ts; p.a_ts_pe = L.a_pe; p.r_ts_pe = L.r_pe;
+    p.comp = comp ? 1 : 0;
+    p.mx = 0;
+    p.y = L.y; p.ldy = L.ldy; p.out_mode = L.out_mode;
+    p.st32 = st32;
+    p.y_amax = (uint32_t*)L.y_amax;
+    p.err = errp;
+    p.a_sf_bytes = ext.a; p.b_sf_bytes = ext.b; p.r_sf_bytes = ext.r; p.ws_sf_bytes = ext.w;
+    p.y_rows = arows;
+    p.timeout_ns = wait_test ? 1000000ull : kTimeoutNs;
+    p.skip_mma = wait_test ? 1 : 0;
+    p.trace = g_trace.exchange(nullptr);
+    int64_t grid = num_sms();
+    if (!L.row_off) grid = std::min<int64_t>(grid, ((L.M + wide::BM - 1) / wide::BM) * p.Nt);
+    wide::wide_gemm_kernel<<<(int)grid, wide::NUM_THREADS, wide::SMEM_BYTES, L.stream>>>(tA, tB, tR, tW, p);
+    return check_launch("gemm", launches);
+  }
   if (!g_pair_kernel) {
     Params p;
     p.E = L.E; p.N = L.N; p.K = L.K; p.kpad = comp ? L.kpad : 0; p.Nt = L.N / BN;
@@ -2114,6 +2641,13 @@ extern "C" quads_status_t quads_mx_gemm(int64_t M, int64_t N, int64_t K, const u
 }
 
 extern "C" void quads_test_gemm_wait_timeout(int32_t enable) { gemm::gemm_wait_test(enable); }
+
+extern "C" int32_t quads_set_gemm_tile_policy(int32_t policy) {
+  if (policy != QUADS_GEMM_TILES_AUTO && policy != QUADS_GEMM_TILES_128 &&
+      policy != QUADS_GEMM_TILES_256)
+    return -1;
+  return gemm::g_tile_policy.exchange(policy);
+}
 
 extern "C" void quads_test_gemm_timeline(uint64_t* device_buffer) {
   gemm::gemm_timeline(reinterpret_cast<unsigned long long*>(device_buffer));

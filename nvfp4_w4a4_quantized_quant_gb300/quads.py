@@ -34,6 +34,7 @@ _SIGS = {
     "quads_device_status": (_I32, [_P, ctypes.POINTER(_I32)]),
     "quads_test_gemm_wait_timeout": (None, [_I32]),
     "quads_test_gemm_timeline": (None, [_P]),
+    "quads_set_gemm_tile_policy": (ctypes.c_int32, [ctypes.c_int32]),
     "quads_workspace_size": (_SZ, [_I32, _I64, _I64, _I64, _I32, _I32]),
     "quads_kpad": (_I32, [_I32]),
     "quads_quantize_nvfp4": (_I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P, _I64, _P,
@@ -167,6 +168,19 @@ def test_gemm_timeline(buf: torch.Tensor) -> None:
     timeline (int64 [7, 64], %globaltimer ns) into `buf`."""
     assert buf.dtype == torch.int64 and buf.numel() >= 7 * 64 and buf.is_cuda
     load().quads_test_gemm_timeline(_ptr(buf))
+
+
+TILES_AUTO, TILES_128, TILES_256 = 0, 1, 2
+
+
+def set_gemm_tile_policy(policy: int) -> int:
+    """GEMM output tile width, process-wide (TILES_AUTO: 128x256 for plain
+    products with N % 256 == 0; TILES_128; TILES_256: also compensated
+    products).  Returns the previous policy."""
+    prev = load().quads_set_gemm_tile_policy(int(policy))
+    if prev < 0:
+        raise ValueError(f"unknown GEMM tile policy {policy}")
+    return prev
 
 
 @dataclass

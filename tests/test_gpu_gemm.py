@@ -209,3 +209,38 @@ def test_gemm_wait_timeout_is_reported_and_the_device_stays_usable(lib):
     assert lib.device_status() == 0
     Y, B, _, _ = _oracle(d["x"], d["w"], d["k"], comp=False)
     _check(y, Y, B, False)
+
+
+@pytest.mark.parametrize("policy", [1, 2])
+@pytest.mark.parametrize("M,N,K,k,comp", [(200, 256, 320, 48, True), (384, 512, 768, 64, True),
+                                          (129, 768, 1024, 256, True), (300, 256, 512, 16, False),
+                                          (64, 256, 64, 64, True)])
+def test_tile_policies_match_the_oracle(lib, policy, M, N, K, k, comp):
+    """Both tile widths on shapes whose N allows 256-wide tiles: 128x128 for
+    everything (policy 1), 128x256 with the correction folded into the single
+    accumulator by scaling its partial sum in tensor memory (policy 2)."""
+    rng = inputs.make_rng(M * 3 + N + K + policy)
+    xb = inputs.f32_to_bf16_bits(inputs.student_t4(rng, (M, K)))
+    wb = inputs.f32_to_bf16_bits(rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02))
+    prev = lib.set_gemm_tile_policy(policy)
+    try:
+        y, sel, _ = _run(lib, xb, wb, k, torch.float32, comp=comp)
+        torch.cuda.synchronize()
+        assert lib.device_status() == 0
+    finally:
+        lib.set_gemm_tile_policy(prev)
+    if comp:
+        Y, B, ref, _ = _oracle(xb, wb, k)
+        assert np.array_equal(sel.cpu().numpy(), ref["sel"])
+    else:
+        Y, B, _, _ = _oracle(xb, wb, k, comp=False)
+    _check(y, Y, B, False)
+
+
+def test_tile_policy_rejects_unknown_values(lib):
+    prev = lib.set_gemm_tile_policy(0)
+    try:
+        with pytest.raises(ValueError):
+            lib.set_gemm_tile_policy(7)
+    finally:
+        lib.set_gemm_tile_policy(prev)
