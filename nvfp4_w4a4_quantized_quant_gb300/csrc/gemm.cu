@@ -56,36 +56,12 @@
 namespace quads {
 namespace gemm {
 
-// Stage geometry (sub-tiles per stage, ring stages, TMEM scale buffers); the
-// build may override it to compare variants.
-#ifndef QUADS_GEMM_KSUBS
-#define QUADS_GEMM_KSUBS 2
-#endif
-#ifndef QUADS_GEMM_STAGES
-#define QUADS_GEMM_STAGES 3
-#endif
-#ifndef QUADS_GEMM_SF_BUFS
-#define QUADS_GEMM_SF_BUFS 2
-#endif
 constexpr int BM = 128, BN = 128;
 constexpr int KSUB = 128;                     // bytes per row of one 128B-swizzled sub-tile (256 FP4)
-constexpr int KSUBS = QUADS_GEMM_KSUBS;       // sub-tiles per stage: K tile = 256 * KSUBS FP4
-constexpr int KSTEPS = 4 * KSUBS;             // K=64 MMA steps per stage
-constexpr int KTILE = 256 * KSUBS;            // FP4 elements per stage
-constexpr int STAGES = QUADS_GEMM_STAGES;
 constexpr int A_SUB = BM * KSUB;              // 16 KB
 constexpr int B_SUB = BN * KSUB;              // 16 KB
-constexpr int A_TILE = A_SUB * KSUBS;
-constexpr int B_TILE = B_SUB * KSUBS;
-constexpr int SF_TILE = KSTEPS * 512;         // scale atoms (128 rows x 4 blocks each) per operand
-constexpr int STAGE_BYTES = A_TILE + B_TILE + 2 * SF_TILE;  // 72 KB
 constexpr int BOX_ROWS = 64;                  // rows per TMA box: half a 128-row sub-tile
 constexpr int BOX_BYTES = BOX_ROWS * KSUB;    // 8 KB
-constexpr int BOXES = 2 * KSUBS * 2;          // per stage: (A, B) x sub-tiles x halves
-constexpr int COPIES = BOXES + 2;             // + the SFA and SFB atom runs (bulk copies)
-constexpr int SF_BUFS = QUADS_GEMM_SF_BUFS;   // TMEM scale buffers
-constexpr int SF_BUF_COLS = 2 * 4 * KSTEPS;   // SFA and SFB: four columns per K step each
-static_assert(SF_BUFS * SF_BUF_COLS <= 128, "scale buffers fit the 128 TMEM columns left");
 constexpr int PRODUCERS = 3;
 constexpr int NUM_THREADS = 512;  // 16 warps: 3 producers, MMA, 4 scale staging, 8 epilogue
 constexpr int EPI_THREADS = 256;
@@ -96,10 +72,36 @@ constexpr int ACC2_COL = 256;
 constexpr int SF_COL = 384;
 constexpr int MAX_GROUPS = 256;                 // experts cached in shared memory
 constexpr int META_BYTES = 1024 + 4 * (MAX_GROUPS + 1) + 4 * 4 * MAX_GROUPS;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + META_BYTES + 1024 /*align*/;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per wait
-// the stage's copies dealt to the producer warps: warp w issues [first, first + count)
-__host__ __device__ constexpr int copies_first(int w) { return w * COPIES / PRODUCERS; }
+
+// Stage geometry of the 128x128-tile kernel: KS 256-element sub-tiles per
+// stage, NS ring stages, NSF TMEM scale buffers.  Two are instantiated: 512-
+// element stages (three of 72 KB, two scale buffers) and 256-element stages
+// (six of 36 KB, four buffers), the latter for K not a multiple of 512, where
+// a 512-element ring would carry half-empty stages (K = 768: 158 -> 144 us
+// for the compensated GEMM2 shape; K = 2048 runs faster on 512).
+template <int KS, int NS, int NSF>
+struct Geo {
+  static constexpr int KSUBS = KS;                     // sub-tiles per stage
+  static constexpr int KSTEPS = 4 * KS;                // K=64 MMA steps per stage
+  static constexpr int KTILE = 256 * KS;               // FP4 elements per stage
+  static constexpr int STAGES = NS;
+  static constexpr int A_TILE = A_SUB * KS;
+  static constexpr int B_TILE = B_SUB * KS;
+  static constexpr int SF_TILE = KSTEPS * 512;         // scale atoms (128 rows x 4 blocks each) per operand
+  static constexpr int STAGE_BYTES = A_TILE + B_TILE + 2 * SF_TILE;
+  static constexpr int BOXES = 2 * KS * 2;             // per stage: (A, B) x sub-tiles x halves
+  static constexpr int COPIES = BOXES + 2;             // + the SFA and SFB atom runs (bulk copies)
+  static constexpr int SF_BUFS = NSF;                  // TMEM scale buffers
+  static constexpr int SF_BUF_COLS = 2 * 4 * KSTEPS;   // SFA and SFB: four columns per K step each
+  static constexpr int SMEM_BYTES = NS * STAGE_BYTES + META_BYTES + 1024 /*align*/;
+  static_assert(NSF * SF_BUF_COLS <= 128, "scale buffers fit the 128 TMEM columns left");
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+  // the stage's copies dealt to the producer warps: warp w issues [first, first + count)
+  __host__ __device__ static constexpr int copies_first(int w) { return w * COPIES / PRODUCERS; }
+};
+using Geo512 = Geo<2, 3, 2>;
+using Geo256 = Geo<1, 6, 4>;
 
 enum { OUT_F32 = 0, OUT_BF16 = 1, OUT_SWIGLU = 2 };
 
@@ -500,24 +502,25 @@ __device__ __forceinline__ Tile decode_tile(const Params& p, const Meta& m, int6
 }
 
 // ---------------------------------------------------------------- the kernel
+template <class G>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmW,
                 const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES);
-  uint64_t* full = bars;                           // [STAGES]
-  uint64_t* empty = full + STAGES;                 // [STAGES]
-  uint64_t* sf_ready = empty + STAGES;             // [SF_BUFS]
-  uint64_t* acc_full = sf_ready + SF_BUFS;         // [2]
+  uint64_t* bars = (uint64_t*)(smem + G::STAGES * G::STAGE_BYTES);
+  uint64_t* full = bars;                           // [G::STAGES]
+  uint64_t* empty = full + G::STAGES;                 // [G::STAGES]
+  uint64_t* sf_ready = empty + G::STAGES;             // [G::SF_BUFS]
+  uint64_t* acc_full = sf_ready + G::SF_BUFS;         // [2]
   uint64_t* acc_empty = acc_full + 2;              // [2]
   uint64_t* drain_mma = acc_empty + 2;
   uint64_t* drain_sf = drain_mma + 1;
   uint32_t* tmem_holder = (uint32_t*)(drain_sf + 1);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
   Meta meta;
-  meta.off = (int32_t*)(smem + STAGES * STAGE_BYTES + 1024);
+  meta.off = (int32_t*)(smem + G::STAGES * G::STAGE_BYTES + 1024);
   meta.cnt = meta.off + (MAX_GROUPS + 1);
   meta.a1 = (float*)(meta.cnt + MAX_GROUPS);
   meta.a2 = meta.a1 + MAX_GROUPS;
@@ -536,8 +539,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0 && p.row_off) meta.off[p.E] = p.row_off[p.E];
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) { mbar_init(&full[i], COPIES); mbar_init(&empty[i], 1); }
-    for (int i = 0; i < SF_BUFS; ++i) mbar_init(&sf_ready[i], SF_WARPS);
+    for (int i = 0; i < G::STAGES; ++i) { mbar_init(&full[i], G::COPIES); mbar_init(&empty[i], 1); }
+    for (int i = 0; i < G::SF_BUFS; ++i) mbar_init(&sf_ready[i], SF_WARPS);
     for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], EPI_THREADS); }
     mbar_init(drain_mma, 1);
     mbar_init(drain_sf, SF_WARPS);
@@ -559,11 +562,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const Sync dr{abort_flag, p.err, kDrainNs};
 
   const int64_t ntiles = total_tiles(p, meta);
-  const int KT = (p.K + KTILE - 1) / KTILE;
-  const int KTc = p.comp ? (p.kpad + KTILE - 1) / KTILE : 0;
+  const int KT = (p.K + G::KTILE - 1) / G::KTILE;
+  const int KTc = p.comp ? (p.kpad + G::KTILE - 1) / G::KTILE : 0;
   // scale bytes per 128-row block and per stage (MXFP4: one scale per 32 elements)
   const int64_t a_sf_rb = (int64_t)(p.K / (p.mx ? 128 : 64)) * 512;
-  const int sf_stage = p.mx ? SF_TILE / 2 : SF_TILE;
+  const int sf_stage = p.mx ? G::SF_TILE / 2 : G::SF_TILE;
   const int64_t r_sf_rb = (int64_t)(p.kpad / 64) * 512;
 
   if (warp < PRODUCERS) {
@@ -576,22 +579,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // bytes, or without any when the stage's K range ends before its
     // sub-tile).  The whole warp runs the loop (so addresses and coordinates
     // stay warp-uniform); one elected lane issues.
-    const int b_lo = copies_first(warp);
-    const int b_hi = copies_first(warp + 1);
+    const int b_lo = G::copies_first(warp);
+    const int b_hi = G::copies_first(warp + 1);
     uint32_t it = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       const Tile tl = decode_tile(p, meta, t);
       const int64_t brow = (int64_t)tl.e * p.N + tl.n0;
       for (int kt = 0; kt < KT + KTc && ok; ++kt, ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
+        const int s = it % G::STAGES;
+        const uint32_t ph = (it / G::STAGES) & 1;
         const bool corr = kt >= KT;
         const int kk = corr ? kt - KT : kt;
         const int klen = corr ? p.kpad : p.K;
-        const int ksteps = min(KSTEPS, (klen - kk * KTILE) / 64);
+        const int ksteps = min(G::KSTEPS, (klen - kk * G::KTILE) / 64);
         const int nsub = (ksteps + 3) >> 2;   // 128-byte sub-tiles holding real columns
-        uint8_t* st = smem + s * STAGE_BYTES;
+        uint8_t* st = smem + s * G::STAGE_BYTES;
         const CUtensorMap* ma = corr ? &tmR : &tmA;
         const CUtensorMap* mb = corr ? &tmW : &tmB;
         const uint8_t* sfa = corr ? p.r_sf + (tl.m0 / BM) * r_sf_rb : p.a_sf + (tl.m0 / BM) * a_sf_rb;
@@ -600,29 +603,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (warp == 0) trace_mark(p.trace, 0, it);
         if (elect_one()) {
           for (int b = b_lo; b < b_hi; ++b) {
-            if (b >= BOXES) {
+            if (b >= G::BOXES) {
               const uint32_t sfbytes = (p.mx ? ksteps / 2 : ksteps) * 512;
-              const uint8_t* src = (b == BOXES ? sfa : sfb) + kk * sf_stage;
+              const uint8_t* src = (b == G::BOXES ? sfa : sfb) + kk * sf_stage;
               [[maybe_unused]] const uint8_t* base =
-                  b == BOXES ? (corr ? p.r_sf : p.a_sf) : (corr ? p.ws_sf : p.b_sf);
-              [[maybe_unused]] const int64_t lim = b == BOXES ? (corr ? p.r_sf_bytes : p.a_sf_bytes)
+                  b == G::BOXES ? (corr ? p.r_sf : p.a_sf) : (corr ? p.ws_sf : p.b_sf);
+              [[maybe_unused]] const int64_t lim = b == G::BOXES ? (corr ? p.r_sf_bytes : p.a_sf_bytes)
                                                               : (corr ? p.ws_sf_bytes : p.b_sf_bytes);
               if (!QDBGV(src >= base && src - base + sfbytes <= lim,
-                         (tl.m0 << 20) | ((int64_t)tl.e << 8) | (corr ? 2 : 0) | (b == BOXES ? 0 : 4))) {
+                         (tl.m0 << 20) | ((int64_t)tl.e << 8) | (corr ? 2 : 0) | (b == G::BOXES ? 0 : 4))) {
                 mbar_arrive(&full[s]);   // skipped copy: the stage still completes
                 continue;
               }
               mbar_expect_tx(&full[s], sfbytes);
-              if (b == BOXES) bulk_load(st + A_TILE + B_TILE, src, sfbytes, &full[s]);
-              else bulk_load(st + A_TILE + B_TILE + SF_TILE, src, sfbytes, &full[s]);
+              if (b == G::BOXES) bulk_load(st + G::A_TILE + G::B_TILE, src, sfbytes, &full[s]);
+              else bulk_load(st + G::A_TILE + G::B_TILE + G::SF_TILE, src, sfbytes, &full[s]);
               continue;
             }
             const int u = b >> 2, isb = (b >> 1) & 1, hf = b & 1;
             if (u < nsub) {
               mbar_expect_tx(&full[s], BOX_BYTES);
-              const int x = kk * (KSUB * KSUBS) + u * KSUB;
+              const int x = kk * (KSUB * G::KSUBS) + u * KSUB;
               if (isb)
-                tma_load_2d(st + A_TILE + u * B_SUB + hf * BOX_BYTES, mb, x,
+                tma_load_2d(st + G::A_TILE + u * B_SUB + hf * BOX_BYTES, mb, x,
                             (int)(brow + hf * BOX_ROWS), &full[s]);
               else
                 tma_load_2d(st + u * A_SUB + hf * BOX_BYTES, ma, x, (int)(tl.m0 + hf * BOX_ROWS),
@@ -671,33 +674,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         trace_mark(p.trace, 3, mit);
         tc_fence_after();
         const int klen = corr ? p.kpad : p.K;
-        const int ksteps = min(KSTEPS, (klen - kk * KTILE) / 64);
-        const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-        const uint32_t sbb = sa + A_TILE;
-        const uint32_t tsf = tmem + SF_COL + sb * SF_BUF_COLS;
+        const int ksteps = min(G::KSTEPS, (klen - kk * G::KTILE) / 64);
+        const uint32_t sa = smem_u32(smem + s * G::STAGE_BYTES);
+        const uint32_t sbb = sa + G::A_TILE;
+        const uint32_t tsf = tmem + SF_COL + sb * G::SF_BUF_COLS;
         const uint32_t dcol = corr ? (tmem + ACC2_COL) : (tmem + b * BN);
         if (p.mx) {
           for (int q = 0; q < ksteps; ++q) {
             const uint32_t off = (q >> 2) * A_SUB + (q & 3) * 32;
             const uint32_t id = (q & 1) ? idesc_mxf4(BM, BN, 2) : idesc_mxf4(BM, BN, 0);
             tc_mma_mx_el(dcol, desc_sw128(sa + off), desc_sw128(sbb + off), id,
-                         tsf + (q >> 1) * 4, tsf + 4 * KSTEPS + (q >> 1) * 4,
+                         tsf + (q >> 1) * 4, tsf + 4 * G::KSTEPS + (q >> 1) * 4,
                          (kk > 0 || q > 0) ? 1u : 0u);
           }
-        } else if (KSTEPS == 8 && ksteps == 8) {
-          tc_mma_stage8(dcol, desc_sw128(sa), desc_sw128(sbb), idesc, tsf, tsf + 4 * KSTEPS,
+        } else if (G::KSTEPS == 8 && ksteps == 8) {
+          tc_mma_stage8(dcol, desc_sw128(sa), desc_sw128(sbb), idesc, tsf, tsf + 4 * G::KSTEPS,
                         kk > 0 ? 1u : 0u);
         } else {
           for (int q = 0; q < ksteps; ++q) {
             const uint32_t off = (q >> 2) * A_SUB + (q & 3) * 32;
             tc_mma_el(dcol, desc_sw128(sa + off), desc_sw128(sbb + off), idesc, tsf + q * 4,
-                      tsf + 4 * KSTEPS + q * 4, (kk > 0 || q > 0) ? 1u : 0u);
+                      tsf + 4 * G::KSTEPS + q * 4, (kk > 0 || q > 0) ? 1u : 0u);
           }
         }
         tc_commit_el(&empty[s]);   // also frees this stage's scale buffer
         trace_mark(p.trace, 4, mit++);
-        if (++s == STAGES) s = 0;
-        if (++sb == SF_BUFS) { sb = 0; sph ^= 1; }
+        if (++s == G::STAGES) s = 0;
+        if (++sb == G::SF_BUFS) { sb = 0; sph ^= 1; }
       }
       if (!ok) break;
       tc_commit_el(&acc_full[b]);
@@ -714,7 +717,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // four scales at lane r % 32, column r / 32).  Warp w copies the atoms of
     // K steps 2w and 2w+1.  The warps wait for the stage's TMA data, so
     // sf_ready alone tells the MMA warp that the stage is complete.
-    // Scale buffer sb was last read by the MMAs of ring iteration it - SF_BUFS,
+    // Scale buffer sb was last read by the MMAs of ring iteration it - G::SF_BUFS,
     // whose completion the MMA warp signals on that stage's empty barrier.
     const int w = warp - SF_WARP0;
     uint32_t s = 0, ph = 0, sb = 0, it = 0;
@@ -722,9 +725,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       for (int kt = 0; kt < KT + KTc; ++kt, ++it) {
         bool okw = conv_wait(&full[s], ph, sy);
-        if (okw && it >= (uint32_t)SF_BUFS) {
-          const uint32_t prev = it - SF_BUFS;
-          okw = conv_wait(&empty[prev % STAGES], (prev / STAGES) & 1, sy);
+        if (okw && it >= (uint32_t)G::SF_BUFS) {
+          const uint32_t prev = it - G::SF_BUFS;
+          okw = conv_wait(&empty[prev % G::STAGES], (prev / G::STAGES) & 1, sy);
         }
         if (!okw) {
           ok = false;
@@ -735,32 +738,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool corr = kt >= KT;
         const int kk = corr ? kt - KT : kt;
         const int klen = corr ? p.kpad : p.K;
-        const int ksteps = min(KSTEPS, (klen - kk * KTILE) / 64);
-        const uint32_t ssf = smem_u32(smem + s * STAGE_BYTES + A_TILE + B_TILE);
-        const uint32_t tsf = tmem + SF_COL + sb * SF_BUF_COLS;
+        const int ksteps = min(G::KSTEPS, (klen - kk * G::KTILE) / 64);
+        const uint32_t ssf = smem_u32(smem + s * G::STAGE_BYTES + G::A_TILE + G::B_TILE);
+        const uint32_t tsf = tmem + SF_COL + sb * G::SF_BUF_COLS;
         if (p.mx) {
           // MXFP4: one atom covers two K steps; warp w copies atom w
           if (2 * w < ksteps) {
             tc_cp_sf_el(tsf + w * 4, desc_sf(ssf + w * 512));
-            tc_cp_sf_el(tsf + 4 * KSTEPS + w * 4, desc_sf(ssf + SF_TILE + w * 512));
+            tc_cp_sf_el(tsf + 4 * G::KSTEPS + w * 4, desc_sf(ssf + G::SF_TILE + w * 512));
           }
-        } else if (KSTEPS == 2 * SF_WARPS && 4 * KSTEPS == 32 && 2 * w + 1 < ksteps) {
+        } else if (G::KSTEPS == 2 * SF_WARPS && 4 * G::KSTEPS == 32 && 2 * w + 1 < ksteps) {
           const int q = 2 * w;
-          tc_cp_sf_pair_el(tsf + q * 4, desc_sf(ssf + q * 512), desc_sf(ssf + SF_TILE + q * 512));
+          tc_cp_sf_pair_el(tsf + q * 4, desc_sf(ssf + q * 512), desc_sf(ssf + G::SF_TILE + q * 512));
         } else {
 #pragma unroll
-          for (int i = 0; i < KSTEPS / SF_WARPS; ++i) {
-            const int q = w * (KSTEPS / SF_WARPS) + i;
+          for (int i = 0; i < G::KSTEPS / SF_WARPS; ++i) {
+            const int q = w * (G::KSTEPS / SF_WARPS) + i;
             if (q < ksteps) {
               tc_cp_sf_el(tsf + q * 4, desc_sf(ssf + q * 512));
-              tc_cp_sf_el(tsf + 4 * KSTEPS + q * 4, desc_sf(ssf + SF_TILE + q * 512));
+              tc_cp_sf_el(tsf + 4 * G::KSTEPS + q * 4, desc_sf(ssf + G::SF_TILE + q * 512));
             }
           }
         }
         tc_commit_el(&sf_ready[sb]);
         if (w == 0) trace_mark(p.trace, 2, it);
-        if (++s == STAGES) { s = 0; ph ^= 1; }
-        if (++sb == SF_BUFS) sb = 0;
+        if (++s == G::STAGES) { s = 0; ph ^= 1; }
+        if (++sb == G::SF_BUFS) sb = 0;
       }
     }
     // the scale copies this warp issued complete before TMEM goes away
@@ -2344,8 +2347,12 @@ static quads_status_t launch(const Launch& L) {
         errp_dev[dev] = nullptr;
         return fail(QUADS_ERR_CUDA, "gemm: cannot resolve the device error word");
       }
-      cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           SMEM_BYTES);
+      cudaError_t e = cudaFuncSetAttribute(gemm_kernel<Geo512>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           Geo512::SMEM_BYTES);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_kernel<Geo256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Geo256::SMEM_BYTES);
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(pair::pair_gemm_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
@@ -2423,7 +2430,11 @@ static quads_status_t launch(const Launch& L) {
     p.trace = g_trace.exchange(nullptr);
     int64_t grid = num_sms();
     if (!L.row_off) grid = std::min<int64_t>(grid, ((L.M + BM - 1) / BM) * (L.N / BN));
-    gemm_kernel<<<(int)grid, NUM_THREADS, SMEM_BYTES, L.stream>>>(tA, tB, tR, tW, p);
+    // 256-element stages when K leaves a 512-element ring with a half-empty stage
+    if (L.K % 512)
+      gemm_kernel<Geo256><<<(int)grid, NUM_THREADS, Geo256::SMEM_BYTES, L.stream>>>(tA, tB, tR, tW, p);
+    else
+      gemm_kernel<Geo512><<<(int)grid, NUM_THREADS, Geo512::SMEM_BYTES, L.stream>>>(tA, tB, tR, tW, p);
     return check_launch("gemm", launches);
   }
   pair::Params p;
