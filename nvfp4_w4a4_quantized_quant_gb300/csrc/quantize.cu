@@ -403,42 +403,46 @@ __global__ void __launch_bounds__(256) score_chain_kernel(const float* __restric
 
 
 // Top-k of `cols` keys held PER per thread by a block of NT threads (key i of
-// thread t is channel t + i*NT): radix selection on the bit patterns (scores
+// thread t is channel t*PER + i): radix selection on the bit patterns (scores
 // are >= 0, so the unsigned order of the bits is the float order) finds the
 // k-th largest key T byte by byte; the channels with key > T and the
 // lowest-index channels with key == T are written to sel_out in ascending
-// order.  Shared scratch: hist[256], *s_prefix, *s_need, warp_sums[NT/32].
+// order.  Each of the four byte passes has its own histogram (zeroed up
+// front), so a pass costs two block barriers (histogram complete; warp 0 has
+// found the byte); the output positions come from one block-wide scan of the
+// per-thread (key > T, key == T) counts.  Shared scratch: hist[4*256],
+// warp_tot[NT/32], dn[2].
 template <int NT, int PER>
 __device__ __forceinline__ void block_topk(const uint32_t (&key)[PER], int cols, int k,
-                                           int32_t* sel_out, int* hist, uint32_t* s_prefix,
-                                           int* s_need, int* warp_sums) {
+                                           int32_t* sel_out, int* hist, int* warp_tot, int* dn) {
   constexpr int NW = NT / 32;
-  if (threadIdx.x == 0) { *s_prefix = 0u; *s_need = k; }
-  uint32_t mask_hi = 0u;  // bits already fixed in *s_prefix
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += NT) hist[i] = 0;
-    __syncthreads();
-    const uint32_t prefix = *s_prefix;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < 4 * 256; i += NT) hist[i] = 0;
+  __syncthreads();
+  uint32_t prefix = 0u, mask_hi = 0u;   // bytes fixed so far
+  int need = k;                         // how many of the keys matching prefix are still taken
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    int* h = hist + 256 * pass;
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
-      const int c = threadIdx.x + i * NT;
-      if (c < cols && (key[i] & mask_hi) == prefix) atomicAdd(&hist[(key[i] >> shift) & 255u], 1);
+      const int c = threadIdx.x * PER + i;
+      if (c < cols && (key[i] & mask_hi) == prefix) atomicAdd(&h[(key[i] >> shift) & 255u], 1);
     }
     __syncthreads();
-    if (threadIdx.x < 32) {
-      // warp 0: lane l owns bins 255-8l .. 248-8l (descending); find the bin in
-      // which the running count from the top reaches `need`
-      const int lane = threadIdx.x;
+    if (w == 0) {
+      // lane l owns bins 255-8l .. 248-8l (descending); the bin in which the
+      // running count from the top reaches `need` holds the k-th key
       int c8[8], lsum = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) { c8[i] = hist[255 - 8 * lane - i]; lsum += c8[i]; }
+      for (int i = 0; i < 8; ++i) { c8[i] = h[255 - 8 * lane - i]; lsum += c8[i]; }
       int incl = lsum;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int u = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += u;
       }
-      const int need = *s_need;
       const int excl = incl - lsum;
       const unsigned found = __ballot_sync(0xffffffffu, excl < need && incl >= need);
       if (lane == __ffs(found) - 1) {
@@ -447,43 +451,52 @@ __device__ __forceinline__ void block_topk(const uint32_t (&key)[PER], int cols,
           if (c8[i] >= nd) break;
           nd -= c8[i];
         }
-        *s_need = nd;
-        *s_prefix = prefix | ((uint32_t)(255 - 8 * lane - i) << shift);
+        dn[0] = 255 - 8 * lane - i;
+        dn[1] = nd;
       }
     }
+    __syncthreads();
+    // dn is rewritten only after the next pass's first barrier, which every
+    // thread reaches after this read
+    prefix |= (uint32_t)dn[0] << shift;
+    need = dn[1];
     mask_hi |= 255u << shift;
-    __syncthreads();
   }
-  const uint32_t T = *s_prefix;
-  const int need_eq = *s_need;  // how many channels with key == T are taken
-  // ordered pass over channels: selected = key > T, or key == T among the first need_eq
-  // equal keys in index order; chunks of NT channels, block-wide exclusive scans.
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  int taken_eq = 0, written = 0;
-  for (int i = 0; i < PER && i * NT < cols; ++i) {
-    const int c = threadIdx.x + i * NT;
-    const bool eq = c < cols && key[i] == T;
-    const bool gt = c < cols && key[i] > T;
-    // rank among equal keys in this chunk
-    unsigned bal = __ballot_sync(0xffffffffu, eq);
-    int pre_eq = __popc(bal & ((1u << lane) - 1u));
-    if (lane == 0) warp_sums[w] = __popc(bal);
-    __syncthreads();
-    int before = 0, total = 0;
-    for (int j = 0; j < NW; ++j) { if (j < w) before += warp_sums[j]; total += warp_sums[j]; }
-    const bool take = gt || (eq && taken_eq + before + pre_eq < need_eq);
-    __syncthreads();
-    bal = __ballot_sync(0xffffffffu, take);
-    const int pre_t = __popc(bal & ((1u << lane) - 1u));
-    if (lane == 0) warp_sums[w] = __popc(bal);
-    __syncthreads();
-    int before_t = 0, total_t = 0;
-    for (int j = 0; j < NW; ++j) { if (j < w) before_t += warp_sums[j]; total_t += warp_sums[j]; }
-    const int pos = written + before_t + pre_t;
-    if (take && pos < k) sel_out[pos] = c;
-    written += total_t;
-    taken_eq += total;
-    __syncthreads();
+  // selected: key > T, and the first `need` channels (in index order) with key == T
+  const uint32_t T = prefix;
+  int ngt = 0, neq = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int c = threadIdx.x * PER + i;
+    ngt += (c < cols && key[i] > T) ? 1 : 0;
+    neq += (c < cols && key[i] == T) ? 1 : 0;
+  }
+  // both counts in one word (each total <= cols <= 65535): exclusive block scan
+  const int v = (ngt << 16) | neq;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  int before = 0;
+#pragma unroll
+  for (int j = 0; j < NW; ++j)
+    if (j < w) before += warp_tot[j];
+  const int ex = before + incl - v;
+  int gt_b = ex >> 16, eq_b = ex & 0xffff;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int c = threadIdx.x * PER + i;
+    if (c < cols && key[i] > T) {
+      sel_out[gt_b + min(eq_b, need)] = c;
+      ++gt_b;
+    } else if (c < cols && key[i] == T) {
+      if (eq_b < need) sel_out[gt_b + eq_b] = c;
+      ++eq_b;
+    }
   }
 }
 
@@ -495,51 +508,62 @@ __device__ __forceinline__ void block_topk(const uint32_t (&key)[PER], int cols,
 // itself -- the chunk partials added in ascending chunk order from 0 -- and
 // stores them to `scores`; otherwise it reads the scores score_chain_kernel
 // left there.
-// NT threads x PER channels per thread cover cols (256 x 8 up to 2048
-// channels: fewer warps per block barrier; 1024 x 8 up to 8192).
-template <int NT>
+// NT threads x PER channels per thread cover cols: 256 x 8 up to 2048
+// precomputed scores, 256 x 4 up to 1024 and 1024 x 2 up to 2048 channels
+// formed from partials, 1024 x 8 up to 8192 (a barrier costs more with more
+// warps; more threads keep more partial loads in flight).
+template <int NT, int PER, int U>
 __global__ void __launch_bounds__(NT) topk_kernel(float* __restrict__ scores, int cols,
                                                   int k, int32_t* __restrict__ sel,
                                                   const float* __restrict__ partials,
                                                   const int32_t* __restrict__ goff,
                                                   int64_t rows) {
-  __shared__ int hist[256];
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_need;
-  __shared__ int warp_sums[NT / 32];   // one per warp
+  __shared__ int hist[4 * 256];
+  __shared__ int warp_tot[NT / 32];
+  __shared__ int dn[2];
   const int g = blockIdx.y;
   float* sc = scores + (int64_t)g * cols;
-  constexpr int PER = 8;
   uint32_t key[PER];
   if (partials) {
     const int64_t a = goff ? (int64_t)goff[g] : 0;
     const int64_t b = goff ? (int64_t)goff[g + 1] : rows;
     const int64_t c0 = a / kScoreChunk, c1 = (b + kScoreChunk - 1) / kScoreChunk;
+    // every column of the thread advances together, U chunks at a time, so
+    // that PER x U loads are in flight per round (the round trips, not the
+    // adds, set this phase's time); each column's sum still adds its chunks
+    // in ascending order
+    float t[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) t[i] = 0.0f;
+    for (int64_t ch = c0; ch < c1; ch += U) {
+      float v[PER][U];
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int c = threadIdx.x * PER + i;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          v[i][u] = (c < cols && ch + u < c1) ? __ldg(partials + (ch + u) * cols + c) : 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < PER; ++i)
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (ch + u < c1) t[i] = __fadd_rn(t[i], v[i][u]);
+    }
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
-      const int c = threadIdx.x + i * blockDim.x;
-      float t = 0.0f;
-      if (c < cols) {
-        for (int64_t ch = c0; ch < c1; ch += 8) {
-          float v[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) v[u] = ch + u < c1 ? __ldg(partials + (ch + u) * cols + c) : 0.0f;
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (ch + u < c1) t = __fadd_rn(t, v[u]);
-        }
-        sc[c] = t;
-      }
-      key[i] = c < cols ? __float_as_uint(t) : 0u;
+      const int c = threadIdx.x * PER + i;
+      if (c < cols) sc[c] = t[i];
+      key[i] = c < cols ? __float_as_uint(t[i]) : 0u;
     }
   } else {
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
-      const int c = threadIdx.x + i * blockDim.x;
+      const int c = threadIdx.x * PER + i;
       key[i] = c < cols ? __float_as_uint(sc[c]) : 0u;
     }
   }
-  block_topk<NT, PER>(key, cols, k, sel + (int64_t)g * k, hist, &s_prefix, &s_need, warp_sums);
+  block_topk<NT, PER>(key, cols, k, sel + (int64_t)g * k, hist, warp_tot, dn);
 }
 
 // ---------------------------------------------------------------- residual slice
@@ -824,10 +848,9 @@ __global__ void __launch_bounds__(kFusedThreads, 4) quantize_select_kernel(
   // share one buffer
   __shared__ __align__(16) float sbuf[256 * 33];
   float (*tile)[33] = reinterpret_cast<float (*)[33]>(sbuf);
-  __shared__ int hist[256];
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_need;
-  __shared__ int warp_sums[kFusedThreads / 32];
+  __shared__ int hist[4 * 256];
+  __shared__ int warp_tot[kFusedThreads / 32];
+  __shared__ int dn[2];
   __shared__ int32_t s_sel[kFusedMaxK];
   __shared__ float red[kFusedThreads / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -907,10 +930,10 @@ __global__ void __launch_bounds__(kFusedThreads, 4) quantize_select_kernel(
     uint32_t key[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
-      const int c = threadIdx.x + i * kFusedThreads;
+      const int c = threadIdx.x * PER + i;
       key[i] = c < cols ? __float_as_uint(__ldcg(scores + c)) : 0u;
     }
-    block_topk<kFusedThreads, PER>(key, cols, k, s_sel, hist, &s_prefix, &s_need, warp_sums);
+    block_topk<kFusedThreads, PER>(key, cols, k, s_sel, hist, warp_tot, dn);
     __syncthreads();
     if (blockIdx.x == 0)
       for (int j = threadIdx.x; j < k; j += kFusedThreads) sel[j] = s_sel[j];
@@ -1537,14 +1560,16 @@ extern "C" quads_status_t quads_select_residual_channels(
   if (long_groups)
     score_chain_kernel<<<dim3((unsigned)((cols + 31) / 32), (unsigned)G), 256, 0, st>>>(
         score_partials, (int)cols, group_offsets, rows, scores);
+  const float* part = long_groups ? nullptr : score_partials;
+  const dim3 tg(1, (unsigned)G);
   if (cols <= 2048 && long_groups)   // scores precomputed: only the selection
-    topk_kernel<256><<<dim3(1, (unsigned)G), 256, 0, st>>>(scores, (int)cols, k, sel,
-                                                          long_groups ? nullptr : score_partials,
-                                                          group_offsets, rows);
+    topk_kernel<256, 8, 1><<<tg, 256, 0, st>>>(scores, (int)cols, k, sel, part, group_offsets, rows);
+  else if (cols <= 1024)             // e.g. per-expert h: up to 64 partial loads in flight per thread
+    topk_kernel<256, 4, 16><<<tg, 256, 0, st>>>(scores, (int)cols, k, sel, part, group_offsets, rows);
+  else if (cols <= 2048)             // 32 partial loads in flight per thread
+    topk_kernel<1024, 2, 16><<<tg, 1024, 0, st>>>(scores, (int)cols, k, sel, part, group_offsets, rows);
   else
-    topk_kernel<1024><<<dim3(1, (unsigned)G), 1024, 0, st>>>(scores, (int)cols, k, sel,
-                                                            long_groups ? nullptr : score_partials,
-                                                            group_offsets, rows);
+    topk_kernel<1024, 8, 2><<<tg, 1024, 0, st>>>(scores, (int)cols, k, sel, part, group_offsets, rows);
   if (quads_status_t s = sel_ready()) return s;
   if (group_offsets && G >= kRselGroupMin) {
     if (r_scale_layout == QUADS_SCALES_TCGEN05 && rows % 128) {

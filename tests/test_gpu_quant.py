@@ -330,6 +330,46 @@ def test_select_many_groups_one_block_per_group(lib, layout):
     assert not rc[end:].any() and not rsc[end:].any()
 
 
+@pytest.mark.parametrize("rows,cols,k,groups", [
+    (64, 512, 64, 1),       # one group, scores formed by the top-k block
+    (64, 512, 400, 1),      # more channels than non-zero scores: zero-score ties
+    (2112, 512, 64, 1),     # long group: scores from the score chain first
+    (64, 4096, 64, 1),      # more than 2048 channels: 8 channels per thread
+    (96, 512, 32, 3),       # row groups
+])
+def test_select_ties_take_lowest_index(lib, rows, cols, k, groups):
+    """Repeated 16-channel blocks give channels with equal scores and zero
+    blocks give zero scores, so the k-th largest score is tied: the selection
+    takes every larger score and then the lowest channel indices among the
+    equal ones, as the oracle does."""
+    rng = inputs.make_rng(77)
+    distinct = inputs.student_t4(rng, (rows, 64))
+    x = np.zeros((rows, cols), np.float32)
+    live = (cols // 16) * 3 // 4
+    for b in range(live):
+        x[:, 16 * b:16 * b + 16] = distinct[:, 16 * (b % 4):16 * (b % 4) + 16]
+    bits = inputs.f32_to_bf16_bits(x)
+    xt = bf16_tensor(bits)
+    if groups > 1:
+        offs = np.arange(groups + 1, dtype=np.int32) * (rows // groups)
+        ot = torch.from_numpy(offs).cuda()
+        q, part = lib.quantize_nvfp4(xt, group_offsets=ot, num_groups=groups, scores=True)
+        sel, _, _ = lib.select_residual_channels(xt, q, part, k, group_offsets=ot, num_groups=groups)
+        ref = Q.quantize_full(f32(bits), k, offs)
+    else:
+        q, part = lib.quantize_nvfp4(xt, scores=True)
+        sel, _, _ = lib.select_residual_channels(xt, q, part, k)
+        ref = Q.quantize_full(f32(bits), k)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    sc = ref["scores"].reshape(groups, cols)
+    got = sel.cpu().numpy().reshape(groups, k)
+    for g in range(groups):
+        kth = np.sort(sc[g])[::-1][k - 1]
+        assert (sc[g] == kth).sum() > 1   # the case really has a tie at the threshold
+    assert np.array_equal(got, ref["sel"].reshape(groups, k))
+
+
 def test_w4a16_qdq_full_expert_stack_sampled_experts(lib):
     """The benchmark's QDQ configuration: the 128 experts' gate/up weights
     (196608 x 2048, one tensor scale per expert); three experts checked bit for
