@@ -220,6 +220,34 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// ------------------------------------------------------------ dependent launches
+// The kernels of the layer path open with griddep_wait(): launched with
+// programmatic stream serialization (launch_dep) a kernel may be scheduled
+// while its stream predecessor still runs, and blocks there until that grid
+// has completed and its memory writes are visible (launched plainly, the
+// wait returns at once).  griddep_launch_dependents() then allows the
+// stream's next kernel to be scheduled in turn, so its launch overlaps this
+// kernel instead of following it.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+template <typename... P, typename... A>
+static inline cudaError_t launch_dep(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t st, A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...);
+}
+
 // Group index of `row` for ascending offsets goff[0..G] (binary search).
 __device__ __forceinline__ int group_of(const int32_t* goff, int G, int64_t row) {
   int lo = 0, hi = G - 1;

@@ -507,6 +507,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmW,
                 const Params p) {
+  griddep_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + G::STAGES * G::STAGE_BYTES);
@@ -1709,6 +1710,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     wide_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmW,
                      const Params p) {
+  griddep_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES);
@@ -2119,6 +2121,7 @@ __global__ void __launch_bounds__(256) wsel_cols_kernel(
     const uint8_t* __restrict__ ct, const uint8_t* __restrict__ st, int N, int K, int NC,
     const int32_t* __restrict__ sel, int sel_pe, int k, int kpad, uint8_t* __restrict__ oc,
     uint8_t* __restrict__ osf) {
+  griddep_wait();
   extern __shared__ __align__(16) uint8_t wsm[];
   uint8_t* sc = wsm;                   // [16][NC/2] codes
   uint8_t* ss = wsm + 16 * (NC / 2);   // [16][NC] scale bytes
@@ -2278,8 +2281,9 @@ static void launch_wsel(const uint8_t* b_t, const uint8_t* b_sf_t, int E, int N,
   // row chunks of 512 (or 128) rows: N is a multiple of 128
   const int NC = N % 512 == 0 ? 512 : 128;
   const size_t cols_smem = (size_t)24 * NC;   // 16 columns x (NC/2 code + NC scale bytes)
-  wsel_cols_kernel<<<dim3((unsigned)(kpad / 16), (unsigned)E, (unsigned)(N / NC)), 256, cols_smem,
-                     stream>>>(b_t, b_sf_t, N, K, NC, sel, sel_pe, k, kpad, codes, sf);
+  const dim3 grid((unsigned)(kpad / 16), (unsigned)E, (unsigned)(N / NC));
+  launch_dep(wsel_cols_kernel, grid, 256, cols_smem, stream, b_t, b_sf_t, N, K, NC, sel, sel_pe, k,
+             kpad, codes, sf);
 }
 
 static quads_status_t launch(const Launch& L) {
@@ -2408,7 +2412,8 @@ static quads_status_t launch(const Launch& L) {
     p.trace = g_trace.exchange(nullptr);
     int64_t grid = num_sms();
     if (!L.row_off) grid = std::min<int64_t>(grid, ((L.M + wide::BM - 1) / wide::BM) * p.Nt);
-    wide::wide_gemm_kernel<<<(int)grid, wide::NUM_THREADS, wide::SMEM_BYTES, L.stream>>>(tA, tB, tR, tW, p);
+    launch_dep(wide::wide_gemm_kernel, (int)grid, wide::NUM_THREADS, wide::SMEM_BYTES, L.stream,
+        tA, tB, tR, tW, p);
     return check_launch("gemm", launches);
   }
   if (!g_pair_kernel) {
@@ -2432,9 +2437,11 @@ static quads_status_t launch(const Launch& L) {
     if (!L.row_off) grid = std::min<int64_t>(grid, ((L.M + BM - 1) / BM) * (L.N / BN));
     // 256-element stages when K leaves a 512-element ring with a half-empty stage
     if (L.K % 512)
-      gemm_kernel<Geo256><<<(int)grid, NUM_THREADS, Geo256::SMEM_BYTES, L.stream>>>(tA, tB, tR, tW, p);
+      launch_dep(gemm_kernel<Geo256>, (int)grid, NUM_THREADS, Geo256::SMEM_BYTES, L.stream,
+          tA, tB, tR, tW, p);
     else
-      gemm_kernel<Geo512><<<(int)grid, NUM_THREADS, Geo512::SMEM_BYTES, L.stream>>>(tA, tB, tR, tW, p);
+      launch_dep(gemm_kernel<Geo512>, (int)grid, NUM_THREADS, Geo512::SMEM_BYTES, L.stream,
+          tA, tB, tR, tW, p);
     return check_launch("gemm", launches);
   }
   pair::Params p;

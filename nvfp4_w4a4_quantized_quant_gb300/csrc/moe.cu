@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
                                                      float* __restrict__ gates,
                                                      int32_t* __restrict__ bcount,
                                                      int32_t* __restrict__ local_rank) {
+  griddep_wait();
   __shared__ uint32_t smask[kRouteTokens][kMaxExperts / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t = blockIdx.x * kRouteTokens + warp;
@@ -114,6 +115,7 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
 __global__ void __launch_bounds__(256) plan_kernel(const int32_t* __restrict__ bcount, int nb,
                                                    int32_t* __restrict__ bprefix,
                                                    int32_t* __restrict__ counts) {
+  griddep_wait();
   __shared__ int warp_sums[8];
   const int e = blockIdx.x, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int32_t* bc = bcount + (int64_t)e * nb;
@@ -168,6 +170,7 @@ __global__ void __launch_bounds__(256) assign_kernel(const int32_t* __restrict__
                                                      int32_t* __restrict__ row_token,
                                                      int32_t* __restrict__ token_row,
                                                      int64_t cap) {
+  griddep_wait();
   __shared__ int off[kMaxExperts + 1];
   __shared__ int warp_sums[8];
   {
@@ -215,6 +218,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
                                                      const uint8_t* __restrict__ isf,
                                                      uint8_t* __restrict__ oc,
                                                      uint8_t* __restrict__ osf) {
+  griddep_wait();
   int64_t nrows = off[E];
   if (!QDBG(nrows >= 0 && nrows <= cap)) nrows = 0;
   const int cbytes = cols >> 1;
@@ -293,6 +297,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
                                                       const float* __restrict__ gates, int T,
                                                       int topk, int H, __nv_bfloat16* __restrict__ out,
                                                       int64_t ldo) {
+  griddep_wait();
   const int vec = H >> 3;
   const int64_t total = (int64_t)T * vec;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -368,12 +373,12 @@ extern "C" quads_status_t quads_moe_route(const float* logits, int32_t tokens, i
   int32_t* bprefix = bcount + (size_t)nb * num_experts;         // [E, nb]
   cudaStream_t st = (cudaStream_t)stream;
   if (tokens > 0)
-    route_kernel<<<nb, 32 * kRouteTokens, 0, st>>>(logits, tokens, num_experts, topk, topk_idx,
-                                                    gates, bcount, token_row);
-  plan_kernel<<<num_experts, 256, 0, st>>>(bcount, nb, bprefix, expert_counts);
-  assign_kernel<<<std::max(1, std::min(num_sms() * 4, (tokens * topk + 255) / 256)), 256, 0, st>>>(
-      topk_idx, tokens, num_experts, topk, nb, bprefix, expert_offsets, expert_counts, row_token,
-      token_row, rows_capacity);
+    launch_dep(route_kernel, nb, 32 * kRouteTokens, 0, st,
+        logits, tokens, num_experts, topk, topk_idx, gates, bcount, token_row);
+  launch_dep(plan_kernel, num_experts, 256, 0, st, bcount, nb, bprefix, expert_counts);
+  const int assign_blocks = std::max(1, std::min(num_sms() * 4, (tokens * topk + 255) / 256));
+  launch_dep(assign_kernel, assign_blocks, 256, 0, st, topk_idx, tokens, num_experts, topk, nb,
+             bprefix, expert_offsets, expert_counts, row_token, token_row, rows_capacity);
   return check_launch("moe_route", tokens > 0 ? 3 : 2);
 }
 
@@ -393,8 +398,9 @@ extern "C" quads_status_t quads_moe_gather(const int32_t* row_token, const int32
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "moe_gather: narrow rows need rows * cols / 32 < 2^31");
   const int64_t vecs = rows_capacity * (cols / 32);   // 16-byte code vectors
   const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((vecs / 4 + 255) / 256, (int64_t)num_sms() * 8));
-  gather_kernel<<<blocks, 256, 0, st>>>(row_token, expert_offsets, num_experts, rows_capacity,
-                                        (int)cols, in_codes, in_scales, out_codes, out_scales);
+  launch_dep(gather_kernel, blocks, 256, 0, st,
+      row_token, expert_offsets, num_experts, rows_capacity, (int)cols, in_codes, in_scales,
+      out_codes, out_scales);
   return check_launch("moe_gather", 1);
 }
 
@@ -414,7 +420,8 @@ extern "C" quads_status_t quads_moe_combine(const void* y, int64_t ldy, const in
                 : topk == 2 ? combine_kernel<2>
                 : topk == 1 ? combine_kernel<1>
                             : combine_kernel<0>;
-  kernel<<<blocks, 256, 0, st>>>((const __nv_bfloat16*)y, ldy, token_row, gates, tokens,
-                                         topk, (int)hidden, (__nv_bfloat16*)out, ldo);
+  launch_dep(kernel, blocks, 256, 0, st,
+      (const __nv_bfloat16*)y, ldy, token_row, gates, tokens, topk, (int)hidden,
+      (__nv_bfloat16*)out, ldo);
   return check_launch("moe_combine", 1);
 }

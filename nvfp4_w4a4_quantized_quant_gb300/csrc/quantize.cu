@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restri
                                                    const int32_t* __restrict__ row_index,
                                                    const int32_t* __restrict__ goff, int G,
                                                    uint32_t* __restrict__ amax_bits) {
+  griddep_wait();
   const int64_t end = goff ? (int64_t)goff[G] : rows;
   const int vec_per_row = cols >> 3;
   const int64_t nslices = (end + kAmaxRows - 1) / kAmaxRows;
@@ -250,6 +251,7 @@ __global__ void __launch_bounds__(256, kScores ? 4 : 3) quantize_kernel(
     const float* __restrict__ st, const uint32_t* __restrict__ amax_bits, float* __restrict__ st_out,
     uint8_t* __restrict__ codes, int64_t ldc, uint8_t* __restrict__ scales, int layout,
     float* __restrict__ partials, __nv_bfloat16* __restrict__ qdq, int64_t ldq) {
+  griddep_wait();
   __shared__ __align__(16) float sq[kScores ? kScoreChunk * 256 : 4];
   // groups (up to kSmemGroups): offsets and tensor scales once per block in
   // shared memory, so the per-task group search and scale reads stay on chip
@@ -285,6 +287,7 @@ __global__ void __launch_bounds__(256, 3) quantize_chunk_kernel(
     const float* __restrict__ st, const uint32_t* __restrict__ amax_bits, float* __restrict__ st_out,
     uint8_t* __restrict__ codes, int64_t ldc, uint8_t* __restrict__ scales, int layout,
     float* __restrict__ partials) {
+  griddep_wait();
   __shared__ int32_t s_goff[kSmemGroups + 1];
   __shared__ float s_scale[kSmemGroups];
   if (amax_bits && blockIdx.x == 0)
@@ -371,6 +374,7 @@ __global__ void __launch_bounds__(256) score_chain_kernel(const float* __restric
                                                           const int32_t* __restrict__ goff,
                                                           int64_t rows,
                                                           float* __restrict__ scores) {
+  griddep_wait();
   __shared__ float tile[256][33];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = blockIdx.y;
@@ -518,6 +522,7 @@ __global__ void __launch_bounds__(NT) topk_kernel(float* __restrict__ scores, in
                                                   const float* __restrict__ partials,
                                                   const int32_t* __restrict__ goff,
                                                   int64_t rows) {
+  griddep_wait();
   __shared__ int hist[4 * 256];
   __shared__ int warp_tot[NT / 32];
   __shared__ int dn[2];
@@ -577,6 +582,7 @@ __global__ void __launch_bounds__(256) rsel_residual_kernel(
     const int32_t* __restrict__ goff, int G, const uint8_t* __restrict__ scales, int layout,
     const float* __restrict__ st, const int32_t* __restrict__ sel, int k,
     float* __restrict__ rs, uint32_t* __restrict__ amax_bits, int rb) {
+  griddep_wait();
   __shared__ float red[8];
   const int64_t end = goff ? (int64_t)goff[G] : rows;
   const int64_t nblk = (end + rb - 1) / rb;
@@ -643,6 +649,7 @@ __global__ void __launch_bounds__(kRselGroupThreads) rsel_group_kernel(
     const float* __restrict__ st, const int32_t* __restrict__ sel, int k, int kpad,
     float* __restrict__ rs, uint8_t* __restrict__ rcodes, uint8_t* __restrict__ rscales,
     int rlayout, float* __restrict__ rst) {
+  griddep_wait();
   __shared__ float red[kRselGroupThreads / 32];
   const int ncols16 = cols >> 4, rcols16 = kpad >> 4;
   const int vpr = kpad >> 3;   // 8-element vectors per residual row (even)
@@ -745,6 +752,7 @@ __global__ void __launch_bounds__(256) rsel_quantize_kernel(
     const float* __restrict__ rs, int64_t rows, int k, int kpad, const int32_t* __restrict__ goff,
     int G, const uint32_t* __restrict__ amax_bits, uint8_t* __restrict__ rcodes,
     uint8_t* __restrict__ rscales, int layout, float* __restrict__ rst) {
+  griddep_wait();
   const int64_t end = goff ? (int64_t)goff[G] : rows;
   const int vec_per_row = kpad >> 3;  // even
   const int64_t total = rows * vec_per_row;  // padding rows (>= end) get zeros
@@ -1437,7 +1445,7 @@ static quads_status_t quantize_impl(
     launched = 2;
     uint32_t* amax = (uint32_t*)workspace;
     cudaMemsetAsync(amax, 0, (size_t)G * 4, st);
-    amax_kernel<<<grid_for((rows + kAmaxRows - 1) / kAmaxRows, 1, 8), 256, 0, st>>>(
+    launch_dep(amax_kernel, grid_for((rows + kAmaxRows - 1) / kAmaxRows, 1, 8), 256, 0, st,
         (const __nv_bfloat16*)x, rows, (int)cols, ldx, row_index, group_offsets, G, amax);
     amax_bits = amax;
   } else if (tensor_scale_in != tensor_scale_out) {
@@ -1455,21 +1463,21 @@ static quads_status_t quantize_impl(
   const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(ntasks, (int64_t)num_sms() * 16));
   const __nv_bfloat16* xb = (const __nv_bfloat16*)x;
   if (qdq)
-    quantize_kernel<false, true><<<blocks, 256, 0, st>>>(
+    launch_dep(quantize_kernel<false, true>, blocks, 256, 0, st,
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
         codes, ld_codes, scales, scale_layout, nullptr, qdq, ldq);
   else if (score_partials && ((rows + 31) / 32) * (cols / 16) >= (int64_t)num_sms() * 512 &&
            ((rows + 31) / 32) * (cols / 16) < (1ll << 31))
     // enough (chunk, block) pairs for a thread each: about two blocks per SM
-    quantize_chunk_kernel<<<grid_for(((rows + 31) / 32) * (cols / 16), 256, 3), 256, 0, st>>>(
+    launch_dep(quantize_chunk_kernel, grid_for(((rows + 31) / 32) * (cols / 16), 256, 3), 256, 0, st,
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
         codes, ld_codes, scales, scale_layout, score_partials);
   else if (score_partials)
-    quantize_kernel<true, false><<<blocks, 256, 0, st>>>(
+    launch_dep(quantize_kernel<true, false>, blocks, 256, 0, st,
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
         codes, ld_codes, scales, scale_layout, score_partials, nullptr, 0);
   else
-    quantize_kernel<false, false><<<blocks, 256, 0, st>>>(
+    launch_dep(quantize_kernel<false, false>, blocks, 256, 0, st,
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
         codes, ld_codes, scales, scale_layout, nullptr, nullptr, 0);
   return check_launch(qdq ? "qdq" : "quantize", launched);
@@ -1558,39 +1566,43 @@ extern "C" quads_status_t quads_select_residual_channels(
   const int64_t chunks_per_group = (rows + 31) / 32 / G;
   const bool long_groups = chunks_per_group > 64;
   if (long_groups)
-    score_chain_kernel<<<dim3((unsigned)((cols + 31) / 32), (unsigned)G), 256, 0, st>>>(
+    launch_dep(score_chain_kernel, dim3((unsigned)((cols + 31) / 32), (unsigned)G), 256, 0, st,
         score_partials, (int)cols, group_offsets, rows, scores);
   const float* part = long_groups ? nullptr : score_partials;
   const dim3 tg(1, (unsigned)G);
   if (cols <= 2048 && long_groups)   // scores precomputed: only the selection
-    topk_kernel<256, 8, 1><<<tg, 256, 0, st>>>(scores, (int)cols, k, sel, part, group_offsets, rows);
+    launch_dep(topk_kernel<256, 8, 1>, tg, 256, 0, st,
+        scores, (int)cols, k, sel, part, group_offsets, rows);
   else if (cols <= 1024)             // e.g. per-expert h: up to 64 partial loads in flight per thread
-    topk_kernel<256, 4, 16><<<tg, 256, 0, st>>>(scores, (int)cols, k, sel, part, group_offsets, rows);
+    launch_dep(topk_kernel<256, 4, 16>, tg, 256, 0, st,
+        scores, (int)cols, k, sel, part, group_offsets, rows);
   else if (cols <= 2048)             // 32 partial loads in flight per thread
-    topk_kernel<1024, 2, 16><<<tg, 1024, 0, st>>>(scores, (int)cols, k, sel, part, group_offsets, rows);
+    launch_dep(topk_kernel<1024, 2, 16>, tg, 1024, 0, st,
+        scores, (int)cols, k, sel, part, group_offsets, rows);
   else
-    topk_kernel<1024, 8, 2><<<tg, 1024, 0, st>>>(scores, (int)cols, k, sel, part, group_offsets, rows);
+    launch_dep(topk_kernel<1024, 8, 2>, tg, 1024, 0, st,
+        scores, (int)cols, k, sel, part, group_offsets, rows);
   if (quads_status_t s = sel_ready()) return s;
   if (group_offsets && G >= kRselGroupMin) {
     if (r_scale_layout == QUADS_SCALES_TCGEN05 && rows % 128) {
       const int64_t start = (rows / 128) * (kpad / 64) * 512;
       cudaMemsetAsync(r_scales + start, 0, (size_t)(sf_tc_bytes(rows, kpad) - start), st);
     }
-    rsel_group_kernel<<<G + 2 * num_sms(), kRselGroupThreads, 0, st>>>(
+    launch_dep(rsel_group_kernel, G + 2 * num_sms(), kRselGroupThreads, 0, st,
         (const __nv_bfloat16*)x, rows, (int)cols, ldx, group_offsets, G, scales, scale_layout,
         tensor_scale, sel, k, kpad, rs, r_codes, r_scales, r_scale_layout, r_tensor_scale);
     return check_launch("select", long_groups ? 3 : 2);
   }
   cudaMemsetAsync(amax, 0, (size_t)G * 4, st);
   const int rb = (rows + 31) / 32 < 2 * (int64_t)num_sms() ? 8 : 32;
-  rsel_residual_kernel<<<grid_for((rows + rb - 1) / rb, 1, 16), 256, 0, st>>>(
+  launch_dep(rsel_residual_kernel, grid_for((rows + rb - 1) / rb, 1, 16), 256, 0, st,
       (const __nv_bfloat16*)x, rows, (int)cols, ldx, group_offsets, G, scales, scale_layout,
       tensor_scale, sel, k, rs, amax, rb);
   if (r_scale_layout == QUADS_SCALES_TCGEN05 && rows % 128) {
     const int64_t start = (rows / 128) * (kpad / 64) * 512;
     cudaMemsetAsync(r_scales + start, 0, (size_t)(sf_tc_bytes(rows, kpad) - start), st);
   }
-  rsel_quantize_kernel<<<grid_for(rows * (kpad / 8), 256), 256, 0, st>>>(
+  launch_dep(rsel_quantize_kernel, grid_for(rows * (kpad / 8), 256), 256, 0, st,
       rs, rows, k, kpad, group_offsets, G, amax, r_codes, r_scales, r_scale_layout, r_tensor_scale);
   return check_launch("select", long_groups ? 4 : 3);
 }
