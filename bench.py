@@ -55,7 +55,7 @@ def gemm1_bytes(w=WORKLOAD) -> float:
 # DRAM traffic (read + write) of one GEMM1 launch at this workload, from the
 # committed ncu capture of GEMM1; reset to None whenever gemm_kernel changes
 # until a new capture is taken.
-GEMM1_TRAFFIC_BYTES = 320.348928e6 + 92.565504e6
+GEMM1_TRAFFIC_BYTES = 320.355072e6 + 92.516096e6
 
 
 def peaks():
