@@ -204,12 +204,33 @@ __device__ __forceinline__ float e8m0_inverse(uint32_t byte) {
   return __uint_as_float((254u - byte) << 23);
 }
 
+// Two float32 products per instruction (mul.rn.f32x2, sm_100+): each half is
+// rounded as __fmul_rn rounds it.  Only for products that feed no addition:
+// ptxas contracts an f32x2 multiply and a following f32x2 add or subtract into
+// a fused multiply-add despite the .rn qualifiers (measured on the GB300:
+// 16 % of residuals differed from the scalar two-rounding sequence), which
+// the float32 orders fixed by the score and residual definitions forbid.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 // Quantize 8 values of one block: returns packed codes; writes levels*d residuals
 // when want_residual.
 __device__ __forceinline__ uint32_t quantize8(const float* x, const BlockScale& bs) {
   float v[8];
+  const uint64_t rr = f2_pack(bs.r, bs.r);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(x[i], bs.r);
+  for (int i = 0; i < 8; i += 2) f2_unpack(f2_mul(f2_pack(x[i], x[i + 1]), rr), v[i], v[i + 1]);
   uint32_t c = f32x8_to_e2m1(v);
   return bs.zero ? 0u : c;
 }

@@ -1160,8 +1160,9 @@ __global__ void __launch_bounds__(256) trace_kernel(
       float f[8];
       bf16x8_to_f32(h ? cur.x1 : cur.x0, f);
       float v[8];
+      const uint64_t rr = f2_pack(bs.r, bs.r);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(f[j], bs.r);
+      for (int j = 0; j < 8; j += 2) f2_unpack(f2_mul(f2_pack(f[j], f[j + 1]), rr), v[j], v[j + 1]);
       uint32_t rtn = f32x8_to_e2m1(v);
       float qn[8];
       e2m1x8_to_f32(rtn, qn);
@@ -1346,8 +1347,9 @@ __global__ void __launch_bounds__(256) trace_1bit_kernel(
       float f[8];
       bf16x8_to_f32(h ? x1 : x0, f);
       float v[8];
+      const uint64_t rr = f2_pack(bs.r, bs.r);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(f[j], bs.r);
+      for (int j = 0; j < 8; j += 2) f2_unpack(f2_mul(f2_pack(f[j], f[j + 1]), rr), v[j], v[j + 1]);
       uint32_t rtn = f32x8_to_e2m1(v);
       float qn[8];
       e2m1x8_to_f32(rtn, qn);
