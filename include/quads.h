@@ -188,6 +188,13 @@ int32_t quads_kpad(int32_t k);
  *                  last a multiple of 32; the last (<= rows) is the number of
  *                  rows processed -- rows past it are neither read nor written,
  *                  so `rows` may be a capacity (e.g. padded expert rows).
+ *   group_counts   nullable device int32 [num_groups] (needs group_offsets):
+ *                  rows of group g at or past group_offsets[g] +
+ *                  group_counts[g] are taken as zero rows -- not read, their
+ *                  codes, scale bytes and score partials written as those of
+ *                  zeros (for per-expert rows padded to a tile multiple whose
+ *                  padding is zero anyway, the quantizer then reads only the
+ *                  real rows).
  *   tensor_scale_in nullable device float [num_groups]: use these tensor
  *                  scales instead of computing amax / 2688.
  *   tensor_amax_in nullable device float [num_groups]: the groups' absolute
@@ -204,7 +211,8 @@ int32_t quads_kpad(int32_t k);
  */
 quads_status_t quads_quantize_nvfp4(const void* x, int64_t rows, int64_t cols, int64_t ldx,
                                     const int32_t* row_index, const int32_t* group_offsets,
-                                    int32_t num_groups, const float* tensor_scale_in,
+                                    int32_t num_groups, const int32_t* group_counts,
+                                    const float* tensor_scale_in,
                                     const float* tensor_amax_in, uint8_t* codes,
                                     int64_t ld_codes, uint8_t* scales,
                                     int32_t scale_layout, float* tensor_scale_out,

@@ -38,7 +38,8 @@ __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restri
                                                    int64_t rows, int cols, int64_t ldx,
                                                    const int32_t* __restrict__ row_index,
                                                    const int32_t* __restrict__ goff, int G,
-                                                   uint32_t* __restrict__ amax_bits) {
+                                                   uint32_t* __restrict__ amax_bits,
+                                                   const int32_t* __restrict__ gcnt) {
   griddep_wait();
   const int64_t end = goff ? (int64_t)goff[G] : rows;
   const int vec_per_row = cols >> 3;
@@ -50,7 +51,9 @@ __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restri
     const int g = goff ? group_of(goff, G, r0) : 0;
     if (goff && r1 > goff[g + 1]) atomicExch(&g_quant_error, QUADS_ERR_DEVICE_CHECK);
     __nv_bfloat162 m2 = __floats2bfloat162_rn(0.0f, 0.0f);
-    const int total = (int)(r1 - r0) * vec_per_row;
+    // rows past the group's count (gcnt) are zero rows: not read
+    const int64_t r1r = gcnt ? max(r0, min(r1, (int64_t)goff[g] + __ldg(gcnt + g))) : r1;
+    const int total = (int)(r1r - r0) * vec_per_row;
     for (int i0 = threadIdx.x; i0 < total; i0 += 8 * blockDim.x) {
       uint4 u[8];
 #pragma unroll
@@ -117,7 +120,8 @@ __device__ __forceinline__ void quantize_block_tasks(
     const float* __restrict__ st, const uint32_t* __restrict__ amax_bits,
     uint8_t* __restrict__ codes, int64_t ldc, uint8_t* __restrict__ scales, int layout,
     float* __restrict__ partials, __nv_bfloat16* __restrict__ qdq, int64_t ldq, float* sq,
-    int64_t first, int64_t stride, const float* gscale = nullptr) {
+    int64_t first, int64_t stride, const float* gscale = nullptr,
+    const int32_t* __restrict__ gcnt = nullptr) {
   // tensor scales: a per-block table (gscale, shared memory), given (st), or
   // derived from the groups' amax bits (read through L2: the fused kernel
   // produces them earlier in the same launch)
@@ -135,6 +139,13 @@ __device__ __forceinline__ void quantize_block_tasks(
   const int blk = lane & 15;
   // tensor scale of a single group, once per block
   const float s_single = G == 1 ? scale_of(0) : 0.0f;
+  // with gcnt, rows of a chunk at or past goff[g] + gcnt[g] (its group's
+  // padding) are zero rows: not read (a chunk lies inside one group)
+  auto real_end = [&](int64_t r0, int64_t r1) -> int64_t {
+    if (!gcnt) return r1;
+    const int g = group_of(goff, G, r0);
+    return min(r1, (int64_t)goff[g] + gcnt[g]);
+  };
   // this thread's two rows of a task, loaded one task ahead (task indices fit
   // in 32 bits: the division is a 32-bit one)
   auto load_task = [&](int64_t task, uint4 (&raw)[2][2]) {
@@ -142,7 +153,7 @@ __device__ __forceinline__ void quantize_block_tasks(
     const int64_t chunk = tk / (uint32_t)nslab;
     const int col = (int)(tk - (uint32_t)chunk * (uint32_t)nslab) * 256 + blk * 16;
     const int64_t r0 = chunk * kScoreChunk;
-    const int64_t r1 = min(r0 + kScoreChunk, end);
+    const int64_t r1 = task < ntasks ? real_end(r0, min(r0 + kScoreChunk, end)) : r0;
 #pragma unroll
     for (int it = 0; it < 2; ++it) {
       const int64_t row = r0 + 4 * warp + 2 * it + (lane >> 4);
@@ -169,6 +180,30 @@ __device__ __forceinline__ void quantize_block_tasks(
     const int64_t r0 = chunk * kScoreChunk;
     const int64_t r1 = min(r0 + kScoreChunk, end);
     const int g0 = goff ? group_of(goff, G, r0) : 0;   // same for the whole block
+    if (gcnt && (int64_t)goff[g0] + gcnt[g0] <= r0) {
+      // the whole chunk is group padding: the outputs of zero rows (codes,
+      // scale bytes, QDQ values and residual partials all 0), nothing read
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+        const int64_t row = r0 + 4 * warp + 2 * it + (lane >> 4);
+        if (!active || row >= r1) continue;
+        if (!kQdq || codes) {
+          uint32_t* pc = reinterpret_cast<uint32_t*>(codes + row * ldc + (col >> 1));
+          pc[0] = 0u;
+          pc[1] = 0u;
+          scales[sf_offset(layout, row, col >> 4, ncols16)] = 0;
+        }
+        if (kQdq) {
+          uint4* pq = reinterpret_cast<uint4*>(qdq + row * ldq + col);
+          pq[0] = pq[1] = make_uint4(0, 0, 0, 0);
+        }
+      }
+      if (kScores) {
+        const int c = slab * 256 + (int)threadIdx.x;
+        if (c < cols) partials[chunk * cols + c] = 0.0f;
+      }
+      continue;
+    }
     const float s_t0 = G == 1 ? s_single : scale_of(g0);
 #pragma unroll
     for (int it = 0; it < 2; ++it) {
@@ -250,13 +285,15 @@ __global__ void __launch_bounds__(256, kScores ? 4 : 3) quantize_kernel(
     const int32_t* __restrict__ row_index, const int32_t* __restrict__ goff, int G,
     const float* __restrict__ st, const uint32_t* __restrict__ amax_bits, float* __restrict__ st_out,
     uint8_t* __restrict__ codes, int64_t ldc, uint8_t* __restrict__ scales, int layout,
-    float* __restrict__ partials, __nv_bfloat16* __restrict__ qdq, int64_t ldq) {
+    float* __restrict__ partials, __nv_bfloat16* __restrict__ qdq, int64_t ldq,
+    const int32_t* __restrict__ gcnt) {
   griddep_wait();
   __shared__ __align__(16) float sq[kScores ? kScoreChunk * 256 : 4];
   // groups (up to kSmemGroups): offsets and tensor scales once per block in
   // shared memory, so the per-task group search and scale reads stay on chip
   __shared__ int32_t s_goff[kSmemGroups + 1];
   __shared__ float s_scale[kSmemGroups];
+  __shared__ int32_t s_cnt[kSmemGroups];
   // tensor scales derived from the groups' amax bits are also stored by block 0
   if (amax_bits && blockIdx.x == 0)
     for (int g = threadIdx.x; g < G; g += blockDim.x)
@@ -264,13 +301,16 @@ __global__ void __launch_bounds__(256, kScores ? 4 : 3) quantize_kernel(
   const bool cache = goff && G <= kSmemGroups;
   if (cache) {
     for (int g = threadIdx.x; g <= G; g += blockDim.x) s_goff[g] = goff[g];
-    for (int g = threadIdx.x; g < G; g += blockDim.x)
+    for (int g = threadIdx.x; g < G; g += blockDim.x) {
       s_scale[g] = amax_bits ? tensor_scale_from_amax(__uint_as_float(__ldg(amax_bits + g))) : __ldg(st + g);
+      if (gcnt) s_cnt[g] = __ldg(gcnt + g);
+    }
     __syncthreads();
   }
   quantize_block_tasks<kScores, kQdq>(x, rows, cols, ldx, row_index, cache ? s_goff : goff, G, st,
                                       amax_bits, codes, ldc, scales, layout, partials, qdq, ldq, sq,
-                                      blockIdx.x, gridDim.x, cache ? s_scale : nullptr);
+                                      blockIdx.x, gridDim.x, cache ? s_scale : nullptr,
+                                      cache && gcnt ? s_cnt : gcnt);
 }
 
 // Score mode with one thread per (32-row chunk, 16-column block): the thread
@@ -286,10 +326,11 @@ __global__ void __launch_bounds__(256, 3) quantize_chunk_kernel(
     const int32_t* __restrict__ row_index, const int32_t* __restrict__ goff, int G,
     const float* __restrict__ st, const uint32_t* __restrict__ amax_bits, float* __restrict__ st_out,
     uint8_t* __restrict__ codes, int64_t ldc, uint8_t* __restrict__ scales, int layout,
-    float* __restrict__ partials) {
+    float* __restrict__ partials, const int32_t* __restrict__ gcnt) {
   griddep_wait();
   __shared__ int32_t s_goff[kSmemGroups + 1];
   __shared__ float s_scale[kSmemGroups];
+  __shared__ int32_t s_cnt[kSmemGroups];
   if (amax_bits && blockIdx.x == 0)
     for (int g = threadIdx.x; g < G; g += blockDim.x)
       st_out[g] = tensor_scale_from_amax(__uint_as_float(__ldg(amax_bits + g)));
@@ -297,11 +338,14 @@ __global__ void __launch_bounds__(256, 3) quantize_chunk_kernel(
   if (cache) {
     if (goff)
       for (int g = threadIdx.x; g <= G; g += blockDim.x) s_goff[g] = goff[g];
-    for (int g = threadIdx.x; g < G; g += blockDim.x)
+    for (int g = threadIdx.x; g < G; g += blockDim.x) {
       s_scale[g] = amax_bits ? tensor_scale_from_amax(__uint_as_float(__ldg(amax_bits + g))) : __ldg(st + g);
+      if (gcnt) s_cnt[g] = __ldg(gcnt + g);
+    }
     __syncthreads();
   }
   const int32_t* go = cache ? s_goff : goff;
+  const int32_t* gc = cache && gcnt ? s_cnt : gcnt;
   auto scale_of = [&](int g) {
     if (cache) return s_scale[g];
     return amax_bits ? tensor_scale_from_amax(__uint_as_float(__ldcg(amax_bits + g))) : __ldg(st + g);
@@ -316,13 +360,28 @@ __global__ void __launch_bounds__(256, 3) quantize_chunk_kernel(
     const int nr = (int)min((int64_t)kScoreChunk, end - r0);
     const int g = goff ? group_of(go, G, r0) : 0;
     if (goff && r0 + nr > (int64_t)go[g + 1]) atomicExch(&g_quant_error, QUADS_ERR_DEVICE_CHECK);
+    // rows of the chunk past its group's count (gcnt) are zero rows: not read
+    const int nreal = gc ? (int)max((int64_t)0, min((int64_t)nr, (int64_t)go[g] + gc[g] - r0)) : nr;
+    if (nreal == 0 && nr > 0) {
+      // the whole chunk is group padding: zero codes, scale bytes and partials
+      for (int r = 0; r < nr; ++r) {
+        *reinterpret_cast<uint2*>(codes + (r0 + r) * ldc + cb * 8) = make_uint2(0u, 0u);
+        scales[sf_offset(layout, r0 + r, cb, nblk)] = 0;
+      }
+      float4* pz = reinterpret_cast<float4*>(partials + (int64_t)chunk * cols + cb * 16);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) pz[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      continue;
+    }
     const float s_t = scale_of(g);
     auto load = [&](int r, uint4& lo, uint4& hi) {
-      if (r < nr) {
+      if (r < nreal) {
         const int64_t src = row_index ? (int64_t)row_index[r0 + r] : r0 + r;
         const uint4* px = reinterpret_cast<const uint4*>(x + src * ldx + cb * 16);
         lo = __ldg(px);
         hi = __ldg(px + 1);
+      } else {
+        lo = hi = make_uint4(0, 0, 0, 0);   // padding (or past the chunk): a zero row
       }
     };
     uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, b0 = a0, b1 = a0;
@@ -1410,7 +1469,8 @@ using namespace quads;
 // codes and scales only; codes == nullptr: bf16 QDQ values only).
 static quads_status_t quantize_impl(
     const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* row_index,
-    const int32_t* group_offsets, int32_t num_groups, const float* tensor_scale_in,
+    const int32_t* group_offsets, int32_t num_groups, const int32_t* group_counts,
+    const float* tensor_scale_in,
     const float* tensor_amax_in, uint8_t* codes, int64_t ld_codes, uint8_t* scales,
     int32_t scale_layout, float* tensor_scale_out, float* score_partials,
     __nv_bfloat16* qdq, int64_t ldq, void* workspace, size_t workspace_bytes, void* stream) {
@@ -1432,6 +1492,8 @@ static quads_status_t quantize_impl(
     return fail(QUADS_ERR_MISALIGNED, "quantize: x/codes/score_partials must be 16-byte aligned");
   const int G = group_offsets ? num_groups : 1;
   if (group_offsets && num_groups < 1) return fail(QUADS_ERR_INVALID_ARG, "quantize: num_groups < 1");
+  if (group_counts && !group_offsets)
+    return fail(QUADS_ERR_INVALID_ARG, "quantize: group_counts needs group_offsets");
   if (tensor_scale_in && tensor_amax_in)
     return fail(QUADS_ERR_INVALID_ARG, "quantize: give tensor_scale_in or tensor_amax_in, not both");
   if (rows == 0) return QUADS_OK;
@@ -1448,7 +1510,8 @@ static quads_status_t quantize_impl(
     uint32_t* amax = (uint32_t*)workspace;
     cudaMemsetAsync(amax, 0, (size_t)G * 4, st);
     launch_dep(amax_kernel, grid_for((rows + kAmaxRows - 1) / kAmaxRows, 1, 8), 256, 0, st,
-        (const __nv_bfloat16*)x, rows, (int)cols, ldx, row_index, group_offsets, G, amax);
+        (const __nv_bfloat16*)x, rows, (int)cols, ldx, row_index, group_offsets, G, amax,
+        group_counts);
     amax_bits = amax;
   } else if (tensor_scale_in != tensor_scale_out) {
     cudaMemcpyAsync(tensor_scale_out, tensor_scale_in, (size_t)G * 4, cudaMemcpyDeviceToDevice, st);
@@ -1459,43 +1522,47 @@ static quads_status_t quantize_impl(
     const int64_t start = (rows / 128) * (ncols16 / 4) * 512;
     cudaMemsetAsync(scales + start, 0, (size_t)(sf_tc_bytes(rows, cols) - start), st);
   }
-  const int64_t ntasks = ((rows + 31) / 32) * ((cols + 255) / 256);  // one block per task
+  const int64_t ntasks = ((rows + 31) / 32) * ((cols + 255) / 256);
   if (ntasks >= (1ll << 31))
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "quantize: more than 2^31 32x256 tasks");
-  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(ntasks, (int64_t)num_sms() * 16));
+  // one block per task; with group counts (many tasks only write zeros) one
+  // resident wave of blocks looping over the tasks, so that a block's setup
+  // is not paid again for every padding task
+  const int per_sm = group_counts ? (score_partials ? 4 : 3) : 16;
+  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(ntasks, (int64_t)num_sms() * per_sm));
   const __nv_bfloat16* xb = (const __nv_bfloat16*)x;
   if (qdq)
     launch_dep(quantize_kernel<false, true>, blocks, 256, 0, st,
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
-        codes, ld_codes, scales, scale_layout, nullptr, qdq, ldq);
+        codes, ld_codes, scales, scale_layout, nullptr, qdq, ldq, group_counts);
   else if (score_partials && ((rows + 31) / 32) * (cols / 16) >= (int64_t)num_sms() * 512 &&
            ((rows + 31) / 32) * (cols / 16) < (1ll << 31))
     // enough (chunk, block) pairs for a thread each: about two blocks per SM
     launch_dep(quantize_chunk_kernel, grid_for(((rows + 31) / 32) * (cols / 16), 256, 3), 256, 0, st,
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
-        codes, ld_codes, scales, scale_layout, score_partials);
+        codes, ld_codes, scales, scale_layout, score_partials, group_counts);
   else if (score_partials)
     launch_dep(quantize_kernel<true, false>, blocks, 256, 0, st,
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
-        codes, ld_codes, scales, scale_layout, score_partials, nullptr, 0);
+        codes, ld_codes, scales, scale_layout, score_partials, nullptr, 0, group_counts);
   else
     launch_dep(quantize_kernel<false, false>, blocks, 256, 0, st,
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
-        codes, ld_codes, scales, scale_layout, nullptr, nullptr, 0);
+        codes, ld_codes, scales, scale_layout, nullptr, nullptr, 0, group_counts);
   return check_launch(qdq ? "qdq" : "quantize", launched);
 }
 
 extern "C" quads_status_t quads_quantize_nvfp4(
     const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* row_index,
-    const int32_t* group_offsets, int32_t num_groups, const float* tensor_scale_in,
-    const float* tensor_amax_in, uint8_t* codes, int64_t ld_codes, uint8_t* scales,
-    int32_t scale_layout,
-    float* tensor_scale_out, float* score_partials, void* workspace, size_t workspace_bytes,
-    void* stream) {
+    const int32_t* group_offsets, int32_t num_groups, const int32_t* group_counts,
+    const float* tensor_scale_in, const float* tensor_amax_in, uint8_t* codes, int64_t ld_codes,
+    uint8_t* scales, int32_t scale_layout, float* tensor_scale_out, float* score_partials,
+    void* workspace, size_t workspace_bytes, void* stream) {
   if (!codes && rows > 0) return fail(QUADS_ERR_INVALID_ARG, "quantize: null codes");
-  return quantize_impl(x, rows, cols, ldx, row_index, group_offsets, num_groups, tensor_scale_in,
-                       tensor_amax_in, codes, ld_codes, scales, scale_layout, tensor_scale_out,
-                       score_partials, nullptr, 0, workspace, workspace_bytes, stream);
+  return quantize_impl(x, rows, cols, ldx, row_index, group_offsets, num_groups, group_counts,
+                       tensor_scale_in, tensor_amax_in, codes, ld_codes, scales, scale_layout,
+                       tensor_scale_out, score_partials, nullptr, 0, workspace, workspace_bytes,
+                       stream);
 }
 
 extern "C" quads_status_t quads_qdq_nvfp4(
@@ -1504,9 +1571,10 @@ extern "C" quads_status_t quads_qdq_nvfp4(
     int64_t ld_codes, uint8_t* scales, int32_t scale_layout, float* tensor_scale_out,
     void* workspace, size_t workspace_bytes, void* stream) {
   if (!y && rows > 0) return fail(QUADS_ERR_INVALID_ARG, "qdq: null y");
-  return quantize_impl(x, rows, cols, ldx, nullptr, group_offsets, num_groups, tensor_scale_in,
-                       nullptr, codes, ld_codes, scales, scale_layout, tensor_scale_out, nullptr,
-                       (__nv_bfloat16*)y, ldy, workspace, workspace_bytes, stream);
+  return quantize_impl(x, rows, cols, ldx, nullptr, group_offsets, num_groups, nullptr,
+                       tensor_scale_in, nullptr, codes, ld_codes, scales, scale_layout,
+                       tensor_scale_out, nullptr, (__nv_bfloat16*)y, ldy, workspace,
+                       workspace_bytes, stream);
 }
 
 namespace quads {

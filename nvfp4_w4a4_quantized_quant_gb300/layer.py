@@ -191,7 +191,9 @@ class MoEExpertLayer:
         h = Q.moe_grouped_gemm(plan, a1, self.w1q, E, 2 * F, r1, sel1, self.k1,
                                epilogue=Q.EPI_SWIGLU, y_amax=b["hamax"], w_sel=w1sel,
                                out=b["h"], stream=stream)
+        # h's padding rows (past each expert's count) are zero: not read
         hq, hpart = Q.quantize_nvfp4(h, group_offsets=plan["offsets"], num_groups=E,
+                                     group_counts=plan["counts"],
                                      tensor_amax_in=b["hamax"], scale_layout=Q.TCGEN05,
                                      scores=comp, rows=self.cap,
                                      workspace=ws["q2"], stream=stream,

@@ -37,8 +37,8 @@ _SIGS = {
     "quads_set_gemm_tile_policy": (ctypes.c_int32, [ctypes.c_int32]),
     "quads_workspace_size": (_SZ, [_I32, _I64, _I64, _I64, _I32, _I32]),
     "quads_kpad": (_I32, [_I32]),
-    "quads_quantize_nvfp4": (_I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P, _I64, _P,
-                                    _I32, _P, _P, _P, _SZ, _P]),
+    "quads_quantize_nvfp4": (_I32, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P, _P, _I64,
+                                    _P, _I32, _P, _P, _P, _SZ, _P]),
     "quads_qdq_nvfp4": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _I64, _P, _I64, _P, _I32,
                                _P, _P, _SZ, _P]),
     "quads_select_residual_channels": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _I32, _P, _P,
@@ -198,11 +198,13 @@ class QTensor:
 
 
 def quantize_nvfp4(x: torch.Tensor, *, group_offsets=None, num_groups: int = 1,
-                   tensor_scale_in=None, tensor_amax_in=None, scale_layout: int = LINEAR,
-                   scores: bool = False,
+                   group_counts=None, tensor_scale_in=None, tensor_amax_in=None,
+                   scale_layout: int = LINEAR, scores: bool = False,
                    row_index=None, rows: Optional[int] = None, workspace=None, out=None,
                    stream=None):
-    """x bf16 [rows, cols] -> (QTensor, score partials [ceil(rows/32), cols] or None)."""
+    """x bf16 [rows, cols] -> (QTensor, score partials [ceil(rows/32), cols] or None).
+    group_counts (int32 [num_groups], with group_offsets): rows of group g at or
+    past offsets[g] + counts[g] are taken as zero rows and not read."""
     lib = load()
     assert x.dtype == torch.bfloat16 and x.dim() == 2
     rows = x.shape[0] if rows is None else rows
@@ -220,7 +222,8 @@ def quantize_nvfp4(x: torch.Tensor, *, group_offsets=None, num_groups: int = 1,
         codes, scales, ts, part = out
     ws = _workspace(workspace_size(OP_QUANTIZE, rows, cols, 0, 0, G), dev, workspace, stream)
     _check(lib.quads_quantize_nvfp4(_ptr(x), rows, cols, x.stride(0), _ptr(row_index),
-                                    _ptr(group_offsets), G, _ptr(tensor_scale_in),
+                                    _ptr(group_offsets), G, _ptr(group_counts),
+                                    _ptr(tensor_scale_in),
                                     _ptr(tensor_amax_in), _ptr(codes),
                                     codes.stride(0), _ptr(scales), scale_layout, _ptr(ts),
                                     _ptr(part), _ptr(ws), ws.numel(), _stream(stream)),

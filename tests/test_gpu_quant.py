@@ -116,6 +116,88 @@ def test_quantize_scores_per_expert_groups_sampled_chunks(lib, layout):
         assert np.array_equal(pc[ch:ch + 1], Q.chunk_partials(R))
 
 
+def _padded_groups(rng, counts, tile, cols):
+    """Row groups of `counts` real rows, each padded up to a multiple of
+    `tile` rows (at least one tile), the padding filled with nonzero values;
+    returns (x with garbage padding, x with zero padding, offsets)."""
+    sizes = np.maximum((counts + tile - 1) // tile, 1) * tile
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    x = inputs.student_t4(rng, (int(offs[-1]), cols))
+    xz = x.copy()
+    for g, c in enumerate(counts):
+        xz[offs[g] + c:offs[g + 1]] = 0.0
+    return x, xz, offs
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("scores", [False, True])
+def test_quantize_group_counts_take_padding_rows_as_zero(lib, layout, scores):
+    """With group_counts, rows past each group's count are zero rows whatever
+    they hold: the amax pass, codes, scales and score partials equal the
+    oracle's on x with those rows zeroed (and the call without counts on that
+    zeroed x), on the 32x256-task quantizer."""
+    rng = inputs.make_rng(12)
+    counts = np.array([5, 0, 128, 33, 64, 100, 250], np.int32)
+    x, xz, offs = _padded_groups(rng, counts, 128, 256)
+    G = len(counts)
+    bits, bz = inputs.f32_to_bf16_bits(x), inputs.f32_to_bf16_bits(xz)
+    ot, ct = torch.from_numpy(offs).cuda(), torch.from_numpy(counts).cuda()
+    q, part = lib.quantize_nvfp4(bf16_tensor(bits), group_offsets=ot, num_groups=G, group_counts=ct,
+                                 scores=scores, scale_layout=layout)
+    qz, partz = lib.quantize_nvfp4(bf16_tensor(bz), group_offsets=ot, num_groups=G, scores=scores,
+                                   scale_layout=layout)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    assert torch.equal(q.codes, qz.codes) and torch.equal(q.scales, qz.scales)
+    assert torch.equal(q.tensor_scale, qz.tensor_scale)
+    xf = f32(bz)
+    oc, osc, ost = Q.quantize_groups(xf, offs)
+    assert np.array_equal(q.tensor_scale.cpu().numpy(), ost)
+    assert np.array_equal(codes_np(q.codes, 256), oc)
+    assert np.array_equal(linear_scales(q), osc)
+    if scores:
+        assert torch.equal(part, partz)
+        R = np.concatenate([Q.residual(xf[a:b], oc[a:b], osc[a:b], ost[g])
+                            for g, (a, b) in enumerate(zip(offs[:-1], offs[1:]))])
+        assert np.array_equal(part.cpu().numpy(), Q.chunk_partials(R))
+
+
+def test_quantize_group_counts_thread_per_chunk_kernel(lib):
+    """The same rule on the thread-per-(chunk, block) score kernel (the shape
+    of the per-expert h quantization: 128 groups of up to 512 rows x 768),
+    with the groups' amax given as in the layer: bit-equal to the call without
+    counts on the zeroed input, the oracle checked on sampled chunks, padding
+    chunks included."""
+    rng = inputs.make_rng(13)
+    counts = rng.integers(300, 513, 128).astype(np.int32)   # enough pairs for that kernel
+    counts[:4] = [0, 1, 512, 31]
+    x, xz, offs = _padded_groups(rng, counts, 128, 768)
+    bits, bz = inputs.f32_to_bf16_bits(x), inputs.f32_to_bf16_bits(xz)
+    xf = f32(bz)
+    amax = np.array([np.abs(xf[a:b]).max() if b > a else 0.0
+                     for a, b in zip(offs[:-1], offs[1:])], np.float32)
+    ot, ct = torch.from_numpy(offs).cuda(), torch.from_numpy(counts).cuda()
+    at = torch.from_numpy(amax).cuda()
+    q, part = lib.quantize_nvfp4(bf16_tensor(bits), group_offsets=ot, num_groups=128, group_counts=ct,
+                                 tensor_amax_in=at, scores=True, scale_layout=1)
+    qz, partz = lib.quantize_nvfp4(bf16_tensor(bz), group_offsets=ot, num_groups=128,
+                                   tensor_amax_in=at, scores=True, scale_layout=1)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    assert torch.equal(q.codes, qz.codes) and torch.equal(q.scales, qz.scales)
+    assert torch.equal(part, partz)
+    ts = q.tensor_scale.cpu().numpy()
+    codes, scales, pc = codes_np(q.codes, 768), linear_scales(q), part.cpu().numpy()
+    pad_chunks = [c for g in range(128) for c in range((offs[g] + counts[g] + 31) // 32, offs[g + 1] // 32)]
+    sample = list(rng.choice(int(offs[-1]) // 32, 24, replace=False)) + pad_chunks[:8]
+    for ch in sample:
+        a, b = 32 * ch, 32 * ch + 32
+        g = int(np.searchsorted(offs, a, side="right") - 1)
+        oc, osc = Q.quantize(xf[a:b], ts[g])
+        assert np.array_equal(codes[a:b], oc) and np.array_equal(scales[a:b], osc)
+        assert np.array_equal(pc[ch:ch + 1], Q.chunk_partials(Q.residual(xf[a:b], oc, osc, ts[g])))
+
+
 def test_quantize_given_tensor_scale(lib):
     bits = _case("ragged")
     x = bf16_tensor(bits)

@@ -39,16 +39,18 @@ def _err(lib):
 
 def test_host_side_argument_checks_need_no_gpu(lib):
     p = ctypes.c_void_p(16)     # never dereferenced: every call below fails validation first
-    st = lib.quads_quantize_nvfp4(p, 8, 15, 16, None, None, 1, None, None, p, 8, p, 0, p, None, p, 64, None)
+    st = lib.quads_quantize_nvfp4(p, 8, 15, 16, None, None, 1, None, None, None, p, 8, p, 0, p, None, p, 64, None)
     assert st == 2 and "multiple of 16" in _err(lib)
-    st = lib.quads_quantize_nvfp4(None, 8, 16, 16, None, None, 1, None, None, p, 8, p, 0, p, None, p, 64, None)
+    st = lib.quads_quantize_nvfp4(None, 8, 16, 16, None, None, 1, None, None, None, p, 8, p, 0, p, None, p, 64, None)
     assert st == 1
-    st = lib.quads_quantize_nvfp4(p, 8, 32, 16, None, None, 1, None, None, p, 16, p, 0, p, None, p, 64, None)
+    st = lib.quads_quantize_nvfp4(p, 8, 32, 16, None, None, 1, None, None, None, p, 16, p, 0, p, None, p, 64, None)
     assert st == 3                                   # ldx < cols
-    st = lib.quads_quantize_nvfp4(p, 8, 32, 32, None, None, 1, None, None, p, 16, p, 1, p, None, p, 64, None)
+    st = lib.quads_quantize_nvfp4(p, 8, 32, 32, None, None, 1, None, None, None, p, 16, p, 1, p, None, p, 64, None)
     assert st == 2                                   # tcgen05 layout needs cols % 64
-    st = lib.quads_quantize_nvfp4(p, 8, 32, 32, None, None, 1, p, p, p, 16, p, 0, p, None, p, 64, None)
+    st = lib.quads_quantize_nvfp4(p, 8, 32, 32, None, None, 1, None, p, p, p, 16, p, 0, p, None, p, 64, None)
     assert st == 1                                   # both tensor_scale_in and tensor_amax_in
+    st = lib.quads_quantize_nvfp4(p, 8, 32, 32, None, None, 1, p, None, None, p, 16, p, 0, p, None, p, 64, None)
+    assert st == 1 and "group_counts" in _err(lib)   # counts without group offsets
     st = lib.quads_w4a4_gemm_comp(64, 100, 256, p, p, p, p, p, p, None, None, None, None, None, None,
                                   None, None, 0, p, 0, 100, None, 0, None)
     assert st == 2 and "N%128" in _err(lib)
