@@ -142,7 +142,7 @@ class MoEExpertLayer:
         self.side = torch.cuda.Stream(device=dev)
         self.wside = torch.cuda.Stream(device=dev)
         (self.ev_fork, self.ev_xq, self.ev_a1, self.ev_sel1, self.ev_w1, self.ev_sel2,
-         self.ev_w2) = (torch.cuda.Event() for _ in range(7))
+         self.ev_w2, self.ev_plan) = (torch.cuda.Event() for _ in range(8))
         # the weight preparation and buffer fills above ran on the current
         # stream; forward() runs on streams that do not wait for it (and the
         # allocator may already have handed that work's freed scratch to the
@@ -159,6 +159,7 @@ class MoEExpertLayer:
         self.side.wait_event(self.ev_fork)
         plan = Q.moe_route(logits, self.topk, rows_capacity=self.cap, out=b["route"],
                            workspace=ws["rt"], stream=self.side)
+        self.ev_plan.record(self.side)
         r1 = sel1 = w1sel = xr = None
         if comp and self.fused:
             # X's activation side in one cooperative launch: quantization,
@@ -183,10 +184,12 @@ class MoEExpertLayer:
             w1sel = Q.select_weight_channels(self.w1q, sel1, self.k1, E, stream=self.wside,
                                              out=(b["w1sc"], b["w1ss"]))
             self.ev_w1.record(self.wside)
-        main.wait_event(self.ev_a1)
         if comp:
+            # R_sel's rows need only the plan, not the gather of X's rows
+            main.wait_event(self.ev_plan)
             r1 = Q.moe_gather(plan, xr, out=(b["g1c"], b["g1s"]), stream=stream)
             main.wait_event(self.ev_w1)
+        main.wait_event(self.ev_a1)
         # GEMM1's epilogue also leaves each expert's max |h| for h's tensor scale
         h = Q.moe_grouped_gemm(plan, a1, self.w1q, E, 2 * F, r1, sel1, self.k1,
                                epilogue=Q.EPI_SWIGLU, y_amax=b["hamax"], w_sel=w1sel,
