@@ -23,6 +23,12 @@
  *     buffer `workspace` of at least quads_workspace_size(...) bytes.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
  *     only enqueues work on it and returns; no call synchronises the stream.
+ *     The layer-path kernels are launched with programmatic stream
+ *     serialization (a launch may be set up while the stream's previous kernel
+ *     still runs) and each one first waits (griddepcontrol.wait) until every
+ *     kernel it depends on in the stream has completed and its writes are
+ *     visible, so stream order holds as for ordinary launches, the caller's
+ *     own kernels included.
  *   - Host-side argument checks return QUADS_ERR_INVALID_ARG,
  *     QUADS_ERR_UNSUPPORTED_SHAPE or QUADS_ERR_MISALIGNED before anything is
  *     enqueued; a launch failure returns QUADS_ERR_CUDA.  quads_last_error_detail()
@@ -192,9 +198,11 @@ int32_t quads_kpad(int32_t k);
  *                  rows of group g at or past group_offsets[g] +
  *                  group_counts[g] are taken as zero rows -- not read, their
  *                  codes, scale bytes and score partials written as those of
- *                  zeros (for per-expert rows padded to a tile multiple whose
- *                  padding is zero anyway, the quantizer then reads only the
- *                  real rows).
+ *                  zeros, and left out of the group's amax (for per-expert rows
+ *                  padded to a tile multiple whose padding is zero anyway, the
+ *                  quantizer then reads only the real rows).  A count above
+ *                  the group's size means every row is real; a count of 0 or
+ *                  below, none.
  *   tensor_scale_in nullable device float [num_groups]: use these tensor
  *                  scales instead of computing amax / 2688.
  *   tensor_amax_in nullable device float [num_groups]: the groups' absolute
