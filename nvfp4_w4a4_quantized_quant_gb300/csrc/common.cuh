@@ -125,6 +125,21 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
   return (c & 8u) ? -mag : mag;
 }
 
+// A pair of scaled values rounded to E2M1 (nearest even, saturating), and the
+// codes' values back as floats: hardware conversions both ways (a is the low
+// nibble of the pair).
+__device__ __forceinline__ void e2m1_round_pair(float a, float b, float& qa, float& qb) {
+  uint32_t h;
+  asm("{\n\t.reg .b8 c;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c, %2, %1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, c;\n\t}"
+      : "=r"(h)
+      : "f"(a), "f"(b));
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+  qa = f.x;
+  qb = f.y;
+}
+
 // Eight packed codes -> eight floats via the hardware E2M1 -> f16 converter.
 __device__ __forceinline__ void e2m1x8_to_f32(uint32_t packed, float* out) {
   uint32_t h[4];

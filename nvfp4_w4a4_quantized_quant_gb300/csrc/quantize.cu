@@ -631,6 +631,32 @@ __global__ void __launch_bounds__(NT) topk_kernel(float* __restrict__ scores, in
 }
 
 // ---------------------------------------------------------------- residual slice
+// Block-scale table of one tensor scale s_t: for every E4M3 byte, d =
+// E4M3 * s_t and its correctly rounded reciprocal (0 where the block's codes
+// are 0), so that a gathered element needs two shared loads instead of the
+// per-element scale decode.
+__device__ __forceinline__ void fill_scale_table(float s_t, float* td, float* tr) {
+  for (int b = threadIdx.x; b < 256; b += blockDim.x) {
+    const BlockScale bs = block_scale_from_byte((uint32_t)b, s_t);
+    td[b] = bs.d;
+    tr[b] = bs.zero ? 0.0f : bs.r;   // d is finite, so 1/d == 0 only for zero blocks
+  }
+}
+// R = x - fl(DQ(Q(x))) for two elements with their blocks' table entries:
+// the code is the E2M1 rounding of fl(x * r) (0 where r == 0), as
+// quantize_block16 forms it.
+__device__ __forceinline__ void residual_pair(float xa, float xb, uint32_t sa, uint32_t sb,
+                                              const float* td, const float* tr, float& Ra,
+                                              float& Rb) {
+  const float ra = tr[sa], rb = tr[sb];
+  float qa, qb;
+  e2m1_round_pair(__fmul_rn(xa, ra), __fmul_rn(xb, rb), qa, qb);
+  if (ra == 0.0f) qa = 0.0f;
+  if (rb == 0.0f) qb = 0.0f;
+  Ra = __fsub_rn(xa, __fmul_rn(qa, td[sa]));
+  Rb = __fsub_rn(xb, __fmul_rn(qb, td[sb]));
+}
+
 // R[:, sel] recomputed from x and the stored block scales; one block per
 // slice of `rb` rows (8 or 32: group offsets are multiples of 32, so a slice
 // is inside one group; 8 when 32-row slices would leave the GPU short of
@@ -643,13 +669,20 @@ __global__ void __launch_bounds__(256) rsel_residual_kernel(
     float* __restrict__ rs, uint32_t* __restrict__ amax_bits, int rb) {
   griddep_wait();
   __shared__ float red[8];
+  __shared__ float td[256], tr[256];
   const int64_t end = goff ? (int64_t)goff[G] : rows;
   const int64_t nblk = (end + rb - 1) / rb;
   const int ncols16 = cols >> 4;
+  int tab_g = -1;
   for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
     const int64_t r0 = blk * rb, r1 = min(r0 + rb, end);
     const int g = goff ? group_of(goff, G, r0) : 0;
-    const float s_t = st[g];
+    if (g != tab_g) {   // block-uniform: the scale table of the slice's group
+      __syncthreads();
+      fill_scale_table(st[g], td, tr);
+      __syncthreads();
+      tab_g = g;
+    }
     const int32_t* sg = sel + (int64_t)g * k;
     float m = 0.0f;
     const int total = (int)(r1 - r0) * k;
@@ -671,16 +704,15 @@ __global__ void __launch_bounds__(256) rsel_residual_kernel(
         xv[u] = __bfloat162float(x[r[u] * ldx + c[u]]);
         sb[u] = scales[sf_offset(layout, r[u], c[u] >> 4, ncols16)];
       }
+      float R[4];
+      residual_pair(xv[0], xv[1], sb[0], sb[1], td, tr, R[0], R[1]);
+      residual_pair(xv[2], xv[3], sb[2], sb[3], td, tr, R[2], R[3]);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int i = i0 + u * (int)blockDim.x;
         if (i >= total) continue;
-        const BlockScale bs = block_scale_from_byte(sb[u], s_t);
-        float v[8] = {__fmul_rn(xv[u], bs.r), 0, 0, 0, 0, 0, 0, 0};
-        const uint32_t code = bs.zero ? 0u : (f32x8_to_e2m1(v) & 15u);
-        const float R = __fsub_rn(xv[u], __fmul_rn(e2m1_to_f32(code), bs.d));
-        rs[r[u] * k + j[u]] = R;
-        m = fmaxf(m, fabsf(R));
+        rs[r[u] * k + j[u]] = R[u];
+        m = fmaxf(m, fabsf(R[u]));
       }
     }
     m = warp_max(m);
@@ -727,8 +759,10 @@ __global__ void __launch_bounds__(kRselGroupThreads) rsel_group_kernel(
   }
   const int g = blockIdx.x;
   const int64_t r0 = goff[g], r1 = goff[g + 1];
-  const float s_t = st[g];
   const int32_t* sg = sel + (int64_t)g * k;
+  __shared__ float td[256], tr[256];
+  fill_scale_table(st[g], td, tr);
+  __syncthreads();
   const int total = (int)(r1 - r0) * k;
   float m = 0.0f;
   for (int i0 = threadIdx.x; i0 < total; i0 += 4 * blockDim.x) {
@@ -749,16 +783,15 @@ __global__ void __launch_bounds__(kRselGroupThreads) rsel_group_kernel(
       xv[u] = __bfloat162float(x[r[u] * ldx + c[u]]);
       sb[u] = scales[sf_offset(layout, r[u], c[u] >> 4, ncols16)];
     }
+    float R[4];
+    residual_pair(xv[0], xv[1], sb[0], sb[1], td, tr, R[0], R[1]);
+    residual_pair(xv[2], xv[3], sb[2], sb[3], td, tr, R[2], R[3]);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u * (int)blockDim.x;
       if (i >= total) continue;
-      const BlockScale bs = block_scale_from_byte(sb[u], s_t);
-      float v[8] = {__fmul_rn(xv[u], bs.r), 0, 0, 0, 0, 0, 0, 0};
-      const uint32_t code = bs.zero ? 0u : (f32x8_to_e2m1(v) & 15u);
-      const float R = __fsub_rn(xv[u], __fmul_rn(e2m1_to_f32(code), bs.d));
-      rs[r[u] * k + j[u]] = R;
-      m = fmaxf(m, fabsf(R));
+      rs[r[u] * k + j[u]] = R[u];
+      m = fmaxf(m, fabsf(R[u]));
     }
   }
   m = warp_max(m);
