@@ -1558,10 +1558,11 @@ static quads_status_t quantize_impl(
   const int64_t ntasks = ((rows + 31) / 32) * ((cols + 255) / 256);
   if (ntasks >= (1ll << 31))
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "quantize: more than 2^31 32x256 tasks");
-  // one block per task; with group counts (many tasks only write zeros) one
-  // resident wave of blocks looping over the tasks, so that a block's setup
-  // is not paid again for every padding task
-  const int per_sm = group_counts ? (score_partials ? 4 : 3) : 16;
+  // one resident wave of blocks looping over the tasks (the next task's rows
+  // are loaded while the current one is quantized; a block's setup is paid
+  // once): 1 GiB plain 282 -> 270 us, 8192 x 2048 plain 20.3 -> 17.9 us
+  // against a block per task
+  const int per_sm = score_partials ? 4 : 3;
   const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(ntasks, (int64_t)num_sms() * per_sm));
   const __nv_bfloat16* xb = (const __nv_bfloat16*)x;
   if (qdq)
