@@ -2278,8 +2278,18 @@ struct Launch {
 static void launch_wsel(const uint8_t* b_t, const uint8_t* b_sf_t, int E, int N, int K,
                         const int32_t* sel, int sel_pe, int k, int kpad, uint8_t* codes,
                         uint8_t* sf, cudaStream_t stream) {
-  // row chunks of 512 (or 128) rows: N is a multiple of 128
-  const int NC = N % 512 == 0 ? 512 : 128;
+  // rows per CTA: the largest chunk (N is a multiple of 128) that still
+  // gives every SM work and fits one resident wave (eight CTAs per SM), so
+  // that no partial second wave doubles the time; else 128-row chunks
+  const int64_t per_chunk = (int64_t)(kpad / 16) * E;
+  int NC = 128;
+  for (const int c : {1024, 768, 512, 256}) {
+    const int64_t ctas = per_chunk * (N / c);
+    if (N % c == 0 && ctas >= num_sms() && ctas <= 8 * (int64_t)num_sms()) {
+      NC = c;
+      break;
+    }
+  }
   const size_t cols_smem = (size_t)24 * NC;   // 16 columns x (NC/2 code + NC scale bytes)
   const dim3 grid((unsigned)(kpad / 16), (unsigned)E, (unsigned)(N / NC));
   launch_dep(wsel_cols_kernel, grid, 256, cols_smem, stream, b_t, b_sf_t, N, K, NC, sel, sel_pe, k,
