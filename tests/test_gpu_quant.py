@@ -131,14 +131,26 @@ def _padded_groups(rng, counts, tile, cols):
 
 @pytest.mark.parametrize("layout", [0, 1])
 @pytest.mark.parametrize("scores", [False, True])
-def test_quantize_group_counts_take_padding_rows_as_zero(lib, layout, scores):
+@pytest.mark.parametrize("many", [False, True])
+def test_quantize_group_counts_take_padding_rows_as_zero(lib, layout, scores, many):
     """With group_counts, rows past each group's count are zero rows whatever
     they hold: the amax pass, codes, scales and score partials equal the
     oracle's on x with those rows zeroed (and the call without counts on that
-    zeroed x), on the 32x256-task quantizer."""
+    zeroed x), on the 32x256-task quantizer; `many`: 300 groups of 32-row
+    tiles (more groups than the kernel caches in shared memory), counts
+    outside [0, size] included."""
     rng = inputs.make_rng(12)
-    counts = np.array([5, 0, 128, 33, 64, 100, 250], np.int32)
-    x, xz, offs = _padded_groups(rng, counts, 128, 256)
+    if many:
+        sizes = 32 * rng.integers(1, 3, 300)
+        counts = rng.integers(-3, 80, 300).astype(np.int32)   # below 0 and past the size too
+        offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+        x = inputs.student_t4(rng, (int(offs[-1]), 256))
+        xz = x.copy()
+        for g in range(300):
+            xz[offs[g] + min(max(int(counts[g]), 0), int(sizes[g])):offs[g + 1]] = 0.0
+    else:
+        counts = np.array([5, 0, 128, 33, 64, 100, 250], np.int32)
+        x, xz, offs = _padded_groups(rng, counts, 128, 256)
     G = len(counts)
     bits, bz = inputs.f32_to_bf16_bits(x), inputs.f32_to_bf16_bits(xz)
     ot, ct = torch.from_numpy(offs).cuda(), torch.from_numpy(counts).cuda()
