@@ -267,10 +267,11 @@ def secondary(torch, Q, steps, flush, stream):
     xm = torch.from_numpy(dm["x"].view(np.int16)).view(torch.bfloat16).cuda()
     lm = torch.from_numpy(dm["logits"]).cuda()
     moe = {}
-    for name, comp, fused in (("plain", False, False), ("comp", True, False),
-                              ("comp_fused_activation_side", True, True)):
+    for name, comp, fused, fused_h in (("plain", False, False, None), ("comp", True, False, None),
+                                       ("comp_fused_activation_side", True, True, None),
+                                       ("comp_fused_expert_side", True, False, True)):
         lay = MoEExpertLayer(w1, w2, wm["topk"], wm["k1"], wm["k2"], wm["tokens"], compensate=comp,
-                             fused_activation_side=fused)
+                             fused_activation_side=fused, fused_expert_side=fused_h)
         ms = graph_ms(lambda: lay.forward(xm, lm, stream=stream))
         moe[name] = {"ms": round(ms, 4)}
         del lay
@@ -324,14 +325,17 @@ def secondary(torch, Q, steps, flush, stream):
     w1 = (torch.randn((E, 2 * F, H), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
     w2 = (torch.randn((E, H, F), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
     layer = MoEExpertLayer(w1, w2, wl["topk"], wl["k1"], wl["k2"], 512)
+    layer2 = MoEExpertLayer(w1, w2, wl["topk"], wl["k1"], wl["k2"], 512, fused_expert_side=False)
     del w1, w2
     xd = torch.from_numpy(dd["x"].view(np.int16)).view(torch.bfloat16).cuda()
     ld = torch.from_numpy(dd["logits"]).cuda()
     ms = graph_ms(lambda: layer.forward(xd, ld, stream=stream))
+    ms2 = graph_ms(lambda: layer2.forward(xd, ld, stream=stream))
     wbytes = E * (2 * F * H + H * F) * (0.5 + 1.0 / 16)
     out["moe_decode_512"] = {"ms": round(ms, 4), "weight_gbs": round(wbytes / (ms * 1e-3) / 1e9, 1),
-                             "weight_bytes": int(wbytes), "frac_hbm": None}
-    del layer
+                             "weight_bytes": int(wbytes), "frac_hbm": None,
+                             "ms_expert_side_two_calls": round(ms2, 4)}
+    del layer, layer2
 
     t = inputs.trace_rounding(0)
     xr = torch.from_numpy(t["x_rollout"].view(np.int16)).view(torch.bfloat16).cuda()

@@ -92,7 +92,8 @@ enum {
   QUADS_OP_GEMM = 2,
   QUADS_OP_MOE_GEMM = 3,
   QUADS_OP_MOE_ROUTE = 4,
-  QUADS_OP_QUANTIZE_SELECT = 5
+  QUADS_OP_QUANTIZE_SELECT = 5,
+  QUADS_OP_QUANTIZE_SELECT_GROUPS = 6
 };
 
 /* Rows of the score-partial array are chunks of this many consecutive rows. */
@@ -172,6 +173,7 @@ int32_t quads_set_gemm_tile_policy(int32_t policy);
  *   QUADS_OP_QUANTIZE_SELECT: 256 bytes of control words + the score partials
  *                      (ceil(rows/32)*cols floats) + cols floats of scores +
  *                      rows*k floats (the residual slice), each 256-byte aligned.
+ *   QUADS_OP_QUANTIZE_SELECT_GROUPS: rows*k floats (the residual slice).
  * `cols` is the channel count (K) and `n` the output width (N, unused for the
  * activation-side ops).  kpad = k rounded up to 64 (k <= 256) or to 256. */
 size_t quads_workspace_size(int32_t op, int64_t rows, int64_t cols, int64_t n, int32_t k,
@@ -352,6 +354,52 @@ quads_status_t quads_quantize_select_nvfp4(
     int64_t ld_codes, uint8_t* scales, int32_t scale_layout, float* tensor_scale_out, int32_t* sel,
     float* scores_out, uint8_t* r_codes, uint8_t* r_scales, int32_t r_scale_layout,
     float* r_tensor_scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * quads_quantize_select_groups_nvfp4 -- quads_quantize_nvfp4 (row groups,
+ * score partials) followed by quads_select_residual_channels (per-group
+ * selection) for every group at once, one thread block per group: the
+ * group's rows are quantized chunk by chunk, its channel scores kept on chip,
+ * its top-k channels chosen and R[:, sel] quantized a second time in the same
+ * block, so a group's rows are read from memory once for the quantization and
+ * the chunk partials never reach memory.  Groups are independent, so no block
+ * waits on another.  [QUADS] 2.2 B "Mechanism" and "Implementation" (the
+ * high-residual channels chosen online per input; the correction path fused),
+ * [TRACE] "MoE 专家路由敏感性" (one selection per expert).
+ * Outputs are those of the two calls with group_counts given, bit for bit:
+ * codes [rows, ld_codes] and scales (scale_layout) of the groups' rows,
+ * tensor_scale_out[num_groups], sel[num_groups, k] (ascending per group),
+ * scores_out (nullable, [num_groups, cols]), R_sel codes [rows, kpad/2] and
+ * scales (r_scale_layout), r_tensor_scale[num_groups]; no score partials.
+ *   x, rows, cols, ldx   bf16 device rows, row-major; 16 <= cols <= 1024,
+ *                        cols % 16 == 0 (cols % 64 for TCGEN05 scales).
+ *   group_offsets        device int32 [num_groups+1], ascending, multiples of
+ *                        QUADS_SCORE_CHUNK_ROWS (a group that starts elsewhere
+ *                        latches QUADS_ERR_DEVICE_CHECK); rows past the last
+ *                        offset get zero R_sel codes and scales and keep their
+ *                        Q(x) outputs untouched.
+ *   group_counts         nullable device int32 [num_groups]: rows of group g at
+ *                        or past offsets[g] + counts[g] are zero rows, not read
+ *                        (counts are clamped to [0, group size]).
+ *   tensor_scale_in / tensor_amax_in  nullable device float [num_groups], at
+ *                        most one: the groups' tensor scales, or their amax
+ *                        (scale = amax / 2688, 1 when 0); with neither, each
+ *                        block takes its group's amax itself.
+ *   k                    16 <= k <= cols, k % 16 == 0; kpad = quads_kpad(k).
+ *   workspace            >= quads_workspace_size(QUADS_OP_QUANTIZE_SELECT_GROUPS,
+ *                        rows, cols, 0, k, num_groups) bytes, device.
+ *   sel_ready_event      nullable cudaEvent_t, recorded on the stream after the
+ *                        launch (sel is then written).
+ * rows * k < 2^31.  Errors as quads_quantize_nvfp4 and
+ * quads_select_residual_channels; nothing is launched on a host-side error.
+ */
+quads_status_t quads_quantize_select_groups_nvfp4(
+    const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* group_offsets,
+    int32_t num_groups, const int32_t* group_counts, const float* tensor_scale_in,
+    const float* tensor_amax_in, int32_t k, uint8_t* codes, int64_t ld_codes, uint8_t* scales,
+    int32_t scale_layout, float* tensor_scale_out, int32_t* sel, float* scores_out,
+    uint8_t* r_codes, uint8_t* r_scales, int32_t r_scale_layout, float* r_tensor_scale,
+    void* workspace, size_t workspace_bytes, void* sel_ready_event, void* stream);
 
 /*
  * quads_w4a4_gemm_comp -- Y = s_a s_w Q(A) Q(W)^T + s_r s_w Q(R_sel) Q(W_sel)^T

@@ -99,6 +99,8 @@ extern "C" size_t quads_workspace_size(int32_t op, int64_t rows, int64_t cols, i
       auto al = [](size_t b) { return (b + 255) & ~(size_t)255; };
       return 256 + al((r + 31) / 32 * c * 4) + al(c * 4) + al(r * kk * 4);
     }
+    case QUADS_OP_QUANTIZE_SELECT_GROUPS:  // residual slice
+      return rows > 0 && k > 0 ? (size_t)rows * (size_t)k * 4 : 0;
     case QUADS_OP_MOE_ROUTE:  // per-32-token-block expert counts and prefixes: rows = tokens, cols = experts
       return (size_t)((rows > 0 ? rows : 0) + 31) / 32 * (size_t)(cols > 0 ? cols : 0) * 8 + 16;
     case QUADS_OP_GEMM:

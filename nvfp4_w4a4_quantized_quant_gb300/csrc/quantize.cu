@@ -734,35 +734,37 @@ __global__ void __launch_bounds__(256) rsel_residual_kernel(
 // so no grid-wide maximum and no second launch are needed.  Blocks past the
 // groups zero the rows after the last offset.
 constexpr int kRselGroupThreads = 1024;
-__global__ void __launch_bounds__(kRselGroupThreads) rsel_group_kernel(
-    const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
-    const int32_t* __restrict__ goff, int G, const uint8_t* __restrict__ scales, int layout,
-    const float* __restrict__ st, const int32_t* __restrict__ sel, int k, int kpad,
-    float* __restrict__ rs, uint8_t* __restrict__ rcodes, uint8_t* __restrict__ rscales,
-    int rlayout, float* __restrict__ rst) {
-  griddep_wait();
-  __shared__ float red[kRselGroupThreads / 32];
+
+// Zero R_sel codes and scales of rows [end, rows) (past the last group), as
+// block `b` of `nb` blocks.
+__device__ __forceinline__ void rsel_zero_tail(int64_t rows, int64_t end, int kpad,
+                                               uint8_t* __restrict__ rcodes,
+                                               uint8_t* __restrict__ rscales, int rlayout, int b,
+                                               int nb) {
+  const int vpr = kpad >> 3, rcols16 = kpad >> 4;
+  const int64_t total = (rows - end) * vpr;
+  for (int64_t i = (int64_t)b * blockDim.x + threadIdx.x; i < total; i += (int64_t)nb * blockDim.x) {
+    const int64_t r = end + i / vpr;
+    const int col = (int)(i % vpr) * 8;
+    *reinterpret_cast<uint32_t*>(rcodes + r * (kpad >> 1) + (col >> 1)) = 0u;
+    if (((col >> 3) & 1) == 0) rscales[sf_offset(rlayout, r, col >> 4, rcols16)] = 0;
+  }
+}
+
+// R[:, sel] of one group's rows [r0, r1) by the whole block: R into the
+// float32 workspace rs (row r at rs + r * k), the group's amax by a block
+// reduction, then the second quantization of those rows.  Rows at or past
+// rreal are zero rows (not read; their R is 0).  td/tr: the block-scale table
+// of the group's tensor scale (filled, and a barrier passed, by the caller);
+// sg: the group's k selected channels; red: NT/32 floats of shared memory.
+// The group's R_sel tensor scale is stored to *rst_g.
+__device__ __forceinline__ void rsel_group_rows(
+    const __nv_bfloat16* __restrict__ x, int cols, int64_t ldx, int64_t r0, int64_t r1,
+    int64_t rreal, const uint8_t* scales, int layout, const int32_t* sg, int k, int kpad,
+    float* rs, uint8_t* __restrict__ rcodes, uint8_t* __restrict__ rscales, int rlayout,
+    float* rst_g, const float* td, const float* tr, float* red) {
   const int ncols16 = cols >> 4, rcols16 = kpad >> 4;
   const int vpr = kpad >> 3;   // 8-element vectors per residual row (even)
-  if ((int)blockIdx.x >= G) {
-    // rows past the last offset: zero codes and scales
-    const int64_t end = goff[G];
-    const int64_t total = (rows - end) * vpr;
-    for (int64_t i = (int64_t)(blockIdx.x - G) * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)(gridDim.x - G) * blockDim.x) {
-      const int64_t r = end + i / vpr;
-      const int col = (int)(i % vpr) * 8;
-      *reinterpret_cast<uint32_t*>(rcodes + r * (kpad >> 1) + (col >> 1)) = 0u;
-      if (((col >> 3) & 1) == 0) rscales[sf_offset(rlayout, r, col >> 4, rcols16)] = 0;
-    }
-    return;
-  }
-  const int g = blockIdx.x;
-  const int64_t r0 = goff[g], r1 = goff[g + 1];
-  const int32_t* sg = sel + (int64_t)g * k;
-  __shared__ float td[256], tr[256];
-  fill_scale_table(st[g], td, tr);
-  __syncthreads();
   const int total = (int)(r1 - r0) * k;
   float m = 0.0f;
   for (int i0 = threadIdx.x; i0 < total; i0 += 4 * blockDim.x) {
@@ -780,7 +782,7 @@ __global__ void __launch_bounds__(kRselGroupThreads) rsel_group_kernel(
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      xv[u] = __bfloat162float(x[r[u] * ldx + c[u]]);
+      xv[u] = r[u] < rreal ? __bfloat162float(x[r[u] * ldx + c[u]]) : 0.0f;
       sb[u] = scales[sf_offset(layout, r[u], c[u] >> 4, ncols16)];
     }
     float R[4];
@@ -804,7 +806,7 @@ __global__ void __launch_bounds__(kRselGroupThreads) rsel_group_kernel(
   }
   __syncthreads();
   const float rs_t = tensor_scale_from_amax(red[0]);
-  if (threadIdx.x == 0) rst[g] = rs_t;
+  if (threadIdx.x == 0) *rst_g = rs_t;
   const int64_t nvec = (r1 - r0) * vpr;
   // warp-uniform loop: lanes 2i / 2i+1 hold the two halves of one 16-block
   for (int64_t base = (threadIdx.x & ~31); base < nvec; base += blockDim.x) {
@@ -835,6 +837,209 @@ __global__ void __launch_bounds__(kRselGroupThreads) rsel_group_kernel(
       if (((col >> 3) & 1) == 0) rscales[sf_offset(rlayout, r, col >> 4, rcols16)] = (uint8_t)sbyte;
     }
   }
+}
+
+__global__ void __launch_bounds__(kRselGroupThreads) rsel_group_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
+    const int32_t* __restrict__ goff, int G, const uint8_t* __restrict__ scales, int layout,
+    const float* __restrict__ st, const int32_t* __restrict__ sel, int k, int kpad,
+    float* __restrict__ rs, uint8_t* __restrict__ rcodes, uint8_t* __restrict__ rscales,
+    int rlayout, float* __restrict__ rst) {
+  griddep_wait();
+  __shared__ float red[kRselGroupThreads / 32];
+  if ((int)blockIdx.x >= G) {
+    // rows past the last offset: zero codes and scales
+    rsel_zero_tail(rows, goff[G], kpad, rcodes, rscales, rlayout, (int)blockIdx.x - G,
+                   (int)gridDim.x - G);
+    return;
+  }
+  const int g = blockIdx.x;
+  const int64_t r0 = goff[g], r1 = goff[g + 1];
+  __shared__ float td[256], tr[256];
+  fill_scale_table(st[g], td, tr);
+  __syncthreads();
+  rsel_group_rows(x, cols, ldx, r0, r1, r1, scales, layout, sel + (int64_t)g * k, k, kpad, rs,
+                  rcodes, rscales, rlayout, rst + g, td, tr, red);
+}
+
+// ---------------------------------------------------------------- per-group quantize + select
+// One block per group (the MoE layer's h: one per expert) does the whole
+// activation side of that group -- RTN quantization of its rows with the
+// residual energies, the channel scores, the top-k selection, the residual
+// slice R[:, sel] and its second quantization.  Groups are independent, so
+// nothing waits on another block, the chunk partials never leave the block,
+// and R_sel's gather finds the group's rows in L2 right after they were read.
+// Phase 1 takes the group's 32-row chunks in order: thread t quantizes the
+// chunk's (row, 16-column block) items t and t + NT (the next chunk's rows
+// are loaded meanwhile) and parks each residual square in shared memory;
+// after a barrier thread c adds column c's 32 squares in row order from 0 and
+// adds that chunk partial to its running score -- the float32 sequence of the
+// score definition (chunk partials in ascending chunk order from 0).  Chunks
+// past the group's count are padding: zero codes and scales, and a partial
+// of 0, which leaves the score as it is.  Phase 2 is the block top-k of the
+// other select paths, phase 3 the per-group R_sel of rsel_group_kernel.
+constexpr int kQsgThreads = 1024;
+constexpr int kQsgMaxCols = 1024;   // one channel per thread; 32 x cols floats of shared memory
+__global__ void __launch_bounds__(kQsgThreads, 1) quantize_select_groups_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
+    const int32_t* __restrict__ goff, int G, const int32_t* __restrict__ gcnt,
+    const float* __restrict__ st_in, const float* __restrict__ amax_in, uint8_t* codes,
+    int64_t ldc, uint8_t* scales, int layout, float* __restrict__ st_out, int k, int kpad,
+    int32_t* __restrict__ sel, float* __restrict__ scores_out, float* rs,
+    uint8_t* __restrict__ rcodes, uint8_t* __restrict__ rscales, int rlayout,
+    float* __restrict__ rst) {
+  griddep_wait();
+  // residual squares of one chunk, [32][cols]: the four 4-column quarters of a
+  // 16-block at quarter q ^ ((block >> 1) & 3), so that the eight lanes of a
+  // 16-byte store phase and the 32 lanes of a column read hit distinct banks
+  extern __shared__ __align__(16) float sq[];
+  __shared__ int hist[4 * 256];
+  __shared__ int warp_tot[kQsgThreads / 32];
+  __shared__ int dn[2];
+  __shared__ int32_t s_sel[kQsgMaxCols];
+  __shared__ float td[256], tr[256], red[kQsgThreads / 32];
+  if ((int)blockIdx.x >= G) {
+    // rows past the last offset: zero R_sel codes and scales
+    rsel_zero_tail(rows, goff[G], kpad, rcodes, rscales, rlayout, (int)blockIdx.x - G,
+                   (int)gridDim.x - G);
+    return;
+  }
+  const int g = blockIdx.x;
+  const int64_t r0 = goff[g], r1 = goff[g + 1];
+  if (!QDBG(r0 >= 0 && r1 >= r0 && r1 <= rows)) return;
+  // chunks are the score definition's 32-row chunks only when groups start
+  // at multiples of 32
+  if (threadIdx.x == 0 && r0 % kScoreChunk) atomicExch(&g_quant_error, QUADS_ERR_DEVICE_CHECK);
+  // rows at or past rr are zero rows: not read
+  const int64_t rr = gcnt ? r0 + min(max((int64_t)gcnt[g], (int64_t)0), r1 - r0) : r1;
+  const int ncols16 = cols >> 4;
+
+  // ---- tensor scale: given, from the given amax, or from the group's own amax
+  float s_t;
+  if (st_in) {
+    s_t = st_in[g];
+  } else if (amax_in) {
+    s_t = tensor_scale_from_amax(amax_in[g]);
+  } else {
+    const int vpr = cols >> 3;
+    const int64_t nv = (rr - r0) * vpr;
+    __nv_bfloat162 m2 = __floats2bfloat162_rn(0.0f, 0.0f);
+    for (int64_t i = threadIdx.x; i < nv; i += blockDim.x) {
+      const int64_t rl = i / vpr;
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(x + (r0 + rl) * ldx) + (i - rl * vpr));
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[j])));
+    }
+    const float2 mf = __bfloat1622float2(m2);
+    const float m = warp_max(fmaxf(mf.x, mf.y));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    float v = 0.0f;
+#pragma unroll 1
+    for (int j = 0; j < (int)(blockDim.x >> 5); ++j) v = fmaxf(v, red[j]);
+    s_t = tensor_scale_from_amax(v);
+    __syncthreads();   // red is reused below
+  }
+  if (threadIdx.x == 0) st_out[g] = s_t;
+
+  // ---- phase 1: quantization and channel scores
+  const int items = kScoreChunk * ncols16;   // (row, block) items per chunk, <= 2 * kQsgThreads
+  const int64_t nch = (r1 - r0 + kScoreChunk - 1) / kScoreChunk;
+  const int64_t nreal = (rr - r0 + kScoreChunk - 1) / kScoreChunk;   // chunks holding real rows
+  auto load_chunk = [&](int64_t ch, uint4 (&raw)[2][2]) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
+      const int it = (int)threadIdx.x + u * kQsgThreads;
+      if (ch < nreal && it < items) {
+        const int64_t row = r0 + ch * kScoreChunk + it / ncols16;
+        if (row < rr) {
+          const uint4* px = reinterpret_cast<const uint4*>(x + row * ldx + (it % ncols16) * 16);
+          raw[u][0] = __ldg(px);
+          raw[u][1] = __ldg(px + 1);
+        }
+      }
+    }
+  };
+  float score = 0.0f;   // channel threadIdx.x
+  uint4 nxt[2][2];
+  load_chunk(0, nxt);
+#pragma unroll 1
+  for (int64_t ch = 0; ch < nreal; ++ch) {
+    uint4 raw[2][2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) { raw[u][0] = nxt[u][0]; raw[u][1] = nxt[u][1]; }
+    load_chunk(ch + 1, nxt);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int it = (int)threadIdx.x + u * kQsgThreads;
+      if (it >= items) continue;
+      const int rl = it / ncols16, cb = it - rl * ncols16;
+      const int64_t row = r0 + ch * kScoreChunk + rl;
+      float f[16];
+      BlockScale bs;
+      uint2 c;
+      // rows past rr were loaded as zeros: codes, scale byte and R are 0
+      quantize_block16(raw[u][0], raw[u][1], s_t, f, bs, c);
+      if (row < r1) {
+        uint32_t* pc = reinterpret_cast<uint32_t*>(codes + row * ldc + cb * 8);
+        pc[0] = c.x;
+        pc[1] = c.y;
+        scales[sf_offset(layout, row, cb, ncols16)] = (uint8_t)bs.byte;
+      }
+      float lv[16];
+      e2m1x8_to_f32(c.x, lv);
+      e2m1x8_to_f32(c.y, lv + 8);
+      float4* ps = reinterpret_cast<float4*>(sq + rl * cols + cb * 16);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float R = __fsub_rn(f[4 * q + j], __fmul_rn(lv[4 * q + j], bs.d));
+          v[j] = __fmul_rn(R, R);
+        }
+        ps[q ^ ((cb >> 1) & 3)] = make_float4(v[0], v[1], v[2], v[3]);
+      }
+    }
+    __syncthreads();
+    if ((int)threadIdx.x < cols) {
+      const int c = threadIdx.x, cb = c >> 4;
+      const int pc = (c & ~15) | ((((c >> 2) & 3) ^ ((cb >> 1) & 3)) << 2) | (c & 3);
+      float acc = 0.0f;
+#pragma unroll 8
+      for (int r = 0; r < kScoreChunk; ++r) acc = __fadd_rn(acc, sq[r * cols + pc]);
+      score = __fadd_rn(score, acc);
+    }
+    __syncthreads();
+  }
+  // padding chunks: the outputs of zero rows
+  for (int64_t i = threadIdx.x; i < (nch - nreal) * items; i += blockDim.x) {
+    const int64_t ch = nreal + i / items;
+    const int it = (int)(i % items);
+    const int rl = it / ncols16, cb = it - rl * ncols16;
+    const int64_t row = r0 + ch * kScoreChunk + rl;
+    if (row >= r1) continue;
+    uint32_t* pc = reinterpret_cast<uint32_t*>(codes + row * ldc + cb * 8);
+    pc[0] = 0u;
+    pc[1] = 0u;
+    scales[sf_offset(layout, row, cb, ncols16)] = 0;
+  }
+  if (scores_out && (int)threadIdx.x < cols) scores_out[(int64_t)g * cols + threadIdx.x] = score;
+
+  // ---- phase 2: top-k channels of the group (ascending)
+  {
+    const uint32_t key[1] = {(int)threadIdx.x < cols ? __float_as_uint(score) : 0u};
+    block_topk<kQsgThreads, 1>(key, cols, k, s_sel, hist, warp_tot, dn);
+  }
+  // ---- phase 3: R[:, sel] and its second quantization
+  fill_scale_table(s_t, td, tr);
+  __syncthreads();   // s_sel, the table, and this block's code and scale stores are visible
+  for (int j = threadIdx.x; j < k; j += blockDim.x) sel[(int64_t)g * k + j] = s_sel[j];
+  rsel_group_rows(x, cols, ldx, r0, r1, rr, scales, layout, s_sel, k, kpad, rs, rcodes, rscales,
+                  rlayout, rst + g, td, tr, red);
 }
 
 // Quantize the float32 residual slice [rows, k] (16-blocks along the selection)
@@ -1570,8 +1775,10 @@ static quads_status_t quantize_impl(
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
         codes, ld_codes, scales, scale_layout, nullptr, qdq, ldq, group_counts);
   else if (score_partials && ((rows + 31) / 32) * (cols / 16) >= (int64_t)num_sms() * 512 &&
-           ((rows + 31) / 32) * (cols / 16) < (1ll << 31))
+           ((rows + 31) / 32) * (cols / 16) < (1ll << 31) && ld_codes % 8 == 0)
     // enough (chunk, block) pairs for a thread each: about two blocks per SM
+    // (its 8-byte code stores need ld_codes % 8 == 0; the 32x256-task kernel
+    // stores 4 bytes at a time)
     launch_dep(quantize_chunk_kernel, grid_for(((rows + 31) / 32) * (cols / 16), 256, 3), 256, 0, st,
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
         codes, ld_codes, scales, scale_layout, score_partials, group_counts);
@@ -1782,6 +1989,71 @@ extern "C" quads_status_t quads_quantize_select_nvfp4(
     return fail(QUADS_ERR_CUDA, "quantize_select: cooperative launch: %s", cudaGetErrorString(e));
   }
   return check_launch("quantize_select", 1);
+}
+
+extern "C" quads_status_t quads_quantize_select_groups_nvfp4(
+    const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* group_offsets,
+    int32_t num_groups, const int32_t* group_counts, const float* tensor_scale_in,
+    const float* tensor_amax_in, int32_t k, uint8_t* codes, int64_t ld_codes, uint8_t* scales,
+    int32_t scale_layout, float* tensor_scale_out, int32_t* sel, float* scores_out,
+    uint8_t* r_codes, uint8_t* r_scales, int32_t r_scale_layout, float* r_tensor_scale,
+    void* workspace, size_t workspace_bytes, void* sel_ready_event, void* stream) {
+  if (rows > 0 && (!x || !group_offsets || !codes || !scales || !tensor_scale_out || !sel ||
+                   !r_codes || !r_scales || !r_tensor_scale))
+    return fail(QUADS_ERR_INVALID_ARG, "quantize_select_groups: null pointer argument");
+  if (rows < 0 || cols < 16 || cols % 16 || cols > kQsgMaxCols)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "quantize_select_groups: cols=%lld must be a multiple of 16 in [16, %d]", (long long)cols, kQsgMaxCols);
+  if (k <= 0 || k % 16 || k > cols)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "quantize_select_groups: k=%d must be a multiple of 16 in [16, cols]", k);
+  if (num_groups < 1) return fail(QUADS_ERR_INVALID_ARG, "quantize_select_groups: num_groups < 1");
+  if (tensor_scale_in && tensor_amax_in)
+    return fail(QUADS_ERR_INVALID_ARG, "quantize_select_groups: give tensor_scale_in or tensor_amax_in, not both");
+  if ((scale_layout != QUADS_SCALES_LINEAR && scale_layout != QUADS_SCALES_TCGEN05) ||
+      (r_scale_layout != QUADS_SCALES_LINEAR && r_scale_layout != QUADS_SCALES_TCGEN05))
+    return fail(QUADS_ERR_INVALID_ARG, "quantize_select_groups: bad scale layout");
+  if (scale_layout == QUADS_SCALES_TCGEN05 && cols % 64)
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "quantize_select_groups: TCGEN05 scale layout needs cols %% 64 == 0");
+  if (rows * (int64_t)k >= (1ll << 31))
+    return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "quantize_select_groups: rows * k must be below 2^31");
+  if (ldx < cols || ldx % 8 || ld_codes < cols / 2 || ld_codes % 4 || !aligned16(x) ||
+      !aligned16(codes))
+    return fail(QUADS_ERR_MISALIGNED, "quantize_select_groups: x and codes 16-byte aligned, ldx >= cols (%% 8), ld_codes >= cols/2 (%% 4)");
+  const size_t need = quads_workspace_size(QUADS_OP_QUANTIZE_SELECT_GROUPS, rows, cols, 0, k,
+                                           num_groups);
+  if (rows > 0 && (!workspace || workspace_bytes < need))
+    return fail(QUADS_ERR_WORKSPACE, "quantize_select_groups: workspace needs %zu bytes", need);
+  cudaStream_t st = (cudaStream_t)stream;
+  auto sel_ready = [&]() -> quads_status_t {
+    if (!sel_ready_event) return QUADS_OK;
+    const cudaError_t e = cudaEventRecord((cudaEvent_t)sel_ready_event, st);
+    return e == cudaSuccess ? QUADS_OK
+                            : fail(QUADS_ERR_CUDA, "quantize_select_groups: cudaEventRecord: %s", cudaGetErrorString(e));
+  };
+  if (rows == 0) return sel_ready();
+  const int kpad = quads_kpad(k);
+  // the parts of the TCGEN05 scale arrays past the last full 128-row block
+  // that no row covers read as zero
+  if (scale_layout == QUADS_SCALES_TCGEN05 && rows % 128) {
+    const int64_t start = (rows / 128) * (cols / 64) * 512;
+    cudaMemsetAsync(scales + start, 0, (size_t)(sf_tc_bytes(rows, cols) - start), st);
+  }
+  if (r_scale_layout == QUADS_SCALES_TCGEN05 && rows % 128) {
+    const int64_t start = (rows / 128) * (kpad / 64) * 512;
+    cudaMemsetAsync(r_scales + start, 0, (size_t)(sf_tc_bytes(rows, kpad) - start), st);
+  }
+  const size_t smem = (size_t)kScoreChunk * cols * 4;
+  cudaError_t e = cudaFuncSetAttribute(quantize_select_groups_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess)
+    return fail(QUADS_ERR_CUDA, "quantize_select_groups: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+  // one block per group, plus blocks that zero the R_sel rows past the last group
+  launch_dep(quantize_select_groups_kernel, num_groups + 32, kQsgThreads, smem, st,
+      (const __nv_bfloat16*)x, rows, (int)cols, ldx, group_offsets, (int)num_groups, group_counts,
+      tensor_scale_in, tensor_amax_in, codes, ld_codes, scales, (int)scale_layout,
+      tensor_scale_out, (int)k, kpad, sel, scores_out, (float*)workspace, r_codes, r_scales,
+      (int)r_scale_layout, r_tensor_scale);
+  if (quads_status_t s = check_launch("quantize_select_groups", 1)) return s;
+  return sel_ready();
 }
 
 extern "C" quads_status_t quads_trace_round(const void* x_train, int64_t rows, int64_t cols,

@@ -12,6 +12,8 @@ Side)"; [TRACE digest] "MoE 专家路由敏感性".
 """
 from __future__ import annotations
 
+from typing import Optional
+
 import torch
 
 from . import quads as Q
@@ -85,17 +87,29 @@ class MoEExpertLayer:
     residual compensation on both GEMMs."""
 
     def __init__(self, w1: torch.Tensor, w2: torch.Tensor, topk: int, k1: int, k2: int,
-                 max_tokens: int, compensate: bool = True, fused_activation_side: bool = False):
+                 max_tokens: int, compensate: bool = True, fused_activation_side: bool = False,
+                 fused_expert_side: Optional[bool] = None):
         """fused_activation_side: GEMM1's activation side (quantization,
         selection, R_sel) as one cooperative launch (quantize_select_nvfp4)
         instead of the quantizer and the selection call.  Off by default: the
         cooperative grid holds every SM while it runs, so the routing on the
-        side stream cannot overlap it."""
+        side stream cannot overlap it.
+        fused_expert_side: GEMM2's activation side (h's per-expert
+        quantization, selection and R_sel) as one launch with a block per
+        expert (quantize_select_groups_nvfp4) instead of the quantizer and the
+        selection call; the same outputs bit for bit.  None (default): used
+        when the experts average at most 128 rows (decode-sized batches,
+        where it saves launches); with more rows per expert, one block per
+        expert quantizes slower than the quantizer spread over every SM, and
+        Q(W_sel) could no longer overlap R_sel."""
         self.E, twoF, self.H = w1.shape
         self.F = twoF // 2
         assert w2.shape == (self.E, self.H, self.F)
         self.topk, self.k1, self.k2, self.compensate = topk, k1, k2, compensate
         self.fused = fused_activation_side
+        if fused_expert_side is None:
+            fused_expert_side = max_tokens * topk <= 128 * w1.shape[0]
+        self.fused_h = fused_expert_side
         dev = w1.device
         self.w1q = Q.quantize_expert_weights(w1, swiglu_interleave=True)
         self.w2q = Q.quantize_expert_weights(w2)
@@ -133,6 +147,7 @@ class MoEExpertLayer:
             qs1=e(Q.workspace_size(Q.OP_QUANTIZE_SELECT, T, H, 0, k1) if fused_activation_side else 16),
             q2=e(Q.workspace_size(Q.OP_QUANTIZE, cap, F, 0, 0, E)),
             s2=e(Q.workspace_size(Q.OP_SELECT, cap, F, 0, k2, E)),
+            qs2=e(Q.workspace_size(Q.OP_QUANTIZE_SELECT_GROUPS, cap, F, 0, k2, E)),
         )
         # Work that does not wait on its neighbours runs on two side streams,
         # forked and joined by events (so this also holds inside a captured
@@ -195,19 +210,29 @@ class MoEExpertLayer:
                                epilogue=Q.EPI_SWIGLU, y_amax=b["hamax"], w_sel=w1sel,
                                out=b["h"], stream=stream)
         # h's padding rows (past each expert's count) are zero: not read
-        hq, hpart = Q.quantize_nvfp4(h, group_offsets=plan["offsets"], num_groups=E,
-                                     group_counts=plan["counts"],
-                                     tensor_amax_in=b["hamax"], scale_layout=Q.TCGEN05,
-                                     scores=comp, rows=self.cap,
-                                     workspace=ws["q2"], stream=stream,
-                                     out=(b["hc"], b["hs"], b["hts"], b["hpart"] if comp else None))
         r2 = sel2 = w2sel = None
-        if comp:
+        if comp and self.fused_h:
+            # one block per expert: h's quantization, channel scores, top-k
+            # and the second quantization of R_sel
+            hq, sel2, _, r2 = Q.quantize_select_groups_nvfp4(
+                h, self.k2, plan["offsets"], E, group_counts=plan["counts"],
+                tensor_amax_in=b["hamax"], scale_layout=Q.TCGEN05, r_scale_layout=Q.TCGEN05,
+                rows=self.cap, sel_ready_event=self.ev_sel2, workspace=ws["qs2"], stream=stream,
+                out=(b["hc"], b["hs"], b["hts"], b["sel2"], b["r2c"], b["r2s"], b["r2ts"]))
+        else:
+            hq, hpart = Q.quantize_nvfp4(h, group_offsets=plan["offsets"], num_groups=E,
+                                         group_counts=plan["counts"],
+                                         tensor_amax_in=b["hamax"], scale_layout=Q.TCGEN05,
+                                         scores=comp, rows=self.cap,
+                                         workspace=ws["q2"], stream=stream,
+                                         out=(b["hc"], b["hs"], b["hts"], b["hpart"] if comp else None))
+        if comp and not self.fused_h:
             sel2, _, r2 = Q.select_residual_channels(h, hq, hpart, self.k2,
                                                      group_offsets=plan["offsets"], num_groups=E,
                                                      r_scale_layout=Q.TCGEN05, workspace=ws["s2"],
                                                      sel_ready_event=self.ev_sel2, stream=stream,
                                                      out=(b["sel2"], b["r2c"], b["r2s"], b["r2ts"]))
+        if comp:
             self.wside.wait_event(self.ev_sel2)
             w2sel = Q.select_weight_channels(self.w2q, sel2, self.k2, E, sel_per_group=True,
                                              stream=self.wside, out=(b["w2sc"], b["w2ss"]))

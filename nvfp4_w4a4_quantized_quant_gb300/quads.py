@@ -21,6 +21,7 @@ LINEAR, TCGEN05 = 0, 1
 OUT_F32, OUT_BF16 = 0, 1
 EPI_NONE, EPI_SWIGLU = 0, 1
 OP_QUANTIZE, OP_SELECT, OP_GEMM, OP_MOE_GEMM, OP_MOE_ROUTE, OP_QUANTIZE_SELECT = 0, 1, 2, 3, 4, 5
+OP_QUANTIZE_SELECT_GROUPS = 6
 SCORE_CHUNK_ROWS = 32
 MOE_ROW_ALIGN = 128
 
@@ -47,6 +48,9 @@ _SIGS = {
                                                       _P, _I32, _P, _P, _P, _P, _I32, _P, _P]),
     "quads_quantize_select_nvfp4": (_I32, [_P, _I64, _I64, _I64, _I32, _P, _I64, _P, _I32, _P, _P,
                                            _P, _P, _P, _I32, _P, _P, _SZ, _P]),
+    "quads_quantize_select_groups_nvfp4": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _I32,
+                                                  _P, _I64, _P, _I32, _P, _P, _P, _P, _P, _I32, _P,
+                                                  _P, _SZ, _P, _P]),
     "quads_w4a4_gemm_comp": (_I32, [_I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                     _P, _P, _P, _P, _I32, _P, _I32, _I64, _P, _SZ, _P]),
     "quads_moe_grouped_gemm": (_I32, [_I32, _I64, _I64, _I64, _P, _P, _P, _P, _P, _I32, _P, _P,
@@ -296,6 +300,47 @@ def quantize_select_nvfp4(x: torch.Tensor, k: int, *, scale_layout: int = LINEAR
         _ptr(x), rows, cols, x.stride(0), k, _ptr(codes), codes.stride(0), _ptr(scales),
         scale_layout, _ptr(ts), _ptr(sel), _ptr(sc), _ptr(rc), _ptr(rs), r_scale_layout, _ptr(rts),
         _ptr(ws), ws.numel(), _stream(stream)), "quantize_select_nvfp4")
+    return (QTensor(codes, scales, ts, rows, cols, scale_layout), sel, sc,
+            QTensor(rc, rs, rts, rows, kp, r_scale_layout))
+
+
+def quantize_select_groups_nvfp4(x: torch.Tensor, k: int, group_offsets, num_groups: int, *,
+                                 group_counts=None, tensor_scale_in=None, tensor_amax_in=None,
+                                 scale_layout: int = LINEAR, r_scale_layout: int = LINEAR,
+                                 want_scores: bool = False, rows: Optional[int] = None,
+                                 sel_ready_event=None, workspace=None, out=None, stream=None):
+    """quantize_nvfp4 (row groups, score partials) and select_residual_channels
+    (per group) in one launch, one block per group.
+    -> (QTensor of Q(X), sel int32 [G, k], scores [G, cols] or None, QTensor of Q(R_sel)).
+    out = (codes, scales, tensor_scale [G], sel, r_codes, r_scales, r_tensor_scale [G])."""
+    lib = load()
+    assert x.dtype == torch.bfloat16 and x.dim() == 2
+    rows = x.shape[0] if rows is None else rows
+    cols = x.shape[1]
+    G = num_groups
+    kp = kpad(k)
+    dev = x.device
+    if out is None:
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+        nsf = sf_tc_bytes(rows, cols) if scale_layout == TCGEN05 else rows * (cols // 16)
+        scales = torch.empty(nsf, dtype=torch.uint8, device=dev)
+        ts = torch.empty(G, dtype=torch.float32, device=dev)
+        sel = torch.empty((G, k), dtype=torch.int32, device=dev)
+        rc = torch.empty((rows, kp // 2), dtype=torch.uint8, device=dev)
+        nrs = sf_tc_bytes(rows, kp) if r_scale_layout == TCGEN05 else rows * (kp // 16)
+        rs = torch.empty(nrs, dtype=torch.uint8, device=dev)
+        rts = torch.empty(G, dtype=torch.float32, device=dev)
+    else:
+        codes, scales, ts, sel, rc, rs, rts = out
+    sc = torch.empty((G, cols), dtype=torch.float32, device=dev) if want_scores else None
+    ws = _workspace(workspace_size(OP_QUANTIZE_SELECT_GROUPS, rows, cols, 0, k, G), dev, workspace,
+                    stream)
+    _check(lib.quads_quantize_select_groups_nvfp4(
+        _ptr(x), rows, cols, x.stride(0), _ptr(group_offsets), G, _ptr(group_counts),
+        _ptr(tensor_scale_in), _ptr(tensor_amax_in), k, _ptr(codes), codes.stride(0),
+        _ptr(scales), scale_layout, _ptr(ts), _ptr(sel), _ptr(sc), _ptr(rc), _ptr(rs),
+        r_scale_layout, _ptr(rts), _ptr(ws), ws.numel(), _event(sel_ready_event, stream),
+        _stream(stream)), "quantize_select_groups_nvfp4")
     return (QTensor(codes, scales, ts, rows, cols, scale_layout), sel, sc,
             QTensor(rc, rs, rts, rows, kp, r_scale_layout))
 

@@ -215,3 +215,30 @@ def test_moe_layer_fused_activation_side_gives_the_same_outputs(lib):
         res.append({k: r[k].clone() for k in ("out", "h", "y")} | {"sel1": r["sel1"].clone()})
     for k in res[0]:
         assert torch.equal(res[0][k], res[1][k]), k
+
+
+@pytest.mark.parametrize("tokens,experts", [(300, 4), (40, 16)])
+def test_moe_layer_fused_expert_side_gives_the_same_outputs(lib, tokens, experts):
+    """h's per-expert quantization and selection as one launch with a block
+    per expert gives the layer the same outputs, bit for bit, as the quantizer
+    and selection calls (three tiles per expert, and a few rows per expert)."""
+    from nvfp4_w4a4_quantized_quant_gb300.layer import MoEExpertLayer
+    d = inputs.moe_layer(3, tokens=tokens, hidden=512, experts=experts, topk=2, ffn=256, k=64)
+    E, twoF, H = d["w1"].shape
+    w1 = bf16_tensor(d["w1"].reshape(E * twoF, H)).reshape(E, twoF, H)
+    w2 = bf16_tensor(d["w2"].reshape(E * H, twoF // 2)).reshape(E, H, twoF // 2)
+    x, lg = bf16_tensor(d["x"]), torch.from_numpy(d["logits"]).cuda()
+    res = []
+    for fused in (False, True):
+        layer = MoEExpertLayer(w1, w2, d["topk"], 64, 64, tokens, fused_expert_side=fused)
+        r = layer.forward(x, lg)
+        torch.cuda.synchronize()
+        assert lib.device_status() == 0
+        used = int(r["plan"]["offsets"][-1])
+        res.append({"out": r["out"].clone(), "y": r["y"][:used].clone(), "sel2": r["sel2"].clone(),
+                    "hc": r["hq"].codes[:used].clone(),
+                    "hs": r["hq"].scales[: used * (twoF // 32)].clone(),
+                    "hts": r["hq"].tensor_scale.clone(), "r2c": r["r2"].codes.clone(),
+                    "r2s": r["r2"].scales.clone(), "r2ts": r["r2"].tensor_scale.clone()})
+    for k in res[0]:
+        assert torch.equal(res[0][k], res[1][k]), k

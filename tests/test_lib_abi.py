@@ -51,6 +51,15 @@ def test_host_side_argument_checks_need_no_gpu(lib):
     assert st == 1                                   # both tensor_scale_in and tensor_amax_in
     st = lib.quads_quantize_nvfp4(p, 8, 32, 32, None, None, 1, p, None, None, p, 16, p, 0, p, None, p, 64, None)
     assert st == 1 and "group_counts" in _err(lib)   # counts without group offsets
+    qsg = lambda rows, cols, ldx, k, ts, am, ws: lib.quads_quantize_select_groups_nvfp4(  # noqa: E731
+        p, rows, cols, ldx, p, 4, None, ts, am, k, p, cols // 2, p, 0, p, p, None, p, p, 0, p, p,
+        ws, None, None)
+    assert qsg(64, 2048, 2048, 64, None, None, 1 << 20) == 2   # cols > 1024 (one channel per thread)
+    assert qsg(64, 768, 768, 24, None, None, 1 << 20) == 2     # k % 16
+    assert qsg(64, 768, 768, 64, p, p, 1 << 20) == 1           # both tensor_scale_in and tensor_amax_in
+    assert qsg(64, 768, 512, 64, None, None, 1 << 20) == 3     # ldx < cols
+    assert qsg(64, 768, 768, 64, None, None, 16) == 7          # workspace below rows * k * 4
+    assert lib.quads_workspace_size(quads.OP_QUANTIZE_SELECT_GROUPS, 100, 768, 0, 64, 4) == 100 * 64 * 4
     st = lib.quads_w4a4_gemm_comp(64, 100, 256, p, p, p, p, p, p, None, None, None, None, None, None,
                                   None, None, 0, p, 0, 100, None, 0, None)
     assert st == 2 and "N%128" in _err(lib)
