@@ -1973,8 +1973,12 @@ extern "C" quads_status_t quads_quantize_select_nvfp4(
   at.id = cudaLaunchAttributeCooperative;
   at.val.cooperative = 1;
   // several small blocks per SM (the quantization phase needs the warps to
-  // hide its load latency), all resident at once
-  cfg.gridDim = dim3((unsigned)(num_sms() * std::min(per_sm, 4)), 1, 1);
+  // hide its load latency), all resident at once; no more blocks than
+  // 32x256 quantization tasks, so that a small input (a decode batch) leaves
+  // SMs to the work of other streams
+  const int64_t ntasks = ((rows + 31) / 32) * ((cols + 255) / 256);
+  const int64_t full = (int64_t)num_sms() * std::min(per_sm, 4);
+  cfg.gridDim = dim3((unsigned)std::max<int64_t>(1, std::min(full, ntasks)), 1, 1);
   cfg.blockDim = dim3(kFusedThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;

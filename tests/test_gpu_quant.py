@@ -487,10 +487,12 @@ def test_w4a16_qdq_full_expert_stack_sampled_experts(lib):
 
 
 @pytest.mark.parametrize("rows,cols,k,layout", [(8192, 2048, 64, 0), (4096, 2048, 128, 1),
-                                                (300, 256, 16, 0), (77, 512, 64, 1)])
+                                                (512, 2048, 64, 1), (300, 256, 16, 0),
+                                                (77, 512, 64, 1)])
 def test_fused_quantize_select_matches_the_two_calls(lib, rows, cols, k, layout):
     """The cooperative quantize + select kernel gives exactly the outputs of
-    quantize_nvfp4 (scores on) followed by select_residual_channels."""
+    quantize_nvfp4 (scores on) followed by select_residual_channels (grids of
+    every SM's blocks down to one block per 32x256 task: 128, 10 and 6)."""
     rng = inputs.make_rng(rows + cols + k)
     xf = inputs.student_t4(rng, (rows, cols))
     xf[:, rng.choice(cols, max(1, cols // 100), replace=False)] *= np.float32(20.0)
