@@ -757,15 +757,20 @@ __device__ __forceinline__ void rsel_zero_tail(int64_t rows, int64_t end, int kp
 // rreal are zero rows (not read; their R is 0).  td/tr: the block-scale table
 // of the group's tensor scale (filled, and a barrier passed, by the caller);
 // sg: the group's k selected channels; red: NT/32 floats of shared memory.
-// The group's R_sel tensor scale is stored to *rst_g.
+// The group's R_sel tensor scale is stored to *rst_g.  Optional on-chip
+// copies (shared memory, row r at r - r0) replace the global reads and the
+// workspace: xs the rows' bf16 values (row stride cols), ss their scale
+// bytes (row stride cols/16), rsm R itself (row stride k).
 __device__ __forceinline__ void rsel_group_rows(
     const __nv_bfloat16* __restrict__ x, int cols, int64_t ldx, int64_t r0, int64_t r1,
     int64_t rreal, const uint8_t* scales, int layout, const int32_t* sg, int k, int kpad,
     float* rs, uint8_t* __restrict__ rcodes, uint8_t* __restrict__ rscales, int rlayout,
-    float* rst_g, const float* td, const float* tr, float* red) {
+    float* rst_g, const float* td, const float* tr, float* red,
+    const __nv_bfloat16* xs = nullptr, const uint8_t* ss = nullptr, float* rsm = nullptr) {
   const int ncols16 = cols >> 4, rcols16 = kpad >> 4;
   const int vpr = kpad >> 3;   // 8-element vectors per residual row (even)
-  const int total = (int)(r1 - r0) * k;
+  // rows past rreal: R = 0, so only the real rows are gathered
+  const int total = (int)(rreal - r0) * k;
   float m = 0.0f;
   for (int i0 = threadIdx.x; i0 < total; i0 += 4 * blockDim.x) {
     int64_t r[4];
@@ -782,8 +787,14 @@ __device__ __forceinline__ void rsel_group_rows(
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      xv[u] = r[u] < rreal ? __bfloat162float(x[r[u] * ldx + c[u]]) : 0.0f;
-      sb[u] = scales[sf_offset(layout, r[u], c[u] >> 4, ncols16)];
+      if (xs) {
+        const int64_t rl = r[u] - r0;
+        xv[u] = __bfloat162float(xs[rl * cols + c[u]]);
+        sb[u] = ss[rl * ncols16 + (c[u] >> 4)];
+      } else {
+        xv[u] = __bfloat162float(x[r[u] * ldx + c[u]]);
+        sb[u] = scales[sf_offset(layout, r[u], c[u] >> 4, ncols16)];
+      }
     }
     float R[4];
     residual_pair(xv[0], xv[1], sb[0], sb[1], td, tr, R[0], R[1]);
@@ -792,7 +803,8 @@ __device__ __forceinline__ void rsel_group_rows(
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u * (int)blockDim.x;
       if (i >= total) continue;
-      rs[r[u] * k + j[u]] = R[u];
+      if (rsm) rsm[(r[u] - r0) * k + j[u]] = R[u];
+      else rs[r[u] * k + j[u]] = R[u];
       m = fmaxf(m, fabsf(R[u]));
     }
   }
@@ -814,12 +826,12 @@ __device__ __forceinline__ void rsel_group_rows(
     const bool in = i < nvec;
     const int64_t r = r0 + (in ? i / vpr : 0);
     const int col = in ? (int)(i % vpr) * 8 : 0;
-    const bool live = in && col < k;
+    const bool live = in && col < k && r < rreal;   // rows past rreal: R = 0
     float f[8];
 #pragma unroll
     for (int jj = 0; jj < 8; ++jj) f[jj] = 0.0f;
     if (live) {
-      const float4* p = reinterpret_cast<const float4*>(rs + r * k + col);
+      const float4* p = reinterpret_cast<const float4*>(rsm ? rsm + (r - r0) * k + col : rs + r * k + col);
       const float4 a = p[0], b = p[1];
       f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
       f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
@@ -877,7 +889,10 @@ __global__ void __launch_bounds__(kRselGroupThreads) rsel_group_kernel(
 // score definition (chunk partials in ascending chunk order from 0).  Chunks
 // past the group's count are padding: zero codes and scales, and a partial
 // of 0, which leaves the score as it is.  Phase 2 is the block top-k of the
-// other select paths, phase 3 the per-group R_sel of rsel_group_kernel.
+// other select paths, phase 3 the per-group R_sel of rsel_group_kernel.  A
+// group of at most stash_rows real rows (decode-sized) also keeps its rows
+// and their scale bytes in shared memory during phase 1, and R in the
+// squares' buffer during phase 3, so R_sel reads nothing from memory.
 constexpr int kQsgThreads = 1024;
 constexpr int kQsgMaxCols = 1024;   // one channel per thread; 32 x cols floats of shared memory
 __global__ void __launch_bounds__(kQsgThreads, 1) quantize_select_groups_kernel(
@@ -887,12 +902,15 @@ __global__ void __launch_bounds__(kQsgThreads, 1) quantize_select_groups_kernel(
     int64_t ldc, uint8_t* scales, int layout, float* __restrict__ st_out, int k, int kpad,
     int32_t* __restrict__ sel, float* __restrict__ scores_out, float* rs,
     uint8_t* __restrict__ rcodes, uint8_t* __restrict__ rscales, int rlayout,
-    float* __restrict__ rst) {
+    float* __restrict__ rst, int stash_rows) {
   griddep_wait();
   // residual squares of one chunk, [32][cols]: the four 4-column quarters of a
   // 16-block at quarter q ^ ((block >> 1) & 3), so that the eight lanes of a
-  // 16-byte store phase and the 32 lanes of a column read hit distinct banks
+  // 16-byte store phase and the 32 lanes of a column read hit distinct banks;
+  // then [stash_rows][cols] bf16 rows and [stash_rows][cols/16] scale bytes
   extern __shared__ __align__(16) float sq[];
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(sq + kScoreChunk * cols);
+  uint8_t* ss = reinterpret_cast<uint8_t*>(xs + (int64_t)stash_rows * cols);
   __shared__ int hist[4 * 256];
   __shared__ int warp_tot[kQsgThreads / 32];
   __shared__ int dn[2];
@@ -913,6 +931,7 @@ __global__ void __launch_bounds__(kQsgThreads, 1) quantize_select_groups_kernel(
   // rows at or past rr are zero rows: not read
   const int64_t rr = gcnt ? r0 + min(max((int64_t)gcnt[g], (int64_t)0), r1 - r0) : r1;
   const int ncols16 = cols >> 4;
+  const bool stash = rr - r0 <= stash_rows;
 
   // ---- tensor scale: given, from the given amax, or from the group's own amax
   float s_t;
@@ -989,6 +1008,12 @@ __global__ void __launch_bounds__(kQsgThreads, 1) quantize_select_groups_kernel(
         pc[1] = c.y;
         scales[sf_offset(layout, row, cb, ncols16)] = (uint8_t)bs.byte;
       }
+      if (stash && row < rr) {
+        uint4* px = reinterpret_cast<uint4*>(xs + (row - r0) * cols + cb * 16);
+        px[0] = raw[u][0];
+        px[1] = raw[u][1];
+        ss[(row - r0) * ncols16 + cb] = (uint8_t)bs.byte;
+      }
       float lv[16];
       e2m1x8_to_f32(c.x, lv);
       e2m1x8_to_f32(c.y, lv + 8);
@@ -1038,8 +1063,10 @@ __global__ void __launch_bounds__(kQsgThreads, 1) quantize_select_groups_kernel(
   fill_scale_table(s_t, td, tr);
   __syncthreads();   // s_sel, the table, and this block's code and scale stores are visible
   for (int j = threadIdx.x; j < k; j += blockDim.x) sel[(int64_t)g * k + j] = s_sel[j];
+  // R fits the squares' buffer when (real rows) * k <= 32 * cols
+  float* rsm = (rr - r0) * k <= (int64_t)kScoreChunk * cols ? sq : nullptr;
   rsel_group_rows(x, cols, ldx, r0, r1, rr, scales, layout, s_sel, k, kpad, rs, rcodes, rscales,
-                  rlayout, rst + g, td, tr, red);
+                  rlayout, rst + g, td, tr, red, stash ? xs : nullptr, stash ? ss : nullptr, rsm);
 }
 
 // Quantize the float32 residual slice [rows, k] (16-blocks along the selection)
@@ -2045,9 +2072,22 @@ extern "C" quads_status_t quads_quantize_select_groups_nvfp4(
     const int64_t start = (rows / 128) * (kpad / 64) * 512;
     cudaMemsetAsync(r_scales + start, 0, (size_t)(sf_tc_bytes(rows, kpad) - start), st);
   }
-  const size_t smem = (size_t)kScoreChunk * cols * 4;
-  cudaError_t e = cudaFuncSetAttribute(quantize_select_groups_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // shared memory: the chunk's squares, then as many rows (bf16 values and
+  // scale bytes) as fit what is left -- groups of up to that many real rows
+  // keep them on chip for R_sel
+  int dev = 0, optin = 0;
+  cudaGetDevice(&dev);
+  cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncAttributes fa = {};
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, quantize_select_groups_kernel);
+  if (e != cudaSuccess)
+    return fail(QUADS_ERR_CUDA, "quantize_select_groups: attribute query: %s", cudaGetErrorString(e));
+  const size_t sq_bytes = (size_t)kScoreChunk * cols * 4;
+  const int64_t left = (int64_t)optin - (int64_t)fa.sharedSizeBytes - (int64_t)sq_bytes - 1024;
+  const int stash_rows = (int)std::max<int64_t>(0, std::min<int64_t>(256, left / (cols * 2 + cols / 16)));
+  const size_t smem = sq_bytes + (size_t)stash_rows * (cols * 2 + cols / 16);
+  e = cudaFuncSetAttribute(quantize_select_groups_kernel,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess)
     return fail(QUADS_ERR_CUDA, "quantize_select_groups: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   // one block per group, plus blocks that zero the R_sel rows past the last group
@@ -2055,7 +2095,7 @@ extern "C" quads_status_t quads_quantize_select_groups_nvfp4(
       (const __nv_bfloat16*)x, rows, (int)cols, ldx, group_offsets, (int)num_groups, group_counts,
       tensor_scale_in, tensor_amax_in, codes, ld_codes, scales, (int)scale_layout,
       tensor_scale_out, (int)k, kpad, sel, scores_out, (float*)workspace, r_codes, r_scales,
-      (int)r_scale_layout, r_tensor_scale);
+      (int)r_scale_layout, r_tensor_scale, stash_rows);
   if (quads_status_t s = check_launch("quantize_select_groups", 1)) return s;
   return sel_ready();
 }
