@@ -819,13 +819,14 @@ __device__ __forceinline__ void rsel_group_rows(
   __syncthreads();
   const float rs_t = tensor_scale_from_amax(red[0]);
   if (threadIdx.x == 0) *rst_g = rs_t;
-  const int64_t nvec = (r1 - r0) * vpr;
+  const int nvec = (int)(r1 - r0) * vpr;   // < 2^31: rows * k is (host check)
   // warp-uniform loop: lanes 2i / 2i+1 hold the two halves of one 16-block
-  for (int64_t base = (threadIdx.x & ~31); base < nvec; base += blockDim.x) {
-    const int64_t i = base + (threadIdx.x & 31);
+  for (int base = (int)(threadIdx.x & ~31u); base < nvec; base += blockDim.x) {
+    const int i = base + (int)(threadIdx.x & 31);
     const bool in = i < nvec;
-    const int64_t r = r0 + (in ? i / vpr : 0);
-    const int col = in ? (int)(i % vpr) * 8 : 0;
+    const int rq = in ? i / vpr : 0;
+    const int64_t r = r0 + rq;
+    const int col = in ? (i - rq * vpr) * 8 : 0;
     const bool live = in && col < k && r < rreal;   // rows past rreal: R = 0
     float f[8];
 #pragma unroll
@@ -965,20 +966,24 @@ __global__ void __launch_bounds__(kQsgThreads, 1) quantize_select_groups_kernel(
 
   // ---- phase 1: quantization and channel scores
   const int items = kScoreChunk * ncols16;   // (row, block) items per chunk, <= 2 * kQsgThreads
-  const int64_t nch = (r1 - r0 + kScoreChunk - 1) / kScoreChunk;
   const int64_t nreal = (rr - r0 + kScoreChunk - 1) / kScoreChunk;   // chunks holding real rows
+  // this thread's two items of every chunk: row in the chunk and 16-block
+  int irl[2], icb[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int it = (int)threadIdx.x + u * kQsgThreads;
+    irl[u] = it < items ? it / ncols16 : kScoreChunk;   // kScoreChunk: no item
+    icb[u] = it < items ? it - irl[u] * ncols16 : 0;
+  }
   auto load_chunk = [&](int64_t ch, uint4 (&raw)[2][2]) {
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
-      const int it = (int)threadIdx.x + u * kQsgThreads;
-      if (ch < nreal && it < items) {
-        const int64_t row = r0 + ch * kScoreChunk + it / ncols16;
-        if (row < rr) {
-          const uint4* px = reinterpret_cast<const uint4*>(x + row * ldx + (it % ncols16) * 16);
-          raw[u][0] = __ldg(px);
-          raw[u][1] = __ldg(px + 1);
-        }
+      const int64_t row = r0 + ch * kScoreChunk + irl[u];
+      if (ch < nreal && irl[u] < kScoreChunk && row < rr) {
+        const uint4* px = reinterpret_cast<const uint4*>(x + row * ldx + icb[u] * 16);
+        raw[u][0] = __ldg(px);
+        raw[u][1] = __ldg(px + 1);
       }
     }
   };
@@ -993,9 +998,8 @@ __global__ void __launch_bounds__(kQsgThreads, 1) quantize_select_groups_kernel(
     load_chunk(ch + 1, nxt);
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      const int it = (int)threadIdx.x + u * kQsgThreads;
-      if (it >= items) continue;
-      const int rl = it / ncols16, cb = it - rl * ncols16;
+      if (irl[u] >= kScoreChunk) continue;
+      const int rl = irl[u], cb = icb[u];
       const int64_t row = r0 + ch * kScoreChunk + rl;
       float f[16];
       BlockScale bs;
@@ -1040,17 +1044,18 @@ __global__ void __launch_bounds__(kQsgThreads, 1) quantize_select_groups_kernel(
     }
     __syncthreads();
   }
-  // padding chunks: the outputs of zero rows
-  for (int64_t i = threadIdx.x; i < (nch - nreal) * items; i += blockDim.x) {
-    const int64_t ch = nreal + i / items;
-    const int it = (int)(i % items);
-    const int rl = it / ncols16, cb = it - rl * ncols16;
-    const int64_t row = r0 + ch * kScoreChunk + rl;
-    if (row >= r1) continue;
-    uint32_t* pc = reinterpret_cast<uint32_t*>(codes + row * ldc + cb * 8);
-    pc[0] = 0u;
-    pc[1] = 0u;
-    scales[sf_offset(layout, row, cb, ncols16)] = 0;
+  // padding chunks: the outputs of zero rows (a warp per row, lanes over its 16-blocks)
+  {
+    const int64_t p0 = r0 + nreal * kScoreChunk;
+    const int nw = (int)(blockDim.x >> 5), lane = (int)(threadIdx.x & 31);
+    for (int64_t row = p0 + (threadIdx.x >> 5); row < r1; row += nw) {
+      for (int cb = lane; cb < ncols16; cb += 32) {
+        uint32_t* pc = reinterpret_cast<uint32_t*>(codes + row * ldc + cb * 8);
+        pc[0] = 0u;
+        pc[1] = 0u;
+        scales[sf_offset(layout, row, cb, ncols16)] = 0;
+      }
+    }
   }
   if (scores_out && (int)threadIdx.x < cols) scores_out[(int64_t)g * cols + threadIdx.x] = score;
 
