@@ -267,8 +267,11 @@ quads_status_t quads_qdq_nvfp4(const void* x, int64_t rows, int64_t cols, int64_
  * top channels by residual magnitude; here the mask is stored as the sorted
  * index list).
  *
- *   x, rows, cols, ldx, group_offsets, num_groups: as for the quantizer call
- *                  that produced `scales`, `tensor_scale` and `score_partials`.
+ *   x, rows, cols, ldx, group_offsets, num_groups, group_counts: as for the
+ *                  quantizer call that produced `scales`, `tensor_scale` and
+ *                  `score_partials` (group_counts nullable, needs group_offsets:
+ *                  rows of group g at or past offsets[g] + counts[g] are zero
+ *                  rows, not read, and their R is 0).
  *   k              1..cols, multiple of 16.
  *   sel            device int32 [num_groups, k].
  *   scores_out     nullable device float [num_groups, cols].
@@ -288,10 +291,11 @@ quads_status_t quads_qdq_nvfp4(const void* x, int64_t rows, int64_t cols, int64_
  */
 quads_status_t quads_select_residual_channels(
     const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* group_offsets,
-    int32_t num_groups, const uint8_t* scales, int32_t scale_layout, const float* tensor_scale,
-    const float* score_partials, int32_t k, int32_t* sel, float* scores_out, uint8_t* r_codes,
-    uint8_t* r_scales, int32_t r_scale_layout, float* r_tensor_scale, void* workspace,
-    size_t workspace_bytes, void* sel_ready_event, void* stream);
+    int32_t num_groups, const int32_t* group_counts, const uint8_t* scales, int32_t scale_layout,
+    const float* tensor_scale, const float* score_partials, int32_t k, int32_t* sel,
+    float* scores_out, uint8_t* r_codes, uint8_t* r_scales, int32_t r_scale_layout,
+    float* r_tensor_scale, void* workspace, size_t workspace_bytes, void* sel_ready_event,
+    void* stream);
 
 /*
  * quads_select_residual_channels_noalloc -- the same computation and outputs as
@@ -326,9 +330,10 @@ quads_status_t quads_select_residual_channels(
 #define QUADS_NOALLOC_SELECT_SCRATCH_BYTES (32u << 20)
 quads_status_t quads_select_residual_channels_noalloc(
     const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* group_offsets,
-    int32_t num_groups, const uint8_t* scales, int32_t scale_layout, const float* tensor_scale,
-    const float* score_partials, int32_t k, int32_t* sel, float* scores_out, uint8_t* r_codes,
-    uint8_t* r_scales, int32_t r_scale_layout, float* r_tensor_scale, void* stream);
+    int32_t num_groups, const int32_t* group_counts, const uint8_t* scales, int32_t scale_layout,
+    const float* tensor_scale, const float* score_partials, int32_t k, int32_t* sel,
+    float* scores_out, uint8_t* r_codes, uint8_t* r_scales, int32_t r_scale_layout,
+    float* r_tensor_scale, void* stream);
 
 /*
  * quads_quantize_select_nvfp4 -- quads_quantize_nvfp4 (one group, tensor

@@ -27,7 +27,7 @@ quads_status_t check_launch(const char* what, int kernels_launched);
 int num_sms();
 quads_status_t select_check_args(const void* x, int64_t rows, int64_t cols, int64_t ldx,
                                  const int32_t* group_offsets, int32_t num_groups,
-                                 const uint8_t* scales, const float* tensor_scale,
+                                 const int32_t* group_counts, const uint8_t* scales, const float* tensor_scale,
                                  const float* score_partials, int32_t k, const int32_t* sel,
                                  const uint8_t* r_codes, const uint8_t* r_scales,
                                  const float* r_tensor_scale, size_t* need);

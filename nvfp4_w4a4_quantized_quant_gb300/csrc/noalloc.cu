@@ -49,14 +49,15 @@ using namespace quads;
 
 extern "C" quads_status_t quads_select_residual_channels_noalloc(
     const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* group_offsets,
-    int32_t num_groups, const uint8_t* scales, int32_t scale_layout, const float* tensor_scale,
-    const float* score_partials, int32_t k, int32_t* sel, float* scores_out, uint8_t* r_codes,
-    uint8_t* r_scales, int32_t r_scale_layout, float* r_tensor_scale, void* stream) {
+    int32_t num_groups, const int32_t* group_counts, const uint8_t* scales, int32_t scale_layout,
+    const float* tensor_scale, const float* score_partials, int32_t k, int32_t* sel,
+    float* scores_out, uint8_t* r_codes, uint8_t* r_scales, int32_t r_scale_layout,
+    float* r_tensor_scale, void* stream) {
   // the same argument checks, in the same order, as the workspace entry point
   size_t need = 0;
-  if (quads_status_t s = select_check_args(x, rows, cols, ldx, group_offsets, num_groups, scales,
-                                           tensor_scale, score_partials, k, sel, r_codes,
-                                           r_scales, r_tensor_scale, &need))
+  if (quads_status_t s = select_check_args(x, rows, cols, ldx, group_offsets, num_groups,
+                                           group_counts, scales, tensor_scale, score_partials, k,
+                                           sel, r_codes, r_scales, r_tensor_scale, &need))
     return s;
   if (rows > 0 && need > (size_t)QUADS_NOALLOC_SELECT_SCRATCH_BYTES)
     return fail(QUADS_ERR_WORKSPACE,
@@ -70,8 +71,9 @@ extern "C" quads_status_t quads_select_residual_channels_noalloc(
   if (!scratch)
     return fail(QUADS_ERR_CUDA, "select_noalloc: cudaGetSymbolAddress failed: %s",
                 cudaGetErrorString(e));
-  return quads_select_residual_channels(x, rows, cols, ldx, group_offsets, num_groups, scales,
-                                        scale_layout, tensor_scale, score_partials, k, sel,
+  return quads_select_residual_channels(x, rows, cols, ldx, group_offsets, num_groups,
+                                        group_counts, scales, scale_layout, tensor_scale,
+                                        score_partials, k, sel,
                                         scores_out, r_codes, r_scales, r_scale_layout,
                                         r_tensor_scale, scratch,
                                         (size_t)QUADS_NOALLOC_SELECT_SCRATCH_BYTES, nullptr,

@@ -664,7 +664,8 @@ __device__ __forceinline__ void residual_pair(float xa, float xb, uint32_t sa, u
 // |R| by atomicMax on the float bits.
 __global__ void __launch_bounds__(256) rsel_residual_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
-    const int32_t* __restrict__ goff, int G, const uint8_t* __restrict__ scales, int layout,
+    const int32_t* __restrict__ goff, int G, const int32_t* __restrict__ gcnt,
+    const uint8_t* __restrict__ scales, int layout,
     const float* __restrict__ st, const int32_t* __restrict__ sel, int k,
     float* __restrict__ rs, uint32_t* __restrict__ amax_bits, int rb) {
   griddep_wait();
@@ -684,6 +685,8 @@ __global__ void __launch_bounds__(256) rsel_residual_kernel(
       tab_g = g;
     }
     const int32_t* sg = sel + (int64_t)g * k;
+    // rows of the slice past its group's count (gcnt) are zero rows: not read
+    const int64_t rr = gcnt ? max(r0, min(r1, (int64_t)goff[g] + gcnt[g])) : r1;
     float m = 0.0f;
     const int total = (int)(r1 - r0) * k;
     for (int i0 = threadIdx.x; i0 < total; i0 += 4 * blockDim.x) {
@@ -701,8 +704,9 @@ __global__ void __launch_bounds__(256) rsel_residual_kernel(
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        xv[u] = __bfloat162float(x[r[u] * ldx + c[u]]);
-        sb[u] = scales[sf_offset(layout, r[u], c[u] >> 4, ncols16)];
+        const bool real = r[u] < rr;   // a zero row: x = 0 and scale byte 0, so R = 0
+        xv[u] = real ? __bfloat162float(x[r[u] * ldx + c[u]]) : 0.0f;
+        sb[u] = real ? scales[sf_offset(layout, r[u], c[u] >> 4, ncols16)] : 0u;
       }
       float R[4];
       residual_pair(xv[0], xv[1], sb[0], sb[1], td, tr, R[0], R[1]);
@@ -865,7 +869,8 @@ __device__ __forceinline__ void rsel_group_rows(
 
 __global__ void __launch_bounds__(kRselGroupThreads) rsel_group_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
-    const int32_t* __restrict__ goff, int G, const uint8_t* __restrict__ scales, int layout,
+    const int32_t* __restrict__ goff, int G, const int32_t* __restrict__ gcnt,
+    const uint8_t* __restrict__ scales, int layout,
     const float* __restrict__ st, const int32_t* __restrict__ sel, int k, int kpad,
     float* __restrict__ rs, uint8_t* __restrict__ rcodes, uint8_t* __restrict__ rscales,
     int rlayout, float* __restrict__ rst) {
@@ -882,7 +887,9 @@ __global__ void __launch_bounds__(kRselGroupThreads) rsel_group_kernel(
   __shared__ float td[256], tr[256];
   fill_scale_table(st[g], td, tr);
   __syncthreads();
-  rsel_group_rows(x, cols, ldx, r0, r1, r1, scales, layout, sel + (int64_t)g * k, k, kpad, rs,
+  // rows past the group's count (gcnt) are zero rows: not read
+  const int64_t rr = gcnt ? r0 + min(max((int64_t)gcnt[g], (int64_t)0), r1 - r0) : r1;
+  rsel_group_rows(x, cols, ldx, r0, r1, rr, scales, layout, sel + (int64_t)g * k, k, kpad, rs,
                   rcodes, rscales, rlayout, rst + g, td, tr, red);
 }
 
@@ -1867,6 +1874,7 @@ namespace quads {
 // same arguments); on success *need is the scratch the call uses.
 quads_status_t select_check_args(const void* x, int64_t rows, int64_t cols, int64_t ldx,
                                  const int32_t* group_offsets, int32_t num_groups,
+                                 const int32_t* group_counts,
                                  const uint8_t* scales, const float* tensor_scale,
                                  const float* score_partials, int32_t k, const int32_t* sel,
                                  const uint8_t* r_codes, const uint8_t* r_scales,
@@ -1880,6 +1888,8 @@ quads_status_t select_check_args(const void* x, int64_t rows, int64_t cols, int6
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "select: k=%d must be a multiple of 16 in [16, cols]", k);
   if (ldx < cols) return fail(QUADS_ERR_MISALIGNED, "select: ldx < cols");
   if (group_offsets && num_groups < 1) return fail(QUADS_ERR_INVALID_ARG, "select: num_groups < 1");
+  if (group_counts && !group_offsets)
+    return fail(QUADS_ERR_INVALID_ARG, "select: group_counts needs group_offsets");
   *need = quads_workspace_size(QUADS_OP_SELECT, rows, cols, 0, k, group_offsets ? num_groups : 1);
   return QUADS_OK;
 }
@@ -1889,14 +1899,15 @@ int debug_line_quantize(long long* value) { return take_debug_line(value); }
 
 extern "C" quads_status_t quads_select_residual_channels(
     const void* x, int64_t rows, int64_t cols, int64_t ldx, const int32_t* group_offsets,
-    int32_t num_groups, const uint8_t* scales, int32_t scale_layout, const float* tensor_scale,
-    const float* score_partials, int32_t k, int32_t* sel, float* scores_out, uint8_t* r_codes,
-    uint8_t* r_scales, int32_t r_scale_layout, float* r_tensor_scale, void* workspace,
-    size_t workspace_bytes, void* sel_ready_event, void* stream) {
+    int32_t num_groups, const int32_t* group_counts, const uint8_t* scales, int32_t scale_layout,
+    const float* tensor_scale, const float* score_partials, int32_t k, int32_t* sel,
+    float* scores_out, uint8_t* r_codes, uint8_t* r_scales, int32_t r_scale_layout,
+    float* r_tensor_scale, void* workspace, size_t workspace_bytes, void* sel_ready_event,
+    void* stream) {
   size_t need = 0;
-  if (quads_status_t s = select_check_args(x, rows, cols, ldx, group_offsets, num_groups, scales,
-                                           tensor_scale, score_partials, k, sel, r_codes,
-                                           r_scales, r_tensor_scale, &need))
+  if (quads_status_t s = select_check_args(x, rows, cols, ldx, group_offsets, num_groups,
+                                           group_counts, scales, tensor_scale, score_partials, k,
+                                           sel, r_codes, r_scales, r_tensor_scale, &need))
     return s;
   const int G = group_offsets ? num_groups : 1;
   const int kpad = quads_kpad(k);
@@ -1943,15 +1954,16 @@ extern "C" quads_status_t quads_select_residual_channels(
       cudaMemsetAsync(r_scales + start, 0, (size_t)(sf_tc_bytes(rows, kpad) - start), st);
     }
     launch_dep(rsel_group_kernel, G + 2 * num_sms(), kRselGroupThreads, 0, st,
-        (const __nv_bfloat16*)x, rows, (int)cols, ldx, group_offsets, G, scales, scale_layout,
-        tensor_scale, sel, k, kpad, rs, r_codes, r_scales, r_scale_layout, r_tensor_scale);
+        (const __nv_bfloat16*)x, rows, (int)cols, ldx, group_offsets, G, group_counts, scales,
+        scale_layout, tensor_scale, sel, k, kpad, rs, r_codes, r_scales, r_scale_layout,
+        r_tensor_scale);
     return check_launch("select", long_groups ? 3 : 2);
   }
   cudaMemsetAsync(amax, 0, (size_t)G * 4, st);
   const int rb = (rows + 31) / 32 < 2 * (int64_t)num_sms() ? 8 : 32;
   launch_dep(rsel_residual_kernel, grid_for((rows + rb - 1) / rb, 1, 16), 256, 0, st,
-      (const __nv_bfloat16*)x, rows, (int)cols, ldx, group_offsets, G, scales, scale_layout,
-      tensor_scale, sel, k, rs, amax, rb);
+      (const __nv_bfloat16*)x, rows, (int)cols, ldx, group_offsets, G, group_counts, scales,
+      scale_layout, tensor_scale, sel, k, rs, amax, rb);
   if (r_scale_layout == QUADS_SCALES_TCGEN05 && rows % 128) {
     const int64_t start = (rows / 128) * (kpad / 64) * 512;
     cudaMemsetAsync(r_scales + start, 0, (size_t)(sf_tc_bytes(rows, kpad) - start), st);

@@ -229,6 +229,7 @@ class MoEExpertLayer:
         if comp and not self.fused_h:
             sel2, _, r2 = Q.select_residual_channels(h, hq, hpart, self.k2,
                                                      group_offsets=plan["offsets"], num_groups=E,
+                                                     group_counts=plan["counts"],
                                                      r_scale_layout=Q.TCGEN05, workspace=ws["s2"],
                                                      sel_ready_event=self.ev_sel2, stream=stream,
                                                      out=(b["sel2"], b["r2c"], b["r2s"], b["r2ts"]))

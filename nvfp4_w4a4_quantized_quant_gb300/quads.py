@@ -42,10 +42,11 @@ _SIGS = {
                                     _P, _I32, _P, _P, _P, _SZ, _P]),
     "quads_qdq_nvfp4": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _I64, _P, _I64, _P, _I32,
                                _P, _P, _SZ, _P]),
-    "quads_select_residual_channels": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _I32, _P, _P,
-                                              _I32, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P, _P]),
-    "quads_select_residual_channels_noalloc": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _I32, _P,
-                                                      _P, _I32, _P, _P, _P, _P, _I32, _P, _P]),
+    "quads_select_residual_channels": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _I32, _P,
+                                              _P, _I32, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P,
+                                              _P]),
+    "quads_select_residual_channels_noalloc": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _I32,
+                                                      _P, _P, _I32, _P, _P, _P, _P, _I32, _P, _P]),
     "quads_quantize_select_nvfp4": (_I32, [_P, _I64, _I64, _I64, _I32, _P, _I64, _P, _I32, _P, _P,
                                            _P, _P, _P, _I32, _P, _P, _SZ, _P]),
     "quads_quantize_select_groups_nvfp4": (_I32, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _I32,
@@ -346,11 +347,12 @@ def quantize_select_groups_nvfp4(x: torch.Tensor, k: int, group_offsets, num_gro
 
 
 def select_residual_channels(x: torch.Tensor, q: QTensor, partials: torch.Tensor, k: int, *,
-                             group_offsets=None, num_groups: int = 1,
+                             group_offsets=None, num_groups: int = 1, group_counts=None,
                              r_scale_layout: int = LINEAR, want_scores: bool = False,
                              sel_ready_event=None, workspace=None, out=None, stream=None):
     """-> (sel int32 [G, k], scores [G, cols] or None, QTensor of Q(R_sel) [rows, kpad]).
-    sel_ready_event (torch.cuda.Event): recorded once sel is written, before R_sel."""
+    sel_ready_event (torch.cuda.Event): recorded once sel is written, before R_sel.
+    group_counts: as given to quantize_nvfp4 (rows past a group's count are zero rows)."""
     lib = load()
     G = num_groups if group_offsets is not None else 1
     rows, cols = q.rows, q.cols
@@ -367,7 +369,8 @@ def select_residual_channels(x: torch.Tensor, q: QTensor, partials: torch.Tensor
     sc = torch.empty((G, cols), dtype=torch.float32, device=dev) if want_scores else None
     ws = _workspace(workspace_size(OP_SELECT, rows, cols, 0, k, G), dev, workspace, stream)
     _check(lib.quads_select_residual_channels(
-        _ptr(x), rows, cols, x.stride(0), _ptr(group_offsets), G, _ptr(q.scales), q.layout,
+        _ptr(x), rows, cols, x.stride(0), _ptr(group_offsets), G, _ptr(group_counts),
+        _ptr(q.scales), q.layout,
         _ptr(q.tensor_scale), _ptr(partials), k, _ptr(sel), _ptr(sc), _ptr(rc), _ptr(rs),
         r_scale_layout, _ptr(rts), _ptr(ws), ws.numel(), _event(sel_ready_event, stream),
         _stream(stream)), "select_residual_channels")
@@ -375,7 +378,7 @@ def select_residual_channels(x: torch.Tensor, q: QTensor, partials: torch.Tensor
 
 
 def select_residual_channels_noalloc(x: torch.Tensor, q: QTensor, partials: torch.Tensor, k: int, *,
-                                     group_offsets=None, num_groups: int = 1,
+                                     group_offsets=None, num_groups: int = 1, group_counts=None,
                                      r_scale_layout: int = LINEAR, want_scores: bool = False,
                                      out=None, stream=None):
     """As select_residual_channels, with the library's built-in scratch array instead of
@@ -395,7 +398,8 @@ def select_residual_channels_noalloc(x: torch.Tensor, q: QTensor, partials: torc
         sel, rc, rs, rts = out
     sc = torch.empty((G, cols), dtype=torch.float32, device=dev) if want_scores else None
     _check(lib.quads_select_residual_channels_noalloc(
-        _ptr(x), rows, cols, x.stride(0), _ptr(group_offsets), G, _ptr(q.scales), q.layout,
+        _ptr(x), rows, cols, x.stride(0), _ptr(group_offsets), G, _ptr(group_counts),
+        _ptr(q.scales), q.layout,
         _ptr(q.tensor_scale), _ptr(partials), k, _ptr(sel), _ptr(sc), _ptr(rc), _ptr(rs),
         r_scale_layout, _ptr(rts), _stream(stream)), "select_residual_channels_noalloc")
     return sel, sc, QTensor(rc, rs, rts, rows, kp, r_scale_layout)

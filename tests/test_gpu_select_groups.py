@@ -189,3 +189,36 @@ def test_select_groups_flags_groups_off_the_chunk_grid(lib):
     torch.cuda.synchronize()
     assert lib.device_status() == 6      # QUADS_ERR_DEVICE_CHECK (and cleared by the read)
     assert lib.device_status() == 0
+
+
+@pytest.mark.parametrize("groups", [128, 8])
+def test_select_group_counts_take_padding_rows_as_zero(lib, groups):
+    """The selection call given the quantizer's group counts reads no padding
+    row: on garbage padding it gives what it gives without counts on the
+    zeroed padding (128 groups: the per-group R_sel block; 8: the sliced
+    residual kernel), and the oracle's R_sel on sampled groups."""
+    rng = inputs.make_rng(25)
+    counts = rng.integers(0, 200, groups).astype(np.int32)
+    counts[:2] = [0, 128]
+    bits, bz, offs = _padded(rng, counts, 128, 256)
+    G, k = groups, 32
+    ot, ct = torch.from_numpy(offs).cuda(), torch.from_numpy(counts).cuda()
+    q, part = lib.quantize_nvfp4(bf16_tensor(bits), group_offsets=ot, num_groups=G, group_counts=ct,
+                                 scores=True, scale_layout=1)
+    a = lib.select_residual_channels(bf16_tensor(bits), q, part, k, group_offsets=ot, num_groups=G,
+                                     group_counts=ct, r_scale_layout=1, want_scores=True)
+    b = lib.select_residual_channels(bf16_tensor(bz), q, part, k, group_offsets=ot, num_groups=G,
+                                     r_scale_layout=1, want_scores=True)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    assert torch.equal(a[2].codes, b[2].codes) and torch.equal(a[2].scales, b[2].scales)
+    assert torch.equal(a[2].tensor_scale, b[2].tensor_scale)
+    xz, rows, kp = f32(bz), int(offs[-1]), lib.kpad(k)
+    rc, rsc = codes_np(a[2].codes, kp), linear_scales(a[2], rows, kp)
+    rts, sel = a[2].tensor_scale.cpu().numpy(), a[0].cpu().numpy()
+    for g in (0, 1, groups - 1):
+        lo, hi = int(offs[g]), int(offs[g + 1])
+        ref = Q.quantize_full(xz[lo:hi], k)
+        assert np.array_equal(sel[g], ref["sel"][0]) and rts[g] == ref["r_s_t"][0]
+        assert np.array_equal(rc[lo:hi, :k], ref["r_codes"]) and np.array_equal(rsc[lo:hi, :k // 16], ref["r_scales"])

@@ -76,9 +76,12 @@ def test_host_side_argument_checks_need_no_gpu(lib):
     st = lib.quads_w4a4_gemm_comp(64, 128, 256, p, p, p, p, p, p, None, None, q, p, p, p, p, p, 16,
                                   p, 0, 128, None, 0, None)
     assert st == 3                                   # Q(W_sel) not 16-byte aligned
-    st = lib.quads_select_residual_channels(p, 64, 256, 256, None, 1, p, 0, p, p, 17, p, None, p, p, 0, p,
+    st = lib.quads_select_residual_channels(p, 64, 256, 256, None, 1, None, p, 0, p, p, 17, p, None, p, p, 0, p,
                                             p, 1 << 20, None, None)
     assert st == 2
+    st = lib.quads_select_residual_channels(p, 64, 256, 256, None, 1, p, p, 0, p, p, 16, p, None, p, p, 0, p,
+                                            p, 1 << 20, None, None)
+    assert st == 1 and "group_counts" in _err(lib)   # counts without group offsets
     st = lib.quads_moe_route(p, 100, 300, 8, p, p, p, p, p, p, 1 << 20, p, 1 << 20, None)
     assert st == 2                                   # > 256 experts
     st = lib.quads_moe_route(p, 100, 16, 8, p, p, p, p, p, p, 10, p, 1 << 20, None)

@@ -62,7 +62,7 @@ def test_noalloc_rejects_shapes_beyond_the_builtin_scratch(lib):
     rows, cols, k = 200000, 2048, 64          # needs rows*k*4 = 51 MB of scratch
     assert lib.workspace_size(lib.OP_SELECT, rows, cols, 0, k, 1) > limit
     p = ctypes.c_void_p(256)                  # rejected on the host before any use
-    st = raw.quads_select_residual_channels_noalloc(p, rows, cols, cols, None, 1, p, 0, p, p, k,
+    st = raw.quads_select_residual_channels_noalloc(p, rows, cols, cols, None, 1, None, p, 0, p, p, k,
                                                     p, None, p, p, 0, p, None)
     assert st == 7 and b"built-in array" in raw.quads_last_error_detail()
 
@@ -73,8 +73,8 @@ def test_noalloc_reports_the_same_status_as_the_workspace_entry_point(lib):
     raw = lib.load()
     p = ctypes.c_void_p(256)
     for rows, cols, k in [(64, 256, 0), (64, 256, 24), (64, 250, 16), (64, 256, 512)]:
-        st_ws = raw.quads_select_residual_channels(p, rows, cols, cols, None, 1, p, 0, p, p, k,
+        st_ws = raw.quads_select_residual_channels(p, rows, cols, cols, None, 1, None, p, 0, p, p, k,
                                                    p, None, p, p, 0, p, p, 1 << 20, None, None)
-        st_na = raw.quads_select_residual_channels_noalloc(p, rows, cols, cols, None, 1, p, 0, p,
+        st_na = raw.quads_select_residual_channels_noalloc(p, rows, cols, cols, None, 1, None, p, 0, p,
                                                            p, k, p, None, p, p, 0, p, None)
         assert st_ws == st_na != 0, (rows, cols, k, st_ws, st_na)
