@@ -1458,14 +1458,25 @@ struct TraceItem {
   uint32_t sbyte;   // block scale byte
 };
 
+// Row r and 16-block b of a flat block index, advanced by the grid stride
+// (dr rows and db blocks, bpr blocks per row) without a division per step.
+__device__ __forceinline__ void row_block_step(uint32_t& r, uint32_t& b, uint32_t dr, uint32_t db,
+                                               uint32_t bpr) {
+  r += dr;
+  b += db;
+  if (b >= bpr) {
+    b -= bpr;
+    ++r;
+  }
+}
+
 template <bool kMx>
-__device__ __forceinline__ void trace_load(TraceItem& it, uint32_t i, uint32_t total,
-                                           uint32_t blk_per_row, const __nv_bfloat16* xt,
-                                           int64_t ldx, const uint8_t* rcodes, int64_t ldc,
+__device__ __forceinline__ void trace_load(TraceItem& it, uint32_t i, uint32_t total, uint32_t r,
+                                           uint32_t b, const __nv_bfloat16* xt, int64_t ldx,
+                                           const uint8_t* rcodes, int64_t ldc,
                                            const uint8_t* rscales, int cols) {
   if (i >= total) return;
-  const uint32_t r = i / blk_per_row;
-  const int col = (int)(i - r * blk_per_row) * 16;
+  const int col = (int)b * 16;
   const uint4* px = reinterpret_cast<const uint4*>(xt + (int64_t)r * ldx + col);
   it.x0 = __ldg(px);
   it.x1 = __ldg(px + 1);
@@ -1475,8 +1486,9 @@ __device__ __forceinline__ void trace_load(TraceItem& it, uint32_t i, uint32_t t
                  : __ldg(rscales + (int64_t)r * (cols >> 4) + (col >> 4));
 }
 
+// Five blocks per SM (48 registers, no spills).
 template <bool kMx>
-__global__ void __launch_bounds__(256) trace_kernel(
+__global__ void __launch_bounds__(256, 5) trace_kernel(
     const __nv_bfloat16* __restrict__ xt, int64_t rows, int cols, int64_t ldx,
     const uint8_t* __restrict__ rcodes, int64_t ldc, const uint8_t* __restrict__ rscales,
     const float* __restrict__ rst, uint8_t* __restrict__ out,
@@ -1484,22 +1496,33 @@ __global__ void __launch_bounds__(256) trace_kernel(
   const uint32_t blk_per_row = (uint32_t)cols >> 4;
   const uint32_t total = (uint32_t)(rows * blk_per_row);   // < 2^31 (host check)
   const uint32_t stride = gridDim.x * blockDim.x;
-  const float s_t = kMx ? 1.0f : rst[0];
+  // NVFP4: 1/d of every scale byte under the tensor scale (0 for a zero
+  // block), so a block needs one shared load instead of the scale decode and
+  // the correctly rounded reciprocal
+  __shared__ float td[kMx ? 1 : 256], tr[kMx ? 1 : 256];
+  if (!kMx) {
+    fill_scale_table(rst[0], td, tr);
+    __syncthreads();
+  }
   unsigned int n_rtn = 0, n_tr = 0, n_adj = 0;
   uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  const uint32_t dr = stride / blk_per_row, db = stride - dr * blk_per_row;
+  uint32_t nr = i / blk_per_row, nb = i - nr * blk_per_row;   // the next load's row and block
   TraceItem nxt;
-  trace_load<kMx>(nxt, i, total, blk_per_row, xt, ldx, rcodes, ldc, rscales, cols);
+  trace_load<kMx>(nxt, i, total, nr, nb, xt, ldx, rcodes, ldc, rscales, cols);
   for (; i < total; i += stride) {
     const TraceItem cur = nxt;
-    trace_load<kMx>(nxt, i + stride, total, blk_per_row, xt, ldx, rcodes, ldc, rscales, cols);
-    const uint32_t r = i / blk_per_row;
-    const int col = (int)(i - r * blk_per_row) * 16;
+    const uint32_t r = nr;
+    const int col = (int)nb * 16;
+    row_block_step(nr, nb, dr, db, blk_per_row);
+    trace_load<kMx>(nxt, i + stride, total, nr, nb, xt, ldx, rcodes, ldc, rscales, cols);
     BlockScale bs;
     if (kMx) {
       bs.r = e8m0_inverse(cur.sbyte);
       bs.zero = false;
     } else {
-      bs = block_scale_from_byte(cur.sbyte, s_t);
+      bs.r = tr[cur.sbyte];
+      bs.zero = bs.r == 0.0f;
     }
     uint32_t outw[2];
 #pragma unroll
@@ -1664,12 +1687,14 @@ __global__ void __launch_bounds__(256) trace_1bit_kernel(
   const uint32_t blk_per_row = (uint32_t)cols >> 4;
   const uint32_t total = (uint32_t)(rows * blk_per_row);   // < 2^31 (host check)
   const uint32_t stride = gridDim.x * blockDim.x;
-  const float s_t = rst[0];
+  // 1/d of every scale byte (0 for a zero block), as in trace_kernel
+  __shared__ float td[256], tr[256];
+  fill_scale_table(rst[0], td, tr);
+  __syncthreads();
   unsigned int n_chg = 0, n_bit = 0;
-  auto load = [&](uint32_t i, uint4& x0, uint4& x1, uint32_t& mb, uint32_t& sb) {
+  auto load = [&](uint32_t i, uint32_t r, uint32_t bi, uint4& x0, uint4& x1, uint32_t& mb,
+                  uint32_t& sb) {
     if (i >= total) return;
-    const uint32_t r = i / blk_per_row;
-    const uint32_t bi = i - r * blk_per_row;
     const uint4* px = reinterpret_cast<const uint4*>(xt + (int64_t)r * ldx + bi * 16);
     x0 = __ldg(px);
     x1 = __ldg(px + 1);
@@ -1678,16 +1703,20 @@ __global__ void __launch_bounds__(256) trace_1bit_kernel(
     sb = __ldg(rscales + (int64_t)r * (cols >> 4) + bi);
   };
   uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  const uint32_t dr = stride / blk_per_row, db = stride - dr * blk_per_row;
+  uint32_t nr = i / blk_per_row, nb = i - nr * blk_per_row;   // the next load's row and block
   uint4 nx0 = make_uint4(0, 0, 0, 0), nx1 = nx0;
   uint32_t nmb = 0, nsb = 0;
-  load(i, nx0, nx1, nmb, nsb);
+  load(i, nr, nb, nx0, nx1, nmb, nsb);
   for (; i < total; i += stride) {
     const uint4 x0 = nx0, x1 = nx1;
     const uint32_t mb16 = nmb, sbyte = nsb;
-    load(i + stride, nx0, nx1, nmb, nsb);
-    const uint32_t r = i / blk_per_row;
-    const uint32_t bi = i - r * blk_per_row;
-    const BlockScale bs = block_scale_from_byte(sbyte, s_t);
+    const uint32_t r = nr, bi = nb;
+    row_block_step(nr, nb, dr, db, blk_per_row);
+    load(i + stride, nr, nb, nx0, nx1, nmb, nsb);
+    BlockScale bs;
+    bs.r = tr[sbyte];
+    bs.zero = bs.r == 0.0f;
     uint32_t outw[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
