@@ -773,54 +773,43 @@ __device__ __forceinline__ void rsel_group_rows(
     const __nv_bfloat16* xs = nullptr, const uint8_t* ss = nullptr, float* rsm = nullptr) {
   const int ncols16 = cols >> 4, rcols16 = kpad >> 4;
   const int vpr = kpad >> 3;   // 8-element vectors per residual row (even)
-  // rows past rreal: R = 0, so only the real rows are gathered.  Lanes take
-  // selected channels (j = j0 + lane: the channel and its scale column are
-  // looked up once), warps take rows, four rows in flight per lane; a warp
-  // reads 32 selected channels of one row at a time.
-  const int nr = (int)(rreal - r0);
-  const int lane = (int)(threadIdx.x & 31), nw = (int)(blockDim.x >> 5);
+  // rows past rreal: R = 0, so only the real rows are gathered (four
+  // independent gathers in flight per thread)
+  const int total = (int)(rreal - r0) * k;
   float m = 0.0f;
-  for (int j0 = 0; j0 < k; j0 += 32) {
-    const int j = j0 + lane;
-    const bool jv = j < k;
-    int c = jv ? sg[j] : 0;
-    if (!QDBG(c >= 0 && c < cols)) c = 0;
-    const int cb = c >> 4;
-    // the scale byte's offset: a row part and a column part
-    const int64_t sfc = layout == QUADS_SCALES_TCGEN05 ? (int64_t)(cb >> 2) * 512 + (cb & 3) : cb;
-    for (int rb = (int)(threadIdx.x >> 5) * 4; rb < nr; rb += nw * 4) {
-      float xv[4];
-      uint32_t sb[4];
+  for (int i0 = threadIdx.x; i0 < total; i0 += 4 * blockDim.x) {
+    int rl[4], j[4], c[4];
+    float xv[4];
+    uint32_t sb[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        xv[u] = 0.0f;
-        sb[u] = 0u;
-        const int rl = rb + u;
-        if (rl < nr && jv) {
-          if (xs) {
-            xv[u] = __bfloat162float(xs[(int64_t)rl * cols + c]);
-            sb[u] = ss[(int64_t)rl * ncols16 + cb];
-          } else {
-            const int64_t r = r0 + rl;
-            const int64_t sfr = layout == QUADS_SCALES_TCGEN05
-                                    ? (r >> 7) * (int64_t)(ncols16 >> 2) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4
-                                    : r * ncols16;
-            xv[u] = __bfloat162float(x[r * ldx + c]);
-            sb[u] = scales[sfr + sfc];
-          }
-        }
-      }
-      float R[4];
-      residual_pair(xv[0], xv[1], sb[0], sb[1], td, tr, R[0], R[1]);
-      residual_pair(xv[2], xv[3], sb[2], sb[3], td, tr, R[2], R[3]);
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * (int)blockDim.x;
+      rl[u] = i < total ? i / k : 0;
+      j[u] = i < total ? i - rl[u] * k : 0;
+      c[u] = sg[j[u]];
+      if (!QDBG(c[u] >= 0 && c[u] < cols)) c[u] = 0;
+    }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int rl = rb + u;
-        if (rl >= nr || !jv) continue;
-        if (rsm) rsm[(int64_t)rl * k + j] = R[u];
-        else rs[(r0 + rl) * k + j] = R[u];
-        m = fmaxf(m, fabsf(R[u]));
+    for (int u = 0; u < 4; ++u) {
+      if (xs) {
+        xv[u] = __bfloat162float(xs[(int64_t)rl[u] * cols + c[u]]);
+        sb[u] = ss[(int64_t)rl[u] * ncols16 + (c[u] >> 4)];
+      } else {
+        const int64_t r = r0 + rl[u];
+        xv[u] = __bfloat162float(x[r * ldx + c[u]]);
+        sb[u] = scales[sf_offset(layout, r, c[u] >> 4, ncols16)];
       }
+    }
+    float R[4];
+    residual_pair(xv[0], xv[1], sb[0], sb[1], td, tr, R[0], R[1]);
+    residual_pair(xv[2], xv[3], sb[2], sb[3], td, tr, R[2], R[3]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * (int)blockDim.x;
+      if (i >= total) continue;
+      if (rsm) rsm[(int64_t)rl[u] * k + j[u]] = R[u];
+      else rs[(r0 + rl[u]) * k + j[u]] = R[u];
+      m = fmaxf(m, fabsf(R[u]));
     }
   }
   m = warp_max(m);

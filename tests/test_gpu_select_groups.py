@@ -222,3 +222,22 @@ def test_select_group_counts_take_padding_rows_as_zero(lib, groups):
         ref = Q.quantize_full(xz[lo:hi], k)
         assert np.array_equal(sel[g], ref["sel"][0]) and rts[g] == ref["r_s_t"][0]
         assert np.array_equal(rc[lo:hi, :k], ref["r_codes"]) and np.array_equal(rsc[lo:hi, :k // 16], ref["r_scales"])
+
+
+def test_select_groups_on_chip_limits(lib):
+    """Groups on both sides of the kernel's two on-chip limits at 768 channels,
+    k = 64: the real rows kept in shared memory (about 77 rows) and R kept in
+    the squares' buffer ((real rows) * k <= 32 * cols, 384 rows); every output
+    equals the two calls'."""
+    rng = inputs.make_rng(26)
+    counts = np.array(list(range(70, 91)) + list(range(378, 391)), np.int32)
+    bits, bz, offs = _padded(rng, counts, 128, 768)
+    G, k, rows = len(counts), 64, int(offs[-1])
+    ot, ct = torch.from_numpy(offs).cuda(), torch.from_numpy(counts).cuda()
+    fused = lib.quantize_select_groups_nvfp4(bf16_tensor(bits), k, ot, G, group_counts=ct,
+                                             scale_layout=1, r_scale_layout=1, want_scores=True)
+    two = _two_calls(lib, bz, offs, counts, k, 1, 1, rows,
+                     tensor_scale_in=fused[0].tensor_scale)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    _assert_same(lib, fused, two, rows, 768, k)
