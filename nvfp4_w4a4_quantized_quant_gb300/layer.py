@@ -98,17 +98,17 @@ class MoEExpertLayer:
         quantization, selection and R_sel) as one launch with a block per
         expert (quantize_select_groups_nvfp4) instead of the quantizer and the
         selection call; the same outputs bit for bit.  None (default): used
-        when the experts average at most 128 rows (decode-sized batches,
-        where it saves launches); with more rows per expert, one block per
-        expert quantizes slower than the quantizer spread over every SM, and
-        Q(W_sel) could no longer overlap R_sel."""
+        when the experts average at most 256 rows (decode-sized and mid-sized
+        batches, where it saves launches); with more rows per expert, one
+        block per expert quantizes slower than the quantizer spread over
+        every SM, and Q(W_sel) could no longer overlap R_sel."""
         self.E, twoF, self.H = w1.shape
         self.F = twoF // 2
         assert w2.shape == (self.E, self.H, self.F)
         self.topk, self.k1, self.k2, self.compensate = topk, k1, k2, compensate
         self.fused = fused_activation_side
         if fused_expert_side is None:
-            fused_expert_side = max_tokens * topk <= 128 * w1.shape[0]
+            fused_expert_side = max_tokens * topk <= 256 * w1.shape[0]
         self.fused_h = fused_expert_side
         dev = w1.device
         self.w1q = Q.quantize_expert_weights(w1, swiglu_interleave=True)
