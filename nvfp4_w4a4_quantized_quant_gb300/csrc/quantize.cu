@@ -314,14 +314,17 @@ __global__ void __launch_bounds__(256, kScores ? 4 : 3) quantize_kernel(
 }
 
 // Score mode with one thread per (32-row chunk, 16-column block): the thread
-// walks its chunk's rows in order (the next two rows' loads in flight), writes
+// walks its chunk's rows in order (the next D rows' loads in flight), writes
 // each row's codes and block scale, and adds each column's residual square to
 // a register in row order from 0 -- the same float32 sequence the shared-
 // memory column sums form -- so the partials need no shared memory and no
 // barrier.  Chunks never straddle a group (group offsets are multiples of 32
 // in score mode).  Used when there are enough (chunk, block) pairs to fill
-// the GPU.
-__global__ void __launch_bounds__(256, 3) quantize_chunk_kernel(
+// the GPU.  D = 2 at three blocks per SM, D = 4 at two (more bytes in flight
+// per SM; chosen when every resident thread gets several pairs, since one
+// wave fewer threads otherwise leaves a tail).
+template <int D>
+__global__ void __launch_bounds__(256, D == 2 ? 3 : 2) quantize_chunk_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t rows, int cols, int64_t ldx,
     const int32_t* __restrict__ row_index, const int32_t* __restrict__ goff, int G,
     const float* __restrict__ st, const uint32_t* __restrict__ amax_bits, float* __restrict__ st_out,
@@ -384,18 +387,20 @@ __global__ void __launch_bounds__(256, 3) quantize_chunk_kernel(
         lo = hi = make_uint4(0, 0, 0, 0);   // padding (or past the chunk): a zero row
       }
     };
-    uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, b0 = a0, b1 = a0;
-    load(0, a0, a1);
-    load(1, b0, b1);
+    uint4 bl[D], bh[D];   // rows r .. r + D - 1, row r + q in slot (r + q) % D
+#pragma unroll
+    for (int q = 0; q < D; ++q) load(q, bl[q], bh[q]);
     float acc[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
 #pragma unroll 1
-    for (int r = 0; r < nr; ++r) {
-      const uint4 lo = a0, hi = a1;
-      a0 = b0;
-      a1 = b1;
-      load(r + 2, b0, b1);
+    for (int rb = 0; rb < nr; rb += D) {
+#pragma unroll
+    for (int q = 0; q < D; ++q) {
+      const int r = rb + q;
+      if (r >= nr) break;
+      const uint4 lo = bl[q], hi = bh[q];
+      load(r + D, bl[q], bh[q]);
       const int64_t row = r0 + r;
       float f[16];
       BlockScale bs;
@@ -411,6 +416,7 @@ __global__ void __launch_bounds__(256, 3) quantize_chunk_kernel(
         const float R = __fsub_rn(f[j], __fmul_rn(lv[j], bs.d));
         acc[j] = __fadd_rn(acc[j], __fmul_rn(R, R));
       }
+    }
     }
     float4* pp = reinterpret_cast<float4*>(partials + (int64_t)chunk * cols + cb * 16);
 #pragma unroll
@@ -1843,13 +1849,22 @@ static quads_status_t quantize_impl(
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
         codes, ld_codes, scales, scale_layout, nullptr, qdq, ldq, group_counts);
   else if (score_partials && ((rows + 31) / 32) * (cols / 16) >= (int64_t)num_sms() * 512 &&
-           ((rows + 31) / 32) * (cols / 16) < (1ll << 31) && ld_codes % 8 == 0)
+           ((rows + 31) / 32) * (cols / 16) < (1ll << 31) && ld_codes % 8 == 0) {
     // enough (chunk, block) pairs for a thread each: about two blocks per SM
     // (its 8-byte code stores need ld_codes % 8 == 0; the 32x256-task kernel
-    // stores 4 bytes at a time)
-    launch_dep(quantize_chunk_kernel, grid_for(((rows + 31) / 32) * (cols / 16), 256, 3), 256, 0, st,
-        xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
-        codes, ld_codes, scales, scale_layout, score_partials, group_counts);
+    // stores 4 bytes at a time).  Four rows in flight when every resident
+    // thread gets at least three pairs (65536 x 2048: 91 -> 80 us; the 8192-
+    // token layer's h, about 1.3 pairs a thread, keeps two: 52 vs 58 us)
+    const int64_t pairs = ((rows + 31) / 32) * (cols / 16);
+    if (pairs >= (int64_t)num_sms() * 2 * 256 * 3)
+      launch_dep(quantize_chunk_kernel<4>, grid_for(pairs, 256, 2), 256, 0, st,
+          xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
+          codes, ld_codes, scales, scale_layout, score_partials, group_counts);
+    else
+      launch_dep(quantize_chunk_kernel<2>, grid_for(pairs, 256, 3), 256, 0, st,
+          xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,
+          codes, ld_codes, scales, scale_layout, score_partials, group_counts);
+  }
   else if (score_partials)
     launch_dep(quantize_kernel<true, false>, blocks, 256, 0, st,
         xb, rows, (int)cols, ldx, row_index, group_offsets, G, stp, amax_bits, tensor_scale_out,

@@ -512,3 +512,31 @@ def test_fused_quantize_select_matches_the_two_calls(lib, rows, cols, k, layout)
         ref = Q.quantize_full(f32(inputs.f32_to_bf16_bits(xf)), k)
         assert np.array_equal(fsel.cpu().numpy(), ref["sel"])
         assert np.array_equal(codes_np(fr.codes, lib.kpad(k))[:, :k], ref["r_codes"])
+
+
+def test_quantize_scores_large_input_sampled_chunks(lib):
+    """65536 x 2048 with score partials: enough (chunk, 16-column block) pairs
+    that the thread-per-pair kernel keeps four rows of loads in flight; the
+    tensor scale against its definition on the input's max |x|, and codes,
+    scales and partials against the oracle on 24 sampled chunks (the last
+    one included)."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(31)
+    rows, cols = 65536, 2048
+    x = (torch.randn((rows, cols), generator=g, device="cuda") *
+         torch.exp2(torch.randint(-3, 4, (rows, 1), generator=g, device="cuda").float())).to(torch.bfloat16)
+    q, part = lib.quantize_nvfp4(x, scores=True)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    amax = np.float32(x.abs().max().float().item())
+    ts = q.tensor_scale.cpu().numpy()[0]
+    assert ts == Q.tensor_scale(np.array([amax], np.float32))   # the oracle on the maximum alone
+    rng = inputs.make_rng(31)
+    for ch in list(rng.choice(rows // 32 - 1, 23, replace=False)) + [rows // 32 - 1]:
+        a, b = 32 * int(ch), 32 * int(ch) + 32
+        xf = x[a:b].float().cpu().numpy()
+        oc, osc = Q.quantize(xf, ts)
+        assert np.array_equal(codes_np(q.codes[a:b], cols), oc)
+        assert np.array_equal(q.scales.cpu().numpy().reshape(rows, cols // 16)[a:b], osc)
+        R = Q.residual(xf, oc, osc, ts)
+        assert np.array_equal(part[int(ch):int(ch) + 1].cpu().numpy(), Q.chunk_partials(R))
