@@ -207,10 +207,16 @@ __global__ void __launch_bounds__(256) assign_kernel(const int32_t* __restrict__
 }
 
 // Wide rows (>= 32 code vectors of 16 bytes): a warp copies 4 rows at a time,
-// lane = vector, all loads issued before the stores, and the row's 4-byte
-// scale groups go to their TCGEN05 atom positions.  Narrow rows (the k-channel
-// residual slices): a thread per (row, vector) / (row, scale group), 32-bit
-// index math.  Padding rows (row_token -1) get zero codes and scales.
+// lane = vector, all loads issued before the stores; then the scales in a
+// second pass over (128-row block, 4-column group) items: in the TCGEN05
+// layout the 16 bytes at lane l of an atom hold rows l, l+32, l+64 and l+96
+// of the block, so lane l gathers those four rows' 4-byte groups and stores
+// them as one 16-byte word -- a warp writes the atom's 512 bytes whole
+// (4-byte stores at a 512-byte stride left most of each sector to be merged
+// in L2); a block that reaches past the last row keeps 4-byte stores for its
+// rows.  Narrow rows (the k-channel residual slices): a thread per (row,
+// vector) / (row, scale group) in one pass, 32-bit index math.  Padding rows
+// (row_token -1) get zero codes and scales.
 __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__ row_token,
                                                      const int32_t* __restrict__ off, int E,
                                                      int64_t cap, int cols,
@@ -227,9 +233,9 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
   const int natom = ncols16 >> 2;         // 4-byte scale groups per row
   const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = nthreads >> 5;
   if (nvec >= 32) {
-    const int lane = threadIdx.x & 31;
-    const int64_t nwarps = nthreads >> 5;
     for (int64_t r0 = (tid >> 5) * 4; r0 < nrows; r0 += nwarps * 4) {
       int t[4];
 #pragma unroll
@@ -254,34 +260,52 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
               reinterpret_cast<uint4*>(oc + (r0 + u) * cbytes)[v] = buf[u][h];
           }
       }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (t[u] == -2) continue;
-        for (int a = lane; a < natom; a += 32) {
-          uint32_t v = 0;
-          if (t[u] >= 0) v = __ldg(reinterpret_cast<const uint32_t*>(isf + (int64_t)t[u] * ncols16) + a);
-          *reinterpret_cast<uint32_t*>(osf + sf_tc_offset(r0 + u, 4 * a, ncols16)) = v;
-        }
+    }
+  } else {
+    // narrow rows: nvec < 32, natom < 8; rows * nvec fits comfortably in 32
+    // bits.  Codes and the 4-byte scale groups in one pass (one round trip
+    // for the small residual slices, where latency decides)
+    const uint32_t ncode = (uint32_t)(nrows * nvec), nsc = (uint32_t)(nrows * natom);
+    for (uint32_t i = (uint32_t)tid; i < ncode + nsc; i += (uint32_t)nthreads) {
+      if (i < ncode) {
+        const uint32_t r = i / (uint32_t)nvec, v = i - r * (uint32_t)nvec;
+        const int t = __ldg(row_token + r);
+        uint4 x = make_uint4(0, 0, 0, 0);
+        if (t >= 0) x = __ldg(reinterpret_cast<const uint4*>(ic + (int64_t)t * cbytes) + v);
+        reinterpret_cast<uint4*>(oc)[i] = x;
+      } else {
+        const uint32_t j = i - ncode;
+        const uint32_t r = j / (uint32_t)natom, a = j - r * (uint32_t)natom;
+        const int t = __ldg(row_token + r);
+        uint32_t x = 0;
+        if (t >= 0) x = __ldg(reinterpret_cast<const uint32_t*>(isf + (int64_t)t * ncols16) + a);
+        *reinterpret_cast<uint32_t*>(osf + sf_tc_offset(r, 4 * a, ncols16)) = x;
       }
     }
     return;
   }
-  // narrow rows: nvec < 32, natom < 8; rows * nvec fits comfortably in 32 bits
-  const uint32_t ncode = (uint32_t)(nrows * nvec), nsc = (uint32_t)(nrows * natom);
-  for (uint32_t i = (uint32_t)tid; i < ncode + nsc; i += (uint32_t)nthreads) {
-    if (i < ncode) {
-      const uint32_t r = i / (uint32_t)nvec, v = i - r * (uint32_t)nvec;
-      const int t = __ldg(row_token + r);
-      uint4 x = make_uint4(0, 0, 0, 0);
-      if (t >= 0) x = __ldg(reinterpret_cast<const uint4*>(ic + (int64_t)t * cbytes) + v);
-      reinterpret_cast<uint4*>(oc)[i] = x;
+  // wide rows' scales: a warp per (128-row block, 4-column group)
+  const int64_t nblk = (nrows + 127) >> 7;
+  for (int64_t item = tid >> 5; item < nblk * natom; item += nwarps) {
+    const int64_t rb = item / natom;
+    const int a = (int)(item - rb * natom);
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int64_t r = rb * 128 + lane + 32 * q;
+      const int t = r < nrows ? __ldg(row_token + r) : -1;
+      w[q] = t >= 0 && QDBG(t < (1 << 30))
+                 ? __ldg(reinterpret_cast<const uint32_t*>(isf + (int64_t)t * ncols16) + a)
+                 : 0u;
+    }
+    uint8_t* atom = osf + (rb * natom + a) * 512;
+    if (rb * 128 + 128 <= nrows) {
+      *reinterpret_cast<uint4*>(atom + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
     } else {
-      const uint32_t j = i - ncode;
-      const uint32_t r = j / (uint32_t)natom, a = j - r * (uint32_t)natom;
-      const int t = __ldg(row_token + r);
-      uint32_t x = 0;
-      if (t >= 0) x = __ldg(reinterpret_cast<const uint32_t*>(isf + (int64_t)t * ncols16) + a);
-      *reinterpret_cast<uint32_t*>(osf + sf_tc_offset(r, 4 * a, ncols16)) = x;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (rb * 128 + lane + 32 * q < nrows)
+          *reinterpret_cast<uint32_t*>(atom + lane * 16 + q * 4) = w[q];
     }
   }
 }
