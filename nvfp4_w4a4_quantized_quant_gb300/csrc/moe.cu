@@ -28,7 +28,12 @@ constexpr int kRouteTokens = 32;   // tokens per routing block: one warp each
 // assign_kernel), and each expert its count of the block's tokens, written to
 // bcount[e][block] -- no atomics, so every number is independent of
 // scheduling.
-__global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ logits, int T,
+// W: 32-expert words held per lane (the smallest power of two >= E / 32), so
+// an arg-max round scans only the lanes' real expert slots; two 1024-thread
+// blocks per SM (32 registers), so that the token blocks of a large batch are
+// resident in one wave.
+template <int W>
+__global__ void __launch_bounds__(1024, 2) route_kernel(const float* __restrict__ logits, int T,
                                                      int E, int topk, int32_t* __restrict__ idx,
                                                      float* __restrict__ gates,
                                                      int32_t* __restrict__ bcount,
@@ -41,9 +46,9 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
   const bool live = t < T;
   int my_e = 0x7fffffff, rank = 0;
   if (live) {
-    float v[kMaxExperts / 32];
+    float v[W];
 #pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) {
+    for (int i = 0; i < W; ++i) {
       const int e = lane + 32 * i;
       const float l = (i < words && e < E) ? logits[(int64_t)t * E + e] : -INFINITY;
       v[i] = isnan(l) ? -INFINITY : l;   // a NaN logit ranks lowest: every pick is a real expert
@@ -54,7 +59,7 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
       float bv = -INFINITY;
       int be = 0x7fffffff;
 #pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; ++i) {
+      for (int i = 0; i < W; ++i) {
         const int e = lane + 32 * i;
         if (i < words && e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
           bv = v[i];
@@ -190,7 +195,9 @@ __global__ void __launch_bounds__(256) assign_kernel(const int32_t* __restrict__
     if ((int)threadIdx.x < E) off[threadIdx.x + 1] = before + incl;
     if (threadIdx.x == 0) off[0] = 0;
     __syncthreads();
-    if (blockIdx.x == 0 && (int)threadIdx.x <= E) off_out[threadIdx.x] = off[threadIdx.x];
+    // E + 1 offsets (257 with 256 experts: more than the block's threads)
+    if (blockIdx.x == 0)
+      for (int i = threadIdx.x; i <= E; i += blockDim.x) off_out[i] = off[i];
   }
   const int total = T * topk;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
@@ -397,8 +404,13 @@ extern "C" quads_status_t quads_moe_route(const float* logits, int32_t tokens, i
   int32_t* bprefix = bcount + (size_t)nb * num_experts;         // [E, nb]
   cudaStream_t st = (cudaStream_t)stream;
   if (tokens > 0)
-    launch_dep(route_kernel, nb, 32 * kRouteTokens, 0, st,
-        logits, tokens, num_experts, topk, topk_idx, gates, bcount, token_row);
+    {
+      const int words = (num_experts + 31) / 32;
+      auto rk = words <= 1 ? route_kernel<1> : words <= 2 ? route_kernel<2>
+              : words <= 4 ? route_kernel<4> : route_kernel<8>;
+      launch_dep(rk, nb, 32 * kRouteTokens, 0, st,
+          logits, tokens, num_experts, topk, topk_idx, gates, bcount, token_row);
+    }
   launch_dep(plan_kernel, num_experts, 256, 0, st, bcount, nb, bprefix, expert_counts);
   const int assign_blocks = std::max(1, std::min(num_sms() * 4, (tokens * topk + 255) / 256));
   launch_dep(assign_kernel, assign_blocks, 256, 0, st, topk_idx, tokens, num_experts, topk, nb,

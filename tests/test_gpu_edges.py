@@ -65,3 +65,31 @@ def test_moe_layer_one_expert_takes_every_token(lib):
 def test_moe_layer_single_token(lib):
     d = inputs.moe_layer(4, tokens=1, hidden=256, experts=8, topk=2, ffn=128, k=16)
     _check_layer(lib, d, 16, 16)
+
+
+@pytest.mark.parametrize("experts,topk", [(33, 4), (64, 8), (100, 8), (200, 8), (256, 6)])
+def test_routing_across_expert_counts(lib, experts, topk):
+    """moe_route with 33-256 experts (one, two, four and eight 32-expert words
+    per lane) against the oracle: expert ids (exact ties to the lower id),
+    gates within float32 rounding, counts, padded offsets and the row maps."""
+    from oracle import moe as M
+    rng = inputs.make_rng(experts)
+    T = 700
+    logits = rng.standard_normal((T, experts)).astype(np.float32)
+    logits[::7, 5] = logits[::7, 6]                 # exact ties
+    logits[::11, experts - 1] = np.float32(9.0)     # the last expert always taken there
+    plan = lib.moe_route(torch.from_numpy(logits).cuda(), topk)
+    torch.cuda.synchronize()
+    assert lib.device_status() == 0
+    idx, gates = M.route(logits, topk)
+    assert np.array_equal(plan["idx"].cpu().numpy(), idx)
+    assert np.allclose(plan["gates"].cpu().numpy(), gates, rtol=2e-6, atol=1e-7)
+    toks = M.dispatch(idx, experts)
+    cnt, off = plan["counts"].cpu().numpy(), plan["offsets"].cpu().numpy()
+    rt, trow = plan["row_token"].cpu().numpy(), plan["token_row"].cpu().numpy()
+    assert np.array_equal(cnt, [len(t) for t in toks])
+    assert off[0] == 0 and np.all(np.diff(off) == (cnt + 127) // 128 * 128)
+    for e in range(experts):
+        assert np.array_equal(rt[off[e]: off[e] + cnt[e]], toks[e])
+        assert np.all(rt[off[e] + cnt[e]: off[e + 1]] == -1)
+    assert np.all(rt[trow] == np.arange(T)[:, None])
