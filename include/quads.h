@@ -660,6 +660,8 @@ quads_status_t quads_moe_route(const float* logits, int32_t tokens, int32_t num_
  * scales LINEAR, output scales TCGEN05 (the grouped GEMM's operand layout).
  *   in_codes [tokens, cols/2] -> out_codes [rows_capacity, cols/2];
  *   in_scales [tokens, cols/16] -> out_scales TCGEN05 (cols % 64 == 0).
+ * Codes and out_scales 16-byte aligned, in_scales 4-byte aligned, else
+ * QUADS_ERR_MISALIGNED.
  */
 quads_status_t quads_moe_gather(const int32_t* row_token, const int32_t* expert_offsets,
                                 int32_t num_experts, int64_t rows_capacity, int64_t cols,

@@ -221,8 +221,9 @@ __global__ void __launch_bounds__(256) assign_kernel(const int32_t* __restrict__
 // them as one 16-byte word -- a warp writes the atom's 512 bytes whole
 // (4-byte stores at a 512-byte stride left most of each sector to be merged
 // in L2); a block that reaches past the last row keeps 4-byte stores for its
-// rows.  Narrow rows (the k-channel residual slices): a thread per (row,
-// vector) / (row, scale group) in one pass, 32-bit index math.  Padding rows
+// rows.  Narrow rows (the k-channel residual slices): one pass over a thread
+// per (row, vector) and a thread per (128-row block, scale group, lane) with
+// the same whole-word scale stores, 32-bit index math.  Padding rows
 // (row_token -1) get zero codes and scales.
 __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__ row_token,
                                                      const int32_t* __restrict__ off, int E,
@@ -272,7 +273,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
     // narrow rows: nvec < 32, natom < 8; rows * nvec fits comfortably in 32
     // bits.  Codes and the 4-byte scale groups in one pass (one round trip
     // for the small residual slices, where latency decides)
-    const uint32_t ncode = (uint32_t)(nrows * nvec), nsc = (uint32_t)(nrows * natom);
+    // scale items: (128-row block, 4-column group, lane l) -> rows l, l+32,
+    // l+64, l+96 of the block, one 16-byte store (32 lanes: a whole atom)
+    const uint32_t ncode = (uint32_t)(nrows * nvec);
+    const uint32_t nsc = (uint32_t)(((nrows + 127) >> 7) * natom * 32);
     for (uint32_t i = (uint32_t)tid; i < ncode + nsc; i += (uint32_t)nthreads) {
       if (i < ncode) {
         const uint32_t r = i / (uint32_t)nvec, v = i - r * (uint32_t)nvec;
@@ -282,11 +286,23 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
         reinterpret_cast<uint4*>(oc)[i] = x;
       } else {
         const uint32_t j = i - ncode;
-        const uint32_t r = j / (uint32_t)natom, a = j - r * (uint32_t)natom;
-        const int t = __ldg(row_token + r);
-        uint32_t x = 0;
-        if (t >= 0) x = __ldg(reinterpret_cast<const uint32_t*>(isf + (int64_t)t * ncols16) + a);
-        *reinterpret_cast<uint32_t*>(osf + sf_tc_offset(r, 4 * a, ncols16)) = x;
+        const uint32_t item = j >> 5, l = j & 31u;
+        const uint32_t rb = item / (uint32_t)natom, a = item - rb * (uint32_t)natom;
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int64_t r = (int64_t)rb * 128 + l + 32 * q;
+          const int t = r < nrows ? __ldg(row_token + r) : -1;
+          w[q] = t >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(isf + (int64_t)t * ncols16) + a) : 0u;
+        }
+        uint8_t* atom = osf + ((int64_t)rb * natom + a) * 512 + l * 16;
+        if ((int64_t)rb * 128 + 128 <= nrows) {
+          *reinterpret_cast<uint4*>(atom) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if ((int64_t)rb * 128 + l + 32 * q < nrows) *reinterpret_cast<uint32_t*>(atom + q * 4) = w[q];
+        }
       }
     }
     return;
@@ -427,8 +443,9 @@ extern "C" quads_status_t quads_moe_gather(const int32_t* row_token, const int32
     return fail(QUADS_ERR_INVALID_ARG, "moe_gather: null pointer argument");
   if (cols <= 0 || cols % 64 || rows_capacity % 128)
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "moe_gather: cols %% 64 and rows_capacity %% 128");
-  if (((uintptr_t)in_codes | (uintptr_t)out_codes) & 15u || ((uintptr_t)in_scales | (uintptr_t)out_scales) & 3u)
-    return fail(QUADS_ERR_MISALIGNED, "moe_gather: alignment");
+  // output scales go out as whole 16-byte atom words
+  if (((uintptr_t)in_codes | (uintptr_t)out_codes | (uintptr_t)out_scales) & 15u || (uintptr_t)in_scales & 3u)
+    return fail(QUADS_ERR_MISALIGNED, "moe_gather: codes and out_scales 16-byte, in_scales 4-byte aligned");
   cudaStream_t st = (cudaStream_t)stream;
   if (cols / 32 < 32 && rows_capacity * (cols / 32 + cols / 64) >= (int64_t)1 << 31)
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "moe_gather: narrow rows need rows * cols / 32 < 2^31");

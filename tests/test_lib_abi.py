@@ -88,6 +88,10 @@ def test_host_side_argument_checks_need_no_gpu(lib):
     assert st == 1 and "rows_capacity" in _err(lib)
     st = lib.quads_moe_route(p, 100, 16, 8, p, p, p, p, p, p, 1 << 20, p, 4, None)
     assert st == 7                                   # workspace too small
+    st = lib.quads_moe_gather(p, p, 16, 256, 256, p, p, p, ctypes.c_void_p(20), None)
+    assert st == 3 and "out_scales" in _err(lib)     # 16-byte scale words need a 16-byte base
+    st = lib.quads_moe_gather(p, p, 16, 200, 256, p, p, p, p, None)
+    assert st == 2                                   # rows_capacity % 128
     st = lib.quads_moe_grouped_gemm(4, 1000, 256, 256, p, None, p, p, p, 0, p, p, p, None, None, None,
                                     None, None, None, None, 0, None, 0, 0, 0, p, 1, 256, None, None, 0,
                                     None)
