@@ -20,7 +20,9 @@
  * Conventions for every call:
  *   - Every data pointer is a DEVICE pointer owned by the caller; the library
  *     never allocates device memory.  Calls that need scratch take a caller
- *     buffer `workspace` of at least quads_workspace_size(...) bytes.
+ *     buffer `workspace` of at least quads_workspace_size(...) bytes, 16-byte
+ *     aligned (QUADS_ERR_MISALIGNED otherwise; any cudaMalloc'd base is).
+ *     The R_sel code outputs (`r_codes`) are 16-byte aligned too.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
  *     only enqueues work on it and returns; no call synchronises the stream.
  *     The layer-path kernels are launched with programmatic stream

@@ -2311,6 +2311,7 @@ static quads_status_t launch(const Launch& L) {
                                              L.K, L.N, L.k, L.E);
     if (!L.ws || L.ws_bytes < need)
       return fail(QUADS_ERR_WORKSPACE, "gemm: workspace needs %zu bytes", need);
+    if ((uintptr_t)L.ws & 15u) return fail(QUADS_ERR_MISALIGNED, "gemm: workspace must be 16-byte aligned");
     uint8_t* c = (uint8_t*)L.ws;
     uint8_t* f = c + (((size_t)brows * (L.kpad / 2) + 1023) & ~(size_t)1023);
     launch_wsel(L.b_t, L.b_sf_t, L.E, L.N, L.K, L.sel, L.sel_pe, L.k, L.kpad, c, f, L.stream);

@@ -415,6 +415,7 @@ extern "C" quads_status_t quads_moe_route(const float* logits, int32_t tokens, i
   const size_t need = quads_workspace_size(QUADS_OP_MOE_ROUTE, tokens, num_experts, 0, topk, 1);
   if (!workspace || workspace_bytes < need)
     return fail(QUADS_ERR_WORKSPACE, "moe_route: workspace needs %zu bytes", need);
+  if ((uintptr_t)workspace & 15u) return fail(QUADS_ERR_MISALIGNED, "moe_route: workspace must be 16-byte aligned");
   const int nb = (tokens + kRouteTokens - 1) / kRouteTokens;
   int32_t* bcount = (int32_t*)workspace;                       // [E, nb]
   int32_t* bprefix = bcount + (size_t)nb * num_experts;         // [E, nb]

@@ -1811,6 +1811,7 @@ static quads_status_t quantize_impl(
   if (rows == 0) return QUADS_OK;
   if (!tensor_scale_in && !tensor_amax_in && (workspace_bytes < (size_t)G * 4 || !workspace))
     return fail(QUADS_ERR_WORKSPACE, "quantize: workspace needs %d bytes", G * 4);
+  if (!aligned16(workspace)) return fail(QUADS_ERR_MISALIGNED, "quantize: workspace must be 16-byte aligned");
   cudaStream_t st = (cudaStream_t)stream;
   const float* stp = tensor_scale_in;
   const uint32_t* amax_bits = nullptr;   // set: the quantize kernel derives the tensor scales
@@ -1920,6 +1921,7 @@ quads_status_t select_check_args(const void* x, int64_t rows, int64_t cols, int6
   if (k <= 0 || k % 16 || k > cols)
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "select: k=%d must be a multiple of 16 in [16, cols]", k);
   if (ldx < cols) return fail(QUADS_ERR_MISALIGNED, "select: ldx < cols");
+  if ((uintptr_t)r_codes & 15u) return fail(QUADS_ERR_MISALIGNED, "select: r_codes must be 16-byte aligned");
   if (group_offsets && num_groups < 1) return fail(QUADS_ERR_INVALID_ARG, "select: num_groups < 1");
   if (group_counts && !group_offsets)
     return fail(QUADS_ERR_INVALID_ARG, "select: group_counts needs group_offsets");
@@ -1946,6 +1948,7 @@ extern "C" quads_status_t quads_select_residual_channels(
   const int kpad = quads_kpad(k);
   if (rows > 0 && (!workspace || workspace_bytes < need))
     return fail(QUADS_ERR_WORKSPACE, "select: workspace needs %zu bytes", need);
+  if ((uintptr_t)workspace & 15u) return fail(QUADS_ERR_MISALIGNED, "select: workspace must be 16-byte aligned");
   cudaStream_t st = (cudaStream_t)stream;
   auto sel_ready = [&]() -> quads_status_t {
     if (!sel_ready_event) return QUADS_OK;
@@ -2029,6 +2032,8 @@ extern "C" quads_status_t quads_quantize_select_nvfp4(
   const size_t need = quads_workspace_size(QUADS_OP_QUANTIZE_SELECT, rows, cols, 0, k, 1);
   if (rows > 0 && (!workspace || workspace_bytes < need))
     return fail(QUADS_ERR_WORKSPACE, "quantize_select: workspace needs %zu bytes", need);
+  if (((uintptr_t)workspace | (uintptr_t)r_codes) & 15u)
+    return fail(QUADS_ERR_MISALIGNED, "quantize_select: workspace and r_codes must be 16-byte aligned");
   if (rows == 0) return QUADS_OK;
   const int kpad = quads_kpad(k);
   cudaStream_t st = (cudaStream_t)stream;
@@ -2114,6 +2119,8 @@ extern "C" quads_status_t quads_quantize_select_groups_nvfp4(
                                            num_groups);
   if (rows > 0 && (!workspace || workspace_bytes < need))
     return fail(QUADS_ERR_WORKSPACE, "quantize_select_groups: workspace needs %zu bytes", need);
+  if (((uintptr_t)workspace | (uintptr_t)r_codes) & 15u)
+    return fail(QUADS_ERR_MISALIGNED, "quantize_select_groups: workspace and r_codes must be 16-byte aligned");
   cudaStream_t st = (cudaStream_t)stream;
   auto sel_ready = [&]() -> quads_status_t {
     if (!sel_ready_event) return QUADS_OK;

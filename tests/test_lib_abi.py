@@ -82,6 +82,18 @@ def test_host_side_argument_checks_need_no_gpu(lib):
     st = lib.quads_select_residual_channels(p, 64, 256, 256, None, 1, p, p, 0, p, p, 16, p, None, p, p, 0, p,
                                             p, 1 << 20, None, None)
     assert st == 1 and "group_counts" in _err(lib)   # counts without group offsets
+    u = ctypes.c_void_p(20)                          # 4-byte but not 16-byte aligned
+    st = lib.quads_select_residual_channels(p, 64, 256, 256, None, 1, None, p, 0, p, p, 16, p, None, u, p, 0, p,
+                                            p, 1 << 20, None, None)
+    assert st == 3 and "r_codes" in _err(lib)
+    st = lib.quads_select_residual_channels(p, 64, 256, 256, None, 1, None, p, 0, p, p, 16, p, None, p, p, 0, p,
+                                            u, 1 << 20, None, None)
+    assert st == 3 and "workspace" in _err(lib)
+    st = lib.quads_quantize_select_groups_nvfp4(p, 64, 768, 768, p, 4, None, None, None, 64, p, 384, p, 0, p,
+                                                p, None, p, p, 0, p, u, 1 << 20, None, None)
+    assert st == 3 and "workspace" in _err(lib)
+    st = lib.quads_moe_route(p, 100, 16, 8, p, p, p, p, p, p, 1 << 20, u, 1 << 20, None)
+    assert st == 3 and "workspace" in _err(lib)
     st = lib.quads_moe_route(p, 100, 300, 8, p, p, p, p, p, p, 1 << 20, p, 1 << 20, None)
     assert st == 2                                   # > 256 experts
     st = lib.quads_moe_route(p, 100, 16, 8, p, p, p, p, p, p, 10, p, 1 << 20, None)
