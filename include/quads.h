@@ -673,6 +673,8 @@ quads_status_t quads_moe_gather(const int32_t* row_token, const int32_t* expert_
 /*
  * quads_moe_combine -- out[t] = bf16( sum_j gates[t, j] * y[token_row[t, j]] )
  * in float32, j ascending (ascending expert id).  y bf16 [rows, ldy].
+ * hidden, ldy and ldo multiples of 8 (QUADS_ERR_UNSUPPORTED_SHAPE); y and
+ * out 16-byte aligned (QUADS_ERR_MISALIGNED).
  */
 quads_status_t quads_moe_combine(const void* y, int64_t ldy, const int32_t* token_row,
                                  const float* gates, int32_t tokens, int32_t topk,

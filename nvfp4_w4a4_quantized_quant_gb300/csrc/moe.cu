@@ -465,6 +465,8 @@ extern "C" quads_status_t quads_moe_combine(const void* y, int64_t ldy, const in
     return fail(QUADS_ERR_INVALID_ARG, "moe_combine: null pointer");
   if (hidden <= 0 || hidden % 8 || ldy % 8 || ldo % 8 || ldy < hidden || ldo < hidden)
     return fail(QUADS_ERR_UNSUPPORTED_SHAPE, "moe_combine: hidden/ld must be multiples of 8");
+  if (((uintptr_t)y | (uintptr_t)out) & 15u)
+    return fail(QUADS_ERR_MISALIGNED, "moe_combine: y and out must be 16-byte aligned");
   if (tokens == 0) return QUADS_OK;
   cudaStream_t st = (cudaStream_t)stream;
   const int64_t work = (int64_t)tokens * (hidden / 8);

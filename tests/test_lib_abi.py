@@ -94,6 +94,8 @@ def test_host_side_argument_checks_need_no_gpu(lib):
     assert st == 3 and "workspace" in _err(lib)
     st = lib.quads_moe_route(p, 100, 16, 8, p, p, p, p, p, p, 1 << 20, u, 1 << 20, None)
     assert st == 3 and "workspace" in _err(lib)
+    st = lib.quads_moe_combine(u, 2048, p, p, 16, 8, 2048, p, 2048, None)
+    assert st == 3 and "16-byte" in _err(lib)        # y read as 16-byte words
     st = lib.quads_moe_route(p, 100, 300, 8, p, p, p, p, p, p, 1 << 20, p, 1 << 20, None)
     assert st == 2                                   # > 256 experts
     st = lib.quads_moe_route(p, 100, 16, 8, p, p, p, p, p, p, 10, p, 1 << 20, None)
